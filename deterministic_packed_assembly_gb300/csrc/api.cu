@@ -1,0 +1,609 @@
+// The C ABI (include/nspack.h): host-side checks, table allocation through
+// the caller's allocator, and the order of kernel launches that builds a
+// context and assembles updates.  No packing arithmetic runs on the host: the
+// host only validates arguments, sizes tables and reads back the few scalars
+// it needs to size the next ones.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "kernels.h"
+#include "nspack.h"
+
+struct ns_pack_ctx {
+  // recipe
+  uint32_t T = 0, B = 0, K = 0, flags = 0, S = 0, J = 0, n_docs = 0;
+  int32_t pad_id = 0;
+  uint64_t seed = 0, hash_key = 0, n_tokens = 0;
+  const int32_t *tokens = nullptr;
+  const int64_t *offs = nullptr;
+  const int32_t *loss_start = nullptr;
+  cudaStream_t stream = nullptr;
+  ns_alloc_fn alloc = nullptr;
+  ns_free_fn free_fn = nullptr;
+  void *user = nullptr;
+  int n_sms = 0;
+  // host summary
+  std::vector<uint64_t> windows;
+  std::vector<uint8_t> complete;
+  uint32_t valid_steps = 0, levels = 0;
+  uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
+  // device tables kept for the per-update calls
+  int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
+  uint32_t *W = nullptr;
+  int64_t *wbase = nullptr;
+  int32_t *win_start = nullptr;
+  int32_t *next = nullptr;
+  int64_t *node_S = nullptr, *node_src = nullptr;
+  int32_t *node_doc = nullptr, *node_mthr = nullptr;
+  int *err = nullptr;
+  uint64_t *fp_out = nullptr;
+  std::vector<void *> kept;
+};
+
+namespace {
+
+void dev_free(ns_pack_ctx *c, void *p) {
+  if (!p) return;
+  if (c->free_fn)
+    c->free_fn(p, c->user);
+  else
+    cudaFree(p);
+}
+
+struct Arena {
+  ns_pack_ctx *c;
+  std::vector<void *> temps;
+  explicit Arena(ns_pack_ctx *ctx) : c(ctx) {}
+  void *get(size_t bytes, bool keep) {
+    bytes = ((bytes + 255) / 256) * 256;
+    if (bytes == 0) bytes = 256;
+    void *p = nullptr;
+    if (c->alloc) {
+      p = c->alloc(bytes, c->user);
+    } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    if (!p) return nullptr;
+    if (keep) {
+      c->kept.push_back(p);
+      c->table_bytes += bytes;
+    } else {
+      temps.push_back(p);
+    }
+    return p;
+  }
+  template <class T>
+  T *keep(size_t n) {
+    return static_cast<T *>(get(n * sizeof(T), true));
+  }
+  template <class T>
+  T *temp(size_t n) {
+    return static_cast<T *>(get(n * sizeof(T), false));
+  }
+  void release() {
+    for (void *p : temps) dev_free(c, p);
+    temps.clear();
+  }
+};
+
+void release_ctx(ns_pack_ctx *c) {
+  if (!c) return;
+  for (void *p : c->kept) dev_free(c, p);
+  c->kept.clear();
+  delete c;
+}
+
+int check_config(const ns_pack_config *cfg) {
+  if (!cfg || !cfg->tokens || !cfg->doc_offsets) return NS_ERR_INVALID_ARG;
+  if (!cfg->stream_doc_begin || !cfg->stream_source || !cfg->source_weight ||
+      !cfg->stream_weight || !cfg->source_heldout_bp)
+    return NS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cfg->tokens) % 16 != 0) return NS_ERR_INVALID_ARG;
+  if (cfg->T < 16 || cfg->T % 16 != 0 || cfg->T > NS_MAX_T) return NS_ERR_INVALID_ARG;
+  if (cfg->B == 0 || cfg->max_steps == 0) return NS_ERR_INVALID_ARG;
+  if ((uint64_t)cfg->max_steps * cfg->B >= (1ull << 31)) return NS_ERR_INVALID_ARG;
+  if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
+  if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
+  if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
+  if (cfg->flags & ~NS_PACK_DRAIN) return NS_ERR_INVALID_ARG;
+  if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
+  for (uint32_t s = 0; s < cfg->n_sources; s++)
+    if (cfg->source_weight[s] == 0 || cfg->source_heldout_bp[s] > 10000) return NS_ERR_INVALID_ARG;
+  std::vector<uint32_t> per_source(cfg->n_sources, 0);
+  for (uint32_t j = 0; j < cfg->n_streams; j++) {
+    if (cfg->stream_weight[j] == 0 || cfg->stream_source[j] >= cfg->n_sources)
+      return NS_ERR_INVALID_ARG;
+    if (j > 0 && cfg->stream_source[j] < cfg->stream_source[j - 1]) return NS_ERR_INVALID_ARG;
+    if (cfg->stream_doc_begin[j + 1] < cfg->stream_doc_begin[j]) return NS_ERR_INVALID_ARG;
+    per_source[cfg->stream_source[j]]++;
+  }
+  if (cfg->stream_doc_begin[cfg->n_streams] > cfg->n_docs) return NS_ERR_INVALID_ARG;
+  for (uint32_t s = 0; s < cfg->n_sources; s++)
+    if (per_source[s] == 0 || per_source[s] > NS_MAX_STRATA_PER_SOURCE) return NS_ERR_INVALID_ARG;
+  return NS_OK;
+}
+
+// Block layout of a segmented launch: count[j] items per stream, `per`
+// items per block.
+std::vector<uint32_t> seg_layout(const std::vector<uint64_t> &count, uint32_t per) {
+  std::vector<uint32_t> base(count.size() + 1, 0);
+  uint64_t acc = 0;
+  for (size_t j = 0; j < count.size(); j++) {
+    base[j] = (uint32_t)acc;
+    acc += (count[j] + per - 1) / per;
+  }
+  base[count.size()] = (uint32_t)acc;
+  return base;
+}
+
+#define NS_CK(x)                                 \
+  do {                                           \
+    if ((x) != cudaSuccess) {                    \
+      cudaGetLastError();                        \
+      return NS_ERR_CUDA;                        \
+    }                                            \
+  } while (0)
+#define NS_ALLOC(p)               \
+  do {                            \
+    if (!(p)) return NS_ERR_OOM;  \
+  } while (0)
+
+int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st) {
+  *dev = a.get(bytes, false);
+  NS_ALLOC(*dev);
+  if (bytes) NS_CK(cudaMemcpyAsync(*dev, host, bytes, cudaMemcpyHostToDevice, st));
+  return NS_OK;
+}
+
+int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
+  const uint32_t J = c->J, S = c->S, K = c->K, T = c->T;
+  cudaStream_t st = c->stream;
+  int dev = 0;
+  NS_CK(cudaGetDevice(&dev));
+  NS_CK(cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev));
+
+  // ---- recipe tables on the device (temporaries) --------------------------
+  std::vector<uint32_t> sdb(cfg->stream_doc_begin, cfg->stream_doc_begin + J + 1);
+  std::vector<uint32_t> ssrc(cfg->stream_source, cfg->stream_source + J);
+  std::vector<uint32_t> sw(cfg->source_weight, cfg->source_weight + S);
+  std::vector<uint32_t> tw(cfg->stream_weight, cfg->stream_weight + J);
+  std::vector<uint16_t> sbp(cfg->source_heldout_bp, cfg->source_heldout_bp + S);
+  std::vector<uint16_t> stream_bp(J);
+  std::vector<uint32_t> src_first(S + 1, 0);
+  uint32_t max_strata = 0;
+  bool any_heldout = false;
+  for (uint32_t j = 0; j < J; j++) {
+    stream_bp[j] = sbp[ssrc[j]];
+    any_heldout |= stream_bp[j] > 0 && sdb[j + 1] > sdb[j];
+  }
+  for (uint32_t s = 0, j = 0; s < S; s++) {
+    src_first[s] = j;
+    while (j < J && ssrc[j] == s) j++;
+    src_first[s + 1] = j;
+    max_strata = std::max(max_strata, src_first[s + 1] - src_first[s]);
+  }
+  void *d_sdb, *d_ssrc, *d_sw, *d_tw, *d_sbp, *d_stream_bp, *d_src_first;
+  int rc;
+  if ((rc = upload(a, sdb.data(), sdb.size() * 4, &d_sdb, st))) return rc;
+  if ((rc = upload(a, ssrc.data(), ssrc.size() * 4, &d_ssrc, st))) return rc;
+  if ((rc = upload(a, sw.data(), sw.size() * 4, &d_sw, st))) return rc;
+  if ((rc = upload(a, tw.data(), tw.size() * 4, &d_tw, st))) return rc;
+  if ((rc = upload(a, sbp.data(), sbp.size() * 2, &d_sbp, st))) return rc;
+  if ((rc = upload(a, stream_bp.data(), stream_bp.size() * 2, &d_stream_bp, st))) return rc;
+  if ((rc = upload(a, src_first.data(), src_first.size() * 4, &d_src_first, st))) return rc;
+
+  c->err = a.keep<int>(1);
+  NS_ALLOC(c->err);
+  c->fp_out = a.keep<uint64_t>(1);
+  NS_ALLOC(c->fp_out);
+  NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
+
+  // ---- 1. the corpus partition, 2. quotas of every update -----------------
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
+  int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
+  c->quota = a.keep<int32_t>((size_t)K * J);
+  c->cum = a.keep<int32_t>((size_t)(K + 1) * J);
+  c->rb = a.keep<int32_t>((size_t)K * (J + 1));
+  NS_ALLOC(src_quota);
+  NS_ALLOC(c->quota);
+  NS_ALLOC(c->cum);
+  NS_ALLOC(c->rb);
+  NS_CK(nsk::launch_quota_sources(static_cast<uint32_t *>(d_sw), S, c->B, K, src_quota, st));
+  NS_CK(nsk::launch_quota_strata(src_quota, static_cast<uint32_t *>(d_tw),
+                                 static_cast<uint32_t *>(d_src_first), S, J, K, max_strata,
+                                 c->quota, c->cum, st));
+  NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, st));
+
+  std::vector<int32_t> rmax32(J);
+  int err_host = 0;
+  NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaStreamSynchronize(st));
+  if (err_host != 0) return NS_ERR_BAD_INPUT;
+
+  std::vector<uint64_t> rmax(J);
+  std::vector<int64_t> wbase(J + 1, 0);
+  for (uint32_t j = 0; j < J; j++) {
+    rmax[j] = (uint64_t)rmax32[j];
+    wbase[j + 1] = wbase[j] + (int64_t)rmax[j];
+  }
+  c->wbase = a.keep<int64_t>(J + 1);
+  NS_ALLOC(c->wbase);
+  NS_CK(cudaMemcpyAsync(c->wbase, wbase.data(), (J + 1) * sizeof(int64_t),
+                        cudaMemcpyHostToDevice, st));
+
+  // ---- 3. held-out flags --------------------------------------------------
+  uint8_t *heldout = nullptr;
+  if (any_heldout) {
+    heldout = a.temp<uint8_t>(std::max<uint32_t>(c->n_docs, 1));
+    unsigned long long *counter = a.temp<unsigned long long>(1);
+    NS_ALLOC(heldout);
+    NS_ALLOC(counter);
+    NS_CK(cudaMemsetAsync(heldout, 0, std::max<uint32_t>(c->n_docs, 1), st));
+    NS_CK(cudaMemsetAsync(counter, 0, sizeof(unsigned long long), st));
+    NS_CK(nsk::launch_hash_docs(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+                                static_cast<uint16_t *>(d_stream_bp), J, c->hash_key, heldout,
+                                counter, c->n_sms, st));
+  }
+
+  // ---- 4. shuffled order and kept lengths of every position ---------------
+  const uint32_t D0 = sdb[0];
+  const uint64_t n_pos = (uint64_t)sdb[J] - D0;
+  std::vector<uint64_t> N(J);
+  for (uint32_t j = 0; j < J; j++) N[j] = (uint64_t)sdb[j + 1] - sdb[j];
+  uint64_t *keys = a.temp<uint64_t>((size_t)J * 4);
+  uint32_t *order = a.temp<uint32_t>(std::max<uint64_t>(n_pos, 1));
+  uint32_t *klen = a.temp<uint32_t>(std::max<uint64_t>(n_pos, 1));
+  int64_t *kex = a.temp<int64_t>(n_pos + 1);
+  int64_t *pex = a.temp<int64_t>(n_pos + 1);
+  const size_t scan_bytes = nsk::scan_scratch_bytes(n_pos);
+  void *scan_scratch = a.get(scan_bytes, false);
+  NS_ALLOC(keys);
+  NS_ALLOC(order);
+  NS_ALLOC(klen);
+  NS_ALLOC(kex);
+  NS_ALLOC(pex);
+  NS_ALLOC(scan_scratch);
+  NS_CK(nsk::launch_stream_keys(c->seed, J, keys, st));
+  {
+    std::vector<uint32_t> bb = seg_layout(N, 256);
+    void *d_bb;
+    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
+    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, heldout, D0, order,
+                            klen, c->err, st));
+  }
+  NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
+
+  // ---- 5. the prefix of each stream the horizon reaches -------------------
+  uint32_t *cutoff = a.temp<uint32_t>(J);
+  int64_t *npieces = a.temp<int64_t>(J);
+  int64_t *node_base = a.temp<int64_t>(J + 1);
+  NS_ALLOC(cutoff);
+  NS_ALLOC(npieces);
+  NS_ALLOC(node_base);
+  NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
+                           T, cutoff, npieces, st));
+  NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
+  std::vector<uint32_t> cut_h(J);
+  std::vector<int64_t> np_h(J), nb_h(J + 1);
+  NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(nb_h.data(), node_base, (J + 1) * 8, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaStreamSynchronize(st));
+  if (err_host != 0) return NS_ERR_DEVICE;
+  const int64_t n_nodes = nb_h[J];
+  if (n_nodes >= (int64_t)0x7FFFFFFF) return NS_ERR_INVALID_ARG;
+  c->n_pieces = (uint64_t)(n_nodes - J);
+  c->complete.resize(J);
+  int64_t max_pieces = 0;
+  for (uint32_t j = 0; j < J; j++) {
+    c->complete[j] = (cut_h[j] == N[j]) ? 1 : 0;
+    max_pieces = std::max(max_pieces, np_h[j]);
+  }
+  uint32_t L = 1;
+  while ((1ll << L) < max_pieces + 1) L++;
+  c->levels = L;
+
+  // ---- 6. pieces, next window start, pointer jumping ----------------------
+  c->node_src = a.keep<int64_t>(n_nodes);
+  c->node_S = a.keep<int64_t>(n_nodes);
+  c->node_doc = a.keep<int32_t>(n_nodes);
+  c->node_mthr = a.keep<int32_t>(n_nodes);
+  c->next = a.keep<int32_t>(n_nodes);
+  int32_t *levels = a.temp<int32_t>((size_t)L * n_nodes);
+  NS_ALLOC(c->node_src);
+  NS_ALLOC(c->node_S);
+  NS_ALLOC(c->node_doc);
+  NS_ALLOC(c->node_mthr);
+  NS_ALLOC(c->next);
+  NS_ALLOC(levels);
+  {
+    std::vector<uint64_t> cnt(J);
+    for (uint32_t j = 0; j < J; j++) cnt[j] = std::max<uint64_t>(cut_h[j], 1);
+    std::vector<uint32_t> bb = seg_layout(cnt, 256);
+    void *d_bb;
+    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
+    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    NS_CK(nsk::launch_expand(g, static_cast<uint32_t *>(d_sdb), D0, cutoff, order, klen, kex, pex,
+                             node_base, npieces, c->offs, c->loss_start, T, c->node_src,
+                             c->node_doc, c->node_mthr, c->node_S, st));
+  }
+  {
+    std::vector<uint64_t> cnt(J);
+    for (uint32_t j = 0; j < J; j++) cnt[j] = (uint64_t)np_h[j] + 1;
+    std::vector<uint32_t> bb = seg_layout(cnt, 256);
+    void *d_bb;
+    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
+    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    NS_CK(nsk::launch_next(g, node_base, npieces, c->node_S, T, levels, st));
+  }
+  for (uint32_t l = 1; l < L; l++)
+    NS_CK(nsk::launch_jump_level(levels + (size_t)(l - 1) * n_nodes, n_nodes,
+                                 levels + (size_t)l * n_nodes, st));
+  NS_CK(cudaMemcpyAsync(c->next, levels, (size_t)n_nodes * 4, cudaMemcpyDeviceToDevice, st));
+
+  // ---- 7. windows: count, starts, the valid horizon ------------------------
+  c->W = a.keep<uint32_t>(J);
+  c->win_start = a.keep<int32_t>(std::max<int64_t>(wbase[J], 1));
+  uint32_t *first_bad = a.temp<uint32_t>(1);
+  uint32_t *valid = a.temp<uint32_t>(1);
+  NS_ALLOC(c->W);
+  NS_ALLOC(c->win_start);
+  NS_ALLOC(first_bad);
+  NS_ALLOC(valid);
+  NS_CK(nsk::launch_count_windows(levels, n_nodes, L, node_base, npieces, J, c->W, st));
+  std::vector<uint32_t> wb = seg_layout(rmax, 256);
+  void *d_wb;
+  if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
+  nsk::SegGrid wg{static_cast<uint32_t *>(d_wb), J, wb[J]};
+  NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase, c->win_start,
+                                  st));
+  NS_CK(nsk::launch_valid_steps(c->cum, c->W, J, K, (c->flags & NS_PACK_DRAIN) ? 1u : 0u,
+                                first_bad, valid, st));
+
+  // ---- 8. order digest ----------------------------------------------------
+  unsigned long long *dacc = a.temp<unsigned long long>(2);
+  int64_t *ubase = a.temp<int64_t>(J + 1);
+  uint64_t *digest = a.temp<uint64_t>(1);
+  NS_ALLOC(dacc);
+  NS_ALLOC(ubase);
+  NS_ALLOC(digest);
+  NS_CK(cudaMemsetAsync(dacc, 0, 2 * sizeof(unsigned long long), st));
+  nsk::DigestHeader h{};
+  h.scalars[0] = T;
+  h.scalars[1] = c->B;
+  h.scalars[2] = K;
+  h.scalars[3] = 0;  // valid_steps, read on the device
+  h.scalars[4] = (c->flags & NS_PACK_DRAIN) ? 1 : 0;
+  h.scalars[5] = (uint64_t)(uint32_t)c->pad_id;
+  h.scalars[6] = c->seed;
+  h.scalars[7] = c->hash_key;
+  h.scalars[8] = S;
+  h.scalars[9] = J;
+  h.source_weight = static_cast<uint32_t *>(d_sw);
+  h.source_bp = static_cast<uint16_t *>(d_sbp);
+  h.sdb = static_cast<uint32_t *>(d_sdb);
+  h.ssrc = static_cast<uint32_t *>(d_ssrc);
+  h.tw = static_cast<uint32_t *>(d_tw);
+  h.S = S;
+  h.J = J;
+  NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, c->win_start,
+                           c->node_src, c->node_doc, c->offs, T, K, dacc, ubase, digest, st));
+
+  // ---- 9. read back the summary ------------------------------------------
+  std::vector<uint32_t> W_h(J);
+  uint32_t valid_h = 0;
+  uint64_t digest_h = 0;
+  NS_CK(cudaMemcpyAsync(W_h.data(), c->W, J * 4, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(&valid_h, valid, 4, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(&digest_h, digest, 8, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaStreamSynchronize(st));
+  if (err_host != 0) return NS_ERR_DEVICE;
+  c->windows.assign(W_h.begin(), W_h.end());
+  c->valid_steps = valid_h;
+  c->digest = digest_h;
+  return NS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
+  if (!out) return NS_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  ns_pack_ctx *c = new (std::nothrow) ns_pack_ctx();
+  if (!c) return NS_ERR_OOM;
+  c->T = cfg->T;
+  c->B = cfg->B;
+  c->K = cfg->max_steps;
+  c->flags = cfg->flags;
+  c->S = cfg->n_sources;
+  c->J = cfg->n_streams;
+  c->n_docs = cfg->n_docs;
+  c->pad_id = cfg->pad_id;
+  c->seed = cfg->seed;
+  c->hash_key = cfg->hash_key;
+  c->n_tokens = cfg->n_tokens;
+  c->tokens = cfg->tokens;
+  c->offs = cfg->doc_offsets;
+  c->loss_start = cfg->loss_start;
+  c->stream = static_cast<cudaStream_t>(cfg->cuda_stream);
+  c->alloc = cfg->alloc;
+  c->free_fn = cfg->free;
+  c->user = cfg->alloc_user;
+  Arena a(c);
+  rc = build(c, cfg, a);
+  if (rc != NS_OK) {
+    cudaStreamSynchronize(c->stream);
+    cudaGetLastError();
+    a.release();
+    release_ctx(c);
+    return rc;
+  }
+  a.release();
+  *out = c;
+  return NS_OK;
+}
+
+int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,
+                 uint32_t row_end, const ns_pack_out *out, void *cuda_stream) {
+  if (!ctx || !out || n_steps == 0) return NS_ERR_INVALID_ARG;
+  if (row_begin >= row_end || row_end > ctx->B) return NS_ERR_INVALID_ARG;
+  if (!out->tokens || !out->pos || !out->doc || !out->mask || !out->row_fp || !out->row_learned)
+    return NS_ERR_INVALID_ARG;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(out->tokens) |
+                       reinterpret_cast<uintptr_t>(out->pos) |
+                       reinterpret_cast<uintptr_t>(out->doc) | reinterpret_cast<uintptr_t>(out->mask);
+  if (al % 16 != 0) return NS_ERR_INVALID_ARG;
+  if ((uint64_t)n_steps * (row_end - row_begin) >= (1ull << 31)) return NS_ERR_INVALID_ARG;
+  if ((uint64_t)step0 + n_steps > ctx->K) return NS_ERR_HORIZON;
+  if ((uint64_t)step0 + n_steps > ctx->valid_steps) return NS_ERR_EXHAUSTED;
+  nsk::GatherParams p{};
+  p.tokens = ctx->tokens;
+  p.rb = ctx->rb;
+  p.cum = ctx->cum;
+  p.W = ctx->W;
+  p.wbase = ctx->wbase;
+  p.win_start = ctx->win_start;
+  p.next = ctx->next;
+  p.node_S = ctx->node_S;
+  p.node_src = ctx->node_src;
+  p.node_doc = ctx->node_doc;
+  p.node_mthr = ctx->node_mthr;
+  p.err = ctx->err;
+  p.J = ctx->J;
+  p.T = ctx->T;
+  p.step0 = step0;
+  p.n_steps = n_steps;
+  p.row0 = row_begin;
+  p.n_rows = row_end - row_begin;
+  p.pad_id = ctx->pad_id;
+  p.tokens_out = out->tokens;
+  p.pos_out = out->pos;
+  p.doc_out = out->doc;
+  p.mask_out = out->mask;
+  p.row_fp = out->row_fp;
+  p.row_learned = out->row_learned;
+  cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
+  if (nsk::launch_gather(p, st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return NS_OK;
+}
+
+int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
+                     uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream) {
+  if (!ctx || !row_fp_dev || !batch_fp_dev || n_steps == 0 || n_rows == 0)
+    return NS_ERR_INVALID_ARG;
+  cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
+  if (nsk::launch_batch_fp(row_fp_dev, n_steps, n_rows, batch_fp_dev, st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return NS_OK;
+}
+
+static int read_error_word(ns_pack_ctx *ctx, cudaStream_t st) {
+  int e = 0;
+  if (cudaMemcpyAsync(&e, ctx->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return e == 0 ? NS_OK : NS_ERR_DEVICE;
+}
+
+int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,
+                        uint64_t *batch_fp_host, void *cuda_stream) {
+  if (!ctx || !row_fp_dev || !batch_fp_host || n_rows == 0) return NS_ERR_INVALID_ARG;
+  cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
+  if (nsk::launch_batch_fp(row_fp_dev, 1, n_rows, ctx->fp_out, st) != cudaSuccess ||
+      cudaMemcpyAsync(batch_fp_host, ctx->fp_out, sizeof(uint64_t), cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return read_error_word(ctx, st);
+}
+
+int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
+  if (!ctx || !info) return NS_ERR_INVALID_ARG;
+  info->valid_steps = ctx->valid_steps;
+  info->max_steps = ctx->K;
+  info->n_streams = ctx->J;
+  info->T = ctx->T;
+  info->B = ctx->B;
+  info->levels = ctx->levels;
+  info->order_digest = ctx->digest;
+  info->n_pieces = ctx->n_pieces;
+  info->table_bytes = ctx->table_bytes;
+  return NS_OK;
+}
+
+int ns_pack_stream_windows(const ns_pack_ctx *ctx, uint64_t *windows, uint8_t *complete) {
+  if (!ctx) return NS_ERR_INVALID_ARG;
+  if (windows) std::memcpy(windows, ctx->windows.data(), ctx->J * sizeof(uint64_t));
+  if (complete) std::memcpy(complete, ctx->complete.data(), ctx->J);
+  return NS_OK;
+}
+
+int ns_pack_quota_table(const ns_pack_ctx *ctx, int32_t *quota, int32_t *cum) {
+  if (!ctx) return NS_ERR_INVALID_ARG;
+  cudaStream_t st = ctx->stream;
+  if (quota && cudaMemcpyAsync(quota, ctx->quota, (size_t)ctx->K * ctx->J * 4,
+                               cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  if (cum && cudaMemcpyAsync(cum, ctx->cum, (size_t)(ctx->K + 1) * ctx->J * 4,
+                             cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return NS_OK;
+}
+
+int ns_pack_check(ns_pack_ctx *ctx) {
+  if (!ctx) return NS_ERR_INVALID_ARG;
+  return read_error_word(ctx, ctx->stream);
+}
+
+void ns_pack_free(ns_pack_ctx *ctx) {
+  if (!ctx) return;
+  cudaStreamSynchronize(ctx->stream);
+  cudaGetLastError();
+  release_ctx(ctx);
+}
+
+const char *ns_pack_strerror(int code) {
+  switch (code) {
+    case NS_OK: return "ok";
+    case NS_ERR_INVALID_ARG: return "invalid argument";
+    case NS_ERR_CUDA: return "CUDA runtime error";
+    case NS_ERR_OOM: return "out of device memory";
+    case NS_ERR_EXHAUSTED: return "a stream has no window left for this update";
+    case NS_ERR_HORIZON: return "update index at or past max_steps";
+    case NS_ERR_BAD_INPUT: return "doc_offsets malformed";
+    case NS_ERR_DEVICE: return "a kernel recorded an inconsistency";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,900 @@
+// Kernels that build a packing context: offsets check, Feistel keys, the
+// two-level quota tables, the held-out hash, the shuffled order, the scans of
+// kept lengths and piece counts, piece expansion, next-window search, the
+// pointer-jumping tables, window numbering, the valid-step horizon and the
+// order digest.  All integer; every table is written once per context.
+//
+// What each step computes is stated in the NeuronSpark-Trainer README,
+// Concepts (held-out split by a hash of the text; shuffled documents;
+// per-update source and stratum shares; windows cut at document ends) and in
+// the Linnet training docs, Supervised fine-tuning (rows of exactly T
+// positions, padded).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nsk {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+inline unsigned blocks_for(uint64_t n, int threads = kThreads) {
+  return (unsigned)((n + threads - 1) / threads);
+}
+
+// Stream j of this block in a segmented launch, and the block's index within
+// the stream's run of blocks.
+__device__ __forceinline__ void seg_locate(const SegGrid &g, uint32_t &j, uint32_t &blk) {
+  __shared__ uint32_t s_j;
+  if (threadIdx.x == 0) {
+    int64_t jj = last_le<uint32_t, int64_t>(g.blk_base, 0, (int64_t)g.J, (uint32_t)blockIdx.x);
+    s_j = (uint32_t)(jj < 0 ? 0 : jj);
+  }
+  __syncthreads();
+  j = s_j;
+  blk = blockIdx.x - g.blk_base[j];
+}
+
+template <class T>
+__device__ T block_sum(T v, T *scratch /* [33] */) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int nw = (blockDim.x + 31) >> 5;
+    T t = (l < nw) ? scratch[l] : T(0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (l == 0) scratch[32] = t;
+  }
+  __syncthreads();
+  T r = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// doc_offsets must start at >= 0, never decrease, keep every length below
+// 2^31 and end inside the token array.
+__global__ void validate_offsets_kernel(const int64_t *__restrict__ offs, uint32_t n_docs,
+                                        uint64_t n_tokens, int *err) {
+  uint64_t d = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (d > n_docs) return;
+  int64_t o = offs[d];
+  if (d == 0 && o < 0) set_error(err, kDevBadOffsets);
+  if (d == n_docs) {
+    if (o < 0 || (uint64_t)o > n_tokens) set_error(err, kDevBadOffsets);
+    return;
+  }
+  int64_t len = offs[d + 1] - o;
+  if (len < 0 || len > 0x7FFFFFFF) set_error(err, kDevBadOffsets);
+}
+
+// Round keys of the shuffle: K_r = splitmix64(splitmix64(seed) ^
+// splitmix64((stream << 8) | r)), r = 0..3.
+__global__ void stream_keys_kernel(uint64_t seed, uint32_t J, uint64_t *keys) {
+  uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (uint64_t)J * 4) return;
+  uint64_t j = i >> 2, r = i & 3;
+  keys[i] = splitmix64(splitmix64(seed) ^ splitmix64((j << 8) | r));
+}
+
+// ---------------------------------------------------------------------------
+// One update of the apportionment among this block's children (thread c owns
+// child c; inactive threads hold weight 0).  n units now, N counting every
+// update so far including this one; C is the child's count before.
+//   base_c = floor(n v_c / V); R = n - sum base;
+//   delta_c = N v_c - V (C_c + base_c)  (exact, 128-bit);
+//   the R children with the largest delta (ties: lower index) get one more.
+__device__ __forceinline__ int64_t apportion_one(bool act, uint64_t v, uint64_t V, int64_t n,
+                                                 int64_t N, int64_t C, int n_children,
+                                                 __int128 *delta, int64_t *scratch) {
+  int64_t base = act ? (int64_t)(((uint64_t)n * v) / V) : 0;
+  int64_t R = n - block_sum<int64_t>(base, scratch);
+  __int128 d = 0;
+  if (act) {
+    d = (__int128)N * (__int128)v - (__int128)V * (__int128)(C + base);
+    delta[threadIdx.x] = d;
+  }
+  __syncthreads();
+  int64_t a = base;
+  if (act) {
+    int rank = 0;
+    const int c = threadIdx.x;
+    for (int c2 = 0; c2 < n_children; c2++) {
+      __int128 e = delta[c2];
+      rank += (e > d) || (e == d && c2 < c);
+    }
+    a += (rank < R) ? 1 : 0;
+  }
+  __syncthreads();
+  return a;
+}
+
+// Source level: every update hands out B windows among the sources.
+__global__ void quota_sources_kernel(const uint32_t *__restrict__ sw, uint32_t S, uint32_t B,
+                                     uint32_t K, int32_t *__restrict__ src_quota) {
+  __shared__ __int128 delta[1024];
+  __shared__ int64_t scratch[33];
+  __shared__ uint64_t uscratch[33];
+  const bool act = threadIdx.x < S;
+  const uint64_t v = act ? sw[threadIdx.x] : 0;
+  const uint64_t V = block_sum<uint64_t>(v, uscratch);
+  int64_t C = 0;
+  for (uint32_t k = 0; k < K; k++) {
+    int64_t a = apportion_one(act, v, V, (int64_t)B, (int64_t)(k + 1) * B, C, (int)S, delta,
+                              scratch);
+    if (act) src_quota[(size_t)k * S + threadIdx.x] = (int32_t)a;
+    C += a;
+  }
+}
+
+// Stratum level: block s splits source s's windows of every update among its
+// streams; writes the per-stream quota and the counts before each update.
+__global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
+                                    const uint32_t *__restrict__ tw,
+                                    const uint32_t *__restrict__ src_first, uint32_t S,
+                                    uint32_t J, uint32_t K, int32_t *__restrict__ quota,
+                                    int32_t *__restrict__ cum) {
+  __shared__ __int128 delta[1024];
+  __shared__ int64_t scratch[33];
+  __shared__ uint64_t uscratch[33];
+  const uint32_t s = blockIdx.x;
+  const uint32_t f0 = src_first[s], f1 = src_first[s + 1];
+  const int n_st = (int)(f1 - f0);
+  const bool act = (int)threadIdx.x < n_st;
+  const uint32_t j = f0 + threadIdx.x;
+  const uint64_t v = act ? tw[j] : 0;
+  const uint64_t V = block_sum<uint64_t>(v, uscratch);
+  int64_t C = 0, Cs = 0;
+  for (uint32_t k = 0; k < K; k++) {
+    const int64_t n = src_quota[(size_t)k * S + s];
+    int64_t a = apportion_one(act, v, V, n, Cs + n, C, n_st, delta, scratch);
+    if (act) {
+      quota[(size_t)k * J + j] = (int32_t)a;
+      cum[(size_t)k * J + j] = (int32_t)C;
+    }
+    C += a;
+    Cs += n;
+  }
+  if (act) cum[(size_t)K * J + j] = (int32_t)C;
+}
+
+// rb[k][j]: the first row of stream j in update k (rows ordered by stream).
+__global__ void row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
+                                int32_t *__restrict__ rb) {
+  uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= K) return;
+  const int32_t *q = quota + (size_t)k * J;
+  int32_t *r = rb + (size_t)k * (J + 1);
+  int32_t acc = 0;
+  for (uint32_t j = 0; j < J; j++) {
+    r[j] = acc;
+    acc += q[j];
+  }
+  r[J] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Held-out hash.  acc_d = sum_i splitmix64((i << 32) | u32 tok_i),
+// h_d = splitmix64(acc_d ^ splitmix64(hash_key + L_d)); held out iff
+// floor(h_d * 10000 / 2^64) < bp of the document's source.  One warp per
+// document, documents taken dynamically in groups; aligned 16-byte loads that
+// always hold at least one token of the document.
+__device__ __forceinline__ uint64_t hash_terms(int4 v, int64_t g, int64_t o0, int64_t o1) {
+  uint64_t s = 0;
+  const int32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    int64_t idx = g + q;
+    if (idx >= o0 && idx < o1)
+      s += splitmix64(((uint64_t)(idx - o0) << 32) | (uint64_t)(uint32_t)e[q]);
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    hash_docs_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
+                     const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
+                     uint32_t J, uint64_t hash_key, uint8_t *__restrict__ heldout,
+                     unsigned long long *counter) {
+  constexpr uint32_t kGrab = 8;
+  const int lane = threadIdx.x & 31;
+  const uint32_t D0 = sdb[0], D1 = sdb[J];
+  const uint64_t n = D1 - D0;
+  uint32_t cur_lo = 1, cur_hi = 0, bp = 0;
+  while (true) {
+    unsigned long long base = 0;
+    if (lane == 0) base = atomicAdd(counter, (unsigned long long)kGrab);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= n) break;
+    const uint32_t dend = D0 + (uint32_t)min((unsigned long long)n, base + kGrab);
+    for (uint32_t d = D0 + (uint32_t)base; d < dend; d++) {
+      if (d < cur_lo || d >= cur_hi) {
+        int64_t j = last_le<uint32_t, int64_t>(sdb, 0, (int64_t)J, d);
+        cur_lo = sdb[j];
+        cur_hi = sdb[j + 1];
+        bp = stream_bp[j];
+      }
+      if (bp == 0) continue;
+      const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
+      uint64_t acc = 0;
+      for (int64_t g = (o0 & ~(int64_t)3) + 4 * lane; g < o1; g += 256) {
+        const int4 v0 = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
+        const bool has1 = g + 128 < o1;
+        int4 v1 = make_int4(0, 0, 0, 0);
+        if (has1) v1 = __ldcs(reinterpret_cast<const int4 *>(tokens + g + 128));
+        acc += hash_terms(v0, g, o0, o1);
+        if (has1) acc += hash_terms(v1, g + 128, o0, o1);
+      }
+      acc = warp_sum_u64(acc);
+      if (lane == 0) {
+        const uint64_t h = splitmix64(acc ^ splitmix64(hash_key + (uint64_t)(o1 - o0)));
+        heldout[d] = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1 : 0;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The shuffle: position p of stream j reads document b_j + pi_j(p), pi_j a
+// 4-round balanced Feistel network over 2*half bits (half = bits / 2, bits =
+// max(2, ceil(log2 N_j)) rounded up to even), walked until it lands in
+// [0, N_j).  Writes the document and its kept length (0 if empty or held out).
+__device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, uint64_t mask,
+                                            uint64_t x) {
+  uint64_t L = x >> half, R = x & mask;
+#pragma unroll
+  for (int r = 0; r < 4; r++) {
+    const uint64_t F = splitmix64(k[r] ^ R) & mask;
+    const uint64_t nl = R;
+    R = L ^ F;
+    L = nl;
+  }
+  return (L << half) | R;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
+                 const int64_t *__restrict__ offs, const uint8_t *__restrict__ heldout,
+                 uint32_t D0, uint32_t *__restrict__ order, uint32_t *__restrict__ klen,
+                 int *err) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const uint32_t b0 = sdb[j];
+  const uint64_t N = sdb[j + 1] - b0;
+  const uint64_t p = (uint64_t)blk * blockDim.x + threadIdx.x;
+  if (p >= N) return;
+  uint32_t bits = (N <= 1) ? 0u : (uint32_t)(64 - __clzll((long long)(N - 1)));
+  if (bits < 2) bits = 2;
+  bits += bits & 1u;
+  const uint32_t half = bits >> 1;
+  const uint64_t mask = (half >= 64) ? ~0ull : ((1ull << half) - 1);
+  uint64_t k[4];
+#pragma unroll
+  for (int r = 0; r < 4; r++) k[r] = keys[(size_t)j * 4 + r];
+  uint64_t y = feistel(k, half, mask, p);
+  for (uint32_t it = 0; y >= N; it++) {
+    if (it > (1u << 20)) {
+      set_error(err, kDevWalkLimit);
+      y = 0;
+      break;
+    }
+    y = feistel(k, half, mask, y);
+  }
+  const uint32_t d = b0 + (uint32_t)y;
+  const int64_t L = __ldg(offs + d + 1) - __ldg(offs + d);
+  const bool kept = L > 0 && !(heldout && heldout[d]);
+  const uint64_t idx = (uint64_t)b0 + p - D0;
+  order[idx] = d;
+  klen[idx] = kept ? (uint32_t)L : 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Exclusive scans of the kept lengths and of the piece counts ceil(L / T):
+// reduce per tile, scan the tile sums, rescan each tile with its offset.  A
+// warp owns a contiguous run of 32 * kScanRounds elements and scans it with
+// shuffles, round by round, so every load and store is coalesced.
+constexpr int kScanWarps = 8;
+constexpr int kScanRounds = 8;
+constexpr int kScanTile = kScanWarps * kScanRounds * 32;
+
+__global__ void __launch_bounds__(kScanWarps * 32)
+    scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
+                       int64_t *__restrict__ bs_a, int64_t *__restrict__ bs_b) {
+  __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
+  int64_t a = 0, b = 0;
+#pragma unroll
+  for (int r = 0; r < kScanRounds; r++) {
+    const uint64_t i = seg + (uint64_t)r * 32 + lane;
+    if (i < n) {
+      const uint32_t v = klen[i];
+      a += v;
+      b += (v + T - 1) / T;
+    }
+  }
+  a = warp_sum_i64(a);
+  b = warp_sum_i64(b);
+  if (lane == 0) {
+    sa[w] = a;
+    sb[w] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t ta = 0, tb = 0;
+    for (int q = 0; q < kScanWarps; q++) {
+      ta += sa[q];
+      tb += sb[q];
+    }
+    bs_a[blockIdx.x] = ta;
+    bs_b[blockIdx.x] = tb;
+  }
+}
+
+__device__ __forceinline__ int64_t warp_incl_scan(int64_t x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// One block: exclusive scan of the tile sums in place; totals to *tot_a/b.
+__global__ void __launch_bounds__(1024)
+    scan_tiles_kernel(int64_t *bs_a, int64_t *bs_b, uint32_t nb, int64_t *tot_a, int64_t *tot_b) {
+  __shared__ int64_t wa[32], wb[32];
+  __shared__ int64_t carry_a, carry_b;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) carry_a = carry_b = 0;
+  __syncthreads();
+  for (uint32_t c0 = 0; c0 < nb; c0 += 1024) {
+    const uint32_t i = c0 + threadIdx.x;
+    const int64_t va = (i < nb) ? bs_a[i] : 0, vb = (i < nb) ? bs_b[i] : 0;
+    const int64_t xa = warp_incl_scan(va, lane), xb = warp_incl_scan(vb, lane);
+    if (lane == 31) {
+      wa[w] = xa;
+      wb[w] = xb;
+    }
+    __syncthreads();
+    if (w == 0) {
+      const int64_t ya = warp_incl_scan(wa[lane], lane), yb = warp_incl_scan(wb[lane], lane);
+      wa[lane] = ya;
+      wb[lane] = yb;
+    }
+    __syncthreads();
+    const int64_t offa = carry_a + (w ? wa[w - 1] : 0) + xa - va;
+    const int64_t offb = carry_b + (w ? wb[w - 1] : 0) + xb - vb;
+    if (i < nb) {
+      bs_a[i] = offa;
+      bs_b[i] = offb;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry_a += wa[31];
+      carry_b += wb[31];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    *tot_a = carry_a;
+    *tot_b = carry_b;
+  }
+}
+
+__global__ void __launch_bounds__(kScanWarps * 32)
+    scan_apply_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
+                      const int64_t *__restrict__ bs_a, const int64_t *__restrict__ bs_b,
+                      int64_t *__restrict__ kex, int64_t *__restrict__ pex) {
+  __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
+  int64_t a = 0, b = 0;
+#pragma unroll
+  for (int r = 0; r < kScanRounds; r++) {
+    const uint64_t i = seg + (uint64_t)r * 32 + lane;
+    if (i < n) {
+      const uint32_t v = klen[i];
+      a += v;
+      b += (v + T - 1) / T;
+    }
+  }
+  a = warp_sum_i64(a);
+  b = warp_sum_i64(b);
+  if (lane == 0) {
+    sa[w] = a;
+    sb[w] = b;
+  }
+  __syncthreads();
+  int64_t ca = bs_a[blockIdx.x], cb = bs_b[blockIdx.x];
+  for (int q = 0; q < w; q++) {
+    ca += sa[q];
+    cb += sb[q];
+  }
+#pragma unroll
+  for (int r = 0; r < kScanRounds; r++) {
+    const uint64_t i = seg + (uint64_t)r * 32 + lane;
+    const uint32_t v = (i < n) ? klen[i] : 0u;
+    const int64_t va = v, vb = (v + T - 1) / T;
+    const int64_t xa = warp_incl_scan(va, lane), xb = warp_incl_scan(vb, lane);
+    if (i < n) {
+      kex[i] = ca + xa - va;
+      pex[i] = cb + xb - vb;
+    }
+    ca += __shfl_sync(0xffffffffu, xa, 31);
+    cb += __shfl_sync(0xffffffffu, xb, 31);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Prefix of each stream that the horizon can reach: the shortest run of
+// positions whose kept tokens exceed rmax_j * T (rmax_j = windows the horizon
+// asks of stream j), or the whole stream.  Windows 0..rmax_j - 1 hold at most
+// rmax_j * T tokens, so at least one piece follows them inside the prefix and
+// their greedy packing is the same as over the whole stream.
+__global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
+                              const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
+                              const int32_t *__restrict__ cum_last, uint32_t T,
+                              uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces) {
+  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= J) return;
+  const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
+  const uint64_t N = e - b;
+  const int64_t base = kex[b];
+  const int64_t need = (int64_t)cum_last[j] * (int64_t)T;
+  uint64_t c = N;
+  if (kex[e] - base > need) {
+    uint64_t lo = 1, hi = N;
+    while (lo < hi) {
+      const uint64_t mid = lo + (hi - lo) / 2;
+      if (kex[b + mid] - base > need)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    c = lo;
+  }
+  cutoff[j] = (uint32_t)c;
+  npieces[j] = pex[b + c] - pex[b];
+}
+
+// node_base[j] = sum over j' < j of (pieces of j' + 1 terminal node).
+__global__ void node_base_kernel(const int64_t *__restrict__ npieces, uint32_t J,
+                                 int64_t *__restrict__ node_base) {
+  const int lane = threadIdx.x & 31;
+  int64_t carry = 0;
+  for (uint32_t c0 = 0; c0 < J; c0 += 32) {
+    const uint32_t j = c0 + lane;
+    const int64_t v = (j < J) ? npieces[j] + 1 : 0;
+    const int64_t x = warp_incl_scan(v, lane);
+    if (j < J) node_base[j] = carry + x - v;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) node_base[J] = carry;
+}
+
+// ---------------------------------------------------------------------------
+// Pieces: the kept document at position p becomes ceil(L / T) pieces, T-chunks
+// from its start; node k of stream j holds the source index of its first
+// token, its document, its loss-mask threshold relative to the piece, and S,
+// the kept tokens of the stream before it.  The stream's last node is a
+// terminal with S = the prefix's kept tokens.
+__global__ void __launch_bounds__(kThreads)
+    expand_kernel(SegGrid g, const uint32_t *__restrict__ sdb, uint32_t D0,
+                  const uint32_t *__restrict__ cutoff, const uint32_t *__restrict__ order,
+                  const uint32_t *__restrict__ klen, const int64_t *__restrict__ kex,
+                  const int64_t *__restrict__ pex, const int64_t *__restrict__ node_base,
+                  const int64_t *__restrict__ npieces, const int64_t *__restrict__ offs,
+                  const int32_t *__restrict__ loss_start, uint32_t T,
+                  int64_t *__restrict__ node_src, int32_t *__restrict__ node_doc,
+                  int32_t *__restrict__ node_mthr, int64_t *__restrict__ node_S) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const uint64_t p = (uint64_t)blk * blockDim.x + threadIdx.x;
+  const uint64_t b = sdb[j] - D0;
+  const uint32_t c = cutoff[j];
+  if (p == 0) {
+    const int64_t term = node_base[j] + npieces[j];
+    node_S[term] = kex[b + c] - kex[b];
+    node_src[term] = 0;
+    node_doc[term] = -1;
+    node_mthr[term] = 0;
+  }
+  if (p >= c) return;
+  const uint64_t idx = b + p;
+  const uint32_t L = klen[idx];
+  if (L == 0) return;
+  const uint32_t d = order[idx];
+  const uint32_t n = (L + T - 1) / T;
+  const int64_t node0 = node_base[j] + (pex[idx] - pex[b]);
+  const int64_t sb = kex[idx] - kex[b];
+  const int64_t o = offs[d];
+  const int64_t ls = loss_start ? (int64_t)loss_start[d] : 0;
+  for (uint32_t q = 0; q < n; q++) {
+    const int64_t node = node0 + q;
+    const int64_t chunk = (int64_t)q * T;
+    node_src[node] = o + chunk;
+    node_doc[node] = (int32_t)d;
+    int64_t th = ls - chunk;
+    if (th < INT32_MIN) th = INT32_MIN;
+    node_mthr[node] = (int32_t)th;
+    node_S[node] = sb + chunk;
+  }
+}
+
+// next(q) = the last node q' in (q, terminal] with S[q'] - S[q] <= T: the
+// start of the window after a window that starts at q.
+__global__ void __launch_bounds__(kThreads)
+    next_kernel(SegGrid g, const int64_t *__restrict__ node_base,
+                const int64_t *__restrict__ npieces, const int64_t *__restrict__ node_S,
+                uint32_t T, int32_t *__restrict__ next) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const int64_t item = (int64_t)blk * blockDim.x + threadIdx.x;
+  const int64_t first = node_base[j], term = first + npieces[j];
+  const int64_t q = first + item;
+  if (q > term) return;
+  if (q == term) {
+    next[q] = (int32_t)q;
+    return;
+  }
+  const int64_t lim = node_S[q] + (int64_t)T;
+  const int64_t hi = min(term, q + (int64_t)T);
+  next[q] = (int32_t)last_le<int64_t, int64_t>(node_S, q + 1, hi + 1, lim);
+}
+
+__global__ void jump_level_kernel(const int32_t *__restrict__ up, int64_t n,
+                                  int32_t *__restrict__ out) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= n) return;
+  out[x] = __ldg(up + __ldg(up + x));
+}
+
+// W_j: hops from the stream's first node to its terminal, by binary lifting.
+__global__ void count_windows_kernel(const int32_t *__restrict__ levels, int64_t n_nodes,
+                                     uint32_t n_levels, const int64_t *__restrict__ node_base,
+                                     const int64_t *__restrict__ npieces, uint32_t J,
+                                     uint32_t *__restrict__ W) {
+  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= J) return;
+  if (npieces[j] == 0) {
+    W[j] = 0;
+    return;
+  }
+  const int64_t term = node_base[j] + npieces[j];
+  int64_t x = node_base[j];
+  uint64_t m = 0;
+  for (int l = (int)n_levels - 1; l >= 0; l--) {
+    const int64_t y = levels[(size_t)l * n_nodes + x];
+    if (y != term) {
+      x = y;
+      m += 1ull << l;
+    }
+  }
+  W[j] = (uint32_t)(m + 1);
+}
+
+// Window r of stream j starts at next^r(first): r's bits select the levels.
+__global__ void __launch_bounds__(kThreads)
+    window_starts_kernel(SegGrid g, const int32_t *__restrict__ levels, int64_t n_nodes,
+                         uint32_t n_levels, const int64_t *__restrict__ node_base,
+                         const uint32_t *__restrict__ W, const int64_t *__restrict__ wbase,
+                         int32_t *__restrict__ win_start) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
+  if (r >= (uint64_t)(wbase[j + 1] - wbase[j])) return;
+  int32_t s = -1;
+  if (r < W[j]) {
+    int64_t x = node_base[j];
+    for (uint32_t l = 0; l < n_levels; l++)
+      if ((r >> l) & 1) x = levels[(size_t)l * n_nodes + x];
+    s = (int32_t)x;
+  }
+  win_start[wbase[j] + r] = s;
+}
+
+// First update that asks a stream for a window past its last.
+__global__ void set_u32_kernel(uint32_t *p, uint32_t v) { *p = v; }
+
+__global__ void first_bad_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
+                                 uint32_t J, uint32_t K, uint32_t *first_bad) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (uint64_t)K * J) return;
+  const uint32_t k = (uint32_t)(i / J), j = (uint32_t)(i % J);
+  if ((uint32_t)cum[(size_t)(k + 1) * J + j] > W[j]) atomicMin(first_bad, k);
+}
+
+__global__ void valid_kernel(const uint32_t *first_bad, uint32_t K, uint32_t drain,
+                             uint32_t *valid) {
+  const uint32_t f = *first_bad;
+  *valid = (f >= K) ? K : (drain ? f + 1 : f);
+}
+
+// ---------------------------------------------------------------------------
+// Order digest: D = splitmix64(sum_i splitmix64(x_i ^ splitmix64(i)) ^ count)
+// over the item list (recipe scalars, source pairs, stream quads, the quota
+// of every valid update, the first piece of every window those updates use).
+__device__ __forceinline__ uint64_t digest_term(uint64_t item, uint64_t index) {
+  return splitmix64(item ^ splitmix64(index));
+}
+
+__device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long long *acc) {
+  __shared__ uint64_t scratch[33];
+  const uint64_t s = block_sum<uint64_t>(term, scratch);
+  if (threadIdx.x == 0) atomicAdd(acc, (unsigned long long)s);
+}
+
+__global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
+                                     unsigned long long *acc) {
+  const uint64_t n = 10ull + 2ull * h.S + 4ull * h.J;
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint64_t term = 0;
+  if (i < n) {
+    uint64_t x;
+    if (i < 10) {
+      x = (i == 3) ? (uint64_t)*valid : h.scalars[i];
+    } else if (i < 10ull + 2ull * h.S) {
+      const uint64_t q = i - 10, s = q >> 1;
+      x = (q & 1) ? (uint64_t)h.source_bp[s] : (uint64_t)h.source_weight[s];
+    } else {
+      const uint64_t q = i - 10 - 2ull * h.S, j = q >> 2;
+      switch (q & 3) {
+        case 0: x = h.sdb[j]; break;
+        case 1: x = h.sdb[j + 1]; break;
+        case 2: x = h.ssrc[j]; break;
+        default: x = h.tw[j]; break;
+      }
+    }
+    term = digest_term(x, i);
+  }
+  digest_accumulate(term, acc);
+}
+
+__global__ void digest_quota_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
+                                    uint64_t h0, const uint32_t *valid,
+                                    unsigned long long *acc) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint64_t term = 0;
+  if (i < (uint64_t)K * J && i / J < *valid) term = digest_term((uint64_t)quota[i], h0 + i);
+  digest_accumulate(term, acc);
+}
+
+__global__ void digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
+                                   uint32_t J, const uint32_t *valid, int64_t *ubase) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t v = *valid;
+  int64_t carry = 0;
+  for (uint32_t c0 = 0; c0 < J; c0 += 32) {
+    const uint32_t j = c0 + lane;
+    int64_t u = 0;
+    if (j < J) u = min((int64_t)cum[(size_t)v * J + j], (int64_t)W[j]);
+    const int64_t x = warp_incl_scan(u, lane);
+    if (j < J) ubase[j] = carry + x - u;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) ubase[J] = carry;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    digest_windows_kernel(SegGrid g, const int64_t *__restrict__ wbase,
+                          const int32_t *__restrict__ win_start,
+                          const int64_t *__restrict__ node_src,
+                          const int32_t *__restrict__ node_doc, const int64_t *__restrict__ offs,
+                          uint32_t T, uint64_t h0, uint32_t J, const uint32_t *valid,
+                          const int64_t *__restrict__ ubase, unsigned long long *acc) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
+  const uint64_t U = (uint64_t)(ubase[j + 1] - ubase[j]);
+  uint64_t term = 0;
+  if (r < U) {
+    const int32_t node = win_start[wbase[j] + r];
+    const int32_t d = node_doc[node];
+    const uint64_t chunk = (uint64_t)(node_src[node] - offs[d]) / T;
+    const uint64_t x = ((uint64_t)(uint32_t)d << 32) | (chunk & 0xFFFFFFFFull);
+    term = digest_term(x, h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[j] + r);
+  }
+  digest_accumulate(term, acc);
+}
+
+__global__ void digest_final_kernel(const unsigned long long *acc, uint64_t h0, uint32_t J,
+                                    const uint32_t *valid, const int64_t *ubase,
+                                    uint64_t *digest) {
+  const uint64_t count = h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[J];
+  *digest = splitmix64((uint64_t)acc[0] ^ count);
+}
+
+}  // namespace
+
+// ===========================================================================
+// launchers
+cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
+                                    int *err, cudaStream_t st) {
+  validate_offsets_kernel<<<blocks_for((uint64_t)n_docs + 1), kThreads, 0, st>>>(offs, n_docs,
+                                                                                  n_tokens, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st) {
+  stream_keys_kernel<<<blocks_for((uint64_t)J * 4), kThreads, 0, st>>>(seed, J, keys);
+  return cudaGetLastError();
+}
+
+static unsigned round_warps(uint32_t n) {
+  unsigned t = ((n + 31) / 32) * 32;
+  return t < 32 ? 32 : t;
+}
+
+cudaError_t launch_quota_sources(const uint32_t *sw, uint32_t S, uint32_t B, uint32_t K,
+                                 int32_t *src_quota, cudaStream_t st) {
+  quota_sources_kernel<<<1, round_warps(S), 0, st>>>(sw, S, B, K, src_quota);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
+                                const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
+                                uint32_t max_strata, int32_t *quota, int32_t *cum,
+                                cudaStream_t st) {
+  quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(src_quota, tw, src_first, S, J, K,
+                                                             quota, cum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
+                            cudaStream_t st) {
+  row_base_kernel<<<blocks_for(K, 128), 128, 0, st>>>(quota, J, K, rb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hash_docs(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
+                             const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
+                             uint8_t *heldout, unsigned long long *counter, int n_sms,
+                             cudaStream_t st) {
+  hash_docs_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, hash_key,
+                                                   heldout, counter);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
+                         const int64_t *offs, const uint8_t *heldout, uint32_t D0,
+                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
+  if (g.n_blocks == 0) return cudaSuccess;
+  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, heldout, D0, order, klen,
+                                                err);
+  return cudaGetLastError();
+}
+
+size_t scan_scratch_bytes(uint64_t n) {
+  const uint64_t nb = (n + kScanTile - 1) / kScanTile;
+  return (size_t)(nb + 1) * 2 * sizeof(int64_t);
+}
+
+cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
+                               int64_t *pex, void *scratch, size_t scratch_bytes,
+                               cudaStream_t st) {
+  const uint64_t nb = (n + kScanTile - 1) / kScanTile;
+  if (scratch_bytes < scan_scratch_bytes(n)) return cudaErrorInvalidValue;
+  int64_t *bs_a = static_cast<int64_t *>(scratch);
+  int64_t *bs_b = bs_a + (nb + 1);
+  if (nb > 0) {
+    scan_reduce_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  scan_tiles_kernel<<<1, 1024, 0, st>>>(bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || nb == 0) return e;
+  scan_apply_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b, kex, pex);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
+                          const int64_t *pex, const int32_t *cum_last, uint32_t T,
+                          uint32_t *cutoff, int64_t *npieces, cudaStream_t st) {
+  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, cutoff,
+                                                    npieces);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
+                             cudaStream_t st) {
+  node_base_kernel<<<1, 32, 0, st>>>(npieces, J, node_base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uint32_t *cutoff,
+                          const uint32_t *order, const uint32_t *klen, const int64_t *kex,
+                          const int64_t *pex, const int64_t *node_base, const int64_t *npieces,
+                          const int64_t *offs, const int32_t *loss_start, uint32_t T,
+                          int64_t *node_src, int32_t *node_doc, int32_t *node_mthr,
+                          int64_t *node_S, cudaStream_t st) {
+  if (g.n_blocks == 0) return cudaSuccess;
+  expand_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, order, klen, kex, pex,
+                                                 node_base, npieces, offs, loss_start, T,
+                                                 node_src, node_doc, node_mthr, node_S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_next(SegGrid g, const int64_t *node_base, const int64_t *npieces,
+                        const int64_t *node_S, uint32_t T, int32_t *next, cudaStream_t st) {
+  if (g.n_blocks == 0) return cudaSuccess;
+  next_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, node_base, npieces, node_S, T, next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
+                              cudaStream_t st) {
+  jump_level_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
+                                                                         up_next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_t n_levels,
+                                 const int64_t *node_base, const int64_t *npieces, uint32_t J,
+                                 uint32_t *W, cudaStream_t st) {
+  count_windows_kernel<<<blocks_for(J, 128), 128, 0, st>>>(levels, n_nodes, n_levels, node_base,
+                                                           npieces, J, W);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nodes,
+                                 uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
+                                 const int64_t *wbase, int32_t *win_start, cudaStream_t st) {
+  if (g.n_blocks == 0) return cudaSuccess;
+  window_starts_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, levels, n_nodes, n_levels, node_base,
+                                                        W, wbase, win_start);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
+                               uint32_t drain, uint32_t *first_bad, uint32_t *valid,
+                               cudaStream_t st) {
+  set_u32_kernel<<<1, 1, 0, st>>>(first_bad, K);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  first_bad_kernel<<<blocks_for((uint64_t)K * J), kThreads, 0, st>>>(cum, W, J, K, first_bad);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  valid_kernel<<<1, 1, 0, st>>>(first_bad, K, drain, valid);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const int32_t *quota,
+                          const int32_t *cum, const uint32_t *W, SegGrid wg,
+                          const int64_t *wbase, const int32_t *win_start,
+                          const int64_t *node_src, const int32_t *node_doc,
+                          const int64_t *offs, uint32_t T, uint32_t K,
+                          unsigned long long *acc, int64_t *ubase, uint64_t *digest_out,
+                          cudaStream_t st) {
+  const uint64_t h0 = 10ull + 2ull * h.S + 4ull * h.J;
+  digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  digest_quota_kernel<<<blocks_for((uint64_t)K * h.J), kThreads, 0, st>>>(quota, h.J, K, h0,
+                                                                           valid, acc);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  digest_used_kernel<<<1, 32, 0, st>>>(cum, W, h.J, valid, ubase);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (wg.n_blocks > 0) {
+    digest_windows_kernel<<<wg.n_blocks, kThreads, 0, st>>>(wg, wbase, win_start, node_src,
+                                                            node_doc, offs, T, h0, h.J, valid,
+                                                            ubase, acc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  digest_final_kernel<<<1, 1, 0, st>>>(acc, h0, h.J, valid, ubase, digest_out);
+  return cudaGetLastError();
+}
+
+}  // namespace nsk

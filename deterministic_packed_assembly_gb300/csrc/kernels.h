@@ -1,0 +1,122 @@
+// Host-side launchers of the library's kernels (internal interface between
+// the C ABI in api.cu and the kernels in init_kernels.cu / gather.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace nsk {
+
+// A launch over per-stream segments: stream j owns items [0, count_j), laid
+// out in blocks of `block` items; blk_base[j] is the first block of stream j
+// (host-computed prefix, J + 1 entries, on the device).
+struct SegGrid {
+  const uint32_t *blk_base;  // [J + 1]
+  uint32_t J;
+  uint32_t n_blocks;
+};
+
+// ---- validation, keys, quotas ---------------------------------------------
+cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
+                                    int *err, cudaStream_t st);
+cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st);
+cudaError_t launch_quota_sources(const uint32_t *source_weight, uint32_t S, uint32_t B,
+                                 uint32_t K, int32_t *src_quota, cudaStream_t st);
+cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *stream_weight,
+                                const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
+                                uint32_t max_strata, int32_t *quota, int32_t *cum,
+                                cudaStream_t st);
+cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
+                            cudaStream_t st);
+
+// ---- held-out hash, order, scans ------------------------------------------
+cudaError_t launch_hash_docs(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
+                             const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
+                             uint8_t *heldout, unsigned long long *counter, int n_sms,
+                             cudaStream_t st);
+cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
+                         const int64_t *offs, const uint8_t *heldout, uint32_t D0,
+                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st);
+// kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
+cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
+                               int64_t *pex, void *scratch, size_t scratch_bytes,
+                               cudaStream_t st);
+size_t scan_scratch_bytes(uint64_t n);
+// per stream: cutoff c_j, pieces before it, node base; rmax given
+cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
+                          const int64_t *pex, const int32_t *cum_last, uint32_t T,
+                          uint32_t *cutoff, int64_t *npieces, cudaStream_t st);
+cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
+                             cudaStream_t st);
+
+// ---- pieces, next, jump tables, windows -----------------------------------
+cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uint32_t *cutoff,
+                          const uint32_t *order, const uint32_t *klen, const int64_t *kex,
+                          const int64_t *pex, const int64_t *node_base, const int64_t *npieces,
+                          const int64_t *offs, const int32_t *loss_start, uint32_t T,
+                          int64_t *node_src, int32_t *node_doc, int32_t *node_mthr,
+                          int64_t *node_S, cudaStream_t st);
+cudaError_t launch_next(SegGrid g, const int64_t *node_base, const int64_t *npieces,
+                        const int64_t *node_S, uint32_t T, int32_t *next, cudaStream_t st);
+cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
+                              cudaStream_t st);
+// levels: [n_levels][n_nodes], level l maps a node to the node 2^l windows on
+cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_t n_levels,
+                                 const int64_t *node_base, const int64_t *npieces, uint32_t J,
+                                 uint32_t *W, cudaStream_t st);
+cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nodes,
+                                 uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
+                                 const int64_t *wbase, int32_t *win_start, cudaStream_t st);
+cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
+                               uint32_t drain, uint32_t *first_bad, uint32_t *valid,
+                               cudaStream_t st);
+
+// ---- order digest ---------------------------------------------------------
+struct DigestHeader {
+  uint64_t scalars[10];
+  const uint32_t *source_weight;  // [S]
+  const uint16_t *source_bp;      // [S]
+  const uint32_t *sdb;            // [J + 1]
+  const uint32_t *ssrc;           // [J]
+  const uint32_t *tw;             // [J]
+  uint32_t S, J;
+};
+cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const int32_t *quota,
+                          const int32_t *cum, const uint32_t *W, SegGrid wg,
+                          const int64_t *wbase, const int32_t *win_start,
+                          const int64_t *node_src, const int32_t *node_doc,
+                          const int64_t *offs, uint32_t T, uint32_t K,
+                          unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
+                          uint64_t *digest_out, cudaStream_t st);
+
+// ---- per-step assembly ----------------------------------------------------
+struct GatherParams {
+  // corpus
+  const int32_t *tokens;
+  // context tables
+  const int32_t *rb;        // [K][J + 1]
+  const int32_t *cum;       // [K + 1][J]
+  const uint32_t *W;        // [J]
+  const int64_t *wbase;     // [J]
+  const int32_t *win_start; // [sum rmax]
+  const int32_t *next;      // [nodes]
+  const int64_t *node_S;    // [nodes]
+  const int64_t *node_src;  // [nodes]
+  const int32_t *node_doc;  // [nodes]
+  const int32_t *node_mthr; // [nodes]
+  int *err;
+  // launch
+  uint32_t J, T, step0, n_steps, row0, n_rows;
+  int32_t pad_id;
+  // outputs
+  int32_t *tokens_out, *pos_out, *doc_out;
+  uint8_t *mask_out;
+  uint64_t *row_fp;
+  int32_t *row_learned;
+};
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
+cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
+                            uint64_t *out, cudaStream_t st);
+
+}  // namespace nsk

@@ -1,0 +1,188 @@
+"""A thin PyTorch-facing wrapper over the C ABI.
+
+PyTorch supplies device memory (its caching allocator, through the
+library's allocation callback), the CUDA stream and the output tensors.  All
+packing work runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def _u32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=np.uint32)
+
+
+class Packer:
+    """A packing context over a corpus resident on one CUDA device.
+
+    ``tokens`` (int32), ``doc_offsets`` (int64, n_docs + 1) and ``loss_start``
+    (int32 or None) are device tensors that must outlive the packer.  The
+    recipe arrays may be numpy arrays or lists.
+    """
+
+    def __init__(self, tokens: torch.Tensor, doc_offsets: torch.Tensor,
+                 loss_start: Optional[torch.Tensor], *, stream_doc_begin, stream_source,
+                 source_weight, stream_weight, source_heldout_bp, T: int, B: int,
+                 max_steps: int, seed: int = 0, hash_key: int = 0, drain: bool = False,
+                 pad_id: int = 0, stream: Optional[torch.cuda.Stream] = None):
+        if not tokens.is_cuda:
+            raise ValueError("tokens must be a CUDA tensor")
+        assert tokens.dtype == torch.int32 and tokens.is_contiguous()
+        assert doc_offsets.dtype == torch.int64 and doc_offsets.is_contiguous()
+        assert doc_offsets.device == tokens.device
+        if loss_start is not None:
+            assert loss_start.dtype == torch.int32 and loss_start.is_contiguous()
+            assert loss_start.device == tokens.device
+        self.device = tokens.device
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.T, self.B, self.max_steps = int(T), int(B), int(max_steps)
+        self._corpus = (tokens, doc_offsets, loss_start)
+        self._tables = [_u32(stream_doc_begin), _u32(stream_source), _u32(source_weight),
+                        _u32(stream_weight),
+                        np.ascontiguousarray(np.asarray(source_heldout_bp), dtype=np.uint16)]
+        sdb, ssrc, sw, tw, bp = self._tables
+        self.n_streams = int(ssrc.size)
+        self.n_sources = int(sw.size)
+        dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
+        stream_handle = self.stream.cuda_stream
+
+        def _alloc(nbytes, _user):
+            try:
+                return torch.cuda.caching_allocator_alloc(int(nbytes), dev_index, self.stream)
+            except Exception:  # out of memory: the library reports NS_ERR_OOM
+                return None
+
+        def _free(ptr, _user):
+            torch.cuda.caching_allocator_delete(ptr)
+
+        self._alloc_cb = L.ns_alloc_fn(_alloc)
+        self._free_cb = L.ns_free_fn(_free)
+        cfg = L.ns_pack_config()
+        cfg.tokens = tokens.data_ptr()
+        cfg.n_tokens = tokens.numel()
+        cfg.doc_offsets = doc_offsets.data_ptr()
+        cfg.loss_start = None if loss_start is None else loss_start.data_ptr()
+        cfg.n_docs = doc_offsets.numel() - 1
+        cfg.n_sources = self.n_sources
+        cfg.n_streams = self.n_streams
+        cfg.T = self.T
+        cfg.stream_doc_begin = sdb.ctypes.data
+        cfg.stream_source = ssrc.ctypes.data
+        cfg.source_weight = sw.ctypes.data
+        cfg.stream_weight = tw.ctypes.data
+        cfg.source_heldout_bp = bp.ctypes.data
+        cfg.seed = int(seed) & ((1 << 64) - 1)
+        cfg.hash_key = int(hash_key) & ((1 << 64) - 1)
+        cfg.B = self.B
+        cfg.max_steps = self.max_steps
+        cfg.flags = L.NS_PACK_DRAIN if drain else 0
+        cfg.pad_id = int(pad_id)
+        cfg.cuda_stream = stream_handle
+        cfg.alloc = self._alloc_cb
+        cfg.free = self._free_cb
+        cfg.alloc_user = None
+        with torch.cuda.device(self.device):
+            self._ctx = L.ns_pack_init(cfg)
+        info = L.ns_pack_info(self._ctx)
+        self.valid_steps = info["valid_steps"]
+        self.order_digest = info["order_digest"]
+        self.info = info
+
+    @classmethod
+    def from_corpus(cls, corpus, device="cuda", **overrides) -> "Packer":
+        """Copy a ``corpus.Corpus``-like object's arrays to ``device`` and
+        build a packer with its recipe (fields may be overridden)."""
+        dev = torch.device(device)
+        tok = torch.from_numpy(np.ascontiguousarray(corpus.tokens)).to(dev)
+        off = torch.from_numpy(np.ascontiguousarray(corpus.doc_offsets)).to(dev)
+        ls = None
+        if corpus.loss_start is not None:
+            ls = torch.from_numpy(np.ascontiguousarray(corpus.loss_start)).to(dev)
+        kw = dict(stream_doc_begin=corpus.stream_doc_begin, stream_source=corpus.stream_source,
+                  source_weight=corpus.source_weight, stream_weight=corpus.stream_weight,
+                  source_heldout_bp=corpus.source_heldout_bp, T=corpus.T, B=corpus.B,
+                  max_steps=corpus.max_steps, seed=corpus.seed, hash_key=corpus.hash_key,
+                  drain=corpus.drain, pad_id=corpus.pad_id)
+        kw.update(overrides)
+        return cls(tok, off, ls, **kw)
+
+    # ---- outputs -----------------------------------------------------------
+    def empty_out(self, n_steps: int = 1, n_rows: Optional[int] = None) -> dict:
+        n_rows = self.B if n_rows is None else n_rows
+        shape = (n_steps, n_rows, self.T)
+        d = self.device
+        return dict(tokens=torch.empty(shape, dtype=torch.int32, device=d),
+                    pos=torch.empty(shape, dtype=torch.int32, device=d),
+                    doc=torch.empty(shape, dtype=torch.int32, device=d),
+                    mask=torch.empty(shape, dtype=torch.uint8, device=d),
+                    row_fp=torch.empty((n_steps, n_rows), dtype=torch.int64, device=d),
+                    row_learned=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d))
+
+    @staticmethod
+    def _out_struct(out: dict) -> L.ns_pack_out:
+        o = L.ns_pack_out()
+        o.tokens = out["tokens"].data_ptr()
+        o.pos = out["pos"].data_ptr()
+        o.doc = out["doc"].data_ptr()
+        o.mask = out["mask"].data_ptr()
+        o.row_fp = out["row_fp"].data_ptr()
+        o.row_learned = out["row_learned"].data_ptr()
+        return o
+
+    def step(self, step0: int, n_steps: int = 1, rows: Optional[tuple] = None,
+             out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+        """Assemble rows ``rows = (begin, end)`` of updates [step0, step0 +
+        n_steps) into ``out`` (allocated if None); asynchronous."""
+        r0, r1 = (0, self.B) if rows is None else rows
+        if out is None:
+            out = self.empty_out(n_steps, r1 - r0)
+        st = (stream or self.stream).cuda_stream
+        L.ns_pack_step(self._ctx, step0, n_steps, r0, r1, self._out_struct(out), st)
+        return out
+
+    def batch_fp(self, row_fp: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Fold one batch's row fingerprints (device, row order); synchronises."""
+        st = (stream or self.stream).cuda_stream
+        return L.ns_pack_fingerprint(self._ctx, row_fp.data_ptr(), row_fp.numel(), st)
+
+    def batch_fp_many(self, row_fp: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Batch fingerprints of [n_steps, n_rows] row fingerprints (async)."""
+        n_steps, n_rows = row_fp.shape
+        if out is None:
+            out = torch.empty(n_steps, dtype=torch.int64, device=self.device)
+        st = (stream or self.stream).cuda_stream
+        L.ns_pack_batch_fp(self._ctx, row_fp.data_ptr(), n_steps, n_rows, out.data_ptr(), st)
+        return out
+
+    def stream_windows(self):
+        return L.ns_pack_stream_windows(self._ctx, self.n_streams)
+
+    def quota_table(self):
+        return L.ns_pack_quota_table(self._ctx, self.max_steps, self.n_streams)
+
+    def check(self) -> None:
+        L.ns_pack_check(self._ctx)
+
+    def close(self) -> None:
+        if getattr(self, "_ctx", None) is not None and self._ctx.value:
+            L.ns_pack_free(self._ctx)
+            self._ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def as_u64(t: torch.Tensor) -> np.ndarray:
+    """Row fingerprints come back as int64 tensors; view them as uint64."""
+    return t.detach().cpu().numpy().view(np.uint64)

@@ -1,0 +1,197 @@
+/*
+ * nspack.h -- C ABI of the GB300 library for deterministic packed assembly.
+ *
+ * Pre-tokenized documents from a weighted mixture of sources become fixed
+ * [B, T] global batches (tokens, position ids, document ids, loss masks) plus
+ * a 64-bit fingerprint and a learned-position count per row.  A batch depends
+ * only on the recipe, the seed and the update index, never on how its rows are
+ * split between calls, devices or processes.
+ *
+ * What the operations compute, and where it is stated:
+ *  - held-out split: 1 % of every source's documents (5 % for one source), by
+ *    a hash of the document's text, the same in every line -- NeuronSpark-
+ *    Trainer README, Concepts;
+ *  - shuffle: a file's documents are visited in a seed-keyed random order --
+ *    same section;
+ *  - mixture: every update holds each source within two samples of its
+ *    recipe share, and each stratum of a source at its share -- same section;
+ *  - packing: windows of exactly T positions, cut at document ends, padded at
+ *    the end -- same section, and Linnet training docs, Supervised
+ *    fine-tuning; a document longer than T is cut into T-chunks;
+ *  - assembly: a position id of 0 starts a new sequence within a row (Linnet
+ *    training docs, Other trainers); only completion tokens are learned and a
+ *    step is weighed by its count of learned positions (Supervised
+ *    fine-tuning); rows past the end of the data learn nothing (Reinforcement
+ *    learning, JAX);
+ *  - elastic determinism: every global batch is byte-identical whatever the
+ *    number of GPUs -- "Zephon: deterministic data loading", checkpoint on 16
+ *    GPUs, resume on 8/32/64;
+ *  - max_epochs 1: a used-up source is an error, not a second pass --
+ *    NeuronSpark-Trainer README, Concepts; a resume checks the sample order's
+ *    digest -- same README, Training.
+ *
+ * Conventions for every entry point:
+ *  - All integers are little-endian; u64 arithmetic wraps.
+ *  - Every argument is checked on the host before anything is enqueued; a
+ *    failing check returns a negative NS_ERR_* code and changes nothing.
+ *  - Kernels never trap.  An inconsistency found on the device is recorded in
+ *    the context's device error word and reported by the next call that
+ *    synchronises (ns_pack_fingerprint, ns_pack_check).
+ *  - The context is immutable after ns_pack_init returns, so ns_pack_step may
+ *    run concurrently on different CUDA streams.
+ */
+#ifndef NSPACK_H
+#define NSPACK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define NS_OK 0
+#define NS_ERR_INVALID_ARG (-1) /* an argument or the recipe is out of range */
+#define NS_ERR_CUDA (-2)        /* a CUDA runtime call failed */
+#define NS_ERR_OOM (-3)         /* the allocator returned NULL */
+#define NS_ERR_EXHAUSTED (-4)   /* a stream has no window left for this update */
+#define NS_ERR_HORIZON (-5)     /* update index at or past max_steps */
+#define NS_ERR_BAD_INPUT (-6)   /* doc_offsets malformed (found on the device) */
+#define NS_ERR_DEVICE (-7)      /* a kernel recorded an inconsistency */
+
+/* ---- flags -------------------------------------------------------------- */
+/* Allow the first update that runs a stream dry: its rows past the stream's
+ * last window are empty (pad, pos 0, doc -1, mask 0); later updates return
+ * NS_ERR_EXHAUSTED. */
+#define NS_PACK_DRAIN 1u
+
+/* ---- limits ------------------------------------------------------------- */
+#define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
+#define NS_MAX_SOURCES 1024u
+#define NS_MAX_STRATA_PER_SOURCE 1024u
+#define NS_MAX_STREAMS 65536u
+
+typedef struct ns_pack_ctx ns_pack_ctx;
+
+/* Device memory for the context's tables.  Called only inside ns_pack_init
+ * (allocations) and ns_pack_init / ns_pack_free (frees); NULL alloc means
+ * cudaMalloc / cudaFree.  Returned pointers must be 256-byte aligned. */
+typedef void *(*ns_alloc_fn)(size_t bytes, void *user);
+typedef void (*ns_free_fn)(void *ptr, void *user);
+
+typedef struct {
+  /* Corpus, on the device, borrowed (must outlive the context).  Documents
+   * are contiguous runs of tokens: document d is tokens[doc_offsets[d] ..
+   * doc_offsets[d+1]).  tokens must be 16-byte aligned. */
+  const int32_t *tokens;
+  uint64_t n_tokens;
+  const int64_t *doc_offsets; /* [n_docs + 1], nondecreasing, lengths < 2^31 */
+  const int32_t *loss_start;  /* [n_docs] or NULL: a token at in-document
+                                 offset o is learned iff o >= loss_start[d];
+                                 NULL learns every token */
+  uint32_t n_docs;            /* < 2^31 */
+  uint32_t n_sources;         /* 1 .. NS_MAX_SOURCES */
+  uint32_t n_streams;         /* 1 .. NS_MAX_STREAMS: (source, stratum) pairs */
+  uint32_t T;                 /* window length, multiple of 16, <= NS_MAX_T */
+  /* Recipe, on the host, copied by ns_pack_init. */
+  const uint32_t *stream_doc_begin;  /* [n_streams + 1], nondecreasing, <= n_docs:
+                                        stream j owns documents [b[j], b[j+1]) */
+  const uint32_t *stream_source;     /* [n_streams], nondecreasing, < n_sources;
+                                        every source owns >= 1 stream */
+  const uint32_t *source_weight;     /* [n_sources], > 0 */
+  const uint32_t *stream_weight;     /* [n_streams], > 0, relative within its source */
+  const uint16_t *source_heldout_bp; /* [n_sources], 0 .. 10000 basis points */
+  uint64_t seed;     /* keys the shuffle */
+  uint64_t hash_key; /* keys the held-out hash (not the seed: same in every line) */
+  uint32_t B;        /* rows per update (global batch), >= 1 */
+  uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
+  uint32_t flags;    /* NS_PACK_DRAIN */
+  int32_t pad_id;    /* token written at padded positions */
+  void *cuda_stream; /* cudaStream_t for init and default for the other calls */
+  ns_alloc_fn alloc;
+  ns_free_fn free;
+  void *alloc_user;
+} ns_pack_config;
+
+/* Caller-owned device outputs of ns_pack_step, row-major
+ * [n_steps][row_end - row_begin][T]; tokens/pos/doc/mask 16-byte aligned. */
+typedef struct {
+  int32_t *tokens;
+  int32_t *pos;
+  int32_t *doc;
+  uint8_t *mask;
+  uint64_t *row_fp;     /* [n_steps][rows] */
+  int32_t *row_learned; /* [n_steps][rows] */
+} ns_pack_out;
+
+typedef struct {
+  uint32_t valid_steps; /* updates [0, valid_steps) can be assembled */
+  uint32_t max_steps;
+  uint32_t n_streams;
+  uint32_t T;
+  uint32_t B;
+  uint32_t levels;      /* pointer-jumping levels used at init */
+  uint64_t order_digest;
+  uint64_t n_pieces;    /* pieces (document T-chunks) built at init */
+  uint64_t table_bytes; /* device bytes the context keeps */
+} ns_pack_info_t;
+
+/* Build the context: validate, then on cfg->cuda_stream hash the documents of
+ * every source with a held-out rate, shuffle every stream, pack the prefix of
+ * each stream that max_steps can reach, number its windows and apportion every
+ * update of the horizon.  Synchronises the stream (three times).  On success
+ * *out owns device tables allocated through cfg->alloc; on failure nothing is
+ * kept and *out is NULL.  Errors: INVALID_ARG, CUDA, OOM, BAD_INPUT. */
+int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out);
+
+/* Assemble rows [row_begin, row_end) of updates [step0, step0 + n_steps) into
+ * `out`, asynchronously on cuda_stream (NULL: the context's stream).  One
+ * kernel launch.  The bytes of every row are the same whatever the row range
+ * or the step batching.  Errors: INVALID_ARG (n_steps == 0, empty or out-of-
+ * range rows, NULL or misaligned outputs), HORIZON (step0 + n_steps >
+ * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA. */
+int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,
+                 uint32_t row_end, const ns_pack_out *out, void *cuda_stream);
+
+/* Fold n_rows row fingerprints (device, in row order) into the batch
+ * fingerprint F = fold(F ^ fp_i) and copy it to *batch_fp_host; synchronises
+ * cuda_stream (NULL: the context's).  Also reports the device error word.
+ * Errors: INVALID_ARG, CUDA, DEVICE. */
+int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,
+                        uint64_t *batch_fp_host, void *cuda_stream);
+
+/* Asynchronous variant for n_steps consecutive batches of n_rows rows each:
+ * batch_fp_dev[s] = fold of row_fp_dev[s * n_rows .. (s + 1) * n_rows).
+ * Errors: INVALID_ARG, CUDA. */
+int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
+                     uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream);
+
+/* Summary of the context (host memory, no synchronisation). */
+int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info);
+
+/* Per stream (host arrays of n_streams): windows packed at init and whether
+ * that count is the stream's total (1) or only the prefix the horizon reaches
+ * (0, in which case it exceeds every window the horizon asks for). */
+int ns_pack_stream_windows(const ns_pack_ctx *ctx, uint64_t *windows, uint8_t *complete);
+
+/* Copy the quota tables to the host: quota[k][j] windows of stream j in
+ * update k (max_steps x n_streams, int32) and cum[k][j] windows before update
+ * k ((max_steps + 1) x n_streams, int32).  Either may be NULL.  Synchronises
+ * the context's stream.  Errors: INVALID_ARG, CUDA. */
+int ns_pack_quota_table(const ns_pack_ctx *ctx, int32_t *quota, int32_t *cum);
+
+/* Synchronise the context's stream and report the device error word.
+ * Errors: CUDA, DEVICE, BAD_INPUT. */
+int ns_pack_check(ns_pack_ctx *ctx);
+
+/* Release every table of the context (NULL is a no-op).  Synchronises. */
+void ns_pack_free(ns_pack_ctx *ctx);
+
+const char *ns_pack_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSPACK_H */

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library loads, exports every entry point that ``include/nspack.h``
+declares, and rejects bad arguments on the host before touching the device.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w ]+?\**\s*\b(ns_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def nspack():
+    import __graft_entry__
+    __graft_entry__.build()
+    import deterministic_packed_assembly_gb300 as m
+    return m
+
+
+def test_library_exports_every_declared_symbol(nspack):
+    declared = _declared_symbols()
+    assert {"ns_pack_init", "ns_pack_step", "ns_pack_fingerprint"} <= declared
+    lib = C.CDLL(nspack.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert declared == set(nspack.SYMBOLS)
+
+
+def test_strerror(nspack):
+    assert nspack.ns_pack_strerror(0) == "ok"
+    for code in range(-7, 0):
+        assert nspack.ns_pack_strerror(code) != "unknown error"
+
+
+def _cfg(nspack, **kw):
+    L = nspack._lib
+    keep = dict(tok=np.zeros(64, np.int32), off=np.asarray([0, 10, 20], np.int64),
+                sdb=np.asarray([0, 2], np.uint32), ssrc=np.zeros(1, np.uint32),
+                sw=np.ones(1, np.uint32), tw=np.ones(1, np.uint32),
+                bp=np.zeros(1, np.uint16))
+    c = L.ns_pack_config()
+    # host pointers stand in for device ones: every check below fails before use
+    c.tokens = keep["tok"].ctypes.data & ~15
+    c.n_tokens = 64
+    c.doc_offsets = keep["off"].ctypes.data
+    c.n_docs = 2
+    c.n_sources = 1
+    c.n_streams = 1
+    c.T = 16
+    c.stream_doc_begin = keep["sdb"].ctypes.data
+    c.stream_source = keep["ssrc"].ctypes.data
+    c.source_weight = keep["sw"].ctypes.data
+    c.stream_weight = keep["tw"].ctypes.data
+    c.source_heldout_bp = keep["bp"].ctypes.data
+    c.B = 2
+    c.max_steps = 4
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c, keep
+
+
+@pytest.mark.parametrize("field,value", [
+    ("T", 0), ("T", 8), ("T", 24), ("T", (1 << 24) + 16), ("B", 0), ("max_steps", 0),
+    ("max_steps", 1 << 30), ("n_sources", 0), ("n_streams", 0), ("n_streams", 70000),
+    ("flags", 2), ("tokens", None), ("doc_offsets", None), ("stream_doc_begin", None),
+])
+def test_init_rejects_bad_recipe(nspack, field, value):
+    c, keep = _cfg(nspack, **{field: value})
+    with pytest.raises(nspack.NsPackError) as e:
+        nspack.ns_pack_init(c)
+    assert e.value.code == nspack.NS_ERR_INVALID_ARG
+
+
+def test_init_rejects_bad_tables(nspack):
+    for name, arr in (("sw", np.zeros(1, np.uint32)), ("tw", np.zeros(1, np.uint32)),
+                      ("bp", np.asarray([10001], np.uint16)),
+                      ("ssrc", np.asarray([1], np.uint32)),
+                      ("sdb", np.asarray([0, 3], np.uint32))):
+        c, keep = _cfg(nspack)
+        keep[name] = arr
+        field = dict(sw="source_weight", tw="stream_weight", bp="source_heldout_bp",
+                     ssrc="stream_source", sdb="stream_doc_begin")[name]
+        setattr(c, field, arr.ctypes.data)
+        with pytest.raises(nspack.NsPackError) as e:
+            nspack.ns_pack_init(c)
+        assert e.value.code == nspack.NS_ERR_INVALID_ARG, name
+
+
+def test_init_rejects_misaligned_tokens(nspack):
+    c, keep = _cfg(nspack)
+    c.tokens = c.tokens + 4
+    with pytest.raises(nspack.NsPackError) as e:
+        nspack.ns_pack_init(c)
+    assert e.value.code == nspack.NS_ERR_INVALID_ARG
+
+
+def test_null_context_is_rejected(nspack):
+    L = nspack._lib
+    out = L.ns_pack_out()
+    assert L.lib.ns_pack_step(None, 0, 1, 0, 1, C.byref(out), None) == nspack.NS_ERR_INVALID_ARG
+    v = C.c_uint64()
+    assert L.lib.ns_pack_fingerprint(None, None, 1, C.byref(v), None) == nspack.NS_ERR_INVALID_ARG
+    info = L.ns_pack_info_t()
+    assert L.lib.ns_pack_info(None, C.byref(info)) == nspack.NS_ERR_INVALID_ARG
+    assert L.lib.ns_pack_check(None) == nspack.NS_ERR_INVALID_ARG
+    L.lib.ns_pack_free(None)

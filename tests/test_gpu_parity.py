@@ -1,0 +1,211 @@
+"""Parity of the CUDA library with the CPU oracle, element by element.
+
+Integer work: the bar is bit-exact (tolerance 0) on every output -- tokens,
+position ids, document ids, loss masks, row fingerprints, learned counts --
+and on the bookkeeping (valid updates, windows per stream, quota tables, the
+order digest).  Sizes here span many tiles and ragged tails while the oracle
+stays fast; the full-size workloads are in test_gpu_full.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _gpu import assert_rows_equal, batch_sha256, compare_steps, oracle_for, packer_for, to_host
+from _helpers import corpus_from_lengths
+from corpus import make_preset
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_tables(pk, o, c):
+    assert pk.valid_steps == o.valid_steps
+    assert pk.order_digest == o.digest, (hex(pk.order_digest), hex(o.digest))
+    q, cum = pk.quota_table()
+    oq, ocum, _ = o.quota()
+    assert (q == oq).all() and (cum == ocum).all()
+    w, complete = pk.stream_windows()
+    for j in range(c.n_streams):
+        if complete[j]:
+            assert w[j] == o.n_windows(j), j
+        else:
+            assert w[j] > ocum[-1, j] and w[j] <= o.n_windows(j), j
+
+
+@pytest.mark.parametrize("name", ["c1", "c2s", "c3s", "c4s", "c5s"])
+def test_preset_every_step(name):
+    c = make_preset(name)
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    assert o.valid_steps > 0
+    compare_steps(pk, o, range(o.valid_steps), launch=4)
+    pk.check()
+
+
+@pytest.mark.parametrize("name", ["c1", "c3s"])
+def test_slice_invariance(name):
+    c = make_preset(name)
+    pk, o = packer_for(c), oracle_for(c)
+    for k in (0, o.valid_steps - 1):
+        full = to_host(pk.step(k))
+        want = o.rows(k)
+        assert_rows_equal({f: v[0] for f, v in full.items()}, want, f"step {k}")
+        digest = batch_sha256({f: v[0] for f, v in full.items()})
+        fp = pk.batch_fp(pk.step(k)["row_fp"][0])
+        assert fp == oracle.batch_fp(want["row_fp"])
+        R = 1
+        while R <= c.B:
+            parts = [to_host(pk.step(k, rows=(r * c.B // R, (r + 1) * c.B // R))) for r in range(R)]
+            cat = {f: np.concatenate([p[f][0] for p in parts]) for f in parts[0]}
+            assert_rows_equal(cat, want, f"step {k} in {R} slices")
+            assert batch_sha256(cat) == digest
+            R *= 2
+
+
+def test_multi_step_launch_equals_single_steps():
+    c = make_preset("c4s")
+    pk = packer_for(c)
+    n = min(8, pk.valid_steps)
+    many = to_host(pk.step(0, n_steps=n))
+    for k in range(n):
+        one = to_host(pk.step(k))
+        assert_rows_equal({f: v[0] for f, v in one.items()}, {f: v[k] for f, v in many.items()},
+                          f"step {k}")
+
+
+def test_resume_in_a_fresh_context():
+    c = make_preset("c3s")
+    pk1 = packer_for(c)
+    k = pk1.valid_steps // 2
+    a = to_host(pk1.step(k))
+    digest = pk1.order_digest
+    pk1.close()
+    pk2 = packer_for(c)
+    assert pk2.order_digest == digest
+    b = to_host(pk2.step(k))
+    assert_rows_equal({f: v[0] for f, v in a.items()}, {f: v[0] for f, v in b.items()}, "resume")
+    # a resume under another seed is another order: its digest differs
+    assert packer_for(c, seed=1).order_digest != digest
+
+
+def _random_case(rng):
+    T = int(rng.choice([16, 32, 48, 64, 144]))
+    J = int(rng.integers(1, 5))
+    stream_docs = [int(rng.integers(0, 60)) for _ in range(J)]
+    n = sum(stream_docs)
+    lengths = []
+    for _ in range(n):
+        u = rng.random()
+        if u < 0.06:
+            lengths.append(0)
+        elif u < 0.12:
+            lengths.append(T * int(rng.integers(1, 3)))  # exactly T, 2T
+        elif u < 0.75:
+            lengths.append(int(rng.integers(1, T + 1)))
+        else:
+            lengths.append(int(rng.integers(T, 5 * T)))
+    S = int(rng.integers(1, J + 1))
+    stream_source = sorted(list(range(S)) + [int(x) for x in rng.integers(0, S, size=J - S)])
+    B = int(rng.integers(1, 9))
+    drain = bool(rng.integers(0, 2))
+    bp = [int(rng.choice([0, 100, 3000, 10000])) for _ in range(S)]
+    loss_start = None
+    if rng.random() < 0.4:
+        loss_start = [int(rng.integers(-3, max(L, 1) + 5)) for L in lengths]
+    return corpus_from_lengths(
+        lengths, T=T, B=B, max_steps=int(rng.integers(1, 40)), stream_docs=stream_docs,
+        stream_source=stream_source, source_weight=[int(x) for x in rng.integers(1, 9, size=S)],
+        stream_weight=[int(x) for x in rng.integers(1, 9, size=J)], heldout_bp=bp,
+        loss_start=loss_start, seed=int(rng.integers(0, 2**63)),
+        hash_key=int(rng.integers(0, 2**63)), drain=drain, pad_id=int(rng.integers(-5, 50000)))
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_random_tiny_corpora(case):
+    rng = np.random.default_rng(9000 + case)
+    c = _random_case(rng)
+    o = oracle_for(c)
+    pk = packer_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=int(rng.integers(1, 5)))
+    if o.valid_steps < c.max_steps:
+        with pytest.raises(Exception) as e:
+            pk.step(o.valid_steps)
+        assert getattr(e.value, "code", None) == -4  # NS_ERR_EXHAUSTED
+    pk.check()
+
+
+def test_all_held_out_source_is_exhausted_at_once():
+    c = corpus_from_lengths([30] * 8, T=32, B=2, max_steps=3, stream_docs=[4, 4],
+                            heldout_bp=[10000, 0])
+    pk, o = packer_for(c), oracle_for(c)
+    assert pk.valid_steps == o.valid_steps == 0
+    w, complete = pk.stream_windows()
+    assert w[0] == 0 and complete[0]
+    pkd, od = packer_for(c, drain=True), oracle_for(c, drain=True)
+    assert pkd.valid_steps == od.valid_steps == 1
+    compare_steps(pkd, od, [0])
+
+
+def test_empty_streams_and_empty_documents():
+    lengths = [0, 0, 5, 0, 40, 0, 17, 0]
+    c = corpus_from_lengths(lengths, T=32, B=3, max_steps=6, stream_docs=[0, 4, 0, 4],
+                            stream_source=[0, 0, 1, 1], drain=True)
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps))
+
+
+def test_documents_of_exactly_t_are_whole_windows():
+    T = 64
+    c = corpus_from_lengths([T] * 10 + [2 * T] * 3, T=T, B=4, max_steps=4)
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps))
+    r = to_host(pk.step(0))
+    assert (r["row_learned"][0] == T).all()
+    assert (r["pos"][0] == np.arange(T)[None, :]).all()
+
+
+def test_horizon_and_row_range_errors():
+    c = make_preset("c1")
+    pk = packer_for(c)
+    with pytest.raises(Exception) as e:
+        pk.step(c.max_steps)
+    assert e.value.code == -5  # NS_ERR_HORIZON
+    with pytest.raises(Exception) as e:
+        pk.step(c.max_steps - 1, n_steps=2)
+    assert e.value.code == -5
+    out = pk.empty_out(1, c.B)
+    with pytest.raises(Exception) as e:
+        pk.step(0, rows=(3, 3), out=out)
+    assert e.value.code == -1
+    with pytest.raises(Exception) as e:
+        pk.step(0, rows=(0, c.B + 1), out=out)
+    assert e.value.code == -1
+    bad = dict(out)
+    bad["tokens"] = torch.empty(c.B * c.T + 1, dtype=torch.int32, device="cuda:0")[1:]
+    with pytest.raises(Exception) as e:
+        pk.step(0, out=bad)
+    assert e.value.code == -1
+
+
+def test_malformed_offsets_are_reported():
+    c = corpus_from_lengths([3, 4, 5, 6], T=16, B=1, max_steps=2)
+    c.doc_offsets = np.asarray([0, 3, 2, 12, 18], np.int64)
+    with pytest.raises(Exception) as e:
+        packer_for(c)
+    assert e.value.code == -6  # NS_ERR_BAD_INPUT
+    c.doc_offsets = np.asarray([0, 3, 7, 12, 19], np.int64)  # past the last token
+    with pytest.raises(Exception) as e:
+        packer_for(c)
+    assert e.value.code == -6
+
+
+def test_batch_fingerprints_many():
+    c = make_preset("c1")
+    pk, o = packer_for(c), oracle_for(c)
+    out = pk.step(0, n_steps=o.valid_steps)
+    fps = pk.batch_fp_many(out["row_fp"]).cpu().numpy().view(np.uint64)
+    for k in range(o.valid_steps):
+        assert fps[k] == oracle.batch_fp(o.rows(k)["row_fp"])
