@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Benchmark: packed tokens/s of deterministic packed assembly on GB300.
+
+One bench step is one whole pass of the packing path over the workload: the
+context build (held-out hash of every document, Feistel shuffle of every
+stream, scans, piece expansion, next-window search, pointer jumping, window
+numbering, two-level quotas, order digest) followed by the assembly of every
+update of the horizon (row gather with position ids, document ids, loss
+masks, row fingerprints, learned counts) and the batch fingerprint of every
+update.  Inputs are resident in HBM when the timed region starts; outputs go
+to a reused device buffer of ``--launch`` updates.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3]
+    python bench.py --impl reference ...     # the CPU oracle on the same workload
+
+Prints one JSON line (rank 0).  Under torchrun each rank assembles its own
+slice of rows of every update (the same global batch, split by rows) with no
+data-path collective; the timed region is bracketed by barriers and the
+maximum over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOADS = {
+    "c1": "2 sources x 5,000 docs, log-normal median 200 sigma 1.0 [1,8192], vocab 32,000, "
+          "shares 7:3, 1 % held out, T=1024, B=16, 10 updates",
+    "c2": "SFT packing: 200,000 prompt/completion examples (medians 64/128, sigma 1.0, "
+          "<=4096), vocab 128,256, completion-only mask, T=4096, B=8, 500 updates",
+    "c3": "15-source mixture x 3 strata (Dirichlet(1) shares, seed 1), 2,000,000 docs "
+          "log-normal median 600 sigma 1.2 [1,65536], vocab 64,000, 1 % held out (5 % for "
+          "source 15), T=4096, B=512, 1000 updates",
+    "c3m": "a tenth of c3: 200,000 docs, same shape, T=4096, B=512, 96 updates",
+    "c4": "4 equal sources x 2,000,000 docs log-normal median 400 sigma 1.0, vocab 50,257, "
+          "T=8192, B=256, 200 updates",
+    "c5": "1 source of ~1e9 tokens, log-normal median 2048 sigma 1.5 [1,262144], vocab "
+          "151,936, T=32768, B=64, long documents cut into T-chunks, full pass (drain)",
+}
+METRIC = "packed tokens/s"
+UNIT = "tokens/s"
+PROFILES = os.path.join(ROOT, "profiles")
+GATHER_SRC = os.path.join(ROOT, "deterministic_packed_assembly_gb300", "csrc", "gather.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="c3", choices=sorted(WORKLOADS))
+    ap.add_argument("--launch", type=int, default=32, help="updates per ns_pack_step launch")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-updates", type=int, default=40,
+                    help="updates the CPU baseline assembles (its sample)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---- distributed plumbing ---------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def row_slice(rank: int, world: int, B: int) -> tuple[int, int]:
+    """Rows of the global batch that rank `rank` of `world` assembles."""
+    return rank * B // world, (rank + 1) * B // world
+
+
+# ---- clocks -----------------------------------------------------------------
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    def __init__(self, gpu_id: str):
+        self.f = tempfile.NamedTemporaryFile("w+", delete=False, suffix=".csv")
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             + ",".join("clocks_event_reasons." + r for r in REASONS))
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict | None:
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.f.read().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm, mx, seen = [], [], set()
+        for r in rows:
+            if len(r) < 4 + len(REASONS):
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, v in zip(REASONS, r[4:]):
+                if v.strip().lower() == "active":
+                    seen.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(seen),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device) -> str:
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return str(device.index or 0)
+
+
+def clocks_rejected(c: dict | None) -> bool:
+    if not c:
+        return False
+    if any(r in c["reasons"] for r in REJECT):
+        return True
+    return c["sm_mhz"] < 0.6 * c["sm_max_mhz"] and not c["reasons"]
+
+
+# ---- peaks and profiles -----------------------------------------------------
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def gather_source_hash() -> str:
+    with open(GATHER_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str) -> tuple[float | None, str | None]:
+    """DRAM bytes per gather launch from the committed ncu summary, if it was
+    taken on the current gather.cu (else None)."""
+    path = os.path.join(PROFILES, f"gather_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != gather_source_hash():
+        return None, None
+    return float(m.group(1)), os.path.relpath(path, ROOT)
+
+
+# ---- the workload ---------------------------------------------------------
+def make_workload(name: str):
+    from corpus import make_preset
+    t = time.time()
+    c = make_preset(name)
+    log(f"[bench] corpus {name}: {c.n_docs} docs, {c.n_tokens} tokens, {time.time() - t:.1f}s")
+    return c
+
+
+def recipe_kwargs(c) -> dict:
+    return dict(stream_doc_begin=c.stream_doc_begin, stream_source=c.stream_source,
+                source_weight=c.source_weight, stream_weight=c.stream_weight,
+                source_heldout_bp=c.source_heldout_bp, T=c.T, B=c.B, max_steps=c.max_steps,
+                seed=c.seed, hash_key=c.hash_key, drain=c.drain, pad_id=c.pad_id)
+
+
+def config_block(c, args, dist: Dist, rows) -> dict:
+    return {"workload": f"{args.config}: {WORKLOADS[args.config]}",
+            "n_docs": c.n_docs, "n_tokens": c.n_tokens, "T": c.T, "B": c.B,
+            "updates_per_step": None, "rows_per_rank": rows[1] - rows[0],
+            "launch_updates": args.launch,
+            "l2": "inputs larger than L2 (corpus %.1f GB, output buffer > 129 MB)"
+                  % (c.n_tokens * 4 / 1e9),
+            "parallelism": f"rows split over {dist.world} GPU(s), tables replicated"}
+
+
+# ---- our arm ----------------------------------------------------------------
+def run_ours(args, dist: Dist) -> None:
+    import torch
+    import deterministic_packed_assembly_gb300 as nsp
+    from deterministic_packed_assembly_gb300 import Packer
+
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    c = make_workload(args.config)
+    rows = row_slice(dist.rank, dist.world, c.B)
+    n_rows = rows[1] - rows[0]
+    rk = recipe_kwargs(c)
+    stream = torch.cuda.current_stream(device)
+
+    tok_d = torch.from_numpy(c.tokens).to(device)
+    off_d = torch.from_numpy(c.doc_offsets).to(device)
+    ls_d = None if c.loss_start is None else torch.from_numpy(c.loss_start).to(device)
+    torch.cuda.synchronize()
+
+    L = args.launch
+    shape = (L, n_rows, c.T)
+    out = dict(tokens=torch.empty(shape, dtype=torch.int32, device=device),
+               pos=torch.empty(shape, dtype=torch.int32, device=device),
+               doc=torch.empty(shape, dtype=torch.int32, device=device),
+               mask=torch.empty(shape, dtype=torch.uint8, device=device),
+               row_fp=torch.empty((L, n_rows), dtype=torch.int64, device=device),
+               row_learned=torch.empty((L, n_rows), dtype=torch.int32, device=device))
+    fp_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
+
+    state = {"launches": 0, "init_launches": 0, "valid": 0, "events": []}
+
+    def one_pass(record: bool, count: bool = False, e2e=None):
+        """One whole pass; returns real tokens assembled when `count`."""
+        pk = Packer(tok_d if e2e is None else e2e[0], off_d if e2e is None else e2e[1],
+                    ls_d if e2e is None else e2e[2], stream=stream, **rk)
+        valid = pk.valid_steps
+        state["valid"] = valid
+        state["init_launches"] = pk.info["init_launches"]
+        real = torch.zeros((), dtype=torch.int64, device=device) if count else None
+        n = 0
+        for s0 in range(0, valid, L):
+            m = min(L, valid - s0)
+            view = {k: v[:m] for k, v in out.items()}
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            pk.step(s0, m, rows=rows, out=view, stream=stream)
+            if record:
+                b.record(stream)
+                state["events"].append((a, b))
+            if dist.world == 1:
+                pk.batch_fp_many(view["row_fp"], out=fp_all[s0:s0 + m], stream=stream)
+                n += 1
+            if e2e is not None:
+                e2e[3][s0:s0 + m].copy_(view["row_fp"], non_blocking=True)
+                e2e[4][s0:s0 + m].copy_(view["row_learned"], non_blocking=True)
+            if count:
+                real += (view["doc"] >= 0).sum()
+            n += 1
+        if e2e is not None and dist.world == 1:
+            e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
+        pk.close()
+        state["launches"] = n
+        return int(real.item()) if count else None
+
+    # warm-up (the first pass also counts the real tokens of a pass)
+    real_tokens = one_pass(False, count=True)
+    for _ in range(max(args.warmup - 1, 0)):
+        one_pass(False)
+    valid = state["valid"]
+    positions = valid * n_rows * c.T
+    log(f"[bench] rank {dist.rank}: {valid} updates, {real_tokens} real tokens / pass")
+
+    def timed(K: int):
+        state["events"].clear()
+        sampler = ClockSampler(gpu_id_for(device)) if dist.rank == 0 else None
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(K):
+            one_pass(True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        clocks = sampler.stop() if sampler else None
+        ms = t0.elapsed_time(t1)
+        gather_ms = [a.elapsed_time(b) for a, b in state["events"]]
+        return ms, gather_ms, clocks
+
+    K = args.steps
+    ms, gather_ms, clocks = timed(K)
+    retried = False
+    if clocks_rejected(clocks):
+        log(f"[bench] clocks rejected ({clocks}); measuring once more")
+        ms, gather_ms, clocks = timed(K)
+        retried = True
+    ms_max = dist.max(ms)
+    total_real = dist.sum(real_tokens) * K
+    value = total_real / (ms_max / 1e3)
+
+    # roofline of the gather kernel: algorithmic bytes per launch / its time
+    n_launch = (valid + L - 1) // L
+    alg_gather = 13.0 * positions + 4.0 * real_tokens + 12.0 * valid * n_rows
+    bytes_per_launch = alg_gather / n_launch
+    avg_launch_s = (sum(gather_ms) / len(gather_ms)) / 1e3
+    peak, peak_kind = hbm_peak()
+    achieved = bytes_per_launch / avg_launch_s / 1e9
+    traffic, traffic_src = profiled_traffic(args.config)
+    gather_share = sum(gather_ms) / ms
+
+    result = None
+    if dist.rank == 0:
+        hashed_docs_tokens = int(c.n_tokens) if int(c.source_heldout_bp.max()) > 0 else 0
+        alg_step = alg_gather + 4.0 * hashed_docs_tokens + 8.0 * c.n_docs
+        cfg = config_block(c, args, dist, rows)
+        cfg["updates_per_step"] = valid
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "int32",
+            "data": f"synthetic (numpy PCG64, data seed {c.notes.get('data_seed')})",
+            "config": cfg,
+            "positions_per_s": dist.sum(positions) * K / (ms_max / 1e3),
+            "alg_gbps_step": alg_step * K / (ms_max / 1e3) / 1e9,
+            "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": traffic,
+                         "traffic_source": traffic_src,
+                         "bytes_per_launch": bytes_per_launch,
+                         "avg_launch_ms": avg_launch_s * 1e3, "launches": len(gather_ms),
+                         "share_of_step": gather_share},
+            "gpu_launches": K * (state["init_launches"] + state["launches"]),
+            "clocks": clocks, "clocks_retried": retried,
+        }
+
+    # ---- end to end: host inputs, copies inside the timed region -----------
+    if not args.no_e2e:
+        tok_h = torch.from_numpy(c.tokens).pin_memory()
+        off_h = torch.from_numpy(c.doc_offsets).pin_memory()
+        ls_h = None if c.loss_start is None else torch.from_numpy(c.loss_start).pin_memory()
+        fp_h = torch.empty((c.max_steps, n_rows), dtype=torch.int64).pin_memory()
+        ln_h = torch.empty((c.max_steps, n_rows), dtype=torch.int32).pin_memory()
+        bf_h = torch.empty(c.max_steps, dtype=torch.int64).pin_memory()
+        tok_e = torch.empty_like(tok_d)
+        off_e = torch.empty_like(off_d)
+        ls_e = None if ls_d is None else torch.empty_like(ls_d)
+
+        def e2e_pass():
+            tok_e.copy_(tok_h, non_blocking=True)
+            off_e.copy_(off_h, non_blocking=True)
+            if ls_e is not None:
+                ls_e.copy_(ls_h, non_blocking=True)
+            one_pass(False, e2e=(tok_e, off_e, ls_e, fp_h, ln_h, bf_h))
+
+        e2e_pass()
+        dist.barrier()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_pass()
+        torch.cuda.synchronize()
+        e2e_s = dist.max(time.perf_counter() - t)
+        h2d = tok_h.numel() * 4 + off_h.numel() * 8 + (0 if ls_h is None else ls_h.numel() * 4)
+        d2h = valid * n_rows * 12 + (valid * 8 if dist.world == 1 else 0)
+        if result is not None:
+            result["e2e"] = {"value": dist.sum(real_tokens) * args.e2e_steps / e2e_s,
+                             "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                             "steps": args.e2e_steps,
+                             "path": "Packer (C ABI) on pinned host inputs: H2D of the corpus, "
+                                     "full pass, D2H of every row fingerprint and learned count"}
+        else:
+            dist.sum(real_tokens)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) ---------
+    if result is not None and dist.world == 1 and not args.no_cpu_baseline:
+        fp_gpu = fp_all[:valid].cpu().numpy().view(np.uint64)
+        result["cpu_baseline"] = cpu_baseline(c, args, valid, real_tokens, fp_gpu)
+
+    if result is not None:
+        print(json.dumps(result), flush=True)
+
+
+
+def cpu_baseline(c, args, valid: int, real_tokens: int, fp_gpu=None) -> dict:
+    """Time the oracle as it stands (one host thread) on a bounded sample of
+    the workload: its full build (hash, shuffle, pack, quotas over the whole
+    corpus) plus the rows of the first `cpu_updates` updates; the rows time is
+    scaled to all `valid` updates."""
+    import oracle
+    t = time.perf_counter()
+    o = oracle.Oracle(c)
+    t_build = time.perf_counter() - t
+    S = min(args.cpu_updates, valid)
+    fps = []
+    t = time.perf_counter()
+    for k in range(S):
+        fps.append(oracle.batch_fp(o.rows(k)["row_fp"]))
+    t_rows = time.perf_counter() - t
+    t_full = t_build + t_rows * valid / max(S, 1)
+    out = {"value": real_tokens / t_full, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"oracle build over the whole corpus ({t_build:.2f} s) + rows of updates "
+                     f"0..{S - 1} ({t_rows:.2f} s), rows time scaled x{valid / max(S, 1):.1f} "
+                     f"to the {valid}-update pass",
+           "build_s": t_build, "rows_s_per_update": t_rows / max(S, 1)}
+    if fp_gpu is not None:
+        out["bit_exact_sample"] = bool(all(int(fp_gpu[k]) == fps[k] for k in range(S)))
+        out["valid_steps_match"] = bool(o.valid_steps == valid)
+    return out
+
+
+# ---- reference arm: the oracle --------------------------------------------
+def run_reference(args, dist: Dist) -> None:
+    if dist.rank != 0:
+        return
+    import oracle
+    oracle.build()
+    c = make_workload(args.config)
+    o = oracle.Oracle(c)
+    valid = o.valid_steps
+    S = min(args.cpu_updates, valid)
+    # real tokens of a pass, counted by the oracle itself (untimed)
+    real = 0
+    for k in range(valid):
+        real += int((o.rows(k)["doc"] >= 0).sum()) if k < S else 0
+    real_per_update = real / max(S, 1)
+    del o
+
+    def ref_step():
+        t = time.perf_counter()
+        oo = oracle.Oracle(c)
+        tb = time.perf_counter() - t
+        t = time.perf_counter()
+        for k in range(S):
+            oo.rows(k)
+        tr = time.perf_counter() - t
+        return tb + tr * valid / max(S, 1), tb, tr
+
+    for _ in range(args.warmup):
+        ref_step()
+    times = [ref_step() for _ in range(args.steps)]
+    step_s = float(np.mean([t[0] for t in times]))
+    value = real_per_update * valid / step_s
+    sample = (f"each step: oracle build over the whole corpus + rows of updates 0..{S - 1}, "
+              f"rows time scaled x{valid / max(S, 1):.1f} to the {valid}-update pass; "
+              f"real tokens per update averaged over the sample")
+    rows = (0, c.B)
+    result = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "int32",
+        "data": f"synthetic (numpy PCG64, data seed {c.notes.get('data_seed')})",
+        "config": dict(config_block(c, args, dist, rows), updates_per_step=valid),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -246,6 +246,11 @@ def _preset_kwargs(name: str) -> dict:
                     source_weight=[1], stream_source=[0], stream_weight=[1],
                     heldout_bp=[0], target_tokens=1_000_000_000,
                     length=(2048.0, 1.5, 1, 262144), drain=True)
+    # --- a medium cut of c3 (same shape, 1/10 of the documents) for profiles
+    if name == "c3m":
+        kw = _mixture_kwargs(15, 3, 200_000, 100, 500)
+        return dict(data_seed=1013, vocab=64000, T=4096, B=512, max_steps=96,
+                    length=(600.0, 1.2, 1, 65536), **kw)
     # --- shrunk variants with the same structure (CPU-sized) ------------
     if name == "c2s":
         return dict(data_seed=2002, vocab=128256, T=4096, B=8, max_steps=16,
@@ -270,12 +275,13 @@ def _preset_kwargs(name: str) -> dict:
     raise KeyError(name)
 
 
-PRESETS = ("c1", "c2", "c3", "c4", "c5", "c2s", "c3s", "c4s", "c5s")
+PRESETS = ("c1", "c2", "c3", "c4", "c5", "c3m", "c2s", "c3s", "c4s", "c5s")
 
 
 def make_preset(name: str, threads: Optional[int] = None, **overrides) -> Corpus:
-    """One of the named workloads (``c1``..``c5`` full size, ``c2s``..``c5s``
-    shrunk with the same structure); ``overrides`` replace recipe fields."""
+    """One of the named workloads (``c1``..``c5`` full size, ``c3m`` a tenth of
+    ``c3``, ``c2s``..``c5s`` shrunk with the same structure); ``overrides``
+    replace recipe fields."""
     kw = _preset_kwargs(name)
     kw.update(overrides)
     return make_corpus(name, threads=threads, **kw)

@@ -77,6 +77,8 @@ class ns_pack_info_t(C.Structure):
         ("order_digest", C.c_uint64),
         ("n_pieces", C.c_uint64),
         ("table_bytes", C.c_uint64),
+        ("init_launches", C.c_uint32),
+        ("reserved", C.c_uint32),
     ]
 
 

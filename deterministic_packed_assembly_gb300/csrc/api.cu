@@ -29,7 +29,7 @@ struct ns_pack_ctx {
   // host summary
   std::vector<uint64_t> windows;
   std::vector<uint8_t> complete;
-  uint32_t valid_steps = 0, levels = 0;
+  uint32_t valid_steps = 0, levels = 0, init_launches = 0;
   uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
   // device tables kept for the per-update calls
   int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
@@ -444,7 +444,9 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   c->free_fn = cfg->free;
   c->user = cfg->alloc_user;
   Arena a(c);
+  const uint64_t launches0 = nsk::launch_counter();
   rc = build(c, cfg, a);
+  c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
   if (rc != NS_OK) {
     cudaStreamSynchronize(c->stream);
     cudaGetLastError();
@@ -550,6 +552,8 @@ int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
   info->order_digest = ctx->digest;
   info->n_pieces = ctx->n_pieces;
   info->table_bytes = ctx->table_bytes;
+  info->init_launches = ctx->init_launches;
+  info->reserved = 0;
   return NS_OK;
 }
 

@@ -218,12 +218,14 @@ __global__ void batch_fp_kernel(const uint64_t *__restrict__ row_fp, uint32_t n_
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
   const uint64_t n = (uint64_t)p.n_steps * p.n_rows;
   if (n == 0) return cudaSuccess;
+  ++launch_counter();
   gather_kernel<<<(unsigned)n, kGatherWarps * 32, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
                             uint64_t *out, cudaStream_t st) {
+  ++launch_counter();
   batch_fp_kernel<<<(n_steps + 63) / 64, 64, 0, st>>>(row_fp, n_steps, n_rows, out);
   return cudaGetLastError();
 }

@@ -717,14 +717,20 @@ __global__ void digest_final_kernel(const unsigned long long *acc, uint64_t h0, 
 
 // ===========================================================================
 // launchers
+uint64_t &launch_counter() {
+  static thread_local uint64_t n = 0;
+  return n;
+}
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
                                     int *err, cudaStream_t st) {
+  ++launch_counter();
   validate_offsets_kernel<<<blocks_for((uint64_t)n_docs + 1), kThreads, 0, st>>>(offs, n_docs,
                                                                                   n_tokens, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st) {
+  ++launch_counter();
   stream_keys_kernel<<<blocks_for((uint64_t)J * 4), kThreads, 0, st>>>(seed, J, keys);
   return cudaGetLastError();
 }
@@ -736,6 +742,7 @@ static unsigned round_warps(uint32_t n) {
 
 cudaError_t launch_quota_sources(const uint32_t *sw, uint32_t S, uint32_t B, uint32_t K,
                                  int32_t *src_quota, cudaStream_t st) {
+  ++launch_counter();
   quota_sources_kernel<<<1, round_warps(S), 0, st>>>(sw, S, B, K, src_quota);
   return cudaGetLastError();
 }
@@ -744,6 +751,7 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 cudaStream_t st) {
+  ++launch_counter();
   quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(src_quota, tw, src_first, S, J, K,
                                                              quota, cum);
   return cudaGetLastError();
@@ -751,6 +759,7 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
 
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st) {
+  ++launch_counter();
   row_base_kernel<<<blocks_for(K, 128), 128, 0, st>>>(quota, J, K, rb);
   return cudaGetLastError();
 }
@@ -759,6 +768,7 @@ cudaError_t launch_hash_docs(const int32_t *tokens, const int64_t *offs, const u
                              const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
                              uint8_t *heldout, unsigned long long *counter, int n_sms,
                              cudaStream_t st) {
+  ++launch_counter();
   hash_docs_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, hash_key,
                                                    heldout, counter);
   return cudaGetLastError();
@@ -768,6 +778,7 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, const uint8_t *heldout, uint32_t D0,
                          uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
+  ++launch_counter();
   order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, heldout, D0, order, klen,
                                                 err);
   return cudaGetLastError();
@@ -786,13 +797,16 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   int64_t *bs_a = static_cast<int64_t *>(scratch);
   int64_t *bs_b = bs_a + (nb + 1);
   if (nb > 0) {
+    ++launch_counter();
     scan_reduce_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  ++launch_counter();
   scan_tiles_kernel<<<1, 1024, 0, st>>>(bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nb == 0) return e;
+  ++launch_counter();
   scan_apply_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b, kex, pex);
   return cudaGetLastError();
 }
@@ -800,6 +814,7 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T,
                           uint32_t *cutoff, int64_t *npieces, cudaStream_t st) {
+  ++launch_counter();
   cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, cutoff,
                                                     npieces);
   return cudaGetLastError();
@@ -807,6 +822,7 @@ cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const in
 
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st) {
+  ++launch_counter();
   node_base_kernel<<<1, 32, 0, st>>>(npieces, J, node_base);
   return cudaGetLastError();
 }
@@ -818,6 +834,7 @@ cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uin
                           int64_t *node_src, int32_t *node_doc, int32_t *node_mthr,
                           int64_t *node_S, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
+  ++launch_counter();
   expand_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, order, klen, kex, pex,
                                                  node_base, npieces, offs, loss_start, T,
                                                  node_src, node_doc, node_mthr, node_S);
@@ -827,12 +844,14 @@ cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uin
 cudaError_t launch_next(SegGrid g, const int64_t *node_base, const int64_t *npieces,
                         const int64_t *node_S, uint32_t T, int32_t *next, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
+  ++launch_counter();
   next_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, node_base, npieces, node_S, T, next);
   return cudaGetLastError();
 }
 
 cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
                               cudaStream_t st) {
+  ++launch_counter();
   jump_level_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
                                                                          up_next);
   return cudaGetLastError();
@@ -841,6 +860,7 @@ cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *
 cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_t n_levels,
                                  const int64_t *node_base, const int64_t *npieces, uint32_t J,
                                  uint32_t *W, cudaStream_t st) {
+  ++launch_counter();
   count_windows_kernel<<<blocks_for(J, 128), 128, 0, st>>>(levels, n_nodes, n_levels, node_base,
                                                            npieces, J, W);
   return cudaGetLastError();
@@ -850,6 +870,7 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
                                  uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
                                  const int64_t *wbase, int32_t *win_start, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
+  ++launch_counter();
   window_starts_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, levels, n_nodes, n_levels, node_base,
                                                         W, wbase, win_start);
   return cudaGetLastError();
@@ -858,12 +879,15 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
 cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st) {
+  ++launch_counter();
   set_u32_kernel<<<1, 1, 0, st>>>(first_bad, K);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++launch_counter();
   first_bad_kernel<<<blocks_for((uint64_t)K * J), kThreads, 0, st>>>(cum, W, J, K, first_bad);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++launch_counter();
   valid_kernel<<<1, 1, 0, st>>>(first_bad, K, drain, valid);
   return cudaGetLastError();
 }
@@ -876,23 +900,28 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           unsigned long long *acc, int64_t *ubase, uint64_t *digest_out,
                           cudaStream_t st) {
   const uint64_t h0 = 10ull + 2ull * h.S + 4ull * h.J;
+  ++launch_counter();
   digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++launch_counter();
   digest_quota_kernel<<<blocks_for((uint64_t)K * h.J), kThreads, 0, st>>>(quota, h.J, K, h0,
                                                                            valid, acc);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++launch_counter();
   digest_used_kernel<<<1, 32, 0, st>>>(cum, W, h.J, valid, ubase);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (wg.n_blocks > 0) {
+    ++launch_counter();
     digest_windows_kernel<<<wg.n_blocks, kThreads, 0, st>>>(wg, wbase, win_start, node_src,
                                                             node_doc, offs, T, h0, h.J, valid,
                                                             ubase, acc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  ++launch_counter();
   digest_final_kernel<<<1, 1, 0, st>>>(acc, h0, h.J, valid, ubase, digest_out);
   return cudaGetLastError();
 }

@@ -8,6 +8,9 @@
 
 namespace nsk {
 
+// Kernels launched by this thread so far (each launcher adds its own).
+uint64_t &launch_counter();
+
 // A launch over per-stream segments: stream j owns items [0, count_j), laid
 // out in blocks of `block` items; blk_base[j] is the first block of stream j
 // (host-computed prefix, J + 1 entries, on the device).

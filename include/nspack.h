@@ -135,6 +135,8 @@ typedef struct {
   uint64_t order_digest;
   uint64_t n_pieces;    /* pieces (document T-chunks) built at init */
   uint64_t table_bytes; /* device bytes the context keeps */
+  uint32_t init_launches; /* kernels ns_pack_init launched */
+  uint32_t reserved;
 } ns_pack_info_t;
 
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of
