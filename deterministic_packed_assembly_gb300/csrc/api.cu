@@ -10,6 +10,7 @@
 #include <cstring>
 #include <vector>
 
+#include "common.cuh"
 #include "kernels.h"
 #include "nspack.h"
 
@@ -35,8 +36,7 @@ struct ns_pack_ctx {
   int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
   uint32_t *W = nullptr;
   int64_t *wbase = nullptr;
-  int32_t *win_start = nullptr;
-  int32_t *next = nullptr;
+  int2 *row_win = nullptr;
   int64_t *node_S = nullptr, *node_src = nullptr;
   int32_t *node_doc = nullptr, *node_mthr = nullptr;
   int *err = nullptr;
@@ -153,6 +153,25 @@ std::vector<uint32_t> seg_layout(const std::vector<uint64_t> &count, uint32_t pe
     if (!(p)) return NS_ERR_OOM;  \
   } while (0)
 
+// A second stream for work that does not depend on the corpus; synchronised
+// and destroyed on every exit path.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaError_t create() {
+    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    return e;
+  }
+  ~SideStream() {
+    if (s) cudaStreamSynchronize(s);
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    if (s) cudaStreamDestroy(s);
+  }
+};
+
 int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st) {
   *dev = a.get(bytes, false);
   NS_ALLOC(*dev);
@@ -203,42 +222,39 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->fp_out);
   NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
 
-  // ---- 1. the corpus partition, 2. quotas of every update -----------------
-  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
-  int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
+  // ---- 1. quotas of every update, on a side stream ------------------------
+  // They depend only on the weights, so they run while the corpus is hashed
+  // and shuffled; the main stream joins them before the prefix cutoff.
   c->quota = a.keep<int32_t>((size_t)K * J);
   c->cum = a.keep<int32_t>((size_t)(K + 1) * J);
   c->rb = a.keep<int32_t>((size_t)K * (J + 1));
-  NS_ALLOC(src_quota);
   NS_ALLOC(c->quota);
   NS_ALLOC(c->cum);
   NS_ALLOC(c->rb);
-  NS_CK(nsk::launch_quota_sources(static_cast<uint32_t *>(d_sw), S, c->B, K, src_quota, st));
-  NS_CK(nsk::launch_quota_strata(src_quota, static_cast<uint32_t *>(d_tw),
-                                 static_cast<uint32_t *>(d_src_first), S, J, K, max_strata,
-                                 c->quota, c->cum, st));
-  NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, st));
-
-  std::vector<int32_t> rmax32(J);
-  int err_host = 0;
-  NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
-                        cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaStreamSynchronize(st));
-  if (err_host != 0) return NS_ERR_BAD_INPUT;
-
-  std::vector<uint64_t> rmax(J);
-  std::vector<int64_t> wbase(J + 1, 0);
-  for (uint32_t j = 0; j < J; j++) {
-    rmax[j] = (uint64_t)rmax32[j];
-    wbase[j + 1] = wbase[j] + (int64_t)rmax[j];
+  SideStream side;
+  NS_CK(side.create());
+  NS_CK(cudaEventRecord(side.fork, st));
+  NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
+  if (S <= 32 && max_strata <= 32) {
+    NS_CK(nsk::launch_quota_warp(static_cast<uint32_t *>(d_sw), S, static_cast<uint32_t *>(d_tw),
+                                 static_cast<uint32_t *>(d_src_first), J, c->B, K, c->quota,
+                                 c->cum, side.s));
+  } else {
+    int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
+    NS_ALLOC(src_quota);
+    NS_CK(nsk::launch_quota_sources(static_cast<uint32_t *>(d_sw), S, c->B, K, src_quota,
+                                    side.s));
+    NS_CK(nsk::launch_quota_strata(src_quota, static_cast<uint32_t *>(d_tw),
+                                   static_cast<uint32_t *>(d_src_first), S, J, K, max_strata,
+                                   c->quota, c->cum, side.s));
   }
-  c->wbase = a.keep<int64_t>(J + 1);
-  NS_ALLOC(c->wbase);
-  NS_CK(cudaMemcpyAsync(c->wbase, wbase.data(), (J + 1) * sizeof(int64_t),
-                        cudaMemcpyHostToDevice, st));
+  NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
+  NS_CK(cudaEventRecord(side.join, side.s));
 
-  // ---- 3. held-out flags --------------------------------------------------
+  // ---- 2. the corpus partition and the held-out flags ---------------------
+  // Every kernel that reads tokens checks the offsets it uses, so a malformed
+  // partition is reported (BAD_INPUT) at the next readback, never read past.
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
   uint8_t *heldout = nullptr;
   if (any_heldout) {
     heldout = a.temp<uint8_t>(std::max<uint32_t>(c->n_docs, 1));
@@ -247,12 +263,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(counter);
     NS_CK(cudaMemsetAsync(heldout, 0, std::max<uint32_t>(c->n_docs, 1), st));
     NS_CK(cudaMemsetAsync(counter, 0, sizeof(unsigned long long), st));
-    NS_CK(nsk::launch_hash_docs(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+    NS_CK(nsk::launch_hash_docs(c->tokens, c->n_tokens, c->offs, static_cast<uint32_t *>(d_sdb),
                                 static_cast<uint16_t *>(d_stream_bp), J, c->hash_key, heldout,
                                 counter, c->n_sms, st));
   }
 
-  // ---- 4. shuffled order and kept lengths of every position ---------------
+  // ---- 3. shuffled order and kept lengths of every position ---------------
   const uint32_t D0 = sdb[0];
   const uint64_t n_pos = (uint64_t)sdb[J] - D0;
   std::vector<uint64_t> N(J);
@@ -281,24 +297,40 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
 
-  // ---- 5. the prefix of each stream the horizon reaches -------------------
+  // ---- 4. the prefix of each stream the horizon reaches -------------------
   uint32_t *cutoff = a.temp<uint32_t>(J);
   int64_t *npieces = a.temp<int64_t>(J);
   int64_t *node_base = a.temp<int64_t>(J + 1);
   NS_ALLOC(cutoff);
   NS_ALLOC(npieces);
   NS_ALLOC(node_base);
+  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
                            T, cutoff, npieces, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
   std::vector<uint32_t> cut_h(J);
   std::vector<int64_t> np_h(J), nb_h(J + 1);
+  std::vector<int32_t> rmax32(J);
+  int err_host = 0;
   NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(nb_h.data(), node_base, (J + 1) * 8, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
+  if (err_host == nsk::kDevBadOffsets) return NS_ERR_BAD_INPUT;
   if (err_host != 0) return NS_ERR_DEVICE;
+  std::vector<uint64_t> rmax(J);
+  std::vector<int64_t> wbase(J + 1, 0);
+  for (uint32_t j = 0; j < J; j++) {
+    rmax[j] = (uint64_t)rmax32[j];
+    wbase[j + 1] = wbase[j] + (int64_t)rmax[j];
+  }
+  c->wbase = a.keep<int64_t>(J + 1);
+  NS_ALLOC(c->wbase);
+  NS_CK(cudaMemcpyAsync(c->wbase, wbase.data(), (J + 1) * sizeof(int64_t),
+                        cudaMemcpyHostToDevice, st));
   const int64_t n_nodes = nb_h[J];
   if (n_nodes >= (int64_t)0x7FFFFFFF) return NS_ERR_INVALID_ARG;
   c->n_pieces = (uint64_t)(n_nodes - J);
@@ -317,13 +349,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->node_S = a.keep<int64_t>(n_nodes);
   c->node_doc = a.keep<int32_t>(n_nodes);
   c->node_mthr = a.keep<int32_t>(n_nodes);
-  c->next = a.keep<int32_t>(n_nodes);
   int32_t *levels = a.temp<int32_t>((size_t)L * n_nodes);
   NS_ALLOC(c->node_src);
   NS_ALLOC(c->node_S);
   NS_ALLOC(c->node_doc);
   NS_ALLOC(c->node_mthr);
-  NS_ALLOC(c->next);
   NS_ALLOC(levels);
   {
     std::vector<uint64_t> cnt(J);
@@ -348,15 +378,16 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   for (uint32_t l = 1; l < L; l++)
     NS_CK(nsk::launch_jump_level(levels + (size_t)(l - 1) * n_nodes, n_nodes,
                                  levels + (size_t)l * n_nodes, st));
-  NS_CK(cudaMemcpyAsync(c->next, levels, (size_t)n_nodes * 4, cudaMemcpyDeviceToDevice, st));
 
   // ---- 7. windows: count, starts, the valid horizon ------------------------
   c->W = a.keep<uint32_t>(J);
-  c->win_start = a.keep<int32_t>(std::max<int64_t>(wbase[J], 1));
+  int32_t *win_start = a.temp<int32_t>(std::max<int64_t>(wbase[J], 1));
+  c->row_win = a.keep<int2>((size_t)K * c->B);
   uint32_t *first_bad = a.temp<uint32_t>(1);
   uint32_t *valid = a.temp<uint32_t>(1);
   NS_ALLOC(c->W);
-  NS_ALLOC(c->win_start);
+  NS_ALLOC(win_start);
+  NS_ALLOC(c->row_win);
   NS_ALLOC(first_bad);
   NS_ALLOC(valid);
   NS_CK(nsk::launch_count_windows(levels, n_nodes, L, node_base, npieces, J, c->W, st));
@@ -364,8 +395,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   void *d_wb;
   if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
   nsk::SegGrid wg{static_cast<uint32_t *>(d_wb), J, wb[J]};
-  NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase, c->win_start,
+  NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase, win_start,
                                   st));
+  NS_CK(nsk::launch_row_windows(c->rb, c->cum, c->W, c->wbase, win_start, levels, J, c->B, K,
+                                c->row_win, st));
   NS_CK(nsk::launch_valid_steps(c->cum, c->W, J, K, (c->flags & NS_PACK_DRAIN) ? 1u : 0u,
                                 first_bad, valid, st));
 
@@ -395,7 +428,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.tw = static_cast<uint32_t *>(d_tw);
   h.S = S;
   h.J = J;
-  NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, c->win_start,
+  NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, win_start,
                            c->node_src, c->node_doc, c->offs, T, K, dacc, ubase, digest, st));
 
   // ---- 9. read back the summary ------------------------------------------
@@ -474,18 +507,13 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   if ((uint64_t)step0 + n_steps > ctx->valid_steps) return NS_ERR_EXHAUSTED;
   nsk::GatherParams p{};
   p.tokens = ctx->tokens;
-  p.rb = ctx->rb;
-  p.cum = ctx->cum;
-  p.W = ctx->W;
-  p.wbase = ctx->wbase;
-  p.win_start = ctx->win_start;
-  p.next = ctx->next;
+  p.row_win = ctx->row_win;
   p.node_S = ctx->node_S;
   p.node_src = ctx->node_src;
   p.node_doc = ctx->node_doc;
   p.node_mthr = ctx->node_mthr;
   p.err = ctx->err;
-  p.J = ctx->J;
+  p.B = ctx->B;
   p.T = ctx->T;
   p.step0 = step0;
   p.n_steps = n_steps;

@@ -1,8 +1,8 @@
-// Per-update assembly: one CTA per (update, row).  The row's stream and
-// window come from the quota tables; the window's pieces are copied in order
-// into T positions of tokens / position ids / document ids / loss mask, the
-// rest padded; the row's fingerprint and learned-position count are reduced
-// in the same pass.
+// Per-update assembly: one CTA per (update, row).  The row's window comes
+// from the row table built at init; the window's pieces are staged in shared
+// memory and copied in order into T positions of tokens / position ids /
+// document ids / loss mask, the rest padded; the row's fingerprint and
+// learned-position count are reduced in the same pass.
 //
 // Rows of exactly T positions, padded (Linnet training docs, Supervised
 // fine-tuning); a position id of 0 starts each sequence within a row (Other
@@ -10,6 +10,14 @@
 // rows are a pure function of (recipe, seed, update, row), so any split of
 // the rows gives the same bytes ("Zephon: deterministic data loading",
 // checkpoint on 16 GPUs, resume on 8/32/64).
+//
+// Layout of the work: 8 warps per CTA; a warp owns tiles of 128 consecutive
+// positions (4 per lane, so every store is a 16-byte vector and a warp
+// writes 512 contiguous bytes per array) and handles two tiles per round,
+// issuing both tiles' token loads before computing either.  A tile inside one
+// piece reads its tokens with one aligned 16-byte load per lane, realigned
+// across lanes with shuffles; a tile that crosses piece ends reads them one by
+// one.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,26 +30,16 @@ namespace nsk {
 namespace {
 
 constexpr int kGatherWarps = 8;
-constexpr int kTile = 128;  // positions per warp per round: 32 lanes x 4
+constexpr int kTile = 128;       // positions per warp per tile: 32 lanes x 4
+constexpr int kPieceCap = 512;   // pieces of a window staged in shared memory
 
-// Fingerprint terms and learned count of four consecutive positions t0..t0+3:
-// key_t = a_t ^ ((b_t | t << 40) * golden), a_t = (u32 tok << 32) | u32 doc,
-// b_t = (mask << 32) | u32 pos.
-__device__ __forceinline__ void fingerprint4(uint64_t &acc, int &learned, const int4 &tk,
-                                             const int4 &ps, const int4 &dc, uint32_t mk,
-                                             uint32_t t0) {
-  const int32_t tok[4] = {tk.x, tk.y, tk.z, tk.w};
-  const int32_t pos[4] = {ps.x, ps.y, ps.z, ps.w};
-  const int32_t doc[4] = {dc.x, dc.y, dc.z, dc.w};
-#pragma unroll
-  for (int e = 0; e < 4; e++) {
-    const uint64_t m = (mk >> (8 * e)) & 1u;
-    const uint64_t a = ((uint64_t)(uint32_t)tok[e] << 32) | (uint64_t)(uint32_t)doc[e];
-    const uint64_t b = (m << 32) | (uint64_t)(uint32_t)pos[e];
-    const uint64_t key = a ^ ((b | ((uint64_t)(t0 + e) << 40)) * kGolden);
-    acc += splitmix64(key);
-  }
-  learned += __popc(mk);
+// Fingerprint terms of position t: key_t = a_t ^ ((b_t | t << 40) * golden),
+// a_t = (u32 tok << 32) | u32 doc, b_t = (mask << 32) | u32 pos.
+__device__ __forceinline__ uint64_t fp_term(int32_t tok, int32_t pos, int32_t doc, uint32_t m,
+                                            uint32_t t) {
+  const uint64_t a = ((uint64_t)(uint32_t)tok << 32) | (uint64_t)(uint32_t)doc;
+  const uint64_t b = ((uint64_t)m << 32) | (uint64_t)(uint32_t)pos;
+  return splitmix64(a ^ ((b | ((uint64_t)t << 40)) * kGolden));
 }
 
 __device__ __forceinline__ int4 shfl_down4(const int4 &v) {
@@ -53,10 +51,146 @@ __device__ __forceinline__ int4 shfl_down4(const int4 &v) {
   return r;
 }
 
+// The window's pieces, either staged in shared memory or read from the
+// context's tables.  dst(q) is the first row position of piece q (relative to
+// the window), dst(np) the window's used length.
+struct Pieces {
+  const int64_t *S;     // staged: S - S[ws] prefix; global: node_S + ws (absolute)
+  const int64_t *src;   // first token index of each piece
+  const int32_t *doc;
+  const int32_t *mthr;
+  int64_t sbase;        // subtracted from S to make it window-relative
+  int32_t np;
+  __device__ __forceinline__ int64_t dst(int32_t q) const { return S[q] - sbase; }
+  // last piece q in [lo, np) with dst(q) <= t
+  __device__ __forceinline__ int32_t find(int32_t lo, int64_t t) const {
+    int32_t l = lo, h = np;
+    while (l < h) {
+      const int32_t m = l + (h - l) / 2;
+      if (S[m] - sbase <= t)
+        l = m + 1;
+      else
+        h = m;
+    }
+    return l - 1;
+  }
+};
+
+// One tile's state between its load and its stores.
+struct TileLoad {
+  int kind;      // 0 pad, 1 inside piece q, 2 crosses piece ends
+  int32_t q;     // piece of the tile's first position
+  int32_t x0;    // offset of the lane's first position inside piece q (kind 1)
+  int sh;        // source misalignment in tokens (kind 1)
+  int4 v;        // aligned 16-byte load (kind 1)
+  int4 nv;       // lane 31's next 16 bytes (kind 1, sh != 0)
+};
+
+__device__ __forceinline__ void tile_load(const GatherParams &p, const Pieces &P, int32_t used,
+                                          uint32_t t0, int lane, TileLoad &L) {
+  if ((int32_t)t0 >= used) {
+    L.kind = 0;
+    return;
+  }
+  L.q = P.find(0, (int64_t)t0);
+  const int64_t qs = P.dst(L.q);
+  const int64_t qe = P.dst(L.q + 1);
+  if (qe >= (int64_t)t0 + kTile) {
+    L.kind = 1;
+    const int64_t x0 = (int64_t)t0 - qs;
+    const int64_t srcw = P.src[L.q] + x0;
+    L.sh = (int)(srcw & 3);
+    const int4 *src4 = reinterpret_cast<const int4 *>(p.tokens + (srcw - L.sh));
+    L.v = __ldg(src4 + lane);
+    if (L.sh != 0 && lane == 31) L.nv = __ldg(src4 + 32);
+    L.x0 = (int32_t)x0 + 4 * lane;
+  } else {
+    L.kind = 2;
+  }
+}
+
+__device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &P, int32_t used,
+                                           uint32_t t0, int lane, size_t obase, TileLoad &L,
+                                           uint64_t &acc, int &learned) {
+  const uint32_t tp = t0 + 4u * lane;
+  int4 tk, ps, dc;
+  uint32_t mk = 0;
+  if (L.kind == 0) {
+    tk = make_int4(p.pad_id, p.pad_id, p.pad_id, p.pad_id);
+    ps = make_int4(0, 0, 0, 0);
+    dc = make_int4(-1, -1, -1, -1);
+  } else if (L.kind == 1) {
+    if (L.sh == 0) {
+      tk = L.v;
+    } else {
+      int4 nv = shfl_down4(L.v);
+      if (lane == 31) nv = L.nv;
+      if (L.sh == 1)
+        tk = make_int4(L.v.y, L.v.z, L.v.w, nv.x);
+      else if (L.sh == 2)
+        tk = make_int4(L.v.z, L.v.w, nv.x, nv.y);
+      else
+        tk = make_int4(L.v.w, nv.x, nv.y, nv.z);
+    }
+    const int32_t x = L.x0;
+    ps = make_int4(x, x + 1, x + 2, x + 3);
+    const int32_t d = P.doc[L.q];
+    dc = make_int4(d, d, d, d);
+    const int32_t th = P.mthr[L.q];
+    mk = (x >= th ? 1u : 0u) | (x + 1 >= th ? 1u << 8 : 0u) | (x + 2 >= th ? 1u << 16 : 0u) |
+         (x + 3 >= th ? 1u << 24 : 0u);
+  } else {
+    if (tp >= p.T) return;
+    int32_t e0[4], e1[4], e2[4];
+    int32_t qq = -1;
+    int64_t qqe = 0, qqs = 0;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int32_t t = (int32_t)tp + e;
+      if (t >= used) {
+        e0[e] = p.pad_id;
+        e1[e] = 0;
+        e2[e] = -1;
+        continue;
+      }
+      if (qq < 0) {
+        qq = P.find(L.q, (int64_t)t);
+        qqs = P.dst(qq);
+        qqe = P.dst(qq + 1);
+      }
+      while ((int64_t)t >= qqe) {
+        qq++;
+        qqs = qqe;
+        qqe = P.dst(qq + 1);
+      }
+      const int32_t x = t - (int32_t)qqs;
+      e0[e] = __ldg(p.tokens + P.src[qq] + x);
+      e1[e] = x;
+      e2[e] = P.doc[qq];
+      if (x >= P.mthr[qq]) mk |= 1u << (8 * e);
+    }
+    tk = make_int4(e0[0], e0[1], e0[2], e0[3]);
+    ps = make_int4(e1[0], e1[1], e1[2], e1[3]);
+    dc = make_int4(e2[0], e2[1], e2[2], e2[3]);
+  }
+  if (tp >= p.T) return;
+  __stcs(reinterpret_cast<int4 *>(p.tokens_out + obase + tp), tk);
+  __stcs(reinterpret_cast<int4 *>(p.pos_out + obase + tp), ps);
+  __stcs(reinterpret_cast<int4 *>(p.doc_out + obase + tp), dc);
+  __stcs(reinterpret_cast<unsigned int *>(p.mask_out + obase + tp), mk);
+  acc += fp_term(tk.x, ps.x, dc.x, mk & 1u, tp);
+  acc += fp_term(tk.y, ps.y, dc.y, (mk >> 8) & 1u, tp + 1);
+  acc += fp_term(tk.z, ps.z, dc.z, (mk >> 16) & 1u, tp + 2);
+  acc += fp_term(tk.w, ps.w, dc.w, (mk >> 24) & 1u, tp + 3);
+  learned += __popc(mk);
+}
+
 __global__ void __launch_bounds__(kGatherWarps * 32)
     gather_kernel(const GatherParams p) {
-  __shared__ int64_t s_ws, s_we, s_sbase;
-  __shared__ int32_t s_used;
+  __shared__ int64_t s_S[kPieceCap + 1];
+  __shared__ int64_t s_src[kPieceCap];
+  __shared__ int32_t s_doc[kPieceCap];
+  __shared__ int32_t s_mthr[kPieceCap];
   __shared__ uint64_t s_fp[kGatherWarps];
   __shared__ int s_learned[kGatherWarps];
 
@@ -65,121 +199,56 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   const uint32_t row_local = blk - step_local * p.n_rows;
   const uint32_t k = p.step0 + step_local;
   const uint32_t i = p.row0 + row_local;
-  const uint32_t T = p.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  if (threadIdx.x == 0) {
-    const int32_t *rbk = p.rb + (size_t)k * (p.J + 1);
-    const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)p.J, (int32_t)i);
-    const int64_t r = (int64_t)p.cum[(size_t)k * p.J + j] + ((int64_t)i - rbk[j]);
-    int64_t ws = 0, we = 0, sbase = 0;
-    int64_t used = 0;
-    if (r < (int64_t)p.W[j]) {
-      ws = p.win_start[p.wbase[j] + r];
-      if (ws >= 0) {
-        we = p.next[ws];
-        sbase = p.node_S[ws];
-        used = p.node_S[we] - sbase;
-      }
-      if (ws < 0 || we <= ws || used <= 0 || used > (int64_t)T) {
-        set_error(p.err, kDevBadNode);
-        ws = we = sbase = 0;
-        used = 0;
+  // the row's window: pieces [ws, we) of the context's piece table
+  const int2 win = p.row_win[(size_t)k * p.B + i];
+  int64_t ws = win.x, we = win.y;
+  if (ws < 0 || we < ws) ws = we = 0;  // a row past the end of its stream: all padding
+  const int32_t np = (int32_t)(we - ws);
+  Pieces P;
+  P.np = np;
+  const bool staged = np <= kPieceCap;
+  if (staged) {
+    for (int32_t t = threadIdx.x; t <= np; t += blockDim.x) {
+      s_S[t] = __ldg(p.node_S + ws + t);
+      if (t < np) {
+        s_src[t] = __ldg(p.node_src + ws + t);
+        s_doc[t] = __ldg(p.node_doc + ws + t);
+        s_mthr[t] = __ldg(p.node_mthr + ws + t);
       }
     }
-    s_ws = ws;
-    s_we = we;
-    s_sbase = sbase;
-    s_used = (int32_t)used;
+    __syncthreads();
+    P.S = s_S;
+    P.src = s_src;
+    P.doc = s_doc;
+    P.mthr = s_mthr;
+  } else {
+    P.S = p.node_S + ws;
+    P.src = p.node_src + ws;
+    P.doc = p.node_doc + ws;
+    P.mthr = p.node_mthr + ws;
   }
-  __syncthreads();
-  const int64_t ws = s_ws, we = s_we, sbase = s_sbase;
-  const int32_t used = s_used;
+  P.sbase = P.S[0];
+  const int64_t used64 = P.S[np] - P.sbase;
+  int32_t used = (int32_t)used64;
+  if (used64 < 0 || used64 > (int64_t)p.T) {
+    set_error(p.err, kDevBadNode);
+    used = 0;
+  }
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const size_t obase = (size_t)blk * T;
+  const size_t obase = (size_t)blk * p.T;
   uint64_t acc = 0;
   int learned = 0;
-
-  for (uint32_t t0 = (uint32_t)warp * kTile; t0 < T; t0 += kGatherWarps * kTile) {
-    const uint32_t tp = t0 + 4u * lane;
-    int4 tk, ps, dc;
-    uint32_t mk = 0;
-    if ((int32_t)t0 >= used) {
-      tk = make_int4(p.pad_id, p.pad_id, p.pad_id, p.pad_id);
-      ps = make_int4(0, 0, 0, 0);
-      dc = make_int4(-1, -1, -1, -1);
-    } else {
-      // the piece holding the tile's first position
-      const int64_t q = last_le<int64_t, int64_t>(p.node_S, ws, we, sbase + (int64_t)t0);
-      const int64_t qs = __ldg(p.node_S + q) - sbase;
-      const int64_t qe = __ldg(p.node_S + q + 1) - sbase;
-      if (qe >= (int64_t)t0 + kTile) {
-        // the whole tile lies in piece q: one realigned 16-byte load per lane
-        const int64_t x0 = (int64_t)t0 - qs;
-        const int64_t srcw = __ldg(p.node_src + q) + x0;
-        const int sh = (int)(srcw & 3);
-        const int4 *src4 = reinterpret_cast<const int4 *>(p.tokens + (srcw - sh));
-        const int4 v = __ldg(src4 + lane);
-        if (sh == 0) {
-          tk = v;
-        } else {
-          int4 nv = shfl_down4(v);
-          if (lane == 31) nv = __ldg(src4 + 32);
-          if (sh == 1)
-            tk = make_int4(v.y, v.z, v.w, nv.x);
-          else if (sh == 2)
-            tk = make_int4(v.z, v.w, nv.x, nv.y);
-          else
-            tk = make_int4(v.w, nv.x, nv.y, nv.z);
-        }
-        const int32_t x = (int32_t)x0 + 4 * lane;
-        ps = make_int4(x, x + 1, x + 2, x + 3);
-        const int32_t d = __ldg(p.node_doc + q);
-        dc = make_int4(d, d, d, d);
-        const int32_t th = __ldg(p.node_mthr + q);
-        mk = (x >= th ? 1u : 0u) | (x + 1 >= th ? 1u << 8 : 0u) | (x + 2 >= th ? 1u << 16 : 0u) |
-             (x + 3 >= th ? 1u << 24 : 0u);
-      } else if (tp < T) {
-        // the tile crosses piece ends: each lane finds its pieces
-        int32_t tkv[4], psv[4], dcv[4];
-        int64_t qq = -1, qqs = 0, qqe = 0;
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int32_t t = (int32_t)tp + e;
-          if (t >= used) {
-            tkv[e] = p.pad_id;
-            psv[e] = 0;
-            dcv[e] = -1;
-            continue;
-          }
-          if (qq < 0) {
-            qq = last_le<int64_t, int64_t>(p.node_S, q, we, sbase + (int64_t)t);
-            qqs = __ldg(p.node_S + qq) - sbase;
-            qqe = __ldg(p.node_S + qq + 1) - sbase;
-          }
-          while ((int64_t)t >= qqe) {
-            qq++;
-            qqs = qqe;
-            qqe = __ldg(p.node_S + qq + 1) - sbase;
-          }
-          const int32_t x = t - (int32_t)qqs;
-          tkv[e] = __ldg(p.tokens + __ldg(p.node_src + qq) + x);
-          psv[e] = x;
-          dcv[e] = __ldg(p.node_doc + qq);
-          if (x >= __ldg(p.node_mthr + qq)) mk |= 1u << (8 * e);
-        }
-        tk = make_int4(tkv[0], tkv[1], tkv[2], tkv[3]);
-        ps = make_int4(psv[0], psv[1], psv[2], psv[3]);
-        dc = make_int4(dcv[0], dcv[1], dcv[2], dcv[3]);
-      }
-    }
-    if (tp < T) {
-      __stcs(reinterpret_cast<int4 *>(p.tokens_out + obase + tp), tk);
-      __stcs(reinterpret_cast<int4 *>(p.pos_out + obase + tp), ps);
-      __stcs(reinterpret_cast<int4 *>(p.doc_out + obase + tp), dc);
-      __stcs(reinterpret_cast<unsigned int *>(p.mask_out + obase + tp), mk);
-      fingerprint4(acc, learned, tk, ps, dc, mk, tp);
-    }
+  constexpr uint32_t kStride = kGatherWarps * kTile;
+  for (uint32_t ta = (uint32_t)warp * kTile; ta < p.T; ta += 2 * kStride) {
+    const uint32_t tb = ta + kStride;
+    TileLoad A, B;
+    tile_load(p, P, used, ta, lane, A);
+    const bool hasB = tb < p.T;
+    if (hasB) tile_load(p, P, used, tb, lane, B);
+    tile_store(p, P, used, ta, lane, obase, A, acc, learned);
+    if (hasB) tile_store(p, P, used, tb, lane, obase, B, acc, learned);
   }
 
   acc = warp_sum_u64(acc);
@@ -202,15 +271,26 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   }
 }
 
-// Batch fingerprint of each update: F = splitmix64(F ^ fp_i) over its rows.
-__global__ void batch_fp_kernel(const uint64_t *__restrict__ row_fp, uint32_t n_steps,
-                                uint32_t n_rows, uint64_t *__restrict__ out) {
-  const uint32_t s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= n_steps) return;
-  const uint64_t *f = row_fp + (size_t)s * n_rows;
+// Batch fingerprint of each update: F = splitmix64(F ^ fp_i) over its rows,
+// in row order.  One block per update stages the row values in shared memory
+// so the serial fold never waits on global memory.
+constexpr int kFoldChunk = 2048;
+
+__global__ void __launch_bounds__(256)
+    batch_fp_kernel(const uint64_t *__restrict__ row_fp, uint32_t n_rows,
+                    uint64_t *__restrict__ out) {
+  __shared__ uint64_t s[kFoldChunk];
+  const uint64_t *f = row_fp + (size_t)blockIdx.x * n_rows;
   uint64_t F = 0;
-  for (uint32_t i = 0; i < n_rows; i++) F = splitmix64(F ^ f[i]);
-  out[s] = F;
+  for (uint32_t c0 = 0; c0 < n_rows; c0 += kFoldChunk) {
+    const uint32_t n = min((uint32_t)kFoldChunk, n_rows - c0);
+    for (uint32_t t = threadIdx.x; t < n; t += blockDim.x) s[t] = __ldg(f + c0 + t);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (uint32_t t = 0; t < n; t++) F = splitmix64(F ^ s[t]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[blockIdx.x] = F;
 }
 
 }  // namespace
@@ -226,7 +306,7 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
                             uint64_t *out, cudaStream_t st) {
   ++launch_counter();
-  batch_fp_kernel<<<(n_steps + 63) / 64, 64, 0, st>>>(row_fp, n_steps, n_rows, out);
+  batch_fp_kernel<<<n_steps, 256, 0, st>>>(row_fp, n_rows, out);
   return cudaGetLastError();
 }
 

@@ -166,6 +166,76 @@ __global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
   if (act) cum[(size_t)K * J + j] = (int32_t)C;
 }
 
+// Rank of this lane's value among lanes [0, count) by (value desc, lane asc);
+// the value is a 128-bit integer split into a signed high and unsigned low half.
+__device__ __forceinline__ int warp_rank128(int64_t hi, uint64_t lo, int count, int lane) {
+  int r = 0;
+  for (int j = 0; j < count; j++) {
+    const int64_t h = __shfl_sync(0xffffffffu, hi, j);
+    const uint64_t l = __shfl_sync(0xffffffffu, lo, j);
+    r += (h > hi) || (h == hi && (l > lo || (l == lo && j < lane)));
+  }
+  return r;
+}
+
+// The same two-level rule as quota_sources_kernel + quota_strata_kernel for
+// recipes with at most 32 sources and 32 strata per source: one warp per
+// source replays the source level (identical in every block) and splits its
+// source's windows among the strata.  The shortfalls are carried forward
+// instead of recomputed: at the source level delta_c grows by B v_c - V a_c
+// per update; at the stratum level D_c = Cs v_c - V_s C_c grows by
+// n v_c - V_s a_c, and the source's n is its floor share or one more, so both
+// floors of the strata are computed once.
+__global__ void __launch_bounds__(32)
+    quota_warp_kernel(const uint32_t *__restrict__ sw, uint32_t S,
+                      const uint32_t *__restrict__ tw, const uint32_t *__restrict__ src_first,
+                      uint32_t J, uint32_t B, uint32_t K, int32_t *__restrict__ quota,
+                      int32_t *__restrict__ cum) {
+  const int lane = threadIdx.x;
+  const uint32_t s = blockIdx.x;
+  // source level
+  const bool act = lane < (int)S;
+  const uint64_t v = act ? sw[lane] : 0;
+  const uint64_t V = warp_sum_u64(v);
+  const int64_t base = act ? (int64_t)(((uint64_t)B * v) / V) : 0;
+  const int64_t R = (int64_t)B - warp_sum_i64(base);
+  const __int128 step_gain = (__int128)B * (__int128)v;
+  __int128 delta = step_gain - (__int128)V * (__int128)base;
+  // stratum level of source s
+  const uint32_t f0 = src_first[s];
+  const int n_st = (int)(src_first[s + 1] - f0);
+  const bool sact = lane < n_st;
+  const uint64_t w = sact ? tw[f0 + lane] : 0;
+  const uint64_t Vs = warp_sum_u64(w);
+  const int64_t bs = __shfl_sync(0xffffffffu, base, (int)s);
+  const int64_t b0 = sact ? (int64_t)(((uint64_t)bs * w) / Vs) : 0;
+  const int64_t b1 = sact ? (int64_t)(((uint64_t)(bs + 1) * w) / Vs) : 0;
+  const int64_t R0 = bs - warp_sum_i64(b0);
+  const int64_t R1 = bs + 1 - warp_sum_i64(b1);
+  __int128 D = 0;
+  int64_t C = 0;
+  for (uint32_t k = 0; k < K; k++) {
+    const int rs = warp_rank128((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
+    const int64_t a = base + ((act && rs < R) ? 1 : 0);
+    delta += step_gain - (__int128)V * (__int128)a;
+    const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
+    const bool lo_share = (n == bs);
+    const int64_t bsel = lo_share ? b0 : b1;
+    const int64_t Rsel = lo_share ? R0 : R1;
+    const __int128 gain = (__int128)n * (__int128)w;
+    const __int128 d2 = D + gain - (__int128)Vs * (__int128)bsel;
+    const int rt = warp_rank128((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
+    const int64_t a2 = bsel + ((sact && rt < Rsel) ? 1 : 0);
+    if (sact) {
+      quota[(size_t)k * J + f0 + lane] = (int32_t)a2;
+      cum[(size_t)k * J + f0 + lane] = (int32_t)C;
+    }
+    C += a2;
+    D += gain - (__int128)Vs * (__int128)a2;
+  }
+  if (sact) cum[(size_t)K * J + f0 + lane] = (int32_t)C;
+}
+
 // rb[k][j]: the first row of stream j in update k (rows ordered by stream).
 __global__ void row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
                                 int32_t *__restrict__ rb) {
@@ -200,7 +270,8 @@ __device__ __forceinline__ uint64_t hash_terms(int4 v, int64_t g, int64_t o0, in
 }
 
 __global__ void __launch_bounds__(kThreads)
-    hash_docs_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
+    hash_docs_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
+                     const int64_t *__restrict__ offs,
                      const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                      uint32_t J, uint64_t hash_key, uint8_t *__restrict__ heldout,
                      unsigned long long *counter) {
@@ -224,6 +295,9 @@ __global__ void __launch_bounds__(kThreads)
       }
       if (bp == 0) continue;
       const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
+      // a malformed partition is reported by validate_offsets_kernel; never
+      // read outside the tokens because of it
+      if (o0 < 0 || o1 < o0 || (uint64_t)o1 > n_tokens || o1 - o0 > 0x7FFFFFFF) continue;
       uint64_t acc = 0;
       for (int64_t g = (o0 & ~(int64_t)3) + 4 * lane; g < o1; g += 256) {
         const int4 v0 = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
@@ -602,6 +676,30 @@ __global__ void __launch_bounds__(kThreads)
   win_start[wbase[j] + r] = s;
 }
 
+// The window of every row of every update of the horizon.  Rows of an update
+// are ordered by stream, then by rank: row i belongs to the stream whose row
+// range [rb[k][j], rb[k][j+1]) holds it and takes that stream's window
+// cum[k][j] + (i - rb[k][j]); the window ends where the next one starts.
+__global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t *__restrict__ cum,
+                                   const uint32_t *__restrict__ W,
+                                   const int64_t *__restrict__ wbase,
+                                   const int32_t *__restrict__ win_start,
+                                   const int32_t *__restrict__ next, uint32_t J, uint32_t B,
+                                   uint32_t K, int2 *__restrict__ row_win) {
+  const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= (uint64_t)K * B) return;
+  const uint32_t k = (uint32_t)(x / B), i = (uint32_t)(x % B);
+  const int32_t *rbk = rb + (size_t)k * (J + 1);
+  const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)J, (int32_t)i);
+  const int64_t r = (int64_t)cum[(size_t)k * J + j] + ((int64_t)i - rbk[j]);
+  int2 w = make_int2(-1, -1);
+  if (r < (int64_t)W[j]) {
+    const int32_t s = win_start[wbase[j] + r];
+    w = make_int2(s, next[s]);
+  }
+  row_win[x] = w;
+}
+
 // First update that asks a stream for a window past its last.
 __global__ void set_u32_kernel(uint32_t *p, uint32_t v) { *p = v; }
 
@@ -757,6 +855,14 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
   return cudaGetLastError();
 }
 
+cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
+                              const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
+                              int32_t *quota, int32_t *cum, cudaStream_t st) {
+  ++launch_counter();
+  quota_warp_kernel<<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st) {
   ++launch_counter();
@@ -764,12 +870,14 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
   return cudaGetLastError();
 }
 
-cudaError_t launch_hash_docs(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
+cudaError_t launch_hash_docs(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
+                             const uint32_t *sdb,
                              const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
                              uint8_t *heldout, unsigned long long *counter, int n_sms,
                              cudaStream_t st) {
   ++launch_counter();
-  hash_docs_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, hash_key,
+  hash_docs_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, n_tokens, offs, sdb, stream_bp, J,
+                                                   hash_key,
                                                    heldout, counter);
   return cudaGetLastError();
 }
@@ -873,6 +981,17 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
   ++launch_counter();
   window_starts_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, levels, n_nodes, n_levels, node_base,
                                                         W, wbase, win_start);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
+                               const int64_t *wbase, const int32_t *win_start,
+                               const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
+                               int2 *row_win, cudaStream_t st) {
+  ++launch_counter();
+  row_windows_kernel<<<blocks_for((uint64_t)K * B), kThreads, 0, st>>>(rb, cum, W, wbase,
+                                                                       win_start, next, J, B, K,
+                                                                       row_win);
   return cudaGetLastError();
 }
 

@@ -30,11 +30,16 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *stream
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 cudaStream_t st);
+// Both levels in one kernel when n_sources <= 32 and every source has <= 32 strata.
+cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
+                              const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
+                              int32_t *quota, int32_t *cum, cudaStream_t st);
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st);
 
 // ---- held-out hash, order, scans ------------------------------------------
-cudaError_t launch_hash_docs(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
+cudaError_t launch_hash_docs(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
+                             const uint32_t *sdb,
                              const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
                              uint8_t *heldout, unsigned long long *counter, int n_sms,
                              cudaStream_t st);
@@ -71,6 +76,12 @@ cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_
 cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nodes,
                                  uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
                                  const int64_t *wbase, int32_t *win_start, cudaStream_t st);
+// row_win[k][i] = (first piece, end piece) of the window row i of update k
+// takes, or (-1, -1) when the row lies past the end of its stream.
+cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
+                               const int64_t *wbase, const int32_t *win_start,
+                               const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
+                               int2 *row_win, cudaStream_t st);
 cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st);
@@ -98,19 +109,14 @@ struct GatherParams {
   // corpus
   const int32_t *tokens;
   // context tables
-  const int32_t *rb;        // [K][J + 1]
-  const int32_t *cum;       // [K + 1][J]
-  const uint32_t *W;        // [J]
-  const int64_t *wbase;     // [J]
-  const int32_t *win_start; // [sum rmax]
-  const int32_t *next;      // [nodes]
+  const int2 *row_win;      // [K][B]: pieces [x, y) of the row's window; x < 0 past the end
   const int64_t *node_S;    // [nodes]
   const int64_t *node_src;  // [nodes]
   const int32_t *node_doc;  // [nodes]
   const int32_t *node_mthr; // [nodes]
   int *err;
   // launch
-  uint32_t J, T, step0, n_steps, row0, n_rows;
+  uint32_t B, T, step0, n_steps, row0, n_rows;
   int32_t pad_id;
   // outputs
   int32_t *tokens_out, *pos_out, *doc_out;

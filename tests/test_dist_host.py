@@ -1,0 +1,67 @@
+"""Multi-rank host logic of the benchmark, on CPU with the gloo backend.
+
+Each rank assembles its own slice of rows of every update; the slices must
+partition the global batch, and the timing reduction takes the maximum over
+ranks.  The oracle shows that the rows each rank would produce concatenate to
+the global batch.
+"""
+import multiprocessing as mp
+import os
+import socket
+
+import numpy as np
+import pytest
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, B, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
+    import bench
+    d = bench.Dist()
+    r0, r1 = bench.row_slice(rank, world, B)
+    m = d.max(float(rank + 1) * 1.5)
+    s = d.sum(float(r1 - r0))
+    d.barrier()
+    d.close()
+    q.put((rank, r0, r1, m, s))
+
+
+@pytest.mark.parametrize("world,B", [(2, 512), (3, 16), (4, 64)])
+def test_ranks_partition_rows_and_take_the_max(world, B):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, world, port, B, q)) for r in range(world)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    cover = []
+    for rank, r0, r1, m, s in res:
+        cover.extend(range(r0, r1))
+        assert m == world * 1.5
+        assert s == B
+    assert cover == list(range(B))
+
+
+def test_rank_slices_concatenate_to_the_global_batch():
+    import bench
+    import oracle
+    from corpus import make_preset
+    c = make_preset("c1")
+    o = oracle.Oracle(c)
+    full = o.rows(3)
+    for world in (2, 4, 8):
+        parts = [o.rows(3, *bench.row_slice(r, world, c.B)) for r in range(world)]
+        for k in full:
+            assert np.array_equal(np.concatenate([p[k] for p in parts]), full[k])

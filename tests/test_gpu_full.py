@@ -1,0 +1,122 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times (32 updates per ns_pack_step launch, all rows of the global batch).
+
+Sampled updates are compared element by element with the oracle; whole-pass
+properties (valid horizon, order digest, quota tables, exactly-once coverage
+of a full long-context pass, learned counts of every SFT update) are checked
+at any size.  The elastic-determinism workload is also assembled in R = 8, 16,
+32 and 64 row slices ("Zephon: deterministic data loading": the SHA-256 of
+every global batch matches byte for byte at any GPU count).
+"""
+import numpy as np
+import pytest
+import oracle
+from _gpu import assert_rows_equal, batch_sha256, oracle_for, packer_for, to_host
+from corpus import make_preset
+
+pytestmark = pytest.mark.gpu
+
+LAUNCH = 32
+
+_cache = {}
+
+
+def _setup(name):
+    if name not in _cache:
+        c = make_preset(name)
+        _cache[name] = (c, packer_for(c), oracle_for(c))
+    return _cache[name]
+
+
+def _sampled(pk, o, steps):
+    valid = o.valid_steps
+    for k in steps:
+        s0 = (k // LAUNCH) * LAUNCH
+        n = min(LAUNCH, valid - s0)
+        got = to_host(pk.step(s0, n_steps=n))
+        q = k - s0
+        assert_rows_equal({f: v[q] for f, v in got.items()}, o.rows(k), f"update {k}")
+        assert pk.batch_fp(pk.step(k)["row_fp"][0]) == oracle.batch_fp(o.rows(k)["row_fp"])
+
+
+def _tables(pk, o, c):
+    assert pk.valid_steps == o.valid_steps
+    assert pk.order_digest == o.digest
+    q, cum = pk.quota_table()
+    oq, ocum, _ = o.quota()
+    assert (q == oq).all() and (cum == ocum).all()
+    w, complete = pk.stream_windows()
+    for j in range(c.n_streams):
+        if complete[j]:
+            assert w[j] == o.n_windows(j)
+        else:
+            assert ocum[-1, j] < w[j] <= o.n_windows(j)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_full_size_sampled_updates(name):
+    c, pk, o = _setup(name)
+    _tables(pk, o, c)
+    v = o.valid_steps
+    assert v > 0
+    steps = sorted({0, 1, LAUNCH - 1, LAUNCH, v // 2, v - 2, v - 1} & set(range(v)))
+    _sampled(pk, o, steps)
+    pk.check()
+
+
+def test_full_size_mixture_within_two_windows():
+    c, pk, o = _setup("c3")
+    q, _ = pk.quota_table()
+    ss = c.stream_source.astype(np.int64)
+    src = np.zeros((q.shape[0], c.n_sources), np.int64)
+    for j in range(c.n_streams):
+        src[:, ss[j]] += q[:, j]
+    w = c.source_weight.astype(np.float64)
+    share = c.B * w / w.sum()
+    assert (np.abs(src - share[None, :]) <= 1).all()
+    assert (src.sum(1) == c.B).all()
+
+
+def test_full_size_sft_learned_counts_every_update():
+    c, pk, o = _setup("c2")
+    v = o.valid_steps
+    for s0 in range(0, v, LAUNCH):
+        n = min(LAUNCH, v - s0)
+        out = pk.step(s0, n_steps=n)
+        got_l = out["row_learned"].cpu().numpy()
+        got_fp = out["row_fp"].cpu().numpy().view(np.uint64)
+        for q in range(n):
+            want = o.rows(s0 + q)
+            assert (got_l[q] == want["row_learned"]).all(), s0 + q
+            assert (got_fp[q] == want["row_fp"]).all(), s0 + q
+
+
+def test_full_size_elastic_slices():
+    c, pk, o = _setup("c4")
+    for k in (0, o.valid_steps - 1):
+        full = to_host(pk.step(k))
+        want = o.rows(k)
+        assert_rows_equal({f: v[0] for f, v in full.items()}, want, f"update {k}")
+        sha = batch_sha256({f: v[0] for f, v in full.items()})
+        for R in (8, 16, 32, 64):
+            parts = [to_host(pk.step(k, rows=(r * c.B // R, (r + 1) * c.B // R)))
+                     for r in range(R)]
+            cat = {f: np.concatenate([p[f][0] for p in parts]) for f in parts[0]}
+            assert batch_sha256(cat) == sha, (k, R)
+            assert (cat["row_fp"] == want["row_fp"]).all()
+
+
+def test_full_size_long_context_full_pass_exactly_once():
+    c, pk, o = _setup("c5")
+    v = o.valid_steps
+    real = 0
+    learned = 0
+    for s0 in range(0, v, LAUNCH):
+        n = min(LAUNCH, v - s0)
+        out = pk.step(s0, n_steps=n)
+        real += int((out["doc"] >= 0).sum().item())
+        learned += int(out["row_learned"].sum().item())
+    # no held-out rate: every token of the corpus is assembled exactly once
+    assert real == learned == c.n_tokens
+    w, complete = pk.stream_windows()
+    assert complete[0] and w[0] == o.n_windows(0)

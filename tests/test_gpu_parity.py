@@ -209,3 +209,20 @@ def test_batch_fingerprints_many():
     fps = pk.batch_fp_many(out["row_fp"]).cpu().numpy().view(np.uint64)
     for k in range(o.valid_steps):
         assert fps[k] == oracle.batch_fp(o.rows(k)["row_fp"])
+
+
+@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40), (33, 1), (1, 33)])
+def test_quota_tables_beyond_one_warp(S, strata):
+    # more than 32 sources, or more than 32 strata in a source, take the
+    # block-level quota kernels instead of the single-warp one
+    J = S * strata
+    rng = np.random.default_rng(S * 100 + strata)
+    lengths = [int(x) for x in rng.integers(1, 200, size=J * 6)]
+    c = corpus_from_lengths(lengths, T=256, B=97, max_steps=7, stream_docs=[6] * J,
+                            stream_source=[s for s in range(S) for _ in range(strata)],
+                            source_weight=[int(x) for x in rng.integers(1, 1000, size=S)],
+                            stream_weight=[int(x) for x in rng.integers(1, 1000, size=J)],
+                            drain=True)
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=3)
