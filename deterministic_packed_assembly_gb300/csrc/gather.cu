@@ -62,8 +62,14 @@ struct Pieces {
   int64_t sbase;        // subtracted from S to make it window-relative
   int32_t np;
   __device__ __forceinline__ int64_t dst(int32_t q) const { return S[q] - sbase; }
-  // last piece q in [lo, np) with dst(q) <= t
+  // last piece q in [lo, np) with dst(q) <= t (dst(lo) <= t); pieces of one
+  // warp's tiles only move forward, so a few linear probes usually suffice
   __device__ __forceinline__ int32_t find(int32_t lo, int64_t t) const {
+#pragma unroll
+    for (int probe = 0; probe < 3; probe++) {
+      if (lo + 1 >= np || S[lo + 1] - sbase > t) return lo;
+      lo++;
+    }
     int32_t l = lo, h = np;
     while (l < h) {
       const int32_t m = l + (h - l) / 2;
@@ -76,67 +82,88 @@ struct Pieces {
   }
 };
 
-// One tile's state between its load and its stores.
-struct TileLoad {
-  int kind;      // 0 pad, 1 inside piece q, 2 crosses piece ends
+// cp.async: 16 bytes global -> shared, asynchronous, tracked in groups.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+constexpr int kStages = 4;         // tiles in flight per warp
+constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
+
+// What a tile needs between its copy and its stores (kept in shared memory).
+struct TileMeta {
+  int32_t kind;  // 0 pad, 1 inside piece q (staged), 2 crosses piece ends
   int32_t q;     // piece of the tile's first position
-  int32_t x0;    // offset of the lane's first position inside piece q (kind 1)
-  int sh;        // source misalignment in tokens (kind 1)
-  int4 v;        // aligned 16-byte load (kind 1)
-  int4 nv;       // lane 31's next 16 bytes (kind 1, sh != 0)
+  int32_t x0;    // offset of the tile's first position inside piece q
+  int32_t sh;    // source misalignment in tokens (kind 1)
 };
 
-__device__ __forceinline__ void tile_load(const GatherParams &p, const Pieces &P, int32_t used,
-                                          uint32_t t0, int lane, TileLoad &L) {
-  if ((int32_t)t0 >= used) {
-    L.kind = 0;
-    return;
+// Classify tile t0 and, for a tile inside one piece, start copying its tokens
+// (rounded out to 16-byte blocks that each hold at least one of them).
+__device__ __forceinline__ void tile_issue(const GatherParams &p, const Pieces &P, int32_t used,
+                                           uint32_t t0, int32_t q_hint, int lane, int32_t *buf,
+                                           TileMeta *meta) {
+  TileMeta m;
+  m.kind = 0;
+  m.q = q_hint;
+  m.x0 = 0;
+  m.sh = 0;
+  if ((int32_t)t0 < used) {
+    m.q = P.find(q_hint, (int64_t)t0);
+    const int64_t qs = P.dst(m.q);
+    const int64_t qe = P.dst(m.q + 1);
+    m.x0 = (int32_t)((int64_t)t0 - qs);
+    if (qe >= (int64_t)t0 + kTile) {
+      m.kind = 1;
+      const int64_t srcw = P.src[m.q] + m.x0;
+      m.sh = (int32_t)(srcw & 3);
+      const int32_t *g = p.tokens + (srcw - m.sh);
+      cp_async16(buf + 4 * lane, g + 4 * lane);
+      if (lane == 0 && m.sh != 0) cp_async16(buf + 128, g + 128);
+    } else {
+      m.kind = 2;
+    }
   }
-  L.q = P.find(0, (int64_t)t0);
-  const int64_t qs = P.dst(L.q);
-  const int64_t qe = P.dst(L.q + 1);
-  if (qe >= (int64_t)t0 + kTile) {
-    L.kind = 1;
-    const int64_t x0 = (int64_t)t0 - qs;
-    const int64_t srcw = P.src[L.q] + x0;
-    L.sh = (int)(srcw & 3);
-    const int4 *src4 = reinterpret_cast<const int4 *>(p.tokens + (srcw - L.sh));
-    L.v = __ldg(src4 + lane);
-    if (L.sh != 0 && lane == 31) L.nv = __ldg(src4 + 32);
-    L.x0 = (int32_t)x0 + 4 * lane;
-  } else {
-    L.kind = 2;
-  }
+  if (lane == 0) *meta = m;
 }
 
 __device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &P, int32_t used,
-                                           uint32_t t0, int lane, size_t obase, TileLoad &L,
-                                           uint64_t &acc, int &learned) {
+                                           uint32_t t0, int lane, size_t obase, const int32_t *buf,
+                                           const TileMeta &m, uint64_t &acc, int &learned) {
   const uint32_t tp = t0 + 4u * lane;
   int4 tk, ps, dc;
   uint32_t mk = 0;
-  if (L.kind == 0) {
+  if (m.kind == 0) {
     tk = make_int4(p.pad_id, p.pad_id, p.pad_id, p.pad_id);
     ps = make_int4(0, 0, 0, 0);
     dc = make_int4(-1, -1, -1, -1);
-  } else if (L.kind == 1) {
-    if (L.sh == 0) {
-      tk = L.v;
+  } else if (m.kind == 1) {
+    const int4 v = *reinterpret_cast<const int4 *>(buf + 4 * lane);
+    if (m.sh == 0) {
+      tk = v;
     } else {
-      int4 nv = shfl_down4(L.v);
-      if (lane == 31) nv = L.nv;
-      if (L.sh == 1)
-        tk = make_int4(L.v.y, L.v.z, L.v.w, nv.x);
-      else if (L.sh == 2)
-        tk = make_int4(L.v.z, L.v.w, nv.x, nv.y);
+      int4 nv = shfl_down4(v);
+      if (lane == 31) nv = *reinterpret_cast<const int4 *>(buf + 128);
+      if (m.sh == 1)
+        tk = make_int4(v.y, v.z, v.w, nv.x);
+      else if (m.sh == 2)
+        tk = make_int4(v.z, v.w, nv.x, nv.y);
       else
-        tk = make_int4(L.v.w, nv.x, nv.y, nv.z);
+        tk = make_int4(v.w, nv.x, nv.y, nv.z);
     }
-    const int32_t x = L.x0;
+    const int32_t x = m.x0 + 4 * lane;
     ps = make_int4(x, x + 1, x + 2, x + 3);
-    const int32_t d = P.doc[L.q];
+    const int32_t d = P.doc[m.q];
     dc = make_int4(d, d, d, d);
-    const int32_t th = P.mthr[L.q];
+    const int32_t th = P.mthr[m.q];
     mk = (x >= th ? 1u : 0u) | (x + 1 >= th ? 1u << 8 : 0u) | (x + 2 >= th ? 1u << 16 : 0u) |
          (x + 3 >= th ? 1u << 24 : 0u);
   } else {
@@ -154,7 +181,7 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &
         continue;
       }
       if (qq < 0) {
-        qq = P.find(L.q, (int64_t)t);
+        qq = P.find(m.q, (int64_t)t);
         qqs = P.dst(qq);
         qqe = P.dst(qq + 1);
       }
@@ -191,6 +218,8 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   __shared__ int64_t s_src[kPieceCap];
   __shared__ int32_t s_doc[kPieceCap];
   __shared__ int32_t s_mthr[kPieceCap];
+  __shared__ __align__(16) int32_t s_tok[kGatherWarps][kStages][kStageWords];
+  __shared__ TileMeta s_meta[kGatherWarps][kStages];
   __shared__ uint64_t s_fp[kGatherWarps];
   __shared__ int s_learned[kGatherWarps];
 
@@ -237,18 +266,39 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     used = 0;
   }
 
+  // this warp's tiles: t0 = warp * 128 + m * 1024, m < n_tiles, through a
+  // ring of kStages shared-memory buffers filled by cp.async
+  constexpr uint32_t kStride = kGatherWarps * kTile;
+  const uint32_t first = (uint32_t)warp * kTile;
+  const int n_tiles = first < p.T ? (int)((p.T - first + kStride - 1) / kStride) : 0;
+  int32_t(*ring)[kStageWords] = s_tok[warp];
+  TileMeta *meta = s_meta[warp];
+  int32_t q_hint = 0;
+#pragma unroll
+  for (int m = 0; m < kStages - 1; m++) {
+    if (m < n_tiles) {
+      tile_issue(p, P, used, first + m * kStride, q_hint, lane, ring[m], &meta[m]);
+      __syncwarp();
+      q_hint = meta[m].q;
+    }
+    cp_async_commit();
+  }
   const size_t obase = (size_t)blk * p.T;
   uint64_t acc = 0;
   int learned = 0;
-  constexpr uint32_t kStride = kGatherWarps * kTile;
-  for (uint32_t ta = (uint32_t)warp * kTile; ta < p.T; ta += 2 * kStride) {
-    const uint32_t tb = ta + kStride;
-    TileLoad A, B;
-    tile_load(p, P, used, ta, lane, A);
-    const bool hasB = tb < p.T;
-    if (hasB) tile_load(p, P, used, tb, lane, B);
-    tile_store(p, P, used, ta, lane, obase, A, acc, learned);
-    if (hasB) tile_store(p, P, used, tb, lane, obase, B, acc, learned);
+  for (int m = 0; m < n_tiles; m++) {
+    const int mi = m + kStages - 1;
+    if (mi < n_tiles) {
+      tile_issue(p, P, used, first + mi * kStride, q_hint, lane, ring[mi % kStages],
+                 &meta[mi % kStages]);
+    }
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    if (mi < n_tiles) q_hint = meta[mi % kStages].q;
+    const TileMeta mt = meta[m % kStages];
+    tile_store(p, P, used, first + m * kStride, lane, obase, ring[m % kStages], mt, acc, learned);
+    __syncwarp();
   }
 
   acc = warp_sum_u64(acc);

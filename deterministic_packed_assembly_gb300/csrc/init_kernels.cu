@@ -269,6 +269,15 @@ __device__ __forceinline__ uint64_t hash_terms(int4 v, int64_t g, int64_t o0, in
   return s;
 }
 
+// Four tokens that all lie inside the document, the first at in-document
+// index i0 (documents are shorter than 2^31 tokens).
+__device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
+  return splitmix64(((uint64_t)i0 << 32) | (uint32_t)v.x) +
+         splitmix64(((uint64_t)(i0 + 1) << 32) | (uint32_t)v.y) +
+         splitmix64(((uint64_t)(i0 + 2) << 32) | (uint32_t)v.z) +
+         splitmix64(((uint64_t)(i0 + 3) << 32) | (uint32_t)v.w);
+}
+
 __global__ void __launch_bounds__(kThreads)
     hash_docs_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
                      const int64_t *__restrict__ offs,
@@ -304,8 +313,16 @@ __global__ void __launch_bounds__(kThreads)
         const bool has1 = g + 128 < o1;
         int4 v1 = make_int4(0, 0, 0, 0);
         if (has1) v1 = __ldcs(reinterpret_cast<const int4 *>(tokens + g + 128));
-        acc += hash_terms(v0, g, o0, o1);
-        if (has1) acc += hash_terms(v1, g + 128, o0, o1);
+        if (g >= o0 && g + 3 < o1)
+          acc += hash_terms_inside(v0, (uint32_t)(g - o0));
+        else
+          acc += hash_terms(v0, g, o0, o1);
+        if (has1) {
+          if (g + 128 + 3 < o1)
+            acc += hash_terms_inside(v1, (uint32_t)(g + 128 - o0));
+          else
+            acc += hash_terms(v1, g + 128, o0, o1);
+        }
       }
       acc = warp_sum_u64(acc);
       if (lane == 0) {
