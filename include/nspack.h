@@ -142,7 +142,7 @@ typedef struct {
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of
  * every source with a held-out rate, shuffle every stream, pack the prefix of
  * each stream that max_steps can reach, number its windows and apportion every
- * update of the horizon.  Synchronises the stream (three times).  On success
+ * update of the horizon.  Synchronises the stream twice.  On success
  * *out owns device tables allocated through cfg->alloc; on failure nothing is
  * kept and *out is NULL.  Errors: INVALID_ARG, CUDA, OOM, BAD_INPUT. */
 int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out);
