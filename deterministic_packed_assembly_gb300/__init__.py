@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     ns_pack_free,
     ns_pack_info,
     ns_pack_init,
+    ns_pack_quota_noalloc,
     ns_pack_quota_table,
     ns_pack_step,
     ns_pack_stream_windows,

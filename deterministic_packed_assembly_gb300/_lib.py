@@ -85,7 +85,7 @@ class ns_pack_info_t(C.Structure):
 # Every symbol the header declares, for the load check.
 SYMBOLS = ("ns_pack_init", "ns_pack_step", "ns_pack_fingerprint", "ns_pack_batch_fp",
            "ns_pack_info", "ns_pack_stream_windows", "ns_pack_quota_table", "ns_pack_check",
-           "ns_pack_free", "ns_pack_strerror")
+           "ns_pack_free", "ns_pack_strerror", "ns_pack_quota_noalloc")
 
 
 def _load() -> C.CDLL:
@@ -115,6 +115,8 @@ def _load() -> C.CDLL:
     L.ns_pack_free.argtypes = [vp]
     L.ns_pack_strerror.restype = C.c_char_p
     L.ns_pack_strerror.argtypes = [i32]
+    L.ns_pack_quota_noalloc.restype = i32
+    L.ns_pack_quota_noalloc.argtypes = [vp, u32, vp, vp, u32, u32, u32, vp, vp, vp]
     return L
 
 
@@ -187,6 +189,19 @@ def ns_pack_check(ctx) -> None:
 
 def ns_pack_free(ctx) -> None:
     lib.ns_pack_free(ctx)
+
+
+def ns_pack_quota_noalloc(source_weight, stream_source, stream_weight, B: int, max_steps: int,
+                          quota_ptr: int, cum_ptr: int, stream: int | None = None) -> None:
+    """Quota tables of a recipe into caller-owned device buffers, with no
+    device allocation (for callers that cannot call cudaMalloc)."""
+    import numpy as np
+    sw = np.ascontiguousarray(source_weight, dtype=np.uint32)
+    ss = np.ascontiguousarray(stream_source, dtype=np.uint32)
+    tw = np.ascontiguousarray(stream_weight, dtype=np.uint32)
+    check(lib.ns_pack_quota_noalloc(sw.ctypes.data, sw.size, ss.ctypes.data, tw.ctypes.data,
+                                    ss.size, B, max_steps, quota_ptr, cum_ptr, stream),
+          "ns_pack_quota_noalloc")
 
 
 def ns_pack_strerror(code: int) -> str:

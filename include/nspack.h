@@ -192,6 +192,39 @@ void ns_pack_free(ns_pack_ctx *ctx);
 
 const char *ns_pack_strerror(int code);
 
+/* ---- quota tables without allocating --------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc: a trainer that gives all of the GPU's memory to
+ * its own pool at start-up, a process held to a fixed memory budget on a
+ * shared GPU, or a loop that cannot afford the device synchronisation that
+ * cudaMalloc / cudaFree imply.  It computes the same tables that ns_pack_init
+ * builds and ns_pack_quota_table returns -- quota[k][j], the windows of stream
+ * j in update k (max_steps x n_streams), and cum[k][j], its windows before
+ * update k ((max_steps + 1) x n_streams), both int32 -- into device buffers the
+ * caller owns, asynchronously on cuda_stream (NULL: the legacy default
+ * stream).
+ *
+ * Arguments: the recipe's weights on the host (the same meaning and checks as
+ * in ns_pack_config: source_weight[n_sources] > 0, stream_source[n_streams]
+ * nondecreasing with every source owning 1..NS_MAX_STRATA_PER_SOURCE streams,
+ * stream_weight[n_streams] > 0), B >= 1, max_steps >= 1 with max_steps * B <
+ * 2^31.  Nothing is allocated: the device copies of the weights and, when
+ * there are more than 32 sources or more than 32 strata in a source, a
+ * [max_steps][n_sources] int32 table live in one static device array of
+ * NS_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
+ * exit.  A recipe whose scratch does not fit returns NS_ERR_INVALID_ARG, as do
+ * out-of-range arguments; NS_ERR_CUDA if a CUDA call fails.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current) and keeps it: make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents;
+ * calls whose work overlaps on the GPU (on different streams, or from several
+ * threads without ordering) race on it. */
+#define NS_NOALLOC_SCRATCH_BYTES (8u << 20)
+int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_sources,
+                          const uint32_t *stream_source, const uint32_t *stream_weight,
+                          uint32_t n_streams, uint32_t B, uint32_t max_steps,
+                          int32_t *quota_dev, int32_t *cum_dev, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
