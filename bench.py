@@ -293,13 +293,13 @@ def run_ours(args, dist: Dist) -> None:
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            pk.step(s0, m, rows=rows, out=view, stream=stream)
+            # with every row of the batch, the kernel also folds each
+            # update's batch fingerprint
+            pk.step(s0, m, rows=rows, out=view, stream=stream,
+                    batch_fp=fp_all[s0:s0 + m] if dist.world == 1 else None)
             if record:
                 b.record(stream)
                 state["events"].append((a, b))
-            if dist.world == 1:
-                pk.batch_fp_many(view["row_fp"], out=fp_all[s0:s0 + m], stream=stream)
-                n += 1
             if e2e is not None:
                 e2e[3][s0:s0 + m].copy_(view["row_fp"], non_blocking=True)
                 e2e[4][s0:s0 + m].copy_(view["row_learned"], non_blocking=True)

@@ -41,6 +41,7 @@ struct ns_pack_ctx {
   int32_t *node_doc = nullptr, *node_mthr = nullptr;
   int *err = nullptr;
   uint64_t *fp_out = nullptr;
+  uint32_t *fold_count = nullptr;
   std::vector<void *> kept;
 };
 
@@ -220,7 +221,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->err);
   c->fp_out = a.keep<uint64_t>(1);
   NS_ALLOC(c->fp_out);
+  c->fold_count = a.keep<uint32_t>(K);
+  NS_ALLOC(c->fold_count);
   NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
+  NS_CK(cudaMemsetAsync(c->fold_count, 0, (size_t)K * sizeof(uint32_t), st));
 
   // ---- 1. quotas of every update, on a side stream ------------------------
   // They depend only on the weights, so they run while the corpus is hashed
@@ -237,8 +241,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
   if (S <= 32 && max_strata <= 32) {
     NS_CK(nsk::launch_quota_warp(static_cast<uint32_t *>(d_sw), S, static_cast<uint32_t *>(d_tw),
-                                 static_cast<uint32_t *>(d_src_first), J, c->B, K, c->quota,
-                                 c->cum, side.s));
+                                 static_cast<uint32_t *>(d_src_first), J, c->B, K, max_strata,
+                                 c->quota, c->cum, side.s));
   } else {
     int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
     NS_ALLOC(src_quota);
@@ -503,6 +507,7 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
                        reinterpret_cast<uintptr_t>(out->doc) | reinterpret_cast<uintptr_t>(out->mask);
   if (al % 16 != 0) return NS_ERR_INVALID_ARG;
   if ((uint64_t)n_steps * (row_end - row_begin) >= (1ull << 31)) return NS_ERR_INVALID_ARG;
+  if (out->batch_fp && (row_begin != 0 || row_end != ctx->B)) return NS_ERR_INVALID_ARG;
   if ((uint64_t)step0 + n_steps > ctx->K) return NS_ERR_HORIZON;
   if ((uint64_t)step0 + n_steps > ctx->valid_steps) return NS_ERR_EXHAUSTED;
   nsk::GatherParams p{};
@@ -526,6 +531,8 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   p.mask_out = out->mask;
   p.row_fp = out->row_fp;
   p.row_learned = out->row_learned;
+  p.batch_fp = out->batch_fp;
+  p.fold_count = ctx->fold_count;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_gather(p, st) != cudaSuccess) {
     cudaGetLastError();

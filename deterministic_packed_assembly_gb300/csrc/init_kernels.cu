@@ -167,13 +167,28 @@ __global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
 }
 
 // Rank of this lane's value among lanes [0, count) by (value desc, lane asc);
-// the value is a 128-bit integer split into a signed high and unsigned low half.
+// the value is a 128-bit integer split into a signed high and unsigned low
+// half.  MAXC >= count bounds the fully unrolled loop, so the shuffles issue
+// back to back; when every value fits in 64 bits (the usual case: a shortfall
+// is a few windows times the weight sum) half the shuffles suffice.
+template <int MAXC>
 __device__ __forceinline__ int warp_rank128(int64_t hi, uint64_t lo, int count, int lane) {
+  const bool fits = hi == ((int64_t)lo >> 63);
   int r = 0;
-  for (int j = 0; j < count; j++) {
-    const int64_t h = __shfl_sync(0xffffffffu, hi, j);
-    const uint64_t l = __shfl_sync(0xffffffffu, lo, j);
-    r += (h > hi) || (h == hi && (l > lo || (l == lo && j < lane)));
+  if (__all_sync(0xffffffffu, fits || lane >= count)) {
+    const int64_t x = (int64_t)lo;
+#pragma unroll
+    for (int j = 0; j < MAXC; j++) {
+      const int64_t y = __shfl_sync(0xffffffffu, x, j);
+      r += (j < count && (y > x || (y == x && j < lane))) ? 1 : 0;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < MAXC; j++) {
+      const int64_t h = __shfl_sync(0xffffffffu, hi, j);
+      const uint64_t l = __shfl_sync(0xffffffffu, lo, j);
+      r += (j < count && (h > hi || (h == hi && (l > lo || (l == lo && j < lane))))) ? 1 : 0;
+    }
   }
   return r;
 }
@@ -186,6 +201,7 @@ __device__ __forceinline__ int warp_rank128(int64_t hi, uint64_t lo, int count, 
 // per update; at the stratum level D_c = Cs v_c - V_s C_c grows by
 // n v_c - V_s a_c, and the source's n is its floor share or one more, so both
 // floors of the strata are computed once.
+template <int SMAX, int TMAX>
 __global__ void __launch_bounds__(32)
     quota_warp_kernel(const uint32_t *__restrict__ sw, uint32_t S,
                       const uint32_t *__restrict__ tw, const uint32_t *__restrict__ src_first,
@@ -215,7 +231,7 @@ __global__ void __launch_bounds__(32)
   __int128 D = 0;
   int64_t C = 0;
   for (uint32_t k = 0; k < K; k++) {
-    const int rs = warp_rank128((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
+    const int rs = warp_rank128<SMAX>((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
     const int64_t a = base + ((act && rs < R) ? 1 : 0);
     delta += step_gain - (__int128)V * (__int128)a;
     const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(32)
     const int64_t Rsel = lo_share ? R0 : R1;
     const __int128 gain = (__int128)n * (__int128)w;
     const __int128 d2 = D + gain - (__int128)Vs * (__int128)bsel;
-    const int rt = warp_rank128((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
+    const int rt = warp_rank128<TMAX>((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
     const int64_t a2 = bsel + ((sact && rt < Rsel) ? 1 : 0);
     if (sact) {
       quota[(size_t)k * J + f0 + lane] = (int32_t)a2;
@@ -872,11 +888,32 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
   return cudaGetLastError();
 }
 
+template <int SMAX>
+static void launch_quota_warp_s(const uint32_t *sw, uint32_t S, const uint32_t *tw,
+                                const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
+                                uint32_t max_strata, int32_t *quota, int32_t *cum,
+                                cudaStream_t st) {
+  if (max_strata <= 4)
+    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+  else if (max_strata <= 8)
+    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+  else
+    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+}
+
 cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
                               const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
-                              int32_t *quota, int32_t *cum, cudaStream_t st) {
+                              uint32_t max_strata, int32_t *quota, int32_t *cum,
+                              cudaStream_t st) {
   ++launch_counter();
-  quota_warp_kernel<<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+  if (S <= 4)
+    launch_quota_warp_s<4>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+  else if (S <= 8)
+    launch_quota_warp_s<8>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+  else if (S <= 16)
+    launch_quota_warp_s<16>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+  else
+    launch_quota_warp_s<32>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
   return cudaGetLastError();
 }
 

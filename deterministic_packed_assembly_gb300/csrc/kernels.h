@@ -33,7 +33,8 @@ cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *stream
 // Both levels in one kernel when n_sources <= 32 and every source has <= 32 strata.
 cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
                               const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
-                              int32_t *quota, int32_t *cum, cudaStream_t st);
+                              uint32_t max_strata, int32_t *quota, int32_t *cum,
+                              cudaStream_t st);
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st);
 
@@ -123,6 +124,8 @@ struct GatherParams {
   uint8_t *mask_out;
   uint64_t *row_fp;
   int32_t *row_learned;
+  uint64_t *batch_fp;     // [n_steps] or null; only with every row of the batch
+  uint32_t *fold_count;   // [K] rows finished per update (zero between calls)
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
