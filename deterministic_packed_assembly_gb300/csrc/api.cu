@@ -255,24 +255,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
 
-  // ---- 2. the corpus partition and the held-out flags ---------------------
+  // ---- 2. the corpus partition; shuffled order and lengths of every position
   // Every kernel that reads tokens checks the offsets it uses, so a malformed
   // partition is reported (BAD_INPUT) at the next readback, never read past.
   NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
-  uint8_t *heldout = nullptr;
-  if (any_heldout) {
-    heldout = a.temp<uint8_t>(std::max<uint32_t>(c->n_docs, 1));
-    unsigned long long *counter = a.temp<unsigned long long>(1);
-    NS_ALLOC(heldout);
-    NS_ALLOC(counter);
-    NS_CK(cudaMemsetAsync(heldout, 0, std::max<uint32_t>(c->n_docs, 1), st));
-    NS_CK(cudaMemsetAsync(counter, 0, sizeof(unsigned long long), st));
-    NS_CK(nsk::launch_hash_docs(c->tokens, c->n_tokens, c->offs, static_cast<uint32_t *>(d_sdb),
-                                static_cast<uint16_t *>(d_stream_bp), J, c->hash_key, heldout,
-                                counter, c->n_sms, st));
-  }
-
-  // ---- 3. shuffled order and kept lengths of every position ---------------
   const uint32_t D0 = sdb[0];
   const uint64_t n_pos = (uint64_t)sdb[J] - D0;
   std::vector<uint64_t> N(J);
@@ -296,8 +282,23 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     void *d_bb;
     if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
-    NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, heldout, D0, order,
-                            klen, c->err, st));
+    NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
+                            order, klen, c->err, st));
+  }
+
+  // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
+  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
+  if (any_heldout) {
+    unsigned long long *frontier = a.temp<unsigned long long>(J);
+    unsigned long long *kept = a.temp<unsigned long long>(J);
+    NS_ALLOC(frontier);
+    NS_ALLOC(kept);
+    NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
+    NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
+    NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+                                  static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
+                                  c->cum + (size_t)K * J, T, c->hash_key, frontier, kept,
+                                  c->n_sms, st));
   }
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
 
@@ -308,7 +309,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(cutoff);
   NS_ALLOC(npieces);
   NS_ALLOC(node_base);
-  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
                            T, cutoff, npieces, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));

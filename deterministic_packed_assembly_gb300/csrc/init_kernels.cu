@@ -271,8 +271,7 @@ __global__ void row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, u
 // Held-out hash.  acc_d = sum_i splitmix64((i << 32) | u32 tok_i),
 // h_d = splitmix64(acc_d ^ splitmix64(hash_key + L_d)); held out iff
 // floor(h_d * 10000 / 2^64) < bp of the document's source.  One warp per
-// document, documents taken dynamically in groups; aligned 16-byte loads that
-// always hold at least one token of the document.
+// document; aligned 16-byte loads that always hold at least one token of it.
 __device__ __forceinline__ uint64_t hash_terms(int4 v, int64_t g, int64_t o0, int64_t o1) {
   uint64_t s = 0;
   const int32_t e[4] = {v.x, v.y, v.z, v.w};
@@ -294,57 +293,81 @@ __device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
          splitmix64(((uint64_t)(i0 + 3) << 32) | (uint32_t)v.w);
 }
 
+// The whole warp hashes tokens[o0, o1); every lane returns the document's h.
+__device__ __forceinline__ uint64_t warp_doc_hash(const int32_t *__restrict__ tokens, int64_t o0,
+                                                  int64_t o1, uint64_t hash_key, int lane) {
+  uint64_t acc = 0;
+  for (int64_t g = (o0 & ~(int64_t)3) + 4 * lane; g < o1; g += 256) {
+    const int4 v0 = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
+    const bool has1 = g + 128 < o1;
+    int4 v1 = make_int4(0, 0, 0, 0);
+    if (has1) v1 = __ldcs(reinterpret_cast<const int4 *>(tokens + g + 128));
+    if (g >= o0 && g + 3 < o1)
+      acc += hash_terms_inside(v0, (uint32_t)(g - o0));
+    else
+      acc += hash_terms(v0, g, o0, o1);
+    if (has1) {
+      if (g + 128 + 3 < o1)
+        acc += hash_terms_inside(v1, (uint32_t)(g + 128 - o0));
+      else
+        acc += hash_terms(v1, g + 128, o0, o1);
+    }
+  }
+  acc = warp_sum_u64(acc);
+  return splitmix64(acc ^ splitmix64(hash_key + (uint64_t)(o1 - o0)));
+}
+
+// Held-out flags for the prefix of every stream the horizon reaches.  A
+// stream's documents are taken in shuffled-position order, a few at a time
+// from the stream's frontier; a document found held out has its kept length
+// set to 0.  A warp leaves a stream once the kept tokens of the documents
+// already hashed exceed need_j = rmax_j * T (the windows the horizon asks of
+// it hold at most that many), or when the stream runs out, and goes on to the
+// next stream.  Every position below the final frontier is hashed, and the
+// kept tokens below it exceed need_j unless the whole stream was hashed, so
+// the prefix the cutoff kernel then takes only ever holds decided documents.
+// Warps start on different streams so that few overshoot any one stream.
 __global__ void __launch_bounds__(kThreads)
-    hash_docs_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
-                     const int64_t *__restrict__ offs,
-                     const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
-                     uint32_t J, uint64_t hash_key, uint8_t *__restrict__ heldout,
-                     unsigned long long *counter) {
-  constexpr uint32_t kGrab = 8;
+    hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
+                       const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
+                       uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
+                       uint32_t *__restrict__ klen, const int32_t *__restrict__ cum_last,
+                       uint32_t T, uint64_t hash_key, unsigned long long *frontier,
+                       unsigned long long *kept) {
+  constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
-  const uint32_t D0 = sdb[0], D1 = sdb[J];
-  const uint64_t n = D1 - D0;
-  uint32_t cur_lo = 1, cur_hi = 0, bp = 0;
-  while (true) {
-    unsigned long long base = 0;
-    if (lane == 0) base = atomicAdd(counter, (unsigned long long)kGrab);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (base >= n) break;
-    const uint32_t dend = D0 + (uint32_t)min((unsigned long long)n, base + kGrab);
-    for (uint32_t d = D0 + (uint32_t)base; d < dend; d++) {
-      if (d < cur_lo || d >= cur_hi) {
-        int64_t j = last_le<uint32_t, int64_t>(sdb, 0, (int64_t)J, d);
-        cur_lo = sdb[j];
-        cur_hi = sdb[j + 1];
-        bp = stream_bp[j];
+  const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  for (uint32_t jj = 0; jj < J; jj++) {
+    const uint32_t j = (warp_id + jj) % J;
+    const uint32_t bp = stream_bp[j];
+    if (bp == 0) continue;
+    const uint64_t N = sdb[j + 1] - sdb[j];
+    const uint64_t base_pos = (uint64_t)sdb[j] - D0;
+    const unsigned long long need = (unsigned long long)cum_last[j] * T;
+    while (true) {
+      unsigned long long base = 0;
+      if (lane == 0) {
+        const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
+        base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
       }
-      if (bp == 0) continue;
-      const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
-      // a malformed partition is reported by validate_offsets_kernel; never
-      // read outside the tokens because of it
-      if (o0 < 0 || o1 < o0 || (uint64_t)o1 > n_tokens || o1 - o0 > 0x7FFFFFFF) continue;
-      uint64_t acc = 0;
-      for (int64_t g = (o0 & ~(int64_t)3) + 4 * lane; g < o1; g += 256) {
-        const int4 v0 = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
-        const bool has1 = g + 128 < o1;
-        int4 v1 = make_int4(0, 0, 0, 0);
-        if (has1) v1 = __ldcs(reinterpret_cast<const int4 *>(tokens + g + 128));
-        if (g >= o0 && g + 3 < o1)
-          acc += hash_terms_inside(v0, (uint32_t)(g - o0));
-        else
-          acc += hash_terms(v0, g, o0, o1);
-        if (has1) {
-          if (g + 128 + 3 < o1)
-            acc += hash_terms_inside(v1, (uint32_t)(g + 128 - o0));
-          else
-            acc += hash_terms(v1, g + 128, o0, o1);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (base >= N) break;
+      const uint64_t pend = min((uint64_t)N, (uint64_t)base + kGrab);
+      unsigned long long kept_here = 0;
+      for (uint64_t p = base; p < pend; p++) {
+        const uint64_t idx = base_pos + p;
+        const uint32_t L = klen[idx];
+        if (L == 0) continue;
+        const uint32_t d = order[idx];
+        const int64_t o0 = __ldg(offs + d);
+        const uint64_t h = warp_doc_hash(tokens, o0, o0 + L, hash_key, lane);
+        if (__umul64hi(h, 10000ull) < (uint64_t)bp) {
+          if (lane == 0) klen[idx] = 0;
+        } else {
+          kept_here += L;
         }
       }
-      acc = warp_sum_u64(acc);
-      if (lane == 0) {
-        const uint64_t h = splitmix64(acc ^ splitmix64(hash_key + (uint64_t)(o1 - o0)));
-        heldout[d] = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1 : 0;
-      }
+      if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
     }
   }
 }
@@ -353,7 +376,9 @@ __global__ void __launch_bounds__(kThreads)
 // The shuffle: position p of stream j reads document b_j + pi_j(p), pi_j a
 // 4-round balanced Feistel network over 2*half bits (half = bits / 2, bits =
 // max(2, ceil(log2 N_j)) rounded up to even), walked until it lands in
-// [0, N_j).  Writes the document and its kept length (0 if empty or held out).
+// [0, N_j).  Writes the document and its length (0 if empty, or if its
+// offsets are malformed -- validate_offsets_kernel reports that); held-out
+// documents are zeroed afterwards by hash_prefix_kernel.
 __device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, uint64_t mask,
                                             uint64_t x) {
   uint64_t L = x >> half, R = x & mask;
@@ -369,9 +394,8 @@ __device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, 
 
 __global__ void __launch_bounds__(kThreads)
     order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
-                 const int64_t *__restrict__ offs, const uint8_t *__restrict__ heldout,
-                 uint32_t D0, uint32_t *__restrict__ order, uint32_t *__restrict__ klen,
-                 int *err) {
+                 const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
+                 uint32_t *__restrict__ order, uint32_t *__restrict__ klen, int *err) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint32_t b0 = sdb[j];
@@ -396,11 +420,11 @@ __global__ void __launch_bounds__(kThreads)
     y = feistel(k, half, mask, y);
   }
   const uint32_t d = b0 + (uint32_t)y;
-  const int64_t L = __ldg(offs + d + 1) - __ldg(offs + d);
-  const bool kept = L > 0 && !(heldout && heldout[d]);
+  const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
+  const bool ok = o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
   const uint64_t idx = (uint64_t)b0 + p - D0;
   order[idx] = d;
-  klen[idx] = kept ? (uint32_t)L : 0u;
+  klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -924,24 +948,23 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
   return cudaGetLastError();
 }
 
-cudaError_t launch_hash_docs(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
-                             const uint32_t *sdb,
-                             const uint16_t *stream_bp, uint32_t J, uint64_t hash_key,
-                             uint8_t *heldout, unsigned long long *counter, int n_sms,
-                             cudaStream_t st) {
+cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
+                               const uint16_t *stream_bp, uint32_t J, uint32_t D0,
+                               const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
+                               uint32_t T, uint64_t hash_key, unsigned long long *frontier,
+                               unsigned long long *kept, int n_sms, cudaStream_t st) {
   ++launch_counter();
-  hash_docs_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, n_tokens, offs, sdb, stream_bp, J,
-                                                   hash_key,
-                                                   heldout, counter);
+  hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
+                                                     klen, cum_last, T, hash_key, frontier, kept);
   return cudaGetLastError();
 }
 
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
-                         const int64_t *offs, const uint8_t *heldout, uint32_t D0,
-                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
+                         const int64_t *offs, uint64_t n_tokens, uint32_t D0, uint32_t *order,
+                         uint32_t *klen, int *err, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, heldout, D0, order, klen,
+  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, n_tokens, D0, order, klen,
                                                 err);
   return cudaGetLastError();
 }
