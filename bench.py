@@ -270,10 +270,16 @@ def run_ours(args, dist: Dist) -> None:
     out = dict(tokens=torch.empty(shape, dtype=torch.int32, device=device),
                pos=torch.empty(shape, dtype=torch.int32, device=device),
                doc=torch.empty(shape, dtype=torch.int32, device=device),
-               mask=torch.empty(shape, dtype=torch.uint8, device=device),
-               row_fp=torch.empty((L, n_rows), dtype=torch.int64, device=device),
-               row_learned=torch.empty((L, n_rows), dtype=torch.int32, device=device))
+               mask=torch.empty(shape, dtype=torch.uint8, device=device))
+    # row fingerprints and learned counts alternate between two buffers so
+    # that one launch's batch fold (on a second stream) overlaps the next
+    # launch's gather
+    row_fp = [torch.empty((L, n_rows), dtype=torch.int64, device=device) for _ in range(2)]
+    row_ln = [torch.empty((L, n_rows), dtype=torch.int32, device=device) for _ in range(2)]
     fp_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
+    fold_stream = torch.cuda.Stream(device)
+    gathered = [torch.cuda.Event() for _ in range(2)]
+    folded = [torch.cuda.Event() for _ in range(2)]
 
     state = {"launches": 0, "init_launches": 0, "valid": 0, "events": []}
 
@@ -286,26 +292,35 @@ def run_ours(args, dist: Dist) -> None:
         state["init_launches"] = pk.info["init_launches"]
         real = torch.zeros((), dtype=torch.int64, device=device) if count else None
         n = 0
-        for s0 in range(0, valid, L):
+        for li, s0 in enumerate(range(0, valid, L)):
             m = min(L, valid - s0)
+            b = li % 2
+            if li >= 2:
+                stream.wait_event(folded[b])
             view = {k: v[:m] for k, v in out.items()}
+            view["row_fp"] = row_fp[b][:m]
+            view["row_learned"] = row_ln[b][:m]
             if record:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-            # with every row of the batch, the kernel also folds each
-            # update's batch fingerprint
-            pk.step(s0, m, rows=rows, out=view, stream=stream,
-                    batch_fp=fp_all[s0:s0 + m] if dist.world == 1 else None)
+                ea = torch.cuda.Event(enable_timing=True)
+                eb = torch.cuda.Event(enable_timing=True)
+                ea.record(stream)
+            pk.step(s0, m, rows=rows, out=view, stream=stream)
+            n += 1
             if record:
-                b.record(stream)
-                state["events"].append((a, b))
+                eb.record(stream)
+                state["events"].append((ea, eb))
+            if dist.world == 1:
+                gathered[b].record(stream)
+                fold_stream.wait_event(gathered[b])
+                pk.batch_fp_many(view["row_fp"], out=fp_all[s0:s0 + m], stream=fold_stream)
+                folded[b].record(fold_stream)
+                n += 1
             if e2e is not None:
                 e2e[3][s0:s0 + m].copy_(view["row_fp"], non_blocking=True)
                 e2e[4][s0:s0 + m].copy_(view["row_learned"], non_blocking=True)
             if count:
                 real += (view["doc"] >= 0).sum()
-            n += 1
+        stream.wait_stream(fold_stream)
         if e2e is not None and dist.world == 1:
             e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
         pk.close()

@@ -63,7 +63,6 @@ class ns_pack_out(C.Structure):
         ("mask", C.c_void_p),
         ("row_fp", C.c_void_p),
         ("row_learned", C.c_void_p),
-        ("batch_fp", C.c_void_p),
     ]
 
 

@@ -41,7 +41,6 @@ struct ns_pack_ctx {
   int32_t *node_doc = nullptr, *node_mthr = nullptr;
   int *err = nullptr;
   uint64_t *fp_out = nullptr;
-  uint32_t *fold_count = nullptr;
   std::vector<void *> kept;
 };
 
@@ -221,10 +220,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->err);
   c->fp_out = a.keep<uint64_t>(1);
   NS_ALLOC(c->fp_out);
-  c->fold_count = a.keep<uint32_t>(K);
-  NS_ALLOC(c->fold_count);
   NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
-  NS_CK(cudaMemsetAsync(c->fold_count, 0, (size_t)K * sizeof(uint32_t), st));
 
   // ---- 1. quotas of every update, on a side stream ------------------------
   // They depend only on the weights, so they run while the corpus is hashed
@@ -235,6 +231,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->quota);
   NS_ALLOC(c->cum);
   NS_ALLOC(c->rb);
+  unsigned *ready = a.temp<unsigned>(1);
+  NS_ALLOC(ready);
+  NS_CK(cudaMemsetAsync(ready, 0, sizeof(unsigned), st));
   SideStream side;
   NS_CK(side.create());
   NS_CK(cudaEventRecord(side.fork, st));
@@ -242,7 +241,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   if (S <= 32 && max_strata <= 32) {
     NS_CK(nsk::launch_quota_warp(static_cast<uint32_t *>(d_sw), S, static_cast<uint32_t *>(d_tw),
                                  static_cast<uint32_t *>(d_src_first), J, c->B, K, max_strata,
-                                 c->quota, c->cum, side.s));
+                                 c->quota, c->cum, ready, side.s));
   } else {
     int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
     NS_ALLOC(src_quota);
@@ -250,7 +249,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                     side.s));
     NS_CK(nsk::launch_quota_strata(src_quota, static_cast<uint32_t *>(d_tw),
                                    static_cast<uint32_t *>(d_src_first), S, J, K, max_strata,
-                                   c->quota, c->cum, side.s));
+                                   c->quota, c->cum, ready, side.s));
   }
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
@@ -287,7 +286,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
 
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
-  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
+  // Runs beside the quota kernels: it reads each stream's need from their
+  // table once all S quota blocks have published it, and hashes on until then.
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *kept = a.temp<unsigned long long>(J);
@@ -297,9 +297,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
     NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
                                   static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
-                                  c->cum + (size_t)K * J, T, c->hash_key, frontier, kept,
-                                  c->n_sms, st));
+                                  c->cum + (size_t)K * J, ready, S, T, c->hash_key, frontier,
+                                  kept, c->n_sms, st));
   }
+  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
 
   // ---- 4. the prefix of each stream the horizon reaches -------------------
@@ -507,7 +508,6 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
                        reinterpret_cast<uintptr_t>(out->doc) | reinterpret_cast<uintptr_t>(out->mask);
   if (al % 16 != 0) return NS_ERR_INVALID_ARG;
   if ((uint64_t)n_steps * (row_end - row_begin) >= (1ull << 31)) return NS_ERR_INVALID_ARG;
-  if (out->batch_fp && (row_begin != 0 || row_end != ctx->B)) return NS_ERR_INVALID_ARG;
   if ((uint64_t)step0 + n_steps > ctx->K) return NS_ERR_HORIZON;
   if ((uint64_t)step0 + n_steps > ctx->valid_steps) return NS_ERR_EXHAUSTED;
   nsk::GatherParams p{};
@@ -531,8 +531,6 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   p.mask_out = out->mask;
   p.row_fp = out->row_fp;
   p.row_learned = out->row_learned;
-  p.batch_fp = out->batch_fp;
-  p.fold_count = ctx->fold_count;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_gather(p, st) != cudaSuccess) {
     cudaGetLastError();

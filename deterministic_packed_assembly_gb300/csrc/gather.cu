@@ -308,7 +308,6 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     s_learned[warp] = learned;
   }
   __syncthreads();
-  __shared__ int s_last;
   if (threadIdx.x == 0) {
     uint64_t a = 0;
     int l = 0;
@@ -319,35 +318,6 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     }
     p.row_fp[blk] = splitmix64(a);
     p.row_learned[blk] = l;
-    s_last = 0;
-    if (p.batch_fp) {
-      // the last row of this update to finish folds the update's rows
-      __threadfence();
-      s_last = atomicAdd(p.fold_count + k, 1u) == p.n_rows - 1;
-    }
-  }
-  __syncthreads();
-  if (!s_last) return;
-  // Batch fingerprint of update k: F = splitmix64(F ^ fp_i) over its rows in
-  // order.  The rows are staged in the (now idle) token ring and folded by one
-  // thread; the counter is reset for the next call.
-  cp_async_wait<0>();
-  __threadfence();
-  uint64_t *stage = reinterpret_cast<uint64_t *>(&s_tok[0][0][0]);
-  constexpr uint32_t kChunk = sizeof(s_tok) / sizeof(uint64_t);
-  const uint64_t *rows = p.row_fp + (size_t)step_local * p.n_rows;
-  uint64_t F = 0;
-  for (uint32_t c0 = 0; c0 < p.n_rows; c0 += kChunk) {
-    const uint32_t n = min(kChunk, p.n_rows - c0);
-    __syncthreads();
-    for (uint32_t t = threadIdx.x; t < n; t += blockDim.x) stage[t] = __ldcg(rows + c0 + t);
-    __syncthreads();
-    if (threadIdx.x == 0)
-      for (uint32_t t = 0; t < n; t++) F = splitmix64(F ^ stage[t]);
-  }
-  if (threadIdx.x == 0) {
-    p.batch_fp[step_local] = F;
-    p.fold_count[k] = 0;
   }
 }
 

@@ -86,6 +86,18 @@ __global__ void stream_keys_kernel(uint64_t seed, uint32_t J, uint64_t *keys) {
 }
 
 // ---------------------------------------------------------------------------
+// A block that has written its streams' last row of the quota table (the
+// windows each stream gives the whole horizon) counts itself done, so a
+// kernel running beside it can start using those rows once every block has.
+__device__ __forceinline__ void publish_ready(unsigned *ready) {
+  if (!ready) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ready, 1u);
+  }
+}
+
 // One update of the apportionment among this block's children (thread c owns
 // child c; inactive threads hold weight 0).  n units now, N counting every
 // update so far including this one; C is the child's count before.
@@ -141,7 +153,7 @@ __global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
                                     const uint32_t *__restrict__ tw,
                                     const uint32_t *__restrict__ src_first, uint32_t S,
                                     uint32_t J, uint32_t K, int32_t *__restrict__ quota,
-                                    int32_t *__restrict__ cum) {
+                                    int32_t *__restrict__ cum, unsigned *ready) {
   __shared__ __int128 delta[1024];
   __shared__ int64_t scratch[33];
   __shared__ uint64_t uscratch[33];
@@ -164,6 +176,7 @@ __global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
     Cs += n;
   }
   if (act) cum[(size_t)K * J + j] = (int32_t)C;
+  publish_ready(ready);
 }
 
 // Rank of this lane's value among lanes [0, count) by (value desc, lane asc);
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(32)
     quota_warp_kernel(const uint32_t *__restrict__ sw, uint32_t S,
                       const uint32_t *__restrict__ tw, const uint32_t *__restrict__ src_first,
                       uint32_t J, uint32_t B, uint32_t K, int32_t *__restrict__ quota,
-                      int32_t *__restrict__ cum) {
+                      int32_t *__restrict__ cum, unsigned *ready) {
   const int lane = threadIdx.x;
   const uint32_t s = blockIdx.x;
   // source level
@@ -250,6 +263,7 @@ __global__ void __launch_bounds__(32)
     D += gain - (__int128)Vs * (__int128)a2;
   }
   if (sact) cum[(size_t)K * J + f0 + lane] = (int32_t)C;
+  publish_ready(ready);
 }
 
 // rb[k][j]: the first row of stream j in update k (rows ordered by stream).
@@ -331,8 +345,9 @@ __global__ void __launch_bounds__(kThreads)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
-                       uint32_t *__restrict__ klen, const int32_t *__restrict__ cum_last,
-                       uint32_t T, uint64_t hash_key, unsigned long long *frontier,
+                       uint32_t *__restrict__ klen, const int32_t *cum_last,
+                       const unsigned *ready, unsigned ready_at, uint32_t T,
+                       uint64_t hash_key, unsigned long long *frontier,
                        unsigned long long *kept) {
   constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
@@ -343,10 +358,16 @@ __global__ void __launch_bounds__(kThreads)
     if (bp == 0) continue;
     const uint64_t N = sdb[j + 1] - sdb[j];
     const uint64_t base_pos = (uint64_t)sdb[j] - D0;
-    const unsigned long long need = (unsigned long long)cum_last[j] * T;
+    // need_j is known once the quota kernel (on another stream) has written
+    // the last row of its table; until then the stream is hashed on.
+    unsigned long long need = ~0ull;
     while (true) {
       unsigned long long base = 0;
       if (lane == 0) {
+        if (need == ~0ull && *reinterpret_cast<const volatile unsigned *>(ready) >= ready_at) {
+          __threadfence();
+          need = (unsigned long long)*reinterpret_cast<const volatile int32_t *>(cum_last + j) * T;
+        }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
         base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
       }
@@ -905,10 +926,10 @@ cudaError_t launch_quota_sources(const uint32_t *sw, uint32_t S, uint32_t B, uin
 cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
-                                cudaStream_t st) {
+                                unsigned *ready, cudaStream_t st) {
   ++launch_counter();
   quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(src_quota, tw, src_first, S, J, K,
-                                                             quota, cum);
+                                                             quota, cum, ready);
   return cudaGetLastError();
 }
 
@@ -916,28 +937,35 @@ template <int SMAX>
 static void launch_quota_warp_s(const uint32_t *sw, uint32_t S, const uint32_t *tw,
                                 const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
-                                cudaStream_t st) {
+                                unsigned *ready, cudaStream_t st) {
   if (max_strata <= 4)
-    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
+                                                 ready);
   else if (max_strata <= 8)
-    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
+                                                 ready);
   else
-    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum);
+    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
+                                                  ready);
 }
 
 cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
                               const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
                               uint32_t max_strata, int32_t *quota, int32_t *cum,
-                              cudaStream_t st) {
+                              unsigned *ready, cudaStream_t st) {
   ++launch_counter();
   if (S <= 4)
-    launch_quota_warp_s<4>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+    launch_quota_warp_s<4>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
+                            st);
   else if (S <= 8)
-    launch_quota_warp_s<8>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+    launch_quota_warp_s<8>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
+                            st);
   else if (S <= 16)
-    launch_quota_warp_s<16>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+    launch_quota_warp_s<16>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
+                            st);
   else
-    launch_quota_warp_s<32>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, st);
+    launch_quota_warp_s<32>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
+                            st);
   return cudaGetLastError();
 }
 
@@ -951,11 +979,13 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               uint32_t T, uint64_t hash_key, unsigned long long *frontier,
+                               const unsigned *ready, unsigned ready_at, uint32_t T,
+                               uint64_t hash_key, unsigned long long *frontier,
                                unsigned long long *kept, int n_sms, cudaStream_t st) {
   ++launch_counter();
   hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
-                                                     klen, cum_last, T, hash_key, frontier, kept);
+                                                     klen, cum_last, ready, ready_at, T, hash_key,
+                                                     frontier, kept);
   return cudaGetLastError();
 }
 

@@ -26,15 +26,17 @@ cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64
 cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st);
 cudaError_t launch_quota_sources(const uint32_t *source_weight, uint32_t S, uint32_t B,
                                  uint32_t K, int32_t *src_quota, cudaStream_t st);
+// Every quota block adds 1 to *ready (if not null) once its streams' last
+// table row is written.
 cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *stream_weight,
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
-                                cudaStream_t st);
+                                unsigned *ready, cudaStream_t st);
 // Both levels in one kernel when n_sources <= 32 and every source has <= 32 strata.
 cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
                               const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
                               uint32_t max_strata, int32_t *quota, int32_t *cum,
-                              cudaStream_t st);
+                              unsigned *ready, cudaStream_t st);
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st);
 
@@ -46,7 +48,8 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               uint32_t T, uint64_t hash_key, unsigned long long *frontier,
+                               const unsigned *ready, unsigned ready_at, uint32_t T,
+                               uint64_t hash_key, unsigned long long *frontier,
                                unsigned long long *kept, int n_sms, cudaStream_t st);
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
@@ -125,8 +128,6 @@ struct GatherParams {
   uint8_t *mask_out;
   uint64_t *row_fp;
   int32_t *row_learned;
-  uint64_t *batch_fp;     // [n_steps] or null; only with every row of the batch
-  uint32_t *fold_count;   // [K] rows finished per update (zero between calls)
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,

@@ -117,12 +117,14 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
   }
   cudaError_t e;
   if (one_warp) {
-    e = nsk::launch_quota_warp(d_sw, S, d_tw, d_sf, J, B, K, max_strata, quota_dev, cum_dev, st);
+    e = nsk::launch_quota_warp(d_sw, S, d_tw, d_sf, J, B, K, max_strata, quota_dev, cum_dev,
+                               nullptr, st);
   } else {
     int32_t *d_sq = reinterpret_cast<int32_t *>(scratch + o_sq);
     e = nsk::launch_quota_sources(d_sw, S, B, K, d_sq, st);
     if (e == cudaSuccess)
-      e = nsk::launch_quota_strata(d_sq, d_tw, d_sf, S, J, K, max_strata, quota_dev, cum_dev, st);
+      e = nsk::launch_quota_strata(d_sq, d_tw, d_sf, S, J, K, max_strata, quota_dev, cum_dev,
+                                   nullptr, st);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

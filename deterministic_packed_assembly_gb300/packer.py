@@ -134,22 +134,15 @@ class Packer:
         o.mask = out["mask"].data_ptr()
         o.row_fp = out["row_fp"].data_ptr()
         o.row_learned = out["row_learned"].data_ptr()
-        bf = out.get("batch_fp")
-        o.batch_fp = None if bf is None else bf.data_ptr()
         return o
 
     def step(self, step0: int, n_steps: int = 1, rows: Optional[tuple] = None,
-             out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None,
-             batch_fp: Optional[torch.Tensor] = None) -> dict:
+             out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
         """Assemble rows ``rows = (begin, end)`` of updates [step0, step0 +
-        n_steps) into ``out`` (allocated if None); asynchronous.  With every row
-        of the batch, ``batch_fp`` (int64 [n_steps]) also receives each
-        update's batch fingerprint, folded inside the same launch."""
+        n_steps) into ``out`` (allocated if None); asynchronous."""
         r0, r1 = (0, self.B) if rows is None else rows
         if out is None:
             out = self.empty_out(n_steps, r1 - r0)
-        if batch_fp is not None:
-            out = dict(out, batch_fp=batch_fp)
         st = (stream or self.stream).cuda_stream
         L.ns_pack_step(self._ctx, step0, n_steps, r0, r1, self._out_struct(out), st)
         return out

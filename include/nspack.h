@@ -123,12 +123,6 @@ typedef struct {
   uint8_t *mask;
   uint64_t *row_fp;     /* [n_steps][rows] */
   int32_t *row_learned; /* [n_steps][rows] */
-  uint64_t *batch_fp;   /* [n_steps] or NULL: the batch fingerprint of every
-                           update, folded by the kernel itself; only when the
-                           call covers every row (row_begin 0, row_end B).  It
-                           counts finished rows per update in the context, so
-                           two calls that fold the same update must not overlap
-                           on the GPU. */
 } ns_pack_out;
 
 typedef struct {
@@ -158,8 +152,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out);
  * kernel launch.  The bytes of every row are the same whatever the row range
  * or the step batching.  Errors: INVALID_ARG (n_steps == 0, empty or out-of-
  * range rows, NULL or misaligned outputs), HORIZON (step0 + n_steps >
- * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA; batch_fp with a
- * partial row range is INVALID_ARG. */
+ * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA. */
 int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,
                  uint32_t row_end, const ns_pack_out *out, void *cuda_stream);
 

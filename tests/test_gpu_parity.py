@@ -226,21 +226,3 @@ def test_quota_tables_beyond_one_warp(S, strata):
     pk, o = packer_for(c), oracle_for(c)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=3)
-
-
-@pytest.mark.parametrize("name", ["c1", "c3s", "c5s"])
-def test_batch_fingerprint_folded_in_the_gather(name):
-    c = make_preset(name)
-    pk, o = packer_for(c), oracle_for(c)
-    v = o.valid_steps
-    bf = torch.full((v,), -1, dtype=torch.int64, device="cuda:0")
-    for rep in range(2):  # the per-update counters must reset between calls
-        for s0 in range(0, v, 3):
-            n = min(3, v - s0)
-            pk.step(s0, n_steps=n, batch_fp=bf[s0:s0 + n])
-        got = bf.cpu().numpy().view(np.uint64)
-        for k in range(v):
-            assert got[k] == oracle.batch_fp(o.rows(k)["row_fp"]), (rep, k)
-    with pytest.raises(Exception) as e:
-        pk.step(0, rows=(0, c.B - 1), batch_fp=bf[:1])
-    assert e.value.code == -1
