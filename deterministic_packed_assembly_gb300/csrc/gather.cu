@@ -1,8 +1,8 @@
 // Per-update assembly: one CTA per (update, row).  The row's window comes
-// from the row table built at init; the window's pieces are staged in shared
-// memory and copied in order into T positions of tokens / position ids /
-// document ids / loss mask, the rest padded; the row's fingerprint and
-// learned-position count are reduced in the same pass.
+// from the row table built at init; its pieces are copied in order into T
+// positions of tokens / position ids / document ids / loss mask, the rest
+// padded; the row's fingerprint and learned-position count are reduced in the
+// same pass.
 //
 // Rows of exactly T positions, padded (Linnet training docs, Supervised
 // fine-tuning); a position id of 0 starts each sequence within a row (Other
@@ -11,15 +11,19 @@
 // the rows gives the same bytes ("Zephon: deterministic data loading",
 // checkpoint on 16 GPUs, resume on 8/32/64).
 //
-// Layout of the work: 8 warps per CTA; a warp owns tiles of 128 consecutive
-// positions (4 per lane, so every store is a 16-byte vector and a warp
-// writes 512 contiguous bytes per array) and handles two tiles per round,
-// issuing both tiles' token loads before computing either.  A tile inside one
-// piece reads its tokens with one aligned 16-byte load per lane, realigned
-// across lanes with shuffles; a tile that crosses piece ends reads them one by
-// one.
+// Layout of the work: 8 warps per CTA, each on its own; a warp owns tiles of
+// 128 consecutive positions (4 per lane, so every store is a 16-byte vector
+// and a warp writes 512 contiguous bytes per array).  A window of up to 32
+// pieces is held in the warp's registers, piece l in lane l, and looked up
+// with a ballot; longer windows are read from the piece table.  Tokens of a
+// tile inside one piece are copied by cp.async into a four-tile ring in
+// shared memory (aligned 16-byte blocks, realigned across lanes with
+// shuffles); a tile that crosses piece ends reads its tokens one by one.
+// Warps combine the row's fingerprint through shared-memory atomics and the
+// last one to finish writes it, so no warp waits for another.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "common.cuh"
@@ -30,10 +34,11 @@ namespace nsk {
 namespace {
 
 constexpr int kGatherWarps = 8;
-constexpr int kTile = 128;       // positions per warp per tile: 32 lanes x 4
-constexpr int kPieceCap = 512;   // pieces of a window staged in shared memory
+constexpr int kTile = 128;         // positions per warp per tile: 32 lanes x 4
+constexpr int kStages = 4;         // tiles in flight per warp
+constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
 
-// Fingerprint terms of position t: key_t = a_t ^ ((b_t | t << 40) * golden),
+// Fingerprint term of position t: key_t = a_t ^ ((b_t | t << 40) * golden),
 // a_t = (u32 tok << 32) | u32 doc, b_t = (mask << 32) | u32 pos.
 __device__ __forceinline__ uint64_t fp_term(int32_t tok, int32_t pos, int32_t doc, uint32_t m,
                                             uint32_t t) {
@@ -51,37 +56,6 @@ __device__ __forceinline__ int4 shfl_down4(const int4 &v) {
   return r;
 }
 
-// The window's pieces, either staged in shared memory or read from the
-// context's tables.  dst(q) is the first row position of piece q (relative to
-// the window), dst(np) the window's used length.
-struct Pieces {
-  const int64_t *S;     // staged: S - S[ws] prefix; global: node_S + ws (absolute)
-  const int64_t *src;   // first token index of each piece
-  const int32_t *doc;
-  const int32_t *mthr;
-  int64_t sbase;        // subtracted from S to make it window-relative
-  int32_t np;
-  __device__ __forceinline__ int64_t dst(int32_t q) const { return S[q] - sbase; }
-  // last piece q in [lo, np) with dst(q) <= t (dst(lo) <= t); pieces of one
-  // warp's tiles only move forward, so a few linear probes usually suffice
-  __device__ __forceinline__ int32_t find(int32_t lo, int64_t t) const {
-#pragma unroll
-    for (int probe = 0; probe < 3; probe++) {
-      if (lo + 1 >= np || S[lo + 1] - sbase > t) return lo;
-      lo++;
-    }
-    int32_t l = lo, h = np;
-    while (l < h) {
-      const int32_t m = l + (h - l) / 2;
-      if (S[m] - sbase <= t)
-        l = m + 1;
-      else
-        h = m;
-    }
-    return l - 1;
-  }
-};
-
 // cp.async: 16 bytes global -> shared, asynchronous, tracked in groups.
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -95,35 +69,100 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-constexpr int kStages = 4;         // tiles in flight per warp
-constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
+// A piece of the window: its first row position (relative to the window), the
+// token index of its first token, its document and loss threshold.
+struct Piece {
+  int32_t start, end;
+  int64_t src;
+  int32_t doc, mthr;
+};
 
-// What a tile needs between its copy and its stores (kept in shared memory).
+// Window of at most 32 pieces held in the warp's registers: lane l holds
+// piece l.  Every method is called by all 32 lanes together.
+struct WarpPieces {
+  int32_t S;     // start of this lane's piece, INT_MAX past the last piece
+  int64_t src;
+  int32_t doc, mthr;
+  int32_t np, used;
+  // last piece whose start is <= t, for a t the whole warp shares
+  __device__ __forceinline__ int32_t find_uniform(int32_t t) const {
+    return __popc(__ballot_sync(0xffffffffu, S <= t)) - 1;
+  }
+  // last piece whose start is <= t, for a t of this lane's own
+  __device__ __forceinline__ int32_t find_lane(int32_t t) const {
+    int32_t pos = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+      const int32_t v = __shfl_sync(0xffffffffu, S, min(pos + step, 31));
+      if (pos + step < 32 && v <= t) pos += step;
+    }
+    return pos;
+  }
+  __device__ __forceinline__ Piece get(int32_t q) const {
+    Piece p;
+    p.start = __shfl_sync(0xffffffffu, S, q);
+    const int32_t nxt = __shfl_sync(0xffffffffu, S, min(q + 1, 31));
+    p.end = (q + 1 < np) ? nxt : used;
+    p.src = __shfl_sync(0xffffffffu, src, q);
+    p.doc = __shfl_sync(0xffffffffu, doc, q);
+    p.mthr = __shfl_sync(0xffffffffu, mthr, q);
+    return p;
+  }
+};
+
+// Window of any length read from the context's piece table (L1-cached).
+struct TablePieces {
+  const int64_t *S;  // node_S + ws (absolute prefix; sbase subtracted)
+  const int64_t *srcs;
+  const int32_t *docs, *mthrs;
+  int64_t sbase;
+  int32_t np, used;
+  __device__ __forceinline__ int32_t find(int32_t lo, int32_t t) const {
+    int32_t l = lo, h = np;
+    while (l < h) {
+      const int32_t m = l + (h - l) / 2;
+      if (__ldg(S + m) - sbase <= t)
+        l = m + 1;
+      else
+        h = m;
+    }
+    return l - 1;
+  }
+  __device__ __forceinline__ int32_t find_uniform(int32_t t) const { return find(0, t); }
+  __device__ __forceinline__ int32_t find_lane(int32_t t) const { return find(0, t); }
+  __device__ __forceinline__ Piece get(int32_t q) const {
+    Piece p;
+    p.start = (int32_t)(__ldg(S + q) - sbase);
+    p.end = (int32_t)(__ldg(S + q + 1) - sbase);
+    p.src = __ldg(srcs + q);
+    p.doc = __ldg(docs + q);
+    p.mthr = __ldg(mthrs + q);
+    return p;
+  }
+};
+
+// What a tile needs between its copy and its stores.
 struct TileMeta {
-  int32_t kind;  // 0 pad, 1 inside piece q (staged), 2 crosses piece ends
-  int32_t q;     // piece of the tile's first position
-  int32_t x0;    // offset of the tile's first position inside piece q
+  int32_t kind;  // 0 pad, 1 inside one piece (copied), 2 crosses piece ends
+  int32_t x0;    // offset of the tile's first position inside its piece (kind 1)
   int32_t sh;    // source misalignment in tokens (kind 1)
+  int32_t doc, mthr;
 };
 
 // Classify tile t0 and, for a tile inside one piece, start copying its tokens
 // (rounded out to 16-byte blocks that each hold at least one of them).
-__device__ __forceinline__ void tile_issue(const GatherParams &p, const Pieces &P, int32_t used,
-                                           uint32_t t0, int32_t q_hint, int lane, int32_t *buf,
-                                           TileMeta *meta) {
-  TileMeta m;
-  m.kind = 0;
-  m.q = q_hint;
-  m.x0 = 0;
-  m.sh = 0;
-  if ((int32_t)t0 < used) {
-    m.q = P.find(q_hint, (int64_t)t0);
-    const int64_t qs = P.dst(m.q);
-    const int64_t qe = P.dst(m.q + 1);
-    m.x0 = (int32_t)((int64_t)t0 - qs);
-    if (qe >= (int64_t)t0 + kTile) {
+template <class PV>
+__device__ __forceinline__ TileMeta tile_issue(const GatherParams &p, const PV &P, uint32_t t0,
+                                               int lane, int32_t *buf) {
+  TileMeta m{0, 0, 0, -1, 0};
+  if ((int32_t)t0 < P.used) {
+    const Piece pc = P.get(P.find_uniform((int32_t)t0));
+    if (pc.end >= (int32_t)t0 + kTile) {
       m.kind = 1;
-      const int64_t srcw = P.src[m.q] + m.x0;
+      m.x0 = (int32_t)t0 - pc.start;
+      m.doc = pc.doc;
+      m.mthr = pc.mthr;
+      const int64_t srcw = pc.src + m.x0;
       m.sh = (int32_t)(srcw & 3);
       const int32_t *g = p.tokens + (srcw - m.sh);
       cp_async16(buf + 4 * lane, g + 4 * lane);
@@ -132,12 +171,14 @@ __device__ __forceinline__ void tile_issue(const GatherParams &p, const Pieces &
       m.kind = 2;
     }
   }
-  if (lane == 0) *meta = m;
+  return m;
 }
 
-__device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &P, int32_t used,
-                                           uint32_t t0, int lane, size_t obase, const int32_t *buf,
-                                           const TileMeta &m, uint64_t &acc, int &learned) {
+template <class PV>
+__device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, uint32_t t0,
+                                           int lane, size_t obase, const int32_t *buf,
+                                           const TileMeta &mref, uint64_t &acc, int &learned) {
+  const TileMeta m = mref;
   const uint32_t tp = t0 + 4u * lane;
   int4 tk, ps, dc;
   uint32_t mk = 0;
@@ -161,40 +202,32 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &
     }
     const int32_t x = m.x0 + 4 * lane;
     ps = make_int4(x, x + 1, x + 2, x + 3);
-    const int32_t d = P.doc[m.q];
-    dc = make_int4(d, d, d, d);
-    const int32_t th = P.mthr[m.q];
+    dc = make_int4(m.doc, m.doc, m.doc, m.doc);
+    const int32_t th = m.mthr;
     mk = (x >= th ? 1u : 0u) | (x + 1 >= th ? 1u << 8 : 0u) | (x + 2 >= th ? 1u << 16 : 0u) |
          (x + 3 >= th ? 1u << 24 : 0u);
   } else {
-    if (tp >= p.T) return;
+    // every lane looks its four positions up together (the lookups shuffle);
+    // positions past the window's end become padding afterwards
     int32_t e0[4], e1[4], e2[4];
-    int32_t qq = -1;
-    int64_t qqe = 0, qqs = 0;
+    const int32_t last = P.used - 1;
+    int32_t t = min((int32_t)tp, last);
+    Piece pc = P.get(P.find_lane(t));
 #pragma unroll
     for (int e = 0; e < 4; e++) {
-      const int32_t t = (int32_t)tp + e;
-      if (t >= used) {
-        e0[e] = p.pad_id;
-        e1[e] = 0;
-        e2[e] = -1;
-        continue;
+      t = min((int32_t)tp + e, last);
+      const bool same = t < pc.end;
+      if (!__all_sync(0xffffffffu, same)) {
+        const int32_t q = P.find_lane(t);
+        const Piece nq = P.get(q);
+        if (!same) pc = nq;
       }
-      if (qq < 0) {
-        qq = P.find(m.q, (int64_t)t);
-        qqs = P.dst(qq);
-        qqe = P.dst(qq + 1);
-      }
-      while ((int64_t)t >= qqe) {
-        qq++;
-        qqs = qqe;
-        qqe = P.dst(qq + 1);
-      }
-      const int32_t x = t - (int32_t)qqs;
-      e0[e] = __ldg(p.tokens + P.src[qq] + x);
-      e1[e] = x;
-      e2[e] = P.doc[qq];
-      if (x >= P.mthr[qq]) mk |= 1u << (8 * e);
+      const int32_t x = t - pc.start;
+      const bool real = (int32_t)tp + e <= last && tp < p.T;
+      e0[e] = real ? __ldg(p.tokens + pc.src + x) : p.pad_id;
+      e1[e] = real ? x : 0;
+      e2[e] = real ? pc.doc : -1;
+      if (real && x >= pc.mthr) mk |= 1u << (8 * e);
     }
     tk = make_int4(e0[0], e0[1], e0[2], e0[3]);
     ps = make_int4(e1[0], e1[1], e1[2], e1[3]);
@@ -212,16 +245,48 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const Pieces &
   learned += __popc(mk);
 }
 
+// This warp's tiles: t0 = warp * 128 + m * 1024, through a ring of kStages
+// shared-memory buffers filled by cp.async; each tile's description waits in
+// shared memory beside its buffer (written by lane 0, read after __syncwarp).
+template <class PV>
+__device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, int warp, int lane,
+                                           size_t obase, int32_t (*ring)[kStageWords],
+                                           TileMeta *meta, uint64_t &acc, int &learned) {
+  constexpr uint32_t kStride = kGatherWarps * kTile;
+  const uint32_t first = (uint32_t)warp * kTile;
+  const int n_tiles = first < p.T ? (int)((p.T - first + kStride - 1) / kStride) : 0;
+#pragma unroll
+  for (int m = 0; m < kStages - 1; m++) {
+    if (m < n_tiles) {
+      const TileMeta t = tile_issue(p, P, first + m * kStride, lane, ring[m]);
+      if (lane == 0) meta[m] = t;
+    }
+    cp_async_commit();
+  }
+#pragma unroll 1
+  for (int mm = 0; mm < n_tiles; mm++) {
+    const int mi = mm + kStages - 1;
+    const int slot_i = mi % kStages;
+    if (mi < n_tiles) {
+      const TileMeta t = tile_issue(p, P, first + mi * kStride, lane, ring[slot_i]);
+      if (lane == 0) meta[slot_i] = t;
+    }
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int slot = mm % kStages;
+    tile_store(p, P, first + mm * kStride, lane, obase, ring[slot], meta[slot], acc, learned);
+    __syncwarp();
+  }
+}
+
 __global__ void __launch_bounds__(kGatherWarps * 32)
     gather_kernel(const GatherParams p) {
-  __shared__ int64_t s_S[kPieceCap + 1];
-  __shared__ int64_t s_src[kPieceCap];
-  __shared__ int32_t s_doc[kPieceCap];
-  __shared__ int32_t s_mthr[kPieceCap];
   __shared__ __align__(16) int32_t s_tok[kGatherWarps][kStages][kStageWords];
   __shared__ TileMeta s_meta[kGatherWarps][kStages];
-  __shared__ uint64_t s_fp[kGatherWarps];
-  __shared__ int s_learned[kGatherWarps];
+  __shared__ unsigned long long s_acc;
+  __shared__ int s_learned;
+  __shared__ int s_done;
 
   const uint32_t blk = blockIdx.x;
   const uint32_t step_local = blk / p.n_rows;
@@ -229,95 +294,69 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   const uint32_t k = p.step0 + step_local;
   const uint32_t i = p.row0 + row_local;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    s_acc = 0;
+    s_learned = 0;
+    s_done = 0;
+  }
+  __syncthreads();
 
   // the row's window: pieces [ws, we) of the context's piece table
   const int2 win = p.row_win[(size_t)k * p.B + i];
   int64_t ws = win.x, we = win.y;
   if (ws < 0 || we < ws) ws = we = 0;  // a row past the end of its stream: all padding
   const int32_t np = (int32_t)(we - ws);
-  Pieces P;
-  P.np = np;
-  const bool staged = np <= kPieceCap;
-  if (staged) {
-    for (int32_t t = threadIdx.x; t <= np; t += blockDim.x) {
-      s_S[t] = __ldg(p.node_S + ws + t);
-      if (t < np) {
-        s_src[t] = __ldg(p.node_src + ws + t);
-        s_doc[t] = __ldg(p.node_doc + ws + t);
-        s_mthr[t] = __ldg(p.node_mthr + ws + t);
-      }
-    }
-    __syncthreads();
-    P.S = s_S;
-    P.src = s_src;
-    P.doc = s_doc;
-    P.mthr = s_mthr;
-  } else {
-    P.S = p.node_S + ws;
-    P.src = p.node_src + ws;
-    P.doc = p.node_doc + ws;
-    P.mthr = p.node_mthr + ws;
-  }
-  P.sbase = P.S[0];
-  const int64_t used64 = P.S[np] - P.sbase;
+  const int64_t sbase = __ldg(p.node_S + ws);
+  const int64_t used64 = __ldg(p.node_S + we) - sbase;
   int32_t used = (int32_t)used64;
   if (used64 < 0 || used64 > (int64_t)p.T) {
     set_error(p.err, kDevBadNode);
     used = 0;
   }
 
-  // this warp's tiles: t0 = warp * 128 + m * 1024, m < n_tiles, through a
-  // ring of kStages shared-memory buffers filled by cp.async
-  constexpr uint32_t kStride = kGatherWarps * kTile;
-  const uint32_t first = (uint32_t)warp * kTile;
-  const int n_tiles = first < p.T ? (int)((p.T - first + kStride - 1) / kStride) : 0;
-  int32_t(*ring)[kStageWords] = s_tok[warp];
-  TileMeta *meta = s_meta[warp];
-  int32_t q_hint = 0;
-#pragma unroll
-  for (int m = 0; m < kStages - 1; m++) {
-    if (m < n_tiles) {
-      tile_issue(p, P, used, first + m * kStride, q_hint, lane, ring[m], &meta[m]);
-      __syncwarp();
-      q_hint = meta[m].q;
-    }
-    cp_async_commit();
-  }
   const size_t obase = (size_t)blk * p.T;
   uint64_t acc = 0;
   int learned = 0;
-  for (int m = 0; m < n_tiles; m++) {
-    const int mi = m + kStages - 1;
-    if (mi < n_tiles) {
-      tile_issue(p, P, used, first + mi * kStride, q_hint, lane, ring[mi % kStages],
-                 &meta[mi % kStages]);
+  if (np <= 32) {
+    WarpPieces P;
+    P.np = np;
+    P.used = used;
+    P.S = INT_MAX;
+    P.src = 0;
+    P.doc = -1;
+    P.mthr = 0;
+    if (lane < np) {
+      P.S = (int32_t)(__ldg(p.node_S + ws + lane) - sbase);
+      P.src = __ldg(p.node_src + ws + lane);
+      P.doc = __ldg(p.node_doc + ws + lane);
+      P.mthr = __ldg(p.node_mthr + ws + lane);
     }
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    if (mi < n_tiles) q_hint = meta[mi % kStages].q;
-    const TileMeta mt = meta[m % kStages];
-    tile_store(p, P, used, first + m * kStride, lane, obase, ring[m % kStages], mt, acc, learned);
-    __syncwarp();
+    warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
+  } else {
+    TablePieces P;
+    P.S = p.node_S + ws;
+    P.srcs = p.node_src + ws;
+    P.docs = p.node_doc + ws;
+    P.mthrs = p.node_mthr + ws;
+    P.sbase = sbase;
+    P.np = np;
+    P.used = used;
+    warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
   }
 
+  // combine the warps' sums; the last warp to arrive writes the row's values
   acc = warp_sum_u64(acc);
   learned = warp_sum_i32(learned);
   if (lane == 0) {
-    s_fp[warp] = acc;
-    s_learned[warp] = learned;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint64_t a = 0;
-    int l = 0;
-#pragma unroll
-    for (int w = 0; w < kGatherWarps; w++) {
-      a += s_fp[w];
-      l += s_learned[w];
+    atomicAdd(&s_acc, (unsigned long long)acc);
+    atomicAdd(&s_learned, learned);
+    __threadfence_block();
+    if (atomicAdd(&s_done, 1) == kGatherWarps - 1) {
+      __threadfence_block();
+      const uint64_t a = *reinterpret_cast<volatile unsigned long long *>(&s_acc);
+      p.row_fp[blk] = splitmix64(a);
+      p.row_learned[blk] = *reinterpret_cast<volatile int *>(&s_learned);
     }
-    p.row_fp[blk] = splitmix64(a);
-    p.row_learned[blk] = l;
   }
 }
 
