@@ -341,7 +341,7 @@ __device__ __forceinline__ uint64_t warp_doc_hash(const int32_t *__restrict__ to
 // kept tokens below it exceed need_j unless the whole stream was hashed, so
 // the prefix the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads)
                        const unsigned *ready, unsigned ready_at, uint32_t T,
                        uint64_t hash_key, unsigned long long *frontier,
                        unsigned long long *kept) {
-  constexpr uint32_t kGrab = 4;
+  constexpr uint32_t kGrab = 8;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   for (uint32_t jj = 0; jj < J; jj++) {
@@ -374,16 +374,23 @@ __global__ void __launch_bounds__(kThreads)
       base = __shfl_sync(0xffffffffu, base, 0);
       if (base >= N) break;
       const uint64_t pend = min((uint64_t)N, (uint64_t)base + kGrab);
+      // lanes 0..kGrab-1 fetch the grabbed positions' lengths, documents and
+      // first-token offsets together, then the warp hashes them one by one
+      uint32_t L_l = 0;
+      int64_t o_l = 0;
+      if (lane < (int)(pend - base)) {
+        const uint64_t idx = base_pos + base + lane;
+        L_l = klen[idx];
+        if (L_l) o_l = __ldg(offs + order[idx]);
+      }
       unsigned long long kept_here = 0;
-      for (uint64_t p = base; p < pend; p++) {
-        const uint64_t idx = base_pos + p;
-        const uint32_t L = klen[idx];
+      for (int q = 0; q < (int)(pend - base); q++) {
+        const uint32_t L = __shfl_sync(0xffffffffu, L_l, q);
         if (L == 0) continue;
-        const uint32_t d = order[idx];
-        const int64_t o0 = __ldg(offs + d);
+        const int64_t o0 = __shfl_sync(0xffffffffu, o_l, q);
         const uint64_t h = warp_doc_hash(tokens, o0, o0 + L, hash_key, lane);
         if (__umul64hi(h, 10000ull) < (uint64_t)bp) {
-          if (lane == 0) klen[idx] = 0;
+          if (lane == 0) klen[base_pos + base + q] = 0;
         } else {
           kept_here += L;
         }
@@ -391,6 +398,96 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
     }
   }
+}
+
+// The same held-out decision for every document of the streams that hold out
+// any, in document order: a warp takes 32 consecutive documents and sweeps
+// their tokens as one flat run (lane l reads the 16-byte blocks l, l + 32,
+// ... of the run), so no lane idles on a short document.  Each lane follows
+// the document its block lies in with a cursor that only moves forward and
+// adds its partial sums into the warp's per-document slots in shared memory;
+// then lane l finishes document l.  Used when the horizon reaches most of the
+// corpus; the flags go to heldout[d].
+__global__ void __launch_bounds__(kThreads)
+    hash_flat_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
+                     const int64_t *__restrict__ offs, const uint32_t *__restrict__ sdb,
+                     const uint16_t *__restrict__ stream_bp, uint32_t J, uint64_t hash_key,
+                     uint8_t *__restrict__ heldout, unsigned long long *counter) {
+  constexpr int kWarps = kThreads / 32;
+  __shared__ unsigned long long s_acc[kWarps][32];
+  __shared__ int64_t s_off[kWarps][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t D0 = sdb[0], D1 = sdb[J];
+  while (true) {
+    unsigned long long base = 0;
+    if (lane == 0) base = atomicAdd(counter, 32ull);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= (unsigned long long)(D1 - D0)) break;
+    const uint32_t d0 = D0 + (uint32_t)base;
+    const int nd = (int)min(32ull, (unsigned long long)(D1 - D0) - base);
+    // this lane's document: its rate, its offsets
+    uint32_t bp = 0;
+    if (lane < nd) {
+      const int64_t j = last_le<uint32_t, int64_t>(sdb, 0, (int64_t)J, d0 + lane);
+      bp = stream_bp[j];
+    }
+    int64_t o = 0;
+    if (lane < nd) o = __ldg(offs + d0 + lane);
+    const int64_t o_end = __ldg(offs + d0 + nd);
+    const int64_t o_next = __shfl_down_sync(0xffffffffu, o, 1);
+    const int64_t o_hi = (lane + 1 < nd) ? o_next : o_end;
+    // offsets checked here too: a malformed partition is never read past
+    const bool bad = lane < nd && (o < 0 || o_hi < o || o_hi - o > 0x7FFFFFFF ||
+                                   (uint64_t)o_end > n_tokens);
+    if (__any_sync(0xffffffffu, bad) || !__any_sync(0xffffffffu, bp != 0)) continue;
+    const int64_t first = __shfl_sync(0xffffffffu, o, 0);
+    s_off[w][lane] = o;
+    if (lane == 0) s_off[w][nd] = o_end;
+    s_acc[w][lane] = 0;
+    __syncwarp();
+    int q = 0;           // document of this lane's current block
+    int64_t qe = s_off[w][1];
+    uint64_t acc = 0;
+    for (int64_t g = (first & ~(int64_t)3) + 4 * lane; g < o_end; g += 128) {
+      const int4 v = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
+      if (g >= first && g + 3 < qe) {
+        // the whole block lies in document q (the common case)
+        acc += hash_terms_inside(v, (uint32_t)(g - s_off[w][q]));
+        continue;
+      }
+      const int32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const int64_t idx = g + c;
+        if (idx < first || idx >= o_end) continue;
+        while (idx >= qe && q + 1 < nd) {
+          if (acc) atomicAdd(&s_acc[w][q], (unsigned long long)acc);
+          acc = 0;
+          q++;
+          qe = s_off[w][q + 1];
+        }
+        acc += splitmix64(((uint64_t)(idx - s_off[w][q]) << 32) | (uint64_t)(uint32_t)e[c]);
+      }
+    }
+    if (acc) atomicAdd(&s_acc[w][q], (unsigned long long)acc);
+    __syncwarp();
+    if (lane < nd && bp != 0) {
+      const uint64_t L = (uint64_t)(s_off[w][lane + 1] - o);
+      const uint64_t h = splitmix64((uint64_t)s_acc[w][lane] ^ splitmix64(hash_key + L));
+      heldout[d0 + lane] = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1 : 0;
+    }
+    __syncwarp();
+  }
+}
+
+// Positions whose document was found held out by hash_flat_kernel keep no
+// tokens.
+__global__ void apply_heldout_kernel(const uint32_t *__restrict__ order,
+                                     const uint8_t *__restrict__ heldout, uint64_t n_pos,
+                                     uint32_t *__restrict__ klen) {
+  const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= n_pos) return;
+  if (klen[x] && heldout[order[x]]) klen[x] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -986,6 +1083,24 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
   hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
                                                      klen, cum_last, ready, ready_at, T, hash_key,
                                                      frontier, kept);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hash_flat(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
+                             const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
+                             uint64_t hash_key, uint8_t *heldout, unsigned long long *counter,
+                             int n_sms, cudaStream_t st) {
+  ++launch_counter();
+  hash_flat_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, n_tokens, offs, sdb, stream_bp, J,
+                                                   hash_key, heldout, counter);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_heldout(const uint32_t *order, const uint8_t *heldout, uint64_t n_pos,
+                                 uint32_t *klen, cudaStream_t st) {
+  if (n_pos == 0) return cudaSuccess;
+  ++launch_counter();
+  apply_heldout_kernel<<<blocks_for(n_pos), kThreads, 0, st>>>(order, heldout, n_pos, klen);
   return cudaGetLastError();
 }
 

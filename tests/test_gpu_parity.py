@@ -226,3 +226,14 @@ def test_quota_tables_beyond_one_warp(S, strata):
     pk, o = packer_for(c), oracle_for(c)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=3)
+
+
+@pytest.mark.parametrize("max_steps", [2, 6, 40])
+def test_both_held_out_sweeps(max_steps):
+    # a short horizon hashes only the prefix each stream's windows reach (in
+    # shuffled order); a long one hashes every document (in document order):
+    # both must give the oracle's batches
+    c = make_preset("c3s", max_steps=max_steps)
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=2)
