@@ -402,19 +402,22 @@ __global__ void __launch_bounds__(kThreads, 8)
 
 // The same held-out decision for every document of the streams that hold out
 // any, in document order: a warp takes 32 consecutive documents and sweeps
-// their tokens as one flat run (lane l reads the 16-byte blocks l, l + 32,
-// ... of the run), so no lane idles on a short document.  Each lane follows
-// the document its block lies in with a cursor that only moves forward and
-// adds its partial sums into the warp's per-document slots in shared memory;
-// then lane l finishes document l.  Used when the horizon reaches most of the
-// corpus; the flags go to heldout[d].
+// their tokens as one flat run in rounds of 128 (lane l reads the 16-byte
+// block l of the round), so no lane idles on a short document.  A round
+// inside one document is summed in the lanes' registers; a round that crosses
+// a document end (or the run's ends) first hands the registers' sum to the
+// document it belongs to, then sums its tokens per document across the warp,
+// and lane 0 adds each document's share to the warp's per-document slots in
+// shared memory (one writer, no atomics).  Lane l then finishes document l.
+// Used when the horizon reaches most of the corpus; the flags go to
+// heldout[d].
 __global__ void __launch_bounds__(kThreads)
     hash_flat_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
                      const int64_t *__restrict__ offs, const uint32_t *__restrict__ sdb,
                      const uint16_t *__restrict__ stream_bp, uint32_t J, uint64_t hash_key,
                      uint8_t *__restrict__ heldout, unsigned long long *counter) {
   constexpr int kWarps = kThreads / 32;
-  __shared__ unsigned long long s_acc[kWarps][32];
+  __shared__ uint64_t s_acc[kWarps][32];
   __shared__ int64_t s_off[kWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t D0 = sdb[0], D1 = sdb[J];
@@ -441,39 +444,68 @@ __global__ void __launch_bounds__(kThreads)
                                    (uint64_t)o_end > n_tokens);
     if (__any_sync(0xffffffffu, bad) || !__any_sync(0xffffffffu, bp != 0)) continue;
     const int64_t first = __shfl_sync(0xffffffffu, o, 0);
-    s_off[w][lane] = o;
+    if (lane < nd) s_off[w][lane] = o;
     if (lane == 0) s_off[w][nd] = o_end;
     s_acc[w][lane] = 0;
     __syncwarp();
-    int q = 0;           // document of this lane's current block
-    int64_t qe = s_off[w][1];
-    uint64_t acc = 0;
-    for (int64_t g = (first & ~(int64_t)3) + 4 * lane; g < o_end; g += 128) {
-      const int4 v = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
-      if (g >= first && g + 3 < qe) {
-        // the whole block lies in document q (the common case)
-        acc += hash_terms_inside(v, (uint32_t)(g - s_off[w][q]));
+    int qc = 0;          // document of the current round's first token (uniform)
+    int qa = 0;          // document the lanes' register sums belong to (uniform)
+    uint64_t acc = 0;    // this lane's sum for document qa over whole rounds
+    for (int64_t R = first & ~(int64_t)3; R < o_end; R += 128) {
+      const int64_t g = R + 4 * lane;
+      const bool inb = g < o_end;
+      int4 v = make_int4(0, 0, 0, 0);
+      if (inb) v = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
+      const int64_t lo = max(R, first), hi = min(R + 128, o_end);  // round's tokens
+      while (s_off[w][qc + 1] <= lo) qc++;
+      if (qc != qa) {
+        const uint64_t t = warp_sum_u64(acc);
+        if (lane == 0) s_acc[w][qa] += t;
+        acc = 0;
+        qa = qc;
+      }
+      const int64_t qs = s_off[w][qc];
+      if (R >= first && hi <= s_off[w][qc + 1] && R + 128 <= o_end) {
+        // the whole round lies in document qc
+        acc += hash_terms_inside(v, (uint32_t)(g - qs));
         continue;
       }
+      // hand the registers' sum to its document, then split this round
+      const uint64_t t = warp_sum_u64(acc);
+      if (lane == 0) s_acc[w][qa] += t;
+      acc = 0;
       const int32_t e[4] = {v.x, v.y, v.z, v.w};
+      int qb = qc;
+      while (s_off[w][qb + 1] < hi) qb++;  // last document this round touches
+      int qt = qc;
+      uint64_t term[4];
+      int tq[4];
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         const int64_t idx = g + c;
-        if (idx < first || idx >= o_end) continue;
-        while (idx >= qe && q + 1 < nd) {
-          if (acc) atomicAdd(&s_acc[w][q], (unsigned long long)acc);
-          acc = 0;
-          q++;
-          qe = s_off[w][q + 1];
-        }
-        acc += splitmix64(((uint64_t)(idx - s_off[w][q]) << 32) | (uint64_t)(uint32_t)e[c]);
+        term[c] = 0;
+        tq[c] = -1;
+        if (idx < lo || idx >= hi) continue;
+        while (s_off[w][qt + 1] <= idx) qt++;
+        term[c] = splitmix64(((uint64_t)(idx - s_off[w][qt]) << 32) | (uint64_t)(uint32_t)e[c]);
+        tq[c] = qt;
       }
+      for (int q = qc; q <= qb; q++) {
+        uint64_t x = 0;
+#pragma unroll
+        for (int c = 0; c < 4; c++) x += (tq[c] == q) ? term[c] : 0;
+        x = warp_sum_u64(x);
+        if (lane == 0) s_acc[w][q] += x;
+      }
+      qc = qb;
+      qa = qb;
     }
-    if (acc) atomicAdd(&s_acc[w][q], (unsigned long long)acc);
+    const uint64_t t = warp_sum_u64(acc);
+    if (lane == 0) s_acc[w][qa] += t;
     __syncwarp();
     if (lane < nd && bp != 0) {
       const uint64_t L = (uint64_t)(s_off[w][lane + 1] - o);
-      const uint64_t h = splitmix64((uint64_t)s_acc[w][lane] ^ splitmix64(hash_key + L));
+      const uint64_t h = splitmix64(s_acc[w][lane] ^ splitmix64(hash_key + L));
       heldout[d0 + lane] = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1 : 0;
     }
     __syncwarp();
