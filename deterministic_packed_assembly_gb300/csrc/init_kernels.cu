@@ -451,54 +451,65 @@ __global__ void __launch_bounds__(kThreads)
     int qc = 0;          // document of the current round's first token (uniform)
     int qa = 0;          // document the lanes' register sums belong to (uniform)
     uint64_t acc = 0;    // this lane's sum for document qa over whole rounds
-    for (int64_t R = first & ~(int64_t)3; R < o_end; R += 128) {
-      const int64_t g = R + 4 * lane;
-      const bool inb = g < o_end;
-      int4 v = make_int4(0, 0, 0, 0);
-      if (inb) v = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
-      const int64_t lo = max(R, first), hi = min(R + 128, o_end);  // round's tokens
-      while (s_off[w][qc + 1] <= lo) qc++;
-      if (qc != qa) {
+    constexpr int kAhead = 4;  // rounds whose loads are in flight together
+    for (int64_t R0 = first & ~(int64_t)3; R0 < o_end; R0 += 128 * kAhead) {
+      int4 vv[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; u++) {
+        const int64_t g = R0 + 128 * u + 4 * lane;
+        vv[u] = make_int4(0, 0, 0, 0);
+        if (g < o_end) vv[u] = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
+      }
+#pragma unroll
+      for (int u = 0; u < kAhead; u++) {
+        const int64_t R = R0 + 128 * u;
+        if (R >= o_end) break;
+        const int64_t g = R + 4 * lane;
+        const int4 v = vv[u];
+        const int64_t lo = max(R, first), hi = min(R + 128, o_end);  // round's tokens
+        while (s_off[w][qc + 1] <= lo) qc++;
+        if (qc != qa) {
+          const uint64_t t = warp_sum_u64(acc);
+          if (lane == 0) s_acc[w][qa] += t;
+          acc = 0;
+          qa = qc;
+        }
+        const int64_t qs = s_off[w][qc];
+        if (R >= first && hi <= s_off[w][qc + 1] && R + 128 <= o_end) {
+          // the whole round lies in document qc
+          acc += hash_terms_inside(v, (uint32_t)(g - qs));
+          continue;
+        }
+        // hand the registers' sum to its document, then split this round
         const uint64_t t = warp_sum_u64(acc);
         if (lane == 0) s_acc[w][qa] += t;
         acc = 0;
-        qa = qc;
-      }
-      const int64_t qs = s_off[w][qc];
-      if (R >= first && hi <= s_off[w][qc + 1] && R + 128 <= o_end) {
-        // the whole round lies in document qc
-        acc += hash_terms_inside(v, (uint32_t)(g - qs));
-        continue;
-      }
-      // hand the registers' sum to its document, then split this round
-      const uint64_t t = warp_sum_u64(acc);
-      if (lane == 0) s_acc[w][qa] += t;
-      acc = 0;
-      const int32_t e[4] = {v.x, v.y, v.z, v.w};
-      int qb = qc;
-      while (s_off[w][qb + 1] < hi) qb++;  // last document this round touches
-      int qt = qc;
-      uint64_t term[4];
-      int tq[4];
+        const int32_t e[4] = {v.x, v.y, v.z, v.w};
+        int qb = qc;
+        while (s_off[w][qb + 1] < hi) qb++;  // last document this round touches
+        int qt = qc;
+        uint64_t term[4];
+        int tq[4];
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
-        const int64_t idx = g + c;
-        term[c] = 0;
-        tq[c] = -1;
-        if (idx < lo || idx >= hi) continue;
-        while (s_off[w][qt + 1] <= idx) qt++;
-        term[c] = splitmix64(((uint64_t)(idx - s_off[w][qt]) << 32) | (uint64_t)(uint32_t)e[c]);
-        tq[c] = qt;
-      }
-      for (int q = qc; q <= qb; q++) {
-        uint64_t x = 0;
+        for (int c = 0; c < 4; c++) {
+          const int64_t idx = g + c;
+          term[c] = 0;
+          tq[c] = -1;
+          if (idx < lo || idx >= hi) continue;
+          while (s_off[w][qt + 1] <= idx) qt++;
+          term[c] = splitmix64(((uint64_t)(idx - s_off[w][qt]) << 32) | (uint64_t)(uint32_t)e[c]);
+          tq[c] = qt;
+        }
+        for (int q = qc; q <= qb; q++) {
+          uint64_t x = 0;
 #pragma unroll
-        for (int c = 0; c < 4; c++) x += (tq[c] == q) ? term[c] : 0;
-        x = warp_sum_u64(x);
-        if (lane == 0) s_acc[w][q] += x;
+          for (int c = 0; c < 4; c++) x += (tq[c] == q) ? term[c] : 0;
+          x = warp_sum_u64(x);
+          if (lane == 0) s_acc[w][q] += x;
+        }
+        qc = qb;
+        qa = qb;
       }
-      qc = qb;
-      qa = qb;
     }
     const uint64_t t = warp_sum_u64(acc);
     if (lane == 0) s_acc[w][qa] += t;
