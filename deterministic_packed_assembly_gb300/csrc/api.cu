@@ -285,37 +285,20 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                             order, klen, c->err, st));
   }
 
-  // ---- 3. held-out flags ----------------------------------------------------
-  // When the horizon reaches most of the corpus every document of a stream
-  // with a held-out rate is hashed, in document order (the cheapest sweep);
-  // otherwise only the prefix of each stream its windows can reach, in
-  // shuffled order, beside the quota kernels: it reads each stream's need from
-  // their table once all S quota blocks have published it, and hashes on
-  // until then.
+  // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
+  // Runs beside the quota kernels: it reads each stream's need from their
+  // table once all S quota blocks have published it, and hashes on until then.
   if (any_heldout) {
-    if ((uint64_t)K * c->B * T >= c->n_tokens / 2) {
-      uint8_t *heldout = a.temp<uint8_t>(std::max<uint32_t>(c->n_docs, 1));
-      unsigned long long *counter = a.temp<unsigned long long>(1);
-      NS_ALLOC(heldout);
-      NS_ALLOC(counter);
-      NS_CK(cudaMemsetAsync(heldout, 0, std::max<uint32_t>(c->n_docs, 1), st));
-      NS_CK(cudaMemsetAsync(counter, 0, sizeof(unsigned long long), st));
-      NS_CK(nsk::launch_hash_flat(c->tokens, c->n_tokens, c->offs, static_cast<uint32_t *>(d_sdb),
-                                  static_cast<uint16_t *>(d_stream_bp), J, c->hash_key, heldout,
-                                  counter, c->n_sms, st));
-      NS_CK(nsk::launch_apply_heldout(order, heldout, n_pos, klen, st));
-    } else {
-      unsigned long long *frontier = a.temp<unsigned long long>(J);
-      unsigned long long *kept = a.temp<unsigned long long>(J);
-      NS_ALLOC(frontier);
-      NS_ALLOC(kept);
-      NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
-      NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
-      NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
-                                    static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
-                                    c->cum + (size_t)K * J, ready, S, T, c->hash_key, frontier,
-                                    kept, c->n_sms, st));
-    }
+    unsigned long long *frontier = a.temp<unsigned long long>(J);
+    unsigned long long *kept = a.temp<unsigned long long>(J);
+    NS_ALLOC(frontier);
+    NS_ALLOC(kept);
+    NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
+    NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
+    NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+                                  static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
+                                  c->cum + (size_t)K * J, ready, S, T, c->hash_key, frontier,
+                                  kept, c->n_sms, st));
   }
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));

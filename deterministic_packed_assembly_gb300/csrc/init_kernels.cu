@@ -341,7 +341,7 @@ __device__ __forceinline__ uint64_t warp_doc_hash(const int32_t *__restrict__ to
 // kept tokens below it exceed need_j unless the whole stream was hashed, so
 // the prefix the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
-__global__ void __launch_bounds__(kThreads, 8)
+__global__ void __launch_bounds__(kThreads)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
@@ -398,139 +398,6 @@ __global__ void __launch_bounds__(kThreads, 8)
       if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
     }
   }
-}
-
-// The same held-out decision for every document of the streams that hold out
-// any, in document order: a warp takes 32 consecutive documents and sweeps
-// their tokens as one flat run in rounds of 128 (lane l reads the 16-byte
-// block l of the round), so no lane idles on a short document.  A round
-// inside one document is summed in the lanes' registers; a round that crosses
-// a document end (or the run's ends) first hands the registers' sum to the
-// document it belongs to, then sums its tokens per document across the warp,
-// and lane 0 adds each document's share to the warp's per-document slots in
-// shared memory (one writer, no atomics).  Lane l then finishes document l.
-// Used when the horizon reaches most of the corpus; the flags go to
-// heldout[d].
-__global__ void __launch_bounds__(kThreads)
-    hash_flat_kernel(const int32_t *__restrict__ tokens, uint64_t n_tokens,
-                     const int64_t *__restrict__ offs, const uint32_t *__restrict__ sdb,
-                     const uint16_t *__restrict__ stream_bp, uint32_t J, uint64_t hash_key,
-                     uint8_t *__restrict__ heldout, unsigned long long *counter) {
-  constexpr int kWarps = kThreads / 32;
-  __shared__ uint64_t s_acc[kWarps][32];
-  __shared__ int64_t s_off[kWarps][33];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const uint32_t D0 = sdb[0], D1 = sdb[J];
-  while (true) {
-    unsigned long long base = 0;
-    if (lane == 0) base = atomicAdd(counter, 32ull);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (base >= (unsigned long long)(D1 - D0)) break;
-    const uint32_t d0 = D0 + (uint32_t)base;
-    const int nd = (int)min(32ull, (unsigned long long)(D1 - D0) - base);
-    // this lane's document: its rate, its offsets
-    uint32_t bp = 0;
-    if (lane < nd) {
-      const int64_t j = last_le<uint32_t, int64_t>(sdb, 0, (int64_t)J, d0 + lane);
-      bp = stream_bp[j];
-    }
-    int64_t o = 0;
-    if (lane < nd) o = __ldg(offs + d0 + lane);
-    const int64_t o_end = __ldg(offs + d0 + nd);
-    const int64_t o_next = __shfl_down_sync(0xffffffffu, o, 1);
-    const int64_t o_hi = (lane + 1 < nd) ? o_next : o_end;
-    // offsets checked here too: a malformed partition is never read past
-    const bool bad = lane < nd && (o < 0 || o_hi < o || o_hi - o > 0x7FFFFFFF ||
-                                   (uint64_t)o_end > n_tokens);
-    if (__any_sync(0xffffffffu, bad) || !__any_sync(0xffffffffu, bp != 0)) continue;
-    const int64_t first = __shfl_sync(0xffffffffu, o, 0);
-    if (lane < nd) s_off[w][lane] = o;
-    if (lane == 0) s_off[w][nd] = o_end;
-    s_acc[w][lane] = 0;
-    __syncwarp();
-    int qc = 0;          // document of the current round's first token (uniform)
-    int qa = 0;          // document the lanes' register sums belong to (uniform)
-    uint64_t acc = 0;    // this lane's sum for document qa over whole rounds
-    constexpr int kAhead = 4;  // rounds whose loads are in flight together
-    for (int64_t R0 = first & ~(int64_t)3; R0 < o_end; R0 += 128 * kAhead) {
-      int4 vv[kAhead];
-#pragma unroll
-      for (int u = 0; u < kAhead; u++) {
-        const int64_t g = R0 + 128 * u + 4 * lane;
-        vv[u] = make_int4(0, 0, 0, 0);
-        if (g < o_end) vv[u] = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
-      }
-#pragma unroll
-      for (int u = 0; u < kAhead; u++) {
-        const int64_t R = R0 + 128 * u;
-        if (R >= o_end) break;
-        const int64_t g = R + 4 * lane;
-        const int4 v = vv[u];
-        const int64_t lo = max(R, first), hi = min(R + 128, o_end);  // round's tokens
-        while (s_off[w][qc + 1] <= lo) qc++;
-        if (qc != qa) {
-          const uint64_t t = warp_sum_u64(acc);
-          if (lane == 0) s_acc[w][qa] += t;
-          acc = 0;
-          qa = qc;
-        }
-        const int64_t qs = s_off[w][qc];
-        if (R >= first && hi <= s_off[w][qc + 1] && R + 128 <= o_end) {
-          // the whole round lies in document qc
-          acc += hash_terms_inside(v, (uint32_t)(g - qs));
-          continue;
-        }
-        // hand the registers' sum to its document, then split this round
-        const uint64_t t = warp_sum_u64(acc);
-        if (lane == 0) s_acc[w][qa] += t;
-        acc = 0;
-        const int32_t e[4] = {v.x, v.y, v.z, v.w};
-        int qb = qc;
-        while (s_off[w][qb + 1] < hi) qb++;  // last document this round touches
-        int qt = qc;
-        uint64_t term[4];
-        int tq[4];
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-          const int64_t idx = g + c;
-          term[c] = 0;
-          tq[c] = -1;
-          if (idx < lo || idx >= hi) continue;
-          while (s_off[w][qt + 1] <= idx) qt++;
-          term[c] = splitmix64(((uint64_t)(idx - s_off[w][qt]) << 32) | (uint64_t)(uint32_t)e[c]);
-          tq[c] = qt;
-        }
-        for (int q = qc; q <= qb; q++) {
-          uint64_t x = 0;
-#pragma unroll
-          for (int c = 0; c < 4; c++) x += (tq[c] == q) ? term[c] : 0;
-          x = warp_sum_u64(x);
-          if (lane == 0) s_acc[w][q] += x;
-        }
-        qc = qb;
-        qa = qb;
-      }
-    }
-    const uint64_t t = warp_sum_u64(acc);
-    if (lane == 0) s_acc[w][qa] += t;
-    __syncwarp();
-    if (lane < nd && bp != 0) {
-      const uint64_t L = (uint64_t)(s_off[w][lane + 1] - o);
-      const uint64_t h = splitmix64(s_acc[w][lane] ^ splitmix64(hash_key + L));
-      heldout[d0 + lane] = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1 : 0;
-    }
-    __syncwarp();
-  }
-}
-
-// Positions whose document was found held out by hash_flat_kernel keep no
-// tokens.
-__global__ void apply_heldout_kernel(const uint32_t *__restrict__ order,
-                                     const uint8_t *__restrict__ heldout, uint64_t n_pos,
-                                     uint32_t *__restrict__ klen) {
-  const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= n_pos) return;
-  if (klen[x] && heldout[order[x]]) klen[x] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -1126,24 +993,6 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
   hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
                                                      klen, cum_last, ready, ready_at, T, hash_key,
                                                      frontier, kept);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_hash_flat(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
-                             const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
-                             uint64_t hash_key, uint8_t *heldout, unsigned long long *counter,
-                             int n_sms, cudaStream_t st) {
-  ++launch_counter();
-  hash_flat_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, n_tokens, offs, sdb, stream_bp, J,
-                                                   hash_key, heldout, counter);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_apply_heldout(const uint32_t *order, const uint8_t *heldout, uint64_t n_pos,
-                                 uint32_t *klen, cudaStream_t st) {
-  if (n_pos == 0) return cudaSuccess;
-  ++launch_counter();
-  apply_heldout_kernel<<<blocks_for(n_pos), kThreads, 0, st>>>(order, heldout, n_pos, klen);
   return cudaGetLastError();
 }
 

@@ -44,13 +44,6 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0, uint32_t *order,
                          uint32_t *klen, int *err, cudaStream_t st);
-// held-out flags of every document of the streams that hold out any
-cudaError_t launch_hash_flat(const int32_t *tokens, uint64_t n_tokens, const int64_t *offs,
-                             const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
-                             uint64_t hash_key, uint8_t *heldout, unsigned long long *counter,
-                             int n_sms, cudaStream_t st);
-cudaError_t launch_apply_heldout(const uint32_t *order, const uint8_t *heldout, uint64_t n_pos,
-                                 uint32_t *klen, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
