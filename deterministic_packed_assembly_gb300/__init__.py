@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     NS_ERR_OOM,
     NS_OK,
     NS_PACK_DRAIN,
+    NS_PACK_HELDOUT,
     LIB_PATH,
     SYMBOLS,
     NsPackError,

@@ -21,6 +21,7 @@ NS_ERR_HORIZON = -5
 NS_ERR_BAD_INPUT = -6
 NS_ERR_DEVICE = -7
 NS_PACK_DRAIN = 1
+NS_PACK_HELDOUT = 2
 NS_MAX_T = 1 << 24
 
 ns_alloc_fn = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)

@@ -110,7 +110,7 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
-  if (cfg->flags & ~NS_PACK_DRAIN) return NS_ERR_INVALID_ARG;
+  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT)) return NS_ERR_INVALID_ARG;
   if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
   for (uint32_t s = 0; s < cfg->n_sources; s++)
     if (cfg->source_weight[s] == 0 || cfg->source_heldout_bp[s] > 10000) return NS_ERR_INVALID_ARG;
@@ -260,6 +260,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
   const uint32_t D0 = sdb[0];
   const uint64_t n_pos = (uint64_t)sdb[J] - D0;
+  const bool heldout_mode = (c->flags & NS_PACK_HELDOUT) != 0;
   std::vector<uint64_t> N(J);
   for (uint32_t j = 0; j < J; j++) N[j] = (uint64_t)sdb[j + 1] - sdb[j];
   uint64_t *keys = a.temp<uint64_t>((size_t)J * 4);
@@ -282,7 +283,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
-                            order, klen, c->err, st));
+                            heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr, order,
+                            klen, c->err, st));
   }
 
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
@@ -297,8 +299,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
     NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
                                   static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
-                                  c->cum + (size_t)K * J, ready, S, T, c->hash_key, frontier,
-                                  kept, c->n_sms, st));
+                                  c->cum + (size_t)K * J, ready, S, T, c->hash_key,
+                                  heldout_mode ? 1u : 0u, frontier, kept, c->n_sms, st));
   }
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
@@ -420,7 +422,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.scalars[1] = c->B;
   h.scalars[2] = K;
   h.scalars[3] = 0;  // valid_steps, read on the device
-  h.scalars[4] = (c->flags & NS_PACK_DRAIN) ? 1 : 0;
+  h.scalars[4] = c->flags & (NS_PACK_DRAIN | NS_PACK_HELDOUT);
   h.scalars[5] = (uint64_t)(uint32_t)c->pad_id;
   h.scalars[6] = c->seed;
   h.scalars[7] = c->hash_key;

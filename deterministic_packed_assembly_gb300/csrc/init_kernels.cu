@@ -333,8 +333,8 @@ __device__ __forceinline__ uint64_t warp_doc_hash(const int32_t *__restrict__ to
 
 // Held-out flags for the prefix of every stream the horizon reaches.  A
 // stream's documents are taken in shuffled-position order, a few at a time
-// from the stream's frontier; a document found held out has its kept length
-// set to 0.  A warp leaves a stream once the kept tokens of the documents
+// from the stream's frontier; a document the stream does not keep (held out
+// for training, not held out for validation) has its kept length set to 0.  A warp leaves a stream once the kept tokens of the documents
 // already hashed exceed need_j = rmax_j * T (the windows the horizon asks of
 // it hold at most that many), or when the stream runs out, and goes on to the
 // next stream.  Every position below the final frontier is hashed, and the
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads)
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
                        const unsigned *ready, unsigned ready_at, uint32_t T,
-                       uint64_t hash_key, unsigned long long *frontier,
+                       uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
                        unsigned long long *kept) {
   constexpr uint32_t kGrab = 8;
   const int lane = threadIdx.x & 31;
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads)
         if (L == 0) continue;
         const int64_t o0 = __shfl_sync(0xffffffffu, o_l, q);
         const uint64_t h = warp_doc_hash(tokens, o0, o0 + L, hash_key, lane);
-        if (__umul64hi(h, 10000ull) < (uint64_t)bp) {
+        const uint32_t held = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1u : 0u;
+        if (held != want_heldout) {
           if (lane == 0) klen[base_pos + base + q] = 0;
         } else {
           kept_here += L;
@@ -405,8 +406,11 @@ __global__ void __launch_bounds__(kThreads)
 // 4-round balanced Feistel network over 2*half bits (half = bits / 2, bits =
 // max(2, ceil(log2 N_j)) rounded up to even), walked until it lands in
 // [0, N_j).  Writes the document and its length (0 if empty, or if its
-// offsets are malformed -- validate_offsets_kernel reports that); held-out
-// documents are zeroed afterwards by hash_prefix_kernel.
+// offsets are malformed -- validate_offsets_kernel reports that); documents
+// the stream does not keep are zeroed afterwards by hash_prefix_kernel
+// (held-out ones for training, the others for validation).  For the
+// validation stream (stream_bp_heldout_mode given), a stream whose source
+// holds nothing out keeps nothing.
 __device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, uint64_t mask,
                                             uint64_t x) {
   uint64_t L = x >> half, R = x & mask;
@@ -423,6 +427,7 @@ __device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, 
 __global__ void __launch_bounds__(kThreads)
     order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
                  const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
+                 const uint16_t *__restrict__ stream_bp_heldout_mode,
                  uint32_t *__restrict__ order, uint32_t *__restrict__ klen, int *err) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
@@ -449,7 +454,9 @@ __global__ void __launch_bounds__(kThreads)
   }
   const uint32_t d = b0 + (uint32_t)y;
   const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
-  const bool ok = o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
+  bool ok = o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
+  // the validation stream of a source that holds nothing out is empty
+  if (stream_bp_heldout_mode && stream_bp_heldout_mode[j] == 0) ok = false;
   const uint64_t idx = (uint64_t)b0 + p - D0;
   order[idx] = d;
   klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
@@ -987,22 +994,24 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
                                const unsigned *ready, unsigned ready_at, uint32_t T,
-                               uint64_t hash_key, unsigned long long *frontier,
-                               unsigned long long *kept, int n_sms, cudaStream_t st) {
+                               uint64_t hash_key, uint32_t want_heldout,
+                               unsigned long long *frontier, unsigned long long *kept, int n_sms,
+                               cudaStream_t st) {
   ++launch_counter();
   hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
                                                      klen, cum_last, ready, ready_at, T, hash_key,
-                                                     frontier, kept);
+                                                     want_heldout, frontier, kept);
   return cudaGetLastError();
 }
 
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
-                         const int64_t *offs, uint64_t n_tokens, uint32_t D0, uint32_t *order,
-                         uint32_t *klen, int *err, cudaStream_t st) {
+                         const int64_t *offs, uint64_t n_tokens, uint32_t D0,
+                         const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
+                         int *err, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, n_tokens, D0, order, klen,
-                                                err);
+  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, n_tokens, D0,
+                                                stream_bp_heldout_mode, order, klen, err);
   return cudaGetLastError();
 }
 

@@ -41,16 +41,21 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
                             cudaStream_t st);
 
 // ---- held-out hash, order, scans ------------------------------------------
+// stream_bp_heldout_mode: null for the training stream; for the validation
+// stream the per-stream rates (a stream of a source that holds nothing out
+// keeps nothing)
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
-                         const int64_t *offs, uint64_t n_tokens, uint32_t D0, uint32_t *order,
-                         uint32_t *klen, int *err, cudaStream_t st);
+                         const int64_t *offs, uint64_t n_tokens, uint32_t D0,
+                         const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
+                         int *err, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
                                const unsigned *ready, unsigned ready_at, uint32_t T,
-                               uint64_t hash_key, unsigned long long *frontier,
-                               unsigned long long *kept, int n_sms, cudaStream_t st);
+                               uint64_t hash_key, uint32_t want_heldout,
+                               unsigned long long *frontier, unsigned long long *kept, int n_sms,
+                               cudaStream_t st);
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,

@@ -65,6 +65,11 @@ extern "C" {
  * last window are empty (pad, pos 0, doc -1, mask 0); later updates return
  * NS_ERR_EXHAUSTED. */
 #define NS_PACK_DRAIN 1u
+/* Pack the validation stream: the held-out documents of every stream instead
+ * of the kept ones ("each source's validation rows come from those of every
+ * stratum", NeuronSpark-Trainer README, Concepts).  Same shuffle, packing,
+ * quotas and assembly; a source with a held-out rate of 0 has no windows. */
+#define NS_PACK_HELDOUT 2u
 
 /* ---- limits ------------------------------------------------------------- */
 #define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
@@ -106,7 +111,7 @@ typedef struct {
   uint64_t hash_key; /* keys the held-out hash (not the seed: same in every line) */
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
-  uint32_t flags;    /* NS_PACK_DRAIN */
+  uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT */
   int32_t pad_id;    /* token written at padded positions */
   void *cuda_stream; /* cudaStream_t for init and default for the other calls */
   ns_alloc_fn alloc;

@@ -58,6 +58,7 @@ class _Config(C.Structure):
         ("seed", C.c_uint64), ("hash_key", C.c_uint64),
         ("B", C.c_uint32), ("max_steps", C.c_uint32), ("drain", C.c_uint32),
         ("pad_id", C.c_int32),
+        ("heldout_only", C.c_uint32),
     ]
 
 
@@ -187,7 +188,7 @@ class Oracle:
     def __init__(self, corpus, *, seed: Optional[int] = None, hash_key: Optional[int] = None,
                  max_steps: Optional[int] = None, drain: Optional[bool] = None,
                  T: Optional[int] = None, B: Optional[int] = None,
-                 pad_id: Optional[int] = None):
+                 pad_id: Optional[int] = None, heldout_only: bool = False):
         c = corpus
         self.corpus = c
         self.T = int(T if T is not None else c.T)
@@ -227,6 +228,7 @@ class Oracle:
         cfg.max_steps = self.max_steps
         cfg.drain = int(bool(drain if drain is not None else c.drain))
         cfg.pad_id = int(pad_id if pad_id is not None else c.pad_id)
+        cfg.heldout_only = int(bool(heldout_only))
         self._cfg = cfg
         h = C.c_void_p()
         rc = lib().or_build(C.byref(cfg), C.byref(h))

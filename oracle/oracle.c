@@ -20,6 +20,8 @@
  *  - "Zephon: deterministic data loading" (aixai.ru), the section on
  *    checkpointing on 16 GPUs and resuming on 8/32/64: every global batch is
  *    byte-identical (SHA-256) whatever the GPU count.
+ *    Each source's validation rows come from the held-out documents of
+ *    every stratum (same section); a validation stream packs exactly those.
  *  - Linnet training docs, Supervised fine-tuning: rows of exactly T
  *    positions, padded; only the completion is learned; each step weighs by
  *    its count of learned positions.  Other trainers: a position id of 0
@@ -76,6 +78,7 @@ typedef struct {
   uint32_t max_steps;
   uint32_t drain;
   int32_t pad_id;
+  uint32_t heldout_only; /* 1: pack the held-out documents (the validation stream) */
 } or_config;
 
 typedef struct {
@@ -266,7 +269,9 @@ static int pack_stream(or_ctx *x, uint32_t j) {
     while (y >= n) y = or_feistel_encrypt(key, half, y);
     uint32_t d = d0 + (uint32_t)y;
     uint64_t L = doc_len(c, d);
-    if (L == 0 || x->heldout[d]) continue;
+    /* the training stream keeps what is not held out; the validation stream
+       keeps exactly what is */
+    if (L == 0 || x->heldout[d] != (c->heldout_only ? 1 : 0)) continue;
     for (uint64_t off = 0; off < L; off += c->T) {
       uint64_t len = (L - off < c->T) ? (L - off) : c->T;
       if (used + len > c->T) used = 0; /* close the window; the rest is padding */
@@ -363,7 +368,7 @@ static uint64_t build_digest(const or_ctx *x) {
   digest_add(&a, c->B);
   digest_add(&a, c->max_steps);
   digest_add(&a, x->valid_steps);
-  digest_add(&a, c->drain ? 1 : 0);
+  digest_add(&a, (c->drain ? 1u : 0u) | (c->heldout_only ? 2u : 0u));
   digest_add(&a, (uint64_t)(uint32_t)c->pad_id);
   digest_add(&a, c->seed);
   digest_add(&a, c->hash_key);

@@ -230,10 +230,34 @@ def test_quota_tables_beyond_one_warp(S, strata):
 
 @pytest.mark.parametrize("max_steps", [2, 6, 40])
 def test_both_held_out_sweeps(max_steps):
-    # a short horizon hashes only the prefix each stream's windows reach (in
-    # shuffled order); a long one hashes every document (in document order):
-    # both must give the oracle's batches
+    # a short horizon stops hashing each stream once its kept tokens cover
+    # its windows; a horizon past the data hashes all of it
     c = make_preset("c3s", max_steps=max_steps)
     pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=2)
+
+
+@pytest.mark.parametrize("name", ["c1", "c3s", "c5s"])
+def test_validation_stream(name):
+    # the held-out documents of every stream, packed and assembled the same way
+    c = make_preset(name)
+    if int(c.source_heldout_bp.max()) == 0:
+        c.source_heldout_bp = np.full(c.n_sources, 700, np.uint16)
+    pk = packer_for(c, heldout_only=True, drain=True)
+    o = oracle_for(c, heldout_only=True, drain=True)
+    _check_tables(pk, o, c)
+    assert o.valid_steps > 0
+    compare_steps(pk, o, range(o.valid_steps), launch=3)
+    # and the training stream of the same recipe differs from it
+    assert packer_for(c, drain=True).order_digest != pk.order_digest
+
+
+@pytest.mark.parametrize("case", range(20))
+def test_validation_stream_random_tiny_corpora(case):
+    rng = np.random.default_rng(7000 + case)
+    c = _random_case(rng)
+    o = oracle_for(c, heldout_only=True)
+    pk = packer_for(c, heldout_only=True)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=2)
