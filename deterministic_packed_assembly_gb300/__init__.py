@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     NS_OK,
     NS_PACK_DRAIN,
     NS_PACK_HELDOUT,
+    NS_PACK_SHUFFLE_ROWS,
     LIB_PATH,
     SYMBOLS,
     NsPackError,

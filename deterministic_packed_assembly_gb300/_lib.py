@@ -22,6 +22,7 @@ NS_ERR_BAD_INPUT = -6
 NS_ERR_DEVICE = -7
 NS_PACK_DRAIN = 1
 NS_PACK_HELDOUT = 2
+NS_PACK_SHUFFLE_ROWS = 4
 NS_MAX_T = 1 << 24
 
 ns_alloc_fn = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)
@@ -49,6 +50,7 @@ class ns_pack_config(C.Structure):
         ("max_steps", C.c_uint32),
         ("flags", C.c_uint32),
         ("pad_id", C.c_int32),
+        ("window_segment", C.c_uint32),
         ("cuda_stream", C.c_void_p),
         ("alloc", ns_alloc_fn),
         ("free", ns_free_fn),

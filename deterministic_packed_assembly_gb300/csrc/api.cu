@@ -16,7 +16,7 @@
 
 struct ns_pack_ctx {
   // recipe
-  uint32_t T = 0, B = 0, K = 0, flags = 0, S = 0, J = 0, n_docs = 0;
+  uint32_t T = 0, B = 0, K = 0, flags = 0, S = 0, J = 0, n_docs = 0, G = 0;
   int32_t pad_id = 0;
   uint64_t seed = 0, hash_key = 0, n_tokens = 0;
   const int32_t *tokens = nullptr;
@@ -110,7 +110,9 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
-  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT)) return NS_ERR_INVALID_ARG;
+  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS))
+    return NS_ERR_INVALID_ARG;
+  if (cfg->window_segment > NS_MAX_WINDOW_SEGMENT) return NS_ERR_INVALID_ARG;
   if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
   for (uint32_t s = 0; s < cfg->n_sources; s++)
     if (cfg->source_weight[s] == 0 || cfg->source_heldout_bp[s] > 10000) return NS_ERR_INVALID_ARG;
@@ -299,7 +301,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
     NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
                                   static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
-                                  c->cum + (size_t)K * J, ready, S, T, c->hash_key,
+                                  c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                   heldout_mode ? 1u : 0u, frontier, kept, c->n_sms, st));
   }
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
@@ -313,7 +315,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(npieces);
   NS_ALLOC(node_base);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
-                           T, cutoff, npieces, st));
+                           T, c->G, cutoff, npieces, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
   std::vector<uint32_t> cut_h(J);
   std::vector<int64_t> np_h(J), nb_h(J + 1);
@@ -331,7 +333,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   std::vector<uint64_t> rmax(J);
   std::vector<int64_t> wbase(J + 1, 0);
   for (uint32_t j = 0; j < J; j++) {
-    rmax[j] = (uint64_t)rmax32[j];
+    // windows the horizon can read: whole segments when they are shuffled
+    rmax[j] = c->G ? ((uint64_t)rmax32[j] + c->G - 1) / c->G * c->G : (uint64_t)rmax32[j];
     wbase[j + 1] = wbase[j] + (int64_t)rmax[j];
   }
   c->wbase = a.keep<int64_t>(J + 1);
@@ -405,7 +408,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase, win_start,
                                   st));
   NS_CK(nsk::launch_row_windows(c->rb, c->cum, c->W, c->wbase, win_start, levels, J, c->B, K,
-                                c->row_win, st));
+                                c->seed, c->G, (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u,
+                                c->row_win, c->err, st));
   NS_CK(nsk::launch_valid_steps(c->cum, c->W, J, K, (c->flags & NS_PACK_DRAIN) ? 1u : 0u,
                                 first_bad, valid, st));
 
@@ -422,12 +426,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.scalars[1] = c->B;
   h.scalars[2] = K;
   h.scalars[3] = 0;  // valid_steps, read on the device
-  h.scalars[4] = c->flags & (NS_PACK_DRAIN | NS_PACK_HELDOUT);
+  h.scalars[4] = c->flags & (NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS);
   h.scalars[5] = (uint64_t)(uint32_t)c->pad_id;
   h.scalars[6] = c->seed;
   h.scalars[7] = c->hash_key;
   h.scalars[8] = S;
   h.scalars[9] = J;
+  h.scalars[10] = c->G;
   h.source_weight = static_cast<uint32_t *>(d_sw);
   h.source_bp = static_cast<uint16_t *>(d_sbp);
   h.sdb = static_cast<uint32_t *>(d_sdb);
@@ -436,7 +441,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.S = S;
   h.J = J;
   NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, win_start,
-                           c->node_src, c->node_doc, c->offs, T, K, dacc, ubase, digest, st));
+                           c->node_src, c->node_doc, c->offs, T, K, c->seed, c->G, c->err, dacc,
+                           ubase, digest, st));
 
   // ---- 9. read back the summary ------------------------------------------
   std::vector<uint32_t> W_h(J);
@@ -469,6 +475,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   c->B = cfg->B;
   c->K = cfg->max_steps;
   c->flags = cfg->flags;
+  c->G = cfg->window_segment;
   c->S = cfg->n_sources;
   c->J = cfg->n_streams;
   c->n_docs = cfg->n_docs;

@@ -59,6 +59,12 @@ __device__ T block_sum(T v, T *scratch /* [33] */) {
   return r;
 }
 
+// Windows of a stream the horizon can read: its last quota count, rounded up
+// to whole segments when windows are read in a shuffled order within them.
+__device__ __forceinline__ int64_t windows_needed(int32_t rmax, uint32_t G) {
+  return G ? ((int64_t)rmax + G - 1) / G * G : (int64_t)rmax;
+}
+
 // ---------------------------------------------------------------------------
 // doc_offsets must start at >= 0, never decrease, keep every length below
 // 2^31 and end inside the token array.
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(kThreads)
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
-                       const unsigned *ready, unsigned ready_at, uint32_t T,
+                       const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
                        unsigned long long *kept) {
   constexpr uint32_t kGrab = 8;
@@ -366,7 +372,8 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) {
         if (need == ~0ull && *reinterpret_cast<const volatile unsigned *>(ready) >= ready_at) {
           __threadfence();
-          need = (unsigned long long)*reinterpret_cast<const volatile int32_t *>(cum_last + j) * T;
+          need = (unsigned long long)windows_needed(
+                     *reinterpret_cast<const volatile int32_t *>(cum_last + j), G) * T;
         }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
         base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
@@ -422,6 +429,60 @@ __device__ __forceinline__ uint64_t feistel(const uint64_t k[4], uint32_t half, 
     L = nl;
   }
   return (L << half) | R;
+}
+
+// Half width of the balanced Feistel domain for [0, n): bits = max(2,
+// ceil(log2 n)) rounded up to even.
+__device__ __forceinline__ uint32_t feistel_half(uint64_t n) {
+  uint32_t bits = (n <= 1) ? 0u : (uint32_t)(64 - __clzll((long long)(n - 1)));
+  if (bits < 2) bits = 2;
+  bits += bits & 1u;
+  return bits >> 1;
+}
+
+// p in [0, n) -> its image under the keyed network, walked back into [0, n).
+__device__ __forceinline__ uint64_t feistel_walk(const uint64_t k[4], uint64_t n, uint64_t p,
+                                                 int *err) {
+  const uint32_t half = feistel_half(n);
+  const uint64_t mask = (half >= 64) ? ~0ull : ((1ull << half) - 1);
+  uint64_t y = feistel(k, half, mask, p);
+  for (uint32_t it = 0; y >= n; it++) {
+    if (it > (1u << 20)) {
+      set_error(err, kDevWalkLimit);
+      return 0;
+    }
+    y = feistel(k, half, mask, y);
+  }
+  return y;
+}
+
+// Read order of windows: rank r of stream j reads window sG + sigma(r - sG)
+// within its segment s = r / G of min(G, W - sG) windows, sigma keyed by
+// (seed + 1, j, s); G = 0 reads windows in order ("the trainer reads each
+// source's windows of a segment in a random order", NeuronSpark-Trainer
+// README, Concepts).
+__device__ __forceinline__ uint64_t window_of_rank(uint64_t seed, uint32_t j, uint32_t G,
+                                                   uint64_t W, uint64_t r, int *err) {
+  if (G == 0) return r;
+  const uint64_t s = r / G, b = s * G;
+  const uint64_t n = min((uint64_t)G, W - b);
+  uint64_t k[4];
+  const uint64_t ks = splitmix64(seed + 1);
+#pragma unroll
+  for (int q = 0; q < 4; q++)
+    k[q] = splitmix64(ks ^ splitmix64(((uint64_t)j << 40) | (s << 8) | (uint64_t)q));
+  return b + feistel_walk(k, n, r - b, err);
+}
+
+// Row order of an update: slot i holds row rho_k(i), rho_k keyed by
+// (seed + 2, k) over [0, B).
+__device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, uint32_t B,
+                                                uint32_t i, int *err) {
+  uint64_t k[4];
+  const uint64_t ks = splitmix64(seed + 2);
+#pragma unroll
+  for (int q = 0; q < 4; q++) k[q] = splitmix64(ks ^ splitmix64(((uint64_t)step << 8) | q));
+  return (uint32_t)feistel_walk(k, B, i, err);
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -603,19 +664,19 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 // ---------------------------------------------------------------------------
 // Prefix of each stream that the horizon can reach: the shortest run of
 // positions whose kept tokens exceed rmax_j * T (rmax_j = windows the horizon
-// asks of stream j), or the whole stream.  Windows 0..rmax_j - 1 hold at most
+// can read of stream j), or the whole stream.  Windows 0..rmax_j - 1 hold at most
 // rmax_j * T tokens, so at least one piece follows them inside the prefix and
 // their greedy packing is the same as over the whole stream.
 __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
                               const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
-                              const int32_t *__restrict__ cum_last, uint32_t T,
+                              const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
                               uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
   const uint64_t N = e - b;
   const int64_t base = kex[b];
-  const int64_t need = (int64_t)cum_last[j] * (int64_t)T;
+  const int64_t need = windows_needed(cum_last[j], G) * (int64_t)T;
   uint64_t c = N;
   if (kex[e] - base > need) {
     uint64_t lo = 1, hi = N;
@@ -769,24 +830,29 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // The window of every row of every update of the horizon.  Rows of an update
-// are ordered by stream, then by rank: row i belongs to the stream whose row
-// range [rb[k][j], rb[k][j+1]) holds it and takes that stream's window
-// cum[k][j] + (i - rb[k][j]); the window ends where the next one starts.
+// are ordered by stream, then by rank (or shuffled: slot i holds row
+// rho_k(i)): row c belongs to the stream whose row range [rb[k][j],
+// rb[k][j+1]) holds it and takes that stream's rank cum[k][j] + (c -
+// rb[k][j]), which reads window window_of_rank(...); the window ends where the
+// next one starts.
 __global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t *__restrict__ cum,
                                    const uint32_t *__restrict__ W,
                                    const int64_t *__restrict__ wbase,
                                    const int32_t *__restrict__ win_start,
                                    const int32_t *__restrict__ next, uint32_t J, uint32_t B,
-                                   uint32_t K, int2 *__restrict__ row_win) {
+                                   uint32_t K, uint64_t seed, uint32_t G, uint32_t shuffle_rows,
+                                   int2 *__restrict__ row_win, int *err) {
   const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= (uint64_t)K * B) return;
-  const uint32_t k = (uint32_t)(x / B), i = (uint32_t)(x % B);
+  const uint32_t k = (uint32_t)(x / B), slot = (uint32_t)(x % B);
+  const uint32_t i = shuffle_rows ? row_of_slot(seed, k, B, slot, err) : slot;
   const int32_t *rbk = rb + (size_t)k * (J + 1);
   const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)J, (int32_t)i);
   const int64_t r = (int64_t)cum[(size_t)k * J + j] + ((int64_t)i - rbk[j]);
   int2 w = make_int2(-1, -1);
   if (r < (int64_t)W[j]) {
-    const int32_t s = win_start[wbase[j] + r];
+    const uint64_t wi = window_of_rank(seed, (uint32_t)j, G, W[j], (uint64_t)r, err);
+    const int32_t s = win_start[wbase[j] + (int64_t)wi];
     w = make_int2(s, next[s]);
   }
   row_win[x] = w;
@@ -825,18 +891,18 @@ __device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long l
 
 __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
                                      unsigned long long *acc) {
-  const uint64_t n = 10ull + 2ull * h.S + 4ull * h.J;
+  const uint64_t n = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint64_t term = 0;
   if (i < n) {
     uint64_t x;
-    if (i < 10) {
+    if (i < kDigestScalars) {
       x = (i == 3) ? (uint64_t)*valid : h.scalars[i];
-    } else if (i < 10ull + 2ull * h.S) {
-      const uint64_t q = i - 10, s = q >> 1;
+    } else if (i < kDigestScalars + 2ull * h.S) {
+      const uint64_t q = i - kDigestScalars, s = q >> 1;
       x = (q & 1) ? (uint64_t)h.source_bp[s] : (uint64_t)h.source_weight[s];
     } else {
-      const uint64_t q = i - 10 - 2ull * h.S, j = q >> 2;
+      const uint64_t q = i - kDigestScalars - 2ull * h.S, j = q >> 2;
       switch (q & 3) {
         case 0: x = h.sdb[j]; break;
         case 1: x = h.sdb[j + 1]; break;
@@ -880,14 +946,16 @@ __global__ void __launch_bounds__(kThreads)
                           const int64_t *__restrict__ node_src,
                           const int32_t *__restrict__ node_doc, const int64_t *__restrict__ offs,
                           uint32_t T, uint64_t h0, uint32_t J, const uint32_t *valid,
-                          const int64_t *__restrict__ ubase, unsigned long long *acc) {
+                          const int64_t *__restrict__ ubase, const uint32_t *__restrict__ W,
+                          uint64_t seed, uint32_t G, int *err, unsigned long long *acc) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
   const uint64_t U = (uint64_t)(ubase[j + 1] - ubase[j]);
   uint64_t term = 0;
   if (r < U) {
-    const int32_t node = win_start[wbase[j] + r];
+    const uint64_t wi = window_of_rank(seed, j, G, W[j], r, err);
+    const int32_t node = win_start[wbase[j] + (int64_t)wi];
     const int32_t d = node_doc[node];
     const uint64_t chunk = (uint64_t)(node_src[node] - offs[d]) / T;
     const uint64_t x = ((uint64_t)(uint32_t)d << 32) | (chunk & 0xFFFFFFFFull);
@@ -993,14 +1061,14 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               const unsigned *ready, unsigned ready_at, uint32_t T,
+                               const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                                uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept, int n_sms,
                                cudaStream_t st) {
   ++launch_counter();
   hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
-                                                     klen, cum_last, ready, ready_at, T, hash_key,
-                                                     want_heldout, frontier, kept);
+                                                     klen, cum_last, ready, ready_at, T, G,
+                                                     hash_key, want_heldout, frontier, kept);
   return cudaGetLastError();
 }
 
@@ -1043,10 +1111,10 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 }
 
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
-                          const int64_t *pex, const int32_t *cum_last, uint32_t T,
+                          const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
                           uint32_t *cutoff, int64_t *npieces, cudaStream_t st) {
   ++launch_counter();
-  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, cutoff,
+  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G, cutoff,
                                                     npieces);
   return cudaGetLastError();
 }
@@ -1110,11 +1178,11 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
 cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
                                const int64_t *wbase, const int32_t *win_start,
                                const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
-                               int2 *row_win, cudaStream_t st) {
+                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int2 *row_win,
+                               int *err, cudaStream_t st) {
   ++launch_counter();
-  row_windows_kernel<<<blocks_for((uint64_t)K * B), kThreads, 0, st>>>(rb, cum, W, wbase,
-                                                                       win_start, next, J, B, K,
-                                                                       row_win);
+  row_windows_kernel<<<blocks_for((uint64_t)K * B), kThreads, 0, st>>>(
+      rb, cum, W, wbase, win_start, next, J, B, K, seed, G, shuffle_rows, row_win, err);
   return cudaGetLastError();
 }
 
@@ -1138,10 +1206,10 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           const int32_t *cum, const uint32_t *W, SegGrid wg,
                           const int64_t *wbase, const int32_t *win_start,
                           const int64_t *node_src, const int32_t *node_doc,
-                          const int64_t *offs, uint32_t T, uint32_t K,
-                          unsigned long long *acc, int64_t *ubase, uint64_t *digest_out,
-                          cudaStream_t st) {
-  const uint64_t h0 = 10ull + 2ull * h.S + 4ull * h.J;
+                          const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
+                          int *err, unsigned long long *acc, int64_t *ubase,
+                          uint64_t *digest_out, cudaStream_t st) {
+  const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
   ++launch_counter();
   digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
   cudaError_t e = cudaGetLastError();
@@ -1159,7 +1227,7 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
     ++launch_counter();
     digest_windows_kernel<<<wg.n_blocks, kThreads, 0, st>>>(wg, wbase, win_start, node_src,
                                                             node_doc, offs, T, h0, h.J, valid,
-                                                            ubase, acc);
+                                                            ubase, W, seed, G, err, acc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -52,7 +52,7 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
 cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
                                const uint16_t *stream_bp, uint32_t J, uint32_t D0,
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               const unsigned *ready, unsigned ready_at, uint32_t T,
+                               const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                                uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept, int n_sms,
                                cudaStream_t st);
@@ -63,7 +63,7 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 size_t scan_scratch_bytes(uint64_t n);
 // per stream: cutoff c_j, pieces before it, node base; rmax given
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
-                          const int64_t *pex, const int32_t *cum_last, uint32_t T,
+                          const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
                           uint32_t *cutoff, int64_t *npieces, cudaStream_t st);
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st);
@@ -86,19 +86,23 @@ cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_
 cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nodes,
                                  uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
                                  const int64_t *wbase, int32_t *win_start, cudaStream_t st);
-// row_win[k][i] = (first piece, end piece) of the window row i of update k
-// takes, or (-1, -1) when the row lies past the end of its stream.
+// row_win[k][i] = (first piece, end piece) of the window slot i of update k
+// takes, or (-1, -1) when the row lies past the end of its stream; G > 0
+// reads windows in a shuffled order within segments, shuffle_rows shuffles the
+// rows of every update.
 cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
                                const int64_t *wbase, const int32_t *win_start,
                                const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
-                               int2 *row_win, cudaStream_t st);
+                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int2 *row_win,
+                               int *err, cudaStream_t st);
 cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st);
 
 // ---- order digest ---------------------------------------------------------
+constexpr int kDigestScalars = 11;
 struct DigestHeader {
-  uint64_t scalars[10];
+  uint64_t scalars[kDigestScalars];  // T, B, K, valid, flags, pad, seed, key, S, J, G
   const uint32_t *source_weight;  // [S]
   const uint16_t *source_bp;      // [S]
   const uint32_t *sdb;            // [J + 1]
@@ -110,8 +114,8 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           const int32_t *cum, const uint32_t *W, SegGrid wg,
                           const int64_t *wbase, const int32_t *win_start,
                           const int64_t *node_src, const int32_t *node_doc,
-                          const int64_t *offs, uint32_t T, uint32_t K,
-                          unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
+                          const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
+                          int *err, unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
                           uint64_t *digest_out, cudaStream_t st);
 
 // ---- per-step assembly ----------------------------------------------------

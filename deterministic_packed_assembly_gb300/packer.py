@@ -25,15 +25,18 @@ class Packer:
     ``tokens`` (int32), ``doc_offsets`` (int64, n_docs + 1) and ``loss_start``
     (int32 or None) are device tensors that must outlive the packer.  The
     recipe arrays may be numpy arrays or lists.  ``heldout_only`` packs the
-    validation stream (the held-out documents) instead of the training one.
+    validation stream (the held-out documents) instead of the training one;
+    ``window_segment`` > 0 reads each stream's windows in a shuffled order
+    within segments of that many windows; ``shuffle_rows`` shuffles the rows
+    of every update.
     """
 
     def __init__(self, tokens: torch.Tensor, doc_offsets: torch.Tensor,
                  loss_start: Optional[torch.Tensor], *, stream_doc_begin, stream_source,
                  source_weight, stream_weight, source_heldout_bp, T: int, B: int,
                  max_steps: int, seed: int = 0, hash_key: int = 0, drain: bool = False,
-                 pad_id: int = 0, heldout_only: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 pad_id: int = 0, heldout_only: bool = False, window_segment: int = 0,
+                 shuffle_rows: bool = False, stream: Optional[torch.cuda.Stream] = None):
         if not tokens.is_cuda:
             raise ValueError("tokens must be a CUDA tensor")
         assert tokens.dtype == torch.int32 and tokens.is_contiguous()
@@ -84,7 +87,9 @@ class Packer:
         cfg.hash_key = int(hash_key) & ((1 << 64) - 1)
         cfg.B = self.B
         cfg.max_steps = self.max_steps
-        cfg.flags = (L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
+        cfg.flags = ((L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
+                     | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0))
+        cfg.window_segment = int(window_segment)
         cfg.pad_id = int(pad_id)
         cfg.cuda_stream = stream_handle
         cfg.alloc = self._alloc_cb

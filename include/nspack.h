@@ -70,12 +70,16 @@ extern "C" {
  * stratum", NeuronSpark-Trainer README, Concepts).  Same shuffle, packing,
  * quotas and assembly; a source with a held-out rate of 0 has no windows. */
 #define NS_PACK_HELDOUT 2u
+/* Shuffle the rows of every update: slot i holds the row that would otherwise
+ * be row rho_k(i), rho_k a keyed permutation of [0, B) (seed + 2, update k). */
+#define NS_PACK_SHUFFLE_ROWS 4u
 
 /* ---- limits ------------------------------------------------------------- */
 #define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
 #define NS_MAX_SOURCES 1024u
 #define NS_MAX_STRATA_PER_SOURCE 1024u
 #define NS_MAX_STREAMS 65536u
+#define NS_MAX_WINDOW_SEGMENT (1u << 24)
 
 typedef struct ns_pack_ctx ns_pack_ctx;
 
@@ -111,8 +115,14 @@ typedef struct {
   uint64_t hash_key; /* keys the held-out hash (not the seed: same in every line) */
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
-  uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT */
+  uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS */
   int32_t pad_id;    /* token written at padded positions */
+  uint32_t window_segment; /* G > 0: each stream's windows are read in a shuffled
+                              order within segments of G consecutive windows
+                              ("the trainer reads each source's windows of a
+                              segment in a random order", NeuronSpark-Trainer
+                              README, Concepts); 0: in order; at most
+                              NS_MAX_WINDOW_SEGMENT */
   void *cuda_stream; /* cudaStream_t for init and default for the other calls */
   ns_alloc_fn alloc;
   ns_free_fn free;

@@ -59,6 +59,8 @@ class _Config(C.Structure):
         ("B", C.c_uint32), ("max_steps", C.c_uint32), ("drain", C.c_uint32),
         ("pad_id", C.c_int32),
         ("heldout_only", C.c_uint32),
+        ("window_segment", C.c_uint32),
+        ("shuffle_rows", C.c_uint32),
     ]
 
 
@@ -82,6 +84,10 @@ def lib() -> C.CDLL:
         L.or_feistel_round_key.argtypes = [u64, u32, u32]
         L.or_feistel_encrypt.restype = u64
         L.or_feistel_encrypt.argtypes = [vp, u32, u64]
+        L.or_window_of_rank.restype = u64
+        L.or_window_of_rank.argtypes = [u64, u32, u32, u64, u64]
+        L.or_row_of_slot.restype = u32
+        L.or_row_of_slot.argtypes = [u64, u32, u32, u32]
         L.or_feistel_pi.restype = u64
         L.or_feistel_pi.argtypes = [u64, u32, u64, u64]
         L.or_apportion.restype = C.c_int
@@ -151,6 +157,14 @@ def feistel_pi(seed: int, stream: int, n: int, p: int) -> int:
     return lib().or_feistel_pi(seed & M64, stream, n, p)
 
 
+def window_of_rank(seed: int, stream: int, G: int, W: int, r: int) -> int:
+    return lib().or_window_of_rank(seed & M64, stream, G, W, r)
+
+
+def row_of_slot(seed: int, step: int, B: int, i: int) -> int:
+    return lib().or_row_of_slot(seed & M64, step, B, i)
+
+
 def apportion(v: list[int], C_before: list[int], n: int, N: int) -> list[int]:
     vv = np.asarray(v, dtype=np.uint64)
     cc = np.asarray(C_before, dtype=np.int64)
@@ -188,7 +202,8 @@ class Oracle:
     def __init__(self, corpus, *, seed: Optional[int] = None, hash_key: Optional[int] = None,
                  max_steps: Optional[int] = None, drain: Optional[bool] = None,
                  T: Optional[int] = None, B: Optional[int] = None,
-                 pad_id: Optional[int] = None, heldout_only: bool = False):
+                 pad_id: Optional[int] = None, heldout_only: bool = False,
+                 window_segment: int = 0, shuffle_rows: bool = False):
         c = corpus
         self.corpus = c
         self.T = int(T if T is not None else c.T)
@@ -229,6 +244,8 @@ class Oracle:
         cfg.drain = int(bool(drain if drain is not None else c.drain))
         cfg.pad_id = int(pad_id if pad_id is not None else c.pad_id)
         cfg.heldout_only = int(bool(heldout_only))
+        cfg.window_segment = int(window_segment)
+        cfg.shuffle_rows = int(bool(shuffle_rows))
         self._cfg = cfg
         h = C.c_void_p()
         rc = lib().or_build(C.byref(cfg), C.byref(h))

@@ -79,6 +79,9 @@ typedef struct {
   uint32_t drain;
   int32_t pad_id;
   uint32_t heldout_only; /* 1: pack the held-out documents (the validation stream) */
+  uint32_t window_segment; /* G > 0: read each stream's windows in a shuffled order
+                              within segments of G windows; 0: in order */
+  uint32_t shuffle_rows;   /* 1: rows of an update in a shuffled order */
 } or_config;
 
 typedef struct {
@@ -165,6 +168,48 @@ uint64_t or_feistel_pi(uint64_t seed, uint32_t stream, uint64_t n, uint64_t p) {
   uint64_t y = or_feistel_encrypt(key, half, p);
   while (y >= n) y = or_feistel_encrypt(key, half, y);
   return y;
+}
+
+/* ---- the order in which windows and rows are read ----------------------
+ * "The trainer reads each source's windows of a segment in a random order"
+ * (NeuronSpark-Trainer README, Concepts).  With a window segment of G > 0 the
+ * windows of stream j are grouped in segments of G consecutive windows (the
+ * last one shorter); rank r of segment s = r / G reads window
+ * sG + sigma_{j,s}(r - sG), sigma the same keyed Feistel network as the
+ * document shuffle over the segment's length, keyed by (seed + 1, j, s).
+ * With row shuffling, slot i of update k holds the row that would otherwise
+ * be row rho_k(i), rho_k the same network over [0, B) keyed by (seed + 2, k). */
+uint64_t or_window_round_key(uint64_t seed, uint32_t stream, uint64_t segment, uint32_t round) {
+  return or_splitmix64(or_splitmix64(seed + 1) ^
+                       or_splitmix64(((uint64_t)stream << 40) | (segment << 8) | round));
+}
+
+uint64_t or_row_round_key(uint64_t seed, uint32_t step, uint32_t round) {
+  return or_splitmix64(or_splitmix64(seed + 2) ^ or_splitmix64(((uint64_t)step << 8) | round));
+}
+
+static uint64_t walk(const uint64_t key[4], uint64_t n, uint64_t p) {
+  uint32_t half = or_feistel_bits(n) / 2;
+  uint64_t y = or_feistel_encrypt(key, half, p);
+  while (y >= n) y = or_feistel_encrypt(key, half, y);
+  return y;
+}
+
+/* window read by rank r of a stream with W windows */
+uint64_t or_window_of_rank(uint64_t seed, uint32_t stream, uint32_t G, uint64_t W, uint64_t r) {
+  if (G == 0) return r;
+  uint64_t s = r / G, b = s * G;
+  uint64_t n = (W - b < G) ? (W - b) : G;
+  uint64_t key[4];
+  for (uint32_t q = 0; q < 4; q++) key[q] = or_window_round_key(seed, stream, s, q);
+  return b + walk(key, n, r - b);
+}
+
+/* row held by slot i of update k */
+uint32_t or_row_of_slot(uint64_t seed, uint32_t step, uint32_t B, uint32_t i) {
+  uint64_t key[4];
+  for (uint32_t q = 0; q < 4; q++) key[q] = or_row_round_key(seed, step, q);
+  return (uint32_t)walk(key, B, i);
 }
 
 /* ---- per-update apportionment: one level of the quota rule -------------
@@ -368,12 +413,13 @@ static uint64_t build_digest(const or_ctx *x) {
   digest_add(&a, c->B);
   digest_add(&a, c->max_steps);
   digest_add(&a, x->valid_steps);
-  digest_add(&a, (c->drain ? 1u : 0u) | (c->heldout_only ? 2u : 0u));
+  digest_add(&a, (c->drain ? 1u : 0u) | (c->heldout_only ? 2u : 0u) | (c->shuffle_rows ? 4u : 0u));
   digest_add(&a, (uint64_t)(uint32_t)c->pad_id);
   digest_add(&a, c->seed);
   digest_add(&a, c->hash_key);
   digest_add(&a, c->n_sources);
   digest_add(&a, c->n_streams);
+  digest_add(&a, c->window_segment);
   for (uint32_t s = 0; s < c->n_sources; s++) {
     digest_add(&a, c->source_weight[s]);
     digest_add(&a, c->source_heldout_bp[s]);
@@ -391,7 +437,8 @@ static uint64_t build_digest(const or_ctx *x) {
     uint64_t used = (uint64_t)x->cum[(size_t)x->valid_steps * J + j];
     if (used > st->n_windows) used = st->n_windows;
     for (uint64_t r = 0; r < used; r++) {
-      const or_piece *p = &st->pieces[st->win_first[r]];
+      uint64_t w = or_window_of_rank(c->seed, j, c->window_segment, st->n_windows, r);
+      const or_piece *p = &st->pieces[st->win_first[w]];
       digest_add(&a, ((uint64_t)p->doc << 32) | (uint64_t)(p->off / c->T));
     }
   }
@@ -489,7 +536,8 @@ uint64_t or_row_fp(const int32_t *tok, const int32_t *pos, const int32_t *doc,
 }
 
 /* ---- assembly of rows [row0, row1) of update `step` ----------------------
- * Rows are ordered by (source, stratum, rank).  A window's pieces are copied
+ * Rows are ordered by (source, stratum, rank), unless shuffled; a rank reads
+ * its window through the window order above.  A window's pieces are copied
  * in order; pos is the offset inside the piece (0 starts a new sequence);
  * doc is the global document index; mask is 1 iff the token's offset in its
  * document is at or past loss_start; the tail is pad_id / 0 / -1 / 0.  A row
@@ -506,16 +554,18 @@ int or_rows(const or_ctx *x, uint32_t step, uint32_t row0, uint32_t row1, int32_
   for (uint32_t i = row0; i < row1; i++) {
     size_t o = (size_t)(i - row0) * T;
     /* which stream and which of its windows this row takes */
+    uint32_t row = c->shuffle_rows ? or_row_of_slot(c->seed, step, c->B, i) : i;
     uint32_t base = 0, j = 0;
-    while (j < J && i >= base + (uint32_t)x->quota[(size_t)step * J + j]) {
+    while (j < J && row >= base + (uint32_t)x->quota[(size_t)step * J + j]) {
       base += (uint32_t)x->quota[(size_t)step * J + j];
       j++;
     }
-    uint64_t r = (uint64_t)x->cum[(size_t)step * J + j] + (i - base);
+    uint64_t r = (uint64_t)x->cum[(size_t)step * J + j] + (row - base);
     const or_stream *st = &x->streams[j];
     uint32_t t = 0;
     if (r < st->n_windows) {
-      for (uint64_t q = st->win_first[r]; q < st->win_first[r + 1]; q++) {
+      uint64_t w = or_window_of_rank(c->seed, j, c->window_segment, st->n_windows, r);
+      for (uint64_t q = st->win_first[w]; q < st->win_first[w + 1]; q++) {
         const or_piece *p = &st->pieces[q];
         const int32_t *src = c->tokens + c->doc_offsets[p->doc] + p->off;
         int64_t ls = c->loss_start ? c->loss_start[p->doc] : 0;

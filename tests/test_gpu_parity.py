@@ -261,3 +261,31 @@ def test_validation_stream_random_tiny_corpora(case):
     pk = packer_for(c, heldout_only=True)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=2)
+
+
+@pytest.mark.parametrize("name,G,rows", [("c1", 1, False), ("c1", 3, True), ("c3s", 64, False),
+                                         ("c3s", 7, True), ("c5s", 5, True), ("c4s", 0, True)])
+def test_read_order_shuffles(name, G, rows):
+    # windows read in a shuffled order within segments of G, rows of every
+    # update shuffled: both are pure functions of the seed, so any slicing
+    # still gives the oracle's bytes
+    c = make_preset(name)
+    pk = packer_for(c, window_segment=G, shuffle_rows=rows)
+    o = oracle_for(c, window_segment=G, shuffle_rows=rows)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=3)
+    k = o.valid_steps - 1
+    half = c.B // 2
+    compare_steps(pk, o, [k], rows=(half, c.B))
+
+
+@pytest.mark.parametrize("case", range(20))
+def test_read_order_random_tiny_corpora(case):
+    rng = np.random.default_rng(8000 + case)
+    c = _random_case(rng)
+    G = int(rng.choice([0, 1, 2, 3, 9]))
+    rows = bool(rng.integers(0, 2))
+    o = oracle_for(c, window_segment=G, shuffle_rows=rows)
+    pk = packer_for(c, window_segment=G, shuffle_rows=rows)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=2)
