@@ -51,6 +51,11 @@ class ns_pack_config(C.Structure):
         ("flags", C.c_uint32),
         ("pad_id", C.c_int32),
         ("window_segment", C.c_uint32),
+        ("n_pieces", C.c_uint32),
+        ("piece_begin", C.c_void_p),
+        ("piece_B", C.c_void_p),
+        ("piece_source_weight", C.c_void_p),
+        ("piece_stream_weight", C.c_void_p),
         ("cuda_stream", C.c_void_p),
         ("alloc", ns_alloc_fn),
         ("free", ns_free_fn),

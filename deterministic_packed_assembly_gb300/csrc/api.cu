@@ -28,6 +28,7 @@ struct ns_pack_ctx {
   void *user = nullptr;
   int n_sms = 0;
   // host summary
+  std::vector<uint32_t> piece_begin, piece_B;  // the schedule (one piece without one)
   std::vector<uint64_t> windows;
   std::vector<uint8_t> complete;
   uint32_t valid_steps = 0, levels = 0, init_launches = 0;
@@ -127,7 +128,32 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->stream_doc_begin[cfg->n_streams] > cfg->n_docs) return NS_ERR_INVALID_ARG;
   for (uint32_t s = 0; s < cfg->n_sources; s++)
     if (per_source[s] == 0 || per_source[s] > NS_MAX_STRATA_PER_SOURCE) return NS_ERR_INVALID_ARG;
+  if (cfg->n_pieces) {
+    if (!cfg->piece_begin || !cfg->piece_B || !cfg->piece_source_weight ||
+        !cfg->piece_stream_weight)
+      return NS_ERR_INVALID_ARG;
+    if (cfg->n_pieces > cfg->max_steps || cfg->piece_begin[0] != 0) return NS_ERR_INVALID_ARG;
+    for (uint32_t p = 0; p < cfg->n_pieces; p++) {
+      if (p > 0 && cfg->piece_begin[p] <= cfg->piece_begin[p - 1]) return NS_ERR_INVALID_ARG;
+      if (cfg->piece_begin[p] >= cfg->max_steps) return NS_ERR_INVALID_ARG;
+      if (cfg->piece_B[p] == 0 || cfg->piece_B[p] > cfg->B) return NS_ERR_INVALID_ARG;
+      for (uint32_t s = 0; s < cfg->n_sources; s++)
+        if (cfg->piece_source_weight[(size_t)p * cfg->n_sources + s] == 0)
+          return NS_ERR_INVALID_ARG;
+      for (uint32_t j = 0; j < cfg->n_streams; j++)
+        if (cfg->piece_stream_weight[(size_t)p * cfg->n_streams + j] == 0)
+          return NS_ERR_INVALID_ARG;
+    }
+  }
   return NS_OK;
+}
+
+// Rows of update k (the schedule's piece's, or B).
+uint32_t rows_of_step(const ns_pack_ctx *c, uint32_t k) {
+  size_t p = 0;
+  for (size_t q = 0; q < c->piece_begin.size(); q++)
+    if (c->piece_begin[q] <= k) p = q;
+  return c->piece_B[p];
 }
 
 // Block layout of a segmented launch: count[j] items per stream, `per`
@@ -217,6 +243,42 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   if ((rc = upload(a, sbp.data(), sbp.size() * 2, &d_sbp, st))) return rc;
   if ((rc = upload(a, stream_bp.data(), stream_bp.size() * 2, &d_stream_bp, st))) return rc;
   if ((rc = upload(a, src_first.data(), src_first.size() * 4, &d_src_first, st))) return rc;
+  // the schedule: one piece (B, the weights) without one
+  const uint32_t P = cfg->n_pieces ? cfg->n_pieces : 1;
+  std::vector<uint32_t> psw((size_t)P * S), ptw((size_t)P * J);
+  if (cfg->n_pieces) {
+    c->piece_begin.assign(cfg->piece_begin, cfg->piece_begin + P);
+    c->piece_B.assign(cfg->piece_B, cfg->piece_B + P);
+    psw.assign(cfg->piece_source_weight, cfg->piece_source_weight + (size_t)P * S);
+    ptw.assign(cfg->piece_stream_weight, cfg->piece_stream_weight + (size_t)P * J);
+  } else {
+    c->piece_begin.assign(1, 0);
+    c->piece_B.assign(1, c->B);
+    psw = sw;
+    ptw = tw;
+  }
+  void *d_pbegin, *d_pB, *d_psw, *d_ptw;
+  if ((rc = upload(a, c->piece_begin.data(), (size_t)P * 4, &d_pbegin, st))) return rc;
+  if ((rc = upload(a, c->piece_B.data(), (size_t)P * 4, &d_pB, st))) return rc;
+  if ((rc = upload(a, psw.data(), psw.size() * 4, &d_psw, st))) return rc;
+  if ((rc = upload(a, ptw.data(), ptw.size() * 4, &d_ptw, st))) return rc;
+  const nsk::QuotaPieces qp{static_cast<uint32_t *>(d_pbegin), static_cast<uint32_t *>(d_pB),
+                            static_cast<uint32_t *>(d_psw), static_cast<uint32_t *>(d_ptw), P};
+  // the schedule's digest items: count, then per piece begin, B, weights
+  std::vector<uint64_t> piece_items;
+  if (cfg->n_pieces) {
+    piece_items.push_back(P);
+    for (uint32_t p = 0; p < P; p++) {
+      piece_items.push_back(c->piece_begin[p]);
+      piece_items.push_back(c->piece_B[p]);
+      for (uint32_t s2 = 0; s2 < S; s2++) piece_items.push_back(psw[(size_t)p * S + s2]);
+      for (uint32_t j = 0; j < J; j++) piece_items.push_back(ptw[(size_t)p * J + j]);
+    }
+  }
+  void *d_piece_items = nullptr;
+  if (!piece_items.empty() &&
+      (rc = upload(a, piece_items.data(), piece_items.size() * 8, &d_piece_items, st)))
+    return rc;
 
   c->err = a.keep<int>(1);
   NS_ALLOC(c->err);
@@ -241,17 +303,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaEventRecord(side.fork, st));
   NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
   if (S <= 32 && max_strata <= 32) {
-    NS_CK(nsk::launch_quota_warp(static_cast<uint32_t *>(d_sw), S, static_cast<uint32_t *>(d_tw),
-                                 static_cast<uint32_t *>(d_src_first), J, c->B, K, max_strata,
+    NS_CK(nsk::launch_quota_warp(qp, S, static_cast<uint32_t *>(d_src_first), J, K, max_strata,
                                  c->quota, c->cum, ready, side.s));
   } else {
     int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
     NS_ALLOC(src_quota);
-    NS_CK(nsk::launch_quota_sources(static_cast<uint32_t *>(d_sw), S, c->B, K, src_quota,
-                                    side.s));
-    NS_CK(nsk::launch_quota_strata(src_quota, static_cast<uint32_t *>(d_tw),
-                                   static_cast<uint32_t *>(d_src_first), S, J, K, max_strata,
-                                   c->quota, c->cum, ready, side.s));
+    NS_CK(nsk::launch_quota_sources(qp, S, K, src_quota, side.s));
+    NS_CK(nsk::launch_quota_strata(qp, src_quota, static_cast<uint32_t *>(d_src_first), S, J, K,
+                                   max_strata, c->quota, c->cum, ready, side.s));
   }
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
@@ -438,6 +497,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.sdb = static_cast<uint32_t *>(d_sdb);
   h.ssrc = static_cast<uint32_t *>(d_ssrc);
   h.tw = static_cast<uint32_t *>(d_tw);
+  h.piece_items = static_cast<uint64_t *>(d_piece_items);
+  h.n_piece_items = piece_items.size();
   h.S = S;
   h.J = J;
   NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, win_start,
@@ -512,6 +573,9 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   if (row_begin >= row_end || row_end > ctx->B) return NS_ERR_INVALID_ARG;
   if (!out->tokens || !out->pos || !out->doc || !out->mask || !out->row_fp || !out->row_learned)
     return NS_ERR_INVALID_ARG;
+  if ((uint64_t)step0 + n_steps <= ctx->K && ctx->piece_begin.size() > 1)
+    for (uint32_t k = step0; k < step0 + n_steps; k++)
+      if (row_end > rows_of_step(ctx, k)) return NS_ERR_INVALID_ARG;
   const uintptr_t al = reinterpret_cast<uintptr_t>(out->tokens) |
                        reinterpret_cast<uintptr_t>(out->pos) |
                        reinterpret_cast<uintptr_t>(out->doc) | reinterpret_cast<uintptr_t>(out->mask);

@@ -135,28 +135,34 @@ __device__ __forceinline__ int64_t apportion_one(bool act, uint64_t v, uint64_t 
   return a;
 }
 
-// Source level: every update hands out B windows among the sources.
-__global__ void quota_sources_kernel(const uint32_t *__restrict__ sw, uint32_t S, uint32_t B,
-                                     uint32_t K, int32_t *__restrict__ src_quota) {
+// Source level: every update of piece p hands out B_p windows among the
+// sources, with the piece's weights; the rule's counts start again at every
+// piece.
+__global__ void quota_sources_kernel(QuotaPieces q, uint32_t S, uint32_t K,
+                                     int32_t *__restrict__ src_quota) {
   __shared__ __int128 delta[1024];
   __shared__ int64_t scratch[33];
   __shared__ uint64_t uscratch[33];
   const bool act = threadIdx.x < S;
-  const uint64_t v = act ? sw[threadIdx.x] : 0;
-  const uint64_t V = block_sum<uint64_t>(v, uscratch);
-  int64_t C = 0;
-  for (uint32_t k = 0; k < K; k++) {
-    int64_t a = apportion_one(act, v, V, (int64_t)B, (int64_t)(k + 1) * B, C, (int)S, delta,
-                              scratch);
-    if (act) src_quota[(size_t)k * S + threadIdx.x] = (int32_t)a;
-    C += a;
+  for (uint32_t p = 0; p < q.P; p++) {
+    const uint32_t k0 = q.begin[p], k1 = (p + 1 < q.P) ? q.begin[p + 1] : K;
+    const int64_t Bp = q.B[p];
+    const uint64_t v = act ? q.sw[(size_t)p * S + threadIdx.x] : 0;
+    const uint64_t V = block_sum<uint64_t>(v, uscratch);
+    int64_t C = 0;
+    for (uint32_t k = k0; k < k1; k++) {
+      int64_t a = apportion_one(act, v, V, Bp, (int64_t)(k - k0 + 1) * Bp, C, (int)S, delta,
+                                scratch);
+      if (act) src_quota[(size_t)k * S + threadIdx.x] = (int32_t)a;
+      C += a;
+    }
   }
 }
 
 // Stratum level: block s splits source s's windows of every update among its
-// streams; writes the per-stream quota and the counts before each update.
-__global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
-                                    const uint32_t *__restrict__ tw,
+// streams; writes the per-stream quota and the windows each stream has given
+// before each update (which run on across pieces).
+__global__ void quota_strata_kernel(QuotaPieces q, const int32_t *__restrict__ src_quota,
                                     const uint32_t *__restrict__ src_first, uint32_t S,
                                     uint32_t J, uint32_t K, int32_t *__restrict__ quota,
                                     int32_t *__restrict__ cum, unsigned *ready) {
@@ -168,20 +174,25 @@ __global__ void quota_strata_kernel(const int32_t *__restrict__ src_quota,
   const int n_st = (int)(f1 - f0);
   const bool act = (int)threadIdx.x < n_st;
   const uint32_t j = f0 + threadIdx.x;
-  const uint64_t v = act ? tw[j] : 0;
-  const uint64_t V = block_sum<uint64_t>(v, uscratch);
-  int64_t C = 0, Cs = 0;
-  for (uint32_t k = 0; k < K; k++) {
-    const int64_t n = src_quota[(size_t)k * S + s];
-    int64_t a = apportion_one(act, v, V, n, Cs + n, C, n_st, delta, scratch);
-    if (act) {
-      quota[(size_t)k * J + j] = (int32_t)a;
-      cum[(size_t)k * J + j] = (int32_t)C;
+  int64_t Cg = 0;
+  for (uint32_t p = 0; p < q.P; p++) {
+    const uint32_t k0 = q.begin[p], k1 = (p + 1 < q.P) ? q.begin[p + 1] : K;
+    const uint64_t v = act ? q.tw[(size_t)p * J + j] : 0;
+    const uint64_t V = block_sum<uint64_t>(v, uscratch);
+    int64_t C = 0, Cs = 0;
+    for (uint32_t k = k0; k < k1; k++) {
+      const int64_t n = src_quota[(size_t)k * S + s];
+      int64_t a = apportion_one(act, v, V, n, Cs + n, C, n_st, delta, scratch);
+      if (act) {
+        quota[(size_t)k * J + j] = (int32_t)a;
+        cum[(size_t)k * J + j] = (int32_t)Cg;
+      }
+      C += a;
+      Cg += a;
+      Cs += n;
     }
-    C += a;
-    Cs += n;
   }
-  if (act) cum[(size_t)K * J + j] = (int32_t)C;
+  if (act) cum[(size_t)K * J + j] = (int32_t)Cg;
   publish_ready(ready);
 }
 
@@ -216,59 +227,63 @@ __device__ __forceinline__ int warp_rank128(int64_t hi, uint64_t lo, int count, 
 // recipes with at most 32 sources and 32 strata per source: one warp per
 // source replays the source level (identical in every block) and splits its
 // source's windows among the strata.  The shortfalls are carried forward
-// instead of recomputed: at the source level delta_c grows by B v_c - V a_c
+// instead of recomputed: at the source level delta_c grows by B_p v_c - V a_c
 // per update; at the stratum level D_c = Cs v_c - V_s C_c grows by
 // n v_c - V_s a_c, and the source's n is its floor share or one more, so both
-// floors of the strata are computed once.
+// floors of the strata are computed once per piece of the schedule (where
+// every count starts again).
 template <int SMAX, int TMAX>
 __global__ void __launch_bounds__(32)
-    quota_warp_kernel(const uint32_t *__restrict__ sw, uint32_t S,
-                      const uint32_t *__restrict__ tw, const uint32_t *__restrict__ src_first,
-                      uint32_t J, uint32_t B, uint32_t K, int32_t *__restrict__ quota,
+    quota_warp_kernel(QuotaPieces q, uint32_t S, const uint32_t *__restrict__ src_first,
+                      uint32_t J, uint32_t K, int32_t *__restrict__ quota,
                       int32_t *__restrict__ cum, unsigned *ready) {
   const int lane = threadIdx.x;
   const uint32_t s = blockIdx.x;
-  // source level
   const bool act = lane < (int)S;
-  const uint64_t v = act ? sw[lane] : 0;
-  const uint64_t V = warp_sum_u64(v);
-  const int64_t base = act ? (int64_t)(((uint64_t)B * v) / V) : 0;
-  const int64_t R = (int64_t)B - warp_sum_i64(base);
-  const __int128 step_gain = (__int128)B * (__int128)v;
-  __int128 delta = step_gain - (__int128)V * (__int128)base;
-  // stratum level of source s
   const uint32_t f0 = src_first[s];
   const int n_st = (int)(src_first[s + 1] - f0);
   const bool sact = lane < n_st;
-  const uint64_t w = sact ? tw[f0 + lane] : 0;
-  const uint64_t Vs = warp_sum_u64(w);
-  const int64_t bs = __shfl_sync(0xffffffffu, base, (int)s);
-  const int64_t b0 = sact ? (int64_t)(((uint64_t)bs * w) / Vs) : 0;
-  const int64_t b1 = sact ? (int64_t)(((uint64_t)(bs + 1) * w) / Vs) : 0;
-  const int64_t R0 = bs - warp_sum_i64(b0);
-  const int64_t R1 = bs + 1 - warp_sum_i64(b1);
-  __int128 D = 0;
-  int64_t C = 0;
-  for (uint32_t k = 0; k < K; k++) {
-    const int rs = warp_rank128<SMAX>((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
-    const int64_t a = base + ((act && rs < R) ? 1 : 0);
-    delta += step_gain - (__int128)V * (__int128)a;
-    const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
-    const bool lo_share = (n == bs);
-    const int64_t bsel = lo_share ? b0 : b1;
-    const int64_t Rsel = lo_share ? R0 : R1;
-    const __int128 gain = (__int128)n * (__int128)w;
-    const __int128 d2 = D + gain - (__int128)Vs * (__int128)bsel;
-    const int rt = warp_rank128<TMAX>((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
-    const int64_t a2 = bsel + ((sact && rt < Rsel) ? 1 : 0);
-    if (sact) {
-      quota[(size_t)k * J + f0 + lane] = (int32_t)a2;
-      cum[(size_t)k * J + f0 + lane] = (int32_t)C;
+  int64_t Cg = 0;  // windows this lane's stream has given (runs on across pieces)
+  for (uint32_t p = 0; p < q.P; p++) {
+    const uint32_t k0 = q.begin[p], k1 = (p + 1 < q.P) ? q.begin[p + 1] : K;
+    const uint64_t Bp = q.B[p];
+    // source level
+    const uint64_t v = act ? q.sw[(size_t)p * S + lane] : 0;
+    const uint64_t V = warp_sum_u64(v);
+    const int64_t base = act ? (int64_t)((Bp * v) / V) : 0;
+    const int64_t R = (int64_t)Bp - warp_sum_i64(base);
+    const __int128 step_gain = (__int128)Bp * (__int128)v;
+    __int128 delta = step_gain - (__int128)V * (__int128)base;
+    // stratum level of source s
+    const uint64_t w = sact ? q.tw[(size_t)p * J + f0 + lane] : 0;
+    const uint64_t Vs = warp_sum_u64(w);
+    const int64_t bs = __shfl_sync(0xffffffffu, base, (int)s);
+    const int64_t b0 = sact ? (int64_t)(((uint64_t)bs * w) / Vs) : 0;
+    const int64_t b1 = sact ? (int64_t)(((uint64_t)(bs + 1) * w) / Vs) : 0;
+    const int64_t R0 = bs - warp_sum_i64(b0);
+    const int64_t R1 = bs + 1 - warp_sum_i64(b1);
+    __int128 D = 0;
+    for (uint32_t k = k0; k < k1; k++) {
+      const int rs = warp_rank128<SMAX>((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
+      const int64_t a = base + ((act && rs < R) ? 1 : 0);
+      delta += step_gain - (__int128)V * (__int128)a;
+      const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
+      const bool lo_share = (n == bs);
+      const int64_t bsel = lo_share ? b0 : b1;
+      const int64_t Rsel = lo_share ? R0 : R1;
+      const __int128 gain = (__int128)n * (__int128)w;
+      const __int128 d2 = D + gain - (__int128)Vs * (__int128)bsel;
+      const int rt = warp_rank128<TMAX>((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
+      const int64_t a2 = bsel + ((sact && rt < Rsel) ? 1 : 0);
+      if (sact) {
+        quota[(size_t)k * J + f0 + lane] = (int32_t)a2;
+        cum[(size_t)k * J + f0 + lane] = (int32_t)Cg;
+      }
+      Cg += a2;
+      D += gain - (__int128)Vs * (__int128)a2;
     }
-    C += a2;
-    D += gain - (__int128)Vs * (__int128)a2;
   }
-  if (sact) cum[(size_t)K * J + f0 + lane] = (int32_t)C;
+  if (sact) cum[(size_t)K * J + f0 + lane] = (int32_t)Cg;
   publish_ready(ready);
 }
 
@@ -845,8 +860,13 @@ __global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t
   const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= (uint64_t)K * B) return;
   const uint32_t k = (uint32_t)(x / B), slot = (uint32_t)(x % B);
-  const uint32_t i = shuffle_rows ? row_of_slot(seed, k, B, slot, err) : slot;
   const int32_t *rbk = rb + (size_t)k * (J + 1);
+  const uint32_t Bk = (uint32_t)rbk[J];  // rows of this update (a schedule may vary them)
+  if (slot >= Bk) {
+    row_win[x] = make_int2(-1, -1);
+    return;
+  }
+  const uint32_t i = shuffle_rows ? row_of_slot(seed, k, Bk, slot, err) : slot;
   const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)J, (int32_t)i);
   const int64_t r = (int64_t)cum[(size_t)k * J + j] + ((int64_t)i - rbk[j]);
   int2 w = make_int2(-1, -1);
@@ -891,7 +911,8 @@ __device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long l
 
 __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
                                      unsigned long long *acc) {
-  const uint64_t n = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
+  const uint64_t n_fixed = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
+  const uint64_t n = n_fixed + h.n_piece_items;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint64_t term = 0;
   if (i < n) {
@@ -901,6 +922,8 @@ __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
     } else if (i < kDigestScalars + 2ull * h.S) {
       const uint64_t q = i - kDigestScalars, s = q >> 1;
       x = (q & 1) ? (uint64_t)h.source_bp[s] : (uint64_t)h.source_weight[s];
+    } else if (i >= n_fixed) {
+      x = h.piece_items[i - n_fixed];
     } else {
       const uint64_t q = i - kDigestScalars - 2ull * h.S, j = q >> 2;
       switch (q & 3) {
@@ -998,56 +1021,47 @@ static unsigned round_warps(uint32_t n) {
   return t < 32 ? 32 : t;
 }
 
-cudaError_t launch_quota_sources(const uint32_t *sw, uint32_t S, uint32_t B, uint32_t K,
-                                 int32_t *src_quota, cudaStream_t st) {
+cudaError_t launch_quota_sources(QuotaPieces q, uint32_t S, uint32_t K, int32_t *src_quota,
+                                 cudaStream_t st) {
   ++launch_counter();
-  quota_sources_kernel<<<1, round_warps(S), 0, st>>>(sw, S, B, K, src_quota);
+  quota_sources_kernel<<<1, round_warps(S), 0, st>>>(q, S, K, src_quota);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *tw,
+cudaError_t launch_quota_strata(QuotaPieces q, const int32_t *src_quota,
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st) {
   ++launch_counter();
-  quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(src_quota, tw, src_first, S, J, K,
+  quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(q, src_quota, src_first, S, J, K,
                                                              quota, cum, ready);
   return cudaGetLastError();
 }
 
 template <int SMAX>
-static void launch_quota_warp_s(const uint32_t *sw, uint32_t S, const uint32_t *tw,
-                                const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
-                                uint32_t max_strata, int32_t *quota, int32_t *cum,
+static void launch_quota_warp_s(QuotaPieces q, uint32_t S, const uint32_t *src_first, uint32_t J,
+                                uint32_t K, uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st) {
   if (max_strata <= 4)
-    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
-                                                 ready);
+    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
   else if (max_strata <= 8)
-    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
-                                                 ready);
+    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
   else
-    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(sw, S, tw, src_first, J, B, K, quota, cum,
-                                                  ready);
+    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
 }
 
-cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
-                              const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
-                              uint32_t max_strata, int32_t *quota, int32_t *cum,
+cudaError_t launch_quota_warp(QuotaPieces q, uint32_t S, const uint32_t *src_first, uint32_t J,
+                              uint32_t K, uint32_t max_strata, int32_t *quota, int32_t *cum,
                               unsigned *ready, cudaStream_t st) {
   ++launch_counter();
   if (S <= 4)
-    launch_quota_warp_s<4>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
-                            st);
+    launch_quota_warp_s<4>(q, S, src_first, J, K, max_strata, quota, cum, ready, st);
   else if (S <= 8)
-    launch_quota_warp_s<8>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
-                            st);
+    launch_quota_warp_s<8>(q, S, src_first, J, K, max_strata, quota, cum, ready, st);
   else if (S <= 16)
-    launch_quota_warp_s<16>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
-                            st);
+    launch_quota_warp_s<16>(q, S, src_first, J, K, max_strata, quota, cum, ready, st);
   else
-    launch_quota_warp_s<32>(sw, S, tw, src_first, J, B, K, max_strata, quota, cum, ready,
-                            st);
+    launch_quota_warp_s<32>(q, S, src_first, J, K, max_strata, quota, cum, ready, st);
   return cudaGetLastError();
 }
 
@@ -1209,7 +1223,7 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
                           int *err, unsigned long long *acc, int64_t *ubase,
                           uint64_t *digest_out, cudaStream_t st) {
-  const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
+  const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
   ++launch_counter();
   digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
   cudaError_t e = cudaGetLastError();

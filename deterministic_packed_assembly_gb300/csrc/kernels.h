@@ -24,18 +24,27 @@ struct SegGrid {
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
                                     int *err, cudaStream_t st);
 cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st);
-cudaError_t launch_quota_sources(const uint32_t *source_weight, uint32_t S, uint32_t B,
-                                 uint32_t K, int32_t *src_quota, cudaStream_t st);
+// The schedule on the device: piece p covers updates [begin[p], begin[p+1])
+// (the last one up to K) with B[p] rows per update and weights sw[p][S],
+// tw[p][J]; a recipe without a schedule is one piece.
+struct QuotaPieces {
+  const uint32_t *begin;
+  const uint32_t *B;
+  const uint32_t *sw;
+  const uint32_t *tw;
+  uint32_t P;
+};
+cudaError_t launch_quota_sources(QuotaPieces q, uint32_t S, uint32_t K, int32_t *src_quota,
+                                 cudaStream_t st);
 // Every quota block adds 1 to *ready (if not null) once its streams' last
 // table row is written.
-cudaError_t launch_quota_strata(const int32_t *src_quota, const uint32_t *stream_weight,
+cudaError_t launch_quota_strata(QuotaPieces q, const int32_t *src_quota,
                                 const uint32_t *src_first, uint32_t S, uint32_t J, uint32_t K,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st);
 // Both levels in one kernel when n_sources <= 32 and every source has <= 32 strata.
-cudaError_t launch_quota_warp(const uint32_t *sw, uint32_t S, const uint32_t *tw,
-                              const uint32_t *src_first, uint32_t J, uint32_t B, uint32_t K,
-                              uint32_t max_strata, int32_t *quota, int32_t *cum,
+cudaError_t launch_quota_warp(QuotaPieces q, uint32_t S, const uint32_t *src_first, uint32_t J,
+                              uint32_t K, uint32_t max_strata, int32_t *quota, int32_t *cum,
                               unsigned *ready, cudaStream_t st);
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st);
@@ -108,6 +117,8 @@ struct DigestHeader {
   const uint32_t *sdb;            // [J + 1]
   const uint32_t *ssrc;           // [J]
   const uint32_t *tw;             // [J]
+  const uint64_t *piece_items;    // the schedule's items (none without one)
+  uint64_t n_piece_items;
   uint32_t S, J;
 };
 cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const int32_t *quota,

@@ -91,11 +91,13 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
   }
   const bool one_warp = S <= 32 && max_strata <= 32;
   // scratch layout: source weights | stream weights | source -> first stream
-  // | (beyond one warp) sources' windows per update
+  // | the horizon as one piece (begin 0, B) | (beyond one warp) sources'
+  // windows per update
   const size_t o_sw = 0;
   const size_t o_tw = o_sw + round256((size_t)S * 4);
   const size_t o_sf = o_tw + round256((size_t)J * 4);
-  const size_t o_sq = o_sf + round256((size_t)(S + 1) * 4);
+  const size_t o_pc = o_sf + round256((size_t)(S + 1) * 4);  // one piece: begin 0, B
+  const size_t o_sq = o_pc + 256;
   const size_t need = o_sq + (one_warp ? 0 : round256((size_t)K * S * 4));
   if (need > NS_NOALLOC_SCRATCH_BYTES) return NS_ERR_INVALID_ARG;
 
@@ -106,24 +108,27 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
   uint32_t *d_sw = reinterpret_cast<uint32_t *>(scratch + o_sw);
   uint32_t *d_tw = reinterpret_cast<uint32_t *>(scratch + o_tw);
   uint32_t *d_sf = reinterpret_cast<uint32_t *>(scratch + o_sf);
+  uint32_t *d_pc = reinterpret_cast<uint32_t *>(scratch + o_pc);
+  const uint32_t piece[2] = {0, B};
   if (cudaMemcpyAsync(d_sw, source_weight, (size_t)S * 4, cudaMemcpyHostToDevice, st) !=
           cudaSuccess ||
       cudaMemcpyAsync(d_tw, stream_weight, (size_t)J * 4, cudaMemcpyHostToDevice, st) !=
           cudaSuccess ||
       cudaMemcpyAsync(d_sf, src_first.data(), (size_t)(S + 1) * 4, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess) {
+          cudaSuccess ||
+      cudaMemcpyAsync(d_pc, piece, sizeof(piece), cudaMemcpyHostToDevice, st) != cudaSuccess) {
     cudaGetLastError();
     return NS_ERR_CUDA;
   }
+  const nsk::QuotaPieces qp{d_pc, d_pc + 1, d_sw, d_tw, 1};
   cudaError_t e;
   if (one_warp) {
-    e = nsk::launch_quota_warp(d_sw, S, d_tw, d_sf, J, B, K, max_strata, quota_dev, cum_dev,
-                               nullptr, st);
+    e = nsk::launch_quota_warp(qp, S, d_sf, J, K, max_strata, quota_dev, cum_dev, nullptr, st);
   } else {
     int32_t *d_sq = reinterpret_cast<int32_t *>(scratch + o_sq);
-    e = nsk::launch_quota_sources(d_sw, S, B, K, d_sq, st);
+    e = nsk::launch_quota_sources(qp, S, K, d_sq, st);
     if (e == cudaSuccess)
-      e = nsk::launch_quota_strata(d_sq, d_tw, d_sf, S, J, K, max_strata, quota_dev, cum_dev,
+      e = nsk::launch_quota_strata(qp, d_sq, d_sf, S, J, K, max_strata, quota_dev, cum_dev,
                                    nullptr, st);
   }
   if (e != cudaSuccess) {

@@ -28,7 +28,9 @@ class Packer:
     validation stream (the held-out documents) instead of the training one;
     ``window_segment`` > 0 reads each stream's windows in a shuffled order
     within segments of that many windows; ``shuffle_rows`` shuffles the rows
-    of every update.
+    of every update; ``schedule`` (a list of ``dict(begin, B, source_weight,
+    stream_weight)``) gives pieces of the horizon their own rows per update
+    and weights.
     """
 
     def __init__(self, tokens: torch.Tensor, doc_offsets: torch.Tensor,
@@ -36,7 +38,8 @@ class Packer:
                  source_weight, stream_weight, source_heldout_bp, T: int, B: int,
                  max_steps: int, seed: int = 0, hash_key: int = 0, drain: bool = False,
                  pad_id: int = 0, heldout_only: bool = False, window_segment: int = 0,
-                 shuffle_rows: bool = False, stream: Optional[torch.cuda.Stream] = None):
+                 shuffle_rows: bool = False, schedule: Optional[list] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
         if not tokens.is_cuda:
             raise ValueError("tokens must be a CUDA tensor")
         assert tokens.dtype == torch.int32 and tokens.is_contiguous()
@@ -90,6 +93,17 @@ class Packer:
         cfg.flags = ((L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
                      | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0))
         cfg.window_segment = int(window_segment)
+        self.schedule = schedule
+        if schedule:
+            pieces = [np.asarray([int(p["begin"]) for p in schedule], np.uint32),
+                      np.asarray([int(p["B"]) for p in schedule], np.uint32),
+                      np.ascontiguousarray([p["source_weight"] for p in schedule], np.uint32),
+                      np.ascontiguousarray([p["stream_weight"] for p in schedule], np.uint32)]
+            self._tables += pieces
+            cfg.n_pieces = pieces[0].size
+            cfg.piece_begin, cfg.piece_B = pieces[0].ctypes.data, pieces[1].ctypes.data
+            cfg.piece_source_weight = pieces[2].ctypes.data
+            cfg.piece_stream_weight = pieces[3].ctypes.data
         cfg.pad_id = int(pad_id)
         cfg.cuda_stream = stream_handle
         cfg.alloc = self._alloc_cb
@@ -120,6 +134,12 @@ class Packer:
         kw.update(overrides)
         return cls(tok, off, ls, **kw)
 
+    def rows_of_step(self, step: int) -> int:
+        """Rows of update ``step`` (B, or the schedule's piece's)."""
+        if not self.schedule:
+            return self.B
+        return int([p["B"] for p in self.schedule if p["begin"] <= step][-1])
+
     # ---- outputs -----------------------------------------------------------
     def empty_out(self, n_steps: int = 1, n_rows: Optional[int] = None) -> dict:
         n_rows = self.B if n_rows is None else n_rows
@@ -147,7 +167,7 @@ class Packer:
              out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
         """Assemble rows ``rows = (begin, end)`` of updates [step0, step0 +
         n_steps) into ``out`` (allocated if None); asynchronous."""
-        r0, r1 = (0, self.B) if rows is None else rows
+        r0, r1 = (0, self.rows_of_step(step0)) if rows is None else rows
         if out is None:
             out = self.empty_out(n_steps, r1 - r0)
         st = (stream or self.stream).cuda_stream

@@ -123,6 +123,21 @@ typedef struct {
                               segment in a random order", NeuronSpark-Trainer
                               README, Concepts); 0: in order; at most
                               NS_MAX_WINDOW_SEGMENT */
+  /* Schedule (host, copied): pieces of the horizon with their own rows per
+   * update and weights -- an append-only mixture schedule and a batch-size
+   * ramp (NeuronSpark-Trainer README, Concepts and Training; Zephon's work
+   * source changing the weights during a run).  Piece p covers updates
+   * [piece_begin[p], piece_begin[p+1]), the last one up to max_steps.  The
+   * quota rule's counts start again at every piece; the windows each stream
+   * has given run on.  n_pieces 0: one piece of B rows with source_weight and
+   * stream_weight.  With a schedule, B is the largest piece_B (the row stride
+   * of the context's tables) and a call may only ask for rows every update it
+   * covers has. */
+  uint32_t n_pieces;                   /* 0 .. max_steps */
+  const uint32_t *piece_begin;         /* [n_pieces], [0] == 0, increasing, < max_steps */
+  const uint32_t *piece_B;             /* [n_pieces], 1 .. B */
+  const uint32_t *piece_source_weight; /* [n_pieces][n_sources], > 0 */
+  const uint32_t *piece_stream_weight; /* [n_pieces][n_streams], > 0 */
   void *cuda_stream; /* cudaStream_t for init and default for the other calls */
   ns_alloc_fn alloc;
   ns_free_fn free;
@@ -167,7 +182,8 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out);
  * kernel launch.  The bytes of every row are the same whatever the row range
  * or the step batching.  Errors: INVALID_ARG (n_steps == 0, empty or out-of-
  * range rows, NULL or misaligned outputs), HORIZON (step0 + n_steps >
- * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA. */
+ * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA.  With a
+ * schedule, row_end may not exceed the rows of any update of the call. */
 int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,
                  uint32_t row_end, const ns_pack_out *out, void *cuda_stream);
 

@@ -61,6 +61,9 @@ class _Config(C.Structure):
         ("heldout_only", C.c_uint32),
         ("window_segment", C.c_uint32),
         ("shuffle_rows", C.c_uint32),
+        ("n_pieces", C.c_uint32),
+        ("piece_begin", C.c_void_p), ("piece_B", C.c_void_p),
+        ("piece_source_weight", C.c_void_p), ("piece_stream_weight", C.c_void_p),
     ]
 
 
@@ -203,7 +206,8 @@ class Oracle:
                  max_steps: Optional[int] = None, drain: Optional[bool] = None,
                  T: Optional[int] = None, B: Optional[int] = None,
                  pad_id: Optional[int] = None, heldout_only: bool = False,
-                 window_segment: int = 0, shuffle_rows: bool = False):
+                 window_segment: int = 0, shuffle_rows: bool = False,
+                 schedule: Optional[list] = None):
         c = corpus
         self.corpus = c
         self.T = int(T if T is not None else c.T)
@@ -246,6 +250,16 @@ class Oracle:
         cfg.heldout_only = int(bool(heldout_only))
         cfg.window_segment = int(window_segment)
         cfg.shuffle_rows = int(bool(shuffle_rows))
+        self.schedule = schedule
+        if schedule:
+            pb = np.asarray([int(p["begin"]) for p in schedule], np.uint32)
+            pB = np.asarray([int(p["B"]) for p in schedule], np.uint32)
+            psw = np.ascontiguousarray([p["source_weight"] for p in schedule], dtype=np.uint32)
+            ptw = np.ascontiguousarray([p["stream_weight"] for p in schedule], dtype=np.uint32)
+            self._keep += [pb, pB, psw, ptw]
+            cfg.n_pieces = pb.size
+            cfg.piece_begin, cfg.piece_B = _ptr(pb), _ptr(pB)
+            cfg.piece_source_weight, cfg.piece_stream_weight = _ptr(psw), _ptr(ptw)
         self._cfg = cfg
         h = C.c_void_p()
         rc = lib().or_build(C.byref(cfg), C.byref(h))
@@ -300,10 +314,16 @@ class Oracle:
         lib().or_get_quota(self._h, _ptr(q), _ptr(cum), _ptr(sq))
         return q, cum, sq
 
+    def rows_of_step(self, step: int) -> int:
+        """Rows of update ``step`` (B, or the schedule's piece's)."""
+        if not self.schedule:
+            return self.B
+        return int([p["B"] for p in self.schedule if p["begin"] <= step][-1])
+
     def rows(self, step: int, row0: int = 0, row1: Optional[int] = None) -> dict:
         """Rows [row0, row1) of update ``step`` as numpy arrays."""
         if row1 is None:
-            row1 = self.B
+            row1 = self.rows_of_step(step)
         n = max(row1 - row0, 0)
         T = self.T
         out = dict(tokens=np.zeros((n, T), np.int32), pos=np.zeros((n, T), np.int32),

@@ -82,6 +82,13 @@ typedef struct {
   uint32_t window_segment; /* G > 0: read each stream's windows in a shuffled order
                               within segments of G windows; 0: in order */
   uint32_t shuffle_rows;   /* 1: rows of an update in a shuffled order */
+  /* schedule: pieces [begin_p, begin_{p+1}) of the horizon with their own
+     rows per update and weights; 0 pieces: one piece (B and the weights above) */
+  uint32_t n_pieces;
+  const uint32_t *piece_begin;         /* [n_pieces], [0] == 0, increasing */
+  const uint32_t *piece_B;             /* [n_pieces], 1..B */
+  const uint32_t *piece_source_weight; /* [n_pieces][n_sources] */
+  const uint32_t *piece_stream_weight; /* [n_pieces][n_streams] */
 } or_config;
 
 typedef struct {
@@ -254,6 +261,28 @@ int or_apportion(uint32_t n_children, const uint64_t *v, const int64_t *C,
   return OR_OK;
 }
 
+/* ---- the schedule ------------------------------------------------------- */
+static uint32_t piece_of(const or_config *c, uint32_t k) {
+  uint32_t p = 0;
+  for (uint32_t q = 0; q < c->n_pieces; q++)
+    if (c->piece_begin[q] <= k) p = q;
+  return p;
+}
+static uint32_t piece_begin(const or_config *c, uint32_t p) {
+  return c->n_pieces ? c->piece_begin[p] : 0;
+}
+static uint32_t rows_of_piece(const or_config *c, uint32_t p) {
+  return c->n_pieces ? c->piece_B[p] : c->B;
+}
+static uint64_t source_w(const or_config *c, uint32_t p, uint32_t s) {
+  return c->n_pieces ? c->piece_source_weight[(size_t)p * c->n_sources + s] : c->source_weight[s];
+}
+static uint64_t stream_w(const or_config *c, uint32_t p, uint32_t j) {
+  return c->n_pieces ? c->piece_stream_weight[(size_t)p * c->n_streams + j] : c->stream_weight[j];
+}
+/* rows of update k */
+uint32_t or_rows_of_step(const or_config *c, uint32_t k) { return rows_of_piece(c, piece_of(c, k)); }
+
 /* ---- checks of the recipe and of the corpus ----------------------------- */
 static int check_config(const or_config *c) {
   if (!c || !c->tokens || !c->doc_offsets || !c->stream_doc_begin || !c->stream_source ||
@@ -278,6 +307,21 @@ static int check_config(const or_config *c) {
     int found = 0;
     for (uint32_t j = 0; j < c->n_streams; j++) found |= (c->stream_source[j] == s);
     if (!found) return OR_ERR_INVALID_ARG;
+  }
+  /* the schedule: pieces start at 0, in increasing order, inside the horizon */
+  if (c->n_pieces) {
+    if (!c->piece_begin || !c->piece_B || !c->piece_source_weight || !c->piece_stream_weight)
+      return OR_ERR_INVALID_ARG;
+    if (c->n_pieces > c->max_steps || c->piece_begin[0] != 0) return OR_ERR_INVALID_ARG;
+    for (uint32_t p = 0; p < c->n_pieces; p++) {
+      if (p > 0 && c->piece_begin[p] <= c->piece_begin[p - 1]) return OR_ERR_INVALID_ARG;
+      if (c->piece_begin[p] >= c->max_steps) return OR_ERR_INVALID_ARG;
+      if (c->piece_B[p] == 0 || c->piece_B[p] > c->B) return OR_ERR_INVALID_ARG;
+      for (uint32_t s = 0; s < c->n_sources; s++)
+        if (c->piece_source_weight[(size_t)p * c->n_sources + s] == 0) return OR_ERR_INVALID_ARG;
+      for (uint32_t j = 0; j < c->n_streams; j++)
+        if (c->piece_stream_weight[(size_t)p * c->n_streams + j] == 0) return OR_ERR_INVALID_ARG;
+    }
   }
   /* the corpus: offsets start in range, never decrease, end inside the tokens */
   if (c->doc_offsets[0] < 0) return OR_ERR_BAD_INPUT;
@@ -346,7 +390,12 @@ static int pack_stream(or_ctx *x, uint32_t j) {
   return OR_OK;
 }
 
-/* ---- quotas for every update: sources first, then strata of each source -- */
+/* ---- quotas for every update: sources first, then strata of each source --
+ * A schedule splits the horizon into pieces with their own weights and rows
+ * per update (an append-only mixture schedule, a batch-size ramp): the rule's
+ * counts (N, and every child's C) start again from 0 at each piece, while the
+ * windows each stream has given (cum) run on across pieces.  Without a
+ * schedule the whole horizon is one piece. */
 static int build_quotas(or_ctx *x) {
   const or_config *c = &x->cfg;
   uint32_t S = c->n_sources, J = c->n_streams, K = c->max_steps;
@@ -354,32 +403,43 @@ static int build_quotas(or_ctx *x) {
   x->cum = (int64_t *)calloc((size_t)(K + 1) * J, sizeof(int64_t));
   x->src_quota = (int64_t *)calloc((size_t)K * S, sizeof(int64_t));
   uint64_t *vs = (uint64_t *)malloc(sizeof(uint64_t) * S);
-  int64_t *Cs = (int64_t *)calloc(S, sizeof(int64_t));
+  int64_t *Cs = (int64_t *)calloc(S, sizeof(int64_t));      /* per piece */
+  int64_t *Cj = (int64_t *)calloc(J, sizeof(int64_t));      /* per piece */
   uint64_t *vt = (uint64_t *)malloc(sizeof(uint64_t) * J);
   int64_t *Ct = (int64_t *)malloc(sizeof(int64_t) * J);
   int64_t *at = (int64_t *)malloc(sizeof(int64_t) * J);
   int rc = OR_OK;
-  if (!x->quota || !x->cum || !x->src_quota || !vs || !Cs || !vt || !Ct || !at) {
+  if (!x->quota || !x->cum || !x->src_quota || !vs || !Cs || !Cj || !vt || !Ct || !at) {
     rc = OR_ERR_OOM;
     goto done;
   }
-  for (uint32_t s = 0; s < S; s++) vs[s] = c->source_weight[s];
   for (uint32_t k = 0; k < K; k++) {
+    uint32_t p = piece_of(c, k);
+    uint32_t k0 = piece_begin(c, p);
+    int64_t Bk = rows_of_piece(c, p);
+    if (k == k0) {
+      memset(Cs, 0, sizeof(int64_t) * S);
+      memset(Cj, 0, sizeof(int64_t) * J);
+    }
+    for (uint32_t s = 0; s < S; s++) vs[s] = source_w(c, p, s);
     int64_t *as = x->src_quota + (size_t)k * S;
-    rc = or_apportion(S, vs, Cs, (int64_t)c->B, (int64_t)(k + 1) * c->B, as);
+    rc = or_apportion(S, vs, Cs, Bk, (int64_t)(k - k0 + 1) * Bk, as);
     if (rc) goto done;
     for (uint32_t s = 0; s < S; s++) {
       uint32_t n_st = 0, j0 = 0;
       for (uint32_t j = 0; j < J; j++) {
         if (c->stream_source[j] != s) continue;
         if (n_st == 0) j0 = j;
-        vt[n_st] = c->stream_weight[j];
-        Ct[n_st] = x->cum[(size_t)k * J + j];
+        vt[n_st] = stream_w(c, p, j);
+        Ct[n_st] = Cj[j];
         n_st++;
       }
       rc = or_apportion(n_st, vt, Ct, as[s], Cs[s] + as[s], at);
       if (rc) goto done;
-      for (uint32_t t = 0; t < n_st; t++) x->quota[(size_t)k * J + j0 + t] = at[t];
+      for (uint32_t t = 0; t < n_st; t++) {
+        x->quota[(size_t)k * J + j0 + t] = at[t];
+        Cj[j0 + t] += at[t];
+      }
       Cs[s] += as[s];
     }
     for (uint32_t j = 0; j < J; j++)
@@ -388,6 +448,7 @@ static int build_quotas(or_ctx *x) {
 done:
   free(vs);
   free(Cs);
+  free(Cj);
   free(vt);
   free(Ct);
   free(at);
@@ -429,6 +490,15 @@ static uint64_t build_digest(const or_ctx *x) {
     digest_add(&a, c->stream_doc_begin[j + 1]);
     digest_add(&a, c->stream_source[j]);
     digest_add(&a, c->stream_weight[j]);
+  }
+  if (c->n_pieces) {
+    digest_add(&a, c->n_pieces);
+    for (uint32_t p = 0; p < c->n_pieces; p++) {
+      digest_add(&a, c->piece_begin[p]);
+      digest_add(&a, c->piece_B[p]);
+      for (uint32_t s = 0; s < c->n_sources; s++) digest_add(&a, source_w(c, p, s));
+      for (uint32_t j = 0; j < J; j++) digest_add(&a, stream_w(c, p, j));
+    }
   }
   for (uint32_t k = 0; k < x->valid_steps; k++)
     for (uint32_t j = 0; j < J; j++) digest_add(&a, (uint64_t)x->quota[(size_t)k * J + j]);
@@ -548,13 +618,14 @@ int or_rows(const or_ctx *x, uint32_t step, uint32_t row0, uint32_t row1, int32_
             int32_t *row_learned) {
   const or_config *c = &x->cfg;
   uint32_t J = c->n_streams, T = c->T;
-  if (row0 >= row1 || row1 > c->B) return OR_ERR_INVALID_ARG;
   if (step >= c->max_steps) return OR_ERR_HORIZON;
+  const uint32_t Bk = or_rows_of_step(c, step);
+  if (row0 >= row1 || row1 > Bk) return OR_ERR_INVALID_ARG;
   if (step >= x->valid_steps) return OR_ERR_EXHAUSTED;
   for (uint32_t i = row0; i < row1; i++) {
     size_t o = (size_t)(i - row0) * T;
     /* which stream and which of its windows this row takes */
-    uint32_t row = c->shuffle_rows ? or_row_of_slot(c->seed, step, c->B, i) : i;
+    uint32_t row = c->shuffle_rows ? or_row_of_slot(c->seed, step, Bk, i) : i;
     uint32_t base = 0, j = 0;
     while (j < J && row >= base + (uint32_t)x->quota[(size_t)step * J + j]) {
       base += (uint32_t)x->quota[(size_t)step * J + j];

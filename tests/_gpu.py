@@ -41,12 +41,13 @@ def compare_steps(pk: Packer, o: oracle.Oracle, steps, launch: int = 1, rows=Non
     """Assemble `steps` (consecutive runs batched `launch` at a time) and
     compare every element with the oracle."""
     steps = list(steps)
-    r0, r1 = (0, pk.B) if rows is None else rows
     i = 0
     while i < len(steps):
         s0 = steps[i]
+        r0, r1 = (0, pk.rows_of_step(s0)) if rows is None else rows
         n = 1
-        while n < launch and i + n < len(steps) and steps[i + n] == s0 + n:
+        while (n < launch and i + n < len(steps) and steps[i + n] == s0 + n
+               and pk.rows_of_step(s0 + n) == pk.rows_of_step(s0)):
             n += 1
         got = to_host(pk.step(s0, n_steps=n, rows=(r0, r1)))
         for q in range(n):

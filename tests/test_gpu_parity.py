@@ -289,3 +289,47 @@ def test_read_order_random_tiny_corpora(case):
     pk = packer_for(c, window_segment=G, shuffle_rows=rows)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=2)
+
+
+def _schedule_for(c, rng, n_pieces, K):
+    begins = [0] + sorted(int(x) for x in rng.choice(np.arange(1, K), size=n_pieces - 1,
+                                                       replace=False))
+    return [dict(begin=b, B=int(rng.integers(1, c.B + 1)),
+                 source_weight=[int(x) for x in rng.integers(1, 10**6, size=c.n_sources)],
+                 stream_weight=[int(x) for x in rng.integers(1, 10**6, size=c.n_streams)])
+            for b in begins]
+
+
+@pytest.mark.parametrize("name,n_pieces,G,rows", [("c3s", 3, 0, False), ("c3s", 5, 4, True),
+                                                  ("c1", 2, 0, True), ("c4s", 4, 0, False)])
+def test_schedules(name, n_pieces, G, rows):
+    # pieces of the horizon with their own rows per update and weights (a
+    # mixture schedule and a batch-size ramp), with and without the read-order
+    # shuffles
+    c = make_preset(name)
+    rng = np.random.default_rng(n_pieces * 10 + G)
+    sched = _schedule_for(c, rng, n_pieces, c.max_steps)
+    kw = dict(schedule=sched, window_segment=G, shuffle_rows=rows, drain=True)
+    pk, o = packer_for(c, **kw), oracle_for(c, **kw)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=3)
+    # a call may not ask for rows an update of it does not have
+    small = [k for k in range(o.valid_steps) if pk.rows_of_step(k) < c.B]
+    if small:
+        with pytest.raises(Exception) as e:
+            pk.step(small[0], rows=(0, pk.rows_of_step(small[0]) + 1))
+        assert e.value.code == -1
+
+
+@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40)])
+def test_schedules_beyond_one_warp(S, strata):
+    J = S * strata
+    rng = np.random.default_rng(S + strata)
+    lengths = [int(x) for x in rng.integers(1, 200, size=J * 6)]
+    c = corpus_from_lengths(lengths, T=256, B=97, max_steps=9, stream_docs=[6] * J,
+                            stream_source=[s for s in range(S) for _ in range(strata)],
+                            drain=True)
+    sched = _schedule_for(c, rng, 3, 9)
+    pk, o = packer_for(c, schedule=sched), oracle_for(c, schedule=sched)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=2)
