@@ -64,6 +64,7 @@ class _Config(C.Structure):
         ("n_pieces", C.c_uint32),
         ("piece_begin", C.c_void_p), ("piece_B", C.c_void_p),
         ("piece_source_weight", C.c_void_p), ("piece_stream_weight", C.c_void_p),
+        ("wrap", C.c_uint32), ("len_bucket", C.c_uint32),
     ]
 
 
@@ -100,7 +101,7 @@ def lib() -> C.CDLL:
         L.or_free.restype = None
         L.or_free.argtypes = [vp]
         L.or_rows.restype = C.c_int
-        L.or_rows.argtypes = [vp, u32, u32, u32, vp, vp, vp, vp, vp, vp]
+        L.or_rows.argtypes = [vp, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp]
         L.or_row_fp.restype = u64
         L.or_row_fp.argtypes = [vp, vp, vp, vp, u32]
         L.or_batch_fp.restype = u64
@@ -207,7 +208,7 @@ class Oracle:
                  T: Optional[int] = None, B: Optional[int] = None,
                  pad_id: Optional[int] = None, heldout_only: bool = False,
                  window_segment: int = 0, shuffle_rows: bool = False,
-                 schedule: Optional[list] = None):
+                 schedule: Optional[list] = None, wrap: bool = False, len_bucket: int = 0):
         c = corpus
         self.corpus = c
         self.T = int(T if T is not None else c.T)
@@ -250,6 +251,8 @@ class Oracle:
         cfg.heldout_only = int(bool(heldout_only))
         cfg.window_segment = int(window_segment)
         cfg.shuffle_rows = int(bool(shuffle_rows))
+        cfg.wrap = int(bool(wrap))
+        cfg.len_bucket = int(len_bucket)
         self.schedule = schedule
         if schedule:
             pb = np.asarray([int(p["begin"]) for p in schedule], np.uint32)
@@ -328,10 +331,11 @@ class Oracle:
         T = self.T
         out = dict(tokens=np.zeros((n, T), np.int32), pos=np.zeros((n, T), np.int32),
                    doc=np.zeros((n, T), np.int32), mask=np.zeros((n, T), np.uint8),
-                   row_fp=np.zeros(n, np.uint64), row_learned=np.zeros(n, np.int32))
+                   row_fp=np.zeros(n, np.uint64), row_learned=np.zeros(n, np.int32),
+                   row_len=np.zeros(n, np.int32))
         rc = lib().or_rows(self._h, step, row0, row1, _ptr(out["tokens"]), _ptr(out["pos"]),
                            _ptr(out["doc"]), _ptr(out["mask"]), _ptr(out["row_fp"]),
-                           _ptr(out["row_learned"]))
+                           _ptr(out["row_learned"]), _ptr(out["row_len"]))
         if rc != OK:
             raise OracleError(rc, f"or_rows(step={step}, rows=[{row0},{row1}))")
         return out

@@ -39,6 +39,10 @@
  *  - a document longer than T is cut into T-chunks from its start, the last
  *    chunk holding the remainder; a piece fits an open window iff the window's
  *    used positions plus its length are at most T;
+ *  - the "wrap" variant (Zephon's pipeline example: pack_flat with
+ *    algorithm "wrap") concatenates a stream's kept documents and cuts the run
+ *    into windows of exactly T tokens, across document ends; a piece is then
+ *    a document's run inside one window, and its position ids start at 0;
  *  - quotas are counted in windows (samples), by one largest-remainder rule
  *    applied first to sources, then to each source's strata, with the
  *    cumulative shortfall as the remainder's priority;
@@ -89,6 +93,10 @@ typedef struct {
   const uint32_t *piece_B;             /* [n_pieces], 1..B */
   const uint32_t *piece_source_weight; /* [n_pieces][n_sources] */
   const uint32_t *piece_stream_weight; /* [n_pieces][n_streams] */
+  uint32_t wrap;       /* 1: windows are consecutive T-token cuts of the stream's
+                          kept tokens, across document ends */
+  uint32_t len_bucket; /* row length reported as the real length rounded up to a
+                          multiple of this (0: the real length) */
 } or_config;
 
 typedef struct {
@@ -361,9 +369,19 @@ static int pack_stream(or_ctx *x, uint32_t j) {
     /* the training stream keeps what is not held out; the validation stream
        keeps exactly what is */
     if (L == 0 || x->heldout[d] != (c->heldout_only ? 1 : 0)) continue;
-    for (uint64_t off = 0; off < L; off += c->T) {
-      uint64_t len = (L - off < c->T) ? (L - off) : c->T;
-      if (used + len > c->T) used = 0; /* close the window; the rest is padding */
+    for (uint64_t off = 0; off < L;) {
+      uint64_t len;
+      if (c->wrap) {
+        /* concatenate and cut: the piece runs to the document's end or to
+           the window's, whichever comes first */
+        len = L - off;
+        if (len > c->T - used) len = c->T - used;
+      } else {
+        /* greedy, cut at document ends: T-chunks from the document's start;
+           a piece that does not fit closes the window (the rest is padding) */
+        len = (L - off < c->T) ? (L - off) : c->T;
+        if (used + len > c->T) used = 0;
+      }
       if (used == 0) {                  /* open a new window at this piece */
         if (st->n_windows + 1 >= cap_w) {
           cap_w *= 2;
@@ -384,6 +402,8 @@ static int pack_stream(or_ctx *x, uint32_t j) {
       st->pieces[st->n_pieces].len = (uint32_t)len;
       st->n_pieces++;
       used += len;
+      off += len;
+      if (c->wrap && used == c->T) used = 0; /* a full window closes */
     }
   }
   st->win_first[st->n_windows] = st->n_pieces;
@@ -474,13 +494,15 @@ static uint64_t build_digest(const or_ctx *x) {
   digest_add(&a, c->B);
   digest_add(&a, c->max_steps);
   digest_add(&a, x->valid_steps);
-  digest_add(&a, (c->drain ? 1u : 0u) | (c->heldout_only ? 2u : 0u) | (c->shuffle_rows ? 4u : 0u));
+  digest_add(&a, (c->drain ? 1u : 0u) | (c->heldout_only ? 2u : 0u) | (c->shuffle_rows ? 4u : 0u) |
+                    (c->wrap ? 8u : 0u));
   digest_add(&a, (uint64_t)(uint32_t)c->pad_id);
   digest_add(&a, c->seed);
   digest_add(&a, c->hash_key);
   digest_add(&a, c->n_sources);
   digest_add(&a, c->n_streams);
   digest_add(&a, c->window_segment);
+  digest_add(&a, c->len_bucket);
   for (uint32_t s = 0; s < c->n_sources; s++) {
     digest_add(&a, c->source_weight[s]);
     digest_add(&a, c->source_heldout_bp[s]);
@@ -509,7 +531,7 @@ static uint64_t build_digest(const or_ctx *x) {
     for (uint64_t r = 0; r < used; r++) {
       uint64_t w = or_window_of_rank(c->seed, j, c->window_segment, st->n_windows, r);
       const or_piece *p = &st->pieces[st->win_first[w]];
-      digest_add(&a, ((uint64_t)p->doc << 32) | (uint64_t)(p->off / c->T));
+      digest_add(&a, ((uint64_t)p->doc << 32) | (uint64_t)p->off);
     }
   }
   return or_splitmix64(a.sum ^ a.count);
@@ -606,6 +628,10 @@ uint64_t or_row_fp(const int32_t *tok, const int32_t *pos, const int32_t *doc,
 }
 
 /* ---- assembly of rows [row0, row1) of update `step` ----------------------
+ * Each row also reports its length: its real positions (the window's tokens,
+ * which come first), rounded up to a multiple of len_bucket when that is set
+ * ("packed lengths round up to a multiple of bucket", Linnet training docs,
+ * Other trainers).
  * Rows are ordered by (source, stratum, rank), unless shuffled; a rank reads
  * its window through the window order above.  A window's pieces are copied
  * in order; pos is the offset inside the piece (0 starts a new sequence);
@@ -615,7 +641,7 @@ uint64_t or_row_fp(const int32_t *tok, const int32_t *pos, const int32_t *doc,
  * update) is all padding.  Outputs are [row1 - row0][T]. */
 int or_rows(const or_ctx *x, uint32_t step, uint32_t row0, uint32_t row1, int32_t *tok,
             int32_t *pos, int32_t *doc, uint8_t *mask, uint64_t *row_fp,
-            int32_t *row_learned) {
+            int32_t *row_learned, int32_t *row_len) {
   const or_config *c = &x->cfg;
   uint32_t J = c->n_streams, T = c->T;
   if (step >= c->max_steps) return OR_ERR_HORIZON;
@@ -648,6 +674,13 @@ int or_rows(const or_ctx *x, uint32_t step, uint32_t row0, uint32_t row1, int32_
         }
       }
     }
+    /* the row's length: its real positions, rounded up to the bucket */
+    uint32_t len = t;
+    if (c->len_bucket) {
+      len = (t + c->len_bucket - 1) / c->len_bucket * c->len_bucket;
+      if (len > T) len = T;
+    }
+    row_len[i - row0] = (int32_t)len;
     for (; t < T; t++) {
       tok[o + t] = c->pad_id;
       pos[o + t] = 0;
