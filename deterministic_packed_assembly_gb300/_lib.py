@@ -23,6 +23,7 @@ NS_ERR_DEVICE = -7
 NS_PACK_DRAIN = 1
 NS_PACK_HELDOUT = 2
 NS_PACK_SHUFFLE_ROWS = 4
+NS_PACK_WRAP = 8
 NS_MAX_T = 1 << 24
 
 ns_alloc_fn = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)
@@ -56,6 +57,7 @@ class ns_pack_config(C.Structure):
         ("piece_B", C.c_void_p),
         ("piece_source_weight", C.c_void_p),
         ("piece_stream_weight", C.c_void_p),
+        ("len_bucket", C.c_uint32),
         ("cuda_stream", C.c_void_p),
         ("alloc", ns_alloc_fn),
         ("free", ns_free_fn),
@@ -71,6 +73,7 @@ class ns_pack_out(C.Structure):
         ("mask", C.c_void_p),
         ("row_fp", C.c_void_p),
         ("row_learned", C.c_void_p),
+        ("row_len", C.c_void_p),
     ]
 
 

@@ -16,7 +16,7 @@
 
 struct ns_pack_ctx {
   // recipe
-  uint32_t T = 0, B = 0, K = 0, flags = 0, S = 0, J = 0, n_docs = 0, G = 0;
+  uint32_t T = 0, B = 0, K = 0, flags = 0, S = 0, J = 0, n_docs = 0, G = 0, len_bucket = 0;
   int32_t pad_id = 0;
   uint64_t seed = 0, hash_key = 0, n_tokens = 0;
   const int32_t *tokens = nullptr;
@@ -37,7 +37,7 @@ struct ns_pack_ctx {
   int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
   uint32_t *W = nullptr;
   int64_t *wbase = nullptr;
-  int2 *row_win = nullptr;
+  int4 *row_win = nullptr;
   int64_t *node_S = nullptr, *node_src = nullptr;
   int32_t *node_doc = nullptr, *node_mthr = nullptr;
   int *err = nullptr;
@@ -111,7 +111,7 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
-  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS))
+  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP))
     return NS_ERR_INVALID_ARG;
   if (cfg->window_segment > NS_MAX_WINDOW_SEGMENT) return NS_ERR_INVALID_ARG;
   if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
@@ -364,7 +364,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                   heldout_mode ? 1u : 0u, frontier, kept, c->n_sms, st));
   }
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
-  NS_CK(nsk::launch_scan_pieces(klen, n_pos, T, kex, pex, scan_scratch, scan_bytes, st));
+  // greedy packing cuts documents into T-chunks; wrap packing keeps each
+  // kept document whole as one piece (no document reaches 2^31 tokens)
+  const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
+  const uint32_t chunk = wrap ? 0x80000000u : T;
+  NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes, st));
 
   // ---- 4. the prefix of each stream the horizon reaches -------------------
   uint32_t *cutoff = a.temp<uint32_t>(J);
@@ -411,6 +415,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   uint32_t L = 1;
   while ((1ll << L) < max_pieces + 1) L++;
+  if (wrap) L = 0;  // wrap windows are found by position, without pointer jumping
   c->levels = L;
 
   // ---- 6. pieces, next window start, pointer jumping ----------------------
@@ -418,12 +423,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->node_S = a.keep<int64_t>(n_nodes);
   c->node_doc = a.keep<int32_t>(n_nodes);
   c->node_mthr = a.keep<int32_t>(n_nodes);
-  int32_t *levels = a.temp<int32_t>((size_t)L * n_nodes);
+  int32_t *levels = wrap ? nullptr : a.temp<int32_t>((size_t)L * n_nodes);
   NS_ALLOC(c->node_src);
   NS_ALLOC(c->node_S);
   NS_ALLOC(c->node_doc);
   NS_ALLOC(c->node_mthr);
-  NS_ALLOC(levels);
+  if (!wrap) NS_ALLOC(levels);
   {
     std::vector<uint64_t> cnt(J);
     for (uint32_t j = 0; j < J; j++) cnt[j] = std::max<uint64_t>(cut_h[j], 1);
@@ -432,10 +437,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
     NS_CK(nsk::launch_expand(g, static_cast<uint32_t *>(d_sdb), D0, cutoff, order, klen, kex, pex,
-                             node_base, npieces, c->offs, c->loss_start, T, c->node_src,
+                             node_base, npieces, c->offs, c->loss_start, chunk, c->node_src,
                              c->node_doc, c->node_mthr, c->node_S, st));
   }
-  {
+  if (!wrap) {
     std::vector<uint64_t> cnt(J);
     for (uint32_t j = 0; j < J; j++) cnt[j] = (uint64_t)np_h[j] + 1;
     std::vector<uint32_t> bb = seg_layout(cnt, 256);
@@ -450,25 +455,39 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
 
   // ---- 7. windows: count, starts, the valid horizon ------------------------
   c->W = a.keep<uint32_t>(J);
-  int32_t *win_start = a.temp<int32_t>(std::max<int64_t>(wbase[J], 1));
-  c->row_win = a.keep<int2>((size_t)K * c->B);
+  const int64_t n_win = std::max<int64_t>(wbase[J], 1);
+  int32_t *win_start = a.temp<int32_t>(n_win);
+  int32_t *win_end = wrap ? a.temp<int32_t>(n_win) : nullptr;
+  int32_t *win_clip = wrap ? a.temp<int32_t>(n_win) : nullptr;
+  c->row_win = a.keep<int4>((size_t)K * c->B);
   uint32_t *first_bad = a.temp<uint32_t>(1);
   uint32_t *valid = a.temp<uint32_t>(1);
   NS_ALLOC(c->W);
   NS_ALLOC(win_start);
+  if (wrap) {
+    NS_ALLOC(win_end);
+    NS_ALLOC(win_clip);
+  }
   NS_ALLOC(c->row_win);
   NS_ALLOC(first_bad);
   NS_ALLOC(valid);
-  NS_CK(nsk::launch_count_windows(levels, n_nodes, L, node_base, npieces, J, c->W, st));
   std::vector<uint32_t> wb = seg_layout(rmax, 256);
   void *d_wb;
   if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
   nsk::SegGrid wg{static_cast<uint32_t *>(d_wb), J, wb[J]};
-  NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase, win_start,
-                                  st));
-  NS_CK(nsk::launch_row_windows(c->rb, c->cum, c->W, c->wbase, win_start, levels, J, c->B, K,
-                                c->seed, c->G, (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u,
-                                c->row_win, c->err, st));
+  if (wrap) {
+    NS_CK(nsk::launch_wrap_windows(wg, node_base, npieces, c->node_S, cutoff,
+                                   static_cast<uint32_t *>(d_sdb), J, T, c->W, c->wbase,
+                                   win_start, win_end, win_clip, st));
+  } else {
+    NS_CK(nsk::launch_count_windows(levels, n_nodes, L, node_base, npieces, J, c->W, st));
+    NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase,
+                                    win_start, st));
+  }
+  NS_CK(nsk::launch_row_windows(c->rb, c->cum, c->W, c->wbase, win_start, levels, win_end,
+                                win_clip, J, c->B, K, c->seed, c->G,
+                                (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u, c->row_win, c->err,
+                                st));
   NS_CK(nsk::launch_valid_steps(c->cum, c->W, J, K, (c->flags & NS_PACK_DRAIN) ? 1u : 0u,
                                 first_bad, valid, st));
 
@@ -485,13 +504,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.scalars[1] = c->B;
   h.scalars[2] = K;
   h.scalars[3] = 0;  // valid_steps, read on the device
-  h.scalars[4] = c->flags & (NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS);
+  h.scalars[4] = c->flags & (NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP);
   h.scalars[5] = (uint64_t)(uint32_t)c->pad_id;
   h.scalars[6] = c->seed;
   h.scalars[7] = c->hash_key;
   h.scalars[8] = S;
   h.scalars[9] = J;
   h.scalars[10] = c->G;
+  h.scalars[11] = c->len_bucket;
   h.source_weight = static_cast<uint32_t *>(d_sw);
   h.source_bp = static_cast<uint16_t *>(d_sbp);
   h.sdb = static_cast<uint32_t *>(d_sdb);
@@ -502,8 +522,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.S = S;
   h.J = J;
   NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, win_start,
-                           c->node_src, c->node_doc, c->offs, T, K, c->seed, c->G, c->err, dacc,
-                           ubase, digest, st));
+                           c->node_src, c->node_doc, c->offs, T, K, c->seed, c->G, win_clip,
+                           c->err, dacc, ubase, digest, st));
 
   // ---- 9. read back the summary ------------------------------------------
   std::vector<uint32_t> W_h(J);
@@ -537,6 +557,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   c->K = cfg->max_steps;
   c->flags = cfg->flags;
   c->G = cfg->window_segment;
+  c->len_bucket = cfg->len_bucket;
   c->S = cfg->n_sources;
   c->J = cfg->n_streams;
   c->n_docs = cfg->n_docs;
@@ -604,6 +625,8 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   p.mask_out = out->mask;
   p.row_fp = out->row_fp;
   p.row_learned = out->row_learned;
+  p.row_len = out->row_len;
+  p.len_bucket = ctx->len_bucket;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_gather(p, st) != cudaSuccess) {
     cudaGetLastError();

@@ -110,13 +110,18 @@ struct WarpPieces {
   }
 };
 
+// Loss threshold of a piece whose first `clip` tokens lie in an earlier window.
+__device__ __forceinline__ int32_t clip_threshold(int32_t mthr, int32_t clip) {
+  return (int32_t)max((int64_t)mthr - clip, (int64_t)INT_MIN);
+}
+
 // Window of any length read from the context's piece table (L1-cached).
 struct TablePieces {
   const int64_t *S;  // node_S + ws (absolute prefix; sbase subtracted)
   const int64_t *srcs;
   const int32_t *docs, *mthrs;
-  int64_t sbase;
-  int32_t np, used;
+  int64_t sbase;  // node_S[ws] + clip: position 0 of the row
+  int32_t np, used, clip;
   __device__ __forceinline__ int32_t find(int32_t lo, int32_t t) const {
     int32_t l = lo, h = np;
     while (l < h) {
@@ -132,11 +137,11 @@ struct TablePieces {
   __device__ __forceinline__ int32_t find_lane(int32_t t) const { return find(0, t); }
   __device__ __forceinline__ Piece get(int32_t q) const {
     Piece p;
-    p.start = (int32_t)(__ldg(S + q) - sbase);
-    p.end = (int32_t)(__ldg(S + q + 1) - sbase);
-    p.src = __ldg(srcs + q);
+    p.start = q == 0 ? 0 : (int32_t)(__ldg(S + q) - sbase);
+    p.end = q + 1 < np ? (int32_t)(__ldg(S + q + 1) - sbase) : used;
+    p.src = __ldg(srcs + q) + (q == 0 ? clip : 0);
     p.doc = __ldg(docs + q);
-    p.mthr = __ldg(mthrs + q);
+    p.mthr = q == 0 ? clip_threshold(__ldg(mthrs + q), clip) : __ldg(mthrs + q);
     return p;
   }
 };
@@ -301,15 +306,17 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   }
   __syncthreads();
 
-  // the row's window: pieces [ws, we) of the context's piece table
-  const int2 win = p.row_win[(size_t)k * p.B + i];
+  // the row's window: pieces [ws, we) of the context's piece table, from
+  // token `clip` of the first (wrap packing; 0 for greedy windows)
+  const int4 win = p.row_win[(size_t)k * p.B + i];
   int64_t ws = win.x, we = win.y;
-  if (ws < 0 || we < ws) ws = we = 0;  // a row past the end of its stream: all padding
+  int32_t clip = win.z;
+  if (ws < 0 || we < ws) ws = we = clip = 0;  // a row past the end of its stream: all padding
   const int32_t np = (int32_t)(we - ws);
-  const int64_t sbase = __ldg(p.node_S + ws);
-  const int64_t used64 = __ldg(p.node_S + we) - sbase;
+  const int64_t sbase = __ldg(p.node_S + ws) + clip;
+  const int64_t used64 = min(__ldg(p.node_S + we) - sbase, (int64_t)p.T);
   int32_t used = (int32_t)used64;
-  if (used64 < 0 || used64 > (int64_t)p.T) {
+  if (used64 < 0 || clip < 0 || (np == 0 && clip != 0)) {
     set_error(p.err, kDevBadNode);
     used = 0;
   }
@@ -326,10 +333,11 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     P.doc = -1;
     P.mthr = 0;
     if (lane < np) {
-      P.S = (int32_t)(__ldg(p.node_S + ws + lane) - sbase);
-      P.src = __ldg(p.node_src + ws + lane);
+      P.S = lane == 0 ? 0 : (int32_t)(__ldg(p.node_S + ws + lane) - sbase);
+      P.src = __ldg(p.node_src + ws + lane) + (lane == 0 ? clip : 0);
       P.doc = __ldg(p.node_doc + ws + lane);
       P.mthr = __ldg(p.node_mthr + ws + lane);
+      if (lane == 0) P.mthr = clip_threshold(P.mthr, clip);
     }
     warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
   } else {
@@ -341,6 +349,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     P.sbase = sbase;
     P.np = np;
     P.used = used;
+    P.clip = clip;
     warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
   }
 
@@ -356,6 +365,12 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
       const uint64_t a = *reinterpret_cast<volatile unsigned long long *>(&s_acc);
       p.row_fp[blk] = splitmix64(a);
       p.row_learned[blk] = *reinterpret_cast<volatile int *>(&s_learned);
+      if (p.row_len) {
+        // real positions come first; report them rounded up to the bucket
+        const uint64_t b = p.len_bucket;
+        const uint64_t len = b ? min((((uint64_t)used + b - 1) / b) * b, (uint64_t)p.T) : used;
+        p.row_len[blk] = (int32_t)len;
+      }
     }
   }
 }

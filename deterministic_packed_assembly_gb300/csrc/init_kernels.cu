@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     if (i < n) {
       const uint32_t v = klen[i];
       a += v;
-      b += (v + T - 1) / T;
+      b += ((uint64_t)v + T - 1) / T;
     }
   }
   a = warp_sum_i64(a);
@@ -646,7 +646,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     if (i < n) {
       const uint32_t v = klen[i];
       a += v;
-      b += (v + T - 1) / T;
+      b += ((uint64_t)v + T - 1) / T;
     }
   }
   a = warp_sum_i64(a);
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
   for (int r = 0; r < kScanRounds; r++) {
     const uint64_t i = seg + (uint64_t)r * 32 + lane;
     const uint32_t v = (i < n) ? klen[i] : 0u;
-    const int64_t va = v, vb = (v + T - 1) / T;
+    const int64_t va = v, vb = (int64_t)(((uint64_t)v + T - 1) / T);
     const int64_t xa = warp_incl_scan(va, lane), xb = warp_incl_scan(vb, lane);
     if (i < n) {
       kex[i] = ca + xa - va;
@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t L = klen[idx];
   if (L == 0) return;
   const uint32_t d = order[idx];
-  const uint32_t n = (L + T - 1) / T;
+  const uint32_t n = (uint32_t)(((uint64_t)L + T - 1) / T);
   const int64_t node0 = node_base[j] + (pex[idx] - pex[b]);
   const int64_t sb = kex[idx] - kex[b];
   const int64_t o = offs[d];
@@ -844,7 +844,9 @@ __global__ void __launch_bounds__(kThreads)
   win_start[wbase[j] + r] = s;
 }
 
-// The window of every row of every update of the horizon.  Rows of an update
+// The window of every row of every update of the horizon, as (first piece,
+// end piece, offset of the window's first token inside its first piece).
+// Rows of an update
 // are ordered by stream, then by rank (or shuffled: slot i holds row
 // rho_k(i)): row c belongs to the stream whose row range [rb[k][j],
 // rb[k][j+1]) holds it and takes that stream's rank cum[k][j] + (c -
@@ -854,28 +856,79 @@ __global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t
                                    const uint32_t *__restrict__ W,
                                    const int64_t *__restrict__ wbase,
                                    const int32_t *__restrict__ win_start,
-                                   const int32_t *__restrict__ next, uint32_t J, uint32_t B,
+                                   const int32_t *__restrict__ next,
+                                   const int32_t *__restrict__ win_end,
+                                   const int32_t *__restrict__ win_clip, uint32_t J, uint32_t B,
                                    uint32_t K, uint64_t seed, uint32_t G, uint32_t shuffle_rows,
-                                   int2 *__restrict__ row_win, int *err) {
+                                   int4 *__restrict__ row_win, int *err) {
   const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= (uint64_t)K * B) return;
   const uint32_t k = (uint32_t)(x / B), slot = (uint32_t)(x % B);
   const int32_t *rbk = rb + (size_t)k * (J + 1);
   const uint32_t Bk = (uint32_t)rbk[J];  // rows of this update (a schedule may vary them)
-  if (slot >= Bk) {
-    row_win[x] = make_int2(-1, -1);
-    return;
-  }
-  const uint32_t i = shuffle_rows ? row_of_slot(seed, k, Bk, slot, err) : slot;
-  const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)J, (int32_t)i);
-  const int64_t r = (int64_t)cum[(size_t)k * J + j] + ((int64_t)i - rbk[j]);
-  int2 w = make_int2(-1, -1);
-  if (r < (int64_t)W[j]) {
-    const uint64_t wi = window_of_rank(seed, (uint32_t)j, G, W[j], (uint64_t)r, err);
-    const int32_t s = win_start[wbase[j] + (int64_t)wi];
-    w = make_int2(s, next[s]);
+  int4 w = make_int4(-1, -1, 0, 0);
+  if (slot < Bk) {
+    const uint32_t i = shuffle_rows ? row_of_slot(seed, k, Bk, slot, err) : slot;
+    const int64_t j = last_le<int32_t, int64_t>(rbk, 0, (int64_t)J, (int32_t)i);
+    const int64_t r = (int64_t)cum[(size_t)k * J + j] + ((int64_t)i - rbk[j]);
+    if (r < (int64_t)W[j]) {
+      const uint64_t wi = window_of_rank(seed, (uint32_t)j, G, W[j], (uint64_t)r, err);
+      const int64_t e = wbase[j] + (int64_t)wi;
+      const int32_t st = win_start[e];
+      // greedy windows end where the next one starts; wrap windows carry
+      // their end and the offset of their first token inside their first piece
+      w = win_end ? make_int4(st, win_end[e], win_clip[e], 0) : make_int4(st, next[st], 0, 0);
+    }
   }
   row_win[x] = w;
+}
+
+// Wrap packing: the stream's kept tokens cut into windows of exactly T.  W_j
+// counts the stream's windows, the last one partial, when the whole stream was
+// expanded; otherwise only the windows that lie wholly inside the prefix.
+__global__ void wrap_count_kernel(const int64_t *__restrict__ node_base,
+                                  const int64_t *__restrict__ npieces,
+                                  const int64_t *__restrict__ node_S,
+                                  const uint32_t *__restrict__ cutoff,
+                                  const uint32_t *__restrict__ sdb, uint32_t J, uint32_t T,
+                                  uint32_t *__restrict__ W) {
+  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= J) return;
+  const int64_t first = node_base[j], term = first + npieces[j];
+  const int64_t total = node_S[term] - node_S[first];
+  const bool complete = cutoff[j] == sdb[j + 1] - sdb[j];
+  W[j] = (uint32_t)(complete ? (total + T - 1) / T : total / T);
+}
+
+// Window w of a stream under wrap packing: tokens [wT, min((w+1)T, total)) of
+// its kept run; its first piece is the last one starting at or before wT
+// (clip = how far into it the window starts), its end the first piece
+// starting at or after the window's last token + 1.
+__global__ void __launch_bounds__(kThreads)
+    wrap_windows_kernel(SegGrid g, const int64_t *__restrict__ node_base,
+                        const int64_t *__restrict__ npieces, const int64_t *__restrict__ node_S,
+                        const uint32_t *__restrict__ W, const int64_t *__restrict__ wbase,
+                        uint32_t T, int32_t *__restrict__ win_start,
+                        int32_t *__restrict__ win_end, int32_t *__restrict__ win_clip) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const uint64_t w = (uint64_t)blk * blockDim.x + threadIdx.x;
+  if (w >= (uint64_t)(wbase[j + 1] - wbase[j])) return;
+  const int64_t e = wbase[j] + (int64_t)w;
+  if (w >= W[j]) {
+    win_start[e] = win_end[e] = -1;
+    win_clip[e] = 0;
+    return;
+  }
+  const int64_t first = node_base[j], term = first + npieces[j];
+  const int64_t s0 = node_S[first];
+  const int64_t total = node_S[term] - s0;
+  const int64_t a = (int64_t)w * T, b = min(a + (int64_t)T, total);
+  const int64_t ws = last_le<int64_t, int64_t>(node_S, first, term, s0 + a);
+  const int64_t we = last_le<int64_t, int64_t>(node_S, ws, term, s0 + b - 1) + 1;
+  win_start[e] = (int32_t)ws;
+  win_end[e] = (int32_t)we;
+  win_clip[e] = (int32_t)(s0 + a - node_S[ws]);
 }
 
 // First update that asks a stream for a window past its last.
@@ -970,7 +1023,8 @@ __global__ void __launch_bounds__(kThreads)
                           const int32_t *__restrict__ node_doc, const int64_t *__restrict__ offs,
                           uint32_t T, uint64_t h0, uint32_t J, const uint32_t *valid,
                           const int64_t *__restrict__ ubase, const uint32_t *__restrict__ W,
-                          uint64_t seed, uint32_t G, int *err, unsigned long long *acc) {
+                          uint64_t seed, uint32_t G, const int32_t *__restrict__ win_clip,
+                          int *err, unsigned long long *acc) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
@@ -978,10 +1032,11 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t term = 0;
   if (r < U) {
     const uint64_t wi = window_of_rank(seed, j, G, W[j], r, err);
-    const int32_t node = win_start[wbase[j] + (int64_t)wi];
+    const int64_t e = wbase[j] + (int64_t)wi;
+    const int32_t node = win_start[e];
     const int32_t d = node_doc[node];
-    const uint64_t chunk = (uint64_t)(node_src[node] - offs[d]) / T;
-    const uint64_t x = ((uint64_t)(uint32_t)d << 32) | (chunk & 0xFFFFFFFFull);
+    const int64_t off = node_src[node] - offs[d] + (win_clip ? win_clip[e] : 0);
+    const uint64_t x = ((uint64_t)(uint32_t)d << 32) | ((uint64_t)off & 0xFFFFFFFFull);
     term = digest_term(x, h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[j] + r);
   }
   digest_accumulate(term, acc);
@@ -1191,12 +1246,30 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
 
 cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
                                const int64_t *wbase, const int32_t *win_start,
-                               const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
-                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int2 *row_win,
+                               const int32_t *next, const int32_t *win_end,
+                               const int32_t *win_clip, uint32_t J, uint32_t B, uint32_t K,
+                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *row_win,
                                int *err, cudaStream_t st) {
   ++launch_counter();
   row_windows_kernel<<<blocks_for((uint64_t)K * B), kThreads, 0, st>>>(
-      rb, cum, W, wbase, win_start, next, J, B, K, seed, G, shuffle_rows, row_win, err);
+      rb, cum, W, wbase, win_start, next, win_end, win_clip, J, B, K, seed, G, shuffle_rows,
+      row_win, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64_t *npieces,
+                                const int64_t *node_S, const uint32_t *cutoff,
+                                const uint32_t *sdb, uint32_t J, uint32_t T, uint32_t *W,
+                                const int64_t *wbase, int32_t *win_start, int32_t *win_end,
+                                int32_t *win_clip, cudaStream_t st) {
+  ++launch_counter();
+  wrap_count_kernel<<<blocks_for(J, 128), 128, 0, st>>>(node_base, npieces, node_S, cutoff, sdb,
+                                                        J, T, W);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || g.n_blocks == 0) return e;
+  ++launch_counter();
+  wrap_windows_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, node_base, npieces, node_S, W, wbase,
+                                                       T, win_start, win_end, win_clip);
   return cudaGetLastError();
 }
 
@@ -1221,8 +1294,8 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           const int64_t *wbase, const int32_t *win_start,
                           const int64_t *node_src, const int32_t *node_doc,
                           const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
-                          int *err, unsigned long long *acc, int64_t *ubase,
-                          uint64_t *digest_out, cudaStream_t st) {
+                          const int32_t *win_clip, int *err, unsigned long long *acc,
+                          int64_t *ubase, uint64_t *digest_out, cudaStream_t st) {
   const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
   ++launch_counter();
   digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
@@ -1241,7 +1314,8 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
     ++launch_counter();
     digest_windows_kernel<<<wg.n_blocks, kThreads, 0, st>>>(wg, wbase, win_start, node_src,
                                                             node_doc, offs, T, h0, h.J, valid,
-                                                            ubase, W, seed, G, err, acc);
+                                                            ubase, W, seed, G, win_clip, err,
+                                                            acc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

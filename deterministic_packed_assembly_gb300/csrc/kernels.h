@@ -95,23 +95,31 @@ cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_
 cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nodes,
                                  uint32_t n_levels, const int64_t *node_base, const uint32_t *W,
                                  const int64_t *wbase, int32_t *win_start, cudaStream_t st);
-// row_win[k][i] = (first piece, end piece) of the window slot i of update k
-// takes, or (-1, -1) when the row lies past the end of its stream; G > 0
+// row_win[k][i] = (first piece, end piece, clip, 0) of the window slot i of
+// update k takes, or (-1, -1) when the row lies past the end of its stream
+// (win_end / win_clip: wrap packing's tables; null for greedy windows); G > 0
 // reads windows in a shuffled order within segments, shuffle_rows shuffles the
 // rows of every update.
 cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
                                const int64_t *wbase, const int32_t *win_start,
-                               const int32_t *next, uint32_t J, uint32_t B, uint32_t K,
-                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int2 *row_win,
+                               const int32_t *next, const int32_t *win_end,
+                               const int32_t *win_clip, uint32_t J, uint32_t B, uint32_t K,
+                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *row_win,
                                int *err, cudaStream_t st);
+// Wrap packing: windows of exactly T tokens of each stream's kept run.
+cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64_t *npieces,
+                                const int64_t *node_S, const uint32_t *cutoff,
+                                const uint32_t *sdb, uint32_t J, uint32_t T, uint32_t *W,
+                                const int64_t *wbase, int32_t *win_start, int32_t *win_end,
+                                int32_t *win_clip, cudaStream_t st);
 cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st);
 
 // ---- order digest ---------------------------------------------------------
-constexpr int kDigestScalars = 11;
+constexpr int kDigestScalars = 12;
 struct DigestHeader {
-  uint64_t scalars[kDigestScalars];  // T, B, K, valid, flags, pad, seed, key, S, J, G
+  uint64_t scalars[kDigestScalars];  // T, B, K, valid, flags, pad, seed, key, S, J, G, bucket
   const uint32_t *source_weight;  // [S]
   const uint16_t *source_bp;      // [S]
   const uint32_t *sdb;            // [J + 1]
@@ -126,7 +134,8 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           const int64_t *wbase, const int32_t *win_start,
                           const int64_t *node_src, const int32_t *node_doc,
                           const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
-                          int *err, unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
+                          const int32_t *win_clip, int *err,
+                          unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
                           uint64_t *digest_out, cudaStream_t st);
 
 // ---- per-step assembly ----------------------------------------------------
@@ -134,7 +143,8 @@ struct GatherParams {
   // corpus
   const int32_t *tokens;
   // context tables
-  const int2 *row_win;      // [K][B]: pieces [x, y) of the row's window; x < 0 past the end
+  const int4 *row_win;      // [K][B]: pieces [x, y) of the row's window from offset z of
+                            // the first; x < 0 past the end
   const int64_t *node_S;    // [nodes]
   const int64_t *node_src;  // [nodes]
   const int32_t *node_doc;  // [nodes]
@@ -148,6 +158,8 @@ struct GatherParams {
   uint8_t *mask_out;
   uint64_t *row_fp;
   int32_t *row_learned;
+  int32_t *row_len;         // [n_steps][rows] or null
+  uint32_t len_bucket;
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,

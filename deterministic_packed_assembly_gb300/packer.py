@@ -30,7 +30,9 @@ class Packer:
     within segments of that many windows; ``shuffle_rows`` shuffles the rows
     of every update; ``schedule`` (a list of ``dict(begin, B, source_weight,
     stream_weight)``) gives pieces of the horizon their own rows per update
-    and weights.
+    and weights; ``wrap`` cuts each stream's concatenated kept tokens into
+    windows of exactly T (across document ends) instead of greedy packing;
+    ``len_bucket`` rounds the reported row lengths up to its multiples.
     """
 
     def __init__(self, tokens: torch.Tensor, doc_offsets: torch.Tensor,
@@ -39,6 +41,7 @@ class Packer:
                  max_steps: int, seed: int = 0, hash_key: int = 0, drain: bool = False,
                  pad_id: int = 0, heldout_only: bool = False, window_segment: int = 0,
                  shuffle_rows: bool = False, schedule: Optional[list] = None,
+                 wrap: bool = False, len_bucket: int = 0,
                  stream: Optional[torch.cuda.Stream] = None):
         if not tokens.is_cuda:
             raise ValueError("tokens must be a CUDA tensor")
@@ -91,7 +94,9 @@ class Packer:
         cfg.B = self.B
         cfg.max_steps = self.max_steps
         cfg.flags = ((L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
-                     | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0))
+                     | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0)
+                     | (L.NS_PACK_WRAP if wrap else 0))
+        cfg.len_bucket = int(len_bucket)
         cfg.window_segment = int(window_segment)
         self.schedule = schedule
         if schedule:
@@ -150,7 +155,8 @@ class Packer:
                     doc=torch.empty(shape, dtype=torch.int32, device=d),
                     mask=torch.empty(shape, dtype=torch.uint8, device=d),
                     row_fp=torch.empty((n_steps, n_rows), dtype=torch.int64, device=d),
-                    row_learned=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d))
+                    row_learned=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d),
+                    row_len=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d))
 
     @staticmethod
     def _out_struct(out: dict) -> L.ns_pack_out:
@@ -161,6 +167,7 @@ class Packer:
         o.mask = out["mask"].data_ptr()
         o.row_fp = out["row_fp"].data_ptr()
         o.row_learned = out["row_learned"].data_ptr()
+        o.row_len = out["row_len"].data_ptr() if out.get("row_len") is not None else None
         return o
 
     def step(self, step0: int, n_steps: int = 1, rows: Optional[tuple] = None,

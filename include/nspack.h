@@ -73,6 +73,13 @@ extern "C" {
 /* Shuffle the rows of every update: slot i holds the row that would otherwise
  * be row rho_k(i), rho_k a keyed permutation of [0, B) (seed + 2, update k). */
 #define NS_PACK_SHUFFLE_ROWS 4u
+/* Wrap packing: concatenate each stream's kept documents and cut the run into
+ * windows of exactly T tokens, across document ends (the pipeline example's
+ * pack_flat with algorithm "wrap", "Zephon: deterministic data loading").  A
+ * piece is a document's run inside one window and its position ids start at
+ * 0; a stream's last window may be partial (padded), and it counts only once
+ * the whole stream is inside the reachable prefix. */
+#define NS_PACK_WRAP 8u
 
 /* ---- limits ------------------------------------------------------------- */
 #define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
@@ -115,7 +122,8 @@ typedef struct {
   uint64_t hash_key; /* keys the held-out hash (not the seed: same in every line) */
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
-  uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS */
+  uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS |
+                        NS_PACK_WRAP */
   int32_t pad_id;    /* token written at padded positions */
   uint32_t window_segment; /* G > 0: each stream's windows are read in a shuffled
                               order within segments of G consecutive windows
@@ -138,6 +146,11 @@ typedef struct {
   const uint32_t *piece_B;             /* [n_pieces], 1 .. B */
   const uint32_t *piece_source_weight; /* [n_pieces][n_sources], > 0 */
   const uint32_t *piece_stream_weight; /* [n_pieces][n_streams], > 0 */
+  /* Row lengths reported in ns_pack_out.row_len: the row's real positions
+   * rounded up to a multiple of len_bucket, at most T ("packed lengths round
+   * up to a multiple of bucket, so few shapes compile", Linnet training docs,
+   * Other trainers); 0 reports the real length. */
+  uint32_t len_bucket;
   void *cuda_stream; /* cudaStream_t for init and default for the other calls */
   ns_alloc_fn alloc;
   ns_free_fn free;
@@ -153,6 +166,8 @@ typedef struct {
   uint8_t *mask;
   uint64_t *row_fp;     /* [n_steps][rows] */
   int32_t *row_learned; /* [n_steps][rows] */
+  int32_t *row_len;     /* [n_steps][rows] or NULL: real positions of the row
+                           (they come first), rounded up to len_bucket */
 } ns_pack_out;
 
 typedef struct {
@@ -161,9 +176,10 @@ typedef struct {
   uint32_t n_streams;
   uint32_t T;
   uint32_t B;
-  uint32_t levels;      /* pointer-jumping levels used at init */
+  uint32_t levels;      /* pointer-jumping levels used at init (0: wrap packing) */
   uint64_t order_digest;
-  uint64_t n_pieces;    /* pieces (document T-chunks) built at init */
+  uint64_t n_pieces;    /* pieces built at init: document T-chunks, or whole
+                           documents under wrap packing */
   uint64_t table_bytes; /* device bytes the context keeps */
   uint32_t init_launches; /* kernels ns_pack_init launched */
   uint32_t reserved;

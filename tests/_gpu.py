@@ -23,11 +23,12 @@ def to_host(out: dict) -> dict:
     h = {k: out[k].cpu().numpy() for k in FIELDS}
     h["row_fp"] = as_u64(out["row_fp"])
     h["row_learned"] = out["row_learned"].cpu().numpy()
+    h["row_len"] = out["row_len"].cpu().numpy()
     return h
 
 
 def assert_rows_equal(got: dict, want: dict, what: str) -> None:
-    for k in FIELDS + ("row_fp", "row_learned"):
+    for k in FIELDS + ("row_fp", "row_learned", "row_len"):
         g, w = got[k], want[k]
         assert g.shape == w.shape, (what, k, g.shape, w.shape)
         if not np.array_equal(g, w):
