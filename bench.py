@@ -50,6 +50,18 @@ WORKLOADS = {
     "c5": "1 source of ~1e9 tokens, log-normal median 2048 sigma 1.5 [1,262144], vocab "
           "151,936, T=32768, B=64, long documents cut into T-chunks, full pass (drain)",
 }
+VARIANTS = {
+    "default": "training stream, greedy packing cut at document ends, windows and rows in order",
+    "heldout": "validation stream: the held-out documents of every stream, same shuffle, "
+               "packing and quotas (drain)",
+    "shuffled": "windows read in a keyed order within segments of 64, rows of every update "
+                "shuffled",
+    "wrap": "wrap packing: windows of exactly T across document ends, row lengths rounded "
+            "up to buckets of 256",
+    "schedule": "4-piece schedule: batch ramp B/4, B/2, 3B/4, B rows from updates 0, K/8, "
+                "K/4, K/2, each piece with the recipe's weights scaled by draws in "
+                "[0.8, 1.25) (seed 77)",
+}
 METRIC = "packed tokens/s"
 UNIT = "tokens/s"
 PROFILES = os.path.join(ROOT, "profiles")
@@ -64,6 +76,9 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="c3", choices=sorted(WORKLOADS))
     ap.add_argument("--launch", type=int, default=32, help="updates per ns_pack_step launch")
+    ap.add_argument("--variant", default="default", choices=sorted(VARIANTS),
+                    help="packing options of the pass (validation stream, read-order "
+                         "shuffles, wrap packing, schedule)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-updates", type=int, default=40,
                     help="updates the CPU baseline assembles (its sample)")
@@ -236,8 +251,46 @@ def recipe_kwargs(c) -> dict:
                 seed=c.seed, hash_key=c.hash_key, drain=c.drain, pad_id=c.pad_id)
 
 
+def variant_kwargs(c, name: str) -> dict:
+    """Packer / oracle options of a bench variant."""
+    if name == "heldout":
+        return dict(heldout_only=True, drain=True)
+    if name == "shuffled":
+        return dict(window_segment=64, shuffle_rows=True)
+    if name == "wrap":
+        return dict(wrap=True, len_bucket=256)
+    if name == "schedule":
+        rng = np.random.default_rng(77)
+        K, B = int(c.max_steps), int(c.B)
+        begins = sorted({0, K // 8, K // 4, K // 2})
+        Bs = [max(1, B * (i + 1) // 4) for i in range(4)][-len(begins):]
+        sw = np.asarray(c.source_weight, np.float64)
+        tw = np.asarray(c.stream_weight, np.float64)
+        return dict(schedule=[
+            dict(begin=b, B=bb,
+                 source_weight=np.maximum(1, np.rint(sw * rng.uniform(0.8, 1.25, sw.size)))
+                 .astype(np.uint32).tolist(),
+                 stream_weight=np.maximum(1, np.rint(tw * rng.uniform(0.8, 1.25, tw.size)))
+                 .astype(np.uint32).tolist())
+            for b, bb in zip(begins, Bs)])
+    return {}
+
+
+def launch_plan(pk, valid: int, L: int):
+    """(first update, updates, rows per update) of each launch: at most L
+    updates, never across a schedule piece (rows per update may change)."""
+    begins = sorted({int(p["begin"]) for p in pk.schedule}) if pk.schedule else [0]
+    s = 0
+    for e in [b for b in begins if 0 < b < valid] + [valid]:
+        while s < e:
+            m = min(L, e - s)
+            yield s, m, pk.rows_of_step(s)
+            s += m
+
+
 def config_block(c, args, dist: Dist, rows) -> dict:
     return {"workload": f"{args.config}: {WORKLOADS[args.config]}",
+            "variant": f"{args.variant}: {VARIANTS[args.variant]}",
             "n_docs": c.n_docs, "n_tokens": c.n_tokens, "T": c.T, "B": c.B,
             "updates_per_step": None, "rows_per_rank": rows[1] - rows[0],
             "launch_updates": args.launch,
@@ -256,8 +309,8 @@ def run_ours(args, dist: Dist) -> None:
     torch.cuda.set_device(device)
     c = make_workload(args.config)
     rows = row_slice(dist.rank, dist.world, c.B)
-    n_rows = rows[1] - rows[0]
     rk = recipe_kwargs(c)
+    rk.update(variant_kwargs(c, args.variant))
     stream = torch.cuda.current_stream(device)
 
     tok_d = torch.from_numpy(c.tokens).to(device)
@@ -266,22 +319,25 @@ def run_ours(args, dist: Dist) -> None:
     torch.cuda.synchronize()
 
     L = args.launch
-    shape = (L, n_rows, c.T)
-    out = dict(tokens=torch.empty(shape, dtype=torch.int32, device=device),
-               pos=torch.empty(shape, dtype=torch.int32, device=device),
-               doc=torch.empty(shape, dtype=torch.int32, device=device),
-               mask=torch.empty(shape, dtype=torch.uint8, device=device))
+    n_buf = -(-c.B // dist.world)  # bounds this rank's rows of any update
+    n_pos = L * n_buf * c.T
+    # flat buffers, viewed [updates][rows][T] per launch (a schedule changes
+    # the rows per update)
+    out = dict(tokens=torch.empty(n_pos, dtype=torch.int32, device=device),
+               pos=torch.empty(n_pos, dtype=torch.int32, device=device),
+               doc=torch.empty(n_pos, dtype=torch.int32, device=device),
+               mask=torch.empty(n_pos, dtype=torch.uint8, device=device))
     # row fingerprints and learned counts alternate between two buffers so
     # that one launch's batch fold (on a second stream) overlaps the next
     # launch's gather
-    row_fp = [torch.empty((L, n_rows), dtype=torch.int64, device=device) for _ in range(2)]
-    row_ln = [torch.empty((L, n_rows), dtype=torch.int32, device=device) for _ in range(2)]
+    row_fp = [torch.empty(L * n_buf, dtype=torch.int64, device=device) for _ in range(2)]
+    row_ln = [torch.empty(L * n_buf, dtype=torch.int32, device=device) for _ in range(2)]
     fp_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
     fold_stream = torch.cuda.Stream(device)
     gathered = [torch.cuda.Event() for _ in range(2)]
     folded = [torch.cuda.Event() for _ in range(2)]
 
-    state = {"launches": 0, "init_launches": 0, "valid": 0, "events": []}
+    state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0}
 
     def one_pass(record: bool, count: bool = False, e2e=None):
         """One whole pass; returns real tokens assembled when `count`."""
@@ -292,19 +348,24 @@ def run_ours(args, dist: Dist) -> None:
         state["init_launches"] = pk.info["init_launches"]
         real = torch.zeros((), dtype=torch.int64, device=device) if count else None
         n = 0
-        for li, s0 in enumerate(range(0, valid, L)):
-            m = min(L, valid - s0)
+        rows_total = 0
+        for li, (s0, m, Bk) in enumerate(launch_plan(pk, valid, L)):
+            rk0, rk1 = row_slice(dist.rank, dist.world, Bk)
+            r = rk1 - rk0
+            if r == 0:
+                continue
+            rows_total += m * r
             b = li % 2
             if li >= 2:
                 stream.wait_event(folded[b])
-            view = {k: v[:m] for k, v in out.items()}
-            view["row_fp"] = row_fp[b][:m]
-            view["row_learned"] = row_ln[b][:m]
+            view = {k: v[:m * r * c.T].view(m, r, c.T) for k, v in out.items()}
+            view["row_fp"] = row_fp[b][:m * r].view(m, r)
+            view["row_learned"] = row_ln[b][:m * r].view(m, r)
             if record:
                 ea = torch.cuda.Event(enable_timing=True)
                 eb = torch.cuda.Event(enable_timing=True)
                 ea.record(stream)
-            pk.step(s0, m, rows=rows, out=view, stream=stream)
+            pk.step(s0, m, rows=(rk0, rk1), out=view, stream=stream)
             n += 1
             if record:
                 eb.record(stream)
@@ -316,8 +377,8 @@ def run_ours(args, dist: Dist) -> None:
                 folded[b].record(fold_stream)
                 n += 1
             if e2e is not None:
-                e2e[3][s0:s0 + m].copy_(view["row_fp"], non_blocking=True)
-                e2e[4][s0:s0 + m].copy_(view["row_learned"], non_blocking=True)
+                e2e[3][s0:s0 + m, :r].copy_(view["row_fp"], non_blocking=True)
+                e2e[4][s0:s0 + m, :r].copy_(view["row_learned"], non_blocking=True)
             if count:
                 real += (view["doc"] >= 0).sum()
         stream.wait_stream(fold_stream)
@@ -325,6 +386,7 @@ def run_ours(args, dist: Dist) -> None:
             e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
         pk.close()
         state["launches"] = n
+        state["rows_total"] = rows_total
         return int(real.item()) if count else None
 
     # warm-up (the first pass also counts the real tokens of a pass)
@@ -332,7 +394,8 @@ def run_ours(args, dist: Dist) -> None:
     for _ in range(max(args.warmup - 1, 0)):
         one_pass(False)
     valid = state["valid"]
-    positions = valid * n_rows * c.T
+    rows_pass = state["rows_total"]  # rows this rank assembles in a pass
+    positions = rows_pass * c.T
     log(f"[bench] rank {dist.rank}: {valid} updates, {real_tokens} real tokens / pass")
 
     def timed(K: int):
@@ -365,8 +428,8 @@ def run_ours(args, dist: Dist) -> None:
     value = total_real / (ms_max / 1e3)
 
     # roofline of the gather kernel: algorithmic bytes per launch / its time
-    n_launch = (valid + L - 1) // L
-    alg_gather = 13.0 * positions + 4.0 * real_tokens + 12.0 * valid * n_rows
+    n_launch = len(gather_ms) // K
+    alg_gather = 13.0 * positions + 4.0 * real_tokens + 12.0 * rows_pass
     bytes_per_launch = alg_gather / n_launch
     avg_launch_s = (sum(gather_ms) / len(gather_ms)) / 1e3
     peak, peak_kind = hbm_peak()
@@ -404,8 +467,8 @@ def run_ours(args, dist: Dist) -> None:
         tok_h = torch.from_numpy(c.tokens).pin_memory()
         off_h = torch.from_numpy(c.doc_offsets).pin_memory()
         ls_h = None if c.loss_start is None else torch.from_numpy(c.loss_start).pin_memory()
-        fp_h = torch.empty((c.max_steps, n_rows), dtype=torch.int64).pin_memory()
-        ln_h = torch.empty((c.max_steps, n_rows), dtype=torch.int32).pin_memory()
+        fp_h = torch.empty((c.max_steps, n_buf), dtype=torch.int64).pin_memory()
+        ln_h = torch.empty((c.max_steps, n_buf), dtype=torch.int32).pin_memory()
         bf_h = torch.empty(c.max_steps, dtype=torch.int64).pin_memory()
         tok_e = torch.empty_like(tok_d)
         off_e = torch.empty_like(off_d)
@@ -427,7 +490,7 @@ def run_ours(args, dist: Dist) -> None:
         torch.cuda.synchronize()
         e2e_s = dist.max(time.perf_counter() - t)
         h2d = tok_h.numel() * 4 + off_h.numel() * 8 + (0 if ls_h is None else ls_h.numel() * 4)
-        d2h = valid * n_rows * 12 + (valid * 8 if dist.world == 1 else 0)
+        d2h = rows_pass * 12 + (valid * 8 if dist.world == 1 else 0)
         if result is not None:
             result["e2e"] = {"value": dist.sum(real_tokens) * args.e2e_steps / e2e_s,
                              "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -440,21 +503,22 @@ def run_ours(args, dist: Dist) -> None:
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) ---------
     if result is not None and dist.world == 1 and not args.no_cpu_baseline:
         fp_gpu = fp_all[:valid].cpu().numpy().view(np.uint64)
-        result["cpu_baseline"] = cpu_baseline(c, args, valid, real_tokens, fp_gpu)
+        result["cpu_baseline"] = cpu_baseline(c, args, valid, real_tokens, fp_gpu,
+                                              variant_kwargs(c, args.variant))
 
     if result is not None:
         print(json.dumps(result), flush=True)
 
 
 
-def cpu_baseline(c, args, valid: int, real_tokens: int, fp_gpu=None) -> dict:
+def cpu_baseline(c, args, valid: int, real_tokens: int, fp_gpu=None, vk=None) -> dict:
     """Time the oracle as it stands (one host thread) on a bounded sample of
     the workload: its full build (hash, shuffle, pack, quotas over the whole
     corpus) plus the rows of the first `cpu_updates` updates; the rows time is
     scaled to all `valid` updates."""
     import oracle
     t = time.perf_counter()
-    o = oracle.Oracle(c)
+    o = oracle.Oracle(c, **(vk or {}))
     t_build = time.perf_counter() - t
     S = min(args.cpu_updates, valid)
     fps = []
@@ -481,7 +545,8 @@ def run_reference(args, dist: Dist) -> None:
     import oracle
     oracle.build()
     c = make_workload(args.config)
-    o = oracle.Oracle(c)
+    vk = variant_kwargs(c, args.variant)
+    o = oracle.Oracle(c, **vk)
     valid = o.valid_steps
     S = min(args.cpu_updates, valid)
     # real tokens of a pass, counted by the oracle itself (untimed)
@@ -493,7 +558,7 @@ def run_reference(args, dist: Dist) -> None:
 
     def ref_step():
         t = time.perf_counter()
-        oo = oracle.Oracle(c)
+        oo = oracle.Oracle(c, **vk)
         tb = time.perf_counter() - t
         t = time.perf_counter()
         for k in range(S):

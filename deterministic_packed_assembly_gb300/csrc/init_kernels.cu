@@ -473,9 +473,8 @@ __device__ __forceinline__ uint64_t feistel_walk(const uint64_t k[4], uint64_t n
 
 // Read order of windows: rank r of stream j reads window sG + sigma(r - sG)
 // within its segment s = r / G of min(G, W - sG) windows, sigma keyed by
-// (seed + 1, j, s); G = 0 reads windows in order ("the trainer reads each
-// source's windows of a segment in a random order", NeuronSpark-Trainer
-// README, Concepts).
+// (seed + 1, j, s); G = 0 reads windows in order (NeuronSpark-Trainer
+// README, Concepts: the windows of a segment are read in random order).
 __device__ __forceinline__ uint64_t window_of_rank(uint64_t seed, uint32_t j, uint32_t G,
                                                    uint64_t W, uint64_t r, int *err) {
   if (G == 0) return r;

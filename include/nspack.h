@@ -66,16 +66,18 @@ extern "C" {
  * NS_ERR_EXHAUSTED. */
 #define NS_PACK_DRAIN 1u
 /* Pack the validation stream: the held-out documents of every stream instead
- * of the kept ones ("each source's validation rows come from those of every
- * stratum", NeuronSpark-Trainer README, Concepts).  Same shuffle, packing,
+ * of the kept ones (NeuronSpark-Trainer README, Concepts: a source's
+ * validation rows are drawn from the held-out documents of all its strata).
+ * Same shuffle, packing,
  * quotas and assembly; a source with a held-out rate of 0 has no windows. */
 #define NS_PACK_HELDOUT 2u
 /* Shuffle the rows of every update: slot i holds the row that would otherwise
  * be row rho_k(i), rho_k a keyed permutation of [0, B) (seed + 2, update k). */
 #define NS_PACK_SHUFFLE_ROWS 4u
 /* Wrap packing: concatenate each stream's kept documents and cut the run into
- * windows of exactly T tokens, across document ends (the pipeline example's
- * pack_flat with algorithm "wrap", "Zephon: deterministic data loading").  A
+ * windows of exactly T tokens, across document ends (the flat packing with
+ * the wrap algorithm of the pipeline example in "Zephon: deterministic data
+ * loading").  A
  * piece is a document's run inside one window and its position ids start at
  * 0; a stream's last window may be partial (padded), and it counts only once
  * the whole stream is inside the reachable prefix. */
@@ -127,9 +129,9 @@ typedef struct {
   int32_t pad_id;    /* token written at padded positions */
   uint32_t window_segment; /* G > 0: each stream's windows are read in a shuffled
                               order within segments of G consecutive windows
-                              ("the trainer reads each source's windows of a
-                              segment in a random order", NeuronSpark-Trainer
-                              README, Concepts); 0: in order; at most
+                              (NeuronSpark-Trainer README, Concepts: the
+                              windows of a segment are read in random
+                              order); 0: in order; at most
                               NS_MAX_WINDOW_SEGMENT */
   /* Schedule (host, copied): pieces of the horizon with their own rows per
    * update and weights -- an append-only mixture schedule and a batch-size
@@ -147,9 +149,9 @@ typedef struct {
   const uint32_t *piece_source_weight; /* [n_pieces][n_sources], > 0 */
   const uint32_t *piece_stream_weight; /* [n_pieces][n_streams], > 0 */
   /* Row lengths reported in ns_pack_out.row_len: the row's real positions
-   * rounded up to a multiple of len_bucket, at most T ("packed lengths round
-   * up to a multiple of bucket, so few shapes compile", Linnet training docs,
-   * Other trainers); 0 reports the real length. */
+   * rounded up to a multiple of len_bucket, at most T (Linnet training docs,
+   * Other trainers: packed row lengths are rounded up to a bucket so that few
+   * shapes compile); 0 reports the real length. */
   uint32_t len_bucket;
   void *cuda_stream; /* cudaStream_t for init and default for the other calls */
   ns_alloc_fn alloc;

@@ -16,12 +16,14 @@
  *    document's text, 1 % per file (5 % for one source), the same in every
  *    line; documents of a file shuffled; every update holds each source within
  *    two samples of its recipe share; strata of a source at their share; cut
- *    at document ends; max_epochs 1 (a used-up source is an error).
+ *    at document ends; max_epochs 1 (a used-up source is an error); each
+ *    source's validation rows come from the held-out documents of every
+ *    stratum (a validation stream packs exactly those); the windows of a
+ *    segment are read in a random order.  Training: an append-only mixture
+ *    schedule and a batch-size ramp (pieces of the horizon).
  *  - "Zephon: deterministic data loading" (aixai.ru), the section on
  *    checkpointing on 16 GPUs and resuming on 8/32/64: every global batch is
  *    byte-identical (SHA-256) whatever the GPU count.
- *    Each source's validation rows come from the held-out documents of
- *    every stratum (same section); a validation stream packs exactly those.
  *  - Linnet training docs, Supervised fine-tuning: rows of exactly T
  *    positions, padded; only the completion is learned; each step weighs by
  *    its count of learned positions.  Other trainers: a position id of 0
@@ -101,7 +103,8 @@ typedef struct {
 
 typedef struct {
   uint32_t doc; /* global document index */
-  uint32_t off; /* offset of the piece inside its document (multiple of T) */
+  uint32_t off; /* offset of the piece inside its document (a multiple of T
+                   under greedy packing; anywhere under wrap packing) */
   uint32_t len; /* 1..T */
 } or_piece;
 
@@ -186,7 +189,7 @@ uint64_t or_feistel_pi(uint64_t seed, uint32_t stream, uint64_t n, uint64_t p) {
 }
 
 /* ---- the order in which windows and rows are read ----------------------
- * "The trainer reads each source's windows of a segment in a random order"
+ * The trainer reads the windows of a segment of each source in random order
  * (NeuronSpark-Trainer README, Concepts).  With a window segment of G > 0 the
  * windows of stream j are grouped in segments of G consecutive windows (the
  * last one shorter); rank r of segment s = r / G reads window
@@ -630,8 +633,8 @@ uint64_t or_row_fp(const int32_t *tok, const int32_t *pos, const int32_t *doc,
 /* ---- assembly of rows [row0, row1) of update `step` ----------------------
  * Each row also reports its length: its real positions (the window's tokens,
  * which come first), rounded up to a multiple of len_bucket when that is set
- * ("packed lengths round up to a multiple of bucket", Linnet training docs,
- * Other trainers).
+ * (Linnet training docs, Other trainers: packed row lengths are rounded up to
+ * a bucket so that few shapes compile).
  * Rows are ordered by (source, stratum, rank), unless shuffled; a rank reads
  * its window through the window order above.  A window's pieces are copied
  * in order; pos is the offset inside the piece (0 starts a new sequence);
