@@ -337,12 +337,20 @@ def run_ours(args, dist: Dist) -> None:
     gathered = [torch.cuda.Event() for _ in range(2)]
     folded = [torch.cuda.Event() for _ in range(2)]
 
-    state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0}
+    state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0,
+             "init_events": []}
 
     def one_pass(record: bool, count: bool = False, e2e=None):
         """One whole pass; returns real tokens assembled when `count`."""
+        if record:
+            ei0 = torch.cuda.Event(enable_timing=True)
+            ei1 = torch.cuda.Event(enable_timing=True)
+            ei0.record(stream)
         pk = Packer(tok_d if e2e is None else e2e[0], off_d if e2e is None else e2e[1],
                     ls_d if e2e is None else e2e[2], stream=stream, **rk)
+        if record:
+            ei1.record(stream)
+            state["init_events"].append((ei0, ei1))
         valid = pk.valid_steps
         state["valid"] = valid
         state["init_launches"] = pk.info["init_launches"]
@@ -400,6 +408,7 @@ def run_ours(args, dist: Dist) -> None:
 
     def timed(K: int):
         state["events"].clear()
+        state["init_events"].clear()
         sampler = ClockSampler(gpu_id_for(device)) if dist.rank == 0 else None
         dist.barrier()
         torch.cuda.synchronize()
@@ -414,6 +423,7 @@ def run_ours(args, dist: Dist) -> None:
         clocks = sampler.stop() if sampler else None
         ms = t0.elapsed_time(t1)
         gather_ms = [a.elapsed_time(b) for a, b in state["events"]]
+        state["init_ms"] = float(np.mean([a.elapsed_time(b) for a, b in state["init_events"]]))
         return ms, gather_ms, clocks
 
     K = args.steps
@@ -450,6 +460,7 @@ def run_ours(args, dist: Dist) -> None:
             "data": f"synthetic (numpy PCG64, data seed {c.notes.get('data_seed')})",
             "config": cfg,
             "positions_per_s": dist.sum(positions) * K / (ms_max / 1e3),
+            "init_ms_per_step": state["init_ms"],
             "alg_gbps_step": alg_step * K / (ms_max / 1e3) / 1e9,
             "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,

@@ -306,19 +306,9 @@ __global__ void row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, u
 // Held-out hash.  acc_d = sum_i splitmix64((i << 32) | u32 tok_i),
 // h_d = splitmix64(acc_d ^ splitmix64(hash_key + L_d)); held out iff
 // floor(h_d * 10000 / 2^64) < bp of the document's source.  One warp per
-// document; aligned 16-byte loads that always hold at least one token of it.
-__device__ __forceinline__ uint64_t hash_terms(int4 v, int64_t g, int64_t o0, int64_t o1) {
-  uint64_t s = 0;
-  const int32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; q++) {
-    int64_t idx = g + q;
-    if (idx >= o0 && idx < o1)
-      s += splitmix64(((uint64_t)(idx - o0) << 32) | (uint64_t)(uint32_t)e[q]);
-  }
-  return s;
-}
-
+// document, reading aligned 16-byte blocks that each hold at least one of its
+// tokens, four blocks per lane in flight (512 tokens per warp step).
+//
 // Four tokens that all lie inside the document, the first at in-document
 // index i0 (documents are shorter than 2^31 tokens).
 __device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
@@ -328,28 +318,44 @@ __device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
          splitmix64(((uint64_t)(i0 + 3) << 32) | (uint32_t)v.w);
 }
 
-// The whole warp hashes tokens[o0, o1); every lane returns the document's h.
-__device__ __forceinline__ uint64_t warp_doc_hash(const int32_t *__restrict__ tokens, int64_t o0,
-                                                  int64_t o1, uint64_t hash_key, int lane) {
+// Terms of a block whose first token has in-document index i0 (may be
+// negative), only indexes in [0, L).
+__device__ __forceinline__ uint64_t block_terms_edge(int4 v, int32_t i0, uint32_t L) {
+  const int32_t e[4] = {v.x, v.y, v.z, v.w};
+  uint64_t s = 0;
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    const int32_t i = i0 + q;
+    if (i >= 0 && (uint32_t)i < L)
+      s += splitmix64(((uint64_t)(uint32_t)i << 32) | (uint64_t)(uint32_t)e[q]);
+  }
+  return s;
+}
+
+// The whole warp sums the token terms of tokens[o0, o0 + L); every lane gets
+// the sum.  Offsets are taken relative to the 16-byte block holding the
+// first token, in 32 bits (documents are shorter than 2^31 tokens).
+__device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ tokens, int64_t o0,
+                                                   uint32_t L, int lane) {
+  const int64_t a0 = o0 & ~(int64_t)3;
+  const uint32_t sh = (uint32_t)(o0 - a0);
+  const int4 *base = reinterpret_cast<const int4 *>(tokens + a0);
+  const uint32_t end = L + sh;
   uint64_t acc = 0;
-  for (int64_t g = (o0 & ~(int64_t)3) + 4 * lane; g < o1; g += 256) {
-    const int4 v0 = __ldcs(reinterpret_cast<const int4 *>(tokens + g));
-    const bool has1 = g + 128 < o1;
-    int4 v1 = make_int4(0, 0, 0, 0);
-    if (has1) v1 = __ldcs(reinterpret_cast<const int4 *>(tokens + g + 128));
-    if (g >= o0 && g + 3 < o1)
-      acc += hash_terms_inside(v0, (uint32_t)(g - o0));
-    else
-      acc += hash_terms(v0, g, o0, o1);
-    if (has1) {
-      if (g + 128 + 3 < o1)
-        acc += hash_terms_inside(v1, (uint32_t)(g + 128 - o0));
-      else
-        acc += hash_terms(v1, g + 128, o0, o1);
+  for (uint32_t r = 4 * lane; r < end; r += 512) {
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const uint32_t ru = r + 128 * u;
+      if (u == 0 || ru < end) {  // r < end holds for u = 0
+        const int4 v = __ldcs(base + (ru >> 2));
+        if (ru >= sh && ru + 4 <= end)
+          acc += hash_terms_inside(v, ru - sh);
+        else
+          acc += block_terms_edge(v, (int32_t)ru - (int32_t)sh, L);
+      }
     }
   }
-  acc = warp_sum_u64(acc);
-  return splitmix64(acc ^ splitmix64(hash_key + (uint64_t)(o1 - o0)));
+  return warp_sum_u64(acc);
 }
 
 // Held-out flags for the prefix of every stream the horizon reaches.  A
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(kThreads)
   constexpr uint32_t kGrab = 8;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  bool ready_seen = false;
   for (uint32_t jj = 0; jj < J; jj++) {
     const uint32_t j = (warp_id + jj) % J;
     const uint32_t bp = stream_bp[j];
@@ -385,10 +392,14 @@ __global__ void __launch_bounds__(kThreads)
     while (true) {
       unsigned long long base = 0;
       if (lane == 0) {
-        if (need == ~0ull && *reinterpret_cast<const volatile unsigned *>(ready) >= ready_at) {
-          __threadfence();
-          need = (unsigned long long)windows_needed(
-                     *reinterpret_cast<const volatile int32_t *>(cum_last + j), G) * T;
+        if (need == ~0ull) {
+          if (!ready_seen && *reinterpret_cast<const volatile unsigned *>(ready) >= ready_at) {
+            __threadfence();
+            ready_seen = true;
+          }
+          if (ready_seen)
+            need = (unsigned long long)windows_needed(
+                       *reinterpret_cast<const volatile int32_t *>(cum_last + j), G) * T;
         }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
         base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
@@ -405,19 +416,25 @@ __global__ void __launch_bounds__(kThreads)
         L_l = klen[idx];
         if (L_l) o_l = __ldg(offs + order[idx]);
       }
-      unsigned long long kept_here = 0;
+      uint64_t mine = 0;  // lane q: the token-term sum of document q
       for (int q = 0; q < (int)(pend - base); q++) {
         const uint32_t L = __shfl_sync(0xffffffffu, L_l, q);
         if (L == 0) continue;
         const int64_t o0 = __shfl_sync(0xffffffffu, o_l, q);
-        const uint64_t h = warp_doc_hash(tokens, o0, o0 + L, hash_key, lane);
-        const uint32_t held = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1u : 0u;
-        if (held != want_heldout) {
-          if (lane == 0) klen[base_pos + base + q] = 0;
-        } else {
-          kept_here += L;
-        }
+        const uint64_t tot = warp_doc_terms(tokens, o0, L, lane);
+        if (lane == q) mine = tot;
       }
+      // lane q decides document q
+      unsigned long long kept_here = 0;
+      if (L_l) {
+        const uint64_t h = splitmix64(mine ^ splitmix64(hash_key + L_l));
+        const uint32_t held = (__umul64hi(h, 10000ull) < (uint64_t)bp) ? 1u : 0u;
+        if (held != want_heldout)
+          klen[base_pos + base + lane] = 0;
+        else
+          kept_here = L_l;
+      }
+      kept_here = warp_sum_u64(kept_here);
       if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
     }
   }
