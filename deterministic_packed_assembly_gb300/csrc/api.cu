@@ -42,6 +42,7 @@ struct ns_pack_ctx {
   int32_t *node_doc = nullptr, *node_mthr = nullptr;
   int *err = nullptr;
   uint64_t *fp_out = nullptr;
+  uint64_t *pad_tail = nullptr;
   std::vector<void *> kept;
 };
 
@@ -284,6 +285,15 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->err);
   c->fp_out = a.keep<uint64_t>(1);
   NS_ALLOC(c->fp_out);
+  // fingerprint terms of padding, per tile of a row, for the gather
+  {
+    const uint32_t n_tiles = (T + 127) / 128;
+    c->pad_tail = a.keep<uint64_t>(n_tiles + 1);
+    uint64_t *tiles = a.temp<uint64_t>(n_tiles);
+    NS_ALLOC(c->pad_tail);
+    NS_ALLOC(tiles);
+    NS_CK(nsk::launch_pad_tail(c->pad_id, T, tiles, c->pad_tail, st));
+  }
   NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
 
   // ---- 1. quotas of every update, on a side stream ------------------------
@@ -627,6 +637,7 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   p.row_learned = out->row_learned;
   p.row_len = out->row_len;
   p.len_bucket = ctx->len_bucket;
+  p.pad_tail = ctx->pad_tail;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_gather(p, st) != cudaSuccess) {
     cudaGetLastError();

@@ -243,6 +243,9 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
   __stcs(reinterpret_cast<int4 *>(p.pos_out + obase + tp), ps);
   __stcs(reinterpret_cast<int4 *>(p.doc_out + obase + tp), dc);
   __stcs(reinterpret_cast<unsigned int *>(p.mask_out + obase + tp), mk);
+  // an all-padding tile's terms come from the context's table of padding
+  // sums (added once per row by the last warp)
+  if (m.kind == 0) return;
   acc += fp_term(tk.x, ps.x, dc.x, mk & 1u, tp);
   acc += fp_term(tk.y, ps.y, dc.y, (mk >> 8) & 1u, tp + 1);
   acc += fp_term(tk.z, ps.z, dc.z, (mk >> 16) & 1u, tp + 2);
@@ -285,7 +288,7 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
   }
 }
 
-__global__ void __launch_bounds__(kGatherWarps * 32)
+__global__ void __launch_bounds__(kGatherWarps * 32, 5)
     gather_kernel(const GatherParams p) {
   __shared__ __align__(16) int32_t s_tok[kGatherWarps][kStages][kStageWords];
   __shared__ TileMeta s_meta[kGatherWarps][kStages];
@@ -362,7 +365,9 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     __threadfence_block();
     if (atomicAdd(&s_done, 1) == kGatherWarps - 1) {
       __threadfence_block();
-      const uint64_t a = *reinterpret_cast<volatile unsigned long long *>(&s_acc);
+      // tiles from the first one at or after `used` are all padding
+      const uint64_t a = *reinterpret_cast<volatile unsigned long long *>(&s_acc) +
+                         __ldg(p.pad_tail + ((uint32_t)used + kTile - 1) / kTile);
       p.row_fp[blk] = splitmix64(a);
       p.row_learned[blk] = *reinterpret_cast<volatile int *>(&s_learned);
       if (p.row_len) {
@@ -397,7 +402,79 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) out[blockIdx.x] = F;
 }
 
+// Padding sums per tile: tile k (positions [128k, min(128k + 128, T))) of
+// a row of padding; then suffix sums, pad_tail[k] = the terms of positions
+// [128k, T), pad_tail[n_tiles] = 0.
+__global__ void __launch_bounds__(256)
+    pad_tiles_kernel(int32_t pad_id, uint32_t T, uint32_t n_tiles, uint64_t *__restrict__ tile) {
+  const uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (k >= n_tiles) return;
+  uint64_t acc = 0;
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const uint32_t t = k * kTile + 4 * lane + e;
+    if (t < T) acc += fp_term(pad_id, 0, -1, 0u, t);
+  }
+  acc = warp_sum_u64(acc);
+  if (lane == 0) tile[k] = acc;
+}
+
+__global__ void __launch_bounds__(1024)
+    pad_suffix_kernel(const uint64_t *__restrict__ tile, uint32_t n_tiles,
+                      uint64_t *__restrict__ pad_tail) {
+  __shared__ uint64_t s_w[32];
+  __shared__ uint64_t s_carry;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_carry = 0;
+    pad_tail[n_tiles] = 0;
+  }
+  __syncthreads();
+  // chunks of 1024 tiles from the end: suffix sum = carry + inclusive sum of
+  // the reversed chunk
+  for (uint32_t c0 = 0; c0 < n_tiles; c0 += 1024) {
+    const uint32_t r = c0 + threadIdx.x;                // reversed index
+    const uint64_t v = r < n_tiles ? tile[n_tiles - 1 - r] : 0;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_w[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      uint64_t z = s_w[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, z, o);
+        if (lane >= o) z += y;
+      }
+      s_w[lane] = z;
+    }
+    __syncthreads();
+    const uint64_t incl = s_carry + (w ? s_w[w - 1] : 0) + x;
+    if (r < n_tiles) pad_tail[n_tiles - 1 - r] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += s_w[31];
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pad_tail(int32_t pad_id, uint32_t T, uint64_t *tile_scratch,
+                            uint64_t *pad_tail, cudaStream_t st) {
+  const uint32_t n_tiles = (T + kTile - 1) / kTile;
+  ++launch_counter();
+  pad_tiles_kernel<<<(n_tiles * 32 + 255) / 256, 256, 0, st>>>(pad_id, T, n_tiles, tile_scratch);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++launch_counter();
+  pad_suffix_kernel<<<1, 1024, 0, st>>>(tile_scratch, n_tiles, pad_tail);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
   const uint64_t n = (uint64_t)p.n_steps * p.n_rows;

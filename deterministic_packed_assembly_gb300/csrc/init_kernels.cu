@@ -342,18 +342,35 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
   const int4 *base = reinterpret_cast<const int4 *>(tokens + a0);
   const uint32_t end = L + sh;
   uint64_t acc = 0;
-  for (uint32_t r = 4 * lane; r < end; r += 512) {
+  int4 v[4];
+  uint32_t r = 4 * lane;
+#pragma unroll
+  for (int u = 0; u < 4; u++) {
+    const uint32_t ru = r + 128 * u;
+    v[u] = make_int4(0, 0, 0, 0);
+    if (ru < end) v[u] = __ldcs(base + (ru >> 2));
+  }
+  for (; r < end; r += 512) {
+    // the next step's four loads go out before this step's terms
+    int4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const uint32_t ru = r + 512 + 128 * u;
+      w[u] = make_int4(0, 0, 0, 0);
+      if (ru < end) w[u] = __ldcs(base + (ru >> 2));
+    }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const uint32_t ru = r + 128 * u;
-      if (u == 0 || ru < end) {  // r < end holds for u = 0
-        const int4 v = __ldcs(base + (ru >> 2));
+      if (ru < end) {
         if (ru >= sh && ru + 4 <= end)
-          acc += hash_terms_inside(v, ru - sh);
+          acc += hash_terms_inside(v[u], ru - sh);
         else
-          acc += block_terms_edge(v, (int32_t)ru - (int32_t)sh, L);
+          acc += block_terms_edge(v[u], (int32_t)ru - (int32_t)sh, L);
       }
     }
+#pragma unroll
+    for (int u = 0; u < 4; u++) v[u] = w[u];
   }
   return warp_sum_u64(acc);
 }
@@ -368,7 +385,7 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // kept tokens below it exceed need_j unless the whole stream was hashed, so
 // the prefix the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
@@ -1151,7 +1168,7 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
                                unsigned long long *frontier, unsigned long long *kept, int n_sms,
                                cudaStream_t st) {
   ++launch_counter();
-  hash_prefix_kernel<<<n_sms * 8, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
+  hash_prefix_kernel<<<n_sms * 4, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
                                                      klen, cum_last, ready, ready_at, T, G,
                                                      hash_key, want_heldout, frontier, kept);
   return cudaGetLastError();

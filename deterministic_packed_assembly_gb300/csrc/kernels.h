@@ -160,8 +160,13 @@ struct GatherParams {
   int32_t *row_learned;
   int32_t *row_len;         // [n_steps][rows] or null
   uint32_t len_bucket;
+  const uint64_t *pad_tail;  // [T/128 + 1]: fingerprint terms of padding from tile k on
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
+// pad_tail[k] = the sum of the fingerprint terms of a padding row's positions
+// [128k, T); tile_scratch holds ceil(T / 128) words.
+cudaError_t launch_pad_tail(int32_t pad_id, uint32_t T, uint64_t *tile_scratch,
+                            uint64_t *pad_tail, cudaStream_t st);
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
                             uint64_t *out, cudaStream_t st);
 
