@@ -120,3 +120,38 @@ def test_full_size_long_context_full_pass_exactly_once():
     assert real == learned == c.n_tokens
     w, complete = pk.stream_windows()
     assert complete[0] and w[0] == o.n_windows(0)
+
+
+@pytest.mark.parametrize("variant", ["heldout", "shuffled", "wrap", "schedule"])
+def test_full_size_bench_variants(variant):
+    # each packing option the benchmark times, on the benchmark's workload and
+    # in its launch plan (32 updates per launch, never across a schedule piece)
+    import torch
+    import bench
+    c = _setup("c3")[0]
+    kw = bench.variant_kwargs(c, variant)
+    pk, o = packer_for(c, **kw), oracle_for(c, **kw)
+    assert pk.valid_steps == o.valid_steps > 0
+    assert pk.order_digest == o.digest
+    q, cum = pk.quota_table()
+    oq, ocum, _ = o.quota()
+    assert (q == oq).all() and (cum == ocum).all()
+    w, complete = pk.stream_windows()
+    for j in range(c.n_streams):
+        if complete[j]:
+            assert w[j] == o.n_windows(j)
+        else:
+            assert ocum[-1, j] <= w[j] <= o.n_windows(j)
+    v = o.valid_steps
+    plan = list(bench.launch_plan(pk, v, LAUNCH))
+    want_steps = sorted({0, 1, v // 3, v // 2, v - 1} & set(range(v)))
+    for s0, n, Bk in plan:
+        hits = [k for k in want_steps if s0 <= k < s0 + n]
+        if not hits:
+            continue
+        got = to_host(pk.step(s0, n_steps=n, rows=(0, Bk)))
+        for k in hits:
+            assert_rows_equal({f: x[k - s0] for f, x in got.items()}, o.rows(k), f"update {k}")
+    pk.close()
+    del pk
+    torch.cuda.empty_cache()
