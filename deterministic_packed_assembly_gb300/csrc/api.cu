@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -56,13 +57,22 @@ void dev_free(ns_pack_ctx *c, void *p) {
     cudaFree(p);
 }
 
+// Device memory of one init.  Small requests are carved out of slabs that
+// grow geometrically (1 MiB, 2 MiB, ... up to 64 MiB), large ones get their
+// own allocation, so an init makes a handful of allocator calls instead of
+// one per table.  Tables the context keeps and temporaries of the init come
+// from separate slabs; the temporaries go back when the init ends.
 struct Arena {
+  struct Slab {
+    char *base = nullptr;
+    size_t size = 0, used = 0, next = 1u << 20;
+  };
+  static constexpr size_t kMaxSlab = 64u << 20;
   ns_pack_ctx *c;
   std::vector<void *> temps;
+  Slab keep_slab, temp_slab;
   explicit Arena(ns_pack_ctx *ctx) : c(ctx) {}
-  void *get(size_t bytes, bool keep) {
-    bytes = ((bytes + 255) / 256) * 256;
-    if (bytes == 0) bytes = 256;
+  void *raw(size_t bytes, bool keep) {
     void *p = nullptr;
     if (c->alloc) {
       p = c->alloc(bytes, c->user);
@@ -79,6 +89,24 @@ struct Arena {
     }
     return p;
   }
+  void *get(size_t bytes, bool keep) {
+    bytes = ((bytes + 255) / 256) * 256;
+    if (bytes == 0) bytes = 256;
+    Slab &s = keep ? keep_slab : temp_slab;
+    if (s.base && s.used + bytes <= s.size) {
+      void *p = s.base + s.used;
+      s.used += bytes;
+      return p;
+    }
+    if (bytes * 2 > s.next) return raw(bytes, keep);  // large: its own allocation
+    char *b = static_cast<char *>(raw(s.next, keep));
+    if (!b) return nullptr;
+    s.base = b;
+    s.size = s.next;
+    s.used = bytes;
+    s.next = std::min(s.next * 2, kMaxSlab);
+    return b;
+  }
   template <class T>
   T *keep(size_t n) {
     return static_cast<T *>(get(n * sizeof(T), true));
@@ -90,6 +118,7 @@ struct Arena {
   void release() {
     for (void *p : temps) dev_free(c, p);
     temps.clear();
+    temp_slab = Slab();
   }
 };
 
@@ -201,6 +230,28 @@ struct SideStream {
   }
 };
 
+// Host arrays gathered into one buffer and copied to the device in one call.
+struct Staging {
+  std::vector<unsigned char> host;
+  std::vector<std::pair<size_t, void **>> slots;
+  void add(const void *p, size_t bytes, void **dev) {
+    const size_t off = (host.size() + 255) / 256 * 256;
+    host.resize(off + std::max<size_t>(bytes, 1));
+    if (bytes) std::memcpy(host.data() + off, p, bytes);
+    slots.emplace_back(off, dev);
+  }
+  int commit(Arena &a, cudaStream_t st) {
+    unsigned char *d = static_cast<unsigned char *>(a.get(host.size(), false));
+    if (!d) return NS_ERR_OOM;
+    if (cudaMemcpyAsync(d, host.data(), host.size(), cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return NS_ERR_CUDA;
+    }
+    for (auto &s : slots) *s.second = d + s.first;
+    return NS_OK;
+  }
+};
+
 int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st) {
   *dev = a.get(bytes, false);
   NS_ALLOC(*dev);
@@ -237,13 +288,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   void *d_sdb, *d_ssrc, *d_sw, *d_tw, *d_sbp, *d_stream_bp, *d_src_first;
   int rc;
-  if ((rc = upload(a, sdb.data(), sdb.size() * 4, &d_sdb, st))) return rc;
-  if ((rc = upload(a, ssrc.data(), ssrc.size() * 4, &d_ssrc, st))) return rc;
-  if ((rc = upload(a, sw.data(), sw.size() * 4, &d_sw, st))) return rc;
-  if ((rc = upload(a, tw.data(), tw.size() * 4, &d_tw, st))) return rc;
-  if ((rc = upload(a, sbp.data(), sbp.size() * 2, &d_sbp, st))) return rc;
-  if ((rc = upload(a, stream_bp.data(), stream_bp.size() * 2, &d_stream_bp, st))) return rc;
-  if ((rc = upload(a, src_first.data(), src_first.size() * 4, &d_src_first, st))) return rc;
+  Staging up;
+  up.add(sdb.data(), sdb.size() * 4, &d_sdb);
+  up.add(ssrc.data(), ssrc.size() * 4, &d_ssrc);
+  up.add(sw.data(), sw.size() * 4, &d_sw);
+  up.add(tw.data(), tw.size() * 4, &d_tw);
+  up.add(sbp.data(), sbp.size() * 2, &d_sbp);
+  up.add(stream_bp.data(), stream_bp.size() * 2, &d_stream_bp);
+  up.add(src_first.data(), src_first.size() * 4, &d_src_first);
   // the schedule: one piece (B, the weights) without one
   const uint32_t P = cfg->n_pieces ? cfg->n_pieces : 1;
   std::vector<uint32_t> psw((size_t)P * S), ptw((size_t)P * J);
@@ -259,12 +311,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     ptw = tw;
   }
   void *d_pbegin, *d_pB, *d_psw, *d_ptw;
-  if ((rc = upload(a, c->piece_begin.data(), (size_t)P * 4, &d_pbegin, st))) return rc;
-  if ((rc = upload(a, c->piece_B.data(), (size_t)P * 4, &d_pB, st))) return rc;
-  if ((rc = upload(a, psw.data(), psw.size() * 4, &d_psw, st))) return rc;
-  if ((rc = upload(a, ptw.data(), ptw.size() * 4, &d_ptw, st))) return rc;
-  const nsk::QuotaPieces qp{static_cast<uint32_t *>(d_pbegin), static_cast<uint32_t *>(d_pB),
-                            static_cast<uint32_t *>(d_psw), static_cast<uint32_t *>(d_ptw), P};
+  up.add(c->piece_begin.data(), (size_t)P * 4, &d_pbegin);
+  up.add(c->piece_B.data(), (size_t)P * 4, &d_pB);
+  up.add(psw.data(), psw.size() * 4, &d_psw);
+  up.add(ptw.data(), ptw.size() * 4, &d_ptw);
   // the schedule's digest items: count, then per piece begin, B, weights
   std::vector<uint64_t> piece_items;
   if (cfg->n_pieces) {
@@ -277,9 +327,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     }
   }
   void *d_piece_items = nullptr;
-  if (!piece_items.empty() &&
-      (rc = upload(a, piece_items.data(), piece_items.size() * 8, &d_piece_items, st)))
-    return rc;
+  if (!piece_items.empty()) up.add(piece_items.data(), piece_items.size() * 8, &d_piece_items);
+  if ((rc = up.commit(a, st))) return rc;
+  if (piece_items.empty()) d_piece_items = nullptr;
+  const nsk::QuotaPieces qp{static_cast<uint32_t *>(d_pbegin), static_cast<uint32_t *>(d_pB),
+                            static_cast<uint32_t *>(d_psw), static_cast<uint32_t *>(d_ptw), P};
 
   c->err = a.keep<int>(1);
   NS_ALLOC(c->err);
