@@ -65,3 +65,37 @@ def test_rank_slices_concatenate_to_the_global_batch():
         parts = [o.rows(3, *bench.row_slice(r, world, c.B)) for r in range(world)]
         for k in full:
             assert np.array_equal(np.concatenate([p[k] for p in parts]), full[k])
+
+
+def test_schedule_launch_plan_slices_cover_every_update():
+    # the benchmark's launches never cross a schedule piece, and under any rank
+    # count the ranks' slices of each launch concatenate to the global rows
+    import bench
+    import oracle
+    from corpus import make_preset
+    c = make_preset("c1")
+    kw = bench.variant_kwargs(c, "schedule")
+
+    class Plan:
+        schedule = kw["schedule"]
+
+        @staticmethod
+        def rows_of_step(k):
+            return [p["B"] for p in kw["schedule"] if p["begin"] <= k][-1]
+
+    o = oracle.Oracle(c, **kw)
+    v = o.valid_steps
+    assert v > 0
+    plan = list(bench.launch_plan(Plan, v, 3))
+    assert [s for s, _, _ in plan] == sorted(s for s, _, _ in plan)
+    assert sum(m for _, m, _ in plan) == v
+    for s0, m, Bk in plan:
+        assert all(Plan.rows_of_step(s0 + q) == Bk for q in range(m))
+    for world in (2, 3):
+        for s0, m, Bk in plan:
+            for q in range(m):
+                parts = [o.rows(s0 + q, *bench.row_slice(r, world, Bk)) for r in range(world)
+                         if bench.row_slice(r, world, Bk)[1] > bench.row_slice(r, world, Bk)[0]]
+                full = o.rows(s0 + q)
+                for f in full:
+                    assert np.array_equal(np.concatenate([p[f] for p in parts]), full[f])
