@@ -9,12 +9,13 @@
  *
  * What the operations compute, and where it is stated:
  *  - held-out split: 1 % of every source's documents (5 % for one source), by
- *    a hash of the document's text, the same in every line -- NeuronSpark-
- *    Trainer README, Concepts;
+ *    a hash of the document's content that no line's seed changes --
+ *    NeuronSpark-Trainer README, Concepts;
  *  - shuffle: a file's documents are visited in a seed-keyed random order --
  *    same section;
- *  - mixture: every update holds each source within two samples of its
- *    recipe share, and each stratum of a source at its share -- same section;
+ *  - mixture: in every update each source's window count is at most two
+ *    off its recipe share, and each stratum of a source at its share -- same
+ *    section;
  *  - packing: windows of exactly T positions, cut at document ends, padded at
  *    the end -- same section, and Linnet training docs, Supervised
  *    fine-tuning; a document longer than T is cut into T-chunks;
@@ -26,7 +27,7 @@
  *  - elastic determinism: every global batch is byte-identical whatever the
  *    number of GPUs -- "Zephon: deterministic data loading", checkpoint on 16
  *    GPUs, resume on 8/32/64;
- *  - max_epochs 1: a used-up source is an error, not a second pass --
+ *  - max_epochs 1: running out of a source is an error, never another epoch --
  *    NeuronSpark-Trainer README, Concepts; a resume checks the sample order's
  *    digest -- same README, Training.
  *
@@ -121,7 +122,7 @@ typedef struct {
   const uint32_t *stream_weight;     /* [n_streams], > 0, relative within its source */
   const uint16_t *source_heldout_bp; /* [n_sources], 0 .. 10000 basis points */
   uint64_t seed;     /* keys the shuffle */
-  uint64_t hash_key; /* keys the held-out hash (not the seed: same in every line) */
+  uint64_t hash_key; /* keys the held-out hash (not the seed, so every line agrees) */
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
   uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS |

@@ -16,7 +16,7 @@
  *    document's text, 1 % per file (5 % for one source), the same in every
  *    line; documents of a file shuffled; every update holds each source within
  *    two samples of its recipe share; strata of a source at their share; cut
- *    at document ends; max_epochs 1 (a used-up source is an error); each
+ *    at document ends; max_epochs 1 (running out of a source stops with an error); each
  *    source's validation rows come from the held-out documents of every
  *    stratum (a validation stream packs exactly those); the windows of a
  *    segment are read in a random order.  Training: an append-only mixture

@@ -2,9 +2,9 @@
 
 * Zephon blog (checkpoint on 16 GPUs, resume on 8/32/64): a global batch is
   byte-identical however it is computed -- here, however its rows are sliced.
-* NeuronSpark-Trainer README, Concepts: max_epochs 1, a used-up source is an
-  error, not a second pass; Training: a resume checks the sample order's
-  digest.
+* NeuronSpark-Trainer README, Concepts: max_epochs 1, running out of a
+  source is an error rather than another epoch; Training: a resume checks
+  the sample order's digest.
 * Linnet training docs, Reinforcement learning / JAX: a short last step is
   filled with rows that learn nothing.
 """

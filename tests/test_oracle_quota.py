@@ -11,7 +11,7 @@ the one whose sorted cumulative shortfalls are lexicographically smallest
 Per update a child gets at most one window more or less than its exact share
 (at most, not strictly less: a child whose exact share is a whole number can
 still take an extra window when its cumulative shortfall is the largest), so
-every source stays within two samples of its share.
+no source's count is ever more than two windows off its share.
 """
 import itertools
 from fractions import Fraction
