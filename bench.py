@@ -75,7 +75,12 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="c3", choices=sorted(WORKLOADS))
-    ap.add_argument("--launch", type=int, default=32, help="updates per ns_pack_step launch")
+    ap.add_argument("--launch", type=int, default=0,
+                    help="updates per ns_pack_step launch (0: enough for about 2^26 positions "
+                         "per launch, see auto_launch)")
+    ap.add_argument("--slices", type=int, default=1,
+                    help="split every launch into this many row-slice launches (the same "
+                         "bytes per row; batch folds are skipped when > 1)")
     ap.add_argument("--variant", default="default", choices=sorted(VARIANTS),
                     help="packing options of the pass (validation stream, read-order "
                          "shuffles, wrap packing, schedule)")
@@ -276,6 +281,13 @@ def variant_kwargs(c, name: str) -> dict:
     return {}
 
 
+def auto_launch(max_steps: int, rows: int, T: int) -> int:
+    """Updates per launch: about 2^26 positions (tens of thousands of CTAs'
+    worth of rows), at most the horizon.  32 for the 512 x 4096 and 256 x 8192
+    workloads and for 64 x 32768; the whole horizon for 8 x 4096."""
+    return max(1, min(max_steps, -(-(1 << 26) // max(1, rows * T))))
+
+
 def launch_plan(pk, valid: int, L: int):
     """(first update, updates, rows per update) of each launch: at most L
     updates, never across a schedule piece (rows per update may change)."""
@@ -293,7 +305,7 @@ def config_block(c, args, dist: Dist, rows) -> dict:
             "variant": f"{args.variant}: {VARIANTS[args.variant]}",
             "n_docs": c.n_docs, "n_tokens": c.n_tokens, "T": c.T, "B": c.B,
             "updates_per_step": None, "rows_per_rank": rows[1] - rows[0],
-            "launch_updates": args.launch,
+            "launch_updates": args.launch, "row_slices_per_launch": args.slices,
             "l2": "inputs larger than L2 (corpus %.1f GB, output buffer > 129 MB)"
                   % (c.n_tokens * 4 / 1e9),
             "parallelism": f"rows split over {dist.world} GPU(s), tables replicated"}
@@ -318,8 +330,9 @@ def run_ours(args, dist: Dist) -> None:
     ls_d = None if c.loss_start is None else torch.from_numpy(c.loss_start).to(device)
     torch.cuda.synchronize()
 
-    L = args.launch
     n_buf = -(-c.B // dist.world)  # bounds this rank's rows of any update
+    L = args.launch or auto_launch(c.max_steps, n_buf, c.T)
+    args.launch = L
     n_pos = L * n_buf * c.T
     # flat buffers, viewed [updates][rows][T] per launch (a schedule changes
     # the rows per update)
@@ -364,8 +377,8 @@ def run_ours(args, dist: Dist) -> None:
                 continue
             rows_total += m * r
             b = li % 2
-            if li >= 2:
-                stream.wait_event(folded[b])
+            if li >= 2 and dist.world == 1 and args.slices <= 1:
+                stream.wait_event(folded[b])  # the fold of two launches ago is done with b
             view = {k: v[:m * r * c.T].view(m, r, c.T) for k, v in out.items()}
             view["row_fp"] = row_fp[b][:m * r].view(m, r)
             view["row_learned"] = row_ln[b][:m * r].view(m, r)
@@ -373,12 +386,24 @@ def run_ours(args, dist: Dist) -> None:
                 ea = torch.cuda.Event(enable_timing=True)
                 eb = torch.cuda.Event(enable_timing=True)
                 ea.record(stream)
-            pk.step(s0, m, rows=(rk0, rk1), out=view, stream=stream)
-            n += 1
+            if args.slices <= 1:
+                pk.step(s0, m, rows=(rk0, rk1), out=view, stream=stream)
+                n += 1
+            else:
+                # R launches of row slices, each into its own contiguous region
+                for si in range(args.slices):
+                    a, e = row_slice(si, args.slices, r)
+                    if e == a:
+                        continue
+                    vs = {k: v[m * a * c.T:m * e * c.T].view(m, e - a, c.T) for k, v in out.items()}
+                    vs["row_fp"] = row_fp[b][m * a:m * e].view(m, e - a)
+                    vs["row_learned"] = row_ln[b][m * a:m * e].view(m, e - a)
+                    pk.step(s0, m, rows=(rk0 + a, rk0 + e), out=vs, stream=stream)
+                    n += 1
             if record:
                 eb.record(stream)
                 state["events"].append((ea, eb))
-            if dist.world == 1:
+            if dist.world == 1 and args.slices <= 1:
                 gathered[b].record(stream)
                 fold_stream.wait_event(gathered[b])
                 pk.batch_fp_many(view["row_fp"], out=fp_all[s0:s0 + m], stream=fold_stream)
@@ -512,7 +537,7 @@ def run_ours(args, dist: Dist) -> None:
             dist.sum(real_tokens)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) ---------
-    if result is not None and dist.world == 1 and not args.no_cpu_baseline:
+    if result is not None and dist.world == 1 and not args.no_cpu_baseline and args.slices <= 1:
         fp_gpu = fp_all[:valid].cpu().numpy().view(np.uint64)
         result["cpu_baseline"] = cpu_baseline(c, args, valid, real_tokens, fp_gpu,
                                               variant_kwargs(c, args.variant))

@@ -1,5 +1,7 @@
 """The five workloads at full size, in the launch configuration the benchmark
-times (32 updates per ns_pack_step launch, all rows of the global batch).
+times (its auto_launch updates per ns_pack_step launch -- 32 for the three
+large workloads, the whole horizon for the small-batch ones -- all rows of
+the global batch).
 
 Sampled updates are compared element by element with the oracle; whole-pass
 properties (valid horizon, order digest, quota tables, exactly-once coverage
@@ -16,7 +18,11 @@ from corpus import make_preset
 
 pytestmark = pytest.mark.gpu
 
-LAUNCH = 32
+
+
+def _launch(c):
+    import bench
+    return bench.auto_launch(c.max_steps, c.B, c.T)
 
 _cache = {}
 
@@ -28,11 +34,11 @@ def _setup(name):
     return _cache[name]
 
 
-def _sampled(pk, o, steps):
+def _sampled(pk, o, steps, L):
     valid = o.valid_steps
     for k in steps:
-        s0 = (k // LAUNCH) * LAUNCH
-        n = min(LAUNCH, valid - s0)
+        s0 = (k // L) * L
+        n = min(L, valid - s0)
         got = to_host(pk.step(s0, n_steps=n))
         q = k - s0
         assert_rows_equal({f: v[q] for f, v in got.items()}, o.rows(k), f"update {k}")
@@ -59,8 +65,9 @@ def test_full_size_sampled_updates(name):
     _tables(pk, o, c)
     v = o.valid_steps
     assert v > 0
-    steps = sorted({0, 1, LAUNCH - 1, LAUNCH, v // 2, v - 2, v - 1} & set(range(v)))
-    _sampled(pk, o, steps)
+    L = _launch(c)
+    steps = sorted({0, 1, L - 1, L, v // 2, v - 2, v - 1} & set(range(v)))
+    _sampled(pk, o, steps, L)
     pk.check()
 
 
@@ -80,8 +87,9 @@ def test_full_size_mixture_within_two_windows():
 def test_full_size_sft_learned_counts_every_update():
     c, pk, o = _setup("c2")
     v = o.valid_steps
-    for s0 in range(0, v, LAUNCH):
-        n = min(LAUNCH, v - s0)
+    L = _launch(c)
+    for s0 in range(0, v, L):
+        n = min(L, v - s0)
         out = pk.step(s0, n_steps=n)
         got_l = out["row_learned"].cpu().numpy()
         got_fp = out["row_fp"].cpu().numpy().view(np.uint64)
@@ -111,8 +119,9 @@ def test_full_size_long_context_full_pass_exactly_once():
     v = o.valid_steps
     real = 0
     learned = 0
-    for s0 in range(0, v, LAUNCH):
-        n = min(LAUNCH, v - s0)
+    L = _launch(c)
+    for s0 in range(0, v, L):
+        n = min(L, v - s0)
         out = pk.step(s0, n_steps=n)
         real += int((out["doc"] >= 0).sum().item())
         learned += int(out["row_learned"].sum().item())
@@ -143,7 +152,7 @@ def test_full_size_bench_variants(variant):
         else:
             assert ocum[-1, j] <= w[j] <= o.n_windows(j)
     v = o.valid_steps
-    plan = list(bench.launch_plan(pk, v, LAUNCH))
+    plan = list(bench.launch_plan(pk, v, _launch(c)))
     want_steps = sorted({0, 1, v // 3, v // 2, v - 1} & set(range(v)))
     for s0, n, Bk in plan:
         hits = [k for k in want_steps if s0 <= k < s0 + n]
