@@ -18,7 +18,8 @@
 // with a ballot; longer windows are read from the piece table.  Tokens of a
 // tile inside one piece are copied by cp.async into a four-tile ring in
 // shared memory (aligned 16-byte blocks, realigned across lanes with
-// shuffles); a tile that crosses piece ends reads its tokens one by one.
+// shuffles); a tile that crosses piece ends is staged token by token (4-byte
+// copies into the same ring), each lane looking its positions' pieces up.
 // Warps combine the row's fingerprint through shared-memory atomics and the
 // last one to finish writes it, so no warp waits for another.
 #include <cuda_runtime.h>
@@ -63,6 +64,10 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -173,7 +178,24 @@ __device__ __forceinline__ TileMeta tile_issue(const GatherParams &p, const PV &
       cp_async16(buf + 4 * lane, g + 4 * lane);
       if (lane == 0 && m.sh != 0) cp_async16(buf + 128, g + 128);
     } else {
+      // crosses piece ends: each lane stages its own real tokens with 4-byte
+      // copies (the store looks the pieces up again and reads them back)
       m.kind = 2;
+      const uint32_t tp = t0 + 4u * lane;
+      const int32_t last = P.used - 1;
+      int32_t t = min((int32_t)tp, last);
+      Piece q = P.get(P.find_lane(t));
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        t = min((int32_t)tp + e, last);
+        const bool same = t < q.end;
+        if (!__all_sync(0xffffffffu, same)) {
+          const Piece nq = P.get(P.find_lane(t));
+          if (!same) q = nq;
+        }
+        if ((int32_t)tp + e <= last && tp < p.T)
+          cp_async4(buf + 4 * lane + e, p.tokens + q.src + (t - q.start));
+      }
     }
   }
   return m;
@@ -229,7 +251,7 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
       }
       const int32_t x = t - pc.start;
       const bool real = (int32_t)tp + e <= last && tp < p.T;
-      e0[e] = real ? __ldg(p.tokens + pc.src + x) : p.pad_id;
+      e0[e] = real ? buf[4 * lane + e] : p.pad_id;
       e1[e] = real ? x : 0;
       e2[e] = real ? pc.doc : -1;
       if (real && x >= pc.mthr) mk |= 1u << (8 * e);
