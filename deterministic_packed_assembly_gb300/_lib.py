@@ -24,6 +24,7 @@ NS_PACK_DRAIN = 1
 NS_PACK_HELDOUT = 2
 NS_PACK_SHUFFLE_ROWS = 4
 NS_PACK_WRAP = 8
+NS_PACK_HOST_CORPUS = 16
 NS_MAX_T = 1 << 24
 
 ns_alloc_fn = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)

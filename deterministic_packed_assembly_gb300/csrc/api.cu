@@ -134,14 +134,16 @@ int check_config(const ns_pack_config *cfg) {
   if (!cfg->stream_doc_begin || !cfg->stream_source || !cfg->source_weight ||
       !cfg->stream_weight || !cfg->source_heldout_bp)
     return NS_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(cfg->tokens) % 16 != 0) return NS_ERR_INVALID_ARG;
+  if (!(cfg->flags & NS_PACK_HOST_CORPUS) && reinterpret_cast<uintptr_t>(cfg->tokens) % 16 != 0)
+    return NS_ERR_INVALID_ARG;
   if (cfg->T < 16 || cfg->T % 16 != 0 || cfg->T > NS_MAX_T) return NS_ERR_INVALID_ARG;
   if (cfg->B == 0 || cfg->max_steps == 0) return NS_ERR_INVALID_ARG;
   if ((uint64_t)cfg->max_steps * cfg->B >= (1ull << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
-  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP))
+  if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP |
+                     NS_PACK_HOST_CORPUS))
     return NS_ERR_INVALID_ARG;
   if (cfg->window_segment > NS_MAX_WINDOW_SEGMENT) return NS_ERR_INVALID_ARG;
   if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
@@ -230,6 +232,32 @@ struct SideStream {
   }
 };
 
+// A corpus given in host memory: the context's own device copy, filled by a
+// second stream in groups of whole streams so that the hash of one group runs
+// while the next group is copied.
+struct CorpusCopy {
+  cudaStream_t s = nullptr;
+  std::vector<cudaEvent_t> done;          // one per group, on s
+  std::vector<uint32_t> j_first;          // group g holds streams [j_first[g], j_first[g+1])
+  cudaError_t create() { return cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking); }
+  cudaError_t add_group(const int32_t *host, int32_t *dev, uint64_t begin, uint64_t end) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (r != cudaSuccess) return r;
+    done.push_back(e);
+    if (end > begin)
+      r = cudaMemcpyAsync(dev + begin, host + begin, (end - begin) * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, s);
+    if (r == cudaSuccess) r = cudaEventRecord(e, s);
+    return r;
+  }
+  ~CorpusCopy() {
+    if (s) cudaStreamSynchronize(s);
+    for (cudaEvent_t e : done) cudaEventDestroy(e);
+    if (s) cudaStreamDestroy(s);
+  }
+};
+
 // Host arrays gathered into one buffer and copied to the device in one call.
 struct Staging {
   std::vector<unsigned char> host;
@@ -265,6 +293,56 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   int dev = 0;
   NS_CK(cudaGetDevice(&dev));
   NS_CK(cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev));
+  int rc;
+
+  // ---- a corpus in host memory: the context's device copy ----------------
+  // Offsets and loss starts first (the shuffle needs them); the tokens in
+  // groups of whole streams on a second stream, the hash of each group
+  // waiting only for its own copy.
+  const bool host_corpus = (c->flags & NS_PACK_HOST_CORPUS) != 0;
+  CorpusCopy copy;
+  if (host_corpus) {
+    int32_t *tok = a.keep<int32_t>(c->n_tokens + 4);
+    int64_t *offs = a.keep<int64_t>((size_t)c->n_docs + 1);
+    int32_t *ls = cfg->loss_start ? a.keep<int32_t>(std::max<uint32_t>(c->n_docs, 1)) : nullptr;
+    NS_ALLOC(tok);
+    NS_ALLOC(offs);
+    if (cfg->loss_start) NS_ALLOC(ls);
+    NS_CK(cudaMemcpyAsync(offs, cfg->doc_offsets, ((size_t)c->n_docs + 1) * 8,
+                          cudaMemcpyHostToDevice, st));
+    if (ls)
+      NS_CK(cudaMemcpyAsync(ls, cfg->loss_start, (size_t)c->n_docs * 4, cudaMemcpyHostToDevice,
+                            st));
+    NS_CK(copy.create());
+    // group boundaries where whole streams end, about an eighth of the tokens
+    // each; offsets that are not nondecreasing inside [0, n_tokens] at the
+    // streams' bounds make one group (the device check then reports them)
+    const int64_t *ho = cfg->doc_offsets;
+    const uint64_t nt = c->n_tokens;
+    bool ok = true;
+    std::vector<uint64_t> ob(J + 1);
+    for (uint32_t j = 0; j <= J && ok; j++) {
+      const int64_t v = ho[cfg->stream_doc_begin[j]];
+      ok = v >= 0 && (uint64_t)v <= nt && (j == 0 || (uint64_t)v >= ob[j - 1]);
+      ob[j] = ok ? (uint64_t)v : 0;
+    }
+    uint64_t begin = 0;
+    copy.j_first.push_back(0);
+    if (ok) {
+      const uint64_t target = std::max<uint64_t>(nt / 8, 1);
+      for (uint32_t j = 1; j < J; j++)
+        if (ob[j] - begin >= target) {
+          NS_CK(copy.add_group(cfg->tokens, tok, begin, ob[j]));
+          copy.j_first.push_back(j);
+          begin = ob[j];
+        }
+    }
+    NS_CK(copy.add_group(cfg->tokens, tok, begin, nt));
+    copy.j_first.push_back(J);
+    c->tokens = tok;
+    c->offs = offs;
+    c->loss_start = ls;
+  }
 
   // ---- recipe tables on the device (temporaries) --------------------------
   std::vector<uint32_t> sdb(cfg->stream_doc_begin, cfg->stream_doc_begin + J + 1);
@@ -287,7 +365,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     max_strata = std::max(max_strata, src_first[s + 1] - src_first[s]);
   }
   void *d_sdb, *d_ssrc, *d_sw, *d_tw, *d_sbp, *d_stream_bp, *d_src_first;
-  int rc;
   Staging up;
   up.add(sdb.data(), sdb.size() * 4, &d_sdb);
   up.add(ssrc.data(), ssrc.size() * 4, &d_ssrc);
@@ -420,11 +497,21 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(kept);
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
-    NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
-                                  static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
-                                  c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                  heldout_mode ? 1u : 0u, frontier, kept, c->n_sms, st));
+    // one launch over every stream, or one per copied group of streams
+    const size_t n_groups = host_corpus ? copy.done.size() : 1;
+    for (size_t gi = 0; gi < n_groups; gi++) {
+      const uint32_t j0 = host_corpus ? copy.j_first[gi] : 0;
+      const uint32_t j1 = host_corpus ? copy.j_first[gi + 1] : J;
+      if (host_corpus) NS_CK(cudaStreamWaitEvent(st, copy.done[gi], 0));
+      NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+                                    static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
+                                    c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
+                                    heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0,
+                                    c->n_sms, st));
+    }
   }
+  // every token is on the device before anything after the hash reads it
+  if (host_corpus) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)

@@ -392,13 +392,14 @@ __global__ void __launch_bounds__(kThreads, 4)
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
-                       unsigned long long *kept) {
+                       unsigned long long *kept, uint32_t j_begin, uint32_t j_count) {
   constexpr uint32_t kGrab = 8;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   bool ready_seen = false;
-  for (uint32_t jj = 0; jj < J; jj++) {
-    const uint32_t j = (warp_id + jj) % J;
+  // streams [j_begin, j_begin + j_count) of the J
+  for (uint32_t jj = 0; jj < j_count; jj++) {
+    const uint32_t j = j_begin + (warp_id + jj) % j_count;
     const uint32_t bp = stream_bp[j];
     if (bp == 0) continue;
     const uint64_t N = sdb[j + 1] - sdb[j];
@@ -1165,12 +1166,14 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
                                const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                                uint64_t hash_key, uint32_t want_heldout,
-                               unsigned long long *frontier, unsigned long long *kept, int n_sms,
-                               cudaStream_t st) {
+                               unsigned long long *frontier, unsigned long long *kept,
+                               uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st) {
+  if (j_count == 0) return cudaSuccess;
   ++launch_counter();
   hash_prefix_kernel<<<n_sms * 4, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
                                                      klen, cum_last, ready, ready_at, T, G,
-                                                     hash_key, want_heldout, frontier, kept);
+                                                     hash_key, want_heldout, frontier, kept,
+                                                     j_begin, j_count);
   return cudaGetLastError();
 }
 

@@ -63,8 +63,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
                                const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
                                const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                                uint64_t hash_key, uint32_t want_heldout,
-                               unsigned long long *frontier, unsigned long long *kept, int n_sms,
-                               cudaStream_t st);
+                               unsigned long long *frontier, unsigned long long *kept,
+                               uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st);
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,

@@ -23,7 +23,9 @@ class Packer:
     """A packing context over a corpus resident on one CUDA device.
 
     ``tokens`` (int32), ``doc_offsets`` (int64, n_docs + 1) and ``loss_start``
-    (int32 or None) are device tensors that must outlive the packer.  The
+    (int32 or None) are device tensors that must outlive the packer -- or CPU
+    tensors (page-locked for the copies to overlap the hash), which the
+    library copies to ``device`` itself while it builds the context.  The
     recipe arrays may be numpy arrays or lists.  ``heldout_only`` packs the
     validation stream (the held-out documents) instead of the training one;
     ``window_segment`` > 0 reads each stream's windows in a shuffled order
@@ -42,16 +44,22 @@ class Packer:
                  pad_id: int = 0, heldout_only: bool = False, window_segment: int = 0,
                  shuffle_rows: bool = False, schedule: Optional[list] = None,
                  wrap: bool = False, len_bucket: int = 0,
-                 stream: Optional[torch.cuda.Stream] = None):
-        if not tokens.is_cuda:
-            raise ValueError("tokens must be a CUDA tensor")
+                 stream: Optional[torch.cuda.Stream] = None, device=None):
         assert tokens.dtype == torch.int32 and tokens.is_contiguous()
         assert doc_offsets.dtype == torch.int64 and doc_offsets.is_contiguous()
         assert doc_offsets.device == tokens.device
         if loss_start is not None:
             assert loss_start.dtype == torch.int32 and loss_start.is_contiguous()
             assert loss_start.device == tokens.device
-        self.device = tokens.device
+        self.host_corpus = not tokens.is_cuda
+        if self.host_corpus:
+            if tokens.device.type != "cpu":
+                raise ValueError("tokens must be a CUDA or a CPU tensor")
+            self.device = torch.device(device if device is not None else "cuda")
+            if self.device.index is None:
+                self.device = torch.device("cuda", torch.cuda.current_device())
+        else:
+            self.device = tokens.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.T, self.B, self.max_steps = int(T), int(B), int(max_steps)
         self._corpus = (tokens, doc_offsets, loss_start)
@@ -95,7 +103,8 @@ class Packer:
         cfg.max_steps = self.max_steps
         cfg.flags = ((L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
                      | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0)
-                     | (L.NS_PACK_WRAP if wrap else 0))
+                     | (L.NS_PACK_WRAP if wrap else 0)
+                     | (L.NS_PACK_HOST_CORPUS if self.host_corpus else 0))
         cfg.len_bucket = int(len_bucket)
         cfg.window_segment = int(window_segment)
         self.schedule = schedule

@@ -83,6 +83,13 @@ extern "C" {
  * 0; a stream's last window may be partial (padded), and it counts only once
  * the whole stream is inside the reachable prefix. */
 #define NS_PACK_WRAP 8u
+/* The corpus (tokens, doc_offsets, loss_start) is in host memory: the
+ * context copies it to the device (its own copy, kept with the tables and
+ * counted in table_bytes), offsets first and the tokens in groups of whole
+ * streams on a second stream, hashing each group as soon as its copy lands.
+ * Page-locked host memory lets the copies run beside the kernels; the host
+ * buffers may be released once ns_pack_init returns. */
+#define NS_PACK_HOST_CORPUS 16u
 
 /* ---- limits ------------------------------------------------------------- */
 #define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
@@ -100,9 +107,10 @@ typedef void *(*ns_alloc_fn)(size_t bytes, void *user);
 typedef void (*ns_free_fn)(void *ptr, void *user);
 
 typedef struct {
-  /* Corpus, on the device, borrowed (must outlive the context).  Documents
-   * are contiguous runs of tokens: document d is tokens[doc_offsets[d] ..
-   * doc_offsets[d+1]).  tokens must be 16-byte aligned. */
+  /* Corpus, on the device, borrowed (must outlive the context); with
+   * NS_PACK_HOST_CORPUS in host memory instead, copied.  Documents are
+   * contiguous runs of tokens: document d is tokens[doc_offsets[d] ..
+   * doc_offsets[d+1]).  Device tokens must be 16-byte aligned. */
   const int32_t *tokens;
   uint64_t n_tokens;
   const int64_t *doc_offsets; /* [n_docs + 1], nondecreasing, lengths < 2^31 */
@@ -126,7 +134,7 @@ typedef struct {
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
   uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS |
-                        NS_PACK_WRAP */
+                        NS_PACK_WRAP | NS_PACK_HOST_CORPUS */
   int32_t pad_id;    /* token written at padded positions */
   uint32_t window_segment; /* G > 0: each stream's windows are read in a shuffled
                               order within segments of G consecutive windows

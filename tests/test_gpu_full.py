@@ -164,3 +164,23 @@ def test_full_size_bench_variants(variant):
     pk.close()
     del pk
     torch.cuda.empty_cache()
+
+
+def test_full_size_host_corpus():
+    # the 2M-document mixture handed over in page-locked host memory: copied
+    # in groups of streams, each group hashed as it lands
+    import torch
+    from deterministic_packed_assembly_gb300 import Packer
+    c, pk, o = _setup("c3")
+    t = torch.from_numpy(c.tokens).pin_memory()
+    off = torch.from_numpy(c.doc_offsets).pin_memory()
+    import bench
+    hp = Packer(t, off, None, device="cuda:0", **bench.recipe_kwargs(c))
+    assert hp.order_digest == pk.order_digest == o.digest
+    assert hp.valid_steps == pk.valid_steps
+    L = _launch(c)
+    v = o.valid_steps
+    _sampled(hp, o, sorted({0, L, v - 1}), L)
+    hp.close()
+    del hp, t, off
+    torch.cuda.empty_cache()

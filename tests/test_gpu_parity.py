@@ -397,3 +397,38 @@ def test_bucketed_lengths_of_greedy_rows():
         pk, o = packer_for(c, len_bucket=bucket), oracle_for(c, len_bucket=bucket)
         _check_tables(pk, o, c)
         compare_steps(pk, o, [0, o.valid_steps - 1], launch=1)
+
+
+def _host_packer(c, pinned=True, **kw):
+    import torch
+    from deterministic_packed_assembly_gb300 import Packer
+    t = torch.from_numpy(np.ascontiguousarray(c.tokens))
+    o = torch.from_numpy(np.ascontiguousarray(c.doc_offsets))
+    ls = None if c.loss_start is None else torch.from_numpy(np.ascontiguousarray(c.loss_start))
+    if pinned:
+        t, o = t.pin_memory(), o.pin_memory()
+        ls = None if ls is None else ls.pin_memory()
+    args = dict(stream_doc_begin=c.stream_doc_begin, stream_source=c.stream_source,
+                source_weight=c.source_weight, stream_weight=c.stream_weight,
+                source_heldout_bp=c.source_heldout_bp, T=c.T, B=c.B, max_steps=c.max_steps,
+                seed=c.seed, hash_key=c.hash_key, drain=c.drain, pad_id=c.pad_id)
+    args.update(kw)
+    return Packer(t, o, ls, device="cuda:0", **args)
+
+
+@pytest.mark.parametrize("name,pinned,kw", [("c1", True, {}), ("c2s", False, {}),
+                                            ("c3s", True, {}), ("c3s", True, {"wrap": True}),
+                                            ("c5s", True, {"heldout_only": True, "drain": True})])
+def test_host_corpus(name, pinned, kw):
+    # the corpus handed over in host memory: the library's own device copy,
+    # hashed group by group as it lands, gives the same context and rows
+    c = make_preset(name)
+    pk = _host_packer(c, pinned, **kw)
+    assert pk.host_corpus
+    o = oracle_for(c, **kw)
+    _check_tables(pk, o, c)
+    ref = packer_for(c, **kw)
+    assert pk.order_digest == ref.order_digest
+    assert pk.info["table_bytes"] > ref.info["table_bytes"]  # it holds the corpus too
+    compare_steps(pk, o, range(o.valid_steps), launch=4)
+    pk.check()
