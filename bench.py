@@ -340,15 +340,12 @@ def run_ours(args, dist: Dist) -> None:
                pos=torch.empty(n_pos, dtype=torch.int32, device=device),
                doc=torch.empty(n_pos, dtype=torch.int32, device=device),
                mask=torch.empty(n_pos, dtype=torch.uint8, device=device))
-    # row fingerprints and learned counts alternate between two buffers so
-    # that one launch's batch fold (on a second stream) overlaps the next
-    # launch's gather
-    row_fp = [torch.empty(L * n_buf, dtype=torch.int64, device=device) for _ in range(2)]
-    row_ln = [torch.empty(L * n_buf, dtype=torch.int32, device=device) for _ in range(2)]
+    # every update's row fingerprints and learned counts stay for the pass
+    # (8 + 4 bytes a row); the batch fingerprints of all updates are folded at
+    # the end, one launch per run of updates with the same rows
+    row_fp_all = torch.empty(c.max_steps * n_buf, dtype=torch.int64, device=device)
+    row_ln_all = torch.empty(c.max_steps * n_buf, dtype=torch.int32, device=device)
     fp_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
-    fold_stream = torch.cuda.Stream(device)
-    gathered = [torch.cuda.Event() for _ in range(2)]
-    folded = [torch.cuda.Event() for _ in range(2)]
 
     state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0,
              "init_events": []}
@@ -370,18 +367,21 @@ def run_ours(args, dist: Dist) -> None:
         real = torch.zeros((), dtype=torch.int64, device=device) if count else None
         n = 0
         rows_total = 0
+        folds = []  # [first update, updates, rows, offset of their first row]
         for li, (s0, m, Bk) in enumerate(launch_plan(pk, valid, L)):
             rk0, rk1 = row_slice(dist.rank, dist.world, Bk)
             r = rk1 - rk0
             if r == 0:
                 continue
+            ro = rows_total
             rows_total += m * r
-            b = li % 2
-            if li >= 2 and dist.world == 1 and args.slices <= 1:
-                stream.wait_event(folded[b])  # the fold of two launches ago is done with b
+            if folds and folds[-1][2] == r and folds[-1][0] + folds[-1][1] == s0:
+                folds[-1][1] += m
+            else:
+                folds.append([s0, m, r, ro])
             view = {k: v[:m * r * c.T].view(m, r, c.T) for k, v in out.items()}
-            view["row_fp"] = row_fp[b][:m * r].view(m, r)
-            view["row_learned"] = row_ln[b][:m * r].view(m, r)
+            view["row_fp"] = row_fp_all[ro:ro + m * r].view(m, r)
+            view["row_learned"] = row_ln_all[ro:ro + m * r].view(m, r)
             if record:
                 ea = torch.cuda.Event(enable_timing=True)
                 eb = torch.cuda.Event(enable_timing=True)
@@ -396,27 +396,27 @@ def run_ours(args, dist: Dist) -> None:
                     if e == a:
                         continue
                     vs = {k: v[m * a * c.T:m * e * c.T].view(m, e - a, c.T) for k, v in out.items()}
-                    vs["row_fp"] = row_fp[b][m * a:m * e].view(m, e - a)
-                    vs["row_learned"] = row_ln[b][m * a:m * e].view(m, e - a)
+                    vs["row_fp"] = row_fp_all[ro + m * a:ro + m * e].view(m, e - a)
+                    vs["row_learned"] = row_ln_all[ro + m * a:ro + m * e].view(m, e - a)
                     pk.step(s0, m, rows=(rk0 + a, rk0 + e), out=vs, stream=stream)
                     n += 1
             if record:
                 eb.record(stream)
                 state["events"].append((ea, eb))
-            if dist.world == 1 and args.slices <= 1:
-                gathered[b].record(stream)
-                fold_stream.wait_event(gathered[b])
-                pk.batch_fp_many(view["row_fp"], out=fp_all[s0:s0 + m], stream=fold_stream)
-                folded[b].record(fold_stream)
-                n += 1
-            if e2e is not None:
-                e2e[3][s0:s0 + m, :r].copy_(view["row_fp"], non_blocking=True)
-                e2e[4][s0:s0 + m, :r].copy_(view["row_learned"], non_blocking=True)
             if count:
                 real += (view["doc"] >= 0).sum()
-        stream.wait_stream(fold_stream)
-        if e2e is not None and dist.world == 1:
-            e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
+        # batch fingerprints of every update (one GPU holds whole batches; with
+        # row slices the rows are not in batch order)
+        if dist.world == 1 and args.slices <= 1:
+            for f0, fm, fr, fo in folds:
+                pk.batch_fp_many(row_fp_all[fo:fo + fm * fr].view(fm, fr),
+                                 out=fp_all[f0:f0 + fm], stream=stream)
+                n += 1
+        if e2e is not None:
+            e2e[3][:rows_total].copy_(row_fp_all[:rows_total], non_blocking=True)
+            e2e[4][:rows_total].copy_(row_ln_all[:rows_total], non_blocking=True)
+            if dist.world == 1:
+                e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
         pk.close()
         state["launches"] = n
         state["rows_total"] = rows_total
@@ -503,8 +503,8 @@ def run_ours(args, dist: Dist) -> None:
         tok_h = torch.from_numpy(c.tokens).pin_memory()
         off_h = torch.from_numpy(c.doc_offsets).pin_memory()
         ls_h = None if c.loss_start is None else torch.from_numpy(c.loss_start).pin_memory()
-        fp_h = torch.empty((c.max_steps, n_buf), dtype=torch.int64).pin_memory()
-        ln_h = torch.empty((c.max_steps, n_buf), dtype=torch.int32).pin_memory()
+        fp_h = torch.empty(c.max_steps * n_buf, dtype=torch.int64).pin_memory()
+        ln_h = torch.empty(c.max_steps * n_buf, dtype=torch.int32).pin_memory()
         bf_h = torch.empty(c.max_steps, dtype=torch.int64).pin_memory()
 
         def e2e_pass():
