@@ -432,3 +432,98 @@ def test_host_corpus(name, pinned, kw):
     assert pk.info["table_bytes"] > ref.info["table_bytes"]  # it holds the corpus too
     compare_steps(pk, o, range(o.valid_steps), launch=4)
     pk.check()
+
+
+def _raw_config(c, tok, off, alloc, free, **flags):
+    """A config for the C ABI built by hand (device corpus), for the tests that
+    drive the entry points below the Python wrapper."""
+    import deterministic_packed_assembly_gb300._lib as L
+    keep = [np.ascontiguousarray(c.stream_doc_begin, np.uint32),
+            np.ascontiguousarray(c.stream_source, np.uint32),
+            np.ascontiguousarray(c.source_weight, np.uint32),
+            np.ascontiguousarray(c.stream_weight, np.uint32),
+            np.ascontiguousarray(c.source_heldout_bp, np.uint16)]
+    cfg = L.ns_pack_config()
+    cfg.tokens, cfg.n_tokens = tok.data_ptr(), tok.numel()
+    cfg.doc_offsets, cfg.n_docs = off.data_ptr(), off.numel() - 1
+    cfg.loss_start = None
+    cfg.n_sources, cfg.n_streams, cfg.T = keep[2].size, keep[1].size, c.T
+    cfg.stream_doc_begin, cfg.stream_source = keep[0].ctypes.data, keep[1].ctypes.data
+    cfg.source_weight, cfg.stream_weight = keep[2].ctypes.data, keep[3].ctypes.data
+    cfg.source_heldout_bp = keep[4].ctypes.data
+    cfg.seed, cfg.hash_key, cfg.B, cfg.max_steps = c.seed, c.hash_key, c.B, c.max_steps
+    cfg.flags = flags.get("flags", 0)
+    cfg.alloc, cfg.free = alloc, free
+    return cfg, keep
+
+
+@pytest.mark.parametrize("wrap", [False, True])
+def test_allocation_failures_release_everything(wrap):
+    # the allocator fails at its n-th call, for every n the init makes: each
+    # init returns NS_ERR_OOM and gives back every block it was handed
+    import torch
+    import deterministic_packed_assembly_gb300._lib as L
+    c = make_preset("c3s")
+    dev = torch.device("cuda:0")
+    tok = torch.from_numpy(c.tokens).to(dev)
+    off = torch.from_numpy(c.doc_offsets).to(dev)
+    live, state = {}, {"calls": 0, "fail_at": None}
+
+    def _alloc(nbytes, _user):
+        state["calls"] += 1
+        if state["fail_at"] is not None and state["calls"] == state["fail_at"]:
+            return None
+        p = torch.cuda.caching_allocator_alloc(int(nbytes), 0)
+        live[p] = nbytes
+        return p
+
+    def _free(p, _user):
+        assert p in live, "freed a block the allocator never handed out"
+        del live[p]
+        torch.cuda.caching_allocator_delete(p)
+
+    a_cb, f_cb = L.ns_alloc_fn(_alloc), L.ns_free_fn(_free)
+    flags = L.NS_PACK_WRAP if wrap else 0
+    cfg, keep = _raw_config(c, tok, off, a_cb, f_cb, flags=flags)
+    ctx = L.ns_pack_init(cfg)           # a clean run counts the calls
+    total = state["calls"]
+    assert total >= 2 and live
+    L.ns_pack_free(ctx)
+    assert not live
+    for n in range(1, total + 1):
+        state.update(calls=0, fail_at=n)
+        with pytest.raises(L.NsPackError) as e:
+            L.ns_pack_init(cfg)
+        assert e.value.code == L.NS_ERR_OOM, n
+        assert not live, (n, len(live))
+    torch.cuda.synchronize()
+
+
+def test_outputs_stay_inside_their_buffers():
+    # every array is written exactly where the call says: canaries on both
+    # sides of each output are untouched, and what lies between is the oracle's
+    import torch
+    c = make_preset("c3s")
+    pk, o = packer_for(c, wrap=False), oracle_for(c)
+    dev = pk.device
+    k, n, r0, r1 = 1, 2, 3, c.B - 2
+    rows = r1 - r0
+    pad = 64  # elements on each side (keeps 16-byte alignment for every dtype)
+    spec = dict(tokens=(torch.int32, c.T), pos=(torch.int32, c.T), doc=(torch.int32, c.T),
+                mask=(torch.uint8, c.T), row_fp=(torch.int64, 1), row_learned=(torch.int32, 1),
+                row_len=(torch.int32, 1))
+    bufs, out = {}, {}
+    for key, (dt, w) in spec.items():
+        m = n * rows * w
+        b = torch.full((m + 2 * pad,), 0x5A, dtype=dt, device=dev)
+        bufs[key] = (b, m)
+        shape = (n, rows, c.T) if w > 1 else (n, rows)
+        out[key] = b[pad:pad + m].view(*shape)
+    pk.step(k, n_steps=n, rows=(r0, r1), out=out)
+    torch.cuda.synchronize()
+    for key, (b, m) in bufs.items():
+        h = b.cpu()
+        assert (h[:pad] == 0x5A).all() and (h[pad + m:] == 0x5A).all(), key
+    got = to_host(out)
+    for q in range(n):
+        assert_rows_equal({f: v[q] for f, v in got.items()}, o.rows(k + q, r0, r1), f"step {k + q}")
