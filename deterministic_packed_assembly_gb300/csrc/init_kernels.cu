@@ -378,10 +378,10 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // Held-out flags for the prefix of every stream the horizon reaches.  A
 // stream's documents are taken in shuffled-position order, a few at a time
 // from the stream's frontier; a document the stream does not keep (held out
-// for training, not held out for validation) has its kept length set to 0.  A warp leaves a stream once the kept tokens of the documents
-// already hashed exceed need_j = rmax_j * T (the windows the horizon asks of
-// it hold at most that many), or when the stream runs out, and goes on to the
-// next stream.  Every position below the final frontier is hashed, and the
+// for training, not held out for validation) has its kept length set to 0.
+// A warp leaves a stream once the kept tokens of the documents already hashed
+// exceed need_j = rmax_j * T (the windows the horizon asks of it hold at most
+// that many), or when the stream runs out, and goes on to the next stream.  Every position below the final frontier is hashed, and the
 // kept tokens below it exceed need_j unless the whole stream was hashed, so
 // the prefix the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
