@@ -804,7 +804,8 @@ static int read_error_word(ns_pack_ctx *ctx, cudaStream_t st) {
     cudaGetLastError();
     return NS_ERR_CUDA;
   }
-  return e == 0 ? NS_OK : NS_ERR_DEVICE;
+  if (e == 0) return NS_OK;
+  return e == nsk::kDevBadOffsets ? NS_ERR_BAD_INPUT : NS_ERR_DEVICE;
 }
 
 int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,

@@ -217,7 +217,9 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
 /* Fold n_rows row fingerprints (device, in row order) into the batch
  * fingerprint F = fold(F ^ fp_i) and copy it to *batch_fp_host; synchronises
  * cuda_stream (NULL: the context's).  Also reports the device error word.
- * Errors: INVALID_ARG, CUDA, DEVICE. */
+ * Uses one word of the context's memory: calls on one context must not
+ * overlap (ns_pack_batch_fp writes to caller memory and has no such limit).
+ * Errors: INVALID_ARG, CUDA, DEVICE, BAD_INPUT. */
 int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,
                         uint64_t *batch_fp_host, void *cuda_stream);
 
