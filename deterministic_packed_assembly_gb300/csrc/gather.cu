@@ -11,9 +11,9 @@
 // the rows gives the same bytes ("Zephon: deterministic data loading",
 // checkpoint on 16 GPUs, resume on 8/32/64).
 //
-// Layout of the work: 8 warps per CTA, each on its own; a warp owns tiles of
-// 128 consecutive positions (4 per lane, so every store is a 16-byte vector
-// and a warp writes 512 contiguous bytes per array).  A window of up to 32
+// Layout of the work: 4 warps per CTA (10 CTAs per SM), each on its own; a
+// warp owns tiles of 128 consecutive positions (4 per lane, so every store is
+// a 16-byte vector and a warp writes 512 contiguous bytes per array).  A window of up to 32
 // pieces is held in the warp's registers, piece l in lane l, and looked up
 // with a ballot; longer windows are read from the piece table.  Tokens of a
 // tile inside one piece are copied by cp.async into a four-tile ring in
@@ -34,7 +34,7 @@ namespace nsk {
 
 namespace {
 
-constexpr int kGatherWarps = 8;
+constexpr int kGatherWarps = 4;
 constexpr int kTile = 128;         // positions per warp per tile: 32 lanes x 4
 constexpr int kStages = 4;         // tiles in flight per warp
 constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
@@ -310,7 +310,7 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
   }
 }
 
-__global__ void __launch_bounds__(kGatherWarps * 32, 5)
+__global__ void __launch_bounds__(kGatherWarps * 32, 10)
     gather_kernel(const GatherParams p) {
   __shared__ __align__(16) int32_t s_tok[kGatherWarps][kStages][kStageWords];
   __shared__ TileMeta s_meta[kGatherWarps][kStages];
