@@ -11,7 +11,8 @@
 // the rows gives the same bytes ("Zephon: deterministic data loading",
 // checkpoint on 16 GPUs, resume on 8/32/64).
 //
-// Layout of the work: 4 warps per CTA (10 CTAs per SM), each on its own; a
+// Layout of the work: 4 warps per CTA (10 CTAs per SM; 8 and 5 for rows
+// longer than 8192 positions), each on its own; a
 // warp owns tiles of 128 consecutive positions (4 per lane, so every store is
 // a 16-byte vector and a warp writes 512 contiguous bytes per array).  A window of up to 32
 // pieces is held in the warp's registers, piece l in lane l, and looked up
@@ -34,7 +35,6 @@ namespace nsk {
 
 namespace {
 
-constexpr int kGatherWarps = 4;
 constexpr int kTile = 128;         // positions per warp per tile: 32 lanes x 4
 constexpr int kStages = 4;         // tiles in flight per warp
 constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
@@ -278,11 +278,11 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
 // This warp's tiles: t0 = warp * 128 + m * 1024, through a ring of kStages
 // shared-memory buffers filled by cp.async; each tile's description waits in
 // shared memory beside its buffer (written by lane 0, read after __syncwarp).
-template <class PV>
+template <int W, class PV>
 __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, int warp, int lane,
                                            size_t obase, int32_t (*ring)[kStageWords],
                                            TileMeta *meta, uint64_t &acc, int &learned) {
-  constexpr uint32_t kStride = kGatherWarps * kTile;
+  constexpr uint32_t kStride = W * kTile;
   const uint32_t first = (uint32_t)warp * kTile;
   const int n_tiles = first < p.T ? (int)((p.T - first + kStride - 1) / kStride) : 0;
 #pragma unroll
@@ -310,10 +310,13 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
   }
 }
 
-__global__ void __launch_bounds__(kGatherWarps * 32, 10)
+// W warps per row: 4 (ten rows per SM) for rows up to 8192 positions, 8 (five
+// rows per SM) for longer rows, whose launches hold fewer rows.
+template <int W>
+__global__ void __launch_bounds__(W * 32, 40 / W)
     gather_kernel(const GatherParams p) {
-  __shared__ __align__(16) int32_t s_tok[kGatherWarps][kStages][kStageWords];
-  __shared__ TileMeta s_meta[kGatherWarps][kStages];
+  __shared__ __align__(16) int32_t s_tok[W][kStages][kStageWords];
+  __shared__ TileMeta s_meta[W][kStages];
   __shared__ unsigned long long s_acc;
   __shared__ int s_learned;
   __shared__ int s_done;
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32, 10)
       P.mthr = __ldg(p.node_mthr + ws + lane);
       if (lane == 0) P.mthr = clip_threshold(P.mthr, clip);
     }
-    warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
+    warp_tiles<W>(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
   } else {
     TablePieces P;
     P.S = p.node_S + ws;
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32, 10)
     P.np = np;
     P.used = used;
     P.clip = clip;
-    warp_tiles(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
+    warp_tiles<W>(p, P, warp, lane, obase, s_tok[warp], s_meta[warp], acc, learned);
   }
 
   // combine the warps' sums; the last warp to arrive writes the row's values
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32, 10)
     atomicAdd(&s_acc, (unsigned long long)acc);
     atomicAdd(&s_learned, learned);
     __threadfence_block();
-    if (atomicAdd(&s_done, 1) == kGatherWarps - 1) {
+    if (atomicAdd(&s_done, 1) == W - 1) {
       __threadfence_block();
       // tiles from the first one at or after `used` are all padding
       const uint64_t a = *reinterpret_cast<volatile unsigned long long *>(&s_acc) +
@@ -502,7 +505,10 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
   const uint64_t n = (uint64_t)p.n_steps * p.n_rows;
   if (n == 0) return cudaSuccess;
   ++launch_counter();
-  gather_kernel<<<(unsigned)n, kGatherWarps * 32, 0, st>>>(p);
+  if (p.T <= 8192)
+    gather_kernel<4><<<(unsigned)n, 4 * 32, 0, st>>>(p);
+  else
+    gather_kernel<8><<<(unsigned)n, 8 * 32, 0, st>>>(p);
   return cudaGetLastError();
 }
 
