@@ -11,8 +11,8 @@
 // the rows gives the same bytes ("Zephon: deterministic data loading",
 // checkpoint on 16 GPUs, resume on 8/32/64).
 //
-// Layout of the work: 4 warps per CTA (10 CTAs per SM; 8 and 5 for rows
-// longer than 8192 positions), each on its own; a
+// Layout of the work: 4 warps per CTA (10 CTAs per SM; more warps and fewer
+// CTAs for rows longer than 8192 positions), each on its own; a
 // warp owns tiles of 128 consecutive positions (4 per lane, so every store is
 // a 16-byte vector and a warp writes 512 contiguous bytes per array).  A window of up to 32
 // pieces is held in the warp's registers, piece l in lane l, and looked up
@@ -311,7 +311,8 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
 }
 
 // W warps per row: 4 (ten rows per SM) for rows up to 8192 positions, 8 (five
-// rows per SM) for longer rows, whose launches hold fewer rows.
+// rows) up to 16384, 16 (two rows) beyond: long rows come fewer to a launch,
+// so each is given more warps.
 template <int W>
 __global__ void __launch_bounds__(W * 32, 40 / W)
     gather_kernel(const GatherParams p) {
@@ -507,8 +508,10 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
   ++launch_counter();
   if (p.T <= 8192)
     gather_kernel<4><<<(unsigned)n, 4 * 32, 0, st>>>(p);
-  else
+  else if (p.T <= 16384)
     gather_kernel<8><<<(unsigned)n, 8 * 32, 0, st>>>(p);
+  else
+    gather_kernel<16><<<(unsigned)n, 16 * 32, 0, st>>>(p);
   return cudaGetLastError();
 }
 
