@@ -76,7 +76,7 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="c3", choices=sorted(WORKLOADS))
     ap.add_argument("--launch", type=int, default=0,
-                    help="updates per ns_pack_step launch (0: enough for about 2^26 positions "
+                    help="updates per ns_pack_step launch (0: enough for about 2^28 positions "
                          "per launch, see auto_launch)")
     ap.add_argument("--slices", type=int, default=1,
                     help="split every launch into this many row-slice launches (the same "
@@ -227,14 +227,15 @@ def gather_source_hash() -> str:
 
 
 def profiled_traffic(workload: str) -> tuple[float | None, str | None]:
-    """DRAM bytes per gather launch from the committed ncu summary, if it was
-    taken on the current gather.cu (else None)."""
+    """DRAM bytes per gather row position from the committed ncu summary, if
+    it was taken on the current gather.cu (else None); the caller scales it
+    to its launch."""
     path = os.path.join(PROFILES, f"gather_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None, None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)", text)
+    m = re.search(r"traffic_bytes_per_position:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)", text)
     if not m or m.group(2) != gather_source_hash():
         return None, None
     return float(m.group(1)), os.path.relpath(path, ROOT)
@@ -282,10 +283,11 @@ def variant_kwargs(c, name: str) -> dict:
 
 
 def auto_launch(max_steps: int, rows: int, T: int) -> int:
-    """Updates per launch: about 2^26 positions (tens of thousands of CTAs'
-    worth of rows), at most the horizon.  32 for the 512 x 4096 and 256 x 8192
-    workloads and for 64 x 32768; the whole horizon for 8 x 4096."""
-    return max(1, min(max_steps, -(-(1 << 26) // max(1, rows * T))))
+    """Updates per launch: about 2^28 positions (a 3.5 GB output buffer; a
+    launch's tail of partly idle SMs then costs little), at most the
+    horizon.  128 for the 512 x 4096, 256 x 8192 and 64 x 32768 workloads;
+    the whole horizon for 8 x 4096."""
+    return max(1, min(max_steps, -(-(1 << 28) // max(1, rows * T))))
 
 
 def launch_plan(pk, valid: int, L: int):
@@ -469,7 +471,10 @@ def run_ours(args, dist: Dist) -> None:
     avg_launch_s = (sum(gather_ms) / len(gather_ms)) / 1e3
     peak, peak_kind = hbm_peak()
     achieved = bytes_per_launch / avg_launch_s / 1e9
-    traffic, traffic_src = profiled_traffic(args.config)
+    traffic_pp, traffic_src = profiled_traffic(args.config)
+    # per launch, like `achieved`: the captured launch's bytes per position
+    # times this launch's positions (traffic grows with positions)
+    traffic = None if traffic_pp is None else traffic_pp * positions / n_launch
     gather_share = sum(gather_ms) / ms
 
     result = None
