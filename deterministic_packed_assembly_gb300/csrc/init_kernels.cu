@@ -359,14 +359,22 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
       w[u] = make_int4(0, 0, 0, 0);
       if (ru < end) w[u] = __ldcs(base + (ru >> 2));
     }
+    // a step whose blocks all lie inside the document (every lane's, which
+    // the warp decides at once from lane 0's offset) needs no checks
+    const uint32_t r0 = r - 4 * lane;
+    if (r0 >= sh && r0 + 512 <= end) {
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const uint32_t ru = r + 128 * u;
-      if (ru < end) {
-        if (ru >= sh && ru + 4 <= end)
-          acc += hash_terms_inside(v[u], ru - sh);
-        else
-          acc += block_terms_edge(v[u], (int32_t)ru - (int32_t)sh, L);
+      for (int u = 0; u < 4; u++) acc += hash_terms_inside(v[u], r + 128 * u - sh);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const uint32_t ru = r + 128 * u;
+        if (ru < end) {
+          if (ru >= sh && ru + 4 <= end)
+            acc += hash_terms_inside(v[u], ru - sh);
+          else
+            acc += block_terms_edge(v[u], (int32_t)ru - (int32_t)sh, L);
+        }
       }
     }
 #pragma unroll
