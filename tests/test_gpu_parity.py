@@ -527,3 +527,22 @@ def test_outputs_stay_inside_their_buffers():
     got = to_host(out)
     for q in range(n):
         assert_rows_equal({f: v[q] for f, v in got.items()}, o.rows(k + q, r0, r1), f"step {k + q}")
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_every_option_together_random_tiny_corpora(case):
+    # drain, validation stream, segments, row shuffle, wrap, buckets and a
+    # schedule drawn together on random small corpora
+    rng = np.random.default_rng(4000 + case)
+    c = _random_case(rng)
+    kw = dict(heldout_only=bool(rng.random() < 0.25), window_segment=int(rng.choice([0, 1, 3, 8])),
+              shuffle_rows=bool(rng.integers(0, 2)), wrap=bool(rng.integers(0, 2)),
+              len_bucket=int(rng.choice([0, 16, 48])))
+    if c.max_steps >= 3 and rng.random() < 0.6:
+        kw["schedule"] = _schedule_for(c, rng, int(rng.integers(2, min(4, c.max_steps) + 1)),
+                                       c.max_steps)
+    o = oracle_for(c, **kw)
+    pk = packer_for(c, **kw)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=int(rng.integers(1, 4)))
+    pk.check()
