@@ -318,16 +318,19 @@ __device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
          splitmix64(((uint64_t)(i0 + 3) << 32) | (uint32_t)v.w);
 }
 
-// Terms of a block whose first token has in-document index i0 (may be
-// negative), only indexes in [0, L).
-__device__ __forceinline__ uint64_t block_terms_edge(int4 v, int32_t i0, uint32_t L) {
+// Terms of a block whose first token has in-document index i0, taken modulo
+// 2^32 (the head block of a document that does not start on a 16-byte
+// boundary has i0 "below" zero); a token whose index is not in [0, L) adds
+// nothing.  Every lane computes all four mixes and masks them, so a warp
+// whose blocks straddle a document edge runs one path, not two.
+__device__ __forceinline__ uint64_t hash_terms_masked(int4 v, uint32_t i0, uint32_t L) {
   const int32_t e[4] = {v.x, v.y, v.z, v.w};
   uint64_t s = 0;
 #pragma unroll
   for (int q = 0; q < 4; q++) {
-    const int32_t i = i0 + q;
-    if (i >= 0 && (uint32_t)i < L)
-      s += splitmix64(((uint64_t)(uint32_t)i << 32) | (uint64_t)(uint32_t)e[q]);
+    const uint32_t i = i0 + (uint32_t)q;
+    const uint64_t t = splitmix64(((uint64_t)i << 32) | (uint64_t)(uint32_t)e[q]);
+    s += (i < L) ? t : 0ull;
   }
   return s;
 }
@@ -341,41 +344,34 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
   const uint32_t sh = (uint32_t)(o0 - a0);
   const int4 *base = reinterpret_cast<const int4 *>(tokens + a0);
   const uint32_t end = L + sh;
+  const uint32_t l4 = 4 * (uint32_t)lane;
   uint64_t acc = 0;
   int4 v[4];
-  uint32_t r = 4 * lane;
 #pragma unroll
   for (int u = 0; u < 4; u++) {
-    const uint32_t ru = r + 128 * u;
+    const uint32_t ru = l4 + 128 * u;
     v[u] = make_int4(0, 0, 0, 0);
     if (ru < end) v[u] = __ldcs(base + (ru >> 2));
   }
-  for (; r < end; r += 512) {
+  // r0: the step's first block offset, the same in every lane
+  for (uint32_t r0 = 0; r0 < end; r0 += 512) {
     // the next step's four loads go out before this step's terms
     int4 w[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const uint32_t ru = r + 512 + 128 * u;
+      const uint32_t ru = r0 + 512 + 128 * u + l4;
       w[u] = make_int4(0, 0, 0, 0);
       if (ru < end) w[u] = __ldcs(base + (ru >> 2));
     }
-    // a step whose blocks all lie inside the document (every lane's, which
-    // the warp decides at once from lane 0's offset) needs no checks
-    const uint32_t r0 = r - 4 * lane;
-    if (r0 >= sh && r0 + 512 <= end) {
+    // each group of 128 tokens (one block per lane) is decided for the whole
+    // warp: inside the document -> no checks; across an edge -> masked terms
 #pragma unroll
-      for (int u = 0; u < 4; u++) acc += hash_terms_inside(v[u], r + 128 * u - sh);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const uint32_t ru = r + 128 * u;
-        if (ru < end) {
-          if (ru >= sh && ru + 4 <= end)
-            acc += hash_terms_inside(v[u], ru - sh);
-          else
-            acc += block_terms_edge(v[u], (int32_t)ru - (int32_t)sh, L);
-        }
-      }
+    for (int u = 0; u < 4; u++) {
+      const uint32_t b0 = r0 + 128 * u;
+      if (b0 >= sh && b0 + 128 <= end)
+        acc += hash_terms_inside(v[u], b0 + l4 - sh);
+      else if (b0 < end)
+        acc += hash_terms_masked(v[u], b0 + l4 - sh, L);
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) v[u] = w[u];
