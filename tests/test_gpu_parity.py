@@ -169,6 +169,22 @@ def test_documents_of_exactly_t_are_whole_windows():
     assert (r["pos"][0] == np.arange(T)[None, :]).all()
 
 
+@pytest.mark.parametrize("wrap", [False, True])
+def test_largest_window_length(wrap):
+    # T at the library's limit (NS_MAX_T = 2^24): rows of 16 Mi positions,
+    # documents longer than T (cut into a full chunk and a tail), a document
+    # of the held-out hash 16 Mi tokens long, ragged ends everywhere
+    T = 1 << 24
+    lengths = [T + 37, 5, T - 3, 100, 3, T + 1]
+    c = corpus_from_lengths(lengths, T=T, B=2, max_steps=3, heldout_bp=[1], drain=True)
+    pk, o = packer_for(c, wrap=wrap), oracle_for(c, wrap=wrap)
+    _check_tables(pk, o, c)
+    assert o.valid_steps > 0
+    compare_steps(pk, o, range(o.valid_steps))
+    pk.check()
+    pk.close()
+
+
 def test_horizon_and_row_range_errors():
     c = make_preset("c1")
     pk = packer_for(c)
