@@ -21,6 +21,10 @@ namespace nsk {
 namespace {
 
 constexpr int kThreads = 256;
+// The held-out hash: 128-thread CTAs, 7 per SM (72 registers a thread, no
+// spills; its warps are independent, so only the count per SM matters).
+constexpr int kHashThreads = 128;
+constexpr int kHashBlocksPerSM = 7;
 
 inline unsigned blocks_for(uint64_t n, int threads = kThreads) {
   return (unsigned)((n + threads - 1) / threads);
@@ -385,11 +389,12 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // for training, not held out for validation) has its kept length set to 0.
 // A warp leaves a stream once the kept tokens of the documents already hashed
 // exceed need_j = rmax_j * T (the windows the horizon asks of it hold at most
-// that many), or when the stream runs out, and goes on to the next stream.  Every position below the final frontier is hashed, and the
-// kept tokens below it exceed need_j unless the whole stream was hashed, so
-// the prefix the cutoff kernel then takes only ever holds decided documents.
+// that many), or when the stream runs out, and goes on to the next stream.
+// Every position below the final frontier is hashed, and the kept tokens
+// below it exceed need_j unless the whole stream was hashed, so the prefix
+// the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
                        unsigned long long *kept, uint32_t j_begin, uint32_t j_count) {
-  constexpr uint32_t kGrab = 8;
+  constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   bool ready_seen = false;
@@ -1174,10 +1179,9 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
                                uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
   ++launch_counter();
-  hash_prefix_kernel<<<n_sms * 4, kThreads, 0, st>>>(tokens, offs, sdb, stream_bp, J, D0, order,
-                                                     klen, cum_last, ready, ready_at, T, G,
-                                                     hash_key, want_heldout, frontier, kept,
-                                                     j_begin, j_count);
+  hash_prefix_kernel<<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
+      tokens, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, ready_at, T, G, hash_key,
+      want_heldout, frontier, kept, j_begin, j_count);
   return cudaGetLastError();
 }
 
