@@ -47,8 +47,11 @@ WORKLOADS = {
     "c3m": "a tenth of c3: 200,000 docs, same shape, T=4096, B=512, 96 updates",
     "c4": "4 equal sources x 2,000,000 docs log-normal median 400 sigma 1.0, vocab 50,257, "
           "T=8192, B=256, 200 updates",
+    "c4m": "a tenth of c4: 4 x 200,000 docs, same shape, T=8192, B=256, 64 updates",
     "c5": "1 source of ~1e9 tokens, log-normal median 2048 sigma 1.5 [1,262144], vocab "
           "151,936, T=32768, B=64, long documents cut into T-chunks, full pass (drain)",
+    "c5m": "a tenth of c5: 1 source of ~1e8 tokens, same shape, T=32768, B=64, full pass "
+           "(drain)",
 }
 VARIANTS = {
     "default": "training stream, greedy packing cut at document ends, windows and rows in order",

@@ -251,6 +251,18 @@ def _preset_kwargs(name: str) -> dict:
         kw = _mixture_kwargs(15, 3, 200_000, 100, 500)
         return dict(data_seed=1013, vocab=64000, T=4096, B=512, max_steps=96,
                     length=(600.0, 1.2, 1, 65536), **kw)
+    # --- the same cuts of c4 and c5 (the rows of the full workloads over a
+    # tenth of the corpus) for profiles
+    if name == "c4m":
+        return dict(data_seed=1014, vocab=50257, T=8192, B=256, max_steps=64,
+                    source_weight=[1, 1, 1, 1], stream_source=[0, 1, 2, 3],
+                    stream_weight=[1, 1, 1, 1], heldout_bp=[0, 0, 0, 0],
+                    stream_docs=[200_000] * 4, length=(400.0, 1.0, 1, None))
+    if name == "c5m":
+        return dict(data_seed=1015, vocab=151936, T=32768, B=64, max_steps=1024,
+                    source_weight=[1], stream_source=[0], stream_weight=[1],
+                    heldout_bp=[0], target_tokens=100_000_000,
+                    length=(2048.0, 1.5, 1, 262144), drain=True)
     # --- shrunk variants with the same structure (CPU-sized) ------------
     if name == "c2s":
         return dict(data_seed=2002, vocab=128256, T=4096, B=8, max_steps=16,
@@ -275,13 +287,13 @@ def _preset_kwargs(name: str) -> dict:
     raise KeyError(name)
 
 
-PRESETS = ("c1", "c2", "c3", "c4", "c5", "c3m", "c2s", "c3s", "c4s", "c5s")
+PRESETS = ("c1", "c2", "c3", "c4", "c5", "c3m", "c4m", "c5m", "c2s", "c3s", "c4s", "c5s")
 
 
 def make_preset(name: str, threads: Optional[int] = None, **overrides) -> Corpus:
-    """One of the named workloads (``c1``..``c5`` full size, ``c3m`` a tenth of
-    ``c3``, ``c2s``..``c5s`` shrunk with the same structure); ``overrides``
-    replace recipe fields."""
+    """One of the named workloads (``c1``..``c5`` full size, ``c3m``..``c5m``
+    a tenth of ``c3``..``c5``, ``c2s``..``c5s`` shrunk with the same
+    structure); ``overrides`` replace recipe fields."""
     kw = _preset_kwargs(name)
     kw.update(overrides)
     return make_corpus(name, threads=threads, **kw)
