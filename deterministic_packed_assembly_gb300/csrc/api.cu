@@ -478,7 +478,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(scan_scratch);
   NS_CK(nsk::launch_stream_keys(c->seed, J, keys, st));
   {
-    std::vector<uint32_t> bb = seg_layout(N, 256);
+    std::vector<uint32_t> bb = seg_layout(N, 256 * nsk::order_positions_per_thread());
     void *d_bb;
     if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
@@ -598,9 +598,18 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
     NS_CK(nsk::launch_next(g, node_base, npieces, c->node_S, T, levels, st));
   }
-  for (uint32_t l = 1; l < L; l++)
-    NS_CK(nsk::launch_jump_level(levels + (size_t)(l - 1) * n_nodes, n_nodes,
-                                 levels + (size_t)l * n_nodes, st));
+  // two levels per launch while two remain
+  for (uint32_t l = 1; l < L;) {
+    const int32_t *prev = levels + (size_t)(l - 1) * n_nodes;
+    if (l + 1 < L) {
+      NS_CK(nsk::launch_jump_two_levels(prev, n_nodes, levels + (size_t)l * n_nodes,
+                                        levels + (size_t)(l + 1) * n_nodes, st));
+      l += 2;
+    } else {
+      NS_CK(nsk::launch_jump_level(prev, n_nodes, levels + (size_t)l * n_nodes, st));
+      l += 1;
+    }
+  }
 
   // ---- 7. windows: count, starts, the valid horizon ------------------------
   c->W = a.keep<uint32_t>(J);

@@ -543,6 +543,13 @@ __device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, ui
   return (uint32_t)feistel_walk(k, B, i, err);
 }
 
+// Each thread takes kOrderPerThread positions of one stream, p0 + m * 256,
+// one after the other, and every pass of its loop is one evaluation of the
+// network for every lane: a lane whose walk lands in range writes that
+// position and feeds its next one into the same evaluation.  A warp then
+// pays for the average walk of its positions rather than the longest.
+constexpr uint32_t kOrderPerThread = 8;
+
 __global__ void __launch_bounds__(kThreads)
     order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
                  const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
@@ -552,8 +559,8 @@ __global__ void __launch_bounds__(kThreads)
   seg_locate(g, j, blk);
   const uint32_t b0 = sdb[j];
   const uint64_t N = sdb[j + 1] - b0;
-  const uint64_t p = (uint64_t)blk * blockDim.x + threadIdx.x;
-  if (p >= N) return;
+  const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
+  if (p0 >= N) return;
   uint32_t bits = (N <= 1) ? 0u : (uint32_t)(64 - __clzll((long long)(N - 1)));
   if (bits < 2) bits = 2;
   bits += bits & 1u;
@@ -562,23 +569,32 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t k[4];
 #pragma unroll
   for (int r = 0; r < 4; r++) k[r] = keys[(size_t)j * 4 + r];
-  uint64_t y = feistel(k, half, mask, p);
-  for (uint32_t it = 0; y >= N; it++) {
-    if (it > (1u << 20)) {
+  // the validation stream of a source that holds nothing out is empty
+  const bool empty = stream_bp_heldout_mode && stream_bp_heldout_mode[j] == 0;
+  uint64_t p = p0, x = p0;
+  uint32_t m = 0, it = 0;
+  while (true) {
+    uint64_t y = feistel(k, half, mask, x);
+    if (y >= N && ++it > (1u << 20)) {
       set_error(err, kDevWalkLimit);
       y = 0;
-      break;
     }
-    y = feistel(k, half, mask, y);
+    if (y < N) {
+      const uint32_t d = b0 + (uint32_t)y;
+      const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
+      const bool ok =
+          !empty && o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
+      const uint64_t idx = (uint64_t)b0 + p - D0;
+      order[idx] = d;
+      klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
+      p += blockDim.x;
+      if (++m >= kOrderPerThread || p >= N) break;
+      x = p;
+      it = 0;
+    } else {
+      x = y;
+    }
   }
-  const uint32_t d = b0 + (uint32_t)y;
-  const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
-  bool ok = o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
-  // the validation stream of a source that holds nothing out is empty
-  if (stream_bp_heldout_mode && stream_bp_heldout_mode[j] == 0) ok = false;
-  const uint64_t idx = (uint64_t)b0 + p - D0;
-  order[idx] = d;
-  klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -841,6 +857,17 @@ __global__ void jump_level_kernel(const int32_t *__restrict__ up, int64_t n,
   const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= n) return;
   out[x] = __ldg(up + __ldg(up + x));
+}
+
+// Two levels from one: with up = level l, level l + 1 is up o up and level
+// l + 2 is up o up o up o up, so one launch writes both from level l alone.
+__global__ void jump_two_levels_kernel(const int32_t *__restrict__ up, int64_t n,
+                                       int32_t *__restrict__ out1, int32_t *__restrict__ out2) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= n) return;
+  const int32_t b = __ldg(up + __ldg(up + x));
+  out1[x] = b;
+  out2[x] = __ldg(up + __ldg(up + b));
 }
 
 // W_j: hops from the stream's first node to its terminal, by binary lifting.
@@ -1185,6 +1212,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const
   return cudaGetLastError();
 }
 
+uint32_t order_positions_per_thread() { return kOrderPerThread; }
+
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
@@ -1266,6 +1295,14 @@ cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *
   ++launch_counter();
   jump_level_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
                                                                          up_next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_jump_two_levels(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
+                                   int32_t *up_next2, cudaStream_t st) {
+  ++launch_counter();
+  jump_two_levels_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
+                                                                              up_next, up_next2);
   return cudaGetLastError();
 }
 

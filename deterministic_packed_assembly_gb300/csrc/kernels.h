@@ -88,6 +88,12 @@ cudaError_t launch_next(SegGrid g, const int64_t *node_base, const int64_t *npie
                         const int64_t *node_S, uint32_t T, int32_t *next, cudaStream_t st);
 cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
                               cudaStream_t st);
+// levels l and l + 1 from level l - 1 in one launch
+cudaError_t launch_jump_two_levels(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
+                                   int32_t *up_next2, cudaStream_t st);
+// positions a thread of the shuffle kernel takes (its grid: blocks of 256
+// threads over segments of 256 * order_positions_per_thread() positions)
+uint32_t order_positions_per_thread();
 // levels: [n_levels][n_nodes], level l maps a node to the node 2^l windows on
 cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_t n_levels,
                                  const int64_t *node_base, const int64_t *npieces, uint32_t J,
