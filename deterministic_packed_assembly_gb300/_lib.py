@@ -91,6 +91,7 @@ class ns_pack_info_t(C.Structure):
         ("table_bytes", C.c_uint64),
         ("init_launches", C.c_uint32),
         ("reserved", C.c_uint32),
+        ("host_bytes", C.c_uint64),
     ]
 
 

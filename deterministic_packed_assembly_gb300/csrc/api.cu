@@ -21,6 +21,7 @@ struct ns_pack_ctx {
   int32_t pad_id = 0;
   uint64_t seed = 0, hash_key = 0, n_tokens = 0;
   const int32_t *tokens = nullptr;
+  int32_t *tokens_rw = nullptr;  // the context's own copy of a host-resident corpus
   const int64_t *offs = nullptr;
   const int32_t *loss_start = nullptr;
   cudaStream_t stream = nullptr;
@@ -34,6 +35,7 @@ struct ns_pack_ctx {
   std::vector<uint8_t> complete;
   uint32_t valid_steps = 0, levels = 0, init_launches = 0;
   uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
+  uint64_t host_bytes = 0;  // bytes of a host-resident corpus read at init
   // device tables kept for the per-update calls
   int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
   uint32_t *W = nullptr;
@@ -280,6 +282,28 @@ struct Staging {
   }
 };
 
+// The device address of n tokens in host memory when both ends of the range
+// are page-locked memory the device can address (cudaHostAlloc, or
+// registered with cudaHostRegister) and it starts on a 16-byte boundary;
+// NULL otherwise (the corpus is then copied whole).
+const int32_t *device_view(const int32_t *host, uint64_t n) {
+  if (!host || n == 0) return nullptr;
+  cudaPointerAttributes a0{}, a1{};
+  if (cudaPointerGetAttributes(&a0, host) != cudaSuccess ||
+      cudaPointerGetAttributes(&a1, host + (n - 1)) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a0.type != cudaMemoryTypeHost || a1.type != cudaMemoryTypeHost || !a0.devicePointer ||
+      !a1.devicePointer)
+    return nullptr;
+  const char *d0 = static_cast<const char *>(a0.devicePointer);
+  const char *d1 = static_cast<const char *>(a1.devicePointer);
+  if (d1 - d0 != (ptrdiff_t)((n - 1) * sizeof(int32_t))) return nullptr;
+  if (reinterpret_cast<uintptr_t>(d0) & 15) return nullptr;
+  return reinterpret_cast<const int32_t *>(d0);
+}
+
 int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st) {
   *dev = a.get(bytes, false);
   NS_ALLOC(*dev);
@@ -296,12 +320,18 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   int rc;
 
   // ---- a corpus in host memory: the context's device copy ----------------
-  // Offsets and loss starts first (the shuffle needs them); the tokens in
-  // groups of whole streams on a second stream, the hash of each group
-  // waiting only for its own copy.
+  // Offsets and loss starts first (the shuffle needs them).  Tokens in
+  // page-locked memory the device can address are read where they lie: the
+  // hash writes every document it reads into the copy and a copy kernel
+  // brings over the reachable prefix of the streams it does not read, so
+  // only the documents the horizon reaches cross the host link.  Other host
+  // memory is copied whole, in groups of whole streams on a second stream,
+  // the hash of each group waiting only for its own copy.
   const bool host_corpus = (c->flags & NS_PACK_HOST_CORPUS) != 0;
+  const int32_t *htok = nullptr;  // device address of host tokens read in place
   CorpusCopy copy;
   if (host_corpus) {
+    htok = device_view(cfg->tokens, c->n_tokens);
     int32_t *tok = a.keep<int32_t>(c->n_tokens + 4);
     int64_t *offs = a.keep<int64_t>((size_t)c->n_docs + 1);
     int32_t *ls = cfg->loss_start ? a.keep<int32_t>(std::max<uint32_t>(c->n_docs, 1)) : nullptr;
@@ -313,33 +343,39 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     if (ls)
       NS_CK(cudaMemcpyAsync(ls, cfg->loss_start, (size_t)c->n_docs * 4, cudaMemcpyHostToDevice,
                             st));
-    NS_CK(copy.create());
-    // group boundaries where whole streams end, about an eighth of the tokens
-    // each; offsets that are not nondecreasing inside [0, n_tokens] at the
-    // streams' bounds make one group (the device check then reports them)
-    const int64_t *ho = cfg->doc_offsets;
-    const uint64_t nt = c->n_tokens;
-    bool ok = true;
-    std::vector<uint64_t> ob(J + 1);
-    for (uint32_t j = 0; j <= J && ok; j++) {
-      const int64_t v = ho[cfg->stream_doc_begin[j]];
-      ok = v >= 0 && (uint64_t)v <= nt && (j == 0 || (uint64_t)v >= ob[j - 1]);
-      ob[j] = ok ? (uint64_t)v : 0;
+    c->host_bytes = ((uint64_t)c->n_docs + 1) * 8 + (ls ? (uint64_t)c->n_docs * 4 : 0);
+    if (!htok) {
+      NS_CK(copy.create());
+      // group boundaries where whole streams end, about an eighth of the
+      // tokens each; offsets that are not nondecreasing inside [0, n_tokens]
+      // at the streams' bounds make one group (the device check then reports
+      // them)
+      const int64_t *ho = cfg->doc_offsets;
+      const uint64_t nt = c->n_tokens;
+      bool ok = true;
+      std::vector<uint64_t> ob(J + 1);
+      for (uint32_t j = 0; j <= J && ok; j++) {
+        const int64_t v = ho[cfg->stream_doc_begin[j]];
+        ok = v >= 0 && (uint64_t)v <= nt && (j == 0 || (uint64_t)v >= ob[j - 1]);
+        ob[j] = ok ? (uint64_t)v : 0;
+      }
+      uint64_t begin = 0;
+      copy.j_first.push_back(0);
+      if (ok) {
+        const uint64_t target = std::max<uint64_t>(nt / 8, 1);
+        for (uint32_t j = 1; j < J; j++)
+          if (ob[j] - begin >= target) {
+            NS_CK(copy.add_group(cfg->tokens, tok, begin, ob[j]));
+            copy.j_first.push_back(j);
+            begin = ob[j];
+          }
+      }
+      NS_CK(copy.add_group(cfg->tokens, tok, begin, nt));
+      copy.j_first.push_back(J);
+      c->host_bytes += nt * 4;
     }
-    uint64_t begin = 0;
-    copy.j_first.push_back(0);
-    if (ok) {
-      const uint64_t target = std::max<uint64_t>(nt / 8, 1);
-      for (uint32_t j = 1; j < J; j++)
-        if (ob[j] - begin >= target) {
-          NS_CK(copy.add_group(cfg->tokens, tok, begin, ob[j]));
-          copy.j_first.push_back(j);
-          begin = ob[j];
-        }
-    }
-    NS_CK(copy.add_group(cfg->tokens, tok, begin, nt));
-    copy.j_first.push_back(J);
     c->tokens = tok;
+    c->tokens_rw = tok;
     c->offs = offs;
     c->loss_start = ls;
   }
@@ -490,6 +526,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
   // Runs beside the quota kernels: it reads each stream's need from their
   // table once all S quota blocks have published it, and hashes on until then.
+  // tokens read from host memory in place (hash and prefix copy)
+  unsigned long long *tokens_read = nullptr;
+  if (htok) {
+    tokens_read = a.temp<unsigned long long>(1);
+    NS_ALLOC(tokens_read);
+    NS_CK(cudaMemsetAsync(tokens_read, 0, sizeof(unsigned long long), st));
+  }
+  const bool group_copy = host_corpus && !htok;
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *kept = a.temp<unsigned long long>(J);
@@ -498,12 +542,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
     // one launch over every stream, or one per copied group of streams
-    const size_t n_groups = host_corpus ? copy.done.size() : 1;
+    const size_t n_groups = group_copy ? copy.done.size() : 1;
     for (size_t gi = 0; gi < n_groups; gi++) {
-      const uint32_t j0 = host_corpus ? copy.j_first[gi] : 0;
-      const uint32_t j1 = host_corpus ? copy.j_first[gi + 1] : J;
-      if (host_corpus) NS_CK(cudaStreamWaitEvent(st, copy.done[gi], 0));
-      NS_CK(nsk::launch_hash_prefix(c->tokens, c->offs, static_cast<uint32_t *>(d_sdb),
+      const uint32_t j0 = group_copy ? copy.j_first[gi] : 0;
+      const uint32_t j1 = group_copy ? copy.j_first[gi + 1] : J;
+      if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done[gi], 0));
+      NS_CK(nsk::launch_hash_prefix(htok ? htok : c->tokens, htok ? c->tokens_rw : nullptr,
+                                    tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                     heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0,
@@ -511,7 +556,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     }
   }
   // every token is on the device before anything after the hash reads it
-  if (host_corpus) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
+  if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)
@@ -566,6 +611,28 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   while ((1ll << L) < max_pieces + 1) L++;
   if (wrap) L = 0;  // wrap windows are found by position, without pointer jumping
   c->levels = L;
+
+  // ---- 5. tokens of the prefixes the hash did not read --------------------
+  // (host tokens read in place only): on the second stream, beside the
+  // piece tables, which do not read tokens; joined before the summary
+  bool prefix_copy = false;
+  if (htok) {
+    std::vector<uint64_t> cnt(J);
+    for (uint32_t j = 0; j < J; j++) cnt[j] = stream_bp[j] == 0 ? cut_h[j] : 0;
+    std::vector<uint32_t> bb = seg_layout(cnt, 8);
+    if (bb[J] > 0) {
+      void *d_bb;
+      if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
+      nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+      NS_CK(cudaEventRecord(side.fork, st));
+      NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
+      NS_CK(nsk::launch_copy_prefix(g, static_cast<uint32_t *>(d_sdb), D0, cutoff,
+                                    static_cast<uint16_t *>(d_stream_bp), order, klen, c->offs,
+                                    htok, c->tokens_rw, tokens_read, side.s));
+      NS_CK(cudaEventRecord(side.join, side.s));
+      prefix_copy = true;
+    }
+  }
 
   // ---- 6. pieces, next window start, pointer jumping ----------------------
   c->node_src = a.keep<int64_t>(n_nodes);
@@ -684,9 +751,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                            c->err, dacc, ubase, digest, st));
 
   // ---- 9. read back the summary ------------------------------------------
+  if (prefix_copy) NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   std::vector<uint32_t> W_h(J);
   uint32_t valid_h = 0;
   uint64_t digest_h = 0;
+  unsigned long long read_h = 0;
+  if (tokens_read)
+    NS_CK(cudaMemcpyAsync(&read_h, tokens_read, sizeof(read_h), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(W_h.data(), c->W, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&valid_h, valid, 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&digest_h, digest, 8, cudaMemcpyDeviceToHost, st));
@@ -696,6 +767,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->windows.assign(W_h.begin(), W_h.end());
   c->valid_steps = valid_h;
   c->digest = digest_h;
+  c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
   return NS_OK;
 }
 
@@ -843,6 +915,7 @@ int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
   info->table_bytes = ctx->table_bytes;
   info->init_launches = ctx->init_launches;
   info->reserved = 0;
+  info->host_bytes = ctx->host_bytes;
   return NS_OK;
 }
 

@@ -341,12 +341,19 @@ __device__ __forceinline__ uint64_t hash_terms_masked(int4 v, uint32_t i0, uint3
 
 // The whole warp sums the token terms of tokens[o0, o0 + L); every lane gets
 // the sum.  Offsets are taken relative to the 16-byte block holding the
-// first token, in 32 bits (documents are shorter than 2^31 tokens).
-__device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ tokens, int64_t o0,
+// first token, in 32 bits (documents are shorter than 2^31 tokens).  With
+// kCopy, every block read is also written to the same place in dst (a
+// corpus read from host memory lands in the device copy as it is hashed;
+// the few tokens of neighbouring documents that share the first and last
+// blocks are written with the values they have).
+template <bool kCopy>
+__device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ tokens,
+                                                   int32_t *__restrict__ dst, int64_t o0,
                                                    uint32_t L, int lane) {
   const int64_t a0 = o0 & ~(int64_t)3;
   const uint32_t sh = (uint32_t)(o0 - a0);
   const int4 *base = reinterpret_cast<const int4 *>(tokens + a0);
+  int4 *dbase = kCopy ? reinterpret_cast<int4 *>(dst + a0) : nullptr;
   const uint32_t end = L + sh;
   const uint32_t l4 = 4 * (uint32_t)lane;
   uint64_t acc = 0;
@@ -372,6 +379,7 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const uint32_t b0 = r0 + 128 * u;
+      if (kCopy && b0 + l4 < end) dbase[(b0 >> 2) + lane] = v[u];
       if (b0 >= sh && b0 + 128 <= end)
         acc += hash_terms_inside(v[u], b0 + l4 - sh);
       else if (b0 < end)
@@ -394,8 +402,12 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // below it exceed need_j unless the whole stream was hashed, so the prefix
 // the cutoff kernel then takes only ever holds decided documents.
 // Warps start on different streams so that few overshoot any one stream.
+// With kCopy the tokens are read from host memory the device can address
+// and every hashed document is written to copy_dst; tokens_read counts them.
+template <bool kCopy>
 __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
-    hash_prefix_kernel(const int32_t *__restrict__ tokens, const int64_t *__restrict__ offs,
+    hash_prefix_kernel(const int32_t *__restrict__ tokens, int32_t *__restrict__ copy_dst,
+                       unsigned long long *tokens_read, const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
@@ -448,7 +460,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         const uint32_t L = __shfl_sync(0xffffffffu, L_l, q);
         if (L == 0) continue;
         const int64_t o0 = __shfl_sync(0xffffffffu, o_l, q);
-        const uint64_t tot = warp_doc_terms(tokens, o0, L, lane);
+        const uint64_t tot = warp_doc_terms<kCopy>(tokens, copy_dst, o0, L, lane);
         if (lane == q) mine = tot;
       }
       // lane q decides document q
@@ -463,8 +475,50 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
       }
       kept_here = warp_sum_u64(kept_here);
       if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
+      if (kCopy) {
+        const unsigned long long read_here = warp_sum_u64(L_l);
+        if (lane == 0 && read_here) atomicAdd(tokens_read, read_here);
+      }
     }
   }
+}
+
+// The reachable prefix of every stream the hash does not read (no held-out
+// rate), copied from host memory the device can address into the device
+// copy: one warp per position of the prefix, in 16-byte blocks, four in
+// flight per lane.  Positions [0, cutoff[j]) of each such stream; documents
+// whose kept length is 0 (empty, or malformed offsets) are not read.
+constexpr int kCopyWarps = kThreads / 32;
+
+__global__ void __launch_bounds__(kThreads)
+    copy_prefix_kernel(SegGrid g, const uint32_t *__restrict__ sdb, uint32_t D0,
+                       const uint32_t *__restrict__ cutoff, const uint16_t *__restrict__ stream_bp,
+                       const uint32_t *__restrict__ order, const uint32_t *__restrict__ klen,
+                       const int64_t *__restrict__ offs, const int32_t *__restrict__ src,
+                       int32_t *__restrict__ dst, unsigned long long *tokens_read) {
+  uint32_t j, blk;
+  seg_locate(g, j, blk);
+  const int lane = threadIdx.x & 31;
+  const uint64_t p = (uint64_t)blk * kCopyWarps + (threadIdx.x >> 5);
+  if (stream_bp[j] != 0 || p >= cutoff[j]) return;
+  const uint64_t idx = (uint64_t)sdb[j] - D0 + p;
+  const uint32_t L = klen[idx];
+  if (L == 0) return;
+  const int64_t o0 = __ldg(offs + order[idx]);
+  const int64_t a0 = o0 & ~(int64_t)3;
+  const uint32_t end = L + (uint32_t)(o0 - a0);
+  const int4 *s4 = reinterpret_cast<const int4 *>(src + a0);
+  int4 *d4 = reinterpret_cast<int4 *>(dst + a0);
+  for (uint32_t r = 4 * (uint32_t)lane; r < end; r += 512) {
+    int4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      if (r + 128 * u < end) v[u] = __ldcs(s4 + ((r + 128 * u) >> 2));
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      if (r + 128 * u < end) d4[(r + 128 * u) >> 2] = v[u];
+  }
+  if (lane == 0) atomicAdd(tokens_read, (unsigned long long)L);
 }
 
 // ---------------------------------------------------------------------------
@@ -1197,18 +1251,36 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
   return cudaGetLastError();
 }
 
-cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
-                               const uint16_t *stream_bp, uint32_t J, uint32_t D0,
-                               const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
-                               uint64_t hash_key, uint32_t want_heldout,
+cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
+                               unsigned long long *tokens_read, const int64_t *offs,
+                               const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
+                               uint32_t D0, const uint32_t *order, uint32_t *klen,
+                               const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
+                               uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
                                uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
   ++launch_counter();
-  hash_prefix_kernel<<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
-      tokens, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, ready_at, T, G, hash_key,
-      want_heldout, frontier, kept, j_begin, j_count);
+  if (copy_dst)
+    hash_prefix_kernel<true><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
+        tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
+        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count);
+  else
+    hash_prefix_kernel<false><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
+        tokens, nullptr, nullptr, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
+        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
+                               const uint32_t *cutoff, const uint16_t *stream_bp,
+                               const uint32_t *order, const uint32_t *klen, const int64_t *offs,
+                               const int32_t *src, int32_t *dst, unsigned long long *tokens_read,
+                               cudaStream_t st) {
+  if (g.n_blocks == 0) return cudaSuccess;
+  ++launch_counter();
+  copy_prefix_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, stream_bp, order, klen,
+                                                      offs, src, dst, tokens_read);
   return cudaGetLastError();
 }
 

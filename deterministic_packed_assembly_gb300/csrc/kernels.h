@@ -58,13 +58,24 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
                          int *err, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
-cudaError_t launch_hash_prefix(const int32_t *tokens, const int64_t *offs, const uint32_t *sdb,
-                               const uint16_t *stream_bp, uint32_t J, uint32_t D0,
-                               const uint32_t *order, uint32_t *klen, const int32_t *cum_last,
-                               const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
-                               uint64_t hash_key, uint32_t want_heldout,
+// copy_dst non-null: tokens is host memory the device can address, and
+// every hashed document is also written to copy_dst (tokens_read counts them)
+cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
+                               unsigned long long *tokens_read, const int64_t *offs,
+                               const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
+                               uint32_t D0, const uint32_t *order, uint32_t *klen,
+                               const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
+                               uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
                                uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st);
+// Documents of positions [0, cutoff[j]) of every stream with stream_bp[j] ==
+// 0, copied from src (host memory the device can address) to dst; the grid
+// has a block per 8 positions of those prefixes.
+cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
+                               const uint32_t *cutoff, const uint16_t *stream_bp,
+                               const uint32_t *order, const uint32_t *klen, const int64_t *offs,
+                               const int32_t *src, int32_t *dst, unsigned long long *tokens_read,
+                               cudaStream_t st);
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,

@@ -84,11 +84,17 @@ extern "C" {
  * the whole stream is inside the reachable prefix. */
 #define NS_PACK_WRAP 8u
 /* The corpus (tokens, doc_offsets, loss_start) is in host memory: the
- * context copies it to the device (its own copy, kept with the tables and
- * counted in table_bytes), offsets first and the tokens in groups of whole
- * streams on a second stream, hashing each group as soon as its copy lands.
- * Page-locked host memory lets the copies run beside the kernels; the host
- * buffers may be released once ns_pack_init returns. */
+ * context keeps its own device copy (kept with the tables and counted in
+ * table_bytes), offsets and loss starts copied first.  Tokens in page-locked
+ * memory the device can address (cudaHostAlloc, or cudaHostRegister; 16-byte
+ * aligned) are read where they lie, and only the documents the horizon
+ * reaches cross the host link: the held-out hash writes every document it
+ * reads into the copy, and a copy kernel brings over the reachable prefix of
+ * every stream whose source has no held-out rate.  Tokens in other host
+ * memory are copied whole, in groups of whole streams on a second stream,
+ * each group hashed as soon as its copy lands.  ns_pack_info reports the
+ * bytes read (host_bytes); the host buffers may be released once
+ * ns_pack_init returns. */
 #define NS_PACK_HOST_CORPUS 16u
 
 /* ---- limits ------------------------------------------------------------- */
@@ -194,6 +200,10 @@ typedef struct {
   uint64_t table_bytes; /* device bytes the context keeps */
   uint32_t init_launches; /* kernels ns_pack_init launched */
   uint32_t reserved;
+  uint64_t host_bytes;  /* bytes of a host-resident corpus (NS_PACK_HOST_CORPUS)
+                           that ns_pack_init read from host memory: offsets,
+                           loss starts and the tokens it used (the whole
+                           corpus when it had to copy it); 0 otherwise */
 } ns_pack_info_t;
 
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of

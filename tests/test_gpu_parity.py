@@ -432,22 +432,69 @@ def _host_packer(c, pinned=True, **kw):
     return Packer(t, o, ls, device="cuda:0", **args)
 
 
-@pytest.mark.parametrize("name,pinned,kw", [("c1", True, {}), ("c2s", False, {}),
-                                            ("c3s", True, {}), ("c3s", True, {"wrap": True}),
-                                            ("c5s", True, {"heldout_only": True, "drain": True})])
+def _poison_cache(nbytes=1 << 30):
+    """Leave one block of nbytes filled with 0x7f in torch's caching allocator
+    and nothing else, so that the next context's device memory (its copy of a
+    host corpus included) starts as garbage rather than as a corpus an
+    earlier test left behind."""
+    import torch
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.full((nbytes // 4,), 0x7F7F7F7F, dtype=torch.int32, device="cuda:0")
+    torch.cuda.synchronize()
+
+
+def _corpus_bytes(c):
+    return c.n_tokens * 4 + (c.n_docs + 1) * 8 + (0 if c.loss_start is None else c.n_docs * 4)
+
+
+@pytest.mark.parametrize("name,pinned,kw", [
+    ("c1", True, {}), ("c1", False, {}), ("c1", True, {"heldout_only": True, "drain": True}),
+    ("c2s", False, {}), ("c2s", True, {}), ("c3s", True, {}), ("c3s", False, {}),
+    ("c3s", True, {"wrap": True}), ("c4s", True, {}), ("c5s", True, {}),
+    ("c5s", True, {"heldout_only": True, "drain": True})])
 def test_host_corpus(name, pinned, kw):
-    # the corpus handed over in host memory: the library's own device copy,
-    # hashed group by group as it lands, gives the same context and rows
+    # the corpus handed over in host memory gives the same context and rows:
+    # page-locked tokens are read in place (the hash and the prefix copy write
+    # what the horizon reaches into the library's device copy), other host
+    # memory is copied whole, group by group as the hash goes
     c = make_preset(name)
+    _poison_cache()
     pk = _host_packer(c, pinned, **kw)
     assert pk.host_corpus
     o = oracle_for(c, **kw)
     _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=4)
+    pk.check()
+    host = pk.info["host_bytes"]
+    meta = (c.n_docs + 1) * 8 + (0 if c.loss_start is None else c.n_docs * 4)
+    if pinned:
+        assert meta <= host <= _corpus_bytes(c)
+    else:
+        assert host == _corpus_bytes(c)
     ref = packer_for(c, **kw)
     assert pk.order_digest == ref.order_digest
     assert pk.info["table_bytes"] > ref.info["table_bytes"]  # it holds the corpus too
-    compare_steps(pk, o, range(o.valid_steps), launch=4)
-    pk.check()
+    assert ref.info["host_bytes"] == 0
+
+
+@pytest.mark.parametrize("name", ["c3m", "c4s"])
+def test_host_corpus_reads_only_the_reachable_prefix(name):
+    # a horizon of two updates reaches a small part of the corpus: only its
+    # documents cross the host link (held-out hash for the 200,000-document
+    # mixture -- its warps' documents in flight when a stream stops are read
+    # too -- the prefix copy for c4s, whose sources hold nothing out), and
+    # its rows are exact
+    c = make_preset(name, max_steps=2)
+    _poison_cache()
+    pk = _host_packer(c, True)
+    o = oracle_for(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps))
+    meta = (c.n_docs + 1) * 8
+    tokens_read = pk.info["host_bytes"] - meta
+    used = sum(int((o.rows(k)["doc"] >= 0).sum()) for k in range(o.valid_steps)) * 4
+    assert used <= tokens_read < 0.5 * c.n_tokens * 4, (used, tokens_read, c.n_tokens * 4)
 
 
 def _raw_config(c, tok, off, alloc, free, **flags):
