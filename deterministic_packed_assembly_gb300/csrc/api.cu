@@ -282,6 +282,20 @@ struct Staging {
   }
 };
 
+// Token bounds of every stream, ob[j] = doc_offsets[stream_doc_begin[j]],
+// from the host offsets; false if they are not nondecreasing inside [0,
+// n_tokens] (the device check then reports the partition).
+bool stream_token_bounds(const ns_pack_config *cfg, uint32_t J, uint64_t nt,
+                         std::vector<uint64_t> &ob) {
+  ob.assign(J + 1, 0);
+  for (uint32_t j = 0; j <= J; j++) {
+    const int64_t v = cfg->doc_offsets[cfg->stream_doc_begin[j]];
+    if (v < 0 || (uint64_t)v > nt || (j > 0 && (uint64_t)v < ob[j - 1])) return false;
+    ob[j] = (uint64_t)v;
+  }
+  return true;
+}
+
 // The device address of n tokens in host memory when both ends of the range
 // are page-locked memory the device can address (cudaHostAlloc, or
 // registered with cudaHostRegister) and it starts on a 16-byte boundary;
@@ -350,15 +364,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       // tokens each; offsets that are not nondecreasing inside [0, n_tokens]
       // at the streams' bounds make one group (the device check then reports
       // them)
-      const int64_t *ho = cfg->doc_offsets;
       const uint64_t nt = c->n_tokens;
-      bool ok = true;
-      std::vector<uint64_t> ob(J + 1);
-      for (uint32_t j = 0; j <= J && ok; j++) {
-        const int64_t v = ho[cfg->stream_doc_begin[j]];
-        ok = v >= 0 && (uint64_t)v <= nt && (j == 0 || (uint64_t)v >= ob[j - 1]);
-        ob[j] = ok ? (uint64_t)v : 0;
-      }
+      std::vector<uint64_t> ob;
+      const bool ok = stream_token_bounds(cfg, J, nt, ob);
       uint64_t begin = 0;
       copy.j_first.push_back(0);
       if (ok) {
@@ -567,20 +575,23 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // ---- 4. the prefix of each stream the horizon reaches -------------------
   uint32_t *cutoff = a.temp<uint32_t>(J);
   int64_t *npieces = a.temp<int64_t>(J);
+  int64_t *ptokens = a.temp<int64_t>(J);
   int64_t *node_base = a.temp<int64_t>(J + 1);
   NS_ALLOC(cutoff);
   NS_ALLOC(npieces);
+  NS_ALLOC(ptokens);
   NS_ALLOC(node_base);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
-                           T, c->G, cutoff, npieces, st));
+                           T, c->G, cutoff, npieces, ptokens, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
   std::vector<uint32_t> cut_h(J);
-  std::vector<int64_t> np_h(J), nb_h(J + 1);
+  std::vector<int64_t> np_h(J), nb_h(J + 1), pt_h(J);
   std::vector<int32_t> rmax32(J);
   int err_host = 0;
   NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(nb_h.data(), node_base, (J + 1) * 8, cudaMemcpyDeviceToHost, st));
+  if (htok) NS_CK(cudaMemcpyAsync(pt_h.data(), ptokens, J * 8, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
                         cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -614,21 +625,49 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
 
   // ---- 5. tokens of the prefixes the hash did not read --------------------
   // (host tokens read in place only): on the second stream, beside the
-  // piece tables, which do not read tokens; joined before the summary
+  // piece tables, which do not read tokens; joined before the summary.  A
+  // prefix holding more than three quarters of its stream's tokens is copied
+  // whole by the copy engine (one contiguous run, the host link's fastest
+  // path); the others by chunks of their kept tokens.
   bool prefix_copy = false;
   if (htok) {
-    std::vector<uint64_t> cnt(J);
-    for (uint32_t j = 0; j < J; j++) cnt[j] = stream_bp[j] == 0 ? cut_h[j] : 0;
+    std::vector<uint64_t> ob;
+    const bool bounds = stream_token_bounds(cfg, J, c->n_tokens, ob);
+    const uint64_t chunk = nsk::copy_chunk_tokens();
+    std::vector<uint64_t> cnt(J, 0);
+    std::vector<std::pair<uint64_t, uint64_t>> whole;  // token ranges [begin, end)
+    for (uint32_t j = 0; j < J; j++) {
+      if (stream_bp[j] != 0 || pt_h[j] <= 0) continue;
+      if (bounds && 4 * (uint64_t)pt_h[j] > 3 * (ob[j + 1] - ob[j])) {
+        if (!whole.empty() && whole.back().second == ob[j])
+          whole.back().second = ob[j + 1];
+        else
+          whole.emplace_back(ob[j], ob[j + 1]);
+      } else {
+        cnt[j] = ((uint64_t)pt_h[j] + chunk - 1) / chunk;
+      }
+    }
     std::vector<uint32_t> bb = seg_layout(cnt, 8);
-    if (bb[J] > 0) {
-      void *d_bb;
-      if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
-      nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    if (bb[J] > 0 || !whole.empty()) {
       NS_CK(cudaEventRecord(side.fork, st));
       NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
-      NS_CK(nsk::launch_copy_prefix(g, static_cast<uint32_t *>(d_sdb), D0, cutoff,
-                                    static_cast<uint16_t *>(d_stream_bp), order, klen, c->offs,
-                                    htok, c->tokens_rw, tokens_read, side.s));
+      for (const auto &r : whole) {
+        NS_CK(cudaMemcpyAsync(c->tokens_rw + r.first, cfg->tokens + r.first,
+                              (r.second - r.first) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                              side.s));
+        c->host_bytes += (r.second - r.first) * sizeof(int32_t);
+      }
+      if (bb[J] > 0) {
+        void *d_bb;
+        if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
+        nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+        // the grid table is uploaded on the main stream: fork after it
+        NS_CK(cudaEventRecord(side.fork, st));
+        NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
+        NS_CK(nsk::launch_copy_prefix(g, static_cast<uint32_t *>(d_sdb), D0, cutoff,
+                                      static_cast<uint16_t *>(d_stream_bp), order, klen, kex,
+                                      c->offs, htok, c->tokens_rw, tokens_read, side.s));
+      }
       NS_CK(cudaEventRecord(side.join, side.s));
       prefix_copy = true;
     }

@@ -485,40 +485,62 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
 
 // The reachable prefix of every stream the hash does not read (no held-out
 // rate), copied from host memory the device can address into the device
-// copy: one warp per position of the prefix, in 16-byte blocks, four in
-// flight per lane.  Positions [0, cutoff[j]) of each such stream; documents
-// whose kept length is 0 (empty, or malformed offsets) are not read.
+// copy.  The prefix's kept tokens, in position order, are cut into chunks
+// of kCopyChunk tokens, one warp per chunk, so that a long document is
+// shared by many warps: the warp finds the chunk's first position by binary
+// search over the kept-length scan, then copies the part of each document
+// that falls in the chunk in 16-byte blocks, four in flight per lane (the
+// few tokens of neighbouring documents that share a block are written with
+// the values they have).  Positions whose kept length is 0 (empty, or
+// malformed offsets) hold no tokens of the chunk and are never read.
 constexpr int kCopyWarps = kThreads / 32;
+constexpr uint32_t kCopyChunk = 16384;
 
 __global__ void __launch_bounds__(kThreads)
     copy_prefix_kernel(SegGrid g, const uint32_t *__restrict__ sdb, uint32_t D0,
                        const uint32_t *__restrict__ cutoff, const uint16_t *__restrict__ stream_bp,
                        const uint32_t *__restrict__ order, const uint32_t *__restrict__ klen,
-                       const int64_t *__restrict__ offs, const int32_t *__restrict__ src,
-                       int32_t *__restrict__ dst, unsigned long long *tokens_read) {
+                       const int64_t *__restrict__ kex, const int64_t *__restrict__ offs,
+                       const int32_t *__restrict__ src, int32_t *__restrict__ dst,
+                       unsigned long long *tokens_read) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const int lane = threadIdx.x & 31;
-  const uint64_t p = (uint64_t)blk * kCopyWarps + (threadIdx.x >> 5);
-  if (stream_bp[j] != 0 || p >= cutoff[j]) return;
-  const uint64_t idx = (uint64_t)sdb[j] - D0 + p;
-  const uint32_t L = klen[idx];
-  if (L == 0) return;
-  const int64_t o0 = __ldg(offs + order[idx]);
-  const int64_t a0 = o0 & ~(int64_t)3;
-  const uint32_t end = L + (uint32_t)(o0 - a0);
-  const int4 *s4 = reinterpret_cast<const int4 *>(src + a0);
-  int4 *d4 = reinterpret_cast<int4 *>(dst + a0);
-  for (uint32_t r = 4 * (uint32_t)lane; r < end; r += 512) {
-    int4 v[4];
+  const uint64_t chunk = (uint64_t)blk * kCopyWarps + (threadIdx.x >> 5);
+  if (stream_bp[j] != 0) return;
+  const uint64_t b = (uint64_t)sdb[j] - D0, cut = cutoff[j];
+  const int64_t base = kex[b], total = kex[b + cut] - base;
+  const int64_t t0 = (int64_t)chunk * kCopyChunk;
+  if (t0 >= total) return;
+  const int64_t t1 = min(total, t0 + (int64_t)kCopyChunk);
+  // the position holding kept token t0: the last p in [0, cut) with
+  // kex[b + p] - base <= t0 (zero-length positions share their successor's
+  // scan value and are skipped below)
+  int64_t p = last_le<int64_t, int64_t>(kex, (int64_t)b, (int64_t)(b + cut), base + t0) - (int64_t)b;
+  for (; p < (int64_t)cut; p++) {
+    const int64_t k0 = kex[b + p] - base;
+    if (k0 >= t1) break;
+    const uint32_t L = klen[b + p];
+    if (L == 0) continue;
+    // the part of this document inside [t0, t1), as in-document offsets
+    const int64_t s0 = max(t0, k0) - k0, s1 = min(t1, k0 + (int64_t)L) - k0;
+    if (s1 <= s0) continue;
+    const int64_t o0 = __ldg(offs + order[b + p]) + s0;
+    const int64_t a0 = o0 & ~(int64_t)3;
+    const uint32_t end = (uint32_t)(s1 - s0) + (uint32_t)(o0 - a0);
+    const int4 *s4 = reinterpret_cast<const int4 *>(src + a0);
+    int4 *d4 = reinterpret_cast<int4 *>(dst + a0);
+    for (uint32_t r = 4 * (uint32_t)lane; r < end; r += 512) {
+      int4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++)
-      if (r + 128 * u < end) v[u] = __ldcs(s4 + ((r + 128 * u) >> 2));
+      for (int u = 0; u < 4; u++)
+        if (r + 128 * u < end) v[u] = __ldcs(s4 + ((r + 128 * u) >> 2));
 #pragma unroll
-    for (int u = 0; u < 4; u++)
-      if (r + 128 * u < end) d4[(r + 128 * u) >> 2] = v[u];
+      for (int u = 0; u < 4; u++)
+        if (r + 128 * u < end) d4[(r + 128 * u) >> 2] = v[u];
+    }
   }
-  if (lane == 0) atomicAdd(tokens_read, (unsigned long long)L);
+  if (lane == 0) atomicAdd(tokens_read, (unsigned long long)(t1 - t0));
 }
 
 // ---------------------------------------------------------------------------
@@ -798,7 +820,8 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
                               const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
                               const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
-                              uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces) {
+                              uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces,
+                              int64_t *__restrict__ ptokens) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
@@ -819,6 +842,7 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
   }
   cutoff[j] = (uint32_t)c;
   npieces[j] = pex[b + c] - pex[b];
+  ptokens[j] = kex[b + c] - base;
 }
 
 // node_base[j] = sum over j' < j of (pieces of j' + 1 terminal node).
@@ -1274,17 +1298,19 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
 
 cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
                                const uint32_t *cutoff, const uint16_t *stream_bp,
-                               const uint32_t *order, const uint32_t *klen, const int64_t *offs,
-                               const int32_t *src, int32_t *dst, unsigned long long *tokens_read,
-                               cudaStream_t st) {
+                               const uint32_t *order, const uint32_t *klen, const int64_t *kex,
+                               const int64_t *offs, const int32_t *src, int32_t *dst,
+                               unsigned long long *tokens_read, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
   copy_prefix_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, stream_bp, order, klen,
-                                                      offs, src, dst, tokens_read);
+                                                      kex, offs, src, dst, tokens_read);
   return cudaGetLastError();
 }
 
 uint32_t order_positions_per_thread() { return kOrderPerThread; }
+
+uint32_t copy_chunk_tokens() { return kCopyChunk; }
 
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
@@ -1326,10 +1352,10 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          uint32_t *cutoff, int64_t *npieces, cudaStream_t st) {
+                          uint32_t *cutoff, int64_t *npieces, int64_t *ptokens, cudaStream_t st) {
   ++launch_counter();
   cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G, cutoff,
-                                                    npieces);
+                                                    npieces, ptokens);
   return cudaGetLastError();
 }
 

@@ -68,23 +68,25 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
                                uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st);
-// Documents of positions [0, cutoff[j]) of every stream with stream_bp[j] ==
-// 0, copied from src (host memory the device can address) to dst; the grid
-// has a block per 8 positions of those prefixes.
+// The kept tokens of positions [0, cutoff[j]) of every stream with
+// stream_bp[j] == 0, copied from src (host memory the device can address) to
+// dst; the grid has a block per 8 chunks of copy_chunk_tokens() kept tokens
+// of those prefixes.
 cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
                                const uint32_t *cutoff, const uint16_t *stream_bp,
-                               const uint32_t *order, const uint32_t *klen, const int64_t *offs,
-                               const int32_t *src, int32_t *dst, unsigned long long *tokens_read,
-                               cudaStream_t st);
+                               const uint32_t *order, const uint32_t *klen, const int64_t *kex,
+                               const int64_t *offs, const int32_t *src, int32_t *dst,
+                               unsigned long long *tokens_read, cudaStream_t st);
+uint32_t copy_chunk_tokens();
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
                                cudaStream_t st);
 size_t scan_scratch_bytes(uint64_t n);
-// per stream: cutoff c_j, pieces before it, node base; rmax given
+// per stream: cutoff c_j, pieces and kept tokens before it; rmax given
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          uint32_t *cutoff, int64_t *npieces, cudaStream_t st);
+                          uint32_t *cutoff, int64_t *npieces, int64_t *ptokens, cudaStream_t st);
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st);
 

@@ -478,6 +478,29 @@ def test_host_corpus(name, pinned, kw):
     assert ref.info["host_bytes"] == 0
 
 
+def test_host_corpus_unaligned_page_locked_tokens_are_copied_whole():
+    # page-locked tokens that do not start on a 16-byte boundary cannot be
+    # read in place with 16-byte loads: the library copies them whole
+    import torch
+    from deterministic_packed_assembly_gb300 import Packer
+    c = make_preset("c3s")
+    buf = torch.empty(c.n_tokens + 1, dtype=torch.int32).pin_memory()
+    buf[1:] = torch.from_numpy(c.tokens)
+    t = buf[1:]
+    assert t.data_ptr() % 16 != 0
+    off = torch.from_numpy(c.doc_offsets).pin_memory()
+    _poison_cache()
+    pk = Packer(t, off, None, device="cuda:0", stream_doc_begin=c.stream_doc_begin,
+                stream_source=c.stream_source, source_weight=c.source_weight,
+                stream_weight=c.stream_weight, source_heldout_bp=c.source_heldout_bp, T=c.T,
+                B=c.B, max_steps=c.max_steps, seed=c.seed, hash_key=c.hash_key)
+    o = oracle_for(c)
+    assert pk.info["host_bytes"] == _corpus_bytes(c)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, [0, 1, o.valid_steps - 1])
+    pk.check()
+
+
 @pytest.mark.parametrize("name", ["c3m", "c4s"])
 def test_host_corpus_reads_only_the_reachable_prefix(name):
     # a horizon of two updates reaches a small part of the corpus: only its
