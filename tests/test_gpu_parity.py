@@ -628,7 +628,12 @@ def test_every_option_together_random_tiny_corpora(case):
         kw["schedule"] = _schedule_for(c, rng, int(rng.integers(2, min(4, c.max_steps) + 1)),
                                        c.max_steps)
     o = oracle_for(c, **kw)
-    pk = packer_for(c, **kw)
+    # every third case hands the corpus over in page-locked host memory
+    if case % 3 == 2:
+        _poison_cache(64 << 20)
+        pk = _host_packer(c, True, **kw)
+    else:
+        pk = packer_for(c, **kw)
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=int(rng.integers(1, 4)))
     pk.check()
