@@ -90,7 +90,7 @@ class ns_pack_info_t(C.Structure):
         ("n_pieces", C.c_uint64),
         ("table_bytes", C.c_uint64),
         ("init_launches", C.c_uint32),
-        ("reserved", C.c_uint32),
+        ("init_passes", C.c_uint32),
         ("host_bytes", C.c_uint64),
     ]
 

@@ -36,6 +36,8 @@ struct ns_pack_ctx {
   uint32_t valid_steps = 0, levels = 0, init_launches = 0;
   uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
   uint64_t host_bytes = 0;  // bytes of a host-resident corpus read at init
+  bool speculate = true;    // hash to a bound speculated from the measured fill
+  uint32_t init_passes = 1;
   // device tables kept for the per-update calls
   int32_t *rb = nullptr, *cum = nullptr, *quota = nullptr;
   uint32_t *W = nullptr;
@@ -325,6 +327,9 @@ int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st
   return NS_OK;
 }
 
+// build() asks to be run again with the full hash bound (internal, > 0).
+constexpr int kRetryFullBound = 1;
+
 int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   const uint32_t J = c->J, S = c->S, K = c->K, T = c->T;
   cudaStream_t st = c->stream;
@@ -542,6 +547,21 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(tokens_read, 0, sizeof(unsigned long long), st));
   }
   const bool group_copy = host_corpus && !htok;
+  // Greedy windows hold at most T tokens, so a prefix whose kept tokens
+  // exceed (windows needed) * T holds them all, whatever the packing: the
+  // full bound.  Greedy packing fills about four fifths of a window, so the
+  // hash goes in two rounds instead: to half the bound, then -- once every
+  // stream's fill has been measured on a sample of its decided documents --
+  // to that fill plus a margin.  The packing then shows whether each prefix
+  // holds the windows it must; if one does not, the context is built again
+  // with the full bound.  Wrap packing fills every window: full bound.
+  const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
+  const bool speculate = c->speculate && any_heldout && !wrap;
+  uint16_t *need_num = nullptr;  // per stream, of 1024 (NULL: the full bound)
+  if (speculate) {
+    need_num = a.temp<uint16_t>(J);
+    NS_ALLOC(need_num);
+  }
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *kept = a.temp<unsigned long long>(J);
@@ -549,17 +569,33 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(kept);
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
+    const uint32_t first_num = speculate ? 512u : 1024u;
+    const int32_t *src = htok ? htok : c->tokens;
+    int32_t *dst = htok ? c->tokens_rw : nullptr;
     // one launch over every stream, or one per copied group of streams
     const size_t n_groups = group_copy ? copy.done.size() : 1;
     for (size_t gi = 0; gi < n_groups; gi++) {
       const uint32_t j0 = group_copy ? copy.j_first[gi] : 0;
       const uint32_t j1 = group_copy ? copy.j_first[gi + 1] : J;
       if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done[gi], 0));
-      NS_CK(nsk::launch_hash_prefix(htok ? htok : c->tokens, htok ? c->tokens_rw : nullptr,
-                                    tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
+      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                    heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0,
+                                    heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0, nullptr,
+                                    first_num, c->n_sms, st));
+    }
+    if (speculate) {
+      // the fill needs the quota table; the second round every token
+      if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
+      NS_CK(cudaStreamWaitEvent(st, side.join, 0));
+      NS_CK(nsk::launch_fill_need(static_cast<uint32_t *>(d_sdb), J, D0,
+                                  static_cast<uint16_t *>(d_stream_bp), order, klen, c->offs,
+                                  c->n_tokens, c->cum + (size_t)K * J, T, c->G, first_num,
+                                  need_num, st));
+      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
+                                    static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
+                                    c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
+                                    heldout_mode ? 1u : 0u, frontier, kept, 0, J, need_num, 0,
                                     c->n_sms, st));
     }
   }
@@ -568,7 +604,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)
-  const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
   const uint32_t chunk = wrap ? 0x80000000u : T;
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes, st));
 
@@ -582,16 +617,20 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(ptokens);
   NS_ALLOC(node_base);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
-                           T, c->G, cutoff, npieces, ptokens, st));
+                           T, c->G, need_num, cutoff, npieces, ptokens, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
   std::vector<uint32_t> cut_h(J);
   std::vector<int64_t> np_h(J), nb_h(J + 1), pt_h(J);
+  std::vector<uint16_t> num_h(J, 1024);
   std::vector<int32_t> rmax32(J);
   int err_host = 0;
   NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(nb_h.data(), node_base, (J + 1) * 8, cudaMemcpyDeviceToHost, st));
   if (htok) NS_CK(cudaMemcpyAsync(pt_h.data(), ptokens, J * 8, cudaMemcpyDeviceToHost, st));
+  if (need_num)
+    NS_CK(cudaMemcpyAsync(num_h.data(), need_num, J * sizeof(uint16_t), cudaMemcpyDeviceToHost,
+                          st));
   NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
                         cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -803,6 +842,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
   if (err_host != 0) return NS_ERR_DEVICE;
+  // a stream cut short at a speculated bound must hold one window past the
+  // ones the horizon reads (so that those are closed): else, the full bound
+  for (uint32_t j = 0; j < J; j++)
+    if (num_h[j] < 1024 && cut_h[j] < N[j] && (uint64_t)W_h[j] < rmax[j] + 1) return kRetryFullBound;
   c->windows.assign(W_h.begin(), W_h.end());
   c->valid_steps = valid_h;
   c->digest = digest_h;
@@ -819,8 +862,12 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   *out = nullptr;
   int rc = check_config(cfg);
   if (rc) return rc;
+  const uint64_t launches0 = nsk::launch_counter();
+  for (uint32_t pass = 1;; pass++) {
   ns_pack_ctx *c = new (std::nothrow) ns_pack_ctx();
   if (!c) return NS_ERR_OOM;
+  c->speculate = (pass == 1);
+  c->init_passes = pass;
   c->T = cfg->T;
   c->B = cfg->B;
   c->K = cfg->max_steps;
@@ -842,7 +889,6 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   c->free_fn = cfg->free;
   c->user = cfg->alloc_user;
   Arena a(c);
-  const uint64_t launches0 = nsk::launch_counter();
   rc = build(c, cfg, a);
   c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
   if (rc != NS_OK) {
@@ -850,11 +896,13 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
     cudaGetLastError();
     a.release();
     release_ctx(c);
-    return rc;
+    if (rc == kRetryFullBound && pass == 1) continue;
+    return rc == kRetryFullBound ? NS_ERR_DEVICE : rc;
   }
   a.release();
   *out = c;
   return NS_OK;
+  }
 }
 
 int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,
@@ -953,7 +1001,7 @@ int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
   info->n_pieces = ctx->n_pieces;
   info->table_bytes = ctx->table_bytes;
   info->init_launches = ctx->init_launches;
-  info->reserved = 0;
+  info->init_passes = ctx->init_passes;
   info->host_bytes = ctx->host_bytes;
   return NS_OK;
 }

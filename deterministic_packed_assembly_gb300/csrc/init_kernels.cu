@@ -69,6 +69,14 @@ __device__ __forceinline__ int64_t windows_needed(int32_t rmax, uint32_t G) {
   return G ? ((int64_t)rmax + G - 1) / G * G : (int64_t)rmax;
 }
 
+// Kept tokens a stream's prefix must exceed: num / 1024 of its windows times
+// T (num 1024: the bound that holds for any packing; smaller: a bound
+// speculated from the stream's measured fill, checked after packing).
+__device__ __forceinline__ int64_t tokens_needed(int32_t rmax, uint32_t G, uint32_t T,
+                                                 uint32_t num) {
+  return (windows_needed(rmax, G) * (int64_t)T * (int64_t)num) >> 10;
+}
+
 // ---------------------------------------------------------------------------
 // doc_offsets must start at >= 0, never decrease, keep every length below
 // 2^31 and end inside the token array.
@@ -413,7 +421,8 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
-                       unsigned long long *kept, uint32_t j_begin, uint32_t j_count) {
+                       unsigned long long *kept, uint32_t j_begin, uint32_t j_count,
+                       const uint16_t *__restrict__ need_num, uint32_t need_num_all) {
   constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -437,8 +446,9 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
             ready_seen = true;
           }
           if (ready_seen)
-            need = (unsigned long long)windows_needed(
-                       *reinterpret_cast<const volatile int32_t *>(cum_last + j), G) * T;
+            need = (unsigned long long)tokens_needed(
+                *reinterpret_cast<const volatile int32_t *>(cum_last + j), G, T,
+                need_num ? need_num[j] : need_num_all);
         }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
         base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
@@ -480,6 +490,110 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         if (lane == 0 && read_here) atomicAdd(tokens_read, read_here);
       }
     }
+  }
+}
+
+// The fraction of its bound a stream's prefix is hashed to in the second
+// round, from its measured packing fill.  A block per stream: the sample is
+// the longest run of the stream's first 2048 positions whose raw tokens stay
+// within the first round's need (so it depends only on lengths, and every
+// document in it is decided); up to 32 lanes each pack 64 of its positions
+// greedily from an empty window (T-chunks, kept lengths) and count their
+// closed windows and tokens.  With W windows closed, fill = tokens / (W T)
+// and need_num = 1024 * min(1, fill + 0.03 + 0.4 / sqrt(min(W, windows
+// needed))); 1024 (no speculation) for a stream that needs fewer than 256
+// windows or whose sample closes fewer than 256.  Only the amount hashed
+// depends on it: a prefix that then holds fewer windows than needed is
+// caught after packing and the context is built again with the full bound.
+constexpr uint32_t kFillSample = 2048;
+constexpr uint32_t kFillRun = 64;
+
+__device__ __forceinline__ uint32_t raw_length(const int64_t *__restrict__ offs, uint32_t d,
+                                               uint64_t n_tokens) {
+  const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
+  const bool ok = o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
+  return ok ? (uint32_t)(o1 - o0) : 0u;
+}
+
+__global__ void __launch_bounds__(256)
+    fill_need_kernel(const uint32_t *__restrict__ sdb, uint32_t D0,
+                     const uint16_t *__restrict__ stream_bp, const uint32_t *__restrict__ order,
+                     const uint32_t *__restrict__ klen, const int64_t *__restrict__ offs,
+                     uint64_t n_tokens, const int32_t *__restrict__ cum_last, uint32_t T,
+                     uint32_t G, uint32_t first_num, uint16_t *__restrict__ need_num) {
+  // a block per stream: the sample's raw and kept lengths are staged in
+  // shared memory by all its threads at once, then one warp decides
+  __shared__ uint32_t raw_s[kFillSample], kept_s[kFillSample];
+  const uint32_t j = blockIdx.x;
+  const int64_t wn = windows_needed(cum_last[j], G);
+  if (stream_bp[j] == 0 || wn < 256) {
+    if (threadIdx.x == 0) need_num[j] = 1024;
+    return;
+  }
+  const uint64_t b = (uint64_t)sdb[j] - D0, N = sdb[j + 1] - sdb[j];
+  const uint32_t lim = (uint32_t)(N < kFillSample ? N : kFillSample);
+  for (uint32_t p = threadIdx.x; p < lim; p += blockDim.x) {
+    raw_s[p] = raw_length(offs, order[b + p], n_tokens);
+    kept_s[p] = klen[b + p];
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int64_t need1 = tokens_needed(cum_last[j], G, T, first_num);
+  // S: positions [0, S) whose raw tokens add up to at most need1
+  uint32_t S = 0;
+  int64_t acc = 0;
+  for (uint32_t c0 = 0; c0 < lim; c0 += 32) {
+    const uint32_t p = c0 + lane;
+    int64_t incl = (p < lim) ? raw_s[p] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    incl += acc;
+    const unsigned ok = __ballot_sync(0xffffffffu, p < lim && incl <= need1);
+    const uint32_t cnt = __popc(ok);  // the raw sums only grow: ok is a prefix
+    S = c0 + cnt;
+    if (cnt < 32) break;
+    acc = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  // greedy packing of runs of 64 positions of [0, S), one run per lane
+  const uint32_t runs = (S / kFillRun < 32u) ? S / kFillRun : 32u;
+  uint64_t w = 0, tok = 0;
+  if ((uint32_t)lane < runs) {
+    uint64_t used = 0;
+    for (uint32_t p = lane * kFillRun; p < (lane + 1) * kFillRun; p++) {
+      const uint64_t L = kept_s[p];
+      if (L == 0) continue;
+      const uint64_t n = L / T, t = L % T;
+      if (n > 0) {
+        // a full chunk closes an open window, fills one of its own, and the
+        // next chunk or tail closes that one
+        w += (used > 0 ? 1 : 0) + (n - 1) + (t > 0 ? 1 : 0);
+        tok += used + (uint64_t)T * (n - 1) + (t > 0 ? (uint64_t)T : 0);
+        used = (t > 0) ? t : T;
+      } else {
+        if (used + L > T) {
+          w++;
+          tok += used;
+          used = 0;
+        }
+        used += L;
+      }
+    }
+  }
+  w = warp_sum_u64(w);
+  tok = warp_sum_u64(tok);
+  if (lane == 0) {
+    uint32_t num = 1024;
+    if (w >= 256) {
+      const double fill = (double)tok / ((double)w * (double)T);
+      const double wmin = ((int64_t)w < wn) ? (double)w : (double)wn;
+      const double f = fill + 0.03 + 0.4 / sqrt(wmin);
+      num = (uint32_t)min(1024.0, ceil(f * 1024.0));
+    }
+    need_num[j] = (uint16_t)num;
   }
 }
 
@@ -820,6 +934,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
                               const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
                               const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
+                              const uint16_t *__restrict__ need_num,
                               uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces,
                               int64_t *__restrict__ ptokens) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -827,7 +942,7 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
   const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
   const uint64_t N = e - b;
   const int64_t base = kex[b];
-  const int64_t need = windows_needed(cum_last[j], G) * (int64_t)T;
+  const int64_t need = tokens_needed(cum_last[j], G, T, need_num ? need_num[j] : 1024u);
   uint64_t c = N;
   if (kex[e] - base > need) {
     uint64_t lo = 1, hi = N;
@@ -1282,17 +1397,20 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
-                               uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st) {
+                               uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
+                               uint32_t need_num_all, int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
   ++launch_counter();
   if (copy_dst)
     hash_prefix_kernel<true><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
         tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
-        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count);
+        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
+        need_num_all);
   else
     hash_prefix_kernel<false><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
         tokens, nullptr, nullptr, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
-        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count);
+        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
+        need_num_all);
   return cudaGetLastError();
 }
 
@@ -1311,6 +1429,18 @@ cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
 uint32_t order_positions_per_thread() { return kOrderPerThread; }
 
 uint32_t copy_chunk_tokens() { return kCopyChunk; }
+
+cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
+                             const uint16_t *stream_bp, const uint32_t *order, const uint32_t *klen,
+                             const int64_t *offs, uint64_t n_tokens, const int32_t *cum_last,
+                             uint32_t T, uint32_t G, uint32_t first_num, uint16_t *need_num,
+                             cudaStream_t st) {
+  if (J == 0) return cudaSuccess;
+  ++launch_counter();
+  fill_need_kernel<<<J, 256, 0, st>>>(sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
+                                      T, G, first_num, need_num);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
@@ -1352,10 +1482,11 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          uint32_t *cutoff, int64_t *npieces, int64_t *ptokens, cudaStream_t st) {
+                          const uint16_t *need_num, uint32_t *cutoff, int64_t *npieces,
+                          int64_t *ptokens, cudaStream_t st) {
   ++launch_counter();
-  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G, cutoff,
-                                                    npieces, ptokens);
+  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G,
+                                                    need_num, cutoff, npieces, ptokens);
   return cudaGetLastError();
 }
 

@@ -67,7 +67,16 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
-                               uint32_t j_begin, uint32_t j_count, int n_sms, cudaStream_t st);
+                               uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
+                               uint32_t need_num_all, int n_sms, cudaStream_t st);
+// need_num: the fraction (of 1024) of each stream's bound the second hash
+// round stops at, from its measured packing fill (first_num: the first
+// round's)
+cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
+                             const uint16_t *stream_bp, const uint32_t *order, const uint32_t *klen,
+                             const int64_t *offs, uint64_t n_tokens, const int32_t *cum_last,
+                             uint32_t T, uint32_t G, uint32_t first_num, uint16_t *need_num,
+                             cudaStream_t st);
 // The kept tokens of positions [0, cutoff[j]) of every stream with
 // stream_bp[j] == 0, copied from src (host memory the device can address) to
 // dst; the grid has a block per 8 chunks of copy_chunk_tokens() kept tokens
@@ -86,7 +95,8 @@ size_t scan_scratch_bytes(uint64_t n);
 // per stream: cutoff c_j, pieces and kept tokens before it; rmax given
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          uint32_t *cutoff, int64_t *npieces, int64_t *ptokens, cudaStream_t st);
+                          const uint16_t *need_num, uint32_t *cutoff, int64_t *npieces,
+                          int64_t *ptokens, cudaStream_t st);
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st);
 

@@ -199,7 +199,10 @@ typedef struct {
                            documents under wrap packing */
   uint64_t table_bytes; /* device bytes the context keeps */
   uint32_t init_launches; /* kernels ns_pack_init launched */
-  uint32_t reserved;
+  uint32_t init_passes;   /* 1; 2 when the held-out hash's speculated bound left
+                             a stream short of the windows the horizon reads
+                             and the context was built again with the full
+                             bound (the same tables either way) */
   uint64_t host_bytes;  /* bytes of a host-resident corpus (NS_PACK_HOST_CORPUS)
                            that ns_pack_init read from host memory: offsets,
                            loss starts and the tokens it used (the whole

@@ -78,6 +78,8 @@ def test_full_size_sampled_updates(name):
 
 def test_full_size_mixture_within_two_windows():
     c, pk, o = _setup("c3")
+    # the held-out hash's speculated bound held for every stream
+    assert pk.info["init_passes"] == 1
     q, _ = pk.quota_table()
     ss = c.stream_source.astype(np.int64)
     src = np.zeros((q.shape[0], c.n_sources), np.int64)

@@ -185,6 +185,26 @@ def test_largest_window_length(wrap):
     pk.close()
 
 
+def test_speculated_hash_bound_falls_short_and_init_runs_again():
+    # the held-out hash stops at a bound speculated from the packing fill it
+    # measures on a stream's first shuffled positions.  Here those hold
+    # documents that fill a window poorly (33 of 64 tokens) and the later
+    # ones documents that fill it fully (4 tokens): the measured fill (0.52)
+    # leaves the stream short of the 4096 windows the horizon reads, and the
+    # context is built again with the full bound -- same tables, same rows
+    T, n_long, n_short, seed = 64, 2048, 40000, 3
+    N = n_long + n_short
+    lengths = np.zeros(N, np.int64)
+    for p in range(N):
+        lengths[oracle.feistel_pi(seed, 0, N, p)] = 33 if p < n_long else 4
+    c = corpus_from_lengths(lengths, T=T, B=64, max_steps=64, heldout_bp=[1], seed=seed)
+    pk, o = packer_for(c), oracle_for(c)
+    assert pk.info["init_passes"] == 2
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=8)
+    pk.check()
+
+
 def test_horizon_and_row_range_errors():
     c = make_preset("c1")
     pk = packer_for(c)
