@@ -153,18 +153,32 @@ REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons; the
+    samples taken between mark() and stop() describe the timed region (if it
+    was too short to hold one, the last sample before it stands in, flagged
+    ``nearest_before``)."""
 
     def __init__(self, gpu_id: str):
         self.f = tempfile.NamedTemporaryFile("w+", delete=False, suffix=".csv")
+        self.offset = 0
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              + ",".join("clocks_event_reasons." + r for r in REASONS))
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
+            return
+        # sampling is live before the timed region starts
+        t_end = time.time() + 5.0
+        while time.time() < t_end and os.path.getsize(self.f.name) == 0:
+            time.sleep(0.01)
+
+    def mark(self) -> None:
+        """The timed region starts: later samples are the region's."""
+        if self.p is not None:
+            self.offset = os.path.getsize(self.f.name)
 
     def stop(self) -> dict | None:
         if self.p is None:
@@ -176,8 +190,14 @@ class ClockSampler:
             self.p.kill()
         self.f.flush()
         self.f.seek(0)
-        rows = [ln.strip().split(", ") for ln in self.f.read().splitlines() if ln.strip()]
+        text = self.f.read()
         os.unlink(self.f.name)
+        before, inside = text[:self.offset], text[self.offset:]
+        rows = [ln.strip().split(", ") for ln in inside.splitlines() if ln.strip()]
+        nearest = False
+        if not rows:
+            prev = [ln.strip().split(", ") for ln in before.splitlines() if ln.strip()]
+            rows, nearest = prev[-1:], True
         sm, mx, seen = [], [], set()
         for r in rows:
             if len(r) < 4 + len(REASONS):
@@ -192,8 +212,11 @@ class ClockSampler:
                     seen.add(name)
         if not sm:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(seen),
-                "samples": len(sm)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(seen),
+               "samples": len(sm)}
+        if nearest:
+            out["nearest_before"] = True
+        return out
 
 
 def gpu_id_for(device) -> str:
@@ -445,6 +468,8 @@ def run_ours(args, dist: Dist) -> None:
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        if sampler:
+            sampler.mark()
         t0.record(stream)
         for _ in range(K):
             one_pass(True)
