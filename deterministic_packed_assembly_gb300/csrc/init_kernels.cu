@@ -74,7 +74,10 @@ __device__ __forceinline__ int64_t windows_needed(int32_t rmax, uint32_t G) {
 // speculated from the stream's measured fill, checked after packing).
 __device__ __forceinline__ int64_t tokens_needed(int32_t rmax, uint32_t G, uint32_t T,
                                                  uint32_t num) {
-  return (windows_needed(rmax, G) * (int64_t)T * (int64_t)num) >> 10;
+  // windows < 2^31 and T <= 2^24, so wt < 2^55: floor(wt * num / 1024) taken
+  // in two parts so that no product leaves 64 bits
+  const uint64_t wt = (uint64_t)windows_needed(rmax, G) * T;
+  return (int64_t)((wt >> 10) * num + (((wt & 1023u) * num) >> 10));
 }
 
 // ---------------------------------------------------------------------------
