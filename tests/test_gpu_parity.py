@@ -185,6 +185,60 @@ def test_largest_window_length(wrap):
     pk.close()
 
 
+def _medium_case(rng):
+    """A mixture whose streams need hundreds to thousands of windows (the
+    held-out hash speculates its bound for those past 256), documents
+    log-normal around a random fraction of T (window fills from about 0.6 to
+    nearly 1), some documents longer than T."""
+    T = int(rng.choice([128, 256, 512]))
+    J = int(rng.integers(2, 7))
+    S = int(rng.integers(1, J + 1))
+    stream_source = sorted(list(range(S)) + [int(x) for x in rng.integers(0, S, size=J - S)])
+    B = int(rng.integers(24, 65))
+    K = int(rng.integers(40, 121))
+    med = T * float(rng.choice([0.05, 0.15, 0.3, 0.5, 0.9]))
+    sigma = float(rng.uniform(0.4, 1.4))
+    # documents per stream: enough for its share of K * B windows, with room
+    sw = [int(x) for x in rng.integers(1, 9, size=S)]
+    tw = [int(x) for x in rng.integers(1, 9, size=J)]
+    mean_len = med * np.exp(sigma * sigma / 2)
+    stream_docs = []
+    for j in range(J):
+        s = stream_source[j]
+        share = sw[s] / sum(sw) * tw[j] / sum(tw[q] for q in range(J) if stream_source[q] == s)
+        need = K * B * share * T / mean_len
+        stream_docs.append(int(need * float(rng.uniform(1.3, 2.5))) + 50)
+    n = sum(stream_docs)
+    lengths = np.clip(np.rint(med * np.exp(sigma * rng.standard_normal(n))), 1, 4 * T).astype(int)
+    bp = [int(rng.choice([50, 100, 500, 2000])) for _ in range(S)]
+    loss_start = None
+    if rng.random() < 0.3:
+        loss_start = [int(rng.integers(0, L + 1)) for L in lengths]
+    return corpus_from_lengths(
+        lengths, T=T, B=B, max_steps=K, stream_docs=stream_docs, stream_source=stream_source,
+        source_weight=sw, stream_weight=tw, heldout_bp=bp, loss_start=loss_start,
+        seed=int(rng.integers(0, 2**63)), hash_key=int(rng.integers(0, 2**63)),
+        drain=bool(rng.integers(0, 2)), tokens=rng.integers(0, 50000, size=int(lengths.sum())),
+        pad_id=0)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_speculated_hash_bound_random_medium_corpora(case):
+    # every update of mixtures large enough for the held-out hash to stop
+    # at its speculated bound: tables and rows exactly the oracle's, whether
+    # the bound held (one init pass) or a stream fell short (two)
+    rng = np.random.default_rng(7000 + case)
+    c = _medium_case(rng)
+    kw = {}
+    if rng.random() < 0.3:
+        kw = dict(window_segment=int(rng.choice([4, 16])), shuffle_rows=True)
+    pk, o = packer_for(c, **kw), oracle_for(c, **kw)
+    assert pk.info["init_passes"] in (1, 2)
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=int(rng.integers(4, 17)))
+    pk.check()
+
+
 def test_speculated_hash_bound_falls_short_and_init_runs_again():
     # the held-out hash stops at a bound speculated from the packing fill it
     # measures on a stream's first shuffled positions.  Here those hold
