@@ -853,21 +853,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   return NS_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
-  if (!out) return NS_ERR_INVALID_ARG;
-  *out = nullptr;
-  int rc = check_config(cfg);
-  if (rc) return rc;
-  const uint64_t launches0 = nsk::launch_counter();
-  for (uint32_t pass = 1;; pass++) {
+// A context with the recipe's scalars and no tables yet.
+ns_pack_ctx *new_context(const ns_pack_config *cfg) {
   ns_pack_ctx *c = new (std::nothrow) ns_pack_ctx();
-  if (!c) return NS_ERR_OOM;
-  c->speculate = (pass == 1);
-  c->init_passes = pass;
+  if (!c) return nullptr;
   c->T = cfg->T;
   c->B = cfg->B;
   c->K = cfg->max_steps;
@@ -888,21 +877,41 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   c->alloc = cfg->alloc;
   c->free_fn = cfg->free;
   c->user = cfg->alloc_user;
-  Arena a(c);
-  rc = build(c, cfg, a);
-  c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
-  if (rc != NS_OK) {
+  return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
+  if (!out) return NS_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  const uint64_t launches0 = nsk::launch_counter();
+  // pass 1 hashes to a speculated bound; pass 2, only if that left a stream
+  // short of its windows, to the full bound
+  for (uint32_t pass = 1; pass <= 2; pass++) {
+    ns_pack_ctx *c = new_context(cfg);
+    if (!c) return NS_ERR_OOM;
+    c->speculate = (pass == 1);
+    c->init_passes = pass;
+    Arena a(c);
+    rc = build(c, cfg, a);
+    c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
+    if (rc == NS_OK) {
+      a.release();
+      *out = c;
+      return NS_OK;
+    }
     cudaStreamSynchronize(c->stream);
     cudaGetLastError();
     a.release();
     release_ctx(c);
-    if (rc == kRetryFullBound && pass == 1) continue;
-    return rc == kRetryFullBound ? NS_ERR_DEVICE : rc;
+    if (rc != kRetryFullBound) return rc;
   }
-  a.release();
-  *out = c;
-  return NS_OK;
-  }
+  return NS_ERR_DEVICE;  // the full bound cannot fall short
 }
 
 int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t row_begin,

@@ -407,12 +407,15 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // from the stream's frontier; a document the stream does not keep (held out
 // for training, not held out for validation) has its kept length set to 0.
 // A warp leaves a stream once the kept tokens of the documents already hashed
-// exceed need_j = rmax_j * T (the windows the horizon asks of it hold at most
-// that many), or when the stream runs out, and goes on to the next stream.
-// Every position below the final frontier is hashed, and the kept tokens
-// below it exceed need_j unless the whole stream was hashed, so the prefix
-// the cutoff kernel then takes only ever holds decided documents.
-// Warps start on different streams so that few overshoot any one stream.
+// exceed need_j = num_j / 1024 of rmax_j * T (rmax_j * T: the windows the
+// horizon asks of it hold at most that many; num_j from need_num, or
+// need_num_all for every stream), or when the stream runs out, and goes on
+// to the next stream.  A second launch with a larger num_j carries on from
+// the first's frontier.  Every position below the final frontier is hashed,
+// and the kept tokens below it exceed need_j unless the whole stream was
+// hashed, so the prefix the cutoff kernel then takes (with the same num_j)
+// only ever holds decided documents.  Warps start on different streams so
+// that few overshoot any one stream.
 // With kCopy the tokens are read from host memory the device can address
 // and every hashed document is written to copy_dst; tokens_read counts them.
 template <bool kCopy>
