@@ -842,6 +842,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
   if (err_host != 0) return NS_ERR_DEVICE;
+  c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
   // a stream cut short at a speculated bound must hold one window past the
   // ones the horizon reads (so that those are closed): else, the full bound
   for (uint32_t j = 0; j < J; j++)
@@ -849,7 +850,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->windows.assign(W_h.begin(), W_h.end());
   c->valid_steps = valid_h;
   c->digest = digest_h;
-  c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
   return NS_OK;
 }
 
@@ -890,6 +890,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   int rc = check_config(cfg);
   if (rc) return rc;
   const uint64_t launches0 = nsk::launch_counter();
+  uint64_t host_bytes_before = 0;  // a host corpus read by an earlier pass
   // pass 1 hashes to a speculated bound; pass 2, only if that left a stream
   // short of its windows, to the full bound
   for (uint32_t pass = 1; pass <= 2; pass++) {
@@ -900,11 +901,13 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
     Arena a(c);
     rc = build(c, cfg, a);
     c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
+    c->host_bytes += host_bytes_before;
     if (rc == NS_OK) {
       a.release();
       *out = c;
       return NS_OK;
     }
+    host_bytes_before = c->host_bytes;
     cudaStreamSynchronize(c->stream);
     cudaGetLastError();
     a.release();

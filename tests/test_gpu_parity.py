@@ -257,6 +257,16 @@ def test_speculated_hash_bound_falls_short_and_init_runs_again():
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=8)
     pk.check()
+    # the same from page-locked host memory: both passes read it in place,
+    # and both count in host_bytes
+    _poison_cache()
+    hp = _host_packer(c, True)
+    assert hp.info["init_passes"] == 2
+    assert hp.order_digest == pk.order_digest
+    meta = (c.n_docs + 1) * 8
+    assert hp.info["host_bytes"] - meta > c.n_tokens * 4 // 2
+    compare_steps(hp, o, range(o.valid_steps), launch=8)
+    hp.check()
 
 
 def test_horizon_and_row_range_errors():
