@@ -1,11 +1,14 @@
 // The C ABI (include/nspack.h): host-side checks, table allocation through
 // the caller's allocator, and the order of kernel launches that builds a
 // context and assembles updates.  No packing arithmetic runs on the host: the
-// host only validates arguments, sizes tables and reads back the few scalars
-// it needs to size the next ones.
+// host only validates arguments, sizes tables, reads back the few scalars it
+// needs to size the next ones, and estimates from the weights where the held-
+// out hash's first round may stop before the quotas are known (a scheduling
+// hint that no result depends on).
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <utility>
@@ -558,9 +561,38 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
   const bool speculate = c->speculate && any_heldout && !wrap;
   uint16_t *need_num = nullptr;  // per stream, of 1024 (NULL: the full bound)
+  unsigned long long *pre_cap = nullptr;
   if (speculate) {
     need_num = a.temp<uint16_t>(J);
     NS_ALLOC(need_num);
+    // Until the quota kernel publishes each stream's need, the first round
+    // stops a stream at an estimate of it from the recipe (its share of the
+    // horizon's rows, a few windows over), not at no bound at all: a small
+    // stream is then not hashed far past its need while the quotas run.  A
+    // heuristic only: the second round hashes every stream to its exact
+    // bound whatever the first one did.
+    std::vector<double> est(J, 0.0);
+    for (uint32_t p = 0; p < P; p++) {
+      const uint32_t kb = c->piece_begin[p];
+      const uint32_t ke = (p + 1 < P) ? c->piece_begin[p + 1] : K;
+      double swsum = 0.0;
+      for (uint32_t s2 = 0; s2 < S; s2++) swsum += psw[(size_t)p * S + s2];
+      for (uint32_t s2 = 0; s2 < S; s2++) {
+        double twsum = 0.0;
+        for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++) twsum += ptw[(size_t)p * J + j];
+        for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++)
+          est[j] += (double)(ke - kb) * c->piece_B[p] * (psw[(size_t)p * S + s2] / swsum) *
+                    (ptw[(size_t)p * J + j] / twsum);
+      }
+    }
+    std::vector<unsigned long long> cap(J);
+    for (uint32_t j = 0; j < J; j++) {
+      double w = std::ceil(est[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
+      cap[j] = (unsigned long long)(0.5 * w * (double)T);
+    }
+    void *d_cap;
+    if ((rc = upload(a, cap.data(), J * sizeof(unsigned long long), &d_cap, st))) return rc;
+    pre_cap = static_cast<unsigned long long *>(d_cap);
   }
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
@@ -582,7 +614,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                     heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0, nullptr,
-                                    first_num, c->n_sms, st));
+                                    first_num, pre_cap, c->n_sms, st));
     }
     if (speculate) {
       // the fill needs the quota table; the second round every token
@@ -591,12 +623,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       NS_CK(nsk::launch_fill_need(static_cast<uint32_t *>(d_sdb), J, D0,
                                   static_cast<uint16_t *>(d_stream_bp), order, klen, c->offs,
                                   c->n_tokens, c->cum + (size_t)K * J, T, c->G, first_num,
-                                  need_num, st));
+                                  pre_cap, need_num, st));
       NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                     heldout_mode ? 1u : 0u, frontier, kept, 0, J, need_num, 0,
-                                    c->n_sms, st));
+                                    nullptr, c->n_sms, st));
     }
   }
   // every token is on the device before anything after the hash reads it

@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
                        unsigned long long *kept, uint32_t j_begin, uint32_t j_count,
-                       const uint16_t *__restrict__ need_num, uint32_t need_num_all) {
+                       const uint16_t *__restrict__ need_num, uint32_t need_num_all,
+                       const unsigned long long *__restrict__ pre_cap) {
   constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -441,8 +442,10 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
     const uint64_t N = sdb[j + 1] - sdb[j];
     const uint64_t base_pos = (uint64_t)sdb[j] - D0;
     // need_j is known once the quota kernel (on another stream) has written
-    // the last row of its table; until then the stream is hashed on.
+    // the last row of its table; until then the stream is hashed up to an
+    // estimate of it from the recipe (pre_cap; none: on)
     unsigned long long need = ~0ull;
+    const unsigned long long cap = pre_cap ? pre_cap[j] : ~0ull;
     while (true) {
       unsigned long long base = 0;
       if (lane == 0) {
@@ -457,7 +460,8 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                 need_num ? need_num[j] : need_num_all);
         }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
-        base = (done > need) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
+        const unsigned long long lim = ready_seen ? need : cap;
+        base = (done > lim) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
       }
       base = __shfl_sync(0xffffffffu, base, 0);
       if (base >= N) break;
@@ -526,7 +530,9 @@ __global__ void __launch_bounds__(256)
                      const uint16_t *__restrict__ stream_bp, const uint32_t *__restrict__ order,
                      const uint32_t *__restrict__ klen, const int64_t *__restrict__ offs,
                      uint64_t n_tokens, const int32_t *__restrict__ cum_last, uint32_t T,
-                     uint32_t G, uint32_t first_num, uint16_t *__restrict__ need_num) {
+                     uint32_t G, uint32_t first_num,
+                     const unsigned long long *__restrict__ pre_cap,
+                     uint16_t *__restrict__ need_num) {
   // a block per stream: the sample's raw and kept lengths are staged in
   // shared memory by all its threads at once, then one warp decides
   __shared__ uint32_t raw_s[kFillSample], kept_s[kFillSample];
@@ -545,7 +551,10 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
-  const int64_t need1 = tokens_needed(cum_last[j], G, T, first_num);
+  // the first round hashed each stream to its need1, or, if its warps left
+  // it before the quota table was known, to more than its cap
+  int64_t need1 = tokens_needed(cum_last[j], G, T, first_num);
+  if (pre_cap && (int64_t)pre_cap[j] < need1) need1 = (int64_t)pre_cap[j];
   // S: positions [0, S) whose raw tokens add up to at most need1
   uint32_t S = 0;
   int64_t acc = 0;
@@ -1404,19 +1413,20 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
                                uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
-                               uint32_t need_num_all, int n_sms, cudaStream_t st) {
+                               uint32_t need_num_all, const unsigned long long *pre_cap,
+                               int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
   ++launch_counter();
   if (copy_dst)
     hash_prefix_kernel<true><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
         tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
         ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
-        need_num_all);
+        need_num_all, pre_cap);
   else
     hash_prefix_kernel<false><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
         tokens, nullptr, nullptr, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
         ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
-        need_num_all);
+        need_num_all, pre_cap);
   return cudaGetLastError();
 }
 
@@ -1439,12 +1449,13 @@ uint32_t copy_chunk_tokens() { return kCopyChunk; }
 cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
                              const uint16_t *stream_bp, const uint32_t *order, const uint32_t *klen,
                              const int64_t *offs, uint64_t n_tokens, const int32_t *cum_last,
-                             uint32_t T, uint32_t G, uint32_t first_num, uint16_t *need_num,
+                             uint32_t T, uint32_t G, uint32_t first_num,
+                             const unsigned long long *pre_cap, uint16_t *need_num,
                              cudaStream_t st) {
   if (J == 0) return cudaSuccess;
   ++launch_counter();
   fill_need_kernel<<<J, 256, 0, st>>>(sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
-                                      T, G, first_num, need_num);
+                                      T, G, first_num, pre_cap, need_num);
   return cudaGetLastError();
 }
 

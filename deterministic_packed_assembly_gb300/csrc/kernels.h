@@ -59,7 +59,9 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          int *err, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 // copy_dst non-null: tokens is host memory the device can address, and
-// every hashed document is also written to copy_dst (tokens_read counts them)
+// every hashed document is also written to copy_dst (tokens_read counts them).
+// pre_cap (per stream kept tokens, or NULL): where a stream stops before the
+// quota table is known
 cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                unsigned long long *tokens_read, const int64_t *offs,
                                const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
@@ -68,14 +70,16 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
                                uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
-                               uint32_t need_num_all, int n_sms, cudaStream_t st);
+                               uint32_t need_num_all, const unsigned long long *pre_cap,
+                               int n_sms, cudaStream_t st);
 // need_num: the fraction (of 1024) of each stream's bound the second hash
 // round stops at, from its measured packing fill (first_num: the first
 // round's)
 cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
                              const uint16_t *stream_bp, const uint32_t *order, const uint32_t *klen,
                              const int64_t *offs, uint64_t n_tokens, const int32_t *cum_last,
-                             uint32_t T, uint32_t G, uint32_t first_num, uint16_t *need_num,
+                             uint32_t T, uint32_t G, uint32_t first_num,
+                             const unsigned long long *pre_cap, uint16_t *need_num,
                              cudaStream_t st);
 // The kept tokens of positions [0, cutoff[j]) of every stream with
 // stream_bp[j] == 0, copied from src (host memory the device can address) to
