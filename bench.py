@@ -6,9 +6,9 @@ context build (held-out hash of every document, Feistel shuffle of every
 stream, scans, piece expansion, next-window search, pointer jumping, window
 numbering, two-level quotas, order digest) followed by the assembly of every
 update of the horizon (row gather with position ids, document ids, loss
-masks, row fingerprints, learned counts) and the batch fingerprint of every
-update.  Inputs are resident in HBM when the timed region starts; outputs go
-to a reused device buffer of ``--launch`` updates.
+masks, row fingerprints, learned counts) and the batch fingerprint and
+learned positions of every update.  Inputs are resident in HBM when the timed
+region starts; outputs go to a reused device buffer of ``--launch`` updates.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3]
     python bench.py --impl reference ...     # the CPU oracle on the same workload
@@ -374,6 +374,7 @@ def run_ours(args, dist: Dist) -> None:
     row_fp_all = torch.empty(c.max_steps * n_buf, dtype=torch.int64, device=device)
     row_ln_all = torch.empty(c.max_steps * n_buf, dtype=torch.int32, device=device)
     fp_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
+    learned_all = torch.empty(c.max_steps, dtype=torch.int64, device=device)
 
     state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0,
              "init_events": []}
@@ -436,16 +437,23 @@ def run_ours(args, dist: Dist) -> None:
                 real += (view["doc"] >= 0).sum()
         # batch fingerprints of every update (one GPU holds whole batches; with
         # row slices the rows are not in batch order)
+        # and each update's learned positions (this rank's share of them)
         if dist.world == 1 and args.slices <= 1:
             for f0, fm, fr, fo in folds:
                 pk.batch_fp_many(row_fp_all[fo:fo + fm * fr].view(fm, fr),
                                  out=fp_all[f0:f0 + fm], stream=stream)
+                n += 1
+        if args.slices <= 1:
+            for f0, fm, fr, fo in folds:
+                pk.step_learned(row_ln_all[fo:fo + fm * fr].view(fm, fr),
+                                out=learned_all[f0:f0 + fm], stream=stream)
                 n += 1
         if e2e is not None:
             e2e[3][:rows_total].copy_(row_fp_all[:rows_total], non_blocking=True)
             e2e[4][:rows_total].copy_(row_ln_all[:rows_total], non_blocking=True)
             if dist.world == 1:
                 e2e[5][:valid].copy_(fp_all[:valid], non_blocking=True)
+            e2e[6][:valid].copy_(learned_all[:valid], non_blocking=True)
         pk.close()
         state["launches"] = n
         state["rows_total"] = rows_total
@@ -540,13 +548,14 @@ def run_ours(args, dist: Dist) -> None:
         fp_h = torch.empty(c.max_steps * n_buf, dtype=torch.int64).pin_memory()
         ln_h = torch.empty(c.max_steps * n_buf, dtype=torch.int32).pin_memory()
         bf_h = torch.empty(c.max_steps, dtype=torch.int64).pin_memory()
+        sl_h = torch.empty(c.max_steps, dtype=torch.int64).pin_memory()
 
         def e2e_pass():
             # the corpus goes to the library in page-locked host memory: it
             # reads the documents the horizon reaches where they lie (the hash
             # writes what it reads into its device copy) and copies nothing
             # else
-            one_pass(False, e2e=(tok_h, off_h, ls_h, fp_h, ln_h, bf_h))
+            one_pass(False, e2e=(tok_h, off_h, ls_h, fp_h, ln_h, bf_h, sl_h))
 
         e2e_pass()
         dist.barrier()
@@ -559,7 +568,7 @@ def run_ours(args, dist: Dist) -> None:
         # bytes the library read from host memory (offsets, loss starts, the
         # tokens of the documents it used), as it reports them
         h2d = int(state["host_bytes"])
-        d2h = rows_pass * 12 + (valid * 8 if dist.world == 1 else 0)
+        d2h = rows_pass * 12 + (valid * 8 if dist.world == 1 else 0) + valid * 8
         if result is not None:
             result["e2e"] = {"value": dist.sum(real_tokens) * args.e2e_steps / e2e_s,
                              "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -570,7 +579,8 @@ def run_ours(args, dist: Dist) -> None:
                                      "inputs: the library reads the documents the horizon "
                                      "reaches from host memory (hash and prefix copy write "
                                      "them to its device copy), full pass, D2H of every row "
-                                     "fingerprint and learned count"}
+                                     "fingerprint and learned count and of every update's "
+                                     "batch fingerprint and learned positions"}
         else:
             dist.sum(real_tokens)
 

@@ -97,8 +97,9 @@ class ns_pack_info_t(C.Structure):
 
 # Every symbol the header declares, for the load check.
 SYMBOLS = ("ns_pack_init", "ns_pack_step", "ns_pack_fingerprint", "ns_pack_batch_fp",
-           "ns_pack_info", "ns_pack_stream_windows", "ns_pack_quota_table", "ns_pack_check",
-           "ns_pack_free", "ns_pack_strerror", "ns_pack_quota_noalloc")
+           "ns_pack_step_learned", "ns_pack_info", "ns_pack_stream_windows",
+           "ns_pack_quota_table", "ns_pack_check", "ns_pack_free", "ns_pack_strerror",
+           "ns_pack_quota_noalloc")
 
 
 def _load() -> C.CDLL:
@@ -118,6 +119,8 @@ def _load() -> C.CDLL:
     L.ns_pack_batch_fp.argtypes = [vp, vp, u32, u32, vp, vp]
     L.ns_pack_info.restype = i32
     L.ns_pack_info.argtypes = [vp, C.POINTER(ns_pack_info_t)]
+    L.ns_pack_step_learned.restype = i32
+    L.ns_pack_step_learned.argtypes = [vp, vp, u32, u32, vp, vp]
     L.ns_pack_stream_windows.restype = i32
     L.ns_pack_stream_windows.argtypes = [vp, vp, vp]
     L.ns_pack_quota_table.restype = i32
@@ -172,6 +175,12 @@ def ns_pack_batch_fp(ctx, row_fp_ptr: int, n_steps: int, n_rows: int, out_ptr: i
                      stream: int | None = None) -> None:
     check(lib.ns_pack_batch_fp(ctx, row_fp_ptr, n_steps, n_rows, out_ptr, stream),
           "ns_pack_batch_fp")
+
+
+def ns_pack_step_learned(ctx, row_learned_ptr: int, n_steps: int, n_rows: int, out_ptr: int,
+                         stream: int | None = None) -> None:
+    check(lib.ns_pack_step_learned(ctx, row_learned_ptr, n_steps, n_rows, out_ptr, stream),
+          "ns_pack_step_learned")
 
 
 def ns_pack_info(ctx) -> dict:

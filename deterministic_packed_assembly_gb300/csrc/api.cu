@@ -1009,6 +1009,19 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
   return NS_OK;
 }
 
+int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
+                         uint32_t n_rows, int64_t *learned_dev, void *cuda_stream) {
+  if (!ctx || !row_learned_dev || !learned_dev || n_steps == 0 || n_rows == 0)
+    return NS_ERR_INVALID_ARG;
+  cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
+  if (nsk::launch_step_learned(row_learned_dev, n_steps, n_rows, learned_dev, st) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return NS_ERR_CUDA;
+  }
+  return NS_OK;
+}
+
 static int read_error_word(ns_pack_ctx *ctx, cudaStream_t st) {
   int e = 0;
   if (cudaMemcpyAsync(&e, ctx->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||

@@ -200,6 +200,9 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
 // [128k, T); tile_scratch holds ceil(T / 128) words.
 cudaError_t launch_pad_tail(int32_t pad_id, uint32_t T, uint64_t *tile_scratch,
                             uint64_t *pad_tail, cudaStream_t st);
+// out[s] = sum of row_learned[s * n_rows .. (s + 1) * n_rows) (learned.cu)
+cudaError_t launch_step_learned(const int32_t *row_learned, uint32_t n_steps, uint32_t n_rows,
+                                int64_t *out, cudaStream_t st);
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
                             uint64_t *out, cudaStream_t st);
 

@@ -205,6 +205,18 @@ class Packer:
         L.ns_pack_batch_fp(self._ctx, row_fp.data_ptr(), n_steps, n_rows, out.data_ptr(), st)
         return out
 
+    def step_learned(self, row_learned: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Learned positions of each update of [n_steps, n_rows] row counts
+        (int64, async): what a trainer weighs the update's loss by."""
+        n_steps, n_rows = row_learned.shape
+        if out is None:
+            out = torch.empty(n_steps, dtype=torch.int64, device=self.device)
+        st = (stream or self.stream).cuda_stream
+        L.ns_pack_step_learned(self._ctx, row_learned.data_ptr(), n_steps, n_rows,
+                               out.data_ptr(), st)
+        return out
+
     def stream_windows(self):
         return L.ns_pack_stream_windows(self._ctx, self.n_streams)
 

@@ -242,6 +242,16 @@ int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n
 int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
                      uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream);
 
+/* Learned positions of n_steps consecutive updates of n_rows rows each:
+ * learned_dev[s] = sum of row_learned_dev[s * n_rows .. (s + 1) * n_rows)
+ * (device int32 in, device int64 out), the count an update's loss is weighed
+ * by (Linnet training docs, Supervised fine-tuning).  For a row slice it is
+ * the slice's share; the update's count is the sum over its slices.
+ * Asynchronous on cuda_stream (NULL: the context's).  Errors: INVALID_ARG,
+ * CUDA. */
+int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
+                         uint32_t n_rows, int64_t *learned_dev, void *cuda_stream);
+
 /* Summary of the context (host memory, no synchronisation). */
 int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info);
 

@@ -100,10 +100,12 @@ def test_full_size_sft_learned_counts_every_update():
         out = pk.step(s0, n_steps=n)
         got_l = out["row_learned"].cpu().numpy()
         got_fp = out["row_fp"].cpu().numpy().view(np.uint64)
+        step_l = pk.step_learned(out["row_learned"]).cpu().numpy()
         for q in range(n):
             want = o.rows(s0 + q)
             assert (got_l[q] == want["row_learned"]).all(), s0 + q
             assert (got_fp[q] == want["row_fp"]).all(), s0 + q
+            assert step_l[q] == int(want["row_learned"].astype(np.int64).sum()), s0 + q
 
 
 def test_full_size_elastic_slices():

@@ -275,6 +275,23 @@ def test_speculated_hash_bound_falls_short_and_init_runs_again():
     hp.check()
 
 
+@pytest.mark.parametrize("name", ["c2s", "c3s"])
+def test_step_learned_counts(name):
+    # each update's learned positions: the sum of its rows' counts, in 64
+    # bits, for whole batches and for row slices (whose counts add up)
+    c = make_preset(name)
+    pk, o = packer_for(c), oracle_for(c)
+    n = o.valid_steps
+    out = pk.step(0, n_steps=n)
+    got = pk.step_learned(out["row_learned"]).cpu().numpy()
+    want = np.asarray([int(o.rows(k)["row_learned"].astype(np.int64).sum()) for k in range(n)])
+    assert (got == want).all()
+    half = c.B // 2
+    a = pk.step_learned(pk.step(0, n_steps=n, rows=(0, half))["row_learned"]).cpu().numpy()
+    b = pk.step_learned(pk.step(0, n_steps=n, rows=(half, c.B))["row_learned"]).cpu().numpy()
+    assert (a + b == want).all()
+
+
 def test_horizon_and_row_range_errors():
     c = make_preset("c1")
     pk = packer_for(c)
