@@ -418,7 +418,7 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // that few overshoot any one stream.
 // With kCopy the tokens are read from host memory the device can address
 // and every hashed document is written to copy_dst; tokens_read counts them.
-template <bool kCopy>
+template <bool kCopy, bool kChunked>
 __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, int32_t *__restrict__ copy_dst,
                        unsigned long long *tokens_read, const int64_t *__restrict__ offs,
@@ -434,11 +434,39 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   bool ready_seen = false;
-  // streams [j_begin, j_begin + j_count) of the J
-  for (uint32_t jj = 0; jj < j_count; jj++) {
-    const uint32_t j = j_begin + (warp_id + jj) % j_count;
+  // streams [j_begin, j_begin + j_count) of the J.  kChunked (many streams):
+  // 32 looked at a time -- the lanes read their streams' state together and
+  // the warp then works only on those that still need hashing (with
+  // thousands of streams most are done, and one read per stream would take
+  // longer than the hashing); else one after the other
+  for (uint32_t c0 = 0; c0 < j_count; c0 += (kChunked ? 32 : 1)) {
+    bool live = !kChunked;
+    if (kChunked) {
+    if (lane == 0 && !ready_seen &&
+        *reinterpret_cast<const volatile unsigned *>(ready) >= ready_at) {
+      __threadfence();
+      ready_seen = true;
+    }
+    ready_seen = __shfl_sync(0xffffffffu, ready_seen, 0);
+    if (c0 + lane < j_count) {
+      const uint32_t j_l = j_begin + (warp_id + c0 + lane) % j_count;
+      if (stream_bp[j_l] != 0) {
+        const uint64_t n_l = sdb[j_l + 1] - sdb[j_l];
+        const unsigned long long fr = *reinterpret_cast<volatile unsigned long long *>(frontier + j_l);
+        const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j_l);
+        const unsigned long long lim =
+            ready_seen ? (unsigned long long)tokens_needed(
+                             *reinterpret_cast<const volatile int32_t *>(cum_last + j_l), G, T,
+                             need_num ? need_num[j_l] : need_num_all)
+                       : (pre_cap ? pre_cap[j_l] : ~0ull);
+        live = fr < n_l && done <= lim;
+      }
+    }
+    }
+    for (unsigned m = kChunked ? __ballot_sync(0xffffffffu, live) : 1u; m; m &= m - 1) {
+    const uint32_t j = j_begin + (warp_id + c0 + (uint32_t)(__ffs(m) - 1)) % j_count;
     const uint32_t bp = stream_bp[j];
-    if (bp == 0) continue;
+    if (!kChunked && bp == 0) continue;
     const uint64_t N = sdb[j + 1] - sdb[j];
     const uint64_t base_pos = (uint64_t)sdb[j] - D0;
     // need_j is known once the quota kernel (on another stream) has written
@@ -499,6 +527,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         const unsigned long long read_here = warp_sum_u64(L_l);
         if (lane == 0 && read_here) atomicAdd(tokens_read, read_here);
       }
+    }
     }
   }
 }
@@ -1417,16 +1446,26 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
   ++launch_counter();
-  if (copy_dst)
-    hash_prefix_kernel<true><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
-        tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
-        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
-        need_num_all, pre_cap);
-  else
-    hash_prefix_kernel<false><<<n_sms * kHashBlocksPerSM, kHashThreads, 0, st>>>(
-        tokens, nullptr, nullptr, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready,
-        ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,
-        need_num_all, pre_cap);
+  // more streams than this: the warps look at them 32 at a time
+  constexpr uint32_t kChunkFrom = 64;
+  const dim3 grid(n_sms * kHashBlocksPerSM), block(kHashThreads);
+#define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
+  hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
+      tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, \
+      ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,       \
+      need_num_all, pre_cap)
+  if (copy_dst) {
+    if (j_count > kChunkFrom)
+      NS_HASH_LAUNCH(true, true);
+    else
+      NS_HASH_LAUNCH(true, false);
+  } else {
+    if (j_count > kChunkFrom)
+      NS_HASH_LAUNCH(false, true);
+    else
+      NS_HASH_LAUNCH(false, false);
+  }
+#undef NS_HASH_LAUNCH
   return cudaGetLastError();
 }
 
