@@ -125,27 +125,67 @@ __device__ __forceinline__ void publish_ready(unsigned *ready) {
 //   base_c = floor(n v_c / V); R = n - sum base;
 //   delta_c = N v_c - V (C_c + base_c)  (exact, 128-bit);
 //   the R children with the largest delta (ties: lower index) get one more.
+// Children ranked by (shortfall desc, index asc); with more than
+// kRankDirect of them a bitonic sort of (shortfall, index) over the block
+// (blockDim.x a power of two) replaces counting each child's rank against
+// all others, so an update costs O(n log^2 n) compare-exchanges, not O(n^2).
+constexpr int kRankDirect = 64;
+
 __device__ __forceinline__ int64_t apportion_one(bool act, uint64_t v, uint64_t V, int64_t n,
                                                  int64_t N, int64_t C, int n_children,
-                                                 __int128 *delta, int64_t *scratch) {
+                                                 __int128 *delta, int *order_s, int64_t *scratch) {
   int64_t base = act ? (int64_t)(((uint64_t)n * v) / V) : 0;
   int64_t R = n - block_sum<int64_t>(base, scratch);
   __int128 d = 0;
-  if (act) {
-    d = (__int128)N * (__int128)v - (__int128)V * (__int128)(C + base);
-    delta[threadIdx.x] = d;
-  }
-  __syncthreads();
+  if (act) d = (__int128)N * (__int128)v - (__int128)V * (__int128)(C + base);
+  const int c = threadIdx.x;
   int64_t a = base;
-  if (act) {
-    int rank = 0;
-    const int c = threadIdx.x;
-    for (int c2 = 0; c2 < n_children; c2++) {
-      __int128 e = delta[c2];
-      rank += (e > d) || (e == d && c2 < c);
+  if (n_children <= kRankDirect) {
+    if (act) delta[c] = d;
+    __syncthreads();
+    if (act) {
+      int rank = 0;
+      for (int c2 = 0; c2 < n_children; c2++) {
+        __int128 e = delta[c2];
+        rank += (e > d) || (e == d && c2 < c);
+      }
+      a += (rank < R) ? 1 : 0;
     }
-    a += (rank < R) ? 1 : 0;
+    __syncthreads();
+    return a;
   }
+  // sort: inactive slots carry the smallest shortfall, after every child
+  const __int128 kLow = (__int128)1 << 127;  // the most negative value
+  delta[c] = act ? d : kLow;
+  order_s[c] = c;
+  __syncthreads();
+  const int P2 = (int)blockDim.x;
+  for (int k = 2; k <= P2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      const int ix = c ^ jj;
+      if (ix > c) {
+        const __int128 dc = delta[c], dx = delta[ix];
+        const int oc = order_s[c], ox = order_s[ix];
+        // does slot ix's child come before slot c's (larger shortfall, or
+        // equal and lower index)?
+        const bool x_first = dx > dc || (dx == dc && ox < oc);
+        const bool swap = ((c & k) == 0) ? x_first : !x_first;
+        if (swap) {
+          delta[c] = dx;
+          delta[ix] = dc;
+          order_s[c] = ox;
+          order_s[ix] = oc;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // slot r holds the child of rank r: the first R get one more
+  const int child = order_s[c];
+  __syncthreads();
+  order_s[child] = (c < R) ? 1 : 0;
+  __syncthreads();
+  if (act) a += order_s[c];
   __syncthreads();
   return a;
 }
@@ -156,6 +196,7 @@ __device__ __forceinline__ int64_t apportion_one(bool act, uint64_t v, uint64_t 
 __global__ void quota_sources_kernel(QuotaPieces q, uint32_t S, uint32_t K,
                                      int32_t *__restrict__ src_quota) {
   __shared__ __int128 delta[1024];
+  __shared__ int order_s[1024];
   __shared__ int64_t scratch[33];
   __shared__ uint64_t uscratch[33];
   const bool act = threadIdx.x < S;
@@ -167,7 +208,7 @@ __global__ void quota_sources_kernel(QuotaPieces q, uint32_t S, uint32_t K,
     int64_t C = 0;
     for (uint32_t k = k0; k < k1; k++) {
       int64_t a = apportion_one(act, v, V, Bp, (int64_t)(k - k0 + 1) * Bp, C, (int)S, delta,
-                                scratch);
+                                order_s, scratch);
       if (act) src_quota[(size_t)k * S + threadIdx.x] = (int32_t)a;
       C += a;
     }
@@ -182,6 +223,7 @@ __global__ void quota_strata_kernel(QuotaPieces q, const int32_t *__restrict__ s
                                     uint32_t J, uint32_t K, int32_t *__restrict__ quota,
                                     int32_t *__restrict__ cum, unsigned *ready) {
   __shared__ __int128 delta[1024];
+  __shared__ int order_s[1024];
   __shared__ int64_t scratch[33];
   __shared__ uint64_t uscratch[33];
   const uint32_t s = blockIdx.x;
@@ -197,7 +239,7 @@ __global__ void quota_strata_kernel(QuotaPieces q, const int32_t *__restrict__ s
     int64_t C = 0, Cs = 0;
     for (uint32_t k = k0; k < k1; k++) {
       const int64_t n = src_quota[(size_t)k * S + s];
-      int64_t a = apportion_one(act, v, V, n, Cs + n, C, n_st, delta, scratch);
+      int64_t a = apportion_one(act, v, V, n, Cs + n, C, n_st, delta, order_s, scratch);
       if (act) {
         quota[(size_t)k * J + j] = (int32_t)a;
         cum[(size_t)k * J + j] = (int32_t)Cg;
@@ -1378,9 +1420,17 @@ cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaSt
   return cudaGetLastError();
 }
 
+// Threads of a block-level quota kernel over n children: whole warps, and a
+// power of two once the children are ranked by sorting.
 static unsigned round_warps(uint32_t n) {
   unsigned t = ((n + 31) / 32) * 32;
-  return t < 32 ? 32 : t;
+  if (t < 32) t = 32;
+  if (n > (uint32_t)kRankDirect) {
+    unsigned p = 32;
+    while (p < n) p <<= 1;
+    t = p;
+  }
+  return t;
 }
 
 cudaError_t launch_quota_sources(QuotaPieces q, uint32_t S, uint32_t K, int32_t *src_quota,

@@ -336,10 +336,12 @@ def test_batch_fingerprints_many():
         assert fps[k] == oracle.batch_fp(o.rows(k)["row_fp"])
 
 
-@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40), (33, 1), (1, 33)])
+@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40), (33, 1), (1, 33), (100, 1), (2, 100),
+                                      (513, 1), (3, 300)])
 def test_quota_tables_beyond_one_warp(S, strata):
     # more than 32 sources, or more than 32 strata in a source, take the
-    # block-level quota kernels instead of the single-warp one
+    # block-level quota kernels instead of the single-warp one; more than 64
+    # children rank their shortfalls by a bitonic sort
     J = S * strata
     rng = np.random.default_rng(S * 100 + strata)
     lengths = [int(x) for x in rng.integers(1, 200, size=J * 6)]
@@ -446,7 +448,7 @@ def test_schedules(name, n_pieces, G, rows):
         assert e.value.code == -1
 
 
-@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40)])
+@pytest.mark.parametrize("S,strata", [(40, 2), (2, 40), (130, 2), (2, 70)])
 def test_schedules_beyond_one_warp(S, strata):
     J = S * strata
     rng = np.random.default_rng(S + strata)
