@@ -43,6 +43,35 @@ __device__ __forceinline__ void seg_locate(const SegGrid &g, uint32_t &j, uint32
   blk = blockIdx.x - g.blk_base[j];
 }
 
+// Exclusive prefix of one value per thread over the block (blockDim.x a
+// multiple of 32); *total gets the block's sum in every thread.  ws: 33
+// words of shared memory, free again when it returns.
+__device__ __forceinline__ int64_t block_excl_scan(int64_t v, int64_t *ws, int64_t *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int64_t t = (lane < nw) ? ws[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    ws[lane] = t;
+  }
+  __syncthreads();
+  const int64_t excl = (w ? ws[w - 1] : 0) + x - v;
+  *total = ws[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
 template <class T>
 __device__ T block_sum(T v, T *scratch /* [33] */) {
 #pragma unroll
@@ -345,18 +374,22 @@ __global__ void __launch_bounds__(32)
 }
 
 // rb[k][j]: the first row of stream j in update k (rows ordered by stream).
-__global__ void row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
-                                int32_t *__restrict__ rb) {
-  uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k >= K) return;
+// One block per update, a block-wide scan over the streams.
+__global__ void __launch_bounds__(256)
+    row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, int32_t *__restrict__ rb) {
+  __shared__ int64_t ws[33];
+  const uint32_t k = blockIdx.x;
   const int32_t *q = quota + (size_t)k * J;
   int32_t *r = rb + (size_t)k * (J + 1);
-  int32_t acc = 0;
-  for (uint32_t j = 0; j < J; j++) {
-    r[j] = acc;
-    acc += q[j];
+  int64_t carry = 0;
+  for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
+    const uint32_t j = c0 + threadIdx.x;
+    int64_t total;
+    const int64_t e = block_excl_scan((j < J) ? q[j] : 0, ws, &total);
+    if (j < J) r[j] = (int32_t)(carry + e);
+    carry += total;
   }
-  r[J] = acc;
+  if (threadIdx.x == 0) r[J] = (int32_t)carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -1047,18 +1080,19 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
 }
 
 // node_base[j] = sum over j' < j of (pieces of j' + 1 terminal node).
-__global__ void node_base_kernel(const int64_t *__restrict__ npieces, uint32_t J,
-                                 int64_t *__restrict__ node_base) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(1024)
+    node_base_kernel(const int64_t *__restrict__ npieces, uint32_t J,
+                     int64_t *__restrict__ node_base) {
+  __shared__ int64_t ws[33];
   int64_t carry = 0;
-  for (uint32_t c0 = 0; c0 < J; c0 += 32) {
-    const uint32_t j = c0 + lane;
-    const int64_t v = (j < J) ? npieces[j] + 1 : 0;
-    const int64_t x = warp_incl_scan(v, lane);
-    if (j < J) node_base[j] = carry + x - v;
-    carry += __shfl_sync(0xffffffffu, x, 31);
+  for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
+    const uint32_t j = c0 + threadIdx.x;
+    int64_t total;
+    const int64_t e = block_excl_scan((j < J) ? npieces[j] + 1 : 0, ws, &total);
+    if (j < J) node_base[j] = carry + e;
+    carry += total;
   }
-  if (lane == 0) node_base[J] = carry;
+  if (threadIdx.x == 0) node_base[J] = carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -1349,20 +1383,22 @@ __global__ void digest_quota_kernel(const int32_t *__restrict__ quota, uint32_t 
   digest_accumulate(term, acc);
 }
 
-__global__ void digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
-                                   uint32_t J, const uint32_t *valid, int64_t *ubase) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(1024)
+    digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
+                       uint32_t J, const uint32_t *valid, int64_t *ubase) {
+  __shared__ int64_t ws[33];
   const uint32_t v = *valid;
   int64_t carry = 0;
-  for (uint32_t c0 = 0; c0 < J; c0 += 32) {
-    const uint32_t j = c0 + lane;
+  for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
+    const uint32_t j = c0 + threadIdx.x;
     int64_t u = 0;
     if (j < J) u = min((int64_t)cum[(size_t)v * J + j], (int64_t)W[j]);
-    const int64_t x = warp_incl_scan(u, lane);
-    if (j < J) ubase[j] = carry + x - u;
-    carry += __shfl_sync(0xffffffffu, x, 31);
+    int64_t total;
+    const int64_t e = block_excl_scan(u, ws, &total);
+    if (j < J) ubase[j] = carry + e;
+    carry += total;
   }
-  if (lane == 0) ubase[J] = carry;
+  if (threadIdx.x == 0) ubase[J] = carry;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -1480,7 +1516,7 @@ cudaError_t launch_quota_warp(QuotaPieces q, uint32_t S, const uint32_t *src_fir
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st) {
   ++launch_counter();
-  row_base_kernel<<<blocks_for(K, 128), 128, 0, st>>>(quota, J, K, rb);
+  row_base_kernel<<<K, (J <= 32 ? 32 : J <= 128 ? 128 : 256), 0, st>>>(quota, J, rb);
   return cudaGetLastError();
 }
 
@@ -1599,7 +1635,7 @@ cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const in
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st) {
   ++launch_counter();
-  node_base_kernel<<<1, 32, 0, st>>>(npieces, J, node_base);
+  node_base_kernel<<<1, (J <= 32 ? 32 : J <= 256 ? 256 : 1024), 0, st>>>(npieces, J, node_base);
   return cudaGetLastError();
 }
 
@@ -1723,7 +1759,8 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  digest_used_kernel<<<1, 32, 0, st>>>(cum, W, h.J, valid, ubase);
+  digest_used_kernel<<<1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st>>>(cum, W, h.J, valid,
+                                                                            ubase);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (wg.n_blocks > 0) {
