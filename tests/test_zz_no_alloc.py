@@ -29,7 +29,11 @@ def _recipes():
                 stream_source=[s for s in range(40) for _ in range(2)],
                 stream_weight=[int(x) for x in rng.integers(1, 10**6, size=80)],
                 B=300, max_steps=400)
-    return [("mixture", mixture), ("forty_sources", wide)]
+    # 130 sources x 1 stratum: the source level ranks its shortfalls by sorting
+    many = dict(source_weight=[int(x) for x in rng.integers(1, 10**6, size=130)],
+                stream_source=list(range(130)),
+                stream_weight=[1] * 130, B=257, max_steps=300)
+    return [("mixture", mixture), ("forty_sources", wide), ("many_sources", many)]
 
 
 def _tables_by_init(r):
@@ -59,7 +63,8 @@ def test_two_calls_in_a_row_match_the_allocating_path():
     want = {name: _tables_by_init(r) for name, r in recipes}
     # two calls in a row per recipe, then the recipes interleaved, each into
     # buffers the caller owns (filled with garbage first)
-    order = [recipes[0], recipes[0], recipes[1], recipes[1], recipes[0]]
+    order = [recipes[0], recipes[0], recipes[1], recipes[1], recipes[2], recipes[2],
+             recipes[0]]
     for name, r in order:
         K, J = r["max_steps"], len(r["stream_source"])
         q_dev = torch.full((K, J), -7, dtype=torch.int32, device="cuda:0")
