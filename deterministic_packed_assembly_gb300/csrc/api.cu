@@ -999,7 +999,8 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
 
 int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
                      uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream) {
-  if (!ctx || !row_fp_dev || !batch_fp_dev || n_steps == 0 || n_rows == 0)
+  if (!ctx || !row_fp_dev || !batch_fp_dev || n_steps == 0 || n_rows == 0 ||
+      n_steps >= (1u << 31))
     return NS_ERR_INVALID_ARG;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_batch_fp(row_fp_dev, n_steps, n_rows, batch_fp_dev, st) != cudaSuccess) {
@@ -1011,7 +1012,8 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
 
 int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
                          uint32_t n_rows, int64_t *learned_dev, void *cuda_stream) {
-  if (!ctx || !row_learned_dev || !learned_dev || n_steps == 0 || n_rows == 0)
+  if (!ctx || !row_learned_dev || !learned_dev || n_steps == 0 || n_rows == 0 ||
+      n_steps >= (1u << 31))
     return NS_ERR_INVALID_ARG;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_step_learned(row_learned_dev, n_steps, n_rows, learned_dev, st) !=

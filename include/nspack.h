@@ -238,7 +238,8 @@ int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n
 
 /* Asynchronous variant for n_steps consecutive batches of n_rows rows each:
  * batch_fp_dev[s] = fold of row_fp_dev[s * n_rows .. (s + 1) * n_rows).
- * Errors: INVALID_ARG, CUDA. */
+ * Errors: INVALID_ARG (NULL pointers, n_steps or n_rows 0, n_steps >= 2^31),
+ * CUDA. */
 int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
                      uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream);
 
@@ -247,8 +248,8 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
  * (device int32 in, device int64 out), the count an update's loss is weighed
  * by (Linnet training docs, Supervised fine-tuning).  For a row slice it is
  * the slice's share; the update's count is the sum over its slices.
- * Asynchronous on cuda_stream (NULL: the context's).  Errors: INVALID_ARG,
- * CUDA. */
+ * Asynchronous on cuda_stream (NULL: the context's).  Errors: INVALID_ARG
+ * (NULL pointers, n_steps or n_rows 0, n_steps >= 2^31), CUDA. */
 int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
                          uint32_t n_rows, int64_t *learned_dev, void *cuda_stream);
 

@@ -118,4 +118,6 @@ def test_null_context_is_rejected(nspack):
     info = L.ns_pack_info_t()
     assert L.lib.ns_pack_info(None, C.byref(info)) == nspack.NS_ERR_INVALID_ARG
     assert L.lib.ns_pack_check(None) == nspack.NS_ERR_INVALID_ARG
+    assert L.lib.ns_pack_batch_fp(None, None, 1, 1, None, None) == nspack.NS_ERR_INVALID_ARG
+    assert L.lib.ns_pack_step_learned(None, None, 1, 1, None, None) == nspack.NS_ERR_INVALID_ARG
     L.lib.ns_pack_free(None)
