@@ -597,10 +597,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *kept = a.temp<unsigned long long>(J);
+    unsigned long long *in_flight = a.temp<unsigned long long>(J);
     NS_ALLOC(frontier);
     NS_ALLOC(kept);
+    NS_ALLOC(in_flight);
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
     NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
+    NS_CK(cudaMemsetAsync(in_flight, 0, (size_t)J * 8, st));
     const uint32_t first_num = speculate ? 512u : 1024u;
     const int32_t *src = htok ? htok : c->tokens;
     int32_t *dst = htok ? c->tokens_rw : nullptr;
@@ -613,7 +616,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                    heldout_mode ? 1u : 0u, frontier, kept, j0, j1 - j0, nullptr,
+                                    heldout_mode ? 1u : 0u, frontier, kept, in_flight, j0, j1 - j0, nullptr,
                                     first_num, pre_cap, c->n_sms, st));
     }
     if (speculate) {
@@ -627,7 +630,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                    heldout_mode ? 1u : 0u, frontier, kept, 0, J, need_num, 0,
+                                    heldout_mode ? 1u : 0u, frontier, kept, in_flight, 0, J, need_num, 0,
                                     nullptr, c->n_sms, st));
     }
   }

@@ -481,18 +481,39 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // stream's documents are taken in shuffled-position order, a few at a time
 // from the stream's frontier; a document the stream does not keep (held out
 // for training, not held out for validation) has its kept length set to 0.
-// A warp leaves a stream once the kept tokens of the documents already hashed
-// exceed need_j = num_j / 1024 of rmax_j * T (rmax_j * T: the windows the
-// horizon asks of it hold at most that many; num_j from need_num, or
-// need_num_all for every stream), or when the stream runs out, and goes on
-// to the next stream.  A second launch with a larger num_j carries on from
-// the first's frontier.  Every position below the final frontier is hashed,
-// and the kept tokens below it exceed need_j unless the whole stream was
-// hashed, so the prefix the cutoff kernel then takes (with the same num_j)
-// only ever holds decided documents.  Warps start on different streams so
-// that few overshoot any one stream.
+// A warp takes more of a stream while the kept tokens of the documents
+// already hashed, plus a cautious share of the tokens other warps are still
+// hashing there (in_flight), fall short of need_j = num_j / 1024 of
+// rmax_j * T (rmax_j * T: the windows the horizon asks of it hold at most
+// that many; num_j from need_num, or need_num_all for every stream), and
+// goes on to the next stream once that sum reaches need_j or the stream runs
+// out.  A second launch with a larger num_j carries on from the first's
+// frontier.  Counting the tokens in flight keeps the warps that pile onto
+// the last streams from each taking one more grab past the need; the share
+// only sets how far past need_j a stream is hashed: a warp looks again after
+// each grab it finishes, and the one that finishes a stream's last grab in
+// flight sees nothing in flight, so no stream is left with its kept tokens
+// at or below need_j and positions to go.  Every position below the final
+// frontier is hashed, and the kept tokens below it exceed need_j unless the
+// whole stream was hashed, so the prefix the cutoff kernel then takes (with
+// the same num_j) only ever holds decided documents.  Warps start on
+// different streams so that few overshoot any one stream.
 // With kCopy the tokens are read from host memory the device can address
 // and every hashed document is written to copy_dst; tokens_read counts them.
+// The share of a stream's tokens in flight counted as kept when deciding
+// whether to take more: the expected kept fraction less 1/8, so that the
+// documents in flight keep at least that much almost surely (below it, the
+// warps that finish them take the rest one grab at a time).
+__device__ __forceinline__ float inflight_share(uint32_t bp, uint32_t want_heldout) {
+  const float keep = (float)(want_heldout ? bp : 10000u - bp) * 1e-4f;
+  return keep > 0.125f ? keep - 0.125f : 0.0f;
+}
+
+__device__ __forceinline__ bool take_more(unsigned long long done, unsigned long long in_flight,
+                                          unsigned long long lim, float share) {
+  return done + (unsigned long long)(share * (float)in_flight) <= lim;
+}
+
 template <bool kCopy, bool kChunked>
 __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, int32_t *__restrict__ copy_dst,
@@ -502,7 +523,8 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
-                       unsigned long long *kept, uint32_t j_begin, uint32_t j_count,
+                       unsigned long long *kept, unsigned long long *in_flight,
+                       uint32_t j_begin, uint32_t j_count,
                        const uint16_t *__restrict__ need_num, uint32_t need_num_all,
                        const unsigned long long *__restrict__ pre_cap) {
   constexpr uint32_t kGrab = 4;
@@ -529,12 +551,14 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         const uint64_t n_l = sdb[j_l + 1] - sdb[j_l];
         const unsigned long long fr = *reinterpret_cast<volatile unsigned long long *>(frontier + j_l);
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j_l);
+        const unsigned long long fl =
+            *reinterpret_cast<volatile unsigned long long *>(in_flight + j_l);
         const unsigned long long lim =
             ready_seen ? (unsigned long long)tokens_needed(
                              *reinterpret_cast<const volatile int32_t *>(cum_last + j_l), G, T,
                              need_num ? need_num[j_l] : need_num_all)
                        : (pre_cap ? pre_cap[j_l] : ~0ull);
-        live = fr < n_l && done <= lim;
+        live = fr < n_l && take_more(done, fl, lim, inflight_share(stream_bp[j_l], want_heldout));
       }
     }
     }
@@ -563,8 +587,11 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                 need_num ? need_num[j] : need_num_all);
         }
         const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
+        const unsigned long long fl = *reinterpret_cast<volatile unsigned long long *>(in_flight + j);
         const unsigned long long lim = ready_seen ? need : cap;
-        base = (done > lim) ? N : atomicAdd(frontier + j, (unsigned long long)kGrab);
+        base = take_more(done, fl, lim, inflight_share(bp, want_heldout))
+                   ? atomicAdd(frontier + j, (unsigned long long)kGrab)
+                   : N;
       }
       base = __shfl_sync(0xffffffffu, base, 0);
       if (base >= N) break;
@@ -577,6 +604,11 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         const uint64_t idx = base_pos + base + lane;
         L_l = klen[idx];
         if (L_l) o_l = __ldg(offs + order[idx]);
+      }
+      // the grab's tokens are in flight until its decisions are counted
+      {
+        const unsigned long long raw = warp_sum_u64(L_l);
+        if (lane == 0 && raw) atomicAdd(in_flight + j, raw);
       }
       uint64_t mine = 0;  // lane q: the token-term sum of document q
       for (int q = 0; q < (int)(pend - base); q++) {
@@ -597,10 +629,15 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
           kept_here = L_l;
       }
       kept_here = warp_sum_u64(kept_here);
-      if (lane == 0 && kept_here) atomicAdd(kept + j, kept_here);
-      if (kCopy) {
-        const unsigned long long read_here = warp_sum_u64(L_l);
-        if (lane == 0 && read_here) atomicAdd(tokens_read, read_here);
+      const unsigned long long raw_here = warp_sum_u64(L_l);
+      if (lane == 0 && raw_here) {
+        if (kept_here) atomicAdd(kept + j, kept_here);
+        if (kCopy) atomicAdd(tokens_read, raw_here);
+        // kept first, then out of flight: a warp that sees the grab gone
+        // from in_flight sees its kept tokens
+        __threadfence();
+        atomicAdd(in_flight + j, 0ull - raw_here);
+        __threadfence();
       }
     }
     }
@@ -1527,7 +1564,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
                                unsigned long long *frontier, unsigned long long *kept,
-                               uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
+                               unsigned long long *in_flight, uint32_t j_begin,
+                               uint32_t j_count, const uint16_t *need_num,
                                uint32_t need_num_all, const unsigned long long *pre_cap,
                                int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
@@ -1538,8 +1576,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
 #define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
   hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
       tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, \
-      ready_at, T, G, hash_key, want_heldout, frontier, kept, j_begin, j_count, need_num,       \
-      need_num_all, pre_cap)
+      ready_at, T, G, hash_key, want_heldout, frontier, kept, in_flight, j_begin, j_count,      \
+      need_num, need_num_all, pre_cap)
   if (copy_dst) {
     if (j_count > kChunkFrom)
       NS_HASH_LAUNCH(true, true);
