@@ -26,6 +26,7 @@ NS_PACK_SHUFFLE_ROWS = 4
 NS_PACK_WRAP = 8
 NS_PACK_HOST_CORPUS = 16
 NS_MAX_T = 1 << 24
+NS_MAX_TOKENS = 1 << 47
 
 ns_alloc_fn = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)
 ns_free_fn = C.CFUNCTYPE(None, C.c_void_p, C.c_void_p)

@@ -147,6 +147,7 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->B == 0 || cfg->max_steps == 0) return NS_ERR_INVALID_ARG;
   if ((uint64_t)cfg->max_steps * cfg->B >= (1ull << 31)) return NS_ERR_INVALID_ARG;
   if (cfg->n_docs >= (1u << 31)) return NS_ERR_INVALID_ARG;
+  if (cfg->n_tokens >= NS_MAX_TOKENS) return NS_ERR_INVALID_ARG;
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
   if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP |
@@ -596,14 +597,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
-    unsigned long long *kept = a.temp<unsigned long long>(J);
-    unsigned long long *in_flight = a.temp<unsigned long long>(J);
+    unsigned long long *prog = a.temp<unsigned long long>(J);  // per stream, see the kernel
     NS_ALLOC(frontier);
-    NS_ALLOC(kept);
-    NS_ALLOC(in_flight);
+    NS_ALLOC(prog);
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
-    NS_CK(cudaMemsetAsync(kept, 0, (size_t)J * 8, st));
-    NS_CK(cudaMemsetAsync(in_flight, 0, (size_t)J * 8, st));
+    NS_CK(cudaMemsetAsync(prog, 0, (size_t)J * 8, st));
     const uint32_t first_num = speculate ? 512u : 1024u;
     const int32_t *src = htok ? htok : c->tokens;
     int32_t *dst = htok ? c->tokens_rw : nullptr;
@@ -616,7 +614,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                    heldout_mode ? 1u : 0u, frontier, kept, in_flight, j0, j1 - j0, nullptr,
+                                    heldout_mode ? 1u : 0u, frontier, prog, j0, j1 - j0, nullptr,
                                     first_num, pre_cap, c->n_sms, st));
     }
     if (speculate) {
@@ -630,7 +628,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
-                                    heldout_mode ? 1u : 0u, frontier, kept, in_flight, 0, J, need_num, 0,
+                                    heldout_mode ? 1u : 0u, frontier, prog, 0, J, need_num, 0,
                                     nullptr, c->n_sms, st));
     }
   }

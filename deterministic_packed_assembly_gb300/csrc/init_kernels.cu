@@ -481,37 +481,46 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
 // stream's documents are taken in shuffled-position order, a few at a time
 // from the stream's frontier; a document the stream does not keep (held out
 // for training, not held out for validation) has its kept length set to 0.
-// A warp takes more of a stream while the kept tokens of the documents
-// already hashed, plus a cautious share of the tokens other warps are still
-// hashing there (in_flight), fall short of need_j = num_j / 1024 of
-// rmax_j * T (rmax_j * T: the windows the horizon asks of it hold at most
-// that many; num_j from need_num, or need_num_all for every stream), and
-// goes on to the next stream once that sum reaches need_j or the stream runs
-// out.  A second launch with a larger num_j carries on from the first's
-// frontier.  Counting the tokens in flight keeps the warps that pile onto
-// the last streams from each taking one more grab past the need; the share
-// only sets how far past need_j a stream is hashed: a warp looks again after
-// each grab it finishes, and the one that finishes a stream's last grab in
-// flight sees nothing in flight, so no stream is left with its kept tokens
-// at or below need_j and positions to go.  Every position below the final
-// frontier is hashed, and the kept tokens below it exceed need_j unless the
-// whole stream was hashed, so the prefix the cutoff kernel then takes (with
-// the same num_j) only ever holds decided documents.  Warps start on
-// different streams so that few overshoot any one stream.
+// A warp takes more of a stream while its progress word (below) stays at
+// or under need_j = num_j / 1024 of rmax_j * T (rmax_j * T: the windows the
+// horizon asks of it hold at most that many; num_j from need_num, or
+// need_num_all for every stream), and goes on to the next stream once the
+// word passes need_j or the stream runs out.  A second launch with a larger
+// num_j carries on from the first's frontier and words.  Every position
+// below the final frontier is hashed, and the kept tokens below it exceed
+// need_j unless the whole stream was hashed, so the prefix the cutoff kernel
+// then takes (with the same num_j) only ever holds decided documents.  Warps
+// start on different streams so that few overshoot any one stream.
 // With kCopy the tokens are read from host memory the device can address
 // and every hashed document is written to copy_dst; tokens_read counts them.
-// The share of a stream's tokens in flight counted as kept when deciding
-// whether to take more: the expected kept fraction less 1/8, so that the
-// documents in flight keep at least that much almost surely (below it, the
-// warps that finish them take the rest one grab at a time).
-__device__ __forceinline__ float inflight_share(uint32_t bp, uint32_t want_heldout) {
-  const float keep = (float)(want_heldout ? bp : 10000u - bp) * 1e-4f;
-  return keep > 0.125f ? keep - 0.125f : 0.0f;
+//
+// A stream's progress word: bits 16 and up hold the kept tokens of the
+// documents already decided plus, for each grab in flight, an estimate of
+// the tokens it will keep (grab_estimate); bits 0..15 count the grabs in
+// flight (at most one a warp: fewer than 2^16).  Counting grabs in flight
+// keeps the warps that pile onto the last streams of a round from each
+// taking one more grab once the need is already in flight.  The estimate
+// only sets how far past need_j a stream is hashed: a warp reads the word
+// again after each grab it finishes, and after the last update that leaves
+// no grab in flight the word holds the decided kept tokens exactly, so the
+// warp that made it takes more if they do not exceed need_j.  One word, so
+// that both parts are read and updated together.  (A stream holds fewer
+// than 2^47 tokens: the corpus is copied to the device whole.)
+//
+// The estimate: the expected kept fraction less 1/8 of the grab's tokens,
+// which its documents keep almost surely (when they do not, the warp that
+// decides the last of them takes the rest one grab at a time).  A stream
+// that keeps at most 1/8 of its tokens (the validation stream) estimates
+// nothing: its word is then its decided kept tokens alone, and its grabs are
+// not counted either.
+__device__ __forceinline__ uint32_t grab_share(uint32_t bp, uint32_t want_heldout) {
+  const uint32_t keep = want_heldout ? bp : 10000u - bp;  // of 10000
+  return keep > 1250u ? keep - 1250u : 0u;
 }
 
-__device__ __forceinline__ bool take_more(unsigned long long done, unsigned long long in_flight,
-                                          unsigned long long lim, float share) {
-  return done + (unsigned long long)(share * (float)in_flight) <= lim;
+__device__ __forceinline__ unsigned long long grab_estimate(unsigned long long raw,
+                                                            uint32_t share) {
+  return raw * share / 10000u;
 }
 
 template <bool kCopy, bool kChunked>
@@ -523,8 +532,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
                        const unsigned *ready, unsigned ready_at, uint32_t T, uint32_t G,
                        uint64_t hash_key, uint32_t want_heldout, unsigned long long *frontier,
-                       unsigned long long *kept, unsigned long long *in_flight,
-                       uint32_t j_begin, uint32_t j_count,
+                       unsigned long long *prog, uint32_t j_begin, uint32_t j_count,
                        const uint16_t *__restrict__ need_num, uint32_t need_num_all,
                        const unsigned long long *__restrict__ pre_cap) {
   constexpr uint32_t kGrab = 4;
@@ -550,15 +558,13 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
       if (stream_bp[j_l] != 0) {
         const uint64_t n_l = sdb[j_l + 1] - sdb[j_l];
         const unsigned long long fr = *reinterpret_cast<volatile unsigned long long *>(frontier + j_l);
-        const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j_l);
-        const unsigned long long fl =
-            *reinterpret_cast<volatile unsigned long long *>(in_flight + j_l);
+        const unsigned long long w = *reinterpret_cast<volatile unsigned long long *>(prog + j_l);
         const unsigned long long lim =
             ready_seen ? (unsigned long long)tokens_needed(
                              *reinterpret_cast<const volatile int32_t *>(cum_last + j_l), G, T,
                              need_num ? need_num[j_l] : need_num_all)
                        : (pre_cap ? pre_cap[j_l] : ~0ull);
-        live = fr < n_l && take_more(done, fl, lim, inflight_share(stream_bp[j_l], want_heldout));
+        live = fr < n_l && (w >> 16) <= lim;
       }
     }
     }
@@ -586,12 +592,9 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                 *reinterpret_cast<const volatile int32_t *>(cum_last + j), G, T,
                 need_num ? need_num[j] : need_num_all);
         }
-        const unsigned long long done = *reinterpret_cast<volatile unsigned long long *>(kept + j);
-        const unsigned long long fl = *reinterpret_cast<volatile unsigned long long *>(in_flight + j);
+        const unsigned long long w = *reinterpret_cast<volatile unsigned long long *>(prog + j);
         const unsigned long long lim = ready_seen ? need : cap;
-        base = take_more(done, fl, lim, inflight_share(bp, want_heldout))
-                   ? atomicAdd(frontier + j, (unsigned long long)kGrab)
-                   : N;
+        base = ((w >> 16) <= lim) ? atomicAdd(frontier + j, (unsigned long long)kGrab) : N;
       }
       base = __shfl_sync(0xffffffffu, base, 0);
       if (base >= N) break;
@@ -605,10 +608,11 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
         L_l = klen[idx];
         if (L_l) o_l = __ldg(offs + order[idx]);
       }
-      // the grab's tokens are in flight until its decisions are counted
-      {
+      // the grab is in flight until its decisions are counted
+      const uint32_t share = grab_share(bp, want_heldout);
+      if (share) {
         const unsigned long long raw = warp_sum_u64(L_l);
-        if (lane == 0 && raw) atomicAdd(in_flight + j, raw);
+        if (lane == 0 && raw) atomicAdd(prog + j, (grab_estimate(raw, share) << 16) + 1);
       }
       uint64_t mine = 0;  // lane q: the token-term sum of document q
       for (int q = 0; q < (int)(pend - base); q++) {
@@ -631,13 +635,15 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
       kept_here = warp_sum_u64(kept_here);
       const unsigned long long raw_here = warp_sum_u64(L_l);
       if (lane == 0 && raw_here) {
-        if (kept_here) atomicAdd(kept + j, kept_here);
         if (kCopy) atomicAdd(tokens_read, raw_here);
-        // kept first, then out of flight: a warp that sees the grab gone
-        // from in_flight sees its kept tokens
-        __threadfence();
-        atomicAdd(in_flight + j, 0ull - raw_here);
-        __threadfence();
+        // the kept tokens in, the estimate out, one grab fewer in flight
+        // (modulo 2^64: the word's count holds this grab, so nothing
+        // borrows from the tokens)
+        const uint32_t sh = grab_share(bp, want_heldout);
+        if (sh)
+          atomicAdd(prog + j, ((kept_here - grab_estimate(raw_here, sh)) << 16) - 1ull);
+        else if (kept_here)
+          atomicAdd(prog + j, kept_here << 16);
       }
     }
     }
@@ -1563,9 +1569,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t D0, const uint32_t *order, uint32_t *klen,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
-                               unsigned long long *frontier, unsigned long long *kept,
-                               unsigned long long *in_flight, uint32_t j_begin,
-                               uint32_t j_count, const uint16_t *need_num,
+                               unsigned long long *frontier, unsigned long long *prog,
+                               uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
                                uint32_t need_num_all, const unsigned long long *pre_cap,
                                int n_sms, cudaStream_t st) {
   if (j_count == 0) return cudaSuccess;
@@ -1576,8 +1581,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
 #define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
   hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
       tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, \
-      ready_at, T, G, hash_key, want_heldout, frontier, kept, in_flight, j_begin, j_count,      \
-      need_num, need_num_all, pre_cap)
+      ready_at, T, G, hash_key, want_heldout, frontier, prog, j_begin, j_count, need_num,       \
+      need_num_all, pre_cap)
   if (copy_dst) {
     if (j_count > kChunkFrom)
       NS_HASH_LAUNCH(true, true);

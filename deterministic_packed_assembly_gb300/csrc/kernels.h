@@ -68,9 +68,8 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t D0, const uint32_t *order, uint32_t *klen,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
                                uint32_t T, uint32_t G, uint64_t hash_key, uint32_t want_heldout,
-                               unsigned long long *frontier, unsigned long long *kept,
-                               unsigned long long *in_flight, uint32_t j_begin,
-                               uint32_t j_count, const uint16_t *need_num,
+                               unsigned long long *frontier, unsigned long long *prog,
+                               uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
                                uint32_t need_num_all, const unsigned long long *pre_cap,
                                int n_sms, cudaStream_t st);
 // need_num: the fraction (of 1024) of each stream's bound the second hash

@@ -103,6 +103,7 @@ extern "C" {
 #define NS_MAX_STRATA_PER_SOURCE 1024u
 #define NS_MAX_STREAMS 65536u
 #define NS_MAX_WINDOW_SEGMENT (1u << 24)
+#define NS_MAX_TOKENS (1ull << 47)   /* n_tokens must be below this */
 
 typedef struct ns_pack_ctx ns_pack_ctx;
 
@@ -118,7 +119,7 @@ typedef struct {
    * contiguous runs of tokens: document d is tokens[doc_offsets[d] ..
    * doc_offsets[d+1]).  Device tokens must be 16-byte aligned. */
   const int32_t *tokens;
-  uint64_t n_tokens;
+  uint64_t n_tokens;          /* < NS_MAX_TOKENS */
   const int64_t *doc_offsets; /* [n_docs + 1], nondecreasing, lengths < 2^31 */
   const int32_t *loss_start;  /* [n_docs] or NULL: a token at in-document
                                  offset o is learned iff o >= loss_start[d];

@@ -275,6 +275,46 @@ def test_speculated_hash_bound_falls_short_and_init_runs_again():
     hp.check()
 
 
+@pytest.mark.parametrize("host", [False, True])
+def test_hash_carries_a_stream_on_when_grabs_in_flight_keep_less_than_counted(host):
+    # the held-out hash counts each grab in flight as keeping the stream's
+    # expected fraction less 1/8 (here 10 % held out: 0.775) and takes no
+    # more grabs once that count reaches the stream's need.  This stream's
+    # shuffled positions [0, 40000) hold kept documents, the next 4000
+    # held-out ones and the rest kept ones again, all of 16 tokens (four to a
+    # window of 64).  The horizon's 10,000 windows hold exactly the first
+    # 40000 and the need is one kept token more, so the grabs in flight at
+    # the stop keep less than counted: the warp that decides the last of them
+    # has to carry the stream through the held-out block on its own until a
+    # kept document is decided.  Tables and rows are the oracle's
+    T, L, seed, bp, key = 64, 16, 5, 1000, 0
+    n_a, n_h, n_b = 40000, 4000, 16000
+    N = n_a + n_h + n_b
+    rng = np.random.default_rng(11)
+    tokens = np.zeros((N, L), np.int32)
+    for p in range(N):
+        want = n_a <= p < n_a + n_h
+        while True:
+            t = rng.integers(0, 50000, size=L).astype(np.int32)
+            if oracle.is_heldout(oracle.doc_hash(t, key), bp) == want:
+                break
+        tokens[oracle.feistel_pi(seed, 0, N, p)] = t
+    c = corpus_from_lengths(np.full(N, L), T=T, B=100, max_steps=100, heldout_bp=[bp],
+                            seed=seed, hash_key=key, tokens=tokens.ravel())
+    o = oracle_for(c)
+    assert int(o.heldout()[0].sum()) == n_h
+    assert o.valid_steps == 100
+    if host:
+        _poison_cache()
+        pk = _host_packer(c, True)
+    else:
+        pk = packer_for(c)
+    assert pk.info["init_passes"] == 1
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=25)
+    pk.check()
+
+
 @pytest.mark.parametrize("name", ["c2s", "c3s"])
 def test_step_learned_counts(name):
     # each update's learned positions: the sum of its rows' counts, in 64
@@ -627,6 +667,34 @@ def test_host_corpus_reads_only_the_reachable_prefix(name):
     tokens_read = pk.info["host_bytes"] - meta
     used = sum(int((o.rows(k)["doc"] >= 0).sum()) for k in range(o.valid_steps)) * 4
     assert used <= tokens_read < 0.5 * c.n_tokens * 4, (used, tokens_read, c.n_tokens * 4)
+
+
+@pytest.mark.parametrize("name,limit", [("c3m", 1.2), ("c3s", 1.5)])
+def test_host_corpus_hashes_little_past_the_need(name, limit):
+    # the held-out hash stops each stream a little past the kept tokens its
+    # windows need: the speculated margin, and the grabs still in flight when
+    # the need is met (counted before a warp takes another, so the warps that
+    # pile onto the last streams do not each add one).  The tokens it reads
+    # from host memory stay within a fixed factor of the raw tokens of the
+    # prefixes the horizon's windows take
+    c = make_preset(name)
+    pk = _host_packer(c, True)
+    o = oracle_for(c)
+    _, cum, _ = o.quota()
+    bp = np.asarray(c.source_heldout_bp, np.float64)
+    need = 0.0
+    for j in range(c.n_streams):
+        rmax = int(cum[-1, j])
+        if rmax == 0:
+            continue
+        _, _, ln = o.pieces(j)
+        wf = o.window_first(j)
+        kept = int(ln[:int(wf[min(rmax, len(wf) - 1)])].astype(np.int64).sum())
+        need += kept / (1.0 - bp[c.stream_source[j]] / 1e4)
+    read = pk.info["host_bytes"] - (c.n_docs + 1) * 8
+    ratio = read / (4.0 * need)
+    print(f"{name}: read {read} B, need {4.0 * need:.4g} B, ratio {ratio:.4f}")
+    assert 0.97 <= ratio <= limit, ratio
 
 
 def _raw_config(c, tok, off, alloc, free, **flags):
