@@ -1577,7 +1577,10 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
   ++launch_counter();
   // more streams than this: the warps look at them 32 at a time
   constexpr uint32_t kChunkFrom = 64;
-  const dim3 grid(n_sms * kHashBlocksPerSM), block(kHashThreads);
+  // at most one grab in flight a warp: fewer warps than the progress word's
+  // 16-bit count holds
+  constexpr int kMaxBlocks = 0xFFFF / (kHashThreads / 32);
+  const dim3 grid(min(n_sms * kHashBlocksPerSM, kMaxBlocks)), block(kHashThreads);
 #define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
   hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
       tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, \

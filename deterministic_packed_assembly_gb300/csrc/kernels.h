@@ -61,7 +61,11 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
 // copy_dst non-null: tokens is host memory the device can address, and
 // every hashed document is also written to copy_dst (tokens_read counts them).
 // pre_cap (per stream kept tokens, or NULL): where a stream stops before the
-// quota table is known
+// quota table is known.  frontier and prog (per stream, zeroed before the
+// first round, carried into the second): the next position to grab, and the
+// progress word (decided kept tokens plus estimates of the grabs in flight,
+// in bits 16 and up; the grabs in flight below).  The grid is n_sms times the
+// hash's CTAs per SM: fewer than 2^16 warps, so the word's count cannot wrap
 cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                unsigned long long *tokens_read, const int64_t *offs,
                                const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
