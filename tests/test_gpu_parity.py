@@ -420,6 +420,32 @@ def test_validation_stream(name):
     assert packer_for(c, drain=True).order_digest != pk.order_digest
 
 
+@pytest.mark.parametrize("heldout", [False, True])
+def test_heldout_rates_around_the_in_flight_estimate_bounds(heldout):
+    # the held-out hash counts a grab in flight as keeping its stream's
+    # expected fraction less 1/8, and nothing for a stream that keeps at most
+    # 1/8: sources on both sides of that bound (kept fractions 1249, 1250 and
+    # 1251 of 10000, of the training or of the validation stream) and far
+    # from it, each a stream of 20,000 documents.  Tables and rows of every
+    # update are the oracle's
+    keep = [9999, 8751, 8750, 8749, 5000, 1251, 1250, 1249]
+    bps = [k if heldout else 10000 - k for k in keep]
+    rng = np.random.default_rng(99)
+    n = 20000
+    lengths = np.clip(np.rint(200 * np.exp(rng.standard_normal(n * len(bps)))), 1, 2048)
+    c = corpus_from_lengths(lengths.astype(np.int64), T=512, B=8 * len(bps), max_steps=200,
+                            stream_docs=[n] * len(bps), heldout_bp=bps, seed=17, hash_key=5,
+                            drain=True,
+                            tokens=rng.integers(0, 32000, size=int(lengths.sum())))
+    kw = dict(heldout_only=heldout, drain=True)
+    o = oracle_for(c, **kw)
+    pk = packer_for(c, **kw)
+    _check_tables(pk, o, c)
+    assert o.valid_steps == 200
+    compare_steps(pk, o, range(o.valid_steps), launch=16)
+    pk.check()
+
+
 @pytest.mark.parametrize("case", range(20))
 def test_validation_stream_random_tiny_corpora(case):
     rng = np.random.default_rng(7000 + case)
