@@ -184,14 +184,18 @@ __device__ __forceinline__ TileMeta tile_issue(const GatherParams &p, const PV &
       const uint32_t tp = t0 + 4u * lane;
       const int32_t last = P.used - 1;
       int32_t t = min((int32_t)tp, last);
-      Piece q = P.get(P.find_lane(t));
+      int32_t qi = P.find_lane(t);
+      Piece q = P.get(qi);
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         t = min((int32_t)tp + e, last);
         const bool same = t < q.end;
         if (!__all_sync(0xffffffffu, same)) {
-          const Piece nq = P.get(P.find_lane(t));
-          if (!same) q = nq;
+          const Piece nq = P.get(same ? qi : qi + 1);
+          if (!same) {
+            q = nq;
+            qi++;
+          }
         }
         if ((int32_t)tp + e <= last && tp < p.T)
           cp_async4(buf + 4 * lane + e, p.tokens + q.src + (t - q.start));
@@ -239,15 +243,20 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
     int32_t e0[4], e1[4], e2[4];
     const int32_t last = P.used - 1;
     int32_t t = min((int32_t)tp, last);
-    Piece pc = P.get(P.find_lane(t));
+    int32_t qi = P.find_lane(t);
+    Piece pc = P.get(qi);
 #pragma unroll
     for (int e = 0; e < 4; e++) {
       t = min((int32_t)tp + e, last);
       const bool same = t < pc.end;
       if (!__all_sync(0xffffffffu, same)) {
-        const int32_t q = P.find_lane(t);
-        const Piece nq = P.get(q);
-        if (!same) pc = nq;
+        // positions rise one at a time and no piece of a window is empty:
+        // one past a piece's end is the next piece's start
+        const Piece nq = P.get(same ? qi : qi + 1);
+        if (!same) {
+          pc = nq;
+          qi++;
+        }
       }
       const int32_t x = t - pc.start;
       const bool real = (int32_t)tp + e <= last && tp < p.T;
