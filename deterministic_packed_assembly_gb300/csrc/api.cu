@@ -507,6 +507,28 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
 
+  // Each stream's windows over the horizon estimated from the recipe (its
+  // share of every piece's rows, a few windows over): the quota rule keeps
+  // every cumulative count within one window of its share.  Only how much of
+  // a stream is shuffled and hashed before its exact need is known depends
+  // on it.
+  std::vector<double> est_windows(J, 0.0);
+  for (uint32_t p = 0; p < P; p++) {
+    const uint32_t kb = c->piece_begin[p];
+    const uint32_t ke = (p + 1 < P) ? c->piece_begin[p + 1] : K;
+    double swsum = 0.0;
+    for (uint32_t s2 = 0; s2 < S; s2++) swsum += psw[(size_t)p * S + s2];
+    for (uint32_t s2 = 0; s2 < S; s2++) {
+      double twsum = 0.0;
+      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++) twsum += ptw[(size_t)p * J + j];
+      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++)
+        est_windows[j] += (double)(ke - kb) * c->piece_B[p] * (psw[(size_t)p * S + s2] / swsum) *
+                          (ptw[(size_t)p * J + j] / twsum);
+    }
+  }
+  for (uint32_t j = 0; j < J; j++)
+    est_windows[j] = std::ceil(est_windows[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
+
   // ---- 2. the corpus partition; shuffled order and lengths of every position
   // Every kernel that reads tokens checks the offsets it uses, so a malformed
   // partition is reported (BAD_INPUT) at the next readback, never read past.
@@ -530,14 +552,33 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(pex);
   NS_ALLOC(scan_scratch);
   NS_CK(nsk::launch_stream_keys(c->seed, J, keys, st));
+  // A stream without a held-out rate (nothing to hash) needs only the
+  // shuffled positions whose documents hold its horizon's tokens: on the
+  // first pass about that many are taken (a quarter over the recipe's
+  // estimate), the others keep length 0.  A stream whose windows turn out to
+  // need more is caught after the cutoff, and the context is built again
+  // with every position.
+  uint32_t *pos_lim = nullptr;
+  if (c->speculate && !heldout_mode) {
+    std::vector<unsigned long long> est_tok(J);
+    for (uint32_t j = 0; j < J; j++) est_tok[j] = (unsigned long long)(est_windows[j] * T);
+    void *d_est;
+    if ((rc = upload(a, est_tok.data(), J * sizeof(unsigned long long), &d_est, st))) return rc;
+    pos_lim = a.temp<uint32_t>(J);
+    NS_ALLOC(pos_lim);
+    NS_CK(nsk::launch_order_bound(static_cast<uint32_t *>(d_sdb), c->offs, J,
+                                  static_cast<uint16_t *>(d_stream_bp),
+                                  static_cast<unsigned long long *>(d_est), pos_lim, st));
+    NS_CK(cudaMemsetAsync(klen, 0, std::max<uint64_t>(n_pos, 1) * sizeof(uint32_t), st));
+  }
   {
     std::vector<uint32_t> bb = seg_layout(N, 256 * nsk::order_positions_per_thread());
     void *d_bb;
     if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
     nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
-                            heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr, order,
-                            klen, c->err, st));
+                            heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr,
+                            pos_lim, order, klen, c->err, st));
   }
 
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
@@ -567,30 +608,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     need_num = a.temp<uint16_t>(J);
     NS_ALLOC(need_num);
     // Until the quota kernel publishes each stream's need, the first round
-    // stops a stream at an estimate of it from the recipe (its share of the
-    // horizon's rows, a few windows over), not at no bound at all: a small
-    // stream is then not hashed far past its need while the quotas run.  A
-    // heuristic only: the second round hashes every stream to its exact
-    // bound whatever the first one did.
-    std::vector<double> est(J, 0.0);
-    for (uint32_t p = 0; p < P; p++) {
-      const uint32_t kb = c->piece_begin[p];
-      const uint32_t ke = (p + 1 < P) ? c->piece_begin[p + 1] : K;
-      double swsum = 0.0;
-      for (uint32_t s2 = 0; s2 < S; s2++) swsum += psw[(size_t)p * S + s2];
-      for (uint32_t s2 = 0; s2 < S; s2++) {
-        double twsum = 0.0;
-        for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++) twsum += ptw[(size_t)p * J + j];
-        for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++)
-          est[j] += (double)(ke - kb) * c->piece_B[p] * (psw[(size_t)p * S + s2] / swsum) *
-                    (ptw[(size_t)p * J + j] / twsum);
-      }
-    }
+    // stops a stream at half its recipe estimate (est_windows), not at no
+    // bound at all: a small stream is then not hashed far past its need while
+    // the quotas run.  A heuristic only: the second round hashes every stream
+    // to its exact bound whatever the first one did.
     std::vector<unsigned long long> cap(J);
-    for (uint32_t j = 0; j < J; j++) {
-      double w = std::ceil(est[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
-      cap[j] = (unsigned long long)(0.5 * w * (double)T);
-    }
+    for (uint32_t j = 0; j < J; j++)
+      cap[j] = (unsigned long long)(0.5 * est_windows[j] * (double)T);
     void *d_cap;
     if ((rc = upload(a, cap.data(), J * sizeof(unsigned long long), &d_cap, st))) return rc;
     pre_cap = static_cast<unsigned long long *>(d_cap);
@@ -656,6 +680,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   std::vector<int64_t> np_h(J), nb_h(J + 1), pt_h(J);
   std::vector<uint16_t> num_h(J, 1024);
   std::vector<int32_t> rmax32(J);
+  std::vector<uint32_t> lim_h(pos_lim ? J : 0);
   int err_host = 0;
   NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
@@ -666,10 +691,16 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                           st));
   NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
                         cudaMemcpyDeviceToHost, st));
+  if (pos_lim)
+    NS_CK(cudaMemcpyAsync(lim_h.data(), pos_lim, J * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
   if (err_host == nsk::kDevBadOffsets) return NS_ERR_BAD_INPUT;
   if (err_host != 0) return NS_ERR_DEVICE;
+  // a stream shuffled only in part whose windows need more than that part
+  // holds: its cutoff runs to the stream's end
+  for (uint32_t j = 0; j < (uint32_t)lim_h.size(); j++)
+    if (lim_h[j] < N[j] && cut_h[j] > lim_h[j]) return kRetryFullBound;
   std::vector<uint64_t> rmax(J);
   std::vector<int64_t> wbase(J + 1, 0);
   for (uint32_t j = 0; j < J; j++) {

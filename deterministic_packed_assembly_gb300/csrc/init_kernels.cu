@@ -895,6 +895,31 @@ __device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, ui
   return (uint32_t)feistel_walk(k, B, i, err);
 }
 
+// The shuffled positions of each stream a first init pass takes: all of a
+// stream the held-out hash reads, else the recipe's estimate of the tokens
+// its windows hold (est_tok) over the stream's mean document length, a
+// quarter and 1024 positions over, at most all of them.  The rest keep
+// length 0; a stream whose windows need more is caught after the cutoff.
+__global__ void order_bound_kernel(const uint32_t *__restrict__ sdb,
+                                   const int64_t *__restrict__ offs, uint32_t J,
+                                   const uint16_t *__restrict__ stream_bp,
+                                   const unsigned long long *__restrict__ est_tok,
+                                   uint32_t *__restrict__ pos_lim) {
+  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= J) return;
+  const uint32_t b = sdb[j], e = sdb[j + 1];
+  const uint64_t N = e - b;
+  uint64_t lim = N;
+  if (stream_bp[j] == 0 && N > 0) {
+    const int64_t tok = offs[e] - offs[b];  // offsets are checked by their own kernel
+    if (tok > 0) {
+      const double want = 1.25 * (double)est_tok[j] * (double)N / (double)tok + 1024.0;
+      if (want < (double)N) lim = (uint64_t)want;
+    }
+  }
+  pos_lim[j] = (uint32_t)lim;
+}
+
 // Each thread takes kOrderPerThread positions of one stream, p0 + m * 256,
 // one after the other, and every pass of its loop is one evaluation of the
 // network for every lane: a lane whose walk lands in range writes that
@@ -906,13 +931,15 @@ __global__ void __launch_bounds__(kThreads)
     order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
                  const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
                  const uint16_t *__restrict__ stream_bp_heldout_mode,
-                 uint32_t *__restrict__ order, uint32_t *__restrict__ klen, int *err) {
+                 const uint32_t *__restrict__ pos_lim, uint32_t *__restrict__ order,
+                 uint32_t *__restrict__ klen, int *err) {
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint32_t b0 = sdb[j];
-  const uint64_t N = sdb[j + 1] - b0;
+  const uint64_t N = sdb[j + 1] - b0;  // the permutation's domain
+  const uint64_t Nb = pos_lim ? pos_lim[j] : N;  // the positions taken
   const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
-  if (p0 >= N) return;
+  if (p0 >= Nb) return;
   uint32_t bits = (N <= 1) ? 0u : (uint32_t)(64 - __clzll((long long)(N - 1)));
   if (bits < 2) bits = 2;
   bits += bits & 1u;
@@ -940,7 +967,7 @@ __global__ void __launch_bounds__(kThreads)
       order[idx] = d;
       klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
       p += blockDim.x;
-      if (++m >= kOrderPerThread || p >= N) break;
+      if (++m >= kOrderPerThread || p >= Nb) break;
       x = p;
       it = 0;
     } else {
@@ -1630,14 +1657,24 @@ cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
   return cudaGetLastError();
 }
 
+cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_t J,
+                               const uint16_t *stream_bp, const unsigned long long *est_tok,
+                               uint32_t *pos_lim, cudaStream_t st) {
+  ++launch_counter();
+  order_bound_kernel<<<(J + kThreads - 1) / kThreads, kThreads, 0, st>>>(sdb, offs, J, stream_bp,
+                                                                          est_tok, pos_lim);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
-                         const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
-                         int *err, cudaStream_t st) {
+                         const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
+                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
   order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, n_tokens, D0,
-                                                stream_bp_heldout_mode, order, klen, err);
+                                                stream_bp_heldout_mode, pos_lim, order, klen,
+                                                err);
   return cudaGetLastError();
 }
 

@@ -53,10 +53,16 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 // stream_bp_heldout_mode: null for the training stream; for the validation
 // stream the per-stream rates (a stream of a source that holds nothing out
 // keeps nothing)
+// pos_lim (per stream, or NULL: every position): the shuffled positions
+// taken, from launch_order_bound; the others are left as they are
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
-                         const uint16_t *stream_bp_heldout_mode, uint32_t *order, uint32_t *klen,
-                         int *err, cudaStream_t st);
+                         const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
+                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st);
+// est_tok: per stream, the recipe's estimate of the tokens its windows hold
+cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_t J,
+                               const uint16_t *stream_bp, const unsigned long long *est_tok,
+                               uint32_t *pos_lim, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 // copy_dst non-null: tokens is host memory the device can address, and
 // every hashed document is also written to copy_dst (tokens_read counts them).

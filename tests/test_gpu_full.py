@@ -67,6 +67,9 @@ def _tables(pk, o, c):
 @pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
 def test_full_size_sampled_updates(name):
     c, pk, o = _setup(name)
+    # one init pass: neither the held-out hash's speculated bound nor the
+    # shuffle of only the estimated prefix falls short on these workloads
+    assert pk.info["init_passes"] == 1
     _tables(pk, o, c)
     v = o.valid_steps
     assert v > 0

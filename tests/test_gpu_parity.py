@@ -315,6 +315,36 @@ def test_hash_carries_a_stream_on_when_grabs_in_flight_keep_less_than_counted(ho
     pk.check()
 
 
+@pytest.mark.parametrize("host", [False, True])
+def test_partial_shuffle_falls_short_and_init_runs_again(host):
+    # a stream without a held-out rate is shuffled, on the first init pass,
+    # only as far as the recipe's estimate of its windows' tokens over its
+    # mean document length (a quarter and 1024 positions over).  Here its
+    # first 20,000 shuffled positions hold 1-token documents and the other
+    # 40,000 documents of 64 (one window each): the mean (43 tokens) puts
+    # the 400 windows the horizon reads within about 1,800 positions, but
+    # they take about 20,100.  The shortfall is caught after the cutoff and
+    # the context is built again with every position -- same tables, same rows
+    T, seed = 64, 9
+    n_short, n_long = 20000, 40000
+    N = n_short + n_long
+    lengths = np.zeros(N, np.int64)
+    for p in range(N):
+        lengths[oracle.feistel_pi(seed, 0, N, p)] = 1 if p < n_short else 64
+    c = corpus_from_lengths(lengths, T=T, B=8, max_steps=50, seed=seed)
+    o = oracle_for(c)
+    assert o.valid_steps == 50
+    if host:
+        _poison_cache()
+        pk = _host_packer(c, True)
+    else:
+        pk = packer_for(c)
+    assert pk.info["init_passes"] == 2
+    _check_tables(pk, o, c)
+    compare_steps(pk, o, range(o.valid_steps), launch=10)
+    pk.check()
+
+
 @pytest.mark.parametrize("name", ["c2s", "c3s"])
 def test_step_learned_counts(name):
     # each update's learned positions: the sum of its rows' counts, in 64
