@@ -662,7 +662,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)
   const uint32_t chunk = wrap ? 0x80000000u : T;
-  NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes, st));
+  NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes,
+                                static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, st));
 
   // ---- 4. the prefix of each stream the horizon reaches -------------------
   uint32_t *cutoff = a.temp<uint32_t>(J);
@@ -674,7 +675,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(ptokens);
   NS_ALLOC(node_base);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
-                           T, c->G, need_num, cutoff, npieces, ptokens, st));
+                           T, c->G, need_num, pos_lim, cutoff, npieces, ptokens, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
   std::vector<uint32_t> cut_h(J);
   std::vector<int64_t> np_h(J), nb_h(J + 1), pt_h(J);

@@ -985,10 +985,43 @@ constexpr int kScanWarps = 8;
 constexpr int kScanRounds = 8;
 constexpr int kScanTile = kScanWarps * kScanRounds * 32;
 
+// Tiles of the scans that lie wholly inside the unshuffled part of a stream
+// shuffled only in part: positions (b_j + pos_lim_j, e_j) of stream j, whose
+// lengths are 0 and whose prefix sums nothing reads (the cutoff reads them
+// up to b_j + pos_lim_j, and at the stream's end, which is the next
+// stream's start).  The scans neither read nor write them.
+__global__ void scan_tile_zero_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
+                                      const uint32_t *__restrict__ pos_lim, uint64_t n,
+                                      uint64_t nb, uint8_t *__restrict__ tile_zero) {
+  const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= nb) return;
+  const uint64_t t0 = t * kScanTile, t1 = min(n, t0 + kScanTile);
+  // the stream holding position t0: the last j whose range starts at or
+  // before it (empty streams sharing that start come first)
+  uint32_t lo = 0, hi = J;  // invariant: sdb[lo] - D0 <= t0
+  while (hi - lo > 1) {
+    const uint32_t mid = lo + (hi - lo) / 2;
+    if ((uint64_t)(sdb[mid] - D0) <= t0)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const uint64_t b = sdb[lo] - D0, e = sdb[lo + 1] - D0;
+  tile_zero[t] = (t0 >= b + (uint64_t)pos_lim[lo] + 1 && t1 <= e) ? 1 : 0;
+}
+
 __global__ void __launch_bounds__(kScanWarps * 32)
     scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
-                       int64_t *__restrict__ bs_a, int64_t *__restrict__ bs_b) {
+                       const uint8_t *__restrict__ tile_zero, int64_t *__restrict__ bs_a,
+                       int64_t *__restrict__ bs_b) {
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
+  if (tile_zero && tile_zero[blockIdx.x]) {
+    if (threadIdx.x == 0) {
+      bs_a[blockIdx.x] = 0;
+      bs_b[blockIdx.x] = 0;
+    }
+    return;
+  }
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
   int64_t a = 0, b = 0;
@@ -1072,9 +1105,11 @@ __global__ void __launch_bounds__(1024)
 
 __global__ void __launch_bounds__(kScanWarps * 32)
     scan_apply_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
-                      const int64_t *__restrict__ bs_a, const int64_t *__restrict__ bs_b,
-                      int64_t *__restrict__ kex, int64_t *__restrict__ pex) {
+                      const uint8_t *__restrict__ tile_zero, const int64_t *__restrict__ bs_a,
+                      const int64_t *__restrict__ bs_b, int64_t *__restrict__ kex,
+                      int64_t *__restrict__ pex) {
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
+  if (tile_zero && tile_zero[blockIdx.x]) return;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
   int64_t a = 0, b = 0;
@@ -1124,6 +1159,7 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
                               const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
                               const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
                               const uint16_t *__restrict__ need_num,
+                              const uint32_t *__restrict__ pos_lim,
                               uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces,
                               int64_t *__restrict__ ptokens) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1134,7 +1170,9 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
   const int64_t need = tokens_needed(cum_last[j], G, T, need_num ? need_num[j] : 1024u);
   uint64_t c = N;
   if (kex[e] - base > need) {
-    uint64_t lo = 1, hi = N;
+    // a stream shuffled only in part meets its need within that part (its
+    // lengths are 0 past it, and the prefix sums there are not written)
+    uint64_t lo = 1, hi = pos_lim ? min(N, (uint64_t)pos_lim[j]) : N;
     while (lo < hi) {
       const uint64_t mid = lo + (hi - lo) / 2;
       if (kex[b + mid] - base > need)
@@ -1680,19 +1718,30 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
 
 size_t scan_scratch_bytes(uint64_t n) {
   const uint64_t nb = (n + kScanTile - 1) / kScanTile;
-  return (size_t)(nb + 1) * 2 * sizeof(int64_t);
+  return (size_t)(nb + 1) * 2 * sizeof(int64_t) + (size_t)(nb + 15) / 16 * 16;
 }
 
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
-                               cudaStream_t st) {
+                               const uint32_t *sdb, uint32_t J, uint32_t D0,
+                               const uint32_t *pos_lim, cudaStream_t st) {
   const uint64_t nb = (n + kScanTile - 1) / kScanTile;
   if (scratch_bytes < scan_scratch_bytes(n)) return cudaErrorInvalidValue;
   int64_t *bs_a = static_cast<int64_t *>(scratch);
   int64_t *bs_b = bs_a + (nb + 1);
+  uint8_t *tile_zero = nullptr;
+  if (pos_lim && nb > 0) {
+    tile_zero = reinterpret_cast<uint8_t *>(bs_b + (nb + 1));
+    ++launch_counter();
+    scan_tile_zero_kernel<<<(unsigned)((nb + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+        sdb, J, D0, pos_lim, n, nb, tile_zero);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (nb > 0) {
     ++launch_counter();
-    scan_reduce_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b);
+    scan_reduce_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, tile_zero, bs_a,
+                                                                 bs_b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1701,17 +1750,18 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nb == 0) return e;
   ++launch_counter();
-  scan_apply_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, bs_a, bs_b, kex, pex);
+  scan_apply_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, tile_zero, bs_a, bs_b,
+                                                               kex, pex);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          const uint16_t *need_num, uint32_t *cutoff, int64_t *npieces,
-                          int64_t *ptokens, cudaStream_t st) {
+                          const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,
+                          int64_t *npieces, int64_t *ptokens, cudaStream_t st) {
   ++launch_counter();
   cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G,
-                                                    need_num, cutoff, npieces, ptokens);
+                                                    need_num, pos_lim, cutoff, npieces, ptokens);
   return cudaGetLastError();
 }
 

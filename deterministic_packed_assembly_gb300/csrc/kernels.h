@@ -101,16 +101,21 @@ cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
                                const int64_t *offs, const int32_t *src, int32_t *dst,
                                unsigned long long *tokens_read, cudaStream_t st);
 uint32_t copy_chunk_tokens();
-// kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n]
+// kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n].
+// pos_lim (per stream, or NULL): streams shuffled only in part, whose
+// positions past b_j + pos_lim_j have length 0; there kex and pex are written
+// only where a tile of the scan reaches into the shuffled part or the next
+// stream (the cutoff reads them up to b_j + pos_lim_j and at stream ends)
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
-                               cudaStream_t st);
+                               const uint32_t *sdb, uint32_t J, uint32_t D0,
+                               const uint32_t *pos_lim, cudaStream_t st);
 size_t scan_scratch_bytes(uint64_t n);
 // per stream: cutoff c_j, pieces and kept tokens before it; rmax given
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
-                          const uint16_t *need_num, uint32_t *cutoff, int64_t *npieces,
-                          int64_t *ptokens, cudaStream_t st);
+                          const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,
+                          int64_t *npieces, int64_t *ptokens, cudaStream_t st);
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st);
 
