@@ -317,7 +317,10 @@ __device__ __forceinline__ int warp_rank128(int64_t hi, uint64_t lo, int count, 
 // per update; at the stratum level D_c = Cs v_c - V_s C_c grows by
 // n v_c - V_s a_c, and the source's n is its floor share or one more, so both
 // floors of the strata are computed once per piece of the schedule (where
-// every count starts again).
+// every count starts again).  With a_c its floor share plus 0 or 1, each of
+// those growths is the remainder of the floor division (below the weight
+// sum, 64 bits) less the weight sum or nothing: the 128-bit shortfalls only
+// ever add 64-bit numbers.
 template <int SMAX, int TMAX>
 __global__ void __launch_bounds__(32)
     quota_warp_kernel(QuotaPieces q, uint32_t S, const uint32_t *__restrict__ src_first,
@@ -338,8 +341,8 @@ __global__ void __launch_bounds__(32)
     const uint64_t V = warp_sum_u64(v);
     const int64_t base = act ? (int64_t)((Bp * v) / V) : 0;
     const int64_t R = (int64_t)Bp - warp_sum_i64(base);
-    const __int128 step_gain = (__int128)Bp * (__int128)v;
-    __int128 delta = step_gain - (__int128)V * (__int128)base;
+    const int64_t rem = (int64_t)(Bp * v - V * (uint64_t)base);  // in [0, V)
+    __int128 delta = rem;
     // stratum level of source s
     const uint64_t w = sact ? q.tw[(size_t)p * J + f0 + lane] : 0;
     const uint64_t Vs = warp_sum_u64(w);
@@ -348,25 +351,29 @@ __global__ void __launch_bounds__(32)
     const int64_t b1 = sact ? (int64_t)(((uint64_t)(bs + 1) * w) / Vs) : 0;
     const int64_t R0 = bs - warp_sum_i64(b0);
     const int64_t R1 = bs + 1 - warp_sum_i64(b1);
+    // n w - V_s * (floor share) for n = bs and n = bs + 1, each in [0, V_s)
+    const int64_t r0 = (int64_t)((uint64_t)bs * w - Vs * (uint64_t)b0);
+    const int64_t r1 = (int64_t)((uint64_t)(bs + 1) * w - Vs * (uint64_t)b1);
     __int128 D = 0;
     for (uint32_t k = k0; k < k1; k++) {
       const int rs = warp_rank128<SMAX>((int64_t)(delta >> 64), (uint64_t)delta, (int)S, lane);
-      const int64_t a = base + ((act && rs < R) ? 1 : 0);
-      delta += step_gain - (__int128)V * (__int128)a;
+      const bool extra = act && rs < R;
+      const int64_t a = base + (extra ? 1 : 0);
+      delta += (__int128)(extra ? rem - (int64_t)V : rem);
       const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
       const bool lo_share = (n == bs);
       const int64_t bsel = lo_share ? b0 : b1;
       const int64_t Rsel = lo_share ? R0 : R1;
-      const __int128 gain = (__int128)n * (__int128)w;
-      const __int128 d2 = D + gain - (__int128)Vs * (__int128)bsel;
+      const __int128 d2 = D + (__int128)(lo_share ? r0 : r1);
       const int rt = warp_rank128<TMAX>((int64_t)(d2 >> 64), (uint64_t)d2, n_st, lane);
-      const int64_t a2 = bsel + ((sact && rt < Rsel) ? 1 : 0);
+      const bool extra2 = sact && rt < Rsel;
+      const int64_t a2 = bsel + (extra2 ? 1 : 0);
       if (sact) {
         quota[(size_t)k * J + f0 + lane] = (int32_t)a2;
         cum[(size_t)k * J + f0 + lane] = (int32_t)Cg;
       }
       Cg += a2;
-      D += gain - (__int128)Vs * (__int128)a2;
+      D = extra2 ? d2 - (__int128)(int64_t)Vs : d2;
     }
   }
   if (sact) cum[(size_t)K * J + f0 + lane] = (int32_t)Cg;
