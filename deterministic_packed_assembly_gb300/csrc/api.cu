@@ -559,7 +559,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // need more is caught after the cutoff, and the context is built again
   // with every position.
   uint32_t *pos_lim = nullptr;
-  if (c->speculate && !heldout_mode) {
+  bool any_unhashed = false;
+  for (uint32_t j = 0; j < J; j++) any_unhashed |= stream_bp[j] == 0 && N[j] > 0;
+  if (c->speculate && !heldout_mode && any_unhashed) {
     std::vector<unsigned long long> est_tok(J);
     for (uint32_t j = 0; j < J; j++) est_tok[j] = (unsigned long long)(est_windows[j] * T);
     void *d_est;
