@@ -361,6 +361,15 @@ __global__ void __launch_bounds__(32)
       const int64_t a = base + (extra ? 1 : 0);
       delta += (__int128)(extra ? rem - (int64_t)V : rem);
       const int64_t n = __shfl_sync(0xffffffffu, a, (int)s);
+      if (TMAX == 1) {
+        // one stratum: it takes all of its source's windows
+        if (sact) {
+          quota[(size_t)k * J + f0 + lane] = (int32_t)n;
+          cum[(size_t)k * J + f0 + lane] = (int32_t)Cg;
+        }
+        Cg += n;
+        continue;
+      }
       const bool lo_share = (n == bs);
       const int64_t bsel = lo_share ? b0 : b1;
       const int64_t Rsel = lo_share ? R0 : R1;
@@ -1605,7 +1614,9 @@ template <int SMAX>
 static void launch_quota_warp_s(QuotaPieces q, uint32_t S, const uint32_t *src_first, uint32_t J,
                                 uint32_t K, uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st) {
-  if (max_strata <= 4)
+  if (max_strata <= 1)
+    quota_warp_kernel<SMAX, 1><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
+  else if (max_strata <= 4)
     quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
   else if (max_strata <= 8)
     quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
