@@ -194,3 +194,139 @@ def test_order_digest():
     c2 = make_preset("c1")
     c2.source_weight = np.asarray([6, 4], np.uint32)
     assert oracle.Oracle(c2).digest != d0
+
+
+# ---- the row fingerprint's key layout, recovered key by key ------------------
+# fp = mix(sum_t mix(key_t)) with key_t = a_t ^ ((b_t | t << 40) * golden),
+# a_t = (u32 token << 32) | u32 doc and b_t = (mask << 32) | u32 pos.  Un-mixing
+# a one-position row gives its key; in a two-position row whose first position
+# is all zeros (key 0, term mix(0) = the first published SplitMix64 output)
+# the second key follows the same way.  The expected keys are special cases
+# worked out by hand: with b = 0 and t = 0 the key is a itself, and a product
+# of the golden constant with a power of two is a shift of its hex digits.
+# A swapped field, a shift of 32 instead of 40, an OR for the XOR or a missing
+# multiply each gives another key.
+SPLITMIX0 = 0xE220A8397B1DCDAF
+
+
+def _one_pos(tok, pos, doc, mask):
+    return dict(tokens=np.asarray([tok], np.int32), pos=np.asarray([pos], np.int32),
+                doc=np.asarray([doc], np.int32), mask=np.asarray([mask], np.uint8))
+
+
+def _key_t0(tok, pos, doc, mask):
+    return _unmix(_unmix(_fp(_one_pos(tok, pos, doc, mask))))
+
+
+def _key_t1(tok, pos, doc, mask):
+    r = dict(tokens=np.asarray([0, tok], np.int32), pos=np.asarray([0, pos], np.int32),
+             doc=np.asarray([0, doc], np.int32), mask=np.asarray([0, mask], np.uint8))
+    return _unmix((_unmix(_fp(r)) - SPLITMIX0) & M64)
+
+
+@pytest.mark.parametrize("tok,pos,doc,mask,key", [
+    # b = 0, t = 0: the key is (token << 32) | doc
+    (0x12345678, 0, 0x0BADF00D, 0, 0x123456780BADF00D),
+    (-1, 0, -2, 0, 0xFFFFFFFFFFFFFFFE),
+    (0, 0, -1, 0, 0x00000000FFFFFFFF),
+    # a = 0: pos 1 -> golden; pos 2 -> 2 * golden; mask 1 -> golden << 32
+    (0, 1, 0, 0, 0x9E3779B97F4A7C15),
+    (0, 2, 0, 0, 0x3C6EF372FE94F82A),
+    (0, 0, 0, 1, 0x7F4A7C1500000000),
+    # both halves: (tok << 32 | doc) ^ golden
+    (7, 1, 3, 0, 0x9E3779BE7F4A7C16),
+])
+def test_row_fingerprint_key_at_position_0(tok, pos, doc, mask, key):
+    assert _key_t0(tok, pos, doc, mask) == key
+
+
+@pytest.mark.parametrize("tok,pos,doc,mask,key", [
+    # t = 1 adds 1 << 40 to b: golden << 40
+    (0, 0, 0, 0, 0x4A7C150000000000),
+    (7, 0, 3, 0, 0x4A7C150700000003),
+    # (1 << 40 | 1) * golden = golden + golden << 40
+    (0, 1, 0, 0, 0xE8B38EB97F4A7C15),
+    # (1 << 40 | 1 << 32) * golden = golden << 40 + golden << 32
+    (0, 0, 0, 1, 0xC9C6911500000000),
+])
+def test_row_fingerprint_key_at_position_1(tok, pos, doc, mask, key):
+    assert _key_t1(tok, pos, doc, mask) == key
+
+
+# ---- the order digest, item by item ------------------------------------------
+# digest = mix(sum ^ count), sum = sum_i mix(item_i ^ mix(i)) over the items in
+# their order: the recipe's scalars, each source's weight and held-out rate,
+# each stream's document range, source and weight, the schedule, every valid
+# update's quota row, and then, per stream, the first piece (doc << 32 | offset)
+# of every window the valid updates read, in read order.  The items are taken
+# here from the oracle's read-outs, each pinned on its own (quota tables, the
+# packed pieces and windows, the read order); this checks that the digest
+# covers exactly them.
+def _digest_items(o, c, *, seed, G=0, bucket=0, drain=False, heldout_only=False,
+                  shuffle_rows=False, wrap=False, schedule=None):
+    v = o.valid_steps
+    flags = (1 if drain else 0) | (2 if heldout_only else 0) | (4 if shuffle_rows else 0) | \
+        (8 if wrap else 0)
+    items = [c.T, c.B, c.max_steps, v, flags, c.pad_id & 0xFFFFFFFF, seed, c.hash_key,
+             c.n_sources, c.n_streams, G, bucket]
+    for s in range(c.n_sources):
+        items += [int(c.source_weight[s]), int(c.source_heldout_bp[s])]
+    for j in range(c.n_streams):
+        items += [int(c.stream_doc_begin[j]), int(c.stream_doc_begin[j + 1]),
+                  int(c.stream_source[j]), int(c.stream_weight[j])]
+    if schedule:
+        items.append(len(schedule))
+        for p in schedule:
+            items += [p["begin"], p["B"], *p["source_weight"], *p["stream_weight"]]
+    q, cum, _ = o.quota()
+    for k in range(v):
+        items += [int(x) & M64 for x in q[k]]
+    for j in range(c.n_streams):
+        W = o.n_windows(j)
+        used = min(int(cum[v, j]), W)
+        doc, off, _ = o.pieces(j)
+        first = o.window_first(j)
+        for r in range(used):
+            w = oracle.window_of_rank(seed, j, G, W, r)
+            p = int(first[w])
+            items.append((int(doc[p]) << 32) | int(off[p]))
+    return items
+
+
+def _fold_items(items):
+    acc = 0
+    for i, x in enumerate(items):
+        acc = (acc + oracle.splitmix64((x & M64) ^ oracle.splitmix64(i))) & M64
+    return acc ^ len(items)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(window_segment=3, shuffle_rows=True),
+    dict(drain=True, max_steps=40),
+    dict(heldout_only=True),
+    dict(wrap=True, len_bucket=64),
+])
+def test_order_digest_covers_exactly_its_items(kw):
+    c = make_preset("c1")
+    if "max_steps" in kw:
+        c.max_steps = kw.pop("max_steps")
+    o = oracle.Oracle(c, **kw)
+    assert o.valid_steps > 0
+    items = _digest_items(o, c, seed=c.seed, G=kw.get("window_segment", 0),
+                          bucket=kw.get("len_bucket", 0), drain=kw.get("drain", False),
+                          heldout_only=kw.get("heldout_only", False),
+                          shuffle_rows=kw.get("shuffle_rows", False), wrap=kw.get("wrap", False))
+    assert _unmix(o.digest) == _fold_items(items)
+
+
+def test_order_digest_covers_a_schedule():
+    c = corpus_from_lengths([5, 9, 3, 12, 7, 2, 8, 4] * 6, T=16, B=4, max_steps=6,
+                            stream_docs=[16, 16, 16], stream_source=[0, 0, 1],
+                            source_weight=[2, 1], stream_weight=[1, 1, 1])
+    sched = [dict(begin=0, B=4, source_weight=[2, 1], stream_weight=[1, 1, 1]),
+             dict(begin=3, B=3, source_weight=[1, 1], stream_weight=[1, 2, 1])]
+    o = oracle.Oracle(c, schedule=sched)
+    assert o.valid_steps > 3
+    items = _digest_items(o, c, seed=c.seed, schedule=sched)
+    assert _unmix(o.digest) == _fold_items(items)
