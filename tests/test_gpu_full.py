@@ -3,18 +3,24 @@ times (its auto_launch updates per ns_pack_step launch -- 128 for the three
 large workloads, the whole horizon for the small-batch ones -- all rows of
 the global batch).
 
-Sampled updates are compared element by element with the oracle; whole-pass
-properties (valid horizon, order digest, quota tables, exactly-once coverage
-of a full long-context pass, learned counts of every SFT update) are checked
-at any size.  The elastic-determinism workload is also assembled in R = 8, 16,
-32 and 64 row slices ("Zephon: deterministic data loading": the SHA-256 of
-every global batch matches byte for byte at any GPU count).
+Every update of every workload is compared with the oracle on its row
+fingerprints, learned counts, batch fingerprint and update learned count;
+updates at launch boundaries and a few more are compared element by element.
+Whole-pass properties (valid horizon, order digest, quota tables, exactly-once
+coverage of a full long-context pass) are checked at any size.  Every update
+of the elastic-determinism workload is also assembled in R = 8, 16, 32 and 64
+row slices and compared byte for byte with the one-launch batch ("Zephon:
+deterministic data loading": the SHA-256 of every global batch matches byte
+for byte at any GPU count).
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import oracle
-from _gpu import assert_rows_equal, batch_sha256, oracle_for, packer_for, to_host
+from _gpu import FIELDS, assert_rows_equal, batch_sha256, oracle_for, packer_for, to_host
 from corpus import make_preset
+from deterministic_packed_assembly_gb300 import as_u64
 
 pytestmark = pytest.mark.gpu
 
@@ -94,36 +100,104 @@ def test_full_size_mixture_within_two_windows():
     assert (src.sum(1) == c.B).all()
 
 
-def test_full_size_sft_learned_counts_every_update():
-    c, pk, o = _setup("c2")
+def _oracle_summaries(o, steps, full_rows=()):
+    """Per update: the oracle's row fingerprints, row learned counts, batch
+    fingerprint and update learned count, plus the whole rows of the updates
+    in ``full_rows``.  The oracle's calls release the GIL and only read its
+    built state, so updates are assembled on a few host threads; only the
+    summaries are kept."""
+    full_rows = set(full_rows)
+
+    def one(k):
+        r = o.rows(k)
+        s = dict(row_fp=r["row_fp"], row_learned=r["row_learned"],
+                 batch_fp=oracle.batch_fp(r["row_fp"]),
+                 learned=int(r["row_learned"].astype(np.int64).sum()))
+        if k in full_rows:
+            s["rows"] = r
+        return k, s
+
+    with ThreadPoolExecutor(8) as ex:
+        return dict(ex.map(one, steps))
+
+
+def _boundary_updates(v, L):
+    """Updates on both sides of the first launch boundaries and of the last."""
+    ks = {0, 1, v // 2, v - 1}
+    for s0 in list(range(L, v, L))[:3] + list(range(L, v, L))[-1:]:
+        ks |= {s0 - 1, s0}
+    return sorted(k for k in ks if 0 <= k < v)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_full_size_every_update(name):
+    # the whole horizon (c5: the drained full pass) in the benchmark's
+    # launches; every update's row fingerprints, learned counts and batch
+    # fingerprint equal the oracle's, and the updates at launch boundaries
+    # equal it element by element
+    c, pk, o = _setup(name)
     v = o.valid_steps
     L = _launch(c)
+    full = _boundary_updates(v, L)
+    want = _oracle_summaries(o, range(v), full)
+    seen = 0
     for s0 in range(0, v, L):
         n = min(L, v - s0)
         out = pk.step(s0, n_steps=n)
+        bfp = as_u64(pk.batch_fp_many(out["row_fp"]))
+        upd = pk.step_learned(out["row_learned"]).cpu().numpy()
+        got_fp = as_u64(out["row_fp"])
         got_l = out["row_learned"].cpu().numpy()
-        got_fp = out["row_fp"].cpu().numpy().view(np.uint64)
-        step_l = pk.step_learned(out["row_learned"]).cpu().numpy()
         for q in range(n):
-            want = o.rows(s0 + q)
-            assert (got_l[q] == want["row_learned"]).all(), s0 + q
-            assert (got_fp[q] == want["row_fp"]).all(), s0 + q
-            assert step_l[q] == int(want["row_learned"].astype(np.int64).sum()), s0 + q
+            k = s0 + q
+            w = want[k]
+            assert (got_fp[q] == w["row_fp"]).all(), f"{name} update {k}: row_fp"
+            assert (got_l[q] == w["row_learned"]).all(), f"{name} update {k}: row_learned"
+            assert bfp[q] == w["batch_fp"], f"{name} update {k}: batch fingerprint"
+            assert upd[q] == w["learned"], f"{name} update {k}: learned positions"
+            if "rows" in w:
+                assert_rows_equal(_one(out, q), w["rows"], f"{name} update {k}")
+            seen += 1
+        del out
+    assert seen == v
+    pk.check()
 
 
-def test_full_size_elastic_slices():
+def test_full_size_elastic_slices_every_update():
+    # every update of the elastic-determinism workload assembled once whole
+    # and again as R = 8, 16, 32 and 64 independent row-slice launches into
+    # poisoned buffers: all seven outputs byte-identical on the device, row
+    # fingerprints equal to the oracle's, and the host SHA-256 of the four
+    # [B, T] fields equal for every R on a sample of updates
+    import torch
     c, pk, o = _setup("c4")
-    for k in (0, o.valid_steps - 1):
-        full = to_host(pk.step(k))
-        want = o.rows(k)
-        assert_rows_equal({f: v[0] for f, v in full.items()}, want, f"update {k}")
-        sha = batch_sha256({f: v[0] for f, v in full.items()})
-        for R in (8, 16, 32, 64):
-            parts = [to_host(pk.step(k, rows=(r * c.B // R, (r + 1) * c.B // R)))
-                     for r in range(R)]
-            cat = {f: np.concatenate([p[f][0] for p in parts]) for f in parts[0]}
-            assert batch_sha256(cat) == sha, (k, R)
-            assert (cat["row_fp"] == want["row_fp"]).all()
+    v = o.valid_steps
+    assert v == c.max_steps
+    sha_sample = sorted({0, 1, v // 2, v - 1} | set(range(0, v, 25)))
+    want = _oracle_summaries(o, range(v), sha_sample)
+    Rs = (8, 16, 32, 64)
+    bufs = {R: pk.empty_out(1) for R in Rs}
+    for k in range(v):
+        whole = pk.step(k)
+        for R in Rs:
+            b = bufs[R]
+            for t in b.values():
+                t.fill_(-3)
+            for r in range(R):
+                r0, r1 = r * c.B // R, (r + 1) * c.B // R
+                pk.step(k, rows=(r0, r1), out={f: t[:, r0:r1] for f, t in b.items()})
+            for f in b:
+                assert torch.equal(b[f], whole[f]), (k, R, f)
+        assert (as_u64(whole["row_fp"][0]) == want[k]["row_fp"]).all(), k
+        if k in sha_sample:
+            h = to_host(whole)
+            one = {f: x[0] for f, x in h.items()}
+            assert_rows_equal(one, want[k]["rows"], f"update {k}")
+            sha = batch_sha256(one)
+            for R in Rs:
+                hb = {f: bufs[R][f][0].cpu().numpy() for f in FIELDS}
+                assert batch_sha256(hb) == sha, (k, R)
+    pk.check()
 
 
 def test_full_size_long_context_full_pass_exactly_once():
