@@ -22,11 +22,16 @@
 // calls whose work overlaps on the GPU (different streams, or the same stream
 // from several host threads without ordering) race on it.  Nothing in it has
 // to start at zero: every byte a call reads is written earlier by that call.
+//
+// How the recipe reaches the device: a copy from pageable host memory may
+// wait for the stream's earlier work, and the caller's arrays need not be
+// page-locked.  So the weights travel in the parameter block of small upload
+// kernels (a launch copies its parameters when it is enqueued): the call only
+// enqueues kernels and returns without waiting on the stream.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
-#include <vector>
 
 #include "kernels.h"
 #include "nspack.h"
@@ -62,6 +67,29 @@ int scratch_address(void **out) {
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
+// Words one upload launch carries.  A kernel's parameters may take up to
+// 32,764 bytes on this architecture (CUDA 12.1 or later); 30 KB of words
+// leaves room for the rest of the block.
+constexpr uint32_t kUploadWords = 7680;
+struct UploadBlock {
+  uint32_t *dst;
+  uint32_t n;
+  uint32_t w[kUploadWords];
+};
+static_assert(sizeof(UploadBlock) <= 32000, "upload block beyond the parameter limit");
+
+// dst[i] = w[i] for i < n.  __grid_constant__ lets the threads index the
+// parameter block where it lies instead of each taking a private copy.
+__global__ void __launch_bounds__(256) upload_words_kernel(const __grid_constant__ UploadBlock b) {
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < b.n; i += gridDim.x * blockDim.x)
+    b.dst[i] = b.w[i];
+}
+
+// Per host thread, so that calls from several threads do not share them (the
+// device scratch is shared regardless); fixed size, nothing allocated.
+thread_local UploadBlock tl_block;
+thread_local uint32_t tl_src_first[NS_MAX_SOURCES + 1];
+
 }  // namespace
 
 extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_sources,
@@ -73,7 +101,7 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
     return NS_ERR_INVALID_ARG;
   if (S == 0 || S > NS_MAX_SOURCES || J == 0 || J > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
   if (B == 0 || K == 0 || (uint64_t)K * B >= (1ull << 31)) return NS_ERR_INVALID_ARG;
-  std::vector<uint32_t> src_first(S + 1, 0);
+  uint32_t *src_first = tl_src_first;
   uint32_t max_strata = 0;
   for (uint32_t s = 0; s < S; s++)
     if (source_weight[s] == 0) return NS_ERR_INVALID_ARG;
@@ -90,14 +118,13 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
     if (n > max_strata) max_strata = n;
   }
   const bool one_warp = S <= 32 && max_strata <= 32;
-  // scratch layout: source weights | stream weights | source -> first stream
-  // | the horizon as one piece (begin 0, B) | (beyond one warp) sources'
-  // windows per update
-  const size_t o_sw = 0;
-  const size_t o_tw = o_sw + round256((size_t)S * 4);
-  const size_t o_sf = o_tw + round256((size_t)J * 4);
-  const size_t o_pc = o_sf + round256((size_t)(S + 1) * 4);  // one piece: begin 0, B
-  const size_t o_sq = o_pc + 256;
+  // scratch layout, in 32-bit words from the start: source weights [S] |
+  // stream weights [J] | source -> first stream [S + 1] | the horizon as one
+  // piece (begin 0, B); then, 256-byte aligned and only beyond one warp, the
+  // sources' windows per update [K][S]
+  const uint32_t w_sw = 0, w_tw = S, w_sf = S + J, w_pc = 2 * S + J + 1;
+  const uint32_t n_words = w_pc + 2;
+  const size_t o_sq = round256((size_t)n_words * 4);
   const size_t need = o_sq + (one_warp ? 0 : round256((size_t)K * S * 4));
   if (need > NS_NOALLOC_SCRATCH_BYTES) return NS_ERR_INVALID_ARG;
 
@@ -105,21 +132,28 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
   int rc = scratch_address(reinterpret_cast<void **>(&scratch));
   if (rc != NS_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  uint32_t *d_sw = reinterpret_cast<uint32_t *>(scratch + o_sw);
-  uint32_t *d_tw = reinterpret_cast<uint32_t *>(scratch + o_tw);
-  uint32_t *d_sf = reinterpret_cast<uint32_t *>(scratch + o_sf);
-  uint32_t *d_pc = reinterpret_cast<uint32_t *>(scratch + o_pc);
-  const uint32_t piece[2] = {0, B};
-  if (cudaMemcpyAsync(d_sw, source_weight, (size_t)S * 4, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(d_tw, stream_weight, (size_t)J * 4, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(d_sf, src_first.data(), (size_t)(S + 1) * 4, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(d_pc, piece, sizeof(piece), cudaMemcpyHostToDevice, st) != cudaSuccess) {
-    cudaGetLastError();
-    return NS_ERR_CUDA;
+  uint32_t *words = reinterpret_cast<uint32_t *>(scratch);
+  // the words of the layout above, uploaded kUploadWords at a time
+  auto word = [&](uint32_t i) -> uint32_t {
+    if (i < w_tw) return source_weight[i - w_sw];
+    if (i < w_sf) return stream_weight[i - w_tw];
+    if (i < w_pc) return src_first[i - w_sf];
+    return i == w_pc ? 0u : B;
+  };
+  UploadBlock &blk = tl_block;
+  for (uint32_t i0 = 0; i0 < n_words; i0 += kUploadWords) {
+    const uint32_t n = (n_words - i0 < kUploadWords) ? n_words - i0 : kUploadWords;
+    blk.dst = words + i0;
+    blk.n = n;
+    for (uint32_t q = 0; q < n; q++) blk.w[q] = word(i0 + q);
+    upload_words_kernel<<<(n + 255) / 256, 256, 0, st>>>(blk);
+    ++nsk::launch_counter();
+    if (cudaGetLastError() != cudaSuccess) return NS_ERR_CUDA;
   }
+  const uint32_t *d_sw = words + w_sw;
+  const uint32_t *d_tw = words + w_tw;
+  const uint32_t *d_sf = words + w_sf;
+  const uint32_t *d_pc = words + w_pc;
   const nsk::QuotaPieces qp{d_pc, d_pc + 1, d_sw, d_tw, 1};
   cudaError_t e;
   if (one_warp) {

@@ -287,7 +287,10 @@ const char *ns_pack_strerror(int code);
  * j in update k (max_steps x n_streams), and cum[k][j], its windows before
  * update k ((max_steps + 1) x n_streams), both int32 -- into device buffers the
  * caller owns, asynchronously on cuda_stream (NULL: the legacy default
- * stream).
+ * stream).  The call only enqueues kernels: the recipe reaches the device in
+ * the parameter blocks of small upload kernels (about 7,680 weights each), so
+ * no copy from pageable memory waits on the stream, and the caller's arrays
+ * may be released as soon as the call returns.
  *
  * Arguments: the recipe's weights on the host (the same meaning and checks as
  * in ns_pack_config: source_weight[n_sources] > 0, stream_source[n_streams]

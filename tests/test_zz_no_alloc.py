@@ -8,7 +8,8 @@ device array shared by every call, so these tests check that two calls in a
 row, through the C ABI, each give exactly the quota tables the allocating
 path (ns_pack_init, read back with ns_pack_quota_table) builds for the same
 recipe -- one recipe within a warp's reach and one that needs the scratch
-table of per-update source windows.  This file is named to run last.
+table of per-update source windows -- and that a call returns without waiting
+for the work already queued on its stream.  This file is named to run last.
 """
 import numpy as np
 import pytest
@@ -73,6 +74,38 @@ def test_two_calls_in_a_row_match_the_allocating_path():
         wq, wc = want[name]
         assert np.array_equal(q, wq), name
         assert np.array_equal(cum, wc), name
+
+
+def test_call_does_not_wait_on_its_stream():
+    # a kernel that keeps the stream busy for about half a second is queued
+    # first; the call must return long before it ends (the recipe travels in
+    # kernel parameters, not in a copy from pageable memory that would wait
+    # for the stream), and its tables must still be right once it has run.
+    # 64 sources x 1000 strata: the upload takes nine launches.
+    import time
+    r = dict(source_weight=[1 + (s % 5) for s in range(64)],
+             stream_source=[s for s in range(64) for _ in range(1000)],
+             stream_weight=[1 + (j % 7) for j in range(64000)], B=4096, max_steps=4)
+    K, J = r["max_steps"], len(r["stream_source"])
+    q_dev = torch.full((K, J), -7, dtype=torch.int32, device="cuda:0")
+    c_dev = torch.full((K + 1, J), -7, dtype=torch.int32, device="cuda:0")
+    st = torch.cuda.current_stream()
+    import deterministic_packed_assembly_gb300 as nsp
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(1e9))  # about 0.5 s at the SM clock
+    t0 = time.perf_counter()
+    nsp.ns_pack_quota_noalloc(r["source_weight"], r["stream_source"], r["stream_weight"],
+                              r["B"], r["max_steps"], q_dev.data_ptr(), c_dev.data_ptr(),
+                              st.cuda_stream)
+    t_call = time.perf_counter() - t0
+    busy = not st.query()
+    torch.cuda.synchronize()
+    t_all = time.perf_counter() - t0
+    assert busy, "the queued kernel ended before the call returned"
+    assert t_call < 0.5 * t_all, (t_call, t_all)
+    q, cum = q_dev.cpu().numpy(), c_dev.cpu().numpy()
+    wq, wc = _tables_by_init(r)
+    assert np.array_equal(q, wq) and np.array_equal(cum, wc)
 
 
 def test_recipe_beyond_the_scratch_is_rejected():
