@@ -93,6 +93,8 @@ class ns_pack_info_t(C.Structure):
         ("init_launches", C.c_uint32),
         ("init_passes", C.c_uint32),
         ("host_bytes", C.c_uint64),
+        ("hashed_tokens", C.c_uint64),
+        ("hashed_docs", C.c_uint64),
     ]
 
 

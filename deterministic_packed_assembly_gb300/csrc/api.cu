@@ -39,6 +39,7 @@ struct ns_pack_ctx {
   uint32_t valid_steps = 0, levels = 0, init_launches = 0;
   uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
   uint64_t host_bytes = 0;  // bytes of a host-resident corpus read at init
+  uint64_t hashed_tokens = 0, hashed_docs = 0;  // what the held-out hash read at init
   bool speculate = true;    // hash to a bound speculated from the measured fill
   uint32_t init_passes = 1;
   // device tables kept for the per-update calls
@@ -621,6 +622,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     if ((rc = upload(a, cap.data(), J * sizeof(unsigned long long), &d_cap, st))) return rc;
     pre_cap = static_cast<unsigned long long *>(d_cap);
   }
+  unsigned long long *hashed = nullptr;  // tokens and documents hashed
+  if (any_heldout) {
+    hashed = a.temp<unsigned long long>(2);
+    NS_ALLOC(hashed);
+    NS_CK(cudaMemsetAsync(hashed, 0, 2 * sizeof(unsigned long long), st));
+  }
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *prog = a.temp<unsigned long long>(J);  // per stream, see the kernel
@@ -637,7 +644,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
       const uint32_t j0 = group_copy ? copy.j_first[gi] : 0;
       const uint32_t j1 = group_copy ? copy.j_first[gi + 1] : J;
       if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done[gi], 0));
-      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
+      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, hashed, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                     heldout_mode ? 1u : 0u, frontier, prog, j0, j1 - j0, nullptr,
@@ -651,7 +658,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                   static_cast<uint16_t *>(d_stream_bp), order, klen, c->offs,
                                   c->n_tokens, c->cum + (size_t)K * J, T, c->G, first_num,
                                   pre_cap, need_num, st));
-      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, c->offs, static_cast<uint32_t *>(d_sdb),
+      NS_CK(nsk::launch_hash_prefix(src, dst, tokens_read, hashed, c->offs, static_cast<uint32_t *>(d_sdb),
                                     static_cast<uint16_t *>(d_stream_bp), J, D0, order, klen,
                                     c->cum + (size_t)K * J, ready, S, T, c->G, c->hash_key,
                                     heldout_mode ? 1u : 0u, frontier, prog, 0, J, need_num, 0,
@@ -900,9 +907,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   std::vector<uint32_t> W_h(J);
   uint32_t valid_h = 0;
   uint64_t digest_h = 0;
-  unsigned long long read_h = 0;
+  unsigned long long read_h = 0, hashed_h[2] = {0, 0};
   if (tokens_read)
     NS_CK(cudaMemcpyAsync(&read_h, tokens_read, sizeof(read_h), cudaMemcpyDeviceToHost, st));
+  if (hashed)
+    NS_CK(cudaMemcpyAsync(hashed_h, hashed, sizeof(hashed_h), cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(W_h.data(), c->W, J * 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&valid_h, valid, 4, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaMemcpyAsync(&digest_h, digest, 8, cudaMemcpyDeviceToHost, st));
@@ -910,6 +919,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaStreamSynchronize(st));
   if (err_host != 0) return NS_ERR_DEVICE;
   c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
+  c->hashed_tokens += hashed_h[0];
+  c->hashed_docs += hashed_h[1];
   // a stream cut short at a speculated bound must hold one window past the
   // ones the horizon reads (so that those are closed): else, the full bound
   for (uint32_t j = 0; j < J; j++)
@@ -958,6 +969,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   if (rc) return rc;
   const uint64_t launches0 = nsk::launch_counter();
   uint64_t host_bytes_before = 0;  // a host corpus read by an earlier pass
+  uint64_t hashed_before[2] = {0, 0};  // tokens and documents it hashed
   // pass 1 hashes to a speculated bound; pass 2, only if that left a stream
   // short of its windows, to the full bound
   for (uint32_t pass = 1; pass <= 2; pass++) {
@@ -969,12 +981,16 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
     rc = build(c, cfg, a);
     c->init_launches = (uint32_t)(nsk::launch_counter() - launches0);
     c->host_bytes += host_bytes_before;
+    c->hashed_tokens += hashed_before[0];
+    c->hashed_docs += hashed_before[1];
     if (rc == NS_OK) {
       a.release();
       *out = c;
       return NS_OK;
     }
     host_bytes_before = c->host_bytes;
+    hashed_before[0] = c->hashed_tokens;
+    hashed_before[1] = c->hashed_docs;
     cudaStreamSynchronize(c->stream);
     cudaGetLastError();
     a.release();
@@ -1097,6 +1113,8 @@ int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
   info->init_launches = ctx->init_launches;
   info->init_passes = ctx->init_passes;
   info->host_bytes = ctx->host_bytes;
+  info->hashed_tokens = ctx->hashed_tokens;
+  info->hashed_docs = ctx->hashed_docs;
   return NS_OK;
 }
 

@@ -542,7 +542,8 @@ __device__ __forceinline__ unsigned long long grab_estimate(unsigned long long r
 template <bool kCopy, bool kChunked>
 __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
     hash_prefix_kernel(const int32_t *__restrict__ tokens, int32_t *__restrict__ copy_dst,
-                       unsigned long long *tokens_read, const int64_t *__restrict__ offs,
+                       unsigned long long *tokens_read, unsigned long long *hashed,
+                       const int64_t *__restrict__ offs,
                        const uint32_t *__restrict__ sdb, const uint16_t *__restrict__ stream_bp,
                        uint32_t J, uint32_t D0, const uint32_t *__restrict__ order,
                        uint32_t *__restrict__ klen, const int32_t *cum_last,
@@ -650,8 +651,11 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
       }
       kept_here = warp_sum_u64(kept_here);
       const unsigned long long raw_here = warp_sum_u64(L_l);
+      const unsigned docs_here = __popc(__ballot_sync(0xffffffffu, L_l != 0));
       if (lane == 0 && raw_here) {
         if (kCopy) atomicAdd(tokens_read, raw_here);
+        atomicAdd(hashed, raw_here);
+        atomicAdd(hashed + 1, (unsigned long long)docs_here);
         // the kept tokens in, the estimate out, one grab fewer in flight
         // (modulo 2^64: the word's count holds this grab, so nothing
         // borrows from the tokens)
@@ -1647,7 +1651,8 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 }
 
 cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
-                               unsigned long long *tokens_read, const int64_t *offs,
+                               unsigned long long *tokens_read, unsigned long long *hashed,
+                               const int64_t *offs,
                                const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
                                uint32_t D0, const uint32_t *order, uint32_t *klen,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,
@@ -1666,9 +1671,9 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
   const dim3 grid(min(n_sms * kHashBlocksPerSM, kMaxBlocks)), block(kHashThreads);
 #define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
   hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
-      tokens, copy_dst, tokens_read, offs, sdb, stream_bp, J, D0, order, klen, cum_last, ready, \
-      ready_at, T, G, hash_key, want_heldout, frontier, prog, j_begin, j_count, need_num,       \
-      need_num_all, pre_cap)
+      tokens, copy_dst, tokens_read, hashed, offs, sdb, stream_bp, J, D0, order, klen,          \
+      cum_last, ready, ready_at, T, G, hash_key, want_heldout, frontier, prog, j_begin,         \
+      j_count, need_num, need_num_all, pre_cap)
   if (copy_dst) {
     if (j_count > kChunkFrom)
       NS_HASH_LAUNCH(true, true);

@@ -66,6 +66,7 @@ cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 // copy_dst non-null: tokens is host memory the device can address, and
 // every hashed document is also written to copy_dst (tokens_read counts them).
+// hashed[0] and hashed[1] count the tokens and the documents hashed.
 // pre_cap (per stream kept tokens, or NULL): where a stream stops before the
 // quota table is known.  frontier and prog (per stream, zeroed before the
 // first round, carried into the second): the next position to grab, and the
@@ -73,7 +74,8 @@ cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_
 // in bits 16 and up; the grabs in flight below).  The grid is n_sms times the
 // hash's CTAs per SM: fewer than 2^16 warps, so the word's count cannot wrap
 cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
-                               unsigned long long *tokens_read, const int64_t *offs,
+                               unsigned long long *tokens_read, unsigned long long *hashed,
+                               const int64_t *offs,
                                const uint32_t *sdb, const uint16_t *stream_bp, uint32_t J,
                                uint32_t D0, const uint32_t *order, uint32_t *klen,
                                const int32_t *cum_last, const unsigned *ready, unsigned ready_at,

@@ -208,6 +208,9 @@ typedef struct {
                            that ns_pack_init read from host memory: offsets,
                            loss starts and the tokens it used (the whole
                            corpus when it had to copy it); 0 otherwise */
+  uint64_t hashed_tokens; /* tokens the held-out hash read (every init pass;
+                             0 when no source holds documents out) */
+  uint64_t hashed_docs;   /* non-empty documents it decided */
 } ns_pack_info_t;
 
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of

@@ -121,3 +121,33 @@ def test_null_context_is_rejected(nspack):
     assert L.lib.ns_pack_batch_fp(None, None, 1, 1, None, None) == nspack.NS_ERR_INVALID_ARG
     assert L.lib.ns_pack_step_learned(None, None, 1, 1, None, None) == nspack.NS_ERR_INVALID_ARG
     L.lib.ns_pack_free(None)
+
+
+def test_binding_structs_match_the_header_layout(nspack, tmp_path):
+    # the ctypes structures of the binding and the C structures of the header
+    # agree field by field: a C program built against the header prints each
+    # field's offset and each structure's size
+    from deterministic_packed_assembly_gb300 import _lib as L
+    structs = {"ns_pack_config": L.ns_pack_config, "ns_pack_out": L.ns_pack_out,
+               "ns_pack_info_t": L.ns_pack_info_t}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "nspack.h"',
+             'int main(void) {']
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} sizeof %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ['  return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe)])
+    got = {}
+    for ln in subprocess.check_output([str(exe)], text=True).splitlines():
+        s, f, v = ln.split()
+        got[(s, f)] = int(v)
+    for name, cls in structs.items():
+        assert got[(name, "sizeof")] == C.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)

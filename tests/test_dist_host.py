@@ -99,3 +99,86 @@ def test_schedule_launch_plan_slices_cover_every_update():
                 full = o.rows(s0 + q)
                 for f in full:
                     assert np.array_equal(np.concatenate([p[f] for p in parts]), full[f])
+
+
+class _Plan:
+    """The piece of a Packer that bench.launch_plan reads."""
+
+    def __init__(self, schedule, B):
+        self.schedule, self.B = schedule, B
+
+    def rows_of_step(self, k):
+        if not self.schedule:
+            return self.B
+        return [p["B"] for p in self.schedule if p["begin"] <= k][-1]
+
+
+def _collective_worker(rank, world, port, variant, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
+    import torch
+    import bench
+    import oracle
+    from corpus import make_preset
+    c = make_preset("c1")
+    kw = bench.variant_kwargs(c, variant)
+    o = oracle.Oracle(c, **kw)
+    v = o.valid_steps
+    plan = list(bench.launch_plan(_Plan(kw.get("schedule"), c.B), v, 3))
+    d = bench.Dist()
+    # this rank's slice of every update, computed by the oracle: its row
+    # fingerprints (padded to the largest slice) and its learned positions
+    n_buf = -(-c.B // world)
+    local = torch.zeros((v, n_buf), dtype=torch.int64)
+    learned = torch.zeros(v, dtype=torch.int64)
+    for s0, m, Bk in plan:
+        r0, r1 = bench.row_slice(rank, world, Bk)
+        for k in range(s0, s0 + m):
+            if r1 > r0:
+                rows = o.rows(k, r0, r1)
+                local[k, :r1 - r0] = torch.from_numpy(rows["row_fp"].view(np.int64))
+                learned[k] = int(rows["row_learned"].astype(np.int64).sum())
+    bench.reduce_learned(d, learned)
+    runs = bench.fold_runs(plan)
+    got = bench.gather_batch_rows(d, local, runs, world)
+    d.barrier()
+    d.close()
+    q.put((rank, learned.numpy(), [(f0, fm, g.numpy()) for (f0, fm, _), g in zip(runs, got)]))
+
+
+@pytest.mark.parametrize("world,variant", [(2, "default"), (4, "default"), (3, "schedule")])
+def test_row_split_collectives_rebuild_every_global_batch(world, variant):
+    # the two collectives of a row split over ranks: each update's learned
+    # positions summed over the ranks' slices, and the row fingerprints
+    # gathered in row order, whose fold is the global batch fingerprint --
+    # both equal to what one rank holding the whole batch gets
+    import bench
+    import oracle
+    from corpus import make_preset
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_collective_worker, args=(r, world, port, variant, q))
+          for r in range(world)]
+    for p in ps:
+        p.start()
+    res = sorted((q.get(timeout=180) for _ in range(world)), key=lambda x: x[0])
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    c = make_preset("c1")
+    o = oracle.Oracle(c, **bench.variant_kwargs(c, variant))
+    v = o.valid_steps
+    want = [o.rows(k) for k in range(v)]
+    for rank, learned, runs in res:
+        assert [int(x) for x in learned] == [int(w["row_learned"].astype(np.int64).sum())
+                                             for w in want]
+        covered = 0
+        for f0, fm, rows in runs:
+            for i in range(fm):
+                k = f0 + i
+                fp = rows[i].view(np.uint64)
+                assert np.array_equal(fp, want[k]["row_fp"]), (rank, k)
+                assert oracle.batch_fp(fp) == oracle.batch_fp(want[k]["row_fp"])
+                covered += 1
+        assert covered == v
