@@ -65,6 +65,46 @@ void dev_free(ns_pack_ctx *c, void *p) {
     cudaFree(p);
 }
 
+// Page-locked host memory for the small copies of an init (the grid layouts
+// and estimates it uploads, its two readbacks): a copy from pageable memory
+// goes through a driver buffer and may wait for the stream; one from
+// page-locked memory is a plain DMA.  One buffer per host thread, grown at
+// the start of an init when it is too small -- no copy of an earlier init is
+// in flight then, as every init synchronises its streams before it returns
+// -- and handed out front to back during the init.  Ordinary memory stands
+// in if page-locked memory cannot be had.
+struct HostStage {
+  char *pinned = nullptr;
+  std::vector<char> heap;
+  size_t cap = 0, used = 0;
+  void reset(size_t need) {
+    used = 0;
+    if (need <= cap) return;
+    if (pinned) cudaFreeHost(pinned);
+    pinned = nullptr;
+    const size_t c = std::max<size_t>(need, (size_t)1 << 20);
+    void *p = nullptr;
+    if (cudaHostAlloc(&p, c, cudaHostAllocPortable) == cudaSuccess) {
+      pinned = static_cast<char *>(p);
+      std::vector<char>().swap(heap);
+    } else {
+      cudaGetLastError();
+      heap.resize(c);
+    }
+    cap = c;
+  }
+  void *take(size_t bytes) {  // NULL past what the init reserved
+    const size_t off = (used + 255) / 256 * 256;
+    if (off + bytes > cap) return nullptr;
+    used = off + bytes;
+    return (pinned ? pinned : heap.data()) + off;
+  }
+  ~HostStage() {
+    if (pinned) cudaFreeHost(pinned);
+  }
+};
+thread_local HostStage tl_stage;
+
 // Device memory of one init.  Small requests are carved out of slabs that
 // grow geometrically (1 MiB, 2 MiB, ... up to 64 MiB), large ones get their
 // own allocation, so an init makes a handful of allocator calls instead of
@@ -122,6 +162,16 @@ struct Arena {
   template <class T>
   T *temp(size_t n) {
     return static_cast<T *>(get(n * sizeof(T), false));
+  }
+  // Host memory for a copy of this init: the thread's page-locked stage, or,
+  // past what the init reserved of it, ordinary memory kept until the init
+  // ends.
+  std::vector<std::vector<char>> host_extra;
+  void *host(size_t bytes) {
+    void *p = tl_stage.take(bytes);
+    if (p) return p;
+    host_extra.emplace_back(std::max<size_t>(bytes, 1));
+    return host_extra.back().data();
   }
   void release() {
     for (void *p : temps) dev_free(c, p);
@@ -222,22 +272,45 @@ std::vector<uint32_t> seg_layout(const std::vector<uint64_t> &count, uint32_t pe
     if (!(p)) return NS_ERR_OOM;  \
   } while (0)
 
-// A second stream for work that does not depend on the corpus; synchronised
-// and destroyed on every exit path.
+// A second stream for work that does not depend on the corpus, with its fork
+// and join events; synchronised on every exit path.  Created once per host
+// thread and device and kept for the next init (creating a stream and its
+// events costs more than a small init's kernels).
+struct SideHandles {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+thread_local SideHandles tl_side[kMaxSideDevices];
+
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   cudaError_t create() {
-    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-    return e;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    SideHandles local, *h = (dev >= 0 && dev < kMaxSideDevices) ? &tl_side[dev] : &local;
+    if (!h->s) {
+      e = cudaStreamCreateWithFlags(&h->s, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    s = h->s;
+    fork = h->fork;
+    join = h->join;
+    owned = (h == &local);
+    return cudaSuccess;
   }
+  bool owned = false;  // a device beyond the table: destroyed with this object
   ~SideStream() {
     if (s) cudaStreamSynchronize(s);
-    if (fork) cudaEventDestroy(fork);
-    if (join) cudaEventDestroy(join);
-    if (s) cudaStreamDestroy(s);
+    if (owned) {
+      if (fork) cudaEventDestroy(fork);
+      if (join) cudaEventDestroy(join);
+      if (s) cudaStreamDestroy(s);
+    }
   }
 };
 
@@ -280,7 +353,9 @@ struct Staging {
   int commit(Arena &a, cudaStream_t st) {
     unsigned char *d = static_cast<unsigned char *>(a.get(host.size(), false));
     if (!d) return NS_ERR_OOM;
-    if (cudaMemcpyAsync(d, host.data(), host.size(), cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    void *h = a.host(host.size());
+    std::memcpy(h, host.data(), host.size());
+    if (cudaMemcpyAsync(d, h, host.size(), cudaMemcpyHostToDevice, st) != cudaSuccess) {
       cudaGetLastError();
       return NS_ERR_CUDA;
     }
@@ -328,7 +403,11 @@ const int32_t *device_view(const int32_t *host, uint64_t n) {
 int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st) {
   *dev = a.get(bytes, false);
   NS_ALLOC(*dev);
-  if (bytes) NS_CK(cudaMemcpyAsync(*dev, host, bytes, cudaMemcpyHostToDevice, st));
+  if (bytes) {
+    void *h = a.host(bytes);
+    std::memcpy(h, host, bytes);
+    NS_CK(cudaMemcpyAsync(*dev, h, bytes, cudaMemcpyHostToDevice, st));
+  }
   return NS_OK;
 }
 
@@ -338,6 +417,14 @@ constexpr int kRetryFullBound = 1;
 int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   const uint32_t J = c->J, S = c->S, K = c->K, T = c->T;
   cudaStream_t st = c->stream;
+  {
+    // this init's page-locked host memory: the recipe (a schedule's weights
+    // up to 32 MiB; beyond, ordinary memory), the grid layouts and the two
+    // readbacks, all proportional to the streams
+    const size_t P = cfg->n_pieces ? cfg->n_pieces : 1;
+    const size_t recipe = std::min<size_t>(P * ((size_t)S + J) * 12, (size_t)32 << 20);
+    tl_stage.reset(recipe + 192 * ((size_t)J + 1) + 16 * ((size_t)S + 1) + ((size_t)256 << 10));
+  }
   int dev = 0;
   NS_CK(cudaGetDevice(&dev));
   NS_CK(cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev));
@@ -506,6 +593,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                    max_strata, c->quota, c->cum, ready, side.s));
   }
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
+  // The corpus partition, checked whole beside the shuffle and the hash:
+  // every kernel that reads tokens also checks the offsets it uses, so a
+  // malformed partition is reported (BAD_INPUT) at the next readback, never
+  // read past.
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
 
   // Each stream's windows over the horizon estimated from the recipe (its
@@ -530,10 +622,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   for (uint32_t j = 0; j < J; j++)
     est_windows[j] = std::ceil(est_windows[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
 
-  // ---- 2. the corpus partition; shuffled order and lengths of every position
-  // Every kernel that reads tokens checks the offsets it uses, so a malformed
-  // partition is reported (BAD_INPUT) at the next readback, never read past.
-  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, st));
+  // ---- 2. shuffled order and lengths of every position ----------------------
   const uint32_t D0 = sdb[0];
   const uint64_t n_pos = (uint64_t)sdb[J] - D0;
   const bool heldout_mode = (c->flags & NS_PACK_HELDOUT) != 0;
@@ -559,6 +648,16 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // estimate), the others keep length 0.  A stream whose windows turn out to
   // need more is caught after the cutoff, and the context is built again
   // with every position.
+  // What the host reads back after the prefix cutoff, in one block (one
+  // copy): cutoff u32[J] | npieces i64[J] | node_base i64[J + 1] | ptokens
+  // i64[J] | rmax i32[J] | need_num u16[J] | pos_lim u32[J] | error word
+  auto al8 = [](size_t b) { return (b + 7) / 8 * 8; };
+  const size_t r1_np = al8((size_t)J * 4), r1_nb = r1_np + (size_t)J * 8;
+  const size_t r1_pt = r1_nb + ((size_t)J + 1) * 8, r1_rmax = r1_pt + (size_t)J * 8;
+  const size_t r1_num = al8(r1_rmax + (size_t)J * 4), r1_lim = al8(r1_num + (size_t)J * 2);
+  const size_t r1_err = r1_lim + (size_t)J * 4, r1_bytes = r1_err + 8;
+  char *rb1 = a.temp<char>(r1_bytes);
+  NS_ALLOC(rb1);
   uint32_t *pos_lim = nullptr;
   bool any_unhashed = false;
   for (uint32_t j = 0; j < J; j++) any_unhashed |= stream_bp[j] == 0 && N[j] > 0;
@@ -567,8 +666,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     for (uint32_t j = 0; j < J; j++) est_tok[j] = (unsigned long long)(est_windows[j] * T);
     void *d_est;
     if ((rc = upload(a, est_tok.data(), J * sizeof(unsigned long long), &d_est, st))) return rc;
-    pos_lim = a.temp<uint32_t>(J);
-    NS_ALLOC(pos_lim);
+    pos_lim = reinterpret_cast<uint32_t *>(rb1 + r1_lim);
     NS_CK(nsk::launch_order_bound(static_cast<uint32_t *>(d_sdb), c->offs, J,
                                   static_cast<uint16_t *>(d_stream_bp),
                                   static_cast<unsigned long long *>(d_est), pos_lim, st));
@@ -588,12 +686,17 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // Runs beside the quota kernels: it reads each stream's need from their
   // table once all S quota blocks have published it, and hashes on until then.
   // tokens read from host memory in place (hash and prefix copy)
-  unsigned long long *tokens_read = nullptr;
-  if (htok) {
-    tokens_read = a.temp<unsigned long long>(1);
-    NS_ALLOC(tokens_read);
-    NS_CK(cudaMemsetAsync(tokens_read, 0, sizeof(unsigned long long), st));
-  }
+  // The summary the host reads back at the end, in one block (one copy):
+  // tokens read from host memory u64 | tokens and documents hashed u64[2] |
+  // order digest u64 | valid updates u32 | error word | windows u32[J]
+  constexpr size_t r2_read = 0, r2_hashed = 8, r2_digest = 24, r2_valid = 32, r2_err = 36;
+  constexpr size_t r2_W = 40;
+  const size_t r2_bytes = r2_W + (size_t)J * 4;
+  char *rb2 = a.temp<char>(r2_bytes);
+  NS_ALLOC(rb2);
+  NS_CK(cudaMemsetAsync(rb2, 0, r2_digest, st));
+  unsigned long long *tokens_read =
+      htok ? reinterpret_cast<unsigned long long *>(rb2 + r2_read) : nullptr;
   const bool group_copy = host_corpus && !htok;
   // Greedy windows hold at most T tokens, so a prefix whose kept tokens
   // exceed (windows needed) * T holds them all, whatever the packing: the
@@ -608,8 +711,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   uint16_t *need_num = nullptr;  // per stream, of 1024 (NULL: the full bound)
   unsigned long long *pre_cap = nullptr;
   if (speculate) {
-    need_num = a.temp<uint16_t>(J);
-    NS_ALLOC(need_num);
+    need_num = reinterpret_cast<uint16_t *>(rb1 + r1_num);
     // Until the quota kernel publishes each stream's need, the first round
     // stops a stream at half its recipe estimate (est_windows), not at no
     // bound at all: a small stream is then not hashed far past its need while
@@ -622,12 +724,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     if ((rc = upload(a, cap.data(), J * sizeof(unsigned long long), &d_cap, st))) return rc;
     pre_cap = static_cast<unsigned long long *>(d_cap);
   }
-  unsigned long long *hashed = nullptr;  // tokens and documents hashed
-  if (any_heldout) {
-    hashed = a.temp<unsigned long long>(2);
-    NS_ALLOC(hashed);
-    NS_CK(cudaMemsetAsync(hashed, 0, 2 * sizeof(unsigned long long), st));
-  }
+  unsigned long long *hashed =  // tokens and documents hashed
+      any_heldout ? reinterpret_cast<unsigned long long *>(rb2 + r2_hashed) : nullptr;
   if (any_heldout) {
     unsigned long long *frontier = a.temp<unsigned long long>(J);
     unsigned long long *prog = a.temp<unsigned long long>(J);  // per stream, see the kernel
@@ -675,42 +773,43 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                 static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, st));
 
   // ---- 4. the prefix of each stream the horizon reaches -------------------
-  uint32_t *cutoff = a.temp<uint32_t>(J);
-  int64_t *npieces = a.temp<int64_t>(J);
-  int64_t *ptokens = a.temp<int64_t>(J);
-  int64_t *node_base = a.temp<int64_t>(J + 1);
-  NS_ALLOC(cutoff);
-  NS_ALLOC(npieces);
-  NS_ALLOC(ptokens);
-  NS_ALLOC(node_base);
+  uint32_t *cutoff = reinterpret_cast<uint32_t *>(rb1);
+  int64_t *npieces = reinterpret_cast<int64_t *>(rb1 + r1_np);
+  int64_t *ptokens = reinterpret_cast<int64_t *>(rb1 + r1_pt);
+  int64_t *node_base = reinterpret_cast<int64_t *>(rb1 + r1_nb);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
                            T, c->G, need_num, pos_lim, cutoff, npieces, ptokens, st));
   NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
-  std::vector<uint32_t> cut_h(J);
-  std::vector<int64_t> np_h(J), nb_h(J + 1), pt_h(J);
-  std::vector<uint16_t> num_h(J, 1024);
-  std::vector<int32_t> rmax32(J);
-  std::vector<uint32_t> lim_h(pos_lim ? J : 0);
-  int err_host = 0;
-  NS_CK(cudaMemcpyAsync(cut_h.data(), cutoff, J * 4, cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(np_h.data(), npieces, J * 8, cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(nb_h.data(), node_base, (J + 1) * 8, cudaMemcpyDeviceToHost, st));
-  if (htok) NS_CK(cudaMemcpyAsync(pt_h.data(), ptokens, J * 8, cudaMemcpyDeviceToHost, st));
-  if (need_num)
-    NS_CK(cudaMemcpyAsync(num_h.data(), need_num, J * sizeof(uint16_t), cudaMemcpyDeviceToHost,
-                          st));
-  NS_CK(cudaMemcpyAsync(rmax32.data(), c->cum + (size_t)K * J, J * sizeof(int32_t),
-                        cudaMemcpyDeviceToHost, st));
-  if (pos_lim)
-    NS_CK(cudaMemcpyAsync(lim_h.data(), pos_lim, J * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  {
+    nsk::CollectList cl{};
+    cl.src[0] = reinterpret_cast<const uint32_t *>(c->cum + (size_t)K * J);
+    cl.off[0] = (uint32_t)(r1_rmax / 4);
+    cl.words[0] = J;
+    cl.src[1] = reinterpret_cast<const uint32_t *>(c->err);
+    cl.off[1] = (uint32_t)(r1_err / 4);
+    cl.words[1] = 1;
+    cl.n = 2;
+    NS_CK(nsk::launch_collect(cl, reinterpret_cast<uint32_t *>(rb1), st));
+  }
+  char *h1 = static_cast<char *>(a.host(r1_bytes));
+  NS_CK(cudaMemcpyAsync(h1, rb1, r1_bytes, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
+  const uint32_t *cut_h = reinterpret_cast<const uint32_t *>(h1);
+  const int64_t *np_h = reinterpret_cast<const int64_t *>(h1 + r1_np);
+  const int64_t *nb_h = reinterpret_cast<const int64_t *>(h1 + r1_nb);
+  const int64_t *pt_h = reinterpret_cast<const int64_t *>(h1 + r1_pt);
+  const int32_t *rmax32 = reinterpret_cast<const int32_t *>(h1 + r1_rmax);
+  const uint16_t *num_h = reinterpret_cast<const uint16_t *>(h1 + r1_num);
+  const uint32_t *lim_h = reinterpret_cast<const uint32_t *>(h1 + r1_lim);
+  int err_host = 0;
+  std::memcpy(&err_host, h1 + r1_err, sizeof(int));
   if (err_host == nsk::kDevBadOffsets) return NS_ERR_BAD_INPUT;
   if (err_host != 0) return NS_ERR_DEVICE;
   // a stream shuffled only in part whose windows need more than that part
   // holds: its cutoff runs to the stream's end
-  for (uint32_t j = 0; j < (uint32_t)lim_h.size(); j++)
-    if (lim_h[j] < N[j] && cut_h[j] > lim_h[j]) return kRetryFullBound;
+  if (pos_lim)
+    for (uint32_t j = 0; j < J; j++)
+      if (lim_h[j] < N[j] && cut_h[j] > lim_h[j]) return kRetryFullBound;
   std::vector<uint64_t> rmax(J);
   std::vector<int64_t> wbase(J + 1, 0);
   for (uint32_t j = 0; j < J; j++) {
@@ -720,8 +819,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   c->wbase = a.keep<int64_t>(J + 1);
   NS_ALLOC(c->wbase);
-  NS_CK(cudaMemcpyAsync(c->wbase, wbase.data(), (J + 1) * sizeof(int64_t),
-                        cudaMemcpyHostToDevice, st));
+  {
+    void *h = a.host((J + 1) * sizeof(int64_t));
+    std::memcpy(h, wbase.data(), (J + 1) * sizeof(int64_t));
+    NS_CK(cudaMemcpyAsync(c->wbase, h, (J + 1) * sizeof(int64_t), cudaMemcpyHostToDevice, st));
+  }
   const int64_t n_nodes = nb_h[J];
   if (n_nodes >= (int64_t)0x7FFFFFFF) return NS_ERR_INVALID_ARG;
   c->n_pieces = (uint64_t)(n_nodes - J);
@@ -838,7 +940,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   int32_t *win_clip = wrap ? a.temp<int32_t>(n_win) : nullptr;
   c->row_win = a.keep<int4>((size_t)K * c->B);
   uint32_t *first_bad = a.temp<uint32_t>(1);
-  uint32_t *valid = a.temp<uint32_t>(1);
+  uint32_t *valid = reinterpret_cast<uint32_t *>(rb2 + r2_valid);
   NS_ALLOC(c->W);
   NS_ALLOC(win_start);
   if (wrap) {
@@ -847,7 +949,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   NS_ALLOC(c->row_win);
   NS_ALLOC(first_bad);
-  NS_ALLOC(valid);
   std::vector<uint32_t> wb = seg_layout(rmax, 256);
   void *d_wb;
   if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
@@ -871,10 +972,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // ---- 8. order digest ----------------------------------------------------
   unsigned long long *dacc = a.temp<unsigned long long>(2);
   int64_t *ubase = a.temp<int64_t>(J + 1);
-  uint64_t *digest = a.temp<uint64_t>(1);
+  uint64_t *digest = reinterpret_cast<uint64_t *>(rb2 + r2_digest);
   NS_ALLOC(dacc);
   NS_ALLOC(ubase);
-  NS_ALLOC(digest);
   NS_CK(cudaMemsetAsync(dacc, 0, 2 * sizeof(unsigned long long), st));
   nsk::DigestHeader h{};
   h.scalars[0] = T;
@@ -904,19 +1004,29 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
 
   // ---- 9. read back the summary ------------------------------------------
   if (prefix_copy) NS_CK(cudaStreamWaitEvent(st, side.join, 0));
-  std::vector<uint32_t> W_h(J);
+  {
+    nsk::CollectList cl{};
+    cl.src[0] = c->W;
+    cl.off[0] = (uint32_t)(r2_W / 4);
+    cl.words[0] = J;
+    cl.src[1] = reinterpret_cast<const uint32_t *>(c->err);
+    cl.off[1] = (uint32_t)(r2_err / 4);
+    cl.words[1] = 1;
+    cl.n = 2;
+    NS_CK(nsk::launch_collect(cl, reinterpret_cast<uint32_t *>(rb2), st));
+  }
+  char *h2 = static_cast<char *>(a.host(r2_bytes));
+  NS_CK(cudaMemcpyAsync(h2, rb2, r2_bytes, cudaMemcpyDeviceToHost, st));
+  NS_CK(cudaStreamSynchronize(st));
+  unsigned long long read_h = 0, hashed_h[2] = {0, 0};
   uint32_t valid_h = 0;
   uint64_t digest_h = 0;
-  unsigned long long read_h = 0, hashed_h[2] = {0, 0};
-  if (tokens_read)
-    NS_CK(cudaMemcpyAsync(&read_h, tokens_read, sizeof(read_h), cudaMemcpyDeviceToHost, st));
-  if (hashed)
-    NS_CK(cudaMemcpyAsync(hashed_h, hashed, sizeof(hashed_h), cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(W_h.data(), c->W, J * 4, cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(&valid_h, valid, 4, cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(&digest_h, digest, 8, cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaMemcpyAsync(&err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, st));
-  NS_CK(cudaStreamSynchronize(st));
+  if (tokens_read) std::memcpy(&read_h, h2 + r2_read, 8);
+  if (hashed) std::memcpy(hashed_h, h2 + r2_hashed, 16);
+  std::memcpy(&digest_h, h2 + r2_digest, 8);
+  std::memcpy(&valid_h, h2 + r2_valid, 4);
+  std::memcpy(&err_host, h2 + r2_err, 4);
+  const uint32_t *W_h = reinterpret_cast<const uint32_t *>(h2 + r2_W);
   if (err_host != 0) return NS_ERR_DEVICE;
   c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
   c->hashed_tokens += hashed_h[0];
@@ -924,8 +1034,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // a stream cut short at a speculated bound must hold one window past the
   // ones the horizon reads (so that those are closed): else, the full bound
   for (uint32_t j = 0; j < J; j++)
-    if (num_h[j] < 1024 && cut_h[j] < N[j] && (uint64_t)W_h[j] < rmax[j] + 1) return kRetryFullBound;
-  c->windows.assign(W_h.begin(), W_h.end());
+    if (need_num && num_h[j] < 1024 && cut_h[j] < N[j] && (uint64_t)W_h[j] < rmax[j] + 1)
+      return kRetryFullBound;
+  c->windows.assign(W_h, W_h + J);
   c->valid_steps = valid_h;
   c->digest = digest_h;
   return NS_OK;

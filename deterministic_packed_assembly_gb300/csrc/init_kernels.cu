@@ -1778,6 +1778,26 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   return cudaGetLastError();
 }
 
+// Word runs of several device arrays gathered into one buffer (run s at
+// dst + off[s]), so that a single copy brings them all to the host.
+__global__ void __launch_bounds__(256) collect_kernel(CollectList l, uint32_t *__restrict__ dst) {
+  const uint32_t s = blockIdx.y;
+  if (s >= l.n) return;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < l.words[s];
+       i += gridDim.x * blockDim.x)
+    dst[l.off[s] + i] = l.src[s][i];
+}
+
+cudaError_t launch_collect(const CollectList &l, uint32_t *dst, cudaStream_t st) {
+  if (l.n == 0) return cudaSuccess;
+  uint32_t most = 1;
+  for (uint32_t s = 0; s < l.n; s++) most = most > l.words[s] ? most : l.words[s];
+  ++launch_counter();
+  const uint32_t gx = (most + 255) / 256 < 64 ? (most + 255) / 256 : 64;
+  collect_kernel<<<dim3(gx, l.n), 256, 0, st>>>(l, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
                           const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,

@@ -166,6 +166,18 @@ cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st);
 
+// ---- readbacks -------------------------------------------------------------
+// Up to kCollectMax runs of 32-bit words, src[s][0 .. words[s]), copied to
+// dst + off[s] in one launch.
+constexpr uint32_t kCollectMax = 8;
+struct CollectList {
+  const uint32_t *src[kCollectMax];
+  uint32_t off[kCollectMax];
+  uint32_t words[kCollectMax];
+  uint32_t n;
+};
+cudaError_t launch_collect(const CollectList &l, uint32_t *dst, cudaStream_t st);
+
 // ---- order digest ---------------------------------------------------------
 constexpr int kDigestScalars = 12;
 struct DigestHeader {
