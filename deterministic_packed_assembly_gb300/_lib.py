@@ -25,6 +25,7 @@ NS_PACK_HELDOUT = 2
 NS_PACK_SHUFFLE_ROWS = 4
 NS_PACK_WRAP = 8
 NS_PACK_HOST_CORPUS = 16
+NS_PACK_ORDERED_FREE = 32
 NS_MAX_T = 1 << 24
 NS_MAX_TOKENS = 1 << 47
 

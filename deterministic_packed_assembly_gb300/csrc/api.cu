@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -53,6 +54,8 @@ struct ns_pack_ctx {
   uint64_t *fp_out = nullptr;
   uint64_t *pad_tail = nullptr;
   std::vector<void *> kept;
+  int device = 0;                  // the device the tables live on
+  std::atomic<bool> foreign{false};  // a step ran on a stream other than `stream`
 };
 
 namespace {
@@ -202,10 +205,11 @@ int check_config(const ns_pack_config *cfg) {
   if (cfg->n_sources == 0 || cfg->n_sources > NS_MAX_SOURCES) return NS_ERR_INVALID_ARG;
   if (cfg->n_streams == 0 || cfg->n_streams > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
   if (cfg->flags & ~(NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS | NS_PACK_WRAP |
-                     NS_PACK_HOST_CORPUS))
+                     NS_PACK_HOST_CORPUS | NS_PACK_ORDERED_FREE))
     return NS_ERR_INVALID_ARG;
   if (cfg->window_segment > NS_MAX_WINDOW_SEGMENT) return NS_ERR_INVALID_ARG;
   if ((cfg->alloc == nullptr) != (cfg->free == nullptr)) return NS_ERR_INVALID_ARG;
+  if ((cfg->flags & NS_PACK_ORDERED_FREE) && !cfg->free) return NS_ERR_INVALID_ARG;
   for (uint32_t s = 0; s < cfg->n_sources; s++)
     if (cfg->source_weight[s] == 0 || cfg->source_heldout_bp[s] > 10000) return NS_ERR_INVALID_ARG;
   std::vector<uint32_t> per_source(cfg->n_sources, 0);
@@ -427,6 +431,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   int dev = 0;
   NS_CK(cudaGetDevice(&dev));
+  c->device = dev;
   NS_CK(cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev));
   int rc;
 
@@ -1152,6 +1157,7 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
   p.len_bucket = ctx->len_bucket;
   p.pad_tail = ctx->pad_tail;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
+  if (st != ctx->stream) ctx->foreign.store(true, std::memory_order_relaxed);
   if (nsk::launch_gather(p, st) != cudaSuccess) {
     cudaGetLastError();
     return NS_ERR_CUDA;
@@ -1263,7 +1269,16 @@ int ns_pack_check(ns_pack_ctx *ctx) {
 
 void ns_pack_free(ns_pack_ctx *ctx) {
   if (!ctx) return;
-  cudaStreamSynchronize(ctx->stream);
+  if (ctx->foreign.load()) {
+    // a step on another stream may still read the tables: wait for the device
+    int cur = 0;
+    if (cudaGetDevice(&cur) == cudaSuccess && cudaSetDevice(ctx->device) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      cudaSetDevice(cur);
+    }
+  } else if (!(ctx->flags & NS_PACK_ORDERED_FREE) || !ctx->free_fn) {
+    cudaStreamSynchronize(ctx->stream);
+  }
   cudaGetLastError();
   release_ctx(ctx);
 }

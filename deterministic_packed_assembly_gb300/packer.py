@@ -104,7 +104,10 @@ class Packer:
         cfg.flags = ((L.NS_PACK_DRAIN if drain else 0) | (L.NS_PACK_HELDOUT if heldout_only else 0)
                      | (L.NS_PACK_SHUFFLE_ROWS if shuffle_rows else 0)
                      | (L.NS_PACK_WRAP if wrap else 0)
-                     | (L.NS_PACK_HOST_CORPUS if self.host_corpus else 0))
+                     | (L.NS_PACK_HOST_CORPUS if self.host_corpus else 0)
+                     # the caching allocator reuses a freed block only on the
+                     # stream it was allocated on, after the free
+                     | L.NS_PACK_ORDERED_FREE)
         cfg.len_bucket = int(len_bucket)
         cfg.window_segment = int(window_segment)
         self.schedule = schedule

@@ -96,6 +96,12 @@ extern "C" {
  * bytes read (host_bytes); the host buffers may be released once
  * ns_pack_init returns. */
 #define NS_PACK_HOST_CORPUS 16u
+/* The free callback is stream-ordered on cuda_stream: memory it takes back is
+ * reused only by work queued on that stream after the free (a stream-ordered
+ * pool such as PyTorch's caching allocator).  ns_pack_free then releases the
+ * tables without waiting for the stream, unless ns_pack_step ran on another
+ * stream.  Needs alloc and free. */
+#define NS_PACK_ORDERED_FREE 32u
 
 /* ---- limits ------------------------------------------------------------- */
 #define NS_MAX_T (1u << 24)          /* T must be a multiple of 16, at most this */
@@ -141,7 +147,7 @@ typedef struct {
   uint32_t B;        /* rows per update (global batch), >= 1 */
   uint32_t max_steps; /* horizon of the quota tables; max_steps * B < 2^31 */
   uint32_t flags;    /* NS_PACK_DRAIN | NS_PACK_HELDOUT | NS_PACK_SHUFFLE_ROWS |
-                        NS_PACK_WRAP | NS_PACK_HOST_CORPUS */
+                        NS_PACK_WRAP | NS_PACK_HOST_CORPUS | NS_PACK_ORDERED_FREE */
   int32_t pad_id;    /* token written at padded positions */
   uint32_t window_segment; /* G > 0: each stream's windows are read in a shuffled
                               order within segments of G consecutive windows
@@ -275,7 +281,10 @@ int ns_pack_quota_table(const ns_pack_ctx *ctx, int32_t *quota, int32_t *cum);
  * Errors: CUDA, DEVICE, BAD_INPUT. */
 int ns_pack_check(ns_pack_ctx *ctx);
 
-/* Release every table of the context (NULL is a no-op).  Synchronises. */
+/* Release every table of the context (NULL is a no-op).  Waits first for
+ * the work that may still read them: the device, if ns_pack_step ever ran on
+ * a stream other than the context's; else the context's stream, unless the
+ * context was built with NS_PACK_ORDERED_FREE (then it does not wait). */
 void ns_pack_free(ns_pack_ctx *ctx);
 
 const char *ns_pack_strerror(int code);

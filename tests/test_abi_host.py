@@ -77,7 +77,7 @@ def _cfg(nspack, **kw):
 @pytest.mark.parametrize("field,value", [
     ("T", 0), ("T", 8), ("T", 24), ("T", (1 << 24) + 16), ("B", 0), ("max_steps", 0),
     ("max_steps", 1 << 30), ("n_sources", 0), ("n_streams", 0), ("n_streams", 70000),
-    ("flags", 32), ("window_segment", (1 << 24) + 1), ("n_tokens", 1 << 47), ("tokens", None), ("doc_offsets", None), ("stream_doc_begin", None),
+    ("flags", 64), ("flags", 32), ("window_segment", (1 << 24) + 1), ("n_tokens", 1 << 47), ("tokens", None), ("doc_offsets", None), ("stream_doc_begin", None),
 ])
 def test_init_rejects_bad_recipe(nspack, field, value):
     c, keep = _cfg(nspack, **{field: value})

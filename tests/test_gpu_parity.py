@@ -870,3 +870,45 @@ def test_every_option_together_random_tiny_corpora(case):
     _check_tables(pk, o, c)
     compare_steps(pk, o, range(o.valid_steps), launch=int(rng.integers(1, 4)))
     pk.check()
+
+
+def test_free_without_waiting_keeps_queued_updates_right():
+    # The Packer builds its contexts with NS_PACK_ORDERED_FREE: close() hands
+    # the tables back to the caching allocator without waiting for the
+    # stream, and the next context, built at once on the same stream, takes
+    # the same blocks.  The updates queued before the close still read the
+    # first context's tables (the second one's kernels come after them).
+    c = make_preset("c3s")
+    o = oracle_for(c)
+    pk = packer_for(c)
+    n = min(6, o.valid_steps)
+    outs = [pk.step(k) for k in range(n)]
+    pk.close()
+    pk2 = packer_for(c, seed=c.seed + 1)
+    out2 = pk2.step(0)
+    for k in range(n):
+        assert_rows_equal({f: v[0] for f, v in to_host(outs[k]).items()}, o.rows(k),
+                          f"update {k}")
+    o2 = oracle_for(c, seed=c.seed + 1)
+    assert_rows_equal({f: v[0] for f, v in to_host(out2).items()}, o2.rows(0), "second context")
+    pk2.close()
+
+
+def test_free_after_a_step_on_another_stream_waits_for_it():
+    # a step on a stream other than the context's: close() waits for the
+    # device before the tables go back
+    c = make_preset("c3s")
+    o = oracle_for(c)
+    pk = packer_for(c)
+    side = torch.cuda.Stream()
+    n = min(6, o.valid_steps)
+    out = pk.empty_out(n)
+    torch.cuda.synchronize()
+    pk.step(0, n_steps=n, out=out, stream=side)
+    pk.close()
+    pk2 = packer_for(c, seed=c.seed + 1)
+    side.synchronize()
+    got = to_host(out)
+    for k in range(n):
+        assert_rows_equal({f: v[k] for f, v in got.items()}, o.rows(k), f"update {k}")
+    pk2.close()
