@@ -88,7 +88,7 @@ def parse_args():
     ap.add_argument("--variant", default="default", choices=sorted(VARIANTS),
                     help="packing options of the pass (validation stream, read-order "
                          "shuffles, wrap packing, schedule)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also", default="c4",
@@ -427,7 +427,7 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
                 if dist.world > 1 else None)
 
     state = {"launches": 0, "init_launches": 0, "valid": 0, "events": [], "rows_total": 0,
-             "init_events": []}
+             "init_events": [], "hash_ns": []}
 
     def one_pass(record: bool, count: bool = False, e2e_bufs=None):
         """One whole pass; returns real tokens assembled when `count`."""
@@ -443,6 +443,8 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
         valid = pk.valid_steps
         state["valid"] = valid
         state["info"] = pk.info
+        if record:
+            state["hash_ns"].append(pk.info["hash_ns"])
         real = torch.zeros((), dtype=torch.int64, device=device) if count else None
         n = 0
         rows_total = 0
@@ -532,6 +534,7 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
     def timed(K: int):
         state["events"].clear()
         state["init_events"].clear()
+        state["hash_ns"].clear()
         sampler = ClockSampler(gpu_id_for(device)) if dist.rank == 0 else None
         dist.barrier()
         torch.cuda.synchronize()
@@ -614,6 +617,10 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
             "gpu_launches": K * (info["init_launches"] + state["launches"]),
             "clocks": clocks, "clocks_retried": retried,
         }
+        if info["hashed_tokens"] and state["hash_ns"]:
+            result["hash_roofline"] = hash_roofline(info["hashed_tokens"],
+                                                    float(np.mean(state["hash_ns"])) * 1e-9,
+                                                    device, stream)
 
     # ---- end to end: host inputs, copies inside the timed region -----------
     if e2e:
@@ -632,6 +639,9 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
             # else
             one_pass(False, e2e_bufs=(tok_h, off_h, ls_h, fp_h, ln_h, bf_h, sl_h))
 
+        # two untimed passes: the first reads of page-locked memory over the
+        # host link settle in only after a pass or two
+        e2e_pass()
         e2e_pass()
         dist.barrier()
         torch.cuda.synchronize()
@@ -669,6 +679,36 @@ def measure(args, dist: Dist, name: str, *, e2e: bool, cpu: bool, steps: int,
     del out, tok_d, off_d, ls_d, row_fp_all, row_ln_all
     torch.cuda.empty_cache()
     return result
+
+
+def hash_roofline(tokens: int, seconds: float, device, stream) -> dict:
+    """The held-out hash against its integer ceiling: tokens hashed per
+    second inside the pass (its phase of init, both rounds, timed by the
+    library with CUDA events) over the rate of a register-only loop of the
+    same per-token term (ns_pack_probe_hash_terms), timed here."""
+    import torch
+    import deterministic_packed_assembly_gb300 as nsp
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks, per = sms * 8, 8192
+    acc = torch.zeros(1, dtype=torch.int64, device=device)
+    nsp.ns_pack_probe_hash_terms(blocks, per, acc.data_ptr(), stream.cuda_stream)
+    best = None
+    for _ in range(3):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        nsp.ns_pack_probe_hash_terms(blocks, per, acc.data_ptr(), stream.cuda_stream)
+        b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) / 1e3
+        best = t if best is None else min(best, t)
+    peak = blocks * 256 * per / best
+    achieved = tokens / seconds
+    return {"kernel": "hash_prefix_kernel", "bound": "alu", "achieved": achieved,
+            "peak": peak, "unit": "terms/s", "frac": achieved / peak,
+            "peak_kind": "measured: register-only loop of the same per-token term "
+                         "(ns_pack_probe_hash_terms, %d x 256 threads x %d terms)" % (blocks, per),
+            "tokens": tokens, "ms": seconds * 1e3}
 
 
 def run_ours(args, dist: Dist) -> None:

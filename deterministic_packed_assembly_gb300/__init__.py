@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     NS_PACK_DRAIN,
     NS_PACK_HELDOUT,
     NS_PACK_HOST_CORPUS,
+    NS_PACK_ORDERED_FREE,
     NS_PACK_SHUFFLE_ROWS,
     NS_PACK_WRAP,
     LIB_PATH,
@@ -31,6 +32,7 @@ from ._lib import (  # noqa: F401
     ns_pack_free,
     ns_pack_info,
     ns_pack_init,
+    ns_pack_probe_hash_terms,
     ns_pack_quota_noalloc,
     ns_pack_quota_table,
     ns_pack_step,

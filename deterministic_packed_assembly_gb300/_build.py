@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnspack.so")
-SOURCES = ("api.cu", "init_kernels.cu", "gather.cu", "learned.cu", "noalloc.cu")
+SOURCES = ("api.cu", "init_kernels.cu", "gather.cu", "learned.cu", "noalloc.cu", "probe.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -28,7 +28,7 @@ def _nvcc() -> str:
 
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "nspack.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(__file__)
     return files
 

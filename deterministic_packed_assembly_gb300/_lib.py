@@ -96,6 +96,7 @@ class ns_pack_info_t(C.Structure):
         ("host_bytes", C.c_uint64),
         ("hashed_tokens", C.c_uint64),
         ("hashed_docs", C.c_uint64),
+        ("hash_ns", C.c_uint64),
     ]
 
 
@@ -103,7 +104,7 @@ class ns_pack_info_t(C.Structure):
 SYMBOLS = ("ns_pack_init", "ns_pack_step", "ns_pack_fingerprint", "ns_pack_batch_fp",
            "ns_pack_step_learned", "ns_pack_info", "ns_pack_stream_windows",
            "ns_pack_quota_table", "ns_pack_check", "ns_pack_free", "ns_pack_strerror",
-           "ns_pack_quota_noalloc")
+           "ns_pack_quota_noalloc", "ns_pack_probe_hash_terms")
 
 
 def _load() -> C.CDLL:
@@ -135,6 +136,8 @@ def _load() -> C.CDLL:
     L.ns_pack_free.argtypes = [vp]
     L.ns_pack_strerror.restype = C.c_char_p
     L.ns_pack_strerror.argtypes = [i32]
+    L.ns_pack_probe_hash_terms.restype = i32
+    L.ns_pack_probe_hash_terms.argtypes = [u32, u32, vp, vp]
     L.ns_pack_quota_noalloc.restype = i32
     L.ns_pack_quota_noalloc.argtypes = [vp, u32, vp, vp, u32, u32, u32, vp, vp, vp]
     return L
@@ -232,3 +235,11 @@ def ns_pack_quota_noalloc(source_weight, stream_source, stream_weight, B: int, m
 
 def ns_pack_strerror(code: int) -> str:
     return lib.ns_pack_strerror(code).decode()
+
+
+def ns_pack_probe_hash_terms(blocks: int, terms_per_thread: int, sum_dev: int,
+                             stream: int = 0) -> None:
+    """Launch the register-only loop of the held-out hash's term (see
+    include/nspack_probe.h); adds its sum to the device u64 at sum_dev."""
+    check(lib.ns_pack_probe_hash_terms(blocks, terms_per_thread, sum_dev, stream or None),
+          "ns_pack_probe_hash_terms")

@@ -41,6 +41,7 @@ struct ns_pack_ctx {
   uint64_t digest = 0, n_pieces = 0, table_bytes = 0;
   uint64_t host_bytes = 0;  // bytes of a host-resident corpus read at init
   uint64_t hashed_tokens = 0, hashed_docs = 0;  // what the held-out hash read at init
+  uint64_t hash_ns = 0;                          // its device time
   bool speculate = true;    // hash to a bound speculated from the measured fill
   uint32_t init_passes = 1;
   // device tables kept for the per-update calls
@@ -281,15 +282,16 @@ std::vector<uint32_t> seg_layout(const std::vector<uint64_t> &count, uint32_t pe
 // thread and device and kept for the next init (creating a stream and its
 // events costs more than a small init's kernels).
 struct SideHandles {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t s = nullptr, s2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
+  cudaEvent_t t0 = nullptr, t1 = nullptr;  // timing: the held-out hash's phase
 };
 constexpr int kMaxSideDevices = 64;
 thread_local SideHandles tl_side[kMaxSideDevices];
 
 struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t s = nullptr, s2 = nullptr;  // two: the quotas, the offsets check
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr, t0 = nullptr, t1 = nullptr;
   cudaError_t create() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -299,20 +301,33 @@ struct SideStream {
       e = cudaStreamCreateWithFlags(&h->s, cudaStreamNonBlocking);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s2, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join2, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreate(&h->t0);
+      if (e == cudaSuccess) e = cudaEventCreate(&h->t1);
       if (e != cudaSuccess) return e;
     }
     s = h->s;
+    s2 = h->s2;
     fork = h->fork;
     join = h->join;
+    join2 = h->join2;
+    t0 = h->t0;
+    t1 = h->t1;
     owned = (h == &local);
     return cudaSuccess;
   }
   bool owned = false;  // a device beyond the table: destroyed with this object
   ~SideStream() {
     if (s) cudaStreamSynchronize(s);
+    if (s2) cudaStreamSynchronize(s2);
     if (owned) {
       if (fork) cudaEventDestroy(fork);
       if (join) cudaEventDestroy(join);
+      if (join2) cudaEventDestroy(join2);
+      if (s2) cudaStreamDestroy(s2);
+      if (t0) cudaEventDestroy(t0);
+      if (t1) cudaEventDestroy(t1);
       if (s) cudaStreamDestroy(s);
     }
   }
@@ -598,12 +613,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                    max_strata, c->quota, c->cum, ready, side.s));
   }
   NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
-  // The corpus partition, checked whole beside the shuffle and the hash:
-  // every kernel that reads tokens also checks the offsets it uses, so a
-  // malformed partition is reported (BAD_INPUT) at the next readback, never
-  // read past.
-  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, side.s));
   NS_CK(cudaEventRecord(side.join, side.s));
+  // The corpus partition, checked whole on a stream of its own beside the
+  // quotas, the shuffle and the hash: every kernel that reads tokens also
+  // checks the offsets it uses, so a malformed partition is reported
+  // (BAD_INPUT) at the next readback, never read past.
+  NS_CK(cudaStreamWaitEvent(side.s2, side.fork, 0));
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, side.s2));
+  NS_CK(cudaEventRecord(side.join2, side.s2));
 
   // Each stream's windows over the horizon estimated from the recipe (its
   // share of every piece's rows, a few windows over): the quota rule keeps
@@ -738,6 +755,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(prog);
     NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
     NS_CK(cudaMemsetAsync(prog, 0, (size_t)J * 8, st));
+    NS_CK(cudaEventRecord(side.t0, st));
     const uint32_t first_num = speculate ? 512u : 1024u;
     const int32_t *src = htok ? htok : c->tokens;
     int32_t *dst = htok ? c->tokens_rw : nullptr;
@@ -767,10 +785,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                     heldout_mode ? 1u : 0u, frontier, prog, 0, J, need_num, 0,
                                     nullptr, c->n_sms, st));
     }
+    NS_CK(cudaEventRecord(side.t1, st));
   }
   // every token is on the device before anything after the hash reads it
   if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));
+  NS_CK(cudaStreamWaitEvent(st, side.join2, 0));
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)
   const uint32_t chunk = wrap ? 0x80000000u : T;
@@ -1036,6 +1056,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->host_bytes += (uint64_t)read_h * sizeof(int32_t);
   c->hashed_tokens += hashed_h[0];
   c->hashed_docs += hashed_h[1];
+  if (any_heldout) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, side.t0, side.t1) == cudaSuccess)
+      c->hash_ns += (uint64_t)((double)ms * 1e6);
+    cudaGetLastError();
+  }
   // a stream cut short at a speculated bound must hold one window past the
   // ones the horizon reads (so that those are closed): else, the full bound
   for (uint32_t j = 0; j < J; j++)
@@ -1085,7 +1111,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
   if (rc) return rc;
   const uint64_t launches0 = nsk::launch_counter();
   uint64_t host_bytes_before = 0;  // a host corpus read by an earlier pass
-  uint64_t hashed_before[2] = {0, 0};  // tokens and documents it hashed
+  uint64_t hashed_before[3] = {0, 0, 0};  // tokens and documents it hashed, its time
   // pass 1 hashes to a speculated bound; pass 2, only if that left a stream
   // short of its windows, to the full bound
   for (uint32_t pass = 1; pass <= 2; pass++) {
@@ -1099,6 +1125,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
     c->host_bytes += host_bytes_before;
     c->hashed_tokens += hashed_before[0];
     c->hashed_docs += hashed_before[1];
+    c->hash_ns += hashed_before[2];
     if (rc == NS_OK) {
       a.release();
       *out = c;
@@ -1107,6 +1134,7 @@ int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out) {
     host_bytes_before = c->host_bytes;
     hashed_before[0] = c->hashed_tokens;
     hashed_before[1] = c->hashed_docs;
+    hashed_before[2] = c->hash_ns;
     cudaStreamSynchronize(c->stream);
     cudaGetLastError();
     a.release();
@@ -1232,6 +1260,7 @@ int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info) {
   info->host_bytes = ctx->host_bytes;
   info->hashed_tokens = ctx->hashed_tokens;
   info->hashed_docs = ctx->hashed_docs;
+  info->hash_ns = ctx->hash_ns;
   return NS_OK;
 }
 

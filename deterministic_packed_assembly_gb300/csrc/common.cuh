@@ -24,6 +24,11 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
   return z ^ (z >> 31);
 }
 
+// The held-out hash's term of the token `tok` at in-document index i.
+__device__ __forceinline__ uint64_t hash_term(uint32_t i, uint32_t tok) {
+  return splitmix64(((uint64_t)i << 32) | tok);
+}
+
 __device__ __forceinline__ void set_error(int *word, int code) {
   if (word) atomicCAS(word, 0, code);
 }

@@ -418,10 +418,8 @@ __global__ void __launch_bounds__(256)
 // Four tokens that all lie inside the document, the first at in-document
 // index i0 (documents are shorter than 2^31 tokens).
 __device__ __forceinline__ uint64_t hash_terms_inside(int4 v, uint32_t i0) {
-  return splitmix64(((uint64_t)i0 << 32) | (uint32_t)v.x) +
-         splitmix64(((uint64_t)(i0 + 1) << 32) | (uint32_t)v.y) +
-         splitmix64(((uint64_t)(i0 + 2) << 32) | (uint32_t)v.z) +
-         splitmix64(((uint64_t)(i0 + 3) << 32) | (uint32_t)v.w);
+  return hash_term(i0, (uint32_t)v.x) + hash_term(i0 + 1, (uint32_t)v.y) +
+         hash_term(i0 + 2, (uint32_t)v.z) + hash_term(i0 + 3, (uint32_t)v.w);
 }
 
 // Terms of a block whose first token has in-document index i0, taken modulo
@@ -435,7 +433,7 @@ __device__ __forceinline__ uint64_t hash_terms_masked(int4 v, uint32_t i0, uint3
 #pragma unroll
   for (int q = 0; q < 4; q++) {
     const uint32_t i = i0 + (uint32_t)q;
-    const uint64_t t = splitmix64(((uint64_t)i << 32) | (uint64_t)(uint32_t)e[q]);
+    const uint64_t t = hash_term(i, (uint32_t)e[q]);
     s += (i < L) ? t : 0ull;
   }
   return s;

@@ -217,6 +217,10 @@ typedef struct {
   uint64_t hashed_tokens; /* tokens the held-out hash read (every init pass;
                              0 when no source holds documents out) */
   uint64_t hashed_docs;   /* non-empty documents it decided */
+  uint64_t hash_ns;       /* device time from the first held-out hash launch to
+                             the end of the last one (both rounds, and the fill
+                             measurement between them; every init pass), from
+                             CUDA events on cfg->cuda_stream; 0 without a hash */
 } ns_pack_info_t;
 
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of

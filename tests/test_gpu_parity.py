@@ -912,3 +912,20 @@ def test_free_after_a_step_on_another_stream_waits_for_it():
     for k in range(n):
         assert_rows_equal({f: v[k] for f, v in got.items()}, o.rows(k), f"update {k}")
     pk2.close()
+
+
+def test_probe_loop_computes_the_hash_terms():
+    # the register-only loop that sets the hash kernel's arithmetic ceiling
+    # computes the held-out hash's per-token term: its sum over one block of
+    # five terms a thread equals the oracle's SplitMix64 of the same keys
+    import deterministic_packed_assembly_gb300 as nsp
+    acc = torch.zeros(1, dtype=torch.int64, device="cuda:0")
+    nsp.ns_pack_probe_hash_terms(1, 5, acc.data_ptr())
+    torch.cuda.synchronize()
+    M = (1 << 64) - 1
+    want = 0
+    for g in range(256):
+        tok = (g * 2654435761) & 0xFFFFFFFF
+        for t in range(5):
+            want = (want + oracle.splitmix64((((g & 1023) + t) << 32) | (tok ^ t))) & M
+    assert int(acc.item()) & M == want
