@@ -1,6 +1,8 @@
 // Device helpers shared by the library's kernels (not by the CPU oracle).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 namespace nsk {
@@ -27,6 +29,43 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
 // The held-out hash's term of the token `tok` at in-document index i.
 __device__ __forceinline__ uint64_t hash_term(uint32_t i, uint32_t tok) {
   return splitmix64(((uint64_t)i << 32) | tok);
+}
+
+// Programmatic dependent launch: a kernel launched with it (pdl_launch) may
+// be scheduled while the kernel before it in the stream drains.  It calls
+// pdl_wait first thing: wait until that kernel has finished and its writes
+// are visible (a no-op for a kernel launched the ordinary way).  Every
+// kernel in a chain of such launches calls it before any early return, so
+// that a grid never completes before the one it depends on.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// pdl_wait, then let the next kernel's blocks be scheduled at once (they
+// wait in their own pdl_wait): for short kernels.  A long kernel with few
+// blocks calls pdl_wait alone, else the next kernel's blocks would sit on
+// the SMs, waiting, for all of its run.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  pdl_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `k` on `st` with programmatic dependent launch allowed: its blocks
+// may be scheduled while the previous kernel in the stream drains, and wait
+// in pdl_wait_then_release (which every such kernel calls first) for it to
+// finish.  Errors go to cudaGetLastError, as with <<<...>>>.
+template <typename... KArgs, typename... Args>
+inline void pdl_launch(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
 }
 
 __device__ __forceinline__ void set_error(int *word, int code) {

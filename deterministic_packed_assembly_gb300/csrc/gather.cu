@@ -423,6 +423,7 @@ constexpr int kFoldChunk = 2048;
 __global__ void __launch_bounds__(256)
     batch_fp_kernel(const uint64_t *__restrict__ row_fp, uint32_t n_rows,
                     uint64_t *__restrict__ out) {
+  pdl_wait_then_release();
   __shared__ uint64_t s[kFoldChunk];
   const uint64_t *f = row_fp + (size_t)blockIdx.x * n_rows;
   uint64_t F = 0;
@@ -442,6 +443,7 @@ __global__ void __launch_bounds__(256)
 // [128k, T), pad_tail[n_tiles] = 0.
 __global__ void __launch_bounds__(256)
     pad_tiles_kernel(int32_t pad_id, uint32_t T, uint32_t n_tiles, uint64_t *__restrict__ tile) {
+  pdl_wait_then_release();
   const uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (k >= n_tiles) return;
@@ -458,6 +460,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(1024)
     pad_suffix_kernel(const uint64_t *__restrict__ tile, uint32_t n_tiles,
                       uint64_t *__restrict__ pad_tail) {
+  pdl_wait_then_release();
   __shared__ uint64_t s_w[32];
   __shared__ uint64_t s_carry;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,11 +506,11 @@ cudaError_t launch_pad_tail(int32_t pad_id, uint32_t T, uint64_t *tile_scratch,
                             uint64_t *pad_tail, cudaStream_t st) {
   const uint32_t n_tiles = (T + kTile - 1) / kTile;
   ++launch_counter();
-  pad_tiles_kernel<<<(n_tiles * 32 + 255) / 256, 256, 0, st>>>(pad_id, T, n_tiles, tile_scratch);
+  pdl_launch(pad_tiles_kernel, (n_tiles * 32 + 255) / 256, 256, 0, st, pad_id, T, n_tiles, tile_scratch);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  pad_suffix_kernel<<<1, 1024, 0, st>>>(tile_scratch, n_tiles, pad_tail);
+  pdl_launch(pad_suffix_kernel, 1, 1024, 0, st, tile_scratch, n_tiles, pad_tail);
   return cudaGetLastError();
 }
 
@@ -527,7 +530,7 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
 cudaError_t launch_batch_fp(const uint64_t *row_fp, uint32_t n_steps, uint32_t n_rows,
                             uint64_t *out, cudaStream_t st) {
   ++launch_counter();
-  batch_fp_kernel<<<n_steps, 256, 0, st>>>(row_fp, n_rows, out);
+  pdl_launch(batch_fp_kernel, n_steps, 256, 0, st, row_fp, n_rows, out);
   return cudaGetLastError();
 }
 

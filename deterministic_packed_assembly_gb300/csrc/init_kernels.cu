@@ -25,6 +25,9 @@ constexpr int kThreads = 256;
 // spills; its warps are independent, so only the count per SM matters).
 constexpr int kHashThreads = 128;
 constexpr int kHashBlocksPerSM = 7;
+// 16-byte blocks a lane loads per step of the hash (128 tokens each), and as
+// many more in flight for the next step
+constexpr uint32_t kHashBlocksPerLane = 4;
 
 inline unsigned blocks_for(uint64_t n, int threads = kThreads) {
   return (unsigned)((n + threads - 1) / threads);
@@ -114,6 +117,7 @@ __device__ __forceinline__ int64_t tokens_needed(int32_t rmax, uint32_t G, uint3
 // 2^31 and end inside the token array.
 __global__ void validate_offsets_kernel(const int64_t *__restrict__ offs, uint32_t n_docs,
                                         uint64_t n_tokens, int *err) {
+  pdl_wait_then_release();
   uint64_t d = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (d > n_docs) return;
   int64_t o = offs[d];
@@ -129,6 +133,7 @@ __global__ void validate_offsets_kernel(const int64_t *__restrict__ offs, uint32
 // Round keys of the shuffle: K_r = splitmix64(splitmix64(seed) ^
 // splitmix64((stream << 8) | r)), r = 0..3.
 __global__ void stream_keys_kernel(uint64_t seed, uint32_t J, uint64_t *keys) {
+  pdl_wait_then_release();
   uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)J * 4) return;
   uint64_t j = i >> 2, r = i & 3;
@@ -224,6 +229,7 @@ __device__ __forceinline__ int64_t apportion_one(bool act, uint64_t v, uint64_t 
 // piece.
 __global__ void quota_sources_kernel(QuotaPieces q, uint32_t S, uint32_t K,
                                      int32_t *__restrict__ src_quota) {
+  pdl_wait();
   __shared__ __int128 delta[1024];
   __shared__ int order_s[1024];
   __shared__ int64_t scratch[33];
@@ -251,6 +257,7 @@ __global__ void quota_strata_kernel(QuotaPieces q, const int32_t *__restrict__ s
                                     const uint32_t *__restrict__ src_first, uint32_t S,
                                     uint32_t J, uint32_t K, int32_t *__restrict__ quota,
                                     int32_t *__restrict__ cum, unsigned *ready) {
+  pdl_wait();
   __shared__ __int128 delta[1024];
   __shared__ int order_s[1024];
   __shared__ int64_t scratch[33];
@@ -326,6 +333,7 @@ __global__ void __launch_bounds__(32)
     quota_warp_kernel(QuotaPieces q, uint32_t S, const uint32_t *__restrict__ src_first,
                       uint32_t J, uint32_t K, int32_t *__restrict__ quota,
                       int32_t *__restrict__ cum, unsigned *ready) {
+  pdl_wait();
   const int lane = threadIdx.x;
   const uint32_t s = blockIdx.x;
   const bool act = lane < (int)S;
@@ -393,6 +401,7 @@ __global__ void __launch_bounds__(32)
 // One block per update, a block-wide scan over the streams.
 __global__ void __launch_bounds__(256)
     row_base_kernel(const int32_t *__restrict__ quota, uint32_t J, int32_t *__restrict__ rb) {
+  pdl_wait_then_release();
   __shared__ int64_t ws[33];
   const uint32_t k = blockIdx.x;
   const int32_t *q = quota + (size_t)k * J;
@@ -450,6 +459,7 @@ template <bool kCopy>
 __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ tokens,
                                                    int32_t *__restrict__ dst, int64_t o0,
                                                    uint32_t L, int lane) {
+  constexpr uint32_t U = kHashBlocksPerLane, kStep = 128 * U;
   const int64_t a0 = o0 & ~(int64_t)3;
   const uint32_t sh = (uint32_t)(o0 - a0);
   const int4 *base = reinterpret_cast<const int4 *>(tokens + a0);
@@ -457,27 +467,27 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
   const uint32_t end = L + sh;
   const uint32_t l4 = 4 * (uint32_t)lane;
   uint64_t acc = 0;
-  int4 v[4];
+  int4 v[U];
 #pragma unroll
-  for (int u = 0; u < 4; u++) {
+  for (int u = 0; u < (int)U; u++) {
     const uint32_t ru = l4 + 128 * u;
     v[u] = make_int4(0, 0, 0, 0);
     if (ru < end) v[u] = __ldcs(base + (ru >> 2));
   }
   // r0: the step's first block offset, the same in every lane
-  for (uint32_t r0 = 0; r0 < end; r0 += 512) {
-    // the next step's four loads go out before this step's terms
-    int4 w[4];
+  for (uint32_t r0 = 0; r0 < end; r0 += kStep) {
+    // the next step's loads go out before this step's terms
+    int4 w[U];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const uint32_t ru = r0 + 512 + 128 * u + l4;
+    for (int u = 0; u < (int)U; u++) {
+      const uint32_t ru = r0 + kStep + 128 * u + l4;
       w[u] = make_int4(0, 0, 0, 0);
       if (ru < end) w[u] = __ldcs(base + (ru >> 2));
     }
     // each group of 128 tokens (one block per lane) is decided for the whole
     // warp: inside the document -> no checks; across an edge -> masked terms
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
+    for (int u = 0; u < (int)U; u++) {
       const uint32_t b0 = r0 + 128 * u;
       if (kCopy && b0 + l4 < end) dbase[(b0 >> 2) + lane] = v[u];
       if (b0 >= sh && b0 + 128 <= end)
@@ -486,7 +496,7 @@ __device__ __forceinline__ uint64_t warp_doc_terms(const int32_t *__restrict__ t
         acc += hash_terms_masked(v[u], b0 + l4 - sh, L);
     }
 #pragma unroll
-    for (int u = 0; u < 4; u++) v[u] = w[u];
+    for (int u = 0; u < (int)U; u++) v[u] = w[u];
   }
   return warp_sum_u64(acc);
 }
@@ -550,6 +560,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        unsigned long long *prog, uint32_t j_begin, uint32_t j_count,
                        const uint16_t *__restrict__ need_num, uint32_t need_num_all,
                        const unsigned long long *__restrict__ pre_cap) {
+  pdl_wait();
   constexpr uint32_t kGrab = 4;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -698,6 +709,7 @@ __global__ void __launch_bounds__(256)
                      uint32_t G, uint32_t first_num,
                      const unsigned long long *__restrict__ pre_cap,
                      uint16_t *__restrict__ need_num) {
+  pdl_wait_then_release();
   // a block per stream: the sample's raw and kept lengths are staged in
   // shared memory by all its threads at once, then one warp decides
   __shared__ uint32_t raw_s[kFillSample], kept_s[kFillSample];
@@ -797,6 +809,7 @@ __global__ void __launch_bounds__(kThreads)
                        const int64_t *__restrict__ kex, const int64_t *__restrict__ offs,
                        const int32_t *__restrict__ src, int32_t *__restrict__ dst,
                        unsigned long long *tokens_read) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const int lane = threadIdx.x & 31;
@@ -923,6 +936,7 @@ __global__ void order_bound_kernel(const uint32_t *__restrict__ sdb,
                                    const uint16_t *__restrict__ stream_bp,
                                    const unsigned long long *__restrict__ est_tok,
                                    uint32_t *__restrict__ pos_lim) {
+  pdl_wait_then_release();
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   const uint32_t b = sdb[j], e = sdb[j + 1];
@@ -951,6 +965,7 @@ __global__ void __launch_bounds__(kThreads)
                  const uint16_t *__restrict__ stream_bp_heldout_mode,
                  const uint32_t *__restrict__ pos_lim, uint32_t *__restrict__ order,
                  uint32_t *__restrict__ klen, int *err) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint32_t b0 = sdb[j];
@@ -1011,6 +1026,7 @@ constexpr int kScanTile = kScanWarps * kScanRounds * 32;
 __global__ void scan_tile_zero_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
                                       const uint32_t *__restrict__ pos_lim, uint64_t n,
                                       uint64_t nb, uint8_t *__restrict__ tile_zero) {
+  pdl_wait_then_release();
   const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= nb) return;
   const uint64_t t0 = t * kScanTile, t1 = min(n, t0 + kScanTile);
@@ -1032,6 +1048,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
                        const uint8_t *__restrict__ tile_zero, int64_t *__restrict__ bs_a,
                        int64_t *__restrict__ bs_b) {
+  pdl_wait_then_release();
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
   if (tile_zero && tile_zero[blockIdx.x]) {
     if (threadIdx.x == 0) {
@@ -1082,6 +1099,7 @@ __device__ __forceinline__ int64_t warp_incl_scan(int64_t x, int lane) {
 // One block: exclusive scan of the tile sums in place; totals to *tot_a/b.
 __global__ void __launch_bounds__(1024)
     scan_tiles_kernel(int64_t *bs_a, int64_t *bs_b, uint32_t nb, int64_t *tot_a, int64_t *tot_b) {
+  pdl_wait_then_release();
   __shared__ int64_t wa[32], wb[32];
   __shared__ int64_t carry_a, carry_b;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1126,6 +1144,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
                       const uint8_t *__restrict__ tile_zero, const int64_t *__restrict__ bs_a,
                       const int64_t *__restrict__ bs_b, int64_t *__restrict__ kex,
                       int64_t *__restrict__ pex) {
+  pdl_wait_then_release();
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
   if (tile_zero && tile_zero[blockIdx.x]) return;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1180,6 +1199,7 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
                               const uint32_t *__restrict__ pos_lim,
                               uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces,
                               int64_t *__restrict__ ptokens) {
+  pdl_wait_then_release();
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
@@ -1209,6 +1229,7 @@ __global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint
 __global__ void __launch_bounds__(1024)
     node_base_kernel(const int64_t *__restrict__ npieces, uint32_t J,
                      int64_t *__restrict__ node_base) {
+  pdl_wait_then_release();
   __shared__ int64_t ws[33];
   int64_t carry = 0;
   for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
@@ -1236,6 +1257,7 @@ __global__ void __launch_bounds__(kThreads)
                   const int32_t *__restrict__ loss_start, uint32_t T,
                   int64_t *__restrict__ node_src, int32_t *__restrict__ node_doc,
                   int32_t *__restrict__ node_mthr, int64_t *__restrict__ node_S) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t p = (uint64_t)blk * blockDim.x + threadIdx.x;
@@ -1276,6 +1298,7 @@ __global__ void __launch_bounds__(kThreads)
     next_kernel(SegGrid g, const int64_t *__restrict__ node_base,
                 const int64_t *__restrict__ npieces, const int64_t *__restrict__ node_S,
                 uint32_t T, int32_t *__restrict__ next) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const int64_t item = (int64_t)blk * blockDim.x + threadIdx.x;
@@ -1293,6 +1316,7 @@ __global__ void __launch_bounds__(kThreads)
 
 __global__ void jump_level_kernel(const int32_t *__restrict__ up, int64_t n,
                                   int32_t *__restrict__ out) {
+  pdl_wait_then_release();
   const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= n) return;
   out[x] = __ldg(up + __ldg(up + x));
@@ -1302,6 +1326,7 @@ __global__ void jump_level_kernel(const int32_t *__restrict__ up, int64_t n,
 // l + 2 is up o up o up o up, so one launch writes both from level l alone.
 __global__ void jump_two_levels_kernel(const int32_t *__restrict__ up, int64_t n,
                                        int32_t *__restrict__ out1, int32_t *__restrict__ out2) {
+  pdl_wait_then_release();
   const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= n) return;
   const int32_t b = __ldg(up + __ldg(up + x));
@@ -1314,6 +1339,7 @@ __global__ void count_windows_kernel(const int32_t *__restrict__ levels, int64_t
                                      uint32_t n_levels, const int64_t *__restrict__ node_base,
                                      const int64_t *__restrict__ npieces, uint32_t J,
                                      uint32_t *__restrict__ W) {
+  pdl_wait_then_release();
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   if (npieces[j] == 0) {
@@ -1339,6 +1365,7 @@ __global__ void __launch_bounds__(kThreads)
                          uint32_t n_levels, const int64_t *__restrict__ node_base,
                          const uint32_t *__restrict__ W, const int64_t *__restrict__ wbase,
                          int32_t *__restrict__ win_start) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
@@ -1370,6 +1397,7 @@ __global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t
                                    const int32_t *__restrict__ win_clip, uint32_t J, uint32_t B,
                                    uint32_t K, uint64_t seed, uint32_t G, uint32_t shuffle_rows,
                                    int4 *__restrict__ row_win, int *err) {
+  pdl_wait_then_release();
   const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= (uint64_t)K * B) return;
   const uint32_t k = (uint32_t)(x / B), slot = (uint32_t)(x % B);
@@ -1401,6 +1429,7 @@ __global__ void wrap_count_kernel(const int64_t *__restrict__ node_base,
                                   const uint32_t *__restrict__ cutoff,
                                   const uint32_t *__restrict__ sdb, uint32_t J, uint32_t T,
                                   uint32_t *__restrict__ W) {
+  pdl_wait_then_release();
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= J) return;
   const int64_t first = node_base[j], term = first + npieces[j];
@@ -1419,6 +1448,7 @@ __global__ void __launch_bounds__(kThreads)
                         const uint32_t *__restrict__ W, const int64_t *__restrict__ wbase,
                         uint32_t T, int32_t *__restrict__ win_start,
                         int32_t *__restrict__ win_end, int32_t *__restrict__ win_clip) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t w = (uint64_t)blk * blockDim.x + threadIdx.x;
@@ -1441,10 +1471,12 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // First update that asks a stream for a window past its last.
-__global__ void set_u32_kernel(uint32_t *p, uint32_t v) { *p = v; }
+__global__ void set_u32_kernel(uint32_t *p, uint32_t v) {
+  pdl_wait_then_release(); *p = v; }
 
 __global__ void first_bad_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
                                  uint32_t J, uint32_t K, uint32_t *first_bad) {
+  pdl_wait_then_release();
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)K * J) return;
   const uint32_t k = (uint32_t)(i / J), j = (uint32_t)(i % J);
@@ -1453,6 +1485,7 @@ __global__ void first_bad_kernel(const int32_t *__restrict__ cum, const uint32_t
 
 __global__ void valid_kernel(const uint32_t *first_bad, uint32_t K, uint32_t drain,
                              uint32_t *valid) {
+  pdl_wait_then_release();
   const uint32_t f = *first_bad;
   *valid = (f >= K) ? K : (drain ? f + 1 : f);
 }
@@ -1473,6 +1506,7 @@ __device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long l
 
 __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
                                      unsigned long long *acc) {
+  pdl_wait_then_release();
   const uint64_t n_fixed = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
   const uint64_t n = n_fixed + h.n_piece_items;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1503,6 +1537,7 @@ __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
 __global__ void digest_quota_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
                                     uint64_t h0, const uint32_t *valid,
                                     unsigned long long *acc) {
+  pdl_wait_then_release();
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint64_t term = 0;
   if (i < (uint64_t)K * J && i / J < *valid) term = digest_term((uint64_t)quota[i], h0 + i);
@@ -1512,6 +1547,7 @@ __global__ void digest_quota_kernel(const int32_t *__restrict__ quota, uint32_t 
 __global__ void __launch_bounds__(1024)
     digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
                        uint32_t J, const uint32_t *valid, int64_t *ubase) {
+  pdl_wait_then_release();
   __shared__ int64_t ws[33];
   const uint32_t v = *valid;
   int64_t carry = 0;
@@ -1536,6 +1572,7 @@ __global__ void __launch_bounds__(kThreads)
                           const int64_t *__restrict__ ubase, const uint32_t *__restrict__ W,
                           uint64_t seed, uint32_t G, const int32_t *__restrict__ win_clip,
                           int *err, unsigned long long *acc) {
+  pdl_wait_then_release();
   uint32_t j, blk;
   seg_locate(g, j, blk);
   const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
@@ -1556,6 +1593,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void digest_final_kernel(const unsigned long long *acc, uint64_t h0, uint32_t J,
                                     const uint32_t *valid, const int64_t *ubase,
                                     uint64_t *digest) {
+  pdl_wait_then_release();
   const uint64_t count = h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[J];
   *digest = splitmix64((uint64_t)acc[0] ^ count);
 }
@@ -1571,14 +1609,14 @@ uint64_t &launch_counter() {
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
                                     int *err, cudaStream_t st) {
   ++launch_counter();
-  validate_offsets_kernel<<<blocks_for((uint64_t)n_docs + 1), kThreads, 0, st>>>(offs, n_docs,
+  pdl_launch(validate_offsets_kernel, blocks_for((uint64_t)n_docs + 1), kThreads, 0, st, offs, n_docs,
                                                                                   n_tokens, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st) {
   ++launch_counter();
-  stream_keys_kernel<<<blocks_for((uint64_t)J * 4), kThreads, 0, st>>>(seed, J, keys);
+  pdl_launch(stream_keys_kernel, blocks_for((uint64_t)J * 4), kThreads, 0, st, seed, J, keys);
   return cudaGetLastError();
 }
 
@@ -1598,7 +1636,7 @@ static unsigned round_warps(uint32_t n) {
 cudaError_t launch_quota_sources(QuotaPieces q, uint32_t S, uint32_t K, int32_t *src_quota,
                                  cudaStream_t st) {
   ++launch_counter();
-  quota_sources_kernel<<<1, round_warps(S), 0, st>>>(q, S, K, src_quota);
+  pdl_launch(quota_sources_kernel, 1, round_warps(S), 0, st, q, S, K, src_quota);
   return cudaGetLastError();
 }
 
@@ -1607,7 +1645,7 @@ cudaError_t launch_quota_strata(QuotaPieces q, const int32_t *src_quota,
                                 uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st) {
   ++launch_counter();
-  quota_strata_kernel<<<S, round_warps(max_strata), 0, st>>>(q, src_quota, src_first, S, J, K,
+  pdl_launch(quota_strata_kernel, S, round_warps(max_strata), 0, st, q, src_quota, src_first, S, J, K,
                                                              quota, cum, ready);
   return cudaGetLastError();
 }
@@ -1617,13 +1655,13 @@ static void launch_quota_warp_s(QuotaPieces q, uint32_t S, const uint32_t *src_f
                                 uint32_t K, uint32_t max_strata, int32_t *quota, int32_t *cum,
                                 unsigned *ready, cudaStream_t st) {
   if (max_strata <= 1)
-    quota_warp_kernel<SMAX, 1><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
+    pdl_launch(quota_warp_kernel<SMAX, 1>, S, 32, 0, st, q, S, src_first, J, K, quota, cum, ready);
   else if (max_strata <= 4)
-    quota_warp_kernel<SMAX, 4><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
+    pdl_launch(quota_warp_kernel<SMAX, 4>, S, 32, 0, st, q, S, src_first, J, K, quota, cum, ready);
   else if (max_strata <= 8)
-    quota_warp_kernel<SMAX, 8><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
+    pdl_launch(quota_warp_kernel<SMAX, 8>, S, 32, 0, st, q, S, src_first, J, K, quota, cum, ready);
   else
-    quota_warp_kernel<SMAX, 32><<<S, 32, 0, st>>>(q, S, src_first, J, K, quota, cum, ready);
+    pdl_launch(quota_warp_kernel<SMAX, 32>, S, 32, 0, st, q, S, src_first, J, K, quota, cum, ready);
 }
 
 cudaError_t launch_quota_warp(QuotaPieces q, uint32_t S, const uint32_t *src_first, uint32_t J,
@@ -1644,7 +1682,7 @@ cudaError_t launch_quota_warp(QuotaPieces q, uint32_t S, const uint32_t *src_fir
 cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_t *rb,
                             cudaStream_t st) {
   ++launch_counter();
-  row_base_kernel<<<K, (J <= 32 ? 32 : J <= 128 ? 128 : 256), 0, st>>>(quota, J, rb);
+  pdl_launch(row_base_kernel, K, (J <= 32 ? 32 : J <= 128 ? 128 : 256), 0, st, quota, J, rb);
   return cudaGetLastError();
 }
 
@@ -1668,7 +1706,7 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
   constexpr int kMaxBlocks = 0xFFFF / (kHashThreads / 32);
   const dim3 grid(min(n_sms * kHashBlocksPerSM, kMaxBlocks)), block(kHashThreads);
 #define NS_HASH_LAUNCH(COPY, CHUNK)                                                          \
-  hash_prefix_kernel<COPY, CHUNK><<<grid, block, 0, st>>>(                                  \
+  pdl_launch(hash_prefix_kernel<COPY, CHUNK>, grid, block, 0, st,                                   \
       tokens, copy_dst, tokens_read, hashed, offs, sdb, stream_bp, J, D0, order, klen,          \
       cum_last, ready, ready_at, T, G, hash_key, want_heldout, frontier, prog, j_begin,         \
       j_count, need_num, need_num_all, pre_cap)
@@ -1694,7 +1732,7 @@ cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
                                unsigned long long *tokens_read, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  copy_prefix_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, stream_bp, order, klen,
+  pdl_launch(copy_prefix_kernel, g.n_blocks, kThreads, 0, st, g, sdb, D0, cutoff, stream_bp, order, klen,
                                                       kex, offs, src, dst, tokens_read);
   return cudaGetLastError();
 }
@@ -1711,7 +1749,7 @@ cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
                              cudaStream_t st) {
   if (J == 0) return cudaSuccess;
   ++launch_counter();
-  fill_need_kernel<<<J, 256, 0, st>>>(sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
+  pdl_launch(fill_need_kernel, J, 256, 0, st, sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
                                       T, G, first_num, pre_cap, need_num);
   return cudaGetLastError();
 }
@@ -1720,7 +1758,7 @@ cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_
                                const uint16_t *stream_bp, const unsigned long long *est_tok,
                                uint32_t *pos_lim, cudaStream_t st) {
   ++launch_counter();
-  order_bound_kernel<<<(J + kThreads - 1) / kThreads, kThreads, 0, st>>>(sdb, offs, J, stream_bp,
+  pdl_launch(order_bound_kernel, (J + kThreads - 1) / kThreads, kThreads, 0, st, sdb, offs, J, stream_bp,
                                                                           est_tok, pos_lim);
   return cudaGetLastError();
 }
@@ -1731,7 +1769,7 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  order_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, keys, offs, n_tokens, D0,
+  pdl_launch(order_kernel, g.n_blocks, kThreads, 0, st, g, sdb, keys, offs, n_tokens, D0,
                                                 stream_bp_heldout_mode, pos_lim, order, klen,
                                                 err);
   return cudaGetLastError();
@@ -1754,24 +1792,24 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   if (pos_lim && nb > 0) {
     tile_zero = reinterpret_cast<uint8_t *>(bs_b + (nb + 1));
     ++launch_counter();
-    scan_tile_zero_kernel<<<(unsigned)((nb + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+    pdl_launch(scan_tile_zero_kernel, (unsigned)((nb + kThreads - 1) / kThreads), kThreads, 0, st, 
         sdb, J, D0, pos_lim, n, nb, tile_zero);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (nb > 0) {
     ++launch_counter();
-    scan_reduce_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, tile_zero, bs_a,
+    pdl_launch(scan_reduce_kernel, (unsigned)nb, kScanWarps * 32, 0, st, klen, n, T, tile_zero, bs_a,
                                                                  bs_b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   ++launch_counter();
-  scan_tiles_kernel<<<1, 1024, 0, st>>>(bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
+  pdl_launch(scan_tiles_kernel, 1, 1024, 0, st, bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nb == 0) return e;
   ++launch_counter();
-  scan_apply_kernel<<<(unsigned)nb, kScanWarps * 32, 0, st>>>(klen, n, T, tile_zero, bs_a, bs_b,
+  pdl_launch(scan_apply_kernel, (unsigned)nb, kScanWarps * 32, 0, st, klen, n, T, tile_zero, bs_a, bs_b,
                                                                kex, pex);
   return cudaGetLastError();
 }
@@ -1779,6 +1817,7 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
 // Word runs of several device arrays gathered into one buffer (run s at
 // dst + off[s]), so that a single copy brings them all to the host.
 __global__ void __launch_bounds__(256) collect_kernel(CollectList l, uint32_t *__restrict__ dst) {
+  pdl_wait_then_release();
   const uint32_t s = blockIdx.y;
   if (s >= l.n) return;
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < l.words[s];
@@ -1792,7 +1831,7 @@ cudaError_t launch_collect(const CollectList &l, uint32_t *dst, cudaStream_t st)
   for (uint32_t s = 0; s < l.n; s++) most = most > l.words[s] ? most : l.words[s];
   ++launch_counter();
   const uint32_t gx = (most + 255) / 256 < 64 ? (most + 255) / 256 : 64;
-  collect_kernel<<<dim3(gx, l.n), 256, 0, st>>>(l, dst);
+  pdl_launch(collect_kernel, dim3(gx, l.n), 256, 0, st, l, dst);
   return cudaGetLastError();
 }
 
@@ -1801,7 +1840,7 @@ cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const in
                           const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,
                           int64_t *npieces, int64_t *ptokens, cudaStream_t st) {
   ++launch_counter();
-  cutoff_kernel<<<blocks_for(J, 128), 128, 0, st>>>(sdb, J, D0, kex, pex, cum_last, T, G,
+  pdl_launch(cutoff_kernel, blocks_for(J, 128), 128, 0, st, sdb, J, D0, kex, pex, cum_last, T, G,
                                                     need_num, pos_lim, cutoff, npieces, ptokens);
   return cudaGetLastError();
 }
@@ -1809,7 +1848,7 @@ cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const in
 cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
                              cudaStream_t st) {
   ++launch_counter();
-  node_base_kernel<<<1, (J <= 32 ? 32 : J <= 256 ? 256 : 1024), 0, st>>>(npieces, J, node_base);
+  pdl_launch(node_base_kernel, 1, (J <= 32 ? 32 : J <= 256 ? 256 : 1024), 0, st, npieces, J, node_base);
   return cudaGetLastError();
 }
 
@@ -1821,7 +1860,7 @@ cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uin
                           int64_t *node_S, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  expand_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, sdb, D0, cutoff, order, klen, kex, pex,
+  pdl_launch(expand_kernel, g.n_blocks, kThreads, 0, st, g, sdb, D0, cutoff, order, klen, kex, pex,
                                                  node_base, npieces, offs, loss_start, T,
                                                  node_src, node_doc, node_mthr, node_S);
   return cudaGetLastError();
@@ -1831,14 +1870,14 @@ cudaError_t launch_next(SegGrid g, const int64_t *node_base, const int64_t *npie
                         const int64_t *node_S, uint32_t T, int32_t *next, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  next_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, node_base, npieces, node_S, T, next);
+  pdl_launch(next_kernel, g.n_blocks, kThreads, 0, st, g, node_base, npieces, node_S, T, next);
   return cudaGetLastError();
 }
 
 cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
                               cudaStream_t st) {
   ++launch_counter();
-  jump_level_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
+  pdl_launch(jump_level_kernel, blocks_for((uint64_t)n_nodes), kThreads, 0, st, up_prev, n_nodes,
                                                                          up_next);
   return cudaGetLastError();
 }
@@ -1846,7 +1885,7 @@ cudaError_t launch_jump_level(const int32_t *up_prev, int64_t n_nodes, int32_t *
 cudaError_t launch_jump_two_levels(const int32_t *up_prev, int64_t n_nodes, int32_t *up_next,
                                    int32_t *up_next2, cudaStream_t st) {
   ++launch_counter();
-  jump_two_levels_kernel<<<blocks_for((uint64_t)n_nodes), kThreads, 0, st>>>(up_prev, n_nodes,
+  pdl_launch(jump_two_levels_kernel, blocks_for((uint64_t)n_nodes), kThreads, 0, st, up_prev, n_nodes,
                                                                               up_next, up_next2);
   return cudaGetLastError();
 }
@@ -1855,7 +1894,7 @@ cudaError_t launch_count_windows(const int32_t *levels, int64_t n_nodes, uint32_
                                  const int64_t *node_base, const int64_t *npieces, uint32_t J,
                                  uint32_t *W, cudaStream_t st) {
   ++launch_counter();
-  count_windows_kernel<<<blocks_for(J, 128), 128, 0, st>>>(levels, n_nodes, n_levels, node_base,
+  pdl_launch(count_windows_kernel, blocks_for(J, 128), 128, 0, st, levels, n_nodes, n_levels, node_base,
                                                            npieces, J, W);
   return cudaGetLastError();
 }
@@ -1865,7 +1904,7 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
                                  const int64_t *wbase, int32_t *win_start, cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  window_starts_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, levels, n_nodes, n_levels, node_base,
+  pdl_launch(window_starts_kernel, g.n_blocks, kThreads, 0, st, g, levels, n_nodes, n_levels, node_base,
                                                         W, wbase, win_start);
   return cudaGetLastError();
 }
@@ -1877,7 +1916,7 @@ cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint
                                uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *row_win,
                                int *err, cudaStream_t st) {
   ++launch_counter();
-  row_windows_kernel<<<blocks_for((uint64_t)K * B), kThreads, 0, st>>>(
+  pdl_launch(row_windows_kernel, blocks_for((uint64_t)K * B), kThreads, 0, st, 
       rb, cum, W, wbase, win_start, next, win_end, win_clip, J, B, K, seed, G, shuffle_rows,
       row_win, err);
   return cudaGetLastError();
@@ -1889,12 +1928,12 @@ cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64
                                 const int64_t *wbase, int32_t *win_start, int32_t *win_end,
                                 int32_t *win_clip, cudaStream_t st) {
   ++launch_counter();
-  wrap_count_kernel<<<blocks_for(J, 128), 128, 0, st>>>(node_base, npieces, node_S, cutoff, sdb,
+  pdl_launch(wrap_count_kernel, blocks_for(J, 128), 128, 0, st, node_base, npieces, node_S, cutoff, sdb,
                                                         J, T, W);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || g.n_blocks == 0) return e;
   ++launch_counter();
-  wrap_windows_kernel<<<g.n_blocks, kThreads, 0, st>>>(g, node_base, npieces, node_S, W, wbase,
+  pdl_launch(wrap_windows_kernel, g.n_blocks, kThreads, 0, st, g, node_base, npieces, node_S, W, wbase,
                                                        T, win_start, win_end, win_clip);
   return cudaGetLastError();
 }
@@ -1903,15 +1942,15 @@ cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J
                                uint32_t drain, uint32_t *first_bad, uint32_t *valid,
                                cudaStream_t st) {
   ++launch_counter();
-  set_u32_kernel<<<1, 1, 0, st>>>(first_bad, K);
+  pdl_launch(set_u32_kernel, 1, 1, 0, st, first_bad, K);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  first_bad_kernel<<<blocks_for((uint64_t)K * J), kThreads, 0, st>>>(cum, W, J, K, first_bad);
+  pdl_launch(first_bad_kernel, blocks_for((uint64_t)K * J), kThreads, 0, st, cum, W, J, K, first_bad);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  valid_kernel<<<1, 1, 0, st>>>(first_bad, K, drain, valid);
+  pdl_launch(valid_kernel, 1, 1, 0, st, first_bad, K, drain, valid);
   return cudaGetLastError();
 }
 
@@ -1924,22 +1963,22 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
                           int64_t *ubase, uint64_t *digest_out, cudaStream_t st) {
   const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
   ++launch_counter();
-  digest_header_kernel<<<blocks_for(h0), kThreads, 0, st>>>(h, valid, acc);
+  pdl_launch(digest_header_kernel, blocks_for(h0), kThreads, 0, st, h, valid, acc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  digest_quota_kernel<<<blocks_for((uint64_t)K * h.J), kThreads, 0, st>>>(quota, h.J, K, h0,
+  pdl_launch(digest_quota_kernel, blocks_for((uint64_t)K * h.J), kThreads, 0, st, quota, h.J, K, h0,
                                                                            valid, acc);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  digest_used_kernel<<<1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st>>>(cum, W, h.J, valid,
+  pdl_launch(digest_used_kernel, 1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st, cum, W, h.J, valid,
                                                                             ubase);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (wg.n_blocks > 0) {
     ++launch_counter();
-    digest_windows_kernel<<<wg.n_blocks, kThreads, 0, st>>>(wg, wbase, win_start, node_src,
+    pdl_launch(digest_windows_kernel, wg.n_blocks, kThreads, 0, st, wg, wbase, win_start, node_src,
                                                             node_doc, offs, T, h0, h.J, valid,
                                                             ubase, W, seed, G, win_clip, err,
                                                             acc);
@@ -1947,7 +1986,7 @@ cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const in
     if (e != cudaSuccess) return e;
   }
   ++launch_counter();
-  digest_final_kernel<<<1, 1, 0, st>>>(acc, h0, h.J, valid, ubase, digest_out);
+  pdl_launch(digest_final_kernel, 1, 1, 0, st, acc, h0, h.J, valid, ubase, digest_out);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ namespace {
 __global__ void __launch_bounds__(256)
     step_learned_kernel(const int32_t *__restrict__ row_learned, uint32_t n_rows,
                         int64_t *__restrict__ out) {
+  pdl_wait_then_release();
   __shared__ int64_t part[8];
   const int32_t *r = row_learned + (size_t)blockIdx.x * n_rows;
   int64_t acc = 0;
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_step_learned(const int32_t *row_learned, uint32_t n_steps, uint32_t n_rows,
                                 int64_t *out, cudaStream_t st) {
   ++launch_counter();
-  step_learned_kernel<<<n_steps, 256, 0, st>>>(row_learned, n_rows, out);
+  pdl_launch(step_learned_kernel, n_steps, 256, 0, st, row_learned, n_rows, out);
   return cudaGetLastError();
 }
 
