@@ -92,8 +92,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also", default="c4",
-                    help="comma-separated workloads also measured (fewer steps, no CPU "
-                         "baseline) and reported under extra_configs; '' for none")
+                    help="comma-separated workloads also measured (no CPU baseline) and "
+                         "reported under extra_configs; 'none' for none")
     return ap.parse_args()
 
 
@@ -717,7 +717,7 @@ def run_ours(args, dist: Dist) -> None:
     # the other workloads named with it, each timed the same way (GPU pass,
     # gather roofline, e2e); no CPU baseline
     extra = {}
-    for name in [x for x in args.also.split(",") if x and x != args.config]:
+    for name in [x for x in args.also.split(",") if x and x not in ("none", args.config)]:
         # four times the steps: a pass of these is a few ms, and the clock
         # sampler needs a timed region of a few of its 50 ms periods
         r = measure(args, dist, name, e2e=not args.no_e2e, cpu=False,
