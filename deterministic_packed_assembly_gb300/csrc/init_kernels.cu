@@ -953,10 +953,14 @@ __global__ void order_bound_kernel(const uint32_t *__restrict__ sdb,
 }
 
 // Each thread takes kOrderPerThread positions of one stream, p0 + m * 256,
-// one after the other, and every pass of its loop is one evaluation of the
-// network for every lane: a lane whose walk lands in range writes that
-// position and feeds its next one into the same evaluation.  A warp then
-// pays for the average walk of its positions rather than the longest.
+// one after the other, and every pass of its walk loop is one evaluation of
+// the network for every lane: a lane whose walk lands in range records that
+// document and feeds its next position into the same evaluation.  A warp
+// then pays for the average walk of its positions rather than the longest.
+// The documents wait in a register queue (shifted at each landing, so that
+// no register array is indexed at run time); once every walk has landed,
+// the offsets of all of them are read together, so their latencies overlap
+// instead of adding up.
 constexpr uint32_t kOrderPerThread = 8;
 
 __global__ void __launch_bounds__(kThreads)
@@ -973,38 +977,59 @@ __global__ void __launch_bounds__(kThreads)
   const uint64_t Nb = pos_lim ? pos_lim[j] : N;  // the positions taken
   const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
   if (p0 >= Nb) return;
-  uint32_t bits = (N <= 1) ? 0u : (uint32_t)(64 - __clzll((long long)(N - 1)));
-  if (bits < 2) bits = 2;
-  bits += bits & 1u;
-  const uint32_t half = bits >> 1;
+  const uint32_t half = feistel_half(N);
   const uint64_t mask = (half >= 64) ? ~0ull : ((1ull << half) - 1);
   uint64_t k[4];
 #pragma unroll
   for (int r = 0; r < 4; r++) k[r] = keys[(size_t)j * 4 + r];
-  // the validation stream of a source that holds nothing out is empty
-  const bool empty = stream_bp_heldout_mode && stream_bp_heldout_mode[j] == 0;
-  uint64_t p = p0, x = p0;
+  // the positions this thread takes: p0 + m * blockDim.x for m < cnt
+  const uint64_t left = (Nb - p0 + blockDim.x - 1) / blockDim.x;
+  const uint32_t cnt = left < kOrderPerThread ? (uint32_t)left : kOrderPerThread;
+  // walks; the documents of positions m go to q[cnt - 1 - m] (each landing
+  // shifts the queue by one)
+  uint32_t q[kOrderPerThread];
+#pragma unroll
+  for (uint32_t m = 0; m < kOrderPerThread; m++) q[m] = 0;
+  uint64_t x = p0;
   uint32_t m = 0, it = 0;
-  while (true) {
+  while (m < cnt) {
     uint64_t y = feistel(k, half, mask, x);
     if (y >= N && ++it > (1u << 20)) {
       set_error(err, kDevWalkLimit);
       y = 0;
     }
     if (y < N) {
-      const uint32_t d = b0 + (uint32_t)y;
-      const int64_t o0 = __ldg(offs + d), o1 = __ldg(offs + d + 1);
-      const bool ok =
-          !empty && o0 >= 0 && o1 > o0 && (uint64_t)o1 <= n_tokens && o1 - o0 <= 0x7FFFFFFF;
-      const uint64_t idx = (uint64_t)b0 + p - D0;
-      order[idx] = d;
-      klen[idx] = ok ? (uint32_t)(o1 - o0) : 0u;
-      p += blockDim.x;
-      if (++m >= kOrderPerThread || p >= Nb) break;
-      x = p;
+#pragma unroll
+      for (uint32_t u = kOrderPerThread - 1; u > 0; u--) q[u] = q[u - 1];
+      q[0] = b0 + (uint32_t)y;
+      x = p0 + (uint64_t)(++m) * blockDim.x;
       it = 0;
     } else {
       x = y;
+    }
+  }
+  // every document's offsets, read together
+  int64_t o0[kOrderPerThread], o1[kOrderPerThread];
+#pragma unroll
+  for (uint32_t u = 0; u < kOrderPerThread; u++) {
+    o0[u] = 0;
+    o1[u] = 0;
+    if (u < cnt) {
+      o0[u] = __ldg(offs + q[u]);
+      o1[u] = __ldg(offs + q[u] + 1);
+    }
+  }
+  // the validation stream of a source that holds nothing out is empty
+  const bool empty = stream_bp_heldout_mode && stream_bp_heldout_mode[j] == 0;
+#pragma unroll
+  for (uint32_t u = 0; u < kOrderPerThread; u++) {
+    if (u < cnt) {
+      const uint64_t pm = p0 + (uint64_t)(cnt - 1 - u) * blockDim.x;
+      const bool ok = !empty && o0[u] >= 0 && o1[u] > o0[u] && (uint64_t)o1[u] <= n_tokens &&
+                      o1[u] - o0[u] <= 0x7FFFFFFF;
+      const uint64_t idx = (uint64_t)b0 + pm - D0;
+      order[idx] = q[u];
+      klen[idx] = ok ? (uint32_t)(o1[u] - o0[u]) : 0u;
     }
   }
 }
