@@ -14,7 +14,10 @@ Parity status: every function is pinned by tests that do not re-derive it --
 published SplitMix64 outputs, a hand-worked packing example and quota
 example, brute-force properties on tiny inputs (Feistel bijectivity and its
 inverse, greedy maximality, exactly-once coverage, quota bounds and the
-exhaustive subset choice), binomial bounds on the held-out rate.  The pages
+exhaustive subset choice), binomial bounds on the held-out rate, the row
+fingerprint's keys recovered through the inverse against hand-worked
+special cases, and the order digest against the fold of the items rebuilt
+from the pinned read-outs.  The pages
 print no worked values for this path, so page-level parity of the readings
 (what is hashed, the shuffle's construction, the fingerprint) is unpinned.
 """
