@@ -226,14 +226,24 @@ typedef struct {
 /* Build the context: validate, then on cfg->cuda_stream hash the documents of
  * every source with a held-out rate, shuffle every stream, pack the prefix of
  * each stream that max_steps can reach, number its windows and apportion every
- * update of the horizon.  Synchronises the stream twice.  On success
+ * update of the horizon.  Defined by: NeuronSpark-Trainer README, Concepts
+ * (held out by a hash of the text, the same in every line; documents
+ * shuffled; cut at document ends; every source within two samples of its
+ * share in every update, strata at theirs; max_epochs 1) and Training (the
+ * sample order's digest, ns_pack_info.order_digest, checked on resume).
+ * Synchronises the stream twice.  On success
  * *out owns device tables allocated through cfg->alloc; on failure nothing is
  * kept and *out is NULL.  Errors: INVALID_ARG, CUDA, OOM, BAD_INPUT. */
 int ns_pack_init(const ns_pack_config *cfg, ns_pack_ctx **out);
 
 /* Assemble rows [row_begin, row_end) of updates [step0, step0 + n_steps) into
  * `out`, asynchronously on cuda_stream (NULL: the context's stream).  One
- * kernel launch.  The bytes of every row are the same whatever the row range
+ * kernel launch.  Defined by: Linnet training docs, Supervised fine-tuning
+ * (rows of exactly T positions, padded; completion tokens learned) and Other
+ * trainers (a position id of 0 starts a new sequence); "Zephon:
+ * deterministic data loading", checkpoint on 16 GPUs and resume on 8/32/64
+ * (a batch's bytes do not depend on how its rows are split); per-row
+ * fingerprint and learned count in the same pass.  The bytes of every row are the same whatever the row range
  * or the step batching.  Errors: INVALID_ARG (n_steps == 0, empty or out-of-
  * range rows, NULL or misaligned outputs), HORIZON (step0 + n_steps >
  * max_steps), EXHAUSTED (step0 + n_steps > valid_steps), CUDA.  With a
@@ -242,7 +252,9 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
                  uint32_t row_end, const ns_pack_out *out, void *cuda_stream);
 
 /* Fold n_rows row fingerprints (device, in row order) into the batch
- * fingerprint F = fold(F ^ fp_i) and copy it to *batch_fp_host; synchronises
+ * fingerprint F = fold(F ^ fp_i) and copy it to *batch_fp_host (a hash of
+ * every global batch: "Zephon: deterministic data loading", checkpoint on
+ * 16 GPUs, resume on 8/32/64); synchronises
  * cuda_stream (NULL: the context's).  Also reports the device error word.
  * Uses one word of the context's memory: calls on one context must not
  * overlap (ns_pack_batch_fp writes to caller memory and has no such limit).
@@ -267,21 +279,27 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
 int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
                          uint32_t n_rows, int64_t *learned_dev, void *cuda_stream);
 
-/* Summary of the context (host memory, no synchronisation). */
+/* Summary of the context (host memory, no synchronisation): the valid
+ * horizon (NeuronSpark-Trainer README, Concepts: running out of a source is
+ * an error), the order digest (same README, Training), what init read. */
 int ns_pack_info(const ns_pack_ctx *ctx, ns_pack_info_t *info);
 
-/* Per stream (host arrays of n_streams): windows packed at init and whether
+/* Per stream (host arrays of n_streams; the greedy packing of NeuronSpark-
+ * Trainer README, Concepts, cut at document ends): windows packed at init and whether
  * that count is the stream's total (1) or only the prefix the horizon reaches
  * (0, in which case it exceeds every window the horizon asks for). */
 int ns_pack_stream_windows(const ns_pack_ctx *ctx, uint64_t *windows, uint8_t *complete);
 
-/* Copy the quota tables to the host: quota[k][j] windows of stream j in
+/* Copy the quota tables (NeuronSpark-Trainer README, Concepts: each source
+ * within two samples of its share in every update, strata at theirs) to the
+ * host: quota[k][j] windows of stream j in
  * update k (max_steps x n_streams, int32) and cum[k][j] windows before update
  * k ((max_steps + 1) x n_streams, int32).  Either may be NULL.  Synchronises
  * the context's stream.  Errors: INVALID_ARG, CUDA. */
 int ns_pack_quota_table(const ns_pack_ctx *ctx, int32_t *quota, int32_t *cum);
 
-/* Synchronise the context's stream and report the device error word.
+/* Synchronise the context's stream and report the device error word (the
+ * checks fail fast: "Zephon: deterministic data loading", TorchTitan).
  * Errors: CUDA, DEVICE, BAD_INPUT. */
 int ns_pack_check(ns_pack_ctx *ctx);
 
