@@ -853,13 +853,18 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   if (n_nodes >= (int64_t)0x7FFFFFFF) return NS_ERR_INVALID_ARG;
   c->n_pieces = (uint64_t)(n_nodes - J);
   c->complete.resize(J);
-  int64_t max_pieces = 0;
+  // Pointer-jumping levels: enough for any stream's window count.  A window
+  // holds at least one piece, and two consecutive greedy windows hold more
+  // than T tokens (the second one's first piece did not fit in the first),
+  // so a prefix of p kept tokens packs fewer than 2 ceil(p / T) + 2 windows.
+  int64_t max_windows = 0;
   for (uint32_t j = 0; j < J; j++) {
     c->complete[j] = (cut_h[j] == N[j]) ? 1 : 0;
-    max_pieces = std::max(max_pieces, np_h[j]);
+    const int64_t by_tokens = 2 * ((pt_h[j] + (int64_t)T - 1) / (int64_t)T) + 1;
+    max_windows = std::max(max_windows, std::min(np_h[j], by_tokens));
   }
   uint32_t L = 1;
-  while ((1ll << L) < max_pieces + 1) L++;
+  while ((1ll << L) < max_windows + 1) L++;
   if (wrap) L = 0;  // wrap windows are found by position, without pointer jumping
   c->levels = L;
 

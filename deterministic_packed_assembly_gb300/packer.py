@@ -182,15 +182,24 @@ class Packer:
         o.row_len = out["row_len"].data_ptr() if out.get("row_len") is not None else None
         return o
 
+    @staticmethod
+    def prepare(out: dict) -> L.ns_pack_out:
+        """The C description of the buffers in ``out``, built once for steps
+        that write the same buffers again (``step(..., prepared=...)``)."""
+        return Packer._out_struct(out)
+
     def step(self, step0: int, n_steps: int = 1, rows: Optional[tuple] = None,
-             out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+             out: Optional[dict] = None, stream: Optional[torch.cuda.Stream] = None,
+             prepared: Optional[L.ns_pack_out] = None) -> dict:
         """Assemble rows ``rows = (begin, end)`` of updates [step0, step0 +
-        n_steps) into ``out`` (allocated if None); asynchronous."""
+        n_steps) into ``out`` (allocated if None); asynchronous.  ``prepared``
+        (from ``prepare(out)``) saves describing ``out`` again."""
         r0, r1 = (0, self.rows_of_step(step0)) if rows is None else rows
         if out is None:
             out = self.empty_out(n_steps, r1 - r0)
         st = (stream or self.stream).cuda_stream
-        L.ns_pack_step(self._ctx, step0, n_steps, r0, r1, self._out_struct(out), st)
+        L.ns_pack_step(self._ctx, step0, n_steps, r0, r1,
+                       prepared if prepared is not None else self._out_struct(out), st)
         return out
 
     def batch_fp(self, row_fp: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
