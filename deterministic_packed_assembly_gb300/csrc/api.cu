@@ -710,9 +710,11 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // tokens read from host memory in place (hash and prefix copy)
   // The summary the host reads back at the end, in one block (one copy):
   // tokens read from host memory u64 | tokens and documents hashed u64[2] |
-  // order digest u64 | valid updates u32 | error word | windows u32[J]
-  constexpr size_t r2_read = 0, r2_hashed = 8, r2_digest = 24, r2_valid = 32, r2_err = 36;
-  constexpr size_t r2_W = 40;
+  // the digest's accumulator u64[2] | the first bad update (K - k) u32 |
+  // order digest u64 | valid updates u32 | error word | windows u32[J]; its
+  // first 48 bytes (counters and accumulators) start at zero
+  constexpr size_t r2_read = 0, r2_hashed = 8, r2_dacc = 24, r2_bad = 40, r2_digest = 48;
+  constexpr size_t r2_valid = 56, r2_err = 60, r2_W = 64;
   const size_t r2_bytes = r2_W + (size_t)J * 4;
   char *rb2 = a.temp<char>(r2_bytes);
   NS_ALLOC(rb2);
@@ -969,7 +971,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   int32_t *win_end = wrap ? a.temp<int32_t>(n_win) : nullptr;
   int32_t *win_clip = wrap ? a.temp<int32_t>(n_win) : nullptr;
   c->row_win = a.keep<int4>((size_t)K * c->B);
-  uint32_t *first_bad = a.temp<uint32_t>(1);
+  uint32_t *bad_inv = reinterpret_cast<uint32_t *>(rb2 + r2_bad);
   uint32_t *valid = reinterpret_cast<uint32_t *>(rb2 + r2_valid);
   NS_ALLOC(c->W);
   NS_ALLOC(win_start);
@@ -978,7 +980,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(win_clip);
   }
   NS_ALLOC(c->row_win);
-  NS_ALLOC(first_bad);
   std::vector<uint32_t> wb = seg_layout(rmax, 256);
   void *d_wb;
   if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
@@ -996,16 +997,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                 win_clip, J, c->B, K, c->seed, c->G,
                                 (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u, c->row_win, c->err,
                                 st));
-  NS_CK(nsk::launch_valid_steps(c->cum, c->W, J, K, (c->flags & NS_PACK_DRAIN) ? 1u : 0u,
-                                first_bad, valid, st));
+  NS_CK(nsk::launch_first_bad(c->cum, c->W, J, K, bad_inv, st));
 
   // ---- 8. order digest ----------------------------------------------------
-  unsigned long long *dacc = a.temp<unsigned long long>(2);
+  unsigned long long *dacc = reinterpret_cast<unsigned long long *>(rb2 + r2_dacc);
   int64_t *ubase = a.temp<int64_t>(J + 1);
   uint64_t *digest = reinterpret_cast<uint64_t *>(rb2 + r2_digest);
-  NS_ALLOC(dacc);
   NS_ALLOC(ubase);
-  NS_CK(cudaMemsetAsync(dacc, 0, 2 * sizeof(unsigned long long), st));
   nsk::DigestHeader h{};
   h.scalars[0] = T;
   h.scalars[1] = c->B;
@@ -1028,9 +1026,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.n_piece_items = piece_items.size();
   h.S = S;
   h.J = J;
-  NS_CK(nsk::launch_digest(h, valid, c->quota, c->cum, c->W, wg, c->wbase, win_start,
-                           c->node_src, c->node_doc, c->offs, T, K, c->seed, c->G, win_clip,
-                           c->err, dacc, ubase, digest, st));
+  NS_CK(nsk::launch_digest(h, bad_inv, (c->flags & NS_PACK_DRAIN) ? 1u : 0u, valid, c->quota,
+                           c->cum, c->W, wg, c->wbase, win_start, c->node_src, c->node_doc,
+                           c->offs, T, K, c->seed, c->G, win_clip, c->err, dacc, ubase, digest,
+                           st));
 
   // ---- 9. read back the summary ------------------------------------------
   if (prefix_copy) NS_CK(cudaStreamWaitEvent(st, side.join, 0));

@@ -1496,23 +1496,24 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // First update that asks a stream for a window past its last.
-__global__ void set_u32_kernel(uint32_t *p, uint32_t v) {
-  pdl_wait_then_release(); *p = v; }
 
+// The first update that asks a stream for a window it does not have, as
+// K - k in *bad_inv (zeroed before: 0 means none).
 __global__ void first_bad_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
-                                 uint32_t J, uint32_t K, uint32_t *first_bad) {
+                                 uint32_t J, uint32_t K, uint32_t *bad_inv) {
   pdl_wait_then_release();
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)K * J) return;
   const uint32_t k = (uint32_t)(i / J), j = (uint32_t)(i % J);
-  if ((uint32_t)cum[(size_t)(k + 1) * J + j] > W[j]) atomicMin(first_bad, k);
+  if ((uint32_t)cum[(size_t)(k + 1) * J + j] > W[j]) atomicMax(bad_inv, K - k);
 }
 
-__global__ void valid_kernel(const uint32_t *first_bad, uint32_t K, uint32_t drain,
-                             uint32_t *valid) {
-  pdl_wait_then_release();
-  const uint32_t f = *first_bad;
-  *valid = (f >= K) ? K : (drain ? f + 1 : f);
+// Updates [0, valid) can be assembled: up to the first bad one, or through
+// it with drain.
+__device__ __forceinline__ uint32_t valid_from(uint32_t bad_inv, uint32_t K, uint32_t drain) {
+  if (bad_inv == 0) return K;
+  const uint32_t f = K - bad_inv;
+  return drain ? f + 1 : f;
 }
 
 // ---------------------------------------------------------------------------
@@ -1529,17 +1530,21 @@ __device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long l
   if (threadIdx.x == 0) atomicAdd(acc, (unsigned long long)s);
 }
 
-__global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
-                                     unsigned long long *acc) {
+// The item list's recipe part (items [0, h0)) and the quota of every valid
+// update (items h0 + k J + j) in one launch.
+__global__ void digest_items_kernel(DigestHeader h, const int32_t *__restrict__ quota,
+                                    uint32_t K, const uint32_t *valid,
+                                    unsigned long long *acc) {
   pdl_wait_then_release();
   const uint64_t n_fixed = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
-  const uint64_t n = n_fixed + h.n_piece_items;
+  const uint64_t h0 = n_fixed + h.n_piece_items;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t v = *valid;
   uint64_t term = 0;
-  if (i < n) {
+  if (i < h0) {
     uint64_t x;
     if (i < kDigestScalars) {
-      x = (i == 3) ? (uint64_t)*valid : h.scalars[i];
+      x = (i == 3) ? (uint64_t)v : h.scalars[i];
     } else if (i < kDigestScalars + 2ull * h.S) {
       const uint64_t q = i - kDigestScalars, s = q >> 1;
       x = (q & 1) ? (uint64_t)h.source_bp[s] : (uint64_t)h.source_weight[s];
@@ -1555,26 +1560,22 @@ __global__ void digest_header_kernel(DigestHeader h, const uint32_t *valid,
       }
     }
     term = digest_term(x, i);
+  } else if (i - h0 < (uint64_t)K * h.J && (i - h0) / h.J < v) {
+    term = digest_term((uint64_t)quota[i - h0], i);
   }
   digest_accumulate(term, acc);
 }
 
-__global__ void digest_quota_kernel(const int32_t *__restrict__ quota, uint32_t J, uint32_t K,
-                                    uint64_t h0, const uint32_t *valid,
-                                    unsigned long long *acc) {
-  pdl_wait_then_release();
-  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  uint64_t term = 0;
-  if (i < (uint64_t)K * J && i / J < *valid) term = digest_term((uint64_t)quota[i], h0 + i);
-  digest_accumulate(term, acc);
-}
-
+// One block: the valid horizon (written to *valid), then the first item of
+// each stream's used windows, ubase[j] (a scan of min(cum[valid][j], W[j])).
 __global__ void __launch_bounds__(1024)
     digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
-                       uint32_t J, const uint32_t *valid, int64_t *ubase) {
+                       uint32_t J, const uint32_t *bad_inv, uint32_t K, uint32_t drain,
+                       uint32_t *valid, int64_t *ubase) {
   pdl_wait_then_release();
   __shared__ int64_t ws[33];
-  const uint32_t v = *valid;
+  const uint32_t v = valid_from(*bad_inv, K, drain);
+  if (threadIdx.x == 0) *valid = v;
   int64_t carry = 0;
   for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
     const uint32_t j = c0 + threadIdx.x;
@@ -1963,42 +1964,31 @@ cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
-                               uint32_t drain, uint32_t *first_bad, uint32_t *valid,
-                               cudaStream_t st) {
+cudaError_t launch_first_bad(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
+                             uint32_t *bad_inv, cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(set_u32_kernel, 1, 1, 0, st, first_bad, K);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ++launch_counter();
-  pdl_launch(first_bad_kernel, blocks_for((uint64_t)K * J), kThreads, 0, st, cum, W, J, K, first_bad);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ++launch_counter();
-  pdl_launch(valid_kernel, 1, 1, 0, st, first_bad, K, drain, valid);
+  pdl_launch(first_bad_kernel, blocks_for((uint64_t)K * J), kThreads, 0, st, cum, W, J, K,
+             bad_inv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const int32_t *quota,
-                          const int32_t *cum, const uint32_t *W, SegGrid wg,
-                          const int64_t *wbase, const int32_t *win_start,
-                          const int64_t *node_src, const int32_t *node_doc,
-                          const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
-                          const int32_t *win_clip, int *err, unsigned long long *acc,
-                          int64_t *ubase, uint64_t *digest_out, cudaStream_t st) {
+cudaError_t launch_digest(const DigestHeader &h, const uint32_t *bad_inv, uint32_t drain,
+                          uint32_t *valid, const int32_t *quota, const int32_t *cum,
+                          const uint32_t *W, SegGrid wg, const int64_t *wbase,
+                          const int32_t *win_start, const int64_t *node_src,
+                          const int32_t *node_doc, const int64_t *offs, uint32_t T, uint32_t K,
+                          uint64_t seed, uint32_t G, const int32_t *win_clip, int *err,
+                          unsigned long long *acc, int64_t *ubase, uint64_t *digest_out,
+                          cudaStream_t st) {
   const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
   ++launch_counter();
-  pdl_launch(digest_header_kernel, blocks_for(h0), kThreads, 0, st, h, valid, acc);
+  pdl_launch(digest_used_kernel, 1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st, cum, W,
+             h.J, bad_inv, K, drain, valid, ubase);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++launch_counter();
-  pdl_launch(digest_quota_kernel, blocks_for((uint64_t)K * h.J), kThreads, 0, st, quota, h.J, K, h0,
-                                                                           valid, acc);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ++launch_counter();
-  pdl_launch(digest_used_kernel, 1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st, cum, W, h.J, valid,
-                                                                            ubase);
+  pdl_launch(digest_items_kernel, blocks_for(h0 + (uint64_t)K * h.J), kThreads, 0, st, h, quota,
+             K, valid, acc);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (wg.n_blocks > 0) {

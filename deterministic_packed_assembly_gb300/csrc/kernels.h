@@ -162,9 +162,11 @@ cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64
                                 const uint32_t *sdb, uint32_t J, uint32_t T, uint32_t *W,
                                 const int64_t *wbase, int32_t *win_start, int32_t *win_end,
                                 int32_t *win_clip, cudaStream_t st);
-cudaError_t launch_valid_steps(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
-                               uint32_t drain, uint32_t *first_bad, uint32_t *valid,
-                               cudaStream_t st);
+// *bad_inv (zeroed before) = K - k for the first update k that asks a stream
+// for a window it does not have, 0 if none; launch_digest turns it into the
+// valid horizon.
+cudaError_t launch_first_bad(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
+                             uint32_t *bad_inv, cudaStream_t st);
 
 // ---- readbacks -------------------------------------------------------------
 // Up to kCollectMax runs of 32-bit words, src[s][0 .. words[s]), copied to
@@ -191,12 +193,14 @@ struct DigestHeader {
   uint64_t n_piece_items;
   uint32_t S, J;
 };
-cudaError_t launch_digest(const DigestHeader &h, const uint32_t *valid, const int32_t *quota,
-                          const int32_t *cum, const uint32_t *W, SegGrid wg,
-                          const int64_t *wbase, const int32_t *win_start,
-                          const int64_t *node_src, const int32_t *node_doc,
-                          const int64_t *offs, uint32_t T, uint32_t K, uint64_t seed, uint32_t G,
-                          const int32_t *win_clip, int *err,
+// Writes the valid horizon (*valid, from *bad_inv and drain), then the order
+// digest.
+cudaError_t launch_digest(const DigestHeader &h, const uint32_t *bad_inv, uint32_t drain,
+                          uint32_t *valid, const int32_t *quota, const int32_t *cum,
+                          const uint32_t *W, SegGrid wg, const int64_t *wbase,
+                          const int32_t *win_start, const int64_t *node_src,
+                          const int32_t *node_doc, const int64_t *offs, uint32_t T, uint32_t K,
+                          uint64_t seed, uint32_t G, const int32_t *win_clip, int *err,
                           unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
                           uint64_t *digest_out, cudaStream_t st);
 
