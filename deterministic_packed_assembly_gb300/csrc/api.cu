@@ -619,7 +619,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // checks the offsets it uses, so a malformed partition is reported
   // (BAD_INPUT) at the next readback, never read past.
   NS_CK(cudaStreamWaitEvent(side.s2, side.fork, 0));
-  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, side.s2));
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, c->n_sms,
+                                     side.s2));
   NS_CK(cudaEventRecord(side.join2, side.s2));
 
   // Each stream's windows over the horizon estimated from the recipe (its

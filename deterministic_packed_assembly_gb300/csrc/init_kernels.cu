@@ -115,19 +115,45 @@ __device__ __forceinline__ int64_t tokens_needed(int32_t rmax, uint32_t G, uint3
 // ---------------------------------------------------------------------------
 // doc_offsets must start at >= 0, never decrease, keep every length below
 // 2^31 and end inside the token array.
-__global__ void validate_offsets_kernel(const int64_t *__restrict__ offs, uint32_t n_docs,
-                                        uint64_t n_tokens, int *err) {
+// Each warp checks runs of 128 consecutive offsets: lane l holds offsets
+// run + 32q + l (q = 0..3, each load a contiguous 256 bytes), takes its
+// neighbour from the next lane (or the next quarter's first lane, or one
+// extra load at the run's end), and the grid strides over the runs.
+constexpr uint32_t kValidateRun = 128;
+
+__global__ void __launch_bounds__(kThreads)
+    validate_offsets_kernel(const int64_t *__restrict__ offs, uint32_t n_docs,
+                            uint64_t n_tokens, int *err) {
   pdl_wait_then_release();
-  uint64_t d = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (d > n_docs) return;
-  int64_t o = offs[d];
-  if (d == 0 && o < 0) set_error(err, kDevBadOffsets);
-  if (d == n_docs) {
-    if (o < 0 || (uint64_t)o > n_tokens) set_error(err, kDevBadOffsets);
-    return;
+  const int lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  bool bad = false;
+  for (uint64_t run = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       run * kValidateRun <= n_docs; run += warps) {
+    const uint64_t b = run * kValidateRun;
+    int64_t v[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const uint64_t e = b + 32u * q + lane;
+      v[q] = (e <= n_docs) ? __ldcs(offs + e) : 0;
+    }
+    const int64_t tail =
+        (lane == 31 && b + kValidateRun <= n_docs) ? __ldcs(offs + b + kValidateRun) : 0;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int64_t down = __shfl_down_sync(0xffffffffu, v[q], 1);
+      const int64_t wrap = __shfl_sync(0xffffffffu, q < 3 ? v[q < 3 ? q + 1 : 0] : 0, 0);
+      const int64_t next = lane < 31 ? down : (q < 3 ? wrap : tail);
+      const uint64_t e = b + 32u * q + lane;
+      if (e < n_docs) {
+        const int64_t len = next - v[q];
+        bad |= len < 0 || len > 0x7FFFFFFF;
+      }
+      if (e == 0) bad |= v[q] < 0;
+      if (e == n_docs) bad |= v[q] < 0 || (uint64_t)v[q] > n_tokens;
+    }
   }
-  int64_t len = offs[d + 1] - o;
-  if (len < 0 || len > 0x7FFFFFFF) set_error(err, kDevBadOffsets);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, kDevBadOffsets);
 }
 
 // Round keys of the shuffle: K_r = splitmix64(splitmix64(seed) ^
@@ -1633,10 +1659,13 @@ uint64_t &launch_counter() {
   return n;
 }
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
-                                    int *err, cudaStream_t st) {
+                                    int *err, int n_sms, cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(validate_offsets_kernel, blocks_for((uint64_t)n_docs + 1), kThreads, 0, st, offs, n_docs,
-                                                                                  n_tokens, err);
+  // four CTAs of eight warps per SM at most, striding over runs of 128
+  const uint64_t runs = (uint64_t)n_docs / kValidateRun + 1;
+  const uint64_t want = (runs + kThreads / 32 - 1) / (kThreads / 32);
+  const uint32_t grid = (uint32_t)std::min<uint64_t>(want, (uint64_t)n_sms * 4);
+  pdl_launch(validate_offsets_kernel, grid, kThreads, 0, st, offs, n_docs, n_tokens, err);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ struct SegGrid {
 
 // ---- validation, keys, quotas ---------------------------------------------
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
-                                    int *err, cudaStream_t st);
+                                    int *err, int n_sms, cudaStream_t st);
 cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st);
 // The schedule on the device: piece p covers updates [begin[p], begin[p+1])
 // (the last one up to K) with B[p] rows per update and weights sw[p][S],

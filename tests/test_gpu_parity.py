@@ -929,3 +929,21 @@ def test_probe_loop_computes_the_hash_terms():
         for t in range(5):
             want = (want + oracle.splitmix64((((g & 1023) + t) << 32) | (tok ^ t))) & M
     assert int(acc.item()) & M == want
+
+
+@pytest.mark.parametrize("at", [0, 126, 127, 128, 129, 255, 40 * 128 - 1, 40 * 128, 69998])
+def test_malformed_offsets_far_from_the_horizon_are_reported(at):
+    # 70,000 documents of two tokens; one document's offsets decrease (at 0:
+    # the first offset is negative), far from the one window the horizon
+    # reads: only the whole-array check sees it, at run boundaries of its
+    # warps (128 offsets) and at the array's end
+    c = corpus_from_lengths([2] * 70000, T=16, B=1, max_steps=1)
+    offs = c.doc_offsets.copy()
+    if at == 0:
+        offs[0] = -1
+    else:
+        offs[at] = offs[at + 1] + 1
+    c.doc_offsets = offs
+    with pytest.raises(Exception) as e:
+        packer_for(c)
+    assert e.value.code == -6  # NS_ERR_BAD_INPUT
