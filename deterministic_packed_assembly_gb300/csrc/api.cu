@@ -732,7 +732,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // holds the windows it must; if one does not, the context is built again
   // with the full bound.  Wrap packing fills every window: full bound.
   const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
-  const bool speculate = c->speculate && any_heldout && !wrap;
+  // Two rounds only if some hashed stream may need enough windows to be
+  // speculated at all (the recipe's estimate, which is within a few windows
+  // of the quota table's; a stream below the threshold keeps the full bound
+  // either way): else one round to the full bound, without the fill kernel
+  bool some_speculated = false;
+  for (uint32_t j = 0; j < J; j++)
+    some_speculated |= stream_bp[j] != 0 && est_windows[j] >= (double)nsk::kSpeculateMinWindows;
+  const bool speculate = c->speculate && any_heldout && !wrap && some_speculated;
   uint16_t *need_num = nullptr;  // per stream, of 1024 (NULL: the full bound)
   unsigned long long *pre_cap = nullptr;
   if (speculate) {
@@ -792,13 +799,15 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   // every token is on the device before anything after the hash reads it
   if (group_copy) NS_CK(cudaStreamWaitEvent(st, copy.done.back(), 0));
-  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
-  NS_CK(cudaStreamWaitEvent(st, side.join2, 0));
   // greedy packing cuts documents into T-chunks; wrap packing keeps each
   // kept document whole as one piece (no document reaches 2^31 tokens)
   const uint32_t chunk = wrap ? 0x80000000u : T;
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes,
                                 static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, st));
+  // the cutoff reads the quota table, and the readback after it the error
+  // word the offsets check sets: the side streams join here, after the scans
+  NS_CK(cudaStreamWaitEvent(st, side.join, 0));
+  NS_CK(cudaStreamWaitEvent(st, side.join2, 0));
 
   // ---- 4. the prefix of each stream the horizon reaches -------------------
   uint32_t *cutoff = reinterpret_cast<uint32_t *>(rb1);

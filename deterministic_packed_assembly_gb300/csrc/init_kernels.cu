@@ -366,6 +366,23 @@ __global__ void __launch_bounds__(32)
   const uint32_t f0 = src_first[s];
   const int n_st = (int)(src_first[s + 1] - f0);
   const bool sact = lane < n_st;
+  if (S == 1 && n_st == 1) {
+    // one stream: the rule gives it every window of every update (floor
+    // share n, no remainder), so the updates are written in parallel
+    int64_t C0 = 0;  // windows given before the piece
+    for (uint32_t p = 0; p < q.P; p++) {
+      const uint32_t k0 = q.begin[p], k1 = (p + 1 < q.P) ? q.begin[p + 1] : K;
+      const int64_t Bp = q.B[p];
+      for (uint32_t k = k0 + lane; k < k1; k += 32) {
+        quota[(size_t)k * J + f0] = (int32_t)Bp;
+        cum[(size_t)k * J + f0] = (int32_t)(C0 + (int64_t)(k - k0) * Bp);
+      }
+      C0 += (int64_t)(k1 - k0) * Bp;
+    }
+    if (lane == 0) cum[(size_t)K * J + f0] = (int32_t)C0;
+    publish_ready(ready);
+    return;
+  }
   int64_t Cg = 0;  // windows this lane's stream has given (runs on across pieces)
   for (uint32_t p = 0; p < q.P; p++) {
     const uint32_t k0 = q.begin[p], k1 = (p + 1 < q.P) ? q.begin[p + 1] : K;
@@ -741,7 +758,7 @@ __global__ void __launch_bounds__(256)
   __shared__ uint32_t raw_s[kFillSample], kept_s[kFillSample];
   const uint32_t j = blockIdx.x;
   const int64_t wn = windows_needed(cum_last[j], G);
-  if (stream_bp[j] == 0 || wn < 256) {
+  if (stream_bp[j] == 0 || wn < kSpeculateMinWindows) {
     if (threadIdx.x == 0) need_num[j] = 1024;
     return;
   }

@@ -84,6 +84,9 @@ cudaError_t launch_hash_prefix(const int32_t *tokens, int32_t *copy_dst,
                                uint32_t j_begin, uint32_t j_count, const uint16_t *need_num,
                                uint32_t need_num_all, const unsigned long long *pre_cap,
                                int n_sms, cudaStream_t st);
+// A stream whose windows needed are fewer than this keeps the full bound in
+// the hash's second round (its sample would be too small to measure a fill).
+constexpr int64_t kSpeculateMinWindows = 256;
 // need_num: the fraction (of 1024) of each stream's bound the second hash
 // round stops at, from its measured packing fill (first_num: the first
 // round's)
