@@ -37,7 +37,15 @@ namespace {
 
 constexpr int kTile = 128;         // positions per warp per tile: 32 lanes x 4
 constexpr int kStages = 4;         // tiles in flight per warp
-constexpr int kStageWords = 132;   // 128 tokens + up to 3 of misalignment, 16-byte multiple
+constexpr int kHalfStage = 132;    // 128 tokens + up to 3 of misalignment, 16-byte multiple
+// Words of a ring slot: room for two runs (a tile over two pieces) with up to
+// 8 warps a CTA; with 16 (rows beyond 16384 positions, whose pieces are
+// long) one run, so that the CTA's shared memory stays within 48 KB, and
+// such tiles are staged token by token.
+template <int W>
+__host__ __device__ constexpr int stage_words() {
+  return W <= 8 ? 2 * kHalfStage : kHalfStage;
+}
 
 // Fingerprint term of position t: key_t = a_t ^ ((b_t | t << 40) * golden),
 // a_t = (u32 tok << 32) | u32 doc, b_t = (mask << 32) | u32 pos.
@@ -153,20 +161,28 @@ struct TablePieces {
 
 // What a tile needs between its copy and its stores.
 struct TileMeta {
-  int32_t kind;  // 0 pad, 1 inside one piece (copied), 2 crosses piece ends
-  int32_t x0;    // offset of the tile's first position inside its piece (kind 1)
-  int32_t sh;    // source misalignment in tokens (kind 1)
+  int32_t kind;  // 0 pad; 1 inside one piece; 2 three or more pieces (staged token
+                 // by token); 3 at most two pieces, then padding (a run of each copied)
+  int32_t x0;    // offset of the tile's first position inside its (first) piece
+  int32_t sh;    // source misalignment in tokens of the (first) piece's run
   int32_t doc, mthr;
+  int32_t bnd;    // kind 3: tile offset where the second piece starts
+  int32_t nreal;  // kind 3: real positions of the tile, the padding after them
+  int32_t sh2, doc2, mthr2;  // kind 3: the second piece's run
 };
 
-// Classify tile t0 and, for a tile inside one piece, start copying its tokens
-// (rounded out to 16-byte blocks that each hold at least one of them).
-template <class PV>
+// Classify tile t0 and start copying its tokens: a tile inside one piece, or
+// over at most two pieces and padding, copies each piece's run rounded out
+// to 16-byte blocks that each hold at least one of its tokens (the second
+// run into the second half of the slot); a tile over more pieces stages its
+// tokens one by one.
+template <bool kTwoRuns, class PV>
 __device__ __forceinline__ TileMeta tile_issue(const GatherParams &p, const PV &P, uint32_t t0,
                                                int lane, int32_t *buf) {
-  TileMeta m{0, 0, 0, -1, 0};
+  TileMeta m{0, 0, 0, -1, 0, 0, 0, 0, -1, 0};
   if ((int32_t)t0 < P.used) {
-    const Piece pc = P.get(P.find_uniform((int32_t)t0));
+    const int32_t qa = P.find_uniform((int32_t)t0);
+    const Piece pc = P.get(qa);
     if (pc.end >= (int32_t)t0 + kTile) {
       m.kind = 1;
       m.x0 = (int32_t)t0 - pc.start;
@@ -177,7 +193,45 @@ __device__ __forceinline__ TileMeta tile_issue(const GatherParams &p, const PV &
       const int32_t *g = p.tokens + (srcw - m.sh);
       cp_async16(buf + 4 * lane, g + 4 * lane);
       if (lane == 0 && m.sh != 0) cp_async16(buf + 128, g + 128);
-    } else {
+      return m;
+    }
+    // the tile's real positions end at lim; piece a holds [t0, min(end, lim))
+    const int32_t lim = min((int32_t)t0 + kTile, P.used);
+    const int32_t la = min(pc.end, lim) - (int32_t)t0;
+    int32_t lb = 0;
+    Piece pb{0, 0, 0, -1, 0};
+    bool two = kTwoRuns;
+    if (kTwoRuns && pc.end < lim) {
+      pb = P.get(qa + 1);
+      two = pb.end >= lim;
+      lb = lim - pc.end;
+    }
+    if (two) {
+      m.kind = 3;
+      m.x0 = (int32_t)t0 - pc.start;
+      m.doc = pc.doc;
+      m.mthr = pc.mthr;
+      m.bnd = la;
+      m.nreal = la + lb;
+      const int64_t sa = pc.src + m.x0;
+      m.sh = (int32_t)(sa & 3);
+      const int32_t *ga = p.tokens + (sa - m.sh);
+      const int32_t na = (m.sh + la + 3) >> 2;  // at most 33 blocks
+      if (lane < na) cp_async16(buf + 4 * lane, ga + 4 * lane);
+      if (lane == 0 && na > 32) cp_async16(buf + 128, ga + 128);
+      if (lb > 0) {
+        // the second piece's run starts at its first token
+        m.sh2 = (int32_t)(pb.src & 3);
+        m.doc2 = pb.doc;
+        m.mthr2 = pb.mthr;
+        const int32_t *gb = p.tokens + (pb.src - m.sh2);
+        const int32_t nb = (m.sh2 + lb + 3) >> 2;
+        if (lane < nb) cp_async16(buf + kHalfStage + 4 * lane, gb + 4 * lane);
+        if (lane == 0 && nb > 32) cp_async16(buf + kHalfStage + 128, gb + 128);
+      }
+      return m;
+    }
+    {
       // crosses piece ends: each lane stages its own real tokens with 4-byte
       // copies (the store looks the pieces up again and reads them back)
       m.kind = 2;
@@ -237,6 +291,34 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
     const int32_t th = m.mthr;
     mk = (x >= th ? 1u : 0u) | (x + 1 >= th ? 1u << 8 : 0u) | (x + 2 >= th ? 1u << 16 : 0u) |
          (x + 3 >= th ? 1u << 24 : 0u);
+  } else if (m.kind == 3) {
+    // at most two pieces: position i of the tile reads run a (i < bnd) or run
+    // b, then padding from nreal on
+    int32_t e0[4], e1[4], e2[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int32_t i = 4 * lane + e;
+      if (i < m.bnd) {
+        const int32_t x = m.x0 + i;
+        e0[e] = buf[m.sh + i];
+        e1[e] = x;
+        e2[e] = m.doc;
+        if (x >= m.mthr) mk |= 1u << (8 * e);
+      } else if (i < m.nreal) {
+        const int32_t x = i - m.bnd;
+        e0[e] = buf[kHalfStage + m.sh2 + x];
+        e1[e] = x;
+        e2[e] = m.doc2;
+        if (x >= m.mthr2) mk |= 1u << (8 * e);
+      } else {
+        e0[e] = p.pad_id;
+        e1[e] = 0;
+        e2[e] = -1;
+      }
+    }
+    tk = make_int4(e0[0], e0[1], e0[2], e0[3]);
+    ps = make_int4(e1[0], e1[1], e1[2], e1[3]);
+    dc = make_int4(e2[0], e2[1], e2[2], e2[3]);
   } else {
     // every lane looks its four positions up together (the lookups shuffle);
     // positions past the window's end become padding afterwards
@@ -289,7 +371,7 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
 // shared memory beside its buffer (written by lane 0, read after __syncwarp).
 template <int W, class PV>
 __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, int warp, int lane,
-                                           size_t obase, int32_t (*ring)[kStageWords],
+                                           size_t obase, int32_t (*ring)[stage_words<W>()],
                                            TileMeta *meta, uint64_t &acc, int &learned) {
   constexpr uint32_t kStride = W * kTile;
   const uint32_t first = (uint32_t)warp * kTile;
@@ -297,7 +379,7 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
 #pragma unroll
   for (int m = 0; m < kStages - 1; m++) {
     if (m < n_tiles) {
-      const TileMeta t = tile_issue(p, P, first + m * kStride, lane, ring[m]);
+      const TileMeta t = tile_issue<(W <= 8)>(p, P, first + m * kStride, lane, ring[m]);
       if (lane == 0) meta[m] = t;
     }
     cp_async_commit();
@@ -307,7 +389,7 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
     const int mi = mm + kStages - 1;
     const int slot_i = mi % kStages;
     if (mi < n_tiles) {
-      const TileMeta t = tile_issue(p, P, first + mi * kStride, lane, ring[slot_i]);
+      const TileMeta t = tile_issue<(W <= 8)>(p, P, first + mi * kStride, lane, ring[slot_i]);
       if (lane == 0) meta[slot_i] = t;
     }
     cp_async_commit();
@@ -325,7 +407,7 @@ __device__ __forceinline__ void warp_tiles(const GatherParams &p, const PV &P, i
 template <int W>
 __global__ void __launch_bounds__(W * 32, 40 / W)
     gather_kernel(const GatherParams p) {
-  __shared__ __align__(16) int32_t s_tok[W][kStages][kStageWords];
+  __shared__ __align__(16) int32_t s_tok[W][kStages][stage_words<W>()];
   __shared__ TileMeta s_meta[W][kStages];
   __shared__ unsigned long long s_acc;
   __shared__ int s_learned;
