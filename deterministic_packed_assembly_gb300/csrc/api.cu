@@ -287,7 +287,21 @@ struct SideHandles {
   cudaEvent_t t0 = nullptr, t1 = nullptr;  // timing: the held-out hash's phase
 };
 constexpr int kMaxSideDevices = 64;
-thread_local SideHandles tl_side[kMaxSideDevices];
+// The handles of one host thread, released when the thread ends (errors
+// ignored: at process exit the runtime may already be gone).
+struct SidePool {
+  SideHandles h[kMaxSideDevices];
+  ~SidePool() {
+    for (SideHandles &x : h) {
+      for (cudaEvent_t e : {x.fork, x.join, x.join2, x.t0, x.t1})
+        if (e) cudaEventDestroy(e);
+      if (x.s) cudaStreamDestroy(x.s);
+      if (x.s2) cudaStreamDestroy(x.s2);
+    }
+    cudaGetLastError();
+  }
+};
+thread_local SidePool tl_side;
 
 struct SideStream {
   cudaStream_t s = nullptr, s2 = nullptr;  // two: the quotas, the offsets check
@@ -296,7 +310,7 @@ struct SideStream {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    SideHandles local, *h = (dev >= 0 && dev < kMaxSideDevices) ? &tl_side[dev] : &local;
+    SideHandles local, *h = (dev >= 0 && dev < kMaxSideDevices) ? &tl_side.h[dev] : &local;
     if (!h->s) {
       e = cudaStreamCreateWithFlags(&h->s, cudaStreamNonBlocking);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);

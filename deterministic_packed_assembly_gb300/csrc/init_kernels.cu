@@ -735,6 +735,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
 // depends on it: a prefix that then holds fewer windows than needed is
 // caught after packing and the context is built again with the full bound.
 constexpr uint32_t kFillSample = 2048;
+constexpr uint32_t kFillThreads = 1024;  // threads of a block; kFillSample a multiple
 constexpr uint32_t kFillRun = 64;
 
 __device__ __forceinline__ uint32_t raw_length(const int64_t *__restrict__ offs, uint32_t d,
@@ -744,7 +745,7 @@ __device__ __forceinline__ uint32_t raw_length(const int64_t *__restrict__ offs,
   return ok ? (uint32_t)(o1 - o0) : 0u;
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFillThreads)
     fill_need_kernel(const uint32_t *__restrict__ sdb, uint32_t D0,
                      const uint16_t *__restrict__ stream_bp, const uint32_t *__restrict__ order,
                      const uint32_t *__restrict__ klen, const int64_t *__restrict__ offs,
@@ -764,9 +765,19 @@ __global__ void __launch_bounds__(256)
   }
   const uint64_t b = (uint64_t)sdb[j] - D0, N = sdb[j + 1] - sdb[j];
   const uint32_t lim = (uint32_t)(N < kFillSample ? N : kFillSample);
-  for (uint32_t p = threadIdx.x; p < lim; p += blockDim.x) {
-    raw_s[p] = raw_length(offs, order[b + p], n_tokens);
-    kept_s[p] = klen[b + p];
+  // every thread's documents first, then their offsets: two rounds of reads
+  constexpr uint32_t kPer = kFillSample / kFillThreads;
+  uint32_t d[kPer];
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; q++) {
+    const uint32_t p = threadIdx.x + q * kFillThreads;
+    d[q] = p < lim ? order[b + p] : 0u;
+    if (p < lim) kept_s[p] = klen[b + p];
+  }
+#pragma unroll
+  for (uint32_t q = 0; q < kPer; q++) {
+    const uint32_t p = threadIdx.x + q * kFillThreads;
+    if (p < lim) raw_s[p] = raw_length(offs, d[q], n_tokens);
   }
   __syncthreads();
   if (threadIdx.x >= 32) return;
@@ -1821,7 +1832,7 @@ cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
                              cudaStream_t st) {
   if (J == 0) return cudaSuccess;
   ++launch_counter();
-  pdl_launch(fill_need_kernel, J, 256, 0, st, sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
+  pdl_launch(fill_need_kernel, J, kFillThreads, 0, st, sdb, D0, stream_bp, order, klen, offs, n_tokens, cum_last,
                                       T, G, first_num, pre_cap, need_num);
   return cudaGetLastError();
 }
