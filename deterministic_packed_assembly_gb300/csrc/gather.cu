@@ -297,24 +297,16 @@ __device__ __forceinline__ void tile_store(const GatherParams &p, const PV &P, u
     int32_t e0[4], e1[4], e2[4];
 #pragma unroll
     for (int e = 0; e < 4; e++) {
+      // selects, not branches: the lanes around the boundary do not diverge
       const int32_t i = 4 * lane + e;
-      if (i < m.bnd) {
-        const int32_t x = m.x0 + i;
-        e0[e] = buf[m.sh + i];
-        e1[e] = x;
-        e2[e] = m.doc;
-        if (x >= m.mthr) mk |= 1u << (8 * e);
-      } else if (i < m.nreal) {
-        const int32_t x = i - m.bnd;
-        e0[e] = buf[kHalfStage + m.sh2 + x];
-        e1[e] = x;
-        e2[e] = m.doc2;
-        if (x >= m.mthr2) mk |= 1u << (8 * e);
-      } else {
-        e0[e] = p.pad_id;
-        e1[e] = 0;
-        e2[e] = -1;
-      }
+      const bool in_a = i < m.bnd, real = i < m.nreal;
+      const int32_t x = in_a ? m.x0 + i : i - m.bnd;
+      const int32_t w = in_a ? m.sh + i : kHalfStage + m.sh2 + x;
+      const int32_t v = buf[real ? w : 0];
+      e0[e] = real ? v : p.pad_id;
+      e1[e] = real ? x : 0;
+      e2[e] = real ? (in_a ? m.doc : m.doc2) : -1;
+      if (real && x >= (in_a ? m.mthr : m.mthr2)) mk |= 1u << (8 * e);
     }
     tk = make_int4(e0[0], e0[1], e0[2], e0[3]);
     ps = make_int4(e1[0], e1[1], e1[2], e1[3]);
