@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kHashThreads, kHashBlocksPerSM)
                        const uint16_t *__restrict__ need_num, uint32_t need_num_all,
                        const unsigned long long *__restrict__ pre_cap) {
   pdl_wait();
-  constexpr uint32_t kGrab = 4;
+  constexpr uint32_t kGrab = 8;
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   bool ready_seen = false;
