@@ -159,6 +159,21 @@ struct Arena {
     s.next = std::min(s.next * 2, kMaxSlab);
     return b;
   }
+  // Room for `bytes` more (the sum of the coming arrays, each rounded up to
+  // 256) in one allocation: a phase of the init makes one call of the
+  // allocation callback instead of one per large array.  What does not fit
+  // after all is allocated as before.
+  bool reserve(size_t bytes, bool keep) {
+    Slab &s = keep ? keep_slab : temp_slab;
+    if (bytes == 0 || (s.base && s.size - s.used >= bytes)) return true;
+    char *b = static_cast<char *>(raw(bytes, keep));
+    if (!b) return false;
+    s.base = b;
+    s.size = bytes;
+    s.used = 0;
+    return true;
+  }
+  static size_t rounded(size_t bytes) { return bytes ? (bytes + 255) / 256 * 256 : 256; }
   template <class T>
   T *keep(size_t n) {
     return static_cast<T *>(get(n * sizeof(T), true));
@@ -383,8 +398,10 @@ struct Staging {
     if (bytes) std::memcpy(host.data() + off, p, bytes);
     slots.emplace_back(off, dev);
   }
-  int commit(Arena &a, cudaStream_t st) {
-    unsigned char *d = static_cast<unsigned char *>(a.get(host.size(), false));
+  // One copy of everything added, into temporary memory of the init or, with
+  // `keep`, into memory the context keeps.
+  int commit(Arena &a, cudaStream_t st, bool keep = false) {
+    unsigned char *d = static_cast<unsigned char *>(a.get(host.size(), keep));
     if (!d) return NS_ERR_OOM;
     void *h = a.host(host.size());
     std::memcpy(h, host.data(), host.size());
@@ -580,6 +597,108 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   }
   void *d_piece_items = nullptr;
   if (!piece_items.empty()) up.add(piece_items.data(), piece_items.size() * 8, &d_piece_items);
+
+  // Each stream's windows over the horizon estimated from the recipe (its
+  // share of every piece's rows, a few windows over): the quota rule keeps
+  // every cumulative count within one window of its share.  Only how much of
+  // a stream is shuffled and hashed before its exact need is known depends
+  // on it.
+  std::vector<double> est_windows(J, 0.0);
+  for (uint32_t p = 0; p < P; p++) {
+    const uint32_t kb = c->piece_begin[p];
+    const uint32_t ke = (p + 1 < P) ? c->piece_begin[p + 1] : K;
+    double swsum = 0.0;
+    for (uint32_t s2 = 0; s2 < S; s2++) swsum += psw[(size_t)p * S + s2];
+    for (uint32_t s2 = 0; s2 < S; s2++) {
+      double twsum = 0.0;
+      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++) twsum += ptw[(size_t)p * J + j];
+      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++)
+        est_windows[j] += (double)(ke - kb) * c->piece_B[p] * (psw[(size_t)p * S + s2] / swsum) *
+                          (ptw[(size_t)p * J + j] / twsum);
+    }
+  }
+  for (uint32_t j = 0; j < J; j++)
+    est_windows[j] = std::ceil(est_windows[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
+
+  const uint32_t D0 = sdb[0];
+  const uint64_t n_pos = (uint64_t)sdb[J] - D0;
+  const bool heldout_mode = (c->flags & NS_PACK_HELDOUT) != 0;
+  const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
+  std::vector<uint64_t> N(J);
+  for (uint32_t j = 0; j < J; j++) N[j] = (uint64_t)sdb[j + 1] - sdb[j];
+  // A stream without a held-out rate is shuffled, on the first pass, only
+  // over about the positions its horizon needs (est_tok: the recipe's
+  // estimate of its windows times T; see the shuffle below)
+  bool any_unhashed = false;
+  for (uint32_t j = 0; j < J; j++) any_unhashed |= stream_bp[j] == 0 && N[j] > 0;
+  const bool shuffle_prefix = c->speculate && !heldout_mode && any_unhashed;
+  std::vector<unsigned long long> est_tok;
+  void *d_est = nullptr;
+  if (shuffle_prefix) {
+    est_tok.resize(J);
+    for (uint32_t j = 0; j < J; j++) est_tok[j] = (unsigned long long)(est_windows[j] * T);
+    up.add(est_tok.data(), J * sizeof(unsigned long long), &d_est);
+  }
+  // Two rounds of the hash only if some hashed stream may need enough
+  // windows to be speculated at all (the recipe's estimate, which is within a
+  // few windows of the quota table's; a stream below the threshold keeps the
+  // full bound either way): else one round to the full bound, without the
+  // fill kernel
+  bool some_speculated = false;
+  for (uint32_t j = 0; j < J; j++)
+    some_speculated |= stream_bp[j] != 0 && est_windows[j] >= (double)nsk::kSpeculateMinWindows;
+  const bool speculate = c->speculate && any_heldout && !wrap && some_speculated;
+  // Until the quota kernel publishes each stream's need, the first round
+  // stops a stream at half its recipe estimate (est_windows), not at no
+  // bound at all: a small stream is then not hashed far past its need while
+  // the quotas run.  A heuristic only: the second round hashes every stream
+  // to its exact bound whatever the first one did.
+  std::vector<unsigned long long> cap;
+  void *d_cap = nullptr;
+  if (speculate) {
+    cap.resize(J);
+    for (uint32_t j = 0; j < J; j++)
+      cap[j] = (unsigned long long)(0.5 * est_windows[j] * (double)T);
+    up.add(cap.data(), J * sizeof(unsigned long long), &d_cap);
+  }
+  // the shuffle's block layout
+  const std::vector<uint32_t> order_bb = seg_layout(N, 256 * nsk::order_positions_per_thread());
+  void *d_order_bb;
+  up.add(order_bb.data(), order_bb.size() * 4, &d_order_bb);
+
+  // What the host reads back after the prefix cutoff, in one block (one
+  // copy): cutoff u32[J] | npieces i64[J] | node_base i64[J + 1] | ptokens
+  // i64[J] | rmax i32[J] | need_num u16[J] | pos_lim u32[J] | error word
+  auto al8 = [](size_t b) { return (b + 7) / 8 * 8; };
+  const size_t r1_np = al8((size_t)J * 4), r1_nb = r1_np + (size_t)J * 8;
+  const size_t r1_pt = r1_nb + ((size_t)J + 1) * 8, r1_rmax = r1_pt + (size_t)J * 8;
+  const size_t r1_num = al8(r1_rmax + (size_t)J * 4), r1_lim = al8(r1_num + (size_t)J * 2);
+  const size_t r1_err = r1_lim + (size_t)J * 4, r1_bytes = r1_err + 8;
+  // The summary the host reads back at the end, in one block (one copy):
+  // tokens read from host memory u64 | tokens and documents hashed u64[2] |
+  // the digest's accumulator u64[2] | the first bad update (K - k) u32 |
+  // order digest u64 | valid updates u32 | error word | windows u32[J]; its
+  // first 48 bytes (counters and accumulators) start at zero
+  constexpr size_t r2_read = 0, r2_hashed = 8, r2_dacc = 24, r2_bad = 40, r2_digest = 48;
+  constexpr size_t r2_valid = 56, r2_err = 60, r2_W = 64;
+  const size_t r2_bytes = r2_W + (size_t)J * 4;
+  const uint32_t n_tiles = (T + 127) / 128;
+  const bool quota_warp = S <= 32 && max_strata <= 32;
+  const size_t scan_bytes = nsk::scan_scratch_bytes(n_pos);
+  {
+    // the arrays of the phase up to the first readback, in one allocation
+    // of each kind
+    const auto R = Arena::rounded;
+    const size_t n1 = std::max<uint64_t>(n_pos, 1);
+    const size_t keep = R(sizeof(int)) + R(8) + R(((size_t)n_tiles + 1) * 8) +
+                        R((size_t)K * J * 4) + R(((size_t)K + 1) * J * 4) +
+                        R((size_t)K * (J + 1) * 4);
+    const size_t temp = R(up.host.size()) + R((size_t)n_tiles * 8) + R(4) +
+                        (quota_warp ? 0 : R((size_t)K * S * 4)) + R((size_t)J * 32) +
+                        2 * R(n1 * 4) + 2 * R((n_pos + 1) * 8) + R(scan_bytes) + R(r1_bytes) +
+                        R(r2_bytes) + (any_heldout ? 2 * R((size_t)J * 8) : 0);
+    if (!a.reserve(keep, true) || !a.reserve(temp, false)) return NS_ERR_OOM;
+  }
   if ((rc = up.commit(a, st))) return rc;
   if (piece_items.empty()) d_piece_items = nullptr;
   const nsk::QuotaPieces qp{static_cast<uint32_t *>(d_pbegin), static_cast<uint32_t *>(d_pB),
@@ -591,7 +710,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->fp_out);
   // fingerprint terms of padding, per tile of a row, for the gather
   {
-    const uint32_t n_tiles = (T + 127) / 128;
     c->pad_tail = a.keep<uint64_t>(n_tiles + 1);
     uint64_t *tiles = a.temp<uint64_t>(n_tiles);
     NS_ALLOC(c->pad_tail);
@@ -616,7 +734,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(side.create());
   NS_CK(cudaEventRecord(side.fork, st));
   NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
-  if (S <= 32 && max_strata <= 32) {
+  if (quota_warp) {
     NS_CK(nsk::launch_quota_warp(qp, S, static_cast<uint32_t *>(d_src_first), J, K, max_strata,
                                  c->quota, c->cum, ready, side.s));
   } else {
@@ -637,40 +755,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                                      side.s2));
   NS_CK(cudaEventRecord(side.join2, side.s2));
 
-  // Each stream's windows over the horizon estimated from the recipe (its
-  // share of every piece's rows, a few windows over): the quota rule keeps
-  // every cumulative count within one window of its share.  Only how much of
-  // a stream is shuffled and hashed before its exact need is known depends
-  // on it.
-  std::vector<double> est_windows(J, 0.0);
-  for (uint32_t p = 0; p < P; p++) {
-    const uint32_t kb = c->piece_begin[p];
-    const uint32_t ke = (p + 1 < P) ? c->piece_begin[p + 1] : K;
-    double swsum = 0.0;
-    for (uint32_t s2 = 0; s2 < S; s2++) swsum += psw[(size_t)p * S + s2];
-    for (uint32_t s2 = 0; s2 < S; s2++) {
-      double twsum = 0.0;
-      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++) twsum += ptw[(size_t)p * J + j];
-      for (uint32_t j = src_first[s2]; j < src_first[s2 + 1]; j++)
-        est_windows[j] += (double)(ke - kb) * c->piece_B[p] * (psw[(size_t)p * S + s2] / swsum) *
-                          (ptw[(size_t)p * J + j] / twsum);
-    }
-  }
-  for (uint32_t j = 0; j < J; j++)
-    est_windows[j] = std::ceil(est_windows[j]) + 2.0 + (c->G ? (double)c->G : 0.0);
-
   // ---- 2. shuffled order and lengths of every position ----------------------
-  const uint32_t D0 = sdb[0];
-  const uint64_t n_pos = (uint64_t)sdb[J] - D0;
-  const bool heldout_mode = (c->flags & NS_PACK_HELDOUT) != 0;
-  std::vector<uint64_t> N(J);
-  for (uint32_t j = 0; j < J; j++) N[j] = (uint64_t)sdb[j + 1] - sdb[j];
   uint64_t *keys = a.temp<uint64_t>((size_t)J * 4);
   uint32_t *order = a.temp<uint32_t>(std::max<uint64_t>(n_pos, 1));
   uint32_t *klen = a.temp<uint32_t>(std::max<uint64_t>(n_pos, 1));
   int64_t *kex = a.temp<int64_t>(n_pos + 1);
   int64_t *pex = a.temp<int64_t>(n_pos + 1);
-  const size_t scan_bytes = nsk::scan_scratch_bytes(n_pos);
   void *scan_scratch = a.get(scan_bytes, false);
   NS_ALLOC(keys);
   NS_ALLOC(order);
@@ -685,24 +775,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // estimate), the others keep length 0.  A stream whose windows turn out to
   // need more is caught after the cutoff, and the context is built again
   // with every position.
-  // What the host reads back after the prefix cutoff, in one block (one
-  // copy): cutoff u32[J] | npieces i64[J] | node_base i64[J + 1] | ptokens
-  // i64[J] | rmax i32[J] | need_num u16[J] | pos_lim u32[J] | error word
-  auto al8 = [](size_t b) { return (b + 7) / 8 * 8; };
-  const size_t r1_np = al8((size_t)J * 4), r1_nb = r1_np + (size_t)J * 8;
-  const size_t r1_pt = r1_nb + ((size_t)J + 1) * 8, r1_rmax = r1_pt + (size_t)J * 8;
-  const size_t r1_num = al8(r1_rmax + (size_t)J * 4), r1_lim = al8(r1_num + (size_t)J * 2);
-  const size_t r1_err = r1_lim + (size_t)J * 4, r1_bytes = r1_err + 8;
   char *rb1 = a.temp<char>(r1_bytes);
   NS_ALLOC(rb1);
   uint32_t *pos_lim = nullptr;
-  bool any_unhashed = false;
-  for (uint32_t j = 0; j < J; j++) any_unhashed |= stream_bp[j] == 0 && N[j] > 0;
-  if (c->speculate && !heldout_mode && any_unhashed) {
-    std::vector<unsigned long long> est_tok(J);
-    for (uint32_t j = 0; j < J; j++) est_tok[j] = (unsigned long long)(est_windows[j] * T);
-    void *d_est;
-    if ((rc = upload(a, est_tok.data(), J * sizeof(unsigned long long), &d_est, st))) return rc;
+  if (shuffle_prefix) {
     pos_lim = reinterpret_cast<uint32_t *>(rb1 + r1_lim);
     NS_CK(nsk::launch_order_bound(static_cast<uint32_t *>(d_sdb), c->offs, J,
                                   static_cast<uint16_t *>(d_stream_bp),
@@ -710,10 +786,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(cudaMemsetAsync(klen, 0, std::max<uint64_t>(n_pos, 1) * sizeof(uint32_t), st));
   }
   {
-    std::vector<uint32_t> bb = seg_layout(N, 256 * nsk::order_positions_per_thread());
-    void *d_bb;
-    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
-    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    nsk::SegGrid g{static_cast<uint32_t *>(d_order_bb), J, order_bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
                             heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr,
                             pos_lim, order, klen, c->err, st));
@@ -723,14 +796,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // Runs beside the quota kernels: it reads each stream's need from their
   // table once all S quota blocks have published it, and hashes on until then.
   // tokens read from host memory in place (hash and prefix copy)
-  // The summary the host reads back at the end, in one block (one copy):
-  // tokens read from host memory u64 | tokens and documents hashed u64[2] |
-  // the digest's accumulator u64[2] | the first bad update (K - k) u32 |
-  // order digest u64 | valid updates u32 | error word | windows u32[J]; its
-  // first 48 bytes (counters and accumulators) start at zero
-  constexpr size_t r2_read = 0, r2_hashed = 8, r2_dacc = 24, r2_bad = 40, r2_digest = 48;
-  constexpr size_t r2_valid = 56, r2_err = 60, r2_W = 64;
-  const size_t r2_bytes = r2_W + (size_t)J * 4;
   char *rb2 = a.temp<char>(r2_bytes);
   NS_ALLOC(rb2);
   NS_CK(cudaMemsetAsync(rb2, 0, r2_digest, st));
@@ -745,29 +810,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // to that fill plus a margin.  The packing then shows whether each prefix
   // holds the windows it must; if one does not, the context is built again
   // with the full bound.  Wrap packing fills every window: full bound.
-  const bool wrap = (c->flags & NS_PACK_WRAP) != 0;
-  // Two rounds only if some hashed stream may need enough windows to be
-  // speculated at all (the recipe's estimate, which is within a few windows
-  // of the quota table's; a stream below the threshold keeps the full bound
-  // either way): else one round to the full bound, without the fill kernel
-  bool some_speculated = false;
-  for (uint32_t j = 0; j < J; j++)
-    some_speculated |= stream_bp[j] != 0 && est_windows[j] >= (double)nsk::kSpeculateMinWindows;
-  const bool speculate = c->speculate && any_heldout && !wrap && some_speculated;
   uint16_t *need_num = nullptr;  // per stream, of 1024 (NULL: the full bound)
   unsigned long long *pre_cap = nullptr;
   if (speculate) {
     need_num = reinterpret_cast<uint16_t *>(rb1 + r1_num);
-    // Until the quota kernel publishes each stream's need, the first round
-    // stops a stream at half its recipe estimate (est_windows), not at no
-    // bound at all: a small stream is then not hashed far past its need while
-    // the quotas run.  A heuristic only: the second round hashes every stream
-    // to its exact bound whatever the first one did.
-    std::vector<unsigned long long> cap(J);
-    for (uint32_t j = 0; j < J; j++)
-      cap[j] = (unsigned long long)(0.5 * est_windows[j] * (double)T);
-    void *d_cap;
-    if ((rc = upload(a, cap.data(), J * sizeof(unsigned long long), &d_cap, st))) return rc;
     pre_cap = static_cast<unsigned long long *>(d_cap);
   }
   unsigned long long *hashed =  // tokens and documents hashed
@@ -868,13 +914,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     rmax[j] = c->G ? ((uint64_t)rmax32[j] + c->G - 1) / c->G * c->G : (uint64_t)rmax32[j];
     wbase[j + 1] = wbase[j] + (int64_t)rmax[j];
   }
-  c->wbase = a.keep<int64_t>(J + 1);
-  NS_ALLOC(c->wbase);
-  {
-    void *h = a.host((J + 1) * sizeof(int64_t));
-    std::memcpy(h, wbase.data(), (J + 1) * sizeof(int64_t));
-    NS_CK(cudaMemcpyAsync(c->wbase, h, (J + 1) * sizeof(int64_t), cudaMemcpyHostToDevice, st));
-  }
   const int64_t n_nodes = nb_h[J];
   if (n_nodes >= (int64_t)0x7FFFFFFF) return NS_ERR_INVALID_ARG;
   c->n_pieces = (uint64_t)(n_nodes - J);
@@ -893,6 +932,40 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   while ((1ll << L) < max_windows + 1) L++;
   if (wrap) L = 0;  // wrap windows are found by position, without pointer jumping
   c->levels = L;
+
+  // One upload for what follows, kept with the context: each stream's first
+  // window number and the block layouts of the piece expansion, the next
+  // window search and the window starts.  The arrays of the phase (the piece
+  // tables, the jump levels, the windows, the row table) are reserved in one
+  // allocation of each kind.
+  const int64_t n_win = std::max<int64_t>(wbase[J], 1);
+  std::vector<uint32_t> expand_bb, next_bb, win_bb;
+  void *d_wbase, *d_expand_bb, *d_next_bb = nullptr, *d_win_bb;
+  {
+    Staging up2;
+    up2.add(wbase.data(), (J + 1) * sizeof(int64_t), &d_wbase);
+    std::vector<uint64_t> cnt(J);
+    for (uint32_t j = 0; j < J; j++) cnt[j] = std::max<uint64_t>(cut_h[j], 1);
+    expand_bb = seg_layout(cnt, 256);
+    up2.add(expand_bb.data(), expand_bb.size() * 4, &d_expand_bb);
+    if (!wrap) {
+      for (uint32_t j = 0; j < J; j++) cnt[j] = (uint64_t)np_h[j] + 1;
+      next_bb = seg_layout(cnt, 256);
+      up2.add(next_bb.data(), next_bb.size() * 4, &d_next_bb);
+    }
+    win_bb = seg_layout(rmax, 256);
+    up2.add(win_bb.data(), win_bb.size() * 4, &d_win_bb);
+    const auto R = Arena::rounded;
+    const size_t nn = (size_t)n_nodes;
+    const size_t keep = R(up2.host.size()) + 2 * R(nn * 8) + 2 * R(nn * 4) + R((size_t)J * 4) +
+                        R((size_t)K * c->B * sizeof(int4));
+    const size_t temp = (wrap ? 3 * R((size_t)n_win * 4) : R((size_t)L * nn * 4) +
+                                                              R((size_t)n_win * 4)) +
+                        R(((size_t)J + 1) * 8) + R(((size_t)J + 1) * 4);
+    if (!a.reserve(keep, true) || !a.reserve(temp, false)) return NS_ERR_OOM;
+    if ((rc = up2.commit(a, st, true))) return rc;
+  }
+  c->wbase = static_cast<int64_t *>(d_wbase);
 
   // ---- 5. tokens of the prefixes the hash did not read --------------------
   // (host tokens read in place only): on the second stream, beside the
@@ -956,23 +1029,13 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->node_mthr);
   if (!wrap) NS_ALLOC(levels);
   {
-    std::vector<uint64_t> cnt(J);
-    for (uint32_t j = 0; j < J; j++) cnt[j] = std::max<uint64_t>(cut_h[j], 1);
-    std::vector<uint32_t> bb = seg_layout(cnt, 256);
-    void *d_bb;
-    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
-    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    nsk::SegGrid g{static_cast<uint32_t *>(d_expand_bb), J, expand_bb[J]};
     NS_CK(nsk::launch_expand(g, static_cast<uint32_t *>(d_sdb), D0, cutoff, order, klen, kex, pex,
                              node_base, npieces, c->offs, c->loss_start, chunk, c->node_src,
                              c->node_doc, c->node_mthr, c->node_S, st));
   }
   if (!wrap) {
-    std::vector<uint64_t> cnt(J);
-    for (uint32_t j = 0; j < J; j++) cnt[j] = (uint64_t)np_h[j] + 1;
-    std::vector<uint32_t> bb = seg_layout(cnt, 256);
-    void *d_bb;
-    if ((rc = upload(a, bb.data(), bb.size() * 4, &d_bb, st))) return rc;
-    nsk::SegGrid g{static_cast<uint32_t *>(d_bb), J, bb[J]};
+    nsk::SegGrid g{static_cast<uint32_t *>(d_next_bb), J, next_bb[J]};
     NS_CK(nsk::launch_next(g, node_base, npieces, c->node_S, T, levels, st));
   }
   // two levels per launch while two remain
@@ -990,7 +1053,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
 
   // ---- 7. windows: count, starts, the valid horizon ------------------------
   c->W = a.keep<uint32_t>(J);
-  const int64_t n_win = std::max<int64_t>(wbase[J], 1);
   int32_t *win_start = a.temp<int32_t>(n_win);
   int32_t *win_end = wrap ? a.temp<int32_t>(n_win) : nullptr;
   int32_t *win_clip = wrap ? a.temp<int32_t>(n_win) : nullptr;
@@ -1004,10 +1066,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_ALLOC(win_clip);
   }
   NS_ALLOC(c->row_win);
-  std::vector<uint32_t> wb = seg_layout(rmax, 256);
-  void *d_wb;
-  if ((rc = upload(a, wb.data(), wb.size() * 4, &d_wb, st))) return rc;
-  nsk::SegGrid wg{static_cast<uint32_t *>(d_wb), J, wb[J]};
+  nsk::SegGrid wg{static_cast<uint32_t *>(d_win_bb), J, win_bb[J]};
   if (wrap) {
     NS_CK(nsk::launch_wrap_windows(wg, node_base, npieces, c->node_S, cutoff,
                                    static_cast<uint32_t *>(d_sdb), J, T, c->W, c->wbase,
