@@ -682,6 +682,15 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   constexpr size_t r2_read = 0, r2_hashed = 8, r2_dacc = 24, r2_bad = 40, r2_digest = 48;
   constexpr size_t r2_valid = 56, r2_err = 60, r2_W = 64;
   const size_t r2_bytes = r2_W + (size_t)J * 4;
+  // One block of words that start at zero, cleared by one memset: the
+  // quota kernel's ready count and the done counts of the kernels whose last
+  // block finishes a step (the cutoff, the row table, the digest), then the
+  // summary read back at the end (its counters and accumulators), then the
+  // hash's per-stream frontier and progress words.
+  constexpr size_t kCtlBytes = 256;
+  const size_t zb_rb2 = kCtlBytes, zb_front = zb_rb2 + Arena::rounded(r2_bytes);
+  const size_t zb_prog = zb_front + (any_heldout ? (size_t)J * 8 : 0);
+  const size_t zb_bytes = zb_prog + (any_heldout ? (size_t)J * 8 : 0);
   const uint32_t n_tiles = (T + 127) / 128;
   const bool quota_warp = S <= 32 && max_strata <= 32;
   const size_t scan_bytes = nsk::scan_scratch_bytes(n_pos);
@@ -693,10 +702,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     const size_t keep = R(sizeof(int)) + R(8) + R(((size_t)n_tiles + 1) * 8) +
                         R((size_t)K * J * 4) + R(((size_t)K + 1) * J * 4) +
                         R((size_t)K * (J + 1) * 4);
-    const size_t temp = R(up.host.size()) + R((size_t)n_tiles * 8) + R(4) +
+    const size_t temp = R(up.host.size()) + R((size_t)n_tiles * 8) + R(zb_bytes) +
                         (quota_warp ? 0 : R((size_t)K * S * 4)) + R((size_t)J * 32) +
-                        2 * R(n1 * 4) + 2 * R((n_pos + 1) * 8) + R(scan_bytes) + R(r1_bytes) +
-                        R(r2_bytes) + (any_heldout ? 2 * R((size_t)J * 8) : 0);
+                        2 * R(n1 * 4) + 2 * R((n_pos + 1) * 8) + R(scan_bytes) + R(r1_bytes);
     if (!a.reserve(keep, true) || !a.reserve(temp, false)) return NS_ERR_OOM;
   }
   if ((rc = up.commit(a, st))) return rc;
@@ -709,14 +717,18 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   c->fp_out = a.keep<uint64_t>(1);
   NS_ALLOC(c->fp_out);
   // fingerprint terms of padding, per tile of a row, for the gather
-  {
-    c->pad_tail = a.keep<uint64_t>(n_tiles + 1);
-    uint64_t *tiles = a.temp<uint64_t>(n_tiles);
-    NS_ALLOC(c->pad_tail);
-    NS_ALLOC(tiles);
-    NS_CK(nsk::launch_pad_tail(c->pad_id, T, tiles, c->pad_tail, st));
-  }
+  // (computed on the second side stream below)
+  c->pad_tail = a.keep<uint64_t>(n_tiles + 1);
+  uint64_t *pad_tiles = a.temp<uint64_t>(n_tiles);
+  NS_ALLOC(c->pad_tail);
+  NS_ALLOC(pad_tiles);
   NS_CK(cudaMemsetAsync(c->err, 0, sizeof(int), st));
+  char *zb = a.temp<char>(zb_bytes);
+  NS_ALLOC(zb);
+  NS_CK(cudaMemsetAsync(zb, 0, zb_bytes, st));
+  unsigned *ready = reinterpret_cast<unsigned *>(zb);
+  unsigned *done_cutoff = ready + 1, *done_rows = ready + 2, *done_digest = ready + 3;
+  char *rb2 = zb + zb_rb2;
 
   // ---- 1. quotas of every update, on a side stream ------------------------
   // They depend only on the weights, so they run while the corpus is hashed
@@ -727,9 +739,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->quota);
   NS_ALLOC(c->cum);
   NS_ALLOC(c->rb);
-  unsigned *ready = a.temp<unsigned>(1);
-  NS_ALLOC(ready);
-  NS_CK(cudaMemsetAsync(ready, 0, sizeof(unsigned), st));
   SideStream side;
   NS_CK(side.create());
   NS_CK(cudaEventRecord(side.fork, st));
@@ -753,6 +762,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaStreamWaitEvent(side.s2, side.fork, 0));
   NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, c->n_sms,
                                      side.s2));
+  NS_CK(nsk::launch_pad_tail(c->pad_id, T, pad_tiles, c->pad_tail, side.s2));
   NS_CK(cudaEventRecord(side.join2, side.s2));
 
   // ---- 2. shuffled order and lengths of every position ----------------------
@@ -768,7 +778,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(kex);
   NS_ALLOC(pex);
   NS_ALLOC(scan_scratch);
-  NS_CK(nsk::launch_stream_keys(c->seed, J, keys, st));
   // A stream without a held-out rate (nothing to hash) needs only the
   // shuffled positions whose documents hold its horizon's tokens: on the
   // first pass about that many are taken (a quarter over the recipe's
@@ -778,13 +787,12 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   char *rb1 = a.temp<char>(r1_bytes);
   NS_ALLOC(rb1);
   uint32_t *pos_lim = nullptr;
-  if (shuffle_prefix) {
-    pos_lim = reinterpret_cast<uint32_t *>(rb1 + r1_lim);
-    NS_CK(nsk::launch_order_bound(static_cast<uint32_t *>(d_sdb), c->offs, J,
-                                  static_cast<uint16_t *>(d_stream_bp),
-                                  static_cast<unsigned long long *>(d_est), pos_lim, st));
+  if (shuffle_prefix) pos_lim = reinterpret_cast<uint32_t *>(rb1 + r1_lim);
+  NS_CK(nsk::launch_keys_bound(c->seed, J, keys, static_cast<uint32_t *>(d_sdb), c->offs,
+                               static_cast<uint16_t *>(d_stream_bp),
+                               static_cast<unsigned long long *>(d_est), pos_lim, st));
+  if (shuffle_prefix)
     NS_CK(cudaMemsetAsync(klen, 0, std::max<uint64_t>(n_pos, 1) * sizeof(uint32_t), st));
-  }
   {
     nsk::SegGrid g{static_cast<uint32_t *>(d_order_bb), J, order_bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
@@ -796,9 +804,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // Runs beside the quota kernels: it reads each stream's need from their
   // table once all S quota blocks have published it, and hashes on until then.
   // tokens read from host memory in place (hash and prefix copy)
-  char *rb2 = a.temp<char>(r2_bytes);
-  NS_ALLOC(rb2);
-  NS_CK(cudaMemsetAsync(rb2, 0, r2_digest, st));
   unsigned long long *tokens_read =
       htok ? reinterpret_cast<unsigned long long *>(rb2 + r2_read) : nullptr;
   const bool group_copy = host_corpus && !htok;
@@ -819,12 +824,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   unsigned long long *hashed =  // tokens and documents hashed
       any_heldout ? reinterpret_cast<unsigned long long *>(rb2 + r2_hashed) : nullptr;
   if (any_heldout) {
-    unsigned long long *frontier = a.temp<unsigned long long>(J);
-    unsigned long long *prog = a.temp<unsigned long long>(J);  // per stream, see the kernel
-    NS_ALLOC(frontier);
-    NS_ALLOC(prog);
-    NS_CK(cudaMemsetAsync(frontier, 0, (size_t)J * 8, st));
-    NS_CK(cudaMemsetAsync(prog, 0, (size_t)J * 8, st));
+    // per stream, see the kernel (zeroed with the control block)
+    unsigned long long *frontier = reinterpret_cast<unsigned long long *>(zb + zb_front);
+    unsigned long long *prog = reinterpret_cast<unsigned long long *>(zb + zb_prog);
     NS_CK(cudaEventRecord(side.t0, st));
     const uint32_t first_num = speculate ? 512u : 1024u;
     const int32_t *src = htok ? htok : c->tokens;
@@ -875,19 +877,9 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   int64_t *ptokens = reinterpret_cast<int64_t *>(rb1 + r1_pt);
   int64_t *node_base = reinterpret_cast<int64_t *>(rb1 + r1_nb);
   NS_CK(nsk::launch_cutoff(static_cast<uint32_t *>(d_sdb), J, D0, kex, pex, c->cum + (size_t)K * J,
-                           T, c->G, need_num, pos_lim, cutoff, npieces, ptokens, st));
-  NS_CK(nsk::launch_node_base(npieces, J, node_base, st));
-  {
-    nsk::CollectList cl{};
-    cl.src[0] = reinterpret_cast<const uint32_t *>(c->cum + (size_t)K * J);
-    cl.off[0] = (uint32_t)(r1_rmax / 4);
-    cl.words[0] = J;
-    cl.src[1] = reinterpret_cast<const uint32_t *>(c->err);
-    cl.off[1] = (uint32_t)(r1_err / 4);
-    cl.words[1] = 1;
-    cl.n = 2;
-    NS_CK(nsk::launch_collect(cl, reinterpret_cast<uint32_t *>(rb1), st));
-  }
+                           T, c->G, need_num, pos_lim, cutoff, npieces, ptokens, node_base,
+                           reinterpret_cast<uint32_t *>(rb1), (uint32_t)(r1_rmax / 4),
+                           (uint32_t)(r1_err / 4), c->err, done_cutoff, st));
   char *h1 = static_cast<char *>(a.host(r1_bytes));
   NS_CK(cudaMemcpyAsync(h1, rb1, r1_bytes, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));
@@ -1076,17 +1068,19 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     NS_CK(nsk::launch_window_starts(wg, levels, n_nodes, L, node_base, c->W, c->wbase,
                                     win_start, st));
   }
-  NS_CK(nsk::launch_row_windows(c->rb, c->cum, c->W, c->wbase, win_start, levels, win_end,
-                                win_clip, J, c->B, K, c->seed, c->G,
-                                (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u, c->row_win, c->err,
-                                st));
-  NS_CK(nsk::launch_first_bad(c->cum, c->W, J, K, bad_inv, st));
-
-  // ---- 8. order digest ----------------------------------------------------
-  unsigned long long *dacc = reinterpret_cast<unsigned long long *>(rb2 + r2_dacc);
+  // the row table; in the same launch, the valid horizon and each stream's
+  // first item in the digest
   int64_t *ubase = a.temp<int64_t>(J + 1);
-  uint64_t *digest = reinterpret_cast<uint64_t *>(rb2 + r2_digest);
   NS_ALLOC(ubase);
+  NS_CK(nsk::launch_row_table(c->rb, c->cum, c->W, c->wbase, win_start, levels, win_end, win_clip,
+                              J, c->B, K, c->seed, c->G,
+                              (c->flags & NS_PACK_SHUFFLE_ROWS) ? 1u : 0u, c->row_win, c->err,
+                              bad_inv, (c->flags & NS_PACK_DRAIN) ? 1u : 0u, valid, ubase,
+                              done_rows, st));
+
+  // ---- 8. order digest, and the summary the host reads back ---------------
+  unsigned long long *dacc = reinterpret_cast<unsigned long long *>(rb2 + r2_dacc);
+  uint64_t *digest = reinterpret_cast<uint64_t *>(rb2 + r2_digest);
   nsk::DigestHeader h{};
   h.scalars[0] = T;
   h.scalars[1] = c->B;
@@ -1109,24 +1103,14 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   h.n_piece_items = piece_items.size();
   h.S = S;
   h.J = J;
-  NS_CK(nsk::launch_digest(h, bad_inv, (c->flags & NS_PACK_DRAIN) ? 1u : 0u, valid, c->quota,
-                           c->cum, c->W, wg, c->wbase, win_start, c->node_src, c->node_doc,
-                           c->offs, T, K, c->seed, c->G, win_clip, c->err, dacc, ubase, digest,
-                           st));
+  NS_CK(nsk::launch_digest(h, c->quota, K, wg, c->wbase, win_start, c->node_src, c->node_doc,
+                           c->offs, valid, ubase, c->W, c->seed, c->G, win_clip, c->err, dacc,
+                           digest, reinterpret_cast<uint32_t *>(rb2), (uint32_t)(r2_W / 4),
+                           (uint32_t)(r2_err / 4), done_digest, st));
 
   // ---- 9. read back the summary ------------------------------------------
+  // (the prefix copy, if any, adds its count of the tokens it read)
   if (prefix_copy) NS_CK(cudaStreamWaitEvent(st, side.join, 0));
-  {
-    nsk::CollectList cl{};
-    cl.src[0] = c->W;
-    cl.off[0] = (uint32_t)(r2_W / 4);
-    cl.words[0] = J;
-    cl.src[1] = reinterpret_cast<const uint32_t *>(c->err);
-    cl.off[1] = (uint32_t)(r2_err / 4);
-    cl.words[1] = 1;
-    cl.n = 2;
-    NS_CK(nsk::launch_collect(cl, reinterpret_cast<uint32_t *>(rb2), st));
-  }
   char *h2 = static_cast<char *>(a.host(r2_bytes));
   NS_CK(cudaMemcpyAsync(h2, rb2, r2_bytes, cudaMemcpyDeviceToHost, st));
   NS_CK(cudaStreamSynchronize(st));

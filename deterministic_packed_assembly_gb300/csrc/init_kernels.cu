@@ -33,17 +33,37 @@ inline unsigned blocks_for(uint64_t n, int threads = kThreads) {
   return (unsigned)((n + threads - 1) / threads);
 }
 
-// Stream j of this block in a segmented launch, and the block's index within
+// Stream j of block b of a segmented launch, and the block's index within
 // the stream's run of blocks.
-__device__ __forceinline__ void seg_locate(const SegGrid &g, uint32_t &j, uint32_t &blk) {
+__device__ __forceinline__ void seg_locate_at(const SegGrid &g, uint32_t b, uint32_t &j,
+                                              uint32_t &blk) {
   __shared__ uint32_t s_j;
   if (threadIdx.x == 0) {
-    int64_t jj = last_le<uint32_t, int64_t>(g.blk_base, 0, (int64_t)g.J, (uint32_t)blockIdx.x);
+    int64_t jj = last_le<uint32_t, int64_t>(g.blk_base, 0, (int64_t)g.J, b);
     s_j = (uint32_t)(jj < 0 ? 0 : jj);
   }
   __syncthreads();
   j = s_j;
-  blk = blockIdx.x - g.blk_base[j];
+  blk = b - g.blk_base[j];
+}
+__device__ __forceinline__ void seg_locate(const SegGrid &g, uint32_t &j, uint32_t &blk) {
+  seg_locate_at(g, blockIdx.x, j, blk);
+}
+
+// Every thread of the block calls it once its writes are done: true, in
+// every thread of the block, for the last block of the grid to get here
+// (*done counts the blocks, zeroed before the launch).  Each block's writes
+// are made visible before it counts itself, so the last one reads every
+// other block's results (through loads that do not take a line cached
+// before, e.g. __ldcg).  No block waits for another.
+__device__ __forceinline__ bool last_block_done(unsigned *done) {
+  __shared__ bool s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last;
 }
 
 // Exclusive prefix of one value per thread over the block (blockDim.x a
@@ -157,13 +177,35 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // Round keys of the shuffle: K_r = splitmix64(splitmix64(seed) ^
-// splitmix64((stream << 8) | r)), r = 0..3.
-__global__ void stream_keys_kernel(uint64_t seed, uint32_t J, uint64_t *keys) {
+// splitmix64((stream << 8) | r)), r = 0..3; thread 4 j + r writes K_r of
+// stream j.  With est_tok, thread 4 j also bounds the positions the shuffle
+// takes of stream j (pos_lim[j]): a stream without a held-out rate needs
+// only about the documents that hold its estimated tokens, a quarter over
+// and 1024 more (offsets are checked by their own kernel); every position
+// of the others.
+__global__ void keys_bound_kernel(uint64_t seed, uint32_t J, uint64_t *keys,
+                                  const uint32_t *__restrict__ sdb,
+                                  const int64_t *__restrict__ offs,
+                                  const uint16_t *__restrict__ stream_bp,
+                                  const unsigned long long *__restrict__ est_tok,
+                                  uint32_t *__restrict__ pos_lim) {
   pdl_wait_then_release();
   uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)J * 4) return;
-  uint64_t j = i >> 2, r = i & 3;
+  const uint64_t j = i >> 2, r = i & 3;
   keys[i] = splitmix64(splitmix64(seed) ^ splitmix64((j << 8) | r));
+  if (!est_tok || r != 0) return;
+  const uint32_t b = sdb[j], e = sdb[j + 1];
+  const uint64_t N = e - b;
+  uint64_t lim = N;
+  if (stream_bp[j] == 0 && N > 0) {
+    const int64_t tok = offs[e] - offs[b];
+    if (tok > 0) {
+      const double want = 1.25 * (double)est_tok[j] * (double)N / (double)tok + 1024.0;
+      if (want < (double)N) lim = (uint64_t)want;
+    }
+  }
+  pos_lim[j] = (uint32_t)lim;
 }
 
 // ---------------------------------------------------------------------------
@@ -980,32 +1022,6 @@ __device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, ui
   return (uint32_t)feistel_walk(k, B, i, err);
 }
 
-// The shuffled positions of each stream a first init pass takes: all of a
-// stream the held-out hash reads, else the recipe's estimate of the tokens
-// its windows hold (est_tok) over the stream's mean document length, a
-// quarter and 1024 positions over, at most all of them.  The rest keep
-// length 0; a stream whose windows need more is caught after the cutoff.
-__global__ void order_bound_kernel(const uint32_t *__restrict__ sdb,
-                                   const int64_t *__restrict__ offs, uint32_t J,
-                                   const uint16_t *__restrict__ stream_bp,
-                                   const unsigned long long *__restrict__ est_tok,
-                                   uint32_t *__restrict__ pos_lim) {
-  pdl_wait_then_release();
-  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= J) return;
-  const uint32_t b = sdb[j], e = sdb[j + 1];
-  const uint64_t N = e - b;
-  uint64_t lim = N;
-  if (stream_bp[j] == 0 && N > 0) {
-    const int64_t tok = offs[e] - offs[b];  // offsets are checked by their own kernel
-    if (tok > 0) {
-      const double want = 1.25 * (double)est_tok[j] * (double)N / (double)tok + 1024.0;
-      if (want < (double)N) lim = (uint64_t)want;
-    }
-  }
-  pos_lim[j] = (uint32_t)lim;
-}
-
 // Each thread takes kOrderPerThread positions of one stream, p0 + m * 256,
 // one after the other, and every pass of its walk loop is one evaluation of
 // the network for every lane: a lane whose walk lands in range records that
@@ -1271,54 +1287,62 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 // can read of stream j), or the whole stream.  Windows 0..rmax_j - 1 hold at most
 // rmax_j * T tokens, so at least one piece follows them inside the prefix and
 // their greedy packing is the same as over the whole stream.
-__global__ void cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
-                              const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
-                              const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
-                              const uint16_t *__restrict__ need_num,
-                              const uint32_t *__restrict__ pos_lim,
-                              uint32_t *__restrict__ cutoff, int64_t *__restrict__ npieces,
-                              int64_t *__restrict__ ptokens) {
+// The last block to finish then numbers every stream's first node --
+// node_base[j] = the sum over j' < j of (pieces of j' + 1 terminal node) --
+// and gathers what the host reads back besides: each stream's windows over
+// the horizon (the quota table's last row) into rb[rb_rmax + j], the error
+// word into rb[rb_err].
+constexpr int kCutoffThreads = 128;
+__global__ void __launch_bounds__(kCutoffThreads)
+    cutoff_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
+                  const int64_t *__restrict__ kex, const int64_t *__restrict__ pex,
+                  const int32_t *__restrict__ cum_last, uint32_t T, uint32_t G,
+                  const uint16_t *__restrict__ need_num, const uint32_t *__restrict__ pos_lim,
+                  uint32_t *__restrict__ cutoff, int64_t *npieces, int64_t *__restrict__ ptokens,
+                  int64_t *__restrict__ node_base, uint32_t *__restrict__ rb, uint32_t rb_rmax,
+                  uint32_t rb_err, const int *err, unsigned *done) {
   pdl_wait_then_release();
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= J) return;
-  const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
-  const uint64_t N = e - b;
-  const int64_t base = kex[b];
-  const int64_t need = tokens_needed(cum_last[j], G, T, need_num ? need_num[j] : 1024u);
-  uint64_t c = N;
-  if (kex[e] - base > need) {
-    // a stream shuffled only in part meets its need within that part (its
-    // lengths are 0 past it, and the prefix sums there are not written)
-    uint64_t lo = 1, hi = pos_lim ? min(N, (uint64_t)pos_lim[j]) : N;
-    while (lo < hi) {
-      const uint64_t mid = lo + (hi - lo) / 2;
-      if (kex[b + mid] - base > need)
-        hi = mid;
-      else
-        lo = mid + 1;
+  if (j < J) {
+    const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
+    const uint64_t N = e - b;
+    const int64_t base = kex[b];
+    const int64_t need = tokens_needed(cum_last[j], G, T, need_num ? need_num[j] : 1024u);
+    uint64_t c = N;
+    if (kex[e] - base > need) {
+      // a stream shuffled only in part meets its need within that part (its
+      // lengths are 0 past it, and the prefix sums there are not written)
+      uint64_t lo = 1, hi = pos_lim ? min(N, (uint64_t)pos_lim[j]) : N;
+      while (lo < hi) {
+        const uint64_t mid = lo + (hi - lo) / 2;
+        if (kex[b + mid] - base > need)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      c = lo;
     }
-    c = lo;
+    cutoff[j] = (uint32_t)c;
+    npieces[j] = pex[b + c] - pex[b];
+    ptokens[j] = kex[b + c] - base;
   }
-  cutoff[j] = (uint32_t)c;
-  npieces[j] = pex[b + c] - pex[b];
-  ptokens[j] = kex[b + c] - base;
-}
-
-// node_base[j] = sum over j' < j of (pieces of j' + 1 terminal node).
-__global__ void __launch_bounds__(1024)
-    node_base_kernel(const int64_t *__restrict__ npieces, uint32_t J,
-                     int64_t *__restrict__ node_base) {
-  pdl_wait_then_release();
+  if (!last_block_done(done)) return;
   __shared__ int64_t ws[33];
   int64_t carry = 0;
   for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
-    const uint32_t j = c0 + threadIdx.x;
+    const uint32_t jj = c0 + threadIdx.x;
     int64_t total;
-    const int64_t e = block_excl_scan((j < J) ? npieces[j] + 1 : 0, ws, &total);
-    if (j < J) node_base[j] = carry + e;
+    const int64_t x = block_excl_scan((jj < J) ? __ldcg(npieces + jj) + 1 : 0, ws, &total);
+    if (jj < J) {
+      node_base[jj] = carry + x;
+      rb[rb_rmax + jj] = (uint32_t)cum_last[jj];
+    }
     carry += total;
   }
-  if (threadIdx.x == 0) node_base[J] = carry;
+  if (threadIdx.x == 0) {
+    node_base[J] = carry;
+    rb[rb_err] = (uint32_t)*reinterpret_cast<const volatile int *>(err);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1467,18 +1491,17 @@ __global__ void __launch_bounds__(kThreads)
 // rb[k][j+1]) holds it and takes that stream's rank cum[k][j] + (c -
 // rb[k][j]), which reads window window_of_rank(...); the window ends where the
 // next one starts.
-__global__ void row_windows_kernel(const int32_t *__restrict__ rb, const int32_t *__restrict__ cum,
-                                   const uint32_t *__restrict__ W,
-                                   const int64_t *__restrict__ wbase,
-                                   const int32_t *__restrict__ win_start,
-                                   const int32_t *__restrict__ next,
-                                   const int32_t *__restrict__ win_end,
-                                   const int32_t *__restrict__ win_clip, uint32_t J, uint32_t B,
-                                   uint32_t K, uint64_t seed, uint32_t G, uint32_t shuffle_rows,
-                                   int4 *__restrict__ row_win, int *err) {
-  pdl_wait_then_release();
-  const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= (uint64_t)K * B) return;
+__device__ __forceinline__ void row_window(uint64_t x, const int32_t *__restrict__ rb,
+                                           const int32_t *__restrict__ cum,
+                                           const uint32_t *__restrict__ W,
+                                           const int64_t *__restrict__ wbase,
+                                           const int32_t *__restrict__ win_start,
+                                           const int32_t *__restrict__ next,
+                                           const int32_t *__restrict__ win_end,
+                                           const int32_t *__restrict__ win_clip, uint32_t J,
+                                           uint32_t B, uint64_t seed, uint32_t G,
+                                           uint32_t shuffle_rows, int4 *__restrict__ row_win,
+                                           int *err) {
   const uint32_t k = (uint32_t)(x / B), slot = (uint32_t)(x % B);
   const int32_t *rbk = rb + (size_t)k * (J + 1);
   const uint32_t Bk = (uint32_t)rbk[J];  // rows of this update (a schedule may vary them)
@@ -1549,21 +1572,9 @@ __global__ void __launch_bounds__(kThreads)
   win_clip[e] = (int32_t)(s0 + a - node_S[ws]);
 }
 
-// First update that asks a stream for a window past its last.
-
-// The first update that asks a stream for a window it does not have, as
-// K - k in *bad_inv (zeroed before: 0 means none).
-__global__ void first_bad_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
-                                 uint32_t J, uint32_t K, uint32_t *bad_inv) {
-  pdl_wait_then_release();
-  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (uint64_t)K * J) return;
-  const uint32_t k = (uint32_t)(i / J), j = (uint32_t)(i % J);
-  if ((uint32_t)cum[(size_t)(k + 1) * J + j] > W[j]) atomicMax(bad_inv, K - k);
-}
-
-// Updates [0, valid) can be assembled: up to the first bad one, or through
-// it with drain.
+// Updates [0, valid) can be assembled: up to the first bad one (the first
+// that asks a stream for a window it does not have; bad_inv = K - k, 0 if
+// none), or through it with drain.
 __device__ __forceinline__ uint32_t valid_from(uint32_t bad_inv, uint32_t K, uint32_t drain) {
   if (bad_inv == 0) return K;
   const uint32_t f = K - bad_inv;
@@ -1584,17 +1595,13 @@ __device__ __forceinline__ void digest_accumulate(uint64_t term, unsigned long l
   if (threadIdx.x == 0) atomicAdd(acc, (unsigned long long)s);
 }
 
-// The item list's recipe part (items [0, h0)) and the quota of every valid
-// update (items h0 + k J + j) in one launch.
-__global__ void digest_items_kernel(DigestHeader h, const int32_t *__restrict__ quota,
-                                    uint32_t K, const uint32_t *valid,
-                                    unsigned long long *acc) {
-  pdl_wait_then_release();
+// Term of item i of the recipe part (items [0, h0)) and of the quota of every
+// valid update (items h0 + k J + j); 0 past them.
+__device__ __forceinline__ uint64_t digest_item_term(const DigestHeader &h,
+                                                     const int32_t *__restrict__ quota,
+                                                     uint32_t K, uint32_t v, uint64_t i) {
   const uint64_t n_fixed = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J;
   const uint64_t h0 = n_fixed + h.n_piece_items;
-  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const uint32_t v = *valid;
-  uint64_t term = 0;
   if (i < h0) {
     uint64_t x;
     if (i < kDigestScalars) {
@@ -1613,22 +1620,44 @@ __global__ void digest_items_kernel(DigestHeader h, const int32_t *__restrict__ 
         default: x = h.tw[j]; break;
       }
     }
-    term = digest_term(x, i);
-  } else if (i - h0 < (uint64_t)K * h.J && (i - h0) / h.J < v) {
-    term = digest_term((uint64_t)quota[i - h0], i);
+    return digest_term(x, i);
   }
-  digest_accumulate(term, acc);
+  if (i - h0 < (uint64_t)K * h.J && (i - h0) / h.J < v)
+    return digest_term((uint64_t)quota[i - h0], i);
+  return 0;
 }
 
-// One block: the valid horizon (written to *valid), then the first item of
-// each stream's used windows, ubase[j] (a scan of min(cum[valid][j], W[j])).
-__global__ void __launch_bounds__(1024)
-    digest_used_kernel(const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
-                       uint32_t J, const uint32_t *bad_inv, uint32_t K, uint32_t drain,
-                       uint32_t *valid, int64_t *ubase) {
+// The row table in its first n_row_blocks blocks (one thread a row of an
+// update); in the others, the first update that asks a stream for a window
+// it does not have (one thread per (update, stream): atomicMax of K - k into
+// *bad_inv, zeroed before).  The last block to finish then writes the valid
+// horizon (*valid) and the first item of each stream's used windows in the
+// digest, ubase[j] (a scan of min(cum[valid][j], W[j])).
+__global__ void __launch_bounds__(kThreads)
+    row_table_kernel(uint32_t n_row_blocks, const int32_t *__restrict__ rb,
+                     const int32_t *__restrict__ cum, const uint32_t *__restrict__ W,
+                     const int64_t *__restrict__ wbase, const int32_t *__restrict__ win_start,
+                     const int32_t *__restrict__ next, const int32_t *__restrict__ win_end,
+                     const int32_t *__restrict__ win_clip, uint32_t J, uint32_t B, uint32_t K,
+                     uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *__restrict__ row_win,
+                     int *err, uint32_t *bad_inv, uint32_t drain, uint32_t *__restrict__ valid,
+                     int64_t *__restrict__ ubase, unsigned *done) {
   pdl_wait_then_release();
+  if (blockIdx.x < n_row_blocks) {
+    const uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x < (uint64_t)K * B)
+      row_window(x, rb, cum, W, wbase, win_start, next, win_end, win_clip, J, B, seed, G,
+                 shuffle_rows, row_win, err);
+  } else {
+    const uint64_t i = (uint64_t)(blockIdx.x - n_row_blocks) * blockDim.x + threadIdx.x;
+    if (i < (uint64_t)K * J) {
+      const uint32_t k = (uint32_t)(i / J), j = (uint32_t)(i % J);
+      if ((uint32_t)cum[(size_t)(k + 1) * J + j] > W[j]) atomicMax(bad_inv, K - k);
+    }
+  }
+  if (!last_block_done(done)) return;
   __shared__ int64_t ws[33];
-  const uint32_t v = valid_from(*bad_inv, K, drain);
+  const uint32_t v = valid_from(*reinterpret_cast<volatile uint32_t *>(bad_inv), K, drain);
   if (threadIdx.x == 0) *valid = v;
   int64_t carry = 0;
   for (uint32_t c0 = 0; c0 < J; c0 += blockDim.x) {
@@ -1643,39 +1672,52 @@ __global__ void __launch_bounds__(1024)
   if (threadIdx.x == 0) ubase[J] = carry;
 }
 
+// The order digest in one launch: its first n_item_blocks blocks sum the
+// terms of the recipe and quota items, the others (a segmented grid over the
+// streams' used windows) the first piece of every window the valid updates
+// use; each block adds its sum into acc[0].  The last block to finish then
+// writes D = splitmix64(acc ^ count) and gathers what the host reads back
+// besides: each stream's window count into rb[rb_W + j], the error word into
+// rb[rb_err].
 __global__ void __launch_bounds__(kThreads)
-    digest_windows_kernel(SegGrid g, const int64_t *__restrict__ wbase,
-                          const int32_t *__restrict__ win_start,
-                          const int64_t *__restrict__ node_src,
-                          const int32_t *__restrict__ node_doc, const int64_t *__restrict__ offs,
-                          uint32_t T, uint64_t h0, uint32_t J, const uint32_t *valid,
-                          const int64_t *__restrict__ ubase, const uint32_t *__restrict__ W,
-                          uint64_t seed, uint32_t G, const int32_t *__restrict__ win_clip,
-                          int *err, unsigned long long *acc) {
+    digest_kernel(uint32_t n_item_blocks, DigestHeader h, const int32_t *__restrict__ quota,
+                  uint32_t K, SegGrid wg, const int64_t *__restrict__ wbase,
+                  const int32_t *__restrict__ win_start, const int64_t *__restrict__ node_src,
+                  const int32_t *__restrict__ node_doc, const int64_t *__restrict__ offs,
+                  const uint32_t *valid, const int64_t *ubase, const uint32_t *__restrict__ W,
+                  uint64_t seed, uint32_t G, const int32_t *__restrict__ win_clip, int *err,
+                  unsigned long long *acc, uint64_t *digest, uint32_t *__restrict__ rb,
+                  uint32_t rb_W, uint32_t rb_err, unsigned *done) {
   pdl_wait_then_release();
-  uint32_t j, blk;
-  seg_locate(g, j, blk);
-  const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
-  const uint64_t U = (uint64_t)(ubase[j + 1] - ubase[j]);
+  const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
+  const uint32_t J = h.J;
+  const uint32_t v = *valid;
   uint64_t term = 0;
-  if (r < U) {
-    const uint64_t wi = window_of_rank(seed, j, G, W[j], r, err);
-    const int64_t e = wbase[j] + (int64_t)wi;
-    const int32_t node = win_start[e];
-    const int32_t d = node_doc[node];
-    const int64_t off = node_src[node] - offs[d] + (win_clip ? win_clip[e] : 0);
-    const uint64_t x = ((uint64_t)(uint32_t)d << 32) | ((uint64_t)off & 0xFFFFFFFFull);
-    term = digest_term(x, h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[j] + r);
+  if (blockIdx.x < n_item_blocks) {
+    term = digest_item_term(h, quota, K, v, (uint64_t)blockIdx.x * blockDim.x + threadIdx.x);
+  } else {
+    uint32_t j, blk;
+    seg_locate_at(wg, blockIdx.x - n_item_blocks, j, blk);
+    const uint64_t r = (uint64_t)blk * blockDim.x + threadIdx.x;
+    const uint64_t U = (uint64_t)(ubase[j + 1] - ubase[j]);
+    if (r < U) {
+      const uint64_t wi = window_of_rank(seed, j, G, W[j], r, err);
+      const int64_t e = wbase[j] + (int64_t)wi;
+      const int32_t node = win_start[e];
+      const int32_t d = node_doc[node];
+      const int64_t off = node_src[node] - offs[d] + (win_clip ? win_clip[e] : 0);
+      const uint64_t x = ((uint64_t)(uint32_t)d << 32) | ((uint64_t)off & 0xFFFFFFFFull);
+      term = digest_term(x, h0 + (uint64_t)v * J + (uint64_t)ubase[j] + r);
+    }
   }
   digest_accumulate(term, acc);
-}
-
-__global__ void digest_final_kernel(const unsigned long long *acc, uint64_t h0, uint32_t J,
-                                    const uint32_t *valid, const int64_t *ubase,
-                                    uint64_t *digest) {
-  pdl_wait_then_release();
-  const uint64_t count = h0 + (uint64_t)(*valid) * J + (uint64_t)ubase[J];
-  *digest = splitmix64((uint64_t)acc[0] ^ count);
+  if (!last_block_done(done)) return;
+  if (threadIdx.x == 0) {
+    const uint64_t count = h0 + (uint64_t)v * J + (uint64_t)ubase[J];
+    *digest = splitmix64((uint64_t)*reinterpret_cast<volatile unsigned long long *>(acc) ^ count);
+    rb[rb_err] = (uint32_t)*reinterpret_cast<const volatile int *>(err);
+  }
+  for (uint32_t j = threadIdx.x; j < J; j += blockDim.x) rb[rb_W + j] = W[j];
 }
 
 }  // namespace
@@ -1697,9 +1739,13 @@ cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64
   return cudaGetLastError();
 }
 
-cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st) {
+cudaError_t launch_keys_bound(uint64_t seed, uint32_t J, uint64_t *keys, const uint32_t *sdb,
+                              const int64_t *offs, const uint16_t *stream_bp,
+                              const unsigned long long *est_tok, uint32_t *pos_lim,
+                              cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(stream_keys_kernel, blocks_for((uint64_t)J * 4), kThreads, 0, st, seed, J, keys);
+  pdl_launch(keys_bound_kernel, blocks_for((uint64_t)J * 4), kThreads, 0, st, seed, J, keys, sdb,
+             offs, stream_bp, est_tok, pos_lim);
   return cudaGetLastError();
 }
 
@@ -1837,15 +1883,6 @@ cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
   return cudaGetLastError();
 }
 
-cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_t J,
-                               const uint16_t *stream_bp, const unsigned long long *est_tok,
-                               uint32_t *pos_lim, cudaStream_t st) {
-  ++launch_counter();
-  pdl_launch(order_bound_kernel, (J + kThreads - 1) / kThreads, kThreads, 0, st, sdb, offs, J, stream_bp,
-                                                                          est_tok, pos_lim);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
@@ -1897,41 +1934,16 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   return cudaGetLastError();
 }
 
-// Word runs of several device arrays gathered into one buffer (run s at
-// dst + off[s]), so that a single copy brings them all to the host.
-__global__ void __launch_bounds__(256) collect_kernel(CollectList l, uint32_t *__restrict__ dst) {
-  pdl_wait_then_release();
-  const uint32_t s = blockIdx.y;
-  if (s >= l.n) return;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < l.words[s];
-       i += gridDim.x * blockDim.x)
-    dst[l.off[s] + i] = l.src[s][i];
-}
-
-cudaError_t launch_collect(const CollectList &l, uint32_t *dst, cudaStream_t st) {
-  if (l.n == 0) return cudaSuccess;
-  uint32_t most = 1;
-  for (uint32_t s = 0; s < l.n; s++) most = most > l.words[s] ? most : l.words[s];
-  ++launch_counter();
-  const uint32_t gx = (most + 255) / 256 < 64 ? (most + 255) / 256 : 64;
-  pdl_launch(collect_kernel, dim3(gx, l.n), 256, 0, st, l, dst);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
                           const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,
-                          int64_t *npieces, int64_t *ptokens, cudaStream_t st) {
+                          int64_t *npieces, int64_t *ptokens, int64_t *node_base, uint32_t *rb,
+                          uint32_t rb_rmax, uint32_t rb_err, const int *err, unsigned *done,
+                          cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(cutoff_kernel, blocks_for(J, 128), 128, 0, st, sdb, J, D0, kex, pex, cum_last, T, G,
-                                                    need_num, pos_lim, cutoff, npieces, ptokens);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
-                             cudaStream_t st) {
-  ++launch_counter();
-  pdl_launch(node_base_kernel, 1, (J <= 32 ? 32 : J <= 256 ? 256 : 1024), 0, st, npieces, J, node_base);
+  pdl_launch(cutoff_kernel, blocks_for(J, kCutoffThreads), kCutoffThreads, 0, st, sdb, J, D0, kex,
+             pex, cum_last, T, G, need_num, pos_lim, cutoff, npieces, ptokens, node_base, rb,
+             rb_rmax, rb_err, err, done);
   return cudaGetLastError();
 }
 
@@ -1992,19 +2004,6 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
-                               const int64_t *wbase, const int32_t *win_start,
-                               const int32_t *next, const int32_t *win_end,
-                               const int32_t *win_clip, uint32_t J, uint32_t B, uint32_t K,
-                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *row_win,
-                               int *err, cudaStream_t st) {
-  ++launch_counter();
-  pdl_launch(row_windows_kernel, blocks_for((uint64_t)K * B), kThreads, 0, st, 
-      rb, cum, W, wbase, win_start, next, win_end, win_clip, J, B, K, seed, G, shuffle_rows,
-      row_win, err);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64_t *npieces,
                                 const int64_t *node_S, const uint32_t *cutoff,
                                 const uint32_t *sdb, uint32_t J, uint32_t T, uint32_t *W,
@@ -2021,44 +2020,34 @@ cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_first_bad(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
-                             uint32_t *bad_inv, cudaStream_t st) {
+cudaError_t launch_row_table(const int32_t *rb, const int32_t *cum, const uint32_t *W,
+                             const int64_t *wbase, const int32_t *win_start, const int32_t *next,
+                             const int32_t *win_end, const int32_t *win_clip, uint32_t J,
+                             uint32_t B, uint32_t K, uint64_t seed, uint32_t G,
+                             uint32_t shuffle_rows, int4 *row_win, int *err, uint32_t *bad_inv,
+                             uint32_t drain, uint32_t *valid, int64_t *ubase, unsigned *done,
+                             cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(first_bad_kernel, blocks_for((uint64_t)K * J), kThreads, 0, st, cum, W, J, K,
-             bad_inv);
+  const uint32_t n_row = blocks_for((uint64_t)K * B), n_bad = blocks_for((uint64_t)K * J);
+  pdl_launch(row_table_kernel, n_row + n_bad, kThreads, 0, st, n_row, rb, cum, W, wbase,
+             win_start, next, win_end, win_clip, J, B, K, seed, G, shuffle_rows, row_win, err,
+             bad_inv, drain, valid, ubase, done);
   return cudaGetLastError();
 }
 
-cudaError_t launch_digest(const DigestHeader &h, const uint32_t *bad_inv, uint32_t drain,
-                          uint32_t *valid, const int32_t *quota, const int32_t *cum,
-                          const uint32_t *W, SegGrid wg, const int64_t *wbase,
-                          const int32_t *win_start, const int64_t *node_src,
-                          const int32_t *node_doc, const int64_t *offs, uint32_t T, uint32_t K,
+cudaError_t launch_digest(const DigestHeader &h, const int32_t *quota, uint32_t K, SegGrid wg,
+                          const int64_t *wbase, const int32_t *win_start,
+                          const int64_t *node_src, const int32_t *node_doc, const int64_t *offs,
+                          const uint32_t *valid, const int64_t *ubase, const uint32_t *W,
                           uint64_t seed, uint32_t G, const int32_t *win_clip, int *err,
-                          unsigned long long *acc, int64_t *ubase, uint64_t *digest_out,
-                          cudaStream_t st) {
+                          unsigned long long *acc, uint64_t *digest, uint32_t *rb, uint32_t rb_W,
+                          uint32_t rb_err, unsigned *done, cudaStream_t st) {
   const uint64_t h0 = (uint64_t)kDigestScalars + 2ull * h.S + 4ull * h.J + h.n_piece_items;
+  const uint32_t n_items = blocks_for(h0 + (uint64_t)K * h.J);
   ++launch_counter();
-  pdl_launch(digest_used_kernel, 1, (h.J <= 32 ? 32 : h.J <= 256 ? 256 : 1024), 0, st, cum, W,
-             h.J, bad_inv, K, drain, valid, ubase);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ++launch_counter();
-  pdl_launch(digest_items_kernel, blocks_for(h0 + (uint64_t)K * h.J), kThreads, 0, st, h, quota,
-             K, valid, acc);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (wg.n_blocks > 0) {
-    ++launch_counter();
-    pdl_launch(digest_windows_kernel, wg.n_blocks, kThreads, 0, st, wg, wbase, win_start, node_src,
-                                                            node_doc, offs, T, h0, h.J, valid,
-                                                            ubase, W, seed, G, win_clip, err,
-                                                            acc);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  ++launch_counter();
-  pdl_launch(digest_final_kernel, 1, 1, 0, st, acc, h0, h.J, valid, ubase, digest_out);
+  pdl_launch(digest_kernel, n_items + wg.n_blocks, kThreads, 0, st, n_items, h, quota, K, wg,
+             wbase, win_start, node_src, node_doc, offs, valid, ubase, W, seed, G, win_clip, err,
+             acc, digest, rb, rb_W, rb_err, done);
   return cudaGetLastError();
 }
 

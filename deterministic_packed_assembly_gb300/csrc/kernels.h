@@ -23,7 +23,14 @@ struct SegGrid {
 // ---- validation, keys, quotas ---------------------------------------------
 cudaError_t launch_validate_offsets(const int64_t *offs, uint32_t n_docs, uint64_t n_tokens,
                                     int *err, int n_sms, cudaStream_t st);
-cudaError_t launch_stream_keys(uint64_t seed, uint32_t J, uint64_t *keys, cudaStream_t st);
+// The shuffle's round keys of every stream (keys[4 j + r]); with est_tok
+// (per stream, the recipe's estimate of the tokens its windows hold) also
+// pos_lim[j], the shuffled positions taken of stream j (about those its
+// estimate needs for a stream without a held-out rate, all for the others).
+cudaError_t launch_keys_bound(uint64_t seed, uint32_t J, uint64_t *keys, const uint32_t *sdb,
+                              const int64_t *offs, const uint16_t *stream_bp,
+                              const unsigned long long *est_tok, uint32_t *pos_lim,
+                              cudaStream_t st);
 // The schedule on the device: piece p covers updates [begin[p], begin[p+1])
 // (the last one up to K) with B[p] rows per update and weights sw[p][S],
 // tw[p][J]; a recipe without a schedule is one piece.
@@ -54,15 +61,11 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 // stream the per-stream rates (a stream of a source that holds nothing out
 // keeps nothing)
 // pos_lim (per stream, or NULL: every position): the shuffled positions
-// taken, from launch_order_bound; the others are left as they are
+// taken, from launch_keys_bound; the others are left as they are
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
                          uint32_t *order, uint32_t *klen, int *err, cudaStream_t st);
-// est_tok: per stream, the recipe's estimate of the tokens its windows hold
-cudaError_t launch_order_bound(const uint32_t *sdb, const int64_t *offs, uint32_t J,
-                               const uint16_t *stream_bp, const unsigned long long *est_tok,
-                               uint32_t *pos_lim, cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 // copy_dst non-null: tokens is host memory the device can address, and
 // every hashed document is also written to copy_dst (tokens_read counts them).
@@ -116,13 +119,17 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
                                const uint32_t *sdb, uint32_t J, uint32_t D0,
                                const uint32_t *pos_lim, cudaStream_t st);
 size_t scan_scratch_bytes(uint64_t n);
-// per stream: cutoff c_j, pieces and kept tokens before it; rmax given
+// per stream: cutoff c_j, pieces and kept tokens before it (rmax given as
+// cum_last, the quota table's last row); then node_base[j] (J + 1 entries:
+// the first node of each stream, one terminal node after each), and the
+// words the host reads back besides: cum_last[j] at rb[rb_rmax + j], the
+// error word at rb[rb_err].  *done: zeroed before.
 cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const int64_t *kex,
                           const int64_t *pex, const int32_t *cum_last, uint32_t T, uint32_t G,
                           const uint16_t *need_num, const uint32_t *pos_lim, uint32_t *cutoff,
-                          int64_t *npieces, int64_t *ptokens, cudaStream_t st);
-cudaError_t launch_node_base(const int64_t *npieces, uint32_t J, int64_t *node_base,
-                             cudaStream_t st);
+                          int64_t *npieces, int64_t *ptokens, int64_t *node_base, uint32_t *rb,
+                          uint32_t rb_rmax, uint32_t rb_err, const int *err, unsigned *done,
+                          cudaStream_t st);
 
 // ---- pieces, next, jump tables, windows -----------------------------------
 cudaError_t launch_expand(SegGrid g, const uint32_t *sdb, uint32_t D0, const uint32_t *cutoff,
@@ -152,36 +159,24 @@ cudaError_t launch_window_starts(SegGrid g, const int32_t *levels, int64_t n_nod
 // update k takes, or (-1, -1) when the row lies past the end of its stream
 // (win_end / win_clip: wrap packing's tables; null for greedy windows); G > 0
 // reads windows in a shuffled order within segments, shuffle_rows shuffles the
-// rows of every update.
-cudaError_t launch_row_windows(const int32_t *rb, const int32_t *cum, const uint32_t *W,
-                               const int64_t *wbase, const int32_t *win_start,
-                               const int32_t *next, const int32_t *win_end,
-                               const int32_t *win_clip, uint32_t J, uint32_t B, uint32_t K,
-                               uint64_t seed, uint32_t G, uint32_t shuffle_rows, int4 *row_win,
-                               int *err, cudaStream_t st);
+// rows of every update.  In the same launch: *bad_inv (zeroed before) = K - k
+// for the first update k that asks a stream for a window it does not have
+// (0 if none), then the valid horizon *valid (through that update with
+// drain, else before it) and ubase[j] (J + 1 entries: the first digest item
+// of each stream's used windows).  *done: zeroed before.
+cudaError_t launch_row_table(const int32_t *rb, const int32_t *cum, const uint32_t *W,
+                             const int64_t *wbase, const int32_t *win_start, const int32_t *next,
+                             const int32_t *win_end, const int32_t *win_clip, uint32_t J,
+                             uint32_t B, uint32_t K, uint64_t seed, uint32_t G,
+                             uint32_t shuffle_rows, int4 *row_win, int *err, uint32_t *bad_inv,
+                             uint32_t drain, uint32_t *valid, int64_t *ubase, unsigned *done,
+                             cudaStream_t st);
 // Wrap packing: windows of exactly T tokens of each stream's kept run.
 cudaError_t launch_wrap_windows(SegGrid g, const int64_t *node_base, const int64_t *npieces,
                                 const int64_t *node_S, const uint32_t *cutoff,
                                 const uint32_t *sdb, uint32_t J, uint32_t T, uint32_t *W,
                                 const int64_t *wbase, int32_t *win_start, int32_t *win_end,
                                 int32_t *win_clip, cudaStream_t st);
-// *bad_inv (zeroed before) = K - k for the first update k that asks a stream
-// for a window it does not have, 0 if none; launch_digest turns it into the
-// valid horizon.
-cudaError_t launch_first_bad(const int32_t *cum, const uint32_t *W, uint32_t J, uint32_t K,
-                             uint32_t *bad_inv, cudaStream_t st);
-
-// ---- readbacks -------------------------------------------------------------
-// Up to kCollectMax runs of 32-bit words, src[s][0 .. words[s]), copied to
-// dst + off[s] in one launch.
-constexpr uint32_t kCollectMax = 8;
-struct CollectList {
-  const uint32_t *src[kCollectMax];
-  uint32_t off[kCollectMax];
-  uint32_t words[kCollectMax];
-  uint32_t n;
-};
-cudaError_t launch_collect(const CollectList &l, uint32_t *dst, cudaStream_t st);
 
 // ---- order digest ---------------------------------------------------------
 constexpr int kDigestScalars = 12;
@@ -196,16 +191,17 @@ struct DigestHeader {
   uint64_t n_piece_items;
   uint32_t S, J;
 };
-// Writes the valid horizon (*valid, from *bad_inv and drain), then the order
-// digest.
-cudaError_t launch_digest(const DigestHeader &h, const uint32_t *bad_inv, uint32_t drain,
-                          uint32_t *valid, const int32_t *quota, const int32_t *cum,
-                          const uint32_t *W, SegGrid wg, const int64_t *wbase,
-                          const int32_t *win_start, const int64_t *node_src,
-                          const int32_t *node_doc, const int64_t *offs, uint32_t T, uint32_t K,
+// The order digest over the valid horizon (*valid and ubase from
+// launch_row_table) into *digest; in the same launch each stream's window
+// count W[j] is copied to rb[rb_W + j] and the error word to rb[rb_err].
+// acc[0] and *done: zeroed before.
+cudaError_t launch_digest(const DigestHeader &h, const int32_t *quota, uint32_t K, SegGrid wg,
+                          const int64_t *wbase, const int32_t *win_start,
+                          const int64_t *node_src, const int32_t *node_doc, const int64_t *offs,
+                          const uint32_t *valid, const int64_t *ubase, const uint32_t *W,
                           uint64_t seed, uint32_t G, const int32_t *win_clip, int *err,
-                          unsigned long long *acc /* [2] zeroed */, int64_t *ubase,
-                          uint64_t *digest_out, cudaStream_t st);
+                          unsigned long long *acc, uint64_t *digest, uint32_t *rb, uint32_t rb_W,
+                          uint32_t rb_err, unsigned *done, cudaStream_t st);
 
 // ---- per-step assembly ----------------------------------------------------
 struct GatherParams {
