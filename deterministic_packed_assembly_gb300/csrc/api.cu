@@ -797,7 +797,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
     nsk::SegGrid g{static_cast<uint32_t *>(d_order_bb), J, order_bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
                             heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr,
-                            pos_lim, order, klen, c->err, st));
+                            pos_lim, order, klen, c->err, c->n_sms, st));
   }
 
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
@@ -865,7 +865,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // kept document whole as one piece (no document reaches 2^31 tokens)
   const uint32_t chunk = wrap ? 0x80000000u : T;
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes,
-                                static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, st));
+                                static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, c->n_sms, st));
   // the cutoff reads the quota table, and the readback after it the error
   // word the offsets check sets: the side streams join here, after the scans
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));

@@ -1033,20 +1033,15 @@ __device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, ui
 // instead of adding up.
 constexpr uint32_t kOrderPerThread = 8;
 
-__global__ void __launch_bounds__(kThreads)
-    order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
-                 const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
-                 const uint16_t *__restrict__ stream_bp_heldout_mode,
-                 const uint32_t *__restrict__ pos_lim, uint32_t *__restrict__ order,
-                 uint32_t *__restrict__ klen, int *err) {
-  pdl_wait_then_release();
-  uint32_t j, blk;
-  seg_locate(g, j, blk);
-  const uint32_t b0 = sdb[j];
-  const uint64_t N = sdb[j + 1] - b0;  // the permutation's domain
-  const uint64_t Nb = pos_lim ? pos_lim[j] : N;  // the positions taken
-  const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
-  if (p0 >= Nb) return;
+// The positions p0 + m * blockDim.x (m < kOrderPerThread, below Nb) of
+// stream j: their documents and kept lengths.
+__device__ __forceinline__ void order_positions(const uint64_t *__restrict__ keys, uint32_t j,
+                                                uint32_t b0, uint64_t N, uint64_t Nb,
+                                                uint64_t p0, const int64_t *__restrict__ offs,
+                                                uint64_t n_tokens, uint32_t D0,
+                                                const uint16_t *__restrict__ stream_bp_heldout_mode,
+                                                uint32_t *__restrict__ order,
+                                                uint32_t *__restrict__ klen, int *err) {
   const uint32_t half = feistel_half(N);
   const uint64_t mask = (half >= 64) ? ~0ull : ((1ull << half) - 1);
   uint64_t k[4];
@@ -1104,6 +1099,28 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+__global__ void __launch_bounds__(kThreads)
+    order_kernel(SegGrid g, const uint32_t *__restrict__ sdb, const uint64_t *__restrict__ keys,
+                 const int64_t *__restrict__ offs, uint64_t n_tokens, uint32_t D0,
+                 const uint16_t *__restrict__ stream_bp_heldout_mode,
+                 const uint32_t *__restrict__ pos_lim, uint32_t *__restrict__ order,
+                 uint32_t *__restrict__ klen, int *err) {
+  pdl_wait_then_release();
+  // the grid strides over the layout's blocks: those wholly past a stream's
+  // taken positions cost an iteration, not a block
+  for (uint32_t vb = blockIdx.x; vb < g.n_blocks; vb += gridDim.x) {
+    uint32_t j, blk;
+    seg_locate_at(g, vb, j, blk);
+    const uint32_t b0 = sdb[j];
+    const uint64_t N = sdb[j + 1] - b0;  // the permutation's domain
+    const uint64_t Nb = pos_lim ? pos_lim[j] : N;  // the positions taken
+    const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
+    if (p0 < Nb) order_positions(keys, j, b0, N, Nb, p0, offs, n_tokens, D0,
+                                 stream_bp_heldout_mode, order, klen, err);
+    __syncthreads();  // the block's stream is looked up again
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Exclusive scans of the kept lengths and of the piece counts ceil(L / T):
 // reduce per tile, scan the tile sums, rescan each tile with its offset.  A
@@ -1140,45 +1157,50 @@ __global__ void scan_tile_zero_kernel(const uint32_t *__restrict__ sdb, uint32_t
 }
 
 __global__ void __launch_bounds__(kScanWarps * 32)
-    scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
+    scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint64_t nb, uint32_t T,
                        const uint8_t *__restrict__ tile_zero, int64_t *__restrict__ bs_a,
                        int64_t *__restrict__ bs_b) {
   pdl_wait_then_release();
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
-  if (tile_zero && tile_zero[blockIdx.x]) {
-    if (threadIdx.x == 0) {
-      bs_a[blockIdx.x] = 0;
-      bs_b[blockIdx.x] = 0;
-    }
-    return;
-  }
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
-  int64_t a = 0, b = 0;
+  // the grid strides over the tiles (a tile past a stream's shuffled part
+  // costs an iteration, not a block)
+  for (uint64_t t = blockIdx.x; t < nb; t += gridDim.x) {
+    if (tile_zero && tile_zero[t]) {
+      if (threadIdx.x == 0) {
+        bs_a[t] = 0;
+        bs_b[t] = 0;
+      }
+      continue;
+    }
+    const uint64_t seg = t * kScanTile + (uint64_t)w * kScanRounds * 32;
+    int64_t a = 0, b = 0;
 #pragma unroll
-  for (int r = 0; r < kScanRounds; r++) {
-    const uint64_t i = seg + (uint64_t)r * 32 + lane;
-    if (i < n) {
-      const uint32_t v = klen[i];
-      a += v;
-      b += ((uint64_t)v + T - 1) / T;
+    for (int r = 0; r < kScanRounds; r++) {
+      const uint64_t i = seg + (uint64_t)r * 32 + lane;
+      if (i < n) {
+        const uint32_t v = klen[i];
+        a += v;
+        b += ((uint64_t)v + T - 1) / T;
+      }
     }
-  }
-  a = warp_sum_i64(a);
-  b = warp_sum_i64(b);
-  if (lane == 0) {
-    sa[w] = a;
-    sb[w] = b;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int64_t ta = 0, tb = 0;
-    for (int q = 0; q < kScanWarps; q++) {
-      ta += sa[q];
-      tb += sb[q];
+    a = warp_sum_i64(a);
+    b = warp_sum_i64(b);
+    if (lane == 0) {
+      sa[w] = a;
+      sb[w] = b;
     }
-    bs_a[blockIdx.x] = ta;
-    bs_b[blockIdx.x] = tb;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t ta = 0, tb = 0;
+      for (int q = 0; q < kScanWarps; q++) {
+        ta += sa[q];
+        tb += sb[q];
+      }
+      bs_a[t] = ta;
+      bs_b[t] = tb;
+    }
+    __syncthreads();
   }
 }
 
@@ -1235,15 +1257,17 @@ __global__ void __launch_bounds__(1024)
 }
 
 __global__ void __launch_bounds__(kScanWarps * 32)
-    scan_apply_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint32_t T,
+    scan_apply_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint64_t nb, uint32_t T,
                       const uint8_t *__restrict__ tile_zero, const int64_t *__restrict__ bs_a,
                       const int64_t *__restrict__ bs_b, int64_t *__restrict__ kex,
                       int64_t *__restrict__ pex) {
   pdl_wait_then_release();
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
-  if (tile_zero && tile_zero[blockIdx.x]) return;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t seg = (uint64_t)blockIdx.x * kScanTile + (uint64_t)w * kScanRounds * 32;
+  // the grid strides over the tiles, as in scan_reduce_kernel
+  for (uint64_t t = blockIdx.x; t < nb; t += gridDim.x) {
+  if (tile_zero && tile_zero[t]) continue;
+  const uint64_t seg = t * kScanTile + (uint64_t)w * kScanRounds * 32;
   int64_t a = 0, b = 0;
 #pragma unroll
   for (int r = 0; r < kScanRounds; r++) {
@@ -1261,7 +1285,7 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     sb[w] = b;
   }
   __syncthreads();
-  int64_t ca = bs_a[blockIdx.x], cb = bs_b[blockIdx.x];
+  int64_t ca = bs_a[t], cb = bs_b[t];
   for (int q = 0; q < w; q++) {
     ca += sa[q];
     cb += sb[q];
@@ -1279,6 +1303,8 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     ca += __shfl_sync(0xffffffffu, xa, 31);
     cb += __shfl_sync(0xffffffffu, xb, 31);
   }
+  __syncthreads();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1287,6 +1313,10 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 // can read of stream j), or the whole stream.  Windows 0..rmax_j - 1 hold at most
 // rmax_j * T tokens, so at least one piece follows them inside the prefix and
 // their greedy packing is the same as over the whole stream.
+// A warp per stream searches the sorted prefix sums 33 ways at a time (each
+// lane probes one point, a ballot keeps the interval that holds the first
+// position past the need), so the search takes about log_33 of the stream's
+// length in dependent loads rather than log_2.
 // The last block to finish then numbers every stream's first node --
 // node_base[j] = the sum over j' < j of (pieces of j' + 1 terminal node) --
 // and gathers what the host reads back besides: each stream's windows over
@@ -1302,7 +1332,8 @@ __global__ void __launch_bounds__(kCutoffThreads)
                   int64_t *__restrict__ node_base, uint32_t *__restrict__ rb, uint32_t rb_rmax,
                   uint32_t rb_err, const int *err, unsigned *done) {
   pdl_wait_then_release();
-  const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const uint32_t j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (j < J) {
     const uint64_t b = sdb[j] - D0, e = sdb[j + 1] - D0;
     const uint64_t N = e - b;
@@ -1310,21 +1341,34 @@ __global__ void __launch_bounds__(kCutoffThreads)
     const int64_t need = tokens_needed(cum_last[j], G, T, need_num ? need_num[j] : 1024u);
     uint64_t c = N;
     if (kex[e] - base > need) {
-      // a stream shuffled only in part meets its need within that part (its
+      // the first m in [1, hi) whose prefix exceeds the need, else hi; a
+      // stream shuffled only in part meets its need within that part (its
       // lengths are 0 past it, and the prefix sums there are not written)
       uint64_t lo = 1, hi = pos_lim ? min(N, (uint64_t)pos_lim[j]) : N;
-      while (lo < hi) {
-        const uint64_t mid = lo + (hi - lo) / 2;
-        if (kex[b + mid] - base > need)
-          hi = mid;
-        else
-          lo = mid + 1;
+      while (hi - lo > 32) {
+        const uint64_t span = hi - lo;
+        // 32 increasing points in [lo + 1, hi): span / 33 >= 1 apart
+        const uint64_t m = lo + span * (uint64_t)(lane + 1) / 33;
+        const unsigned hit = __ballot_sync(0xffffffffu, kex[b + m] - base > need);
+        const int f = __ffs(hit) - 1;  // first probe past the need (-1: none)
+        const uint64_t m_f = __shfl_sync(0xffffffffu, m, f < 0 ? 31 : f);
+        const uint64_t m_p = __shfl_sync(0xffffffffu, m, f > 0 ? f - 1 : 0);
+        if (f < 0) {
+          lo = m_f + 1;
+        } else {
+          hi = m_f;
+          if (f > 0) lo = m_p + 1;
+        }
       }
-      c = lo;
+      const uint64_t m = lo + (uint64_t)lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, m < hi && kex[b + m] - base > need);
+      c = hit ? lo + (uint64_t)(__ffs(hit) - 1) : hi;
     }
-    cutoff[j] = (uint32_t)c;
-    npieces[j] = pex[b + c] - pex[b];
-    ptokens[j] = kex[b + c] - base;
+    if (lane == 0) {
+      cutoff[j] = (uint32_t)c;
+      npieces[j] = pex[b + c] - pex[b];
+      ptokens[j] = kex[b + c] - base;
+    }
   }
   if (!last_block_done(done)) return;
   __shared__ int64_t ws[33];
@@ -1886,10 +1930,13 @@ cudaError_t launch_fill_need(const uint32_t *sdb, uint32_t J, uint32_t D0,
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
-                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st) {
+                         uint32_t *order, uint32_t *klen, int *err, int n_sms,
+                         cudaStream_t st) {
   if (g.n_blocks == 0) return cudaSuccess;
   ++launch_counter();
-  pdl_launch(order_kernel, g.n_blocks, kThreads, 0, st, g, sdb, keys, offs, n_tokens, D0,
+  // eight blocks of 256 threads an SM at most, striding over the layout
+  const unsigned grid = std::min<unsigned>(g.n_blocks, (unsigned)n_sms * 8u);
+  pdl_launch(order_kernel, grid, kThreads, 0, st, g, sdb, keys, offs, n_tokens, D0,
                                                 stream_bp_heldout_mode, pos_lim, order, klen,
                                                 err);
   return cudaGetLastError();
@@ -1903,8 +1950,10 @@ size_t scan_scratch_bytes(uint64_t n) {
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
                                const uint32_t *sdb, uint32_t J, uint32_t D0,
-                               const uint32_t *pos_lim, cudaStream_t st) {
+                               const uint32_t *pos_lim, int n_sms, cudaStream_t st) {
   const uint64_t nb = (n + kScanTile - 1) / kScanTile;
+  // eight blocks of 256 threads an SM at most, striding over the tiles
+  const unsigned grid = (unsigned)std::min<uint64_t>(nb, (uint64_t)n_sms * 8);
   if (scratch_bytes < scan_scratch_bytes(n)) return cudaErrorInvalidValue;
   int64_t *bs_a = static_cast<int64_t *>(scratch);
   int64_t *bs_b = bs_a + (nb + 1);
@@ -1919,8 +1968,8 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   }
   if (nb > 0) {
     ++launch_counter();
-    pdl_launch(scan_reduce_kernel, (unsigned)nb, kScanWarps * 32, 0, st, klen, n, T, tile_zero, bs_a,
-                                                                 bs_b);
+    pdl_launch(scan_reduce_kernel, grid, kScanWarps * 32, 0, st, klen, n, nb, T, tile_zero, bs_a,
+               bs_b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1929,8 +1978,8 @@ cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nb == 0) return e;
   ++launch_counter();
-  pdl_launch(scan_apply_kernel, (unsigned)nb, kScanWarps * 32, 0, st, klen, n, T, tile_zero, bs_a, bs_b,
-                                                               kex, pex);
+  pdl_launch(scan_apply_kernel, grid, kScanWarps * 32, 0, st, klen, n, nb, T, tile_zero, bs_a,
+             bs_b, kex, pex);
   return cudaGetLastError();
 }
 
@@ -1941,7 +1990,7 @@ cudaError_t launch_cutoff(const uint32_t *sdb, uint32_t J, uint32_t D0, const in
                           uint32_t rb_rmax, uint32_t rb_err, const int *err, unsigned *done,
                           cudaStream_t st) {
   ++launch_counter();
-  pdl_launch(cutoff_kernel, blocks_for(J, kCutoffThreads), kCutoffThreads, 0, st, sdb, J, D0, kex,
+  pdl_launch(cutoff_kernel, blocks_for((uint64_t)J * 32, kCutoffThreads), kCutoffThreads, 0, st, sdb, J, D0, kex,
              pex, cum_last, T, G, need_num, pos_lim, cutoff, npieces, ptokens, node_base, rb,
              rb_rmax, rb_err, err, done);
   return cudaGetLastError();

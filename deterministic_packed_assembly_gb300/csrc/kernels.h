@@ -65,7 +65,8 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
-                         uint32_t *order, uint32_t *klen, int *err, cudaStream_t st);
+                         uint32_t *order, uint32_t *klen, int *err, int n_sms,
+                         cudaStream_t st);
 // held-out documents of the prefix each stream's horizon reaches get klen 0
 // copy_dst non-null: tokens is host memory the device can address, and
 // every hashed document is also written to copy_dst (tokens_read counts them).
@@ -117,7 +118,7 @@ uint32_t copy_chunk_tokens();
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
                                const uint32_t *sdb, uint32_t J, uint32_t D0,
-                               const uint32_t *pos_lim, cudaStream_t st);
+                               const uint32_t *pos_lim, int n_sms, cudaStream_t st);
 size_t scan_scratch_bytes(uint64_t n);
 // per stream: cutoff c_j, pieces and kept tokens before it (rmax given as
 // cum_last, the quota table's last row); then node_base[j] (J + 1 entries:
