@@ -741,29 +741,10 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_ALLOC(c->rb);
   SideStream side;
   NS_CK(side.create());
+  // the side streams start from here (the recipe uploaded, the control block
+  // zeroed); their launches are issued after the main stream's keys and
+  // shuffle, which the host enqueues first
   NS_CK(cudaEventRecord(side.fork, st));
-  NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
-  if (quota_warp) {
-    NS_CK(nsk::launch_quota_warp(qp, S, static_cast<uint32_t *>(d_src_first), J, K, max_strata,
-                                 c->quota, c->cum, ready, side.s));
-  } else {
-    int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
-    NS_ALLOC(src_quota);
-    NS_CK(nsk::launch_quota_sources(qp, S, K, src_quota, side.s));
-    NS_CK(nsk::launch_quota_strata(qp, src_quota, static_cast<uint32_t *>(d_src_first), S, J, K,
-                                   max_strata, c->quota, c->cum, ready, side.s));
-  }
-  NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
-  NS_CK(cudaEventRecord(side.join, side.s));
-  // The corpus partition, checked whole on a stream of its own beside the
-  // quotas, the shuffle and the hash: every kernel that reads tokens also
-  // checks the offsets it uses, so a malformed partition is reported
-  // (BAD_INPUT) at the next readback, never read past.
-  NS_CK(cudaStreamWaitEvent(side.s2, side.fork, 0));
-  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, c->n_sms,
-                                     side.s2));
-  NS_CK(nsk::launch_pad_tail(c->pad_id, T, pad_tiles, c->pad_tail, side.s2));
-  NS_CK(cudaEventRecord(side.join2, side.s2));
 
   // ---- 2. shuffled order and lengths of every position ----------------------
   uint64_t *keys = a.temp<uint64_t>((size_t)J * 4);
@@ -799,6 +780,30 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
                             heldout_mode ? static_cast<uint16_t *>(d_stream_bp) : nullptr,
                             pos_lim, order, klen, c->err, c->n_sms, st));
   }
+
+  // ---- the side streams: quotas; the offsets check and padding terms ------
+  NS_CK(cudaStreamWaitEvent(side.s, side.fork, 0));
+  if (quota_warp) {
+    NS_CK(nsk::launch_quota_warp(qp, S, static_cast<uint32_t *>(d_src_first), J, K, max_strata,
+                                 c->quota, c->cum, ready, side.s));
+  } else {
+    int32_t *src_quota = a.temp<int32_t>((size_t)K * S);
+    NS_ALLOC(src_quota);
+    NS_CK(nsk::launch_quota_sources(qp, S, K, src_quota, side.s));
+    NS_CK(nsk::launch_quota_strata(qp, src_quota, static_cast<uint32_t *>(d_src_first), S, J, K,
+                                   max_strata, c->quota, c->cum, ready, side.s));
+  }
+  NS_CK(nsk::launch_row_base(c->quota, J, K, c->rb, side.s));
+  NS_CK(cudaEventRecord(side.join, side.s));
+  // The corpus partition, checked whole on a stream of its own beside the
+  // quotas, the shuffle and the hash: every kernel that reads tokens also
+  // checks the offsets it uses, so a malformed partition is reported
+  // (BAD_INPUT) at the next readback, never read past.
+  NS_CK(cudaStreamWaitEvent(side.s2, side.fork, 0));
+  NS_CK(nsk::launch_validate_offsets(c->offs, c->n_docs, c->n_tokens, c->err, c->n_sms,
+                                     side.s2));
+  NS_CK(nsk::launch_pad_tail(c->pad_id, T, pad_tiles, c->pad_tail, side.s2));
+  NS_CK(cudaEventRecord(side.join2, side.s2));
 
   // ---- 3. held-out flags of the prefix each stream's horizon reaches -------
   // Runs beside the quota kernels: it reads each stream's need from their
