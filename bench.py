@@ -80,7 +80,7 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="c3", choices=sorted(WORKLOADS))
     ap.add_argument("--launch", type=int, default=0,
-                    help="updates per ns_pack_step launch (0: enough for about 2^28 positions "
+                    help="updates per ns_pack_step launch (0: equal launches of at most 2^30 positions "
                          "per launch, see auto_launch)")
     ap.add_argument("--slices", type=int, default=1,
                     help="split every launch into this many row-slice launches (the same "
@@ -311,21 +311,29 @@ def variant_kwargs(c, name: str) -> dict:
 
 
 def auto_launch(max_steps: int, rows: int, T: int) -> int:
-    """Updates per launch: about 2^28 positions (a 3.5 GB output buffer; a
-    launch's tail of partly idle SMs then costs little), at most the
-    horizon.  128 for the 512 x 4096, 256 x 8192 and 64 x 32768 workloads;
-    the whole horizon for 8 x 4096."""
-    return max(1, min(max_steps, -(-(1 << 28) // max(1, rows * T))))
+    """Most updates a launch takes: the horizon in equal launches of at most
+    2^30 positions (a 14 GB output buffer; the longer a launch, the less its
+    tail of partly idle SMs costs).  500 for the 512 x 4096 rows (1000
+    updates), 200 for 256 x 8192 (200), 512 for 64 x 32768 (a horizon of
+    1024, of which launch_plan splits the 574 valid updates into two of
+    287), the whole horizon for 8 x 4096."""
+    per = max(1, (1 << 30) // max(1, rows * T))
+    n = -(-max_steps // per)
+    return max(1, -(-max_steps // max(1, n)))
 
 
 def launch_plan(pk, valid: int, L: int):
     """(first update, updates, rows per update) of each launch: at most L
-    updates, never across a schedule piece (rows per update may change)."""
+    updates, never across a schedule piece (rows per update may change);
+    each piece in launches of equal size (the fewest that fit L), so that
+    no short launch is left at its end."""
     begins = sorted({int(p["begin"]) for p in pk.schedule}) if pk.schedule else [0]
     s = 0
     for e in [b for b in begins if 0 < b < valid] + [valid]:
+        n = -(-(e - s) // L)
+        per = -(-(e - s) // max(1, n))
         while s < e:
-            m = min(L, e - s)
+            m = min(per, e - s)
             yield s, m, pk.rows_of_step(s)
             s += m
 

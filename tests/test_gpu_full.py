@@ -1,7 +1,7 @@
-"""The five workloads at full size, in the launch configuration the benchmark
-times (its auto_launch updates per ns_pack_step launch -- 128 for the three
-large workloads, the whole horizon for the small-batch ones -- all rows of
-the global batch).
+"""The five workloads at full size, in the launch size the benchmark times
+(its auto_launch updates per ns_pack_step launch -- at most 2^30 positions:
+500 for the 512 x 4096 rows, 200 for 256 x 8192, 512 for 64 x 32768, the
+whole horizon for the small-batch ones -- all rows of the global batch).
 
 Every update of every workload is compared with the oracle on its row
 fingerprints, learned counts, batch fingerprint and update learned count;
