@@ -425,6 +425,27 @@ def test_quota_tables_beyond_one_warp(S, strata):
     compare_steps(pk, o, range(o.valid_steps), launch=3)
 
 
+def test_largest_stream_count():
+    # the most streams a recipe may have (1024 sources x 64 strata): the
+    # cutoff's, row table's and digest's last blocks scan every stream, the
+    # hash looks at streams 32 at a time, the quotas rank 1024 sources by a
+    # bitonic sort; half the sources hold documents out
+    S, strata = 1024, 64
+    J = S * strata
+    rng = np.random.default_rng(65536)
+    lengths = rng.integers(1, 41, size=8 * J)
+    c = corpus_from_lengths(lengths, T=64, B=4096, max_steps=4, stream_docs=[8] * J,
+                            stream_source=[s for s in range(S) for _ in range(strata)],
+                            source_weight=[int(x) for x in rng.integers(500, 1000, size=S)],
+                            stream_weight=[int(x) for x in rng.integers(500, 1000, size=J)],
+                            heldout_bp=[3000 * (s % 2) for s in range(S)], drain=True,
+                            tokens=rng.integers(0, 32000, size=int(lengths.sum())))
+    pk, o = packer_for(c), oracle_for(c)
+    _check_tables(pk, o, c)
+    assert o.valid_steps == 4
+    compare_steps(pk, o, range(o.valid_steps), launch=2)
+
+
 @pytest.mark.parametrize("max_steps", [2, 6, 40])
 def test_both_held_out_sweeps(max_steps):
     # a short horizon stops hashing each stream once its kept tokens cover
