@@ -684,7 +684,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   const size_t r2_bytes = r2_W + (size_t)J * 4;
   // One block of words that start at zero, cleared by one memset: the
   // quota kernel's ready count and the done counts of the kernels whose last
-  // block finishes a step (the cutoff, the row table, the digest), then the
+  // block finishes a step (the cutoff, the row table, the digest, the scans'
+  // tile sums), then the
   // summary read back at the end (its counters and accumulators), then the
   // hash's per-stream frontier and progress words.
   constexpr size_t kCtlBytes = 256;
@@ -728,6 +729,7 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(cudaMemsetAsync(zb, 0, zb_bytes, st));
   unsigned *ready = reinterpret_cast<unsigned *>(zb);
   unsigned *done_cutoff = ready + 1, *done_rows = ready + 2, *done_digest = ready + 3;
+  unsigned *done_scan = ready + 4;
   char *rb2 = zb + zb_rb2;
 
   // ---- 1. quotas of every update, on a side stream ------------------------
@@ -762,7 +764,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // A stream without a held-out rate (nothing to hash) needs only the
   // shuffled positions whose documents hold its horizon's tokens: on the
   // first pass about that many are taken (a quarter over the recipe's
-  // estimate), the others keep length 0.  A stream whose windows turn out to
+  // estimate); the others are not shuffled, and the shuffle gives length 0
+  // to those the scans read.  A stream whose windows turn out to
   // need more is caught after the cutoff, and the context is built again
   // with every position.
   char *rb1 = a.temp<char>(r1_bytes);
@@ -772,8 +775,6 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   NS_CK(nsk::launch_keys_bound(c->seed, J, keys, static_cast<uint32_t *>(d_sdb), c->offs,
                                static_cast<uint16_t *>(d_stream_bp),
                                static_cast<unsigned long long *>(d_est), pos_lim, st));
-  if (shuffle_prefix)
-    NS_CK(cudaMemsetAsync(klen, 0, std::max<uint64_t>(n_pos, 1) * sizeof(uint32_t), st));
   {
     nsk::SegGrid g{static_cast<uint32_t *>(d_order_bb), J, order_bb[J]};
     NS_CK(nsk::launch_order(g, static_cast<uint32_t *>(d_sdb), keys, c->offs, c->n_tokens, D0,
@@ -870,7 +871,8 @@ int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   // kept document whole as one piece (no document reaches 2^31 tokens)
   const uint32_t chunk = wrap ? 0x80000000u : T;
   NS_CK(nsk::launch_scan_pieces(klen, n_pos, chunk, kex, pex, scan_scratch, scan_bytes,
-                                static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, c->n_sms, st));
+                                static_cast<uint32_t *>(d_sdb), J, D0, pos_lim, done_scan,
+                                c->n_sms, st));
   // the cutoff reads the quota table, and the readback after it the error
   // word the offsets check sets: the side streams join here, after the scans
   NS_CK(cudaStreamWaitEvent(st, side.join, 0));

@@ -1032,6 +1032,11 @@ __device__ __forceinline__ uint32_t row_of_slot(uint64_t seed, uint32_t step, ui
 // the offsets of all of them are read together, so their latencies overlap
 // instead of adding up.
 constexpr uint32_t kOrderPerThread = 8;
+// The scans of the kept lengths (below) work in tiles of kScanTile positions
+// of the whole position range.
+constexpr int kScanWarps = 8;
+constexpr int kScanRounds = 8;
+constexpr int kScanTile = kScanWarps * kScanRounds * 32;
 
 // The positions p0 + m * blockDim.x (m < kOrderPerThread, below Nb) of
 // stream j: their documents and kept lengths.
@@ -1114,6 +1119,19 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t b0 = sdb[j];
     const uint64_t N = sdb[j + 1] - b0;  // the permutation's domain
     const uint64_t Nb = pos_lim ? pos_lim[j] : N;  // the positions taken
+    if (blk == 0 && Nb < N) {
+      // a stream taken only in part: its lengths past the part are 0 where
+      // the scans read them -- the scan tile holding the first position past
+      // the part, and the tile holding the stream's last position if that
+      // tile runs into the next stream (the tiles between lie wholly past
+      // the part and are skipped)
+      const uint64_t g0 = (uint64_t)b0 - D0, gl = g0 + Nb, ge = g0 + N;
+      const uint64_t a1 = min(ge, (gl / kScanTile + 1) * kScanTile);
+      const uint64_t a2 = max(gl, (ge - 1) / kScanTile * kScanTile);
+      for (uint64_t q = gl + threadIdx.x; q < a1; q += blockDim.x) klen[q] = 0;
+      if (ge % kScanTile != 0)
+        for (uint64_t q = max(a2, a1) + threadIdx.x; q < ge; q += blockDim.x) klen[q] = 0;
+    }
     const uint64_t p0 = (uint64_t)blk * blockDim.x * kOrderPerThread + threadIdx.x;
     if (p0 < Nb) order_positions(keys, j, b0, N, Nb, p0, offs, n_tokens, D0,
                                  stream_bp_heldout_mode, order, klen, err);
@@ -1126,21 +1144,16 @@ __global__ void __launch_bounds__(kThreads)
 // reduce per tile, scan the tile sums, rescan each tile with its offset.  A
 // warp owns a contiguous run of 32 * kScanRounds elements and scans it with
 // shuffles, round by round, so every load and store is coalesced.
-constexpr int kScanWarps = 8;
-constexpr int kScanRounds = 8;
-constexpr int kScanTile = kScanWarps * kScanRounds * 32;
 
 // Tiles of the scans that lie wholly inside the unshuffled part of a stream
 // shuffled only in part: positions (b_j + pos_lim_j, e_j) of stream j, whose
 // lengths are 0 and whose prefix sums nothing reads (the cutoff reads them
 // up to b_j + pos_lim_j, and at the stream's end, which is the next
 // stream's start).  The scans neither read nor write them.
-__global__ void scan_tile_zero_kernel(const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
-                                      const uint32_t *__restrict__ pos_lim, uint64_t n,
-                                      uint64_t nb, uint8_t *__restrict__ tile_zero) {
-  pdl_wait_then_release();
-  const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= nb) return;
+__device__ __forceinline__ bool scan_tile_skipped(const uint32_t *__restrict__ sdb, uint32_t J,
+                                                  uint32_t D0,
+                                                  const uint32_t *__restrict__ pos_lim,
+                                                  uint64_t n, uint64_t t) {
   const uint64_t t0 = t * kScanTile, t1 = min(n, t0 + kScanTile);
   // the stream holding position t0: the last j whose range starts at or
   // before it (empty streams sharing that start come first)
@@ -1153,25 +1166,41 @@ __global__ void scan_tile_zero_kernel(const uint32_t *__restrict__ sdb, uint32_t
       hi = mid;
   }
   const uint64_t b = sdb[lo] - D0, e = sdb[lo + 1] - D0;
-  tile_zero[t] = (t0 >= b + (uint64_t)pos_lim[lo] + 1 && t1 <= e) ? 1 : 0;
+  return t0 >= b + (uint64_t)pos_lim[lo] + 1 && t1 <= e;
 }
 
+// Sums of every tile (with pos_lim, tiles wholly past a stream's shuffled
+// part are marked in tile_zero and sum to 0).  With `done` (zeroed before),
+// the last block to finish then turns the tile sums into their exclusive
+// prefix in place and writes the totals, as scan_tiles_kernel does.
 __global__ void __launch_bounds__(kScanWarps * 32)
     scan_reduce_kernel(const uint32_t *__restrict__ klen, uint64_t n, uint64_t nb, uint32_t T,
-                       const uint8_t *__restrict__ tile_zero, int64_t *__restrict__ bs_a,
-                       int64_t *__restrict__ bs_b) {
+                       const uint32_t *__restrict__ sdb, uint32_t J, uint32_t D0,
+                       const uint32_t *__restrict__ pos_lim, uint8_t *__restrict__ tile_zero,
+                       int64_t *bs_a, int64_t *bs_b, unsigned *done, int64_t *tot_a,
+                       int64_t *tot_b) {
   pdl_wait_then_release();
   __shared__ int64_t sa[kScanWarps], sb[kScanWarps];
+  __shared__ bool s_skip;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the grid strides over the tiles (a tile past a stream's shuffled part
   // costs an iteration, not a block)
   for (uint64_t t = blockIdx.x; t < nb; t += gridDim.x) {
-    if (tile_zero && tile_zero[t]) {
+    if (pos_lim) {
       if (threadIdx.x == 0) {
-        bs_a[t] = 0;
-        bs_b[t] = 0;
+        s_skip = scan_tile_skipped(sdb, J, D0, pos_lim, n, t);
+        tile_zero[t] = s_skip ? 1 : 0;
       }
-      continue;
+      __syncthreads();
+      const bool skip = s_skip;
+      __syncthreads();
+      if (skip) {
+        if (threadIdx.x == 0) {
+          bs_a[t] = 0;
+          bs_b[t] = 0;
+        }
+        continue;
+      }
     }
     const uint64_t seg = t * kScanTile + (uint64_t)w * kScanRounds * 32;
     int64_t a = 0, b = 0;
@@ -1201,6 +1230,26 @@ __global__ void __launch_bounds__(kScanWarps * 32)
       bs_b[t] = tb;
     }
     __syncthreads();
+  }
+  if (!done || !last_block_done(done)) return;
+  __shared__ int64_t ws[33];
+  int64_t carry_a = 0, carry_b = 0;
+  for (uint64_t c0 = 0; c0 < nb; c0 += blockDim.x) {
+    const uint64_t i = c0 + threadIdx.x;
+    const int64_t va = (i < nb) ? __ldcg(bs_a + i) : 0, vb = (i < nb) ? __ldcg(bs_b + i) : 0;
+    int64_t ta, tb;
+    const int64_t ea = block_excl_scan(va, ws, &ta);
+    const int64_t eb = block_excl_scan(vb, ws, &tb);
+    if (i < nb) {
+      bs_a[i] = carry_a + ea;
+      bs_b[i] = carry_b + eb;
+    }
+    carry_a += ta;
+    carry_b += tb;
+  }
+  if (threadIdx.x == 0) {
+    *tot_a = carry_a;
+    *tot_b = carry_b;
   }
 }
 
@@ -1942,6 +1991,8 @@ cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
   return cudaGetLastError();
 }
 
+constexpr uint64_t kScanFuseTiles = 256;
+
 size_t scan_scratch_bytes(uint64_t n) {
   const uint64_t nb = (n + kScanTile - 1) / kScanTile;
   return (size_t)(nb + 1) * 2 * sizeof(int64_t) + (size_t)(nb + 15) / 16 * 16;
@@ -1950,33 +2001,31 @@ size_t scan_scratch_bytes(uint64_t n) {
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
                                const uint32_t *sdb, uint32_t J, uint32_t D0,
-                               const uint32_t *pos_lim, int n_sms, cudaStream_t st) {
+                               const uint32_t *pos_lim, unsigned *done, int n_sms,
+                               cudaStream_t st) {
   const uint64_t nb = (n + kScanTile - 1) / kScanTile;
   // eight blocks of 256 threads an SM at most, striding over the tiles
   const unsigned grid = (unsigned)std::min<uint64_t>(nb, (uint64_t)n_sms * 8);
   if (scratch_bytes < scan_scratch_bytes(n)) return cudaErrorInvalidValue;
   int64_t *bs_a = static_cast<int64_t *>(scratch);
   int64_t *bs_b = bs_a + (nb + 1);
-  uint8_t *tile_zero = nullptr;
-  if (pos_lim && nb > 0) {
-    tile_zero = reinterpret_cast<uint8_t *>(bs_b + (nb + 1));
-    ++launch_counter();
-    pdl_launch(scan_tile_zero_kernel, (unsigned)((nb + kThreads - 1) / kThreads), kThreads, 0, st, 
-        sdb, J, D0, pos_lim, n, nb, tile_zero);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  uint8_t *tile_zero = pos_lim ? reinterpret_cast<uint8_t *>(bs_b + (nb + 1)) : nullptr;
+  // up to kScanFuseTiles tiles the reduce's last block also scans the tile
+  // sums (one launch fewer); beyond, a block of 1024 threads does
+  const bool fuse = nb <= kScanFuseTiles;
   if (nb > 0) {
     ++launch_counter();
-    pdl_launch(scan_reduce_kernel, grid, kScanWarps * 32, 0, st, klen, n, nb, T, tile_zero, bs_a,
-               bs_b);
+    pdl_launch(scan_reduce_kernel, grid, kScanWarps * 32, 0, st, klen, n, nb, T, sdb, J, D0,
+               pos_lim, tile_zero, bs_a, bs_b, fuse ? done : nullptr, kex + n, pex + n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  ++launch_counter();
-  pdl_launch(scan_tiles_kernel, 1, 1024, 0, st, bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || nb == 0) return e;
+  if (!fuse || nb == 0) {
+    ++launch_counter();
+    pdl_launch(scan_tiles_kernel, 1, 1024, 0, st, bs_a, bs_b, (uint32_t)nb, kex + n, pex + n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nb == 0) return e;
+  }
   ++launch_counter();
   pdl_launch(scan_apply_kernel, grid, kScanWarps * 32, 0, st, klen, n, nb, T, tile_zero, bs_a,
              bs_b, kex, pex);

@@ -61,7 +61,8 @@ cudaError_t launch_row_base(const int32_t *quota, uint32_t J, uint32_t K, int32_
 // stream the per-stream rates (a stream of a source that holds nothing out
 // keeps nothing)
 // pos_lim (per stream, or NULL: every position): the shuffled positions
-// taken, from launch_keys_bound; the others are left as they are
+// taken, from launch_keys_bound; of the others, those a scan tile that is
+// not skipped reads get length 0 (launch_scan_pieces)
 cudaError_t launch_order(SegGrid g, const uint32_t *sdb, const uint64_t *keys,
                          const int64_t *offs, uint64_t n_tokens, uint32_t D0,
                          const uint16_t *stream_bp_heldout_mode, const uint32_t *pos_lim,
@@ -112,13 +113,17 @@ cudaError_t launch_copy_prefix(SegGrid g, const uint32_t *sdb, uint32_t D0,
 uint32_t copy_chunk_tokens();
 // kex[i] = sum_{i' < i} klen[i'], pex[i] = sum_{i' < i} ceil(klen[i'] / T), i in [0, n].
 // pos_lim (per stream, or NULL): streams shuffled only in part, whose
-// positions past b_j + pos_lim_j have length 0; there kex and pex are written
-// only where a tile of the scan reaches into the shuffled part or the next
-// stream (the cutoff reads them up to b_j + pos_lim_j and at stream ends)
+// positions past b_j + pos_lim_j have length 0 (written there by the
+// shuffle only where a scan tile reaches into the shuffled part or the next
+// stream: the other tiles are skipped); there kex and pex are written only
+// where a tile of the scan reaches into the shuffled part or the next stream
+// (the cutoff reads them up to b_j + pos_lim_j and at stream ends).  *done:
+// zeroed before.
 cudaError_t launch_scan_pieces(const uint32_t *klen, uint64_t n, uint32_t T, int64_t *kex,
                                int64_t *pex, void *scratch, size_t scratch_bytes,
                                const uint32_t *sdb, uint32_t J, uint32_t D0,
-                               const uint32_t *pos_lim, int n_sms, cudaStream_t st);
+                               const uint32_t *pos_lim, unsigned *done, int n_sms,
+                               cudaStream_t st);
 size_t scan_scratch_bytes(uint64_t n);
 // per stream: cutoff c_j, pieces and kept tokens before it (rmax given as
 // cum_last, the quota table's last row); then node_base[j] (J + 1 entries:
