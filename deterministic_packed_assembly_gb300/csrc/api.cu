@@ -464,6 +464,24 @@ int upload(Arena &a, const void *host, size_t bytes, void **dev, cudaStream_t st
 // build() asks to be run again with the full hash bound (internal, > 0).
 constexpr int kRetryFullBound = 1;
 
+// Builds every table of a context on cfg->cuda_stream, in this order:
+//   host work and one upload: the recipe, the block layouts and estimates
+//     the host knows, the reservation of this phase's arrays;
+//   1./side streams: the quota tables (beside everything up to the cutoff),
+//     the offsets check and the padding terms;
+//   2. round keys and the shuffle of every stream (or of the estimated
+//      prefix of a stream without a held-out rate);
+//   3. the held-out hash of the prefix each stream's horizon reaches (two
+//      rounds when the bound is speculated);
+//   4. the scans of kept lengths and pieces, the cutoff, and the first
+//      readback (its sizes decide what follows);
+//   5. (host corpus) the tokens of the prefixes the hash did not read;
+//   6. host work and the second upload; pieces, next-window search and
+//      pointer jumping;
+//   7. window counts and starts, the row table and the valid horizon;
+//   8.-9. the order digest and the summary readback.
+// Returns kRetryFullBound when a speculated bound left a stream short (the
+// caller builds again with the full bound).
 int build(ns_pack_ctx *c, const ns_pack_config *cfg, Arena &a) {
   const uint32_t J = c->J, S = c->S, K = c->K, T = c->T;
   cudaStream_t st = c->stream;
