@@ -67,6 +67,45 @@ def test_rank_slices_concatenate_to_the_global_batch():
             assert np.array_equal(np.concatenate([p[k] for p in parts]), full[k])
 
 
+def test_launch_plan_equal_launches_within_each_piece():
+    # the benchmark's launches: the fewest that keep each within the most a
+    # launch takes, equal in size within a schedule piece (the last one at
+    # most as long as the others), never across a piece
+    import bench
+
+    class One:
+        schedule = None
+
+        @staticmethod
+        def rows_of_step(k):
+            return 64
+
+    def sizes(plan_of, valid, L):
+        return [m for _, m, _ in bench.launch_plan(plan_of, valid, L)]
+
+    assert sizes(One, 574, bench.auto_launch(1024, 64, 32768)) == [287, 287]
+    assert sizes(One, 1000, bench.auto_launch(1000, 512, 4096)) == [500, 500]
+    assert sizes(One, 200, bench.auto_launch(200, 256, 8192)) == [200]
+    assert sizes(One, 500, bench.auto_launch(500, 8, 4096)) == [500]
+    for valid in range(1, 60):
+        for L in range(1, 20):
+            m = sizes(One, valid, L)
+            assert sum(m) == valid and max(m) <= L and len(m) == -(-valid // L)
+            # all equal but the last, which is no longer than the others
+            assert len(set(m[:-1])) <= 1 and m[-1] <= m[0]
+
+    class Pieces:
+        schedule = [{"begin": 0, "B": 4}, {"begin": 7, "B": 8}]
+
+        @staticmethod
+        def rows_of_step(k):
+            return 4 if k < 7 else 8
+
+    plan = list(bench.launch_plan(Pieces, 20, 5))
+    assert [(s, m) for s, m, _ in plan] == [(0, 4), (4, 3), (7, 5), (12, 5), (17, 3)]
+    assert all(b == Pieces.rows_of_step(s) for s, _, b in plan)
+
+
 def test_schedule_launch_plan_slices_cover_every_update():
     # the benchmark's launches never cross a schedule piece, and under any rank
     # count the ranks' slices of each launch concatenate to the global rows
