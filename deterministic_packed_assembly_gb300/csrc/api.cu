@@ -206,12 +206,21 @@ void release_ctx(ns_pack_ctx *c) {
   delete c;
 }
 
+// A device pointer aligned for its element type: the kernels' loads and
+// stores of that type would fault on a misaligned one.
+template <class T>
+bool aligned_for(const T *p) {
+  return reinterpret_cast<uintptr_t>(p) % alignof(T) == 0;
+}
+
 int check_config(const ns_pack_config *cfg) {
   if (!cfg || !cfg->tokens || !cfg->doc_offsets) return NS_ERR_INVALID_ARG;
   if (!cfg->stream_doc_begin || !cfg->stream_source || !cfg->source_weight ||
       !cfg->stream_weight || !cfg->source_heldout_bp)
     return NS_ERR_INVALID_ARG;
-  if (!(cfg->flags & NS_PACK_HOST_CORPUS) && reinterpret_cast<uintptr_t>(cfg->tokens) % 16 != 0)
+  if (!(cfg->flags & NS_PACK_HOST_CORPUS) &&
+      (reinterpret_cast<uintptr_t>(cfg->tokens) % 16 != 0 || !aligned_for(cfg->doc_offsets) ||
+       !aligned_for(cfg->loss_start)))
     return NS_ERR_INVALID_ARG;
   if (cfg->T < 16 || cfg->T % 16 != 0 || cfg->T > NS_MAX_T) return NS_ERR_INVALID_ARG;
   if (cfg->B == 0 || cfg->max_steps == 0) return NS_ERR_INVALID_ARG;
@@ -1253,6 +1262,8 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
                        reinterpret_cast<uintptr_t>(out->pos) |
                        reinterpret_cast<uintptr_t>(out->doc) | reinterpret_cast<uintptr_t>(out->mask);
   if (al % 16 != 0) return NS_ERR_INVALID_ARG;
+  if (!aligned_for(out->row_fp) || !aligned_for(out->row_learned) || !aligned_for(out->row_len))
+    return NS_ERR_INVALID_ARG;
   if ((uint64_t)n_steps * (row_end - row_begin) >= (1ull << 31)) return NS_ERR_INVALID_ARG;
   if ((uint64_t)step0 + n_steps > ctx->K) return NS_ERR_HORIZON;
   if ((uint64_t)step0 + n_steps > ctx->valid_steps) return NS_ERR_EXHAUSTED;
@@ -1294,6 +1305,7 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
   if (!ctx || !row_fp_dev || !batch_fp_dev || n_steps == 0 || n_rows == 0 ||
       n_steps >= (1u << 31))
     return NS_ERR_INVALID_ARG;
+  if (!aligned_for(row_fp_dev) || !aligned_for(batch_fp_dev)) return NS_ERR_INVALID_ARG;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_batch_fp(row_fp_dev, n_steps, n_rows, batch_fp_dev, st) != cudaSuccess) {
     cudaGetLastError();
@@ -1307,6 +1319,7 @@ int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint3
   if (!ctx || !row_learned_dev || !learned_dev || n_steps == 0 || n_rows == 0 ||
       n_steps >= (1u << 31))
     return NS_ERR_INVALID_ARG;
+  if (!aligned_for(row_learned_dev) || !aligned_for(learned_dev)) return NS_ERR_INVALID_ARG;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_step_learned(row_learned_dev, n_steps, n_rows, learned_dev, st) !=
       cudaSuccess) {
@@ -1330,6 +1343,7 @@ static int read_error_word(ns_pack_ctx *ctx, cudaStream_t st) {
 int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,
                         uint64_t *batch_fp_host, void *cuda_stream) {
   if (!ctx || !row_fp_dev || !batch_fp_host || n_rows == 0) return NS_ERR_INVALID_ARG;
+  if (!aligned_for(row_fp_dev)) return NS_ERR_INVALID_ARG;
   cudaStream_t st = cuda_stream ? static_cast<cudaStream_t>(cuda_stream) : ctx->stream;
   if (nsk::launch_batch_fp(row_fp_dev, 1, n_rows, ctx->fp_out, st) != cudaSuccess ||
       cudaMemcpyAsync(batch_fp_host, ctx->fp_out, sizeof(uint64_t), cudaMemcpyDeviceToHost, st) !=

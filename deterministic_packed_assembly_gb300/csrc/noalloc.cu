@@ -99,6 +99,10 @@ extern "C" int ns_pack_quota_noalloc(const uint32_t *source_weight, uint32_t n_s
   const uint32_t S = n_sources, J = n_streams, K = max_steps;
   if (!source_weight || !stream_source || !stream_weight || !quota_dev || !cum_dev)
     return NS_ERR_INVALID_ARG;
+  // int32 tables: the kernels' 4-byte stores would fault on a misaligned one
+  if (reinterpret_cast<uintptr_t>(quota_dev) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(cum_dev) % 4 != 0)
+    return NS_ERR_INVALID_ARG;
   if (S == 0 || S > NS_MAX_SOURCES || J == 0 || J > NS_MAX_STREAMS) return NS_ERR_INVALID_ARG;
   if (B == 0 || K == 0 || (uint64_t)K * B >= (1ull << 31)) return NS_ERR_INVALID_ARG;
   uint32_t *src_first = tl_src_first;

@@ -123,7 +123,9 @@ typedef struct {
   /* Corpus, on the device, borrowed (must outlive the context); with
    * NS_PACK_HOST_CORPUS in host memory instead, copied.  Documents are
    * contiguous runs of tokens: document d is tokens[doc_offsets[d] ..
-   * doc_offsets[d+1]).  Device tokens must be 16-byte aligned. */
+   * doc_offsets[d+1]).  On the device, tokens must be 16-byte aligned and
+   * doc_offsets and loss_start aligned for their types (8 and 4 bytes), else
+   * NS_ERR_INVALID_ARG. */
   const int32_t *tokens;
   uint64_t n_tokens;          /* < NS_MAX_TOKENS */
   const int64_t *doc_offsets; /* [n_docs + 1], nondecreasing, lengths < 2^31 */
@@ -182,7 +184,8 @@ typedef struct {
 } ns_pack_config;
 
 /* Caller-owned device outputs of ns_pack_step, row-major
- * [n_steps][row_end - row_begin][T]; tokens/pos/doc/mask 16-byte aligned. */
+ * [n_steps][row_end - row_begin][T]; tokens/pos/doc/mask 16-byte aligned,
+ * row_fp 8-byte, row_learned and row_len 4-byte aligned. */
 typedef struct {
   int32_t *tokens;
   int32_t *pos;
@@ -258,14 +261,15 @@ int ns_pack_step(ns_pack_ctx *ctx, uint32_t step0, uint32_t n_steps, uint32_t ro
  * cuda_stream (NULL: the context's).  Also reports the device error word.
  * Uses one word of the context's memory: calls on one context must not
  * overlap (ns_pack_batch_fp writes to caller memory and has no such limit).
- * Errors: INVALID_ARG, CUDA, DEVICE, BAD_INPUT. */
+ * Errors: INVALID_ARG (NULL or misaligned pointers, n_rows 0), CUDA, DEVICE,
+ * BAD_INPUT. */
 int ns_pack_fingerprint(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_rows,
                         uint64_t *batch_fp_host, void *cuda_stream);
 
 /* Asynchronous variant for n_steps consecutive batches of n_rows rows each:
  * batch_fp_dev[s] = fold of row_fp_dev[s * n_rows .. (s + 1) * n_rows).
- * Errors: INVALID_ARG (NULL pointers, n_steps or n_rows 0, n_steps >= 2^31),
- * CUDA. */
+ * Errors: INVALID_ARG (NULL or misaligned pointers, n_steps or n_rows 0,
+ * n_steps >= 2^31), CUDA. */
 int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_steps,
                      uint32_t n_rows, uint64_t *batch_fp_dev, void *cuda_stream);
 
@@ -275,7 +279,7 @@ int ns_pack_batch_fp(ns_pack_ctx *ctx, const uint64_t *row_fp_dev, uint32_t n_st
  * by (Linnet training docs, Supervised fine-tuning).  For a row slice it is
  * the slice's share; the update's count is the sum over its slices.
  * Asynchronous on cuda_stream (NULL: the context's).  Errors: INVALID_ARG
- * (NULL pointers, n_steps or n_rows 0, n_steps >= 2^31), CUDA. */
+ * (NULL or misaligned pointers, n_steps or n_rows 0, n_steps >= 2^31), CUDA. */
 int ns_pack_step_learned(ns_pack_ctx *ctx, const int32_t *row_learned_dev, uint32_t n_steps,
                          uint32_t n_rows, int64_t *learned_dev, void *cuda_stream);
 
@@ -335,7 +339,8 @@ const char *ns_pack_strerror(int code);
  * [max_steps][n_sources] int32 table live in one static device array of
  * NS_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
  * exit.  A recipe whose scratch does not fit returns NS_ERR_INVALID_ARG, as do
- * out-of-range arguments; NS_ERR_CUDA if a CUDA call fails.  The first call on
+ * out-of-range arguments and quota_dev or cum_dev not 4-byte aligned;
+ * NS_ERR_CUDA if a CUDA call fails.  The first call on
  * each device looks up the array's device address (cudaGetSymbolAddress, with
  * that device current) and keeps it: make that first call before any stream
  * capture.  All calls share the array and it keeps the last call's contents;

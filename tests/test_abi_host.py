@@ -109,6 +109,36 @@ def test_init_rejects_misaligned_tokens(nspack):
     assert e.value.code == nspack.NS_ERR_INVALID_ARG
 
 
+def test_init_rejects_misaligned_offsets_and_loss_starts(nspack):
+    # device offsets are read as int64 and loss starts as int32: a pointer not
+    # aligned for its type is refused before anything is enqueued (without the
+    # check, init would go on to the CUDA calls, which fail here otherwise)
+    c, keep = _cfg(nspack)
+    c.doc_offsets = c.doc_offsets + 4
+    with pytest.raises(nspack.NsPackError) as e:
+        nspack.ns_pack_init(c)
+    assert e.value.code == nspack.NS_ERR_INVALID_ARG
+    c, keep = _cfg(nspack)
+    keep["ls"] = np.zeros(4, np.int32)
+    c.loss_start = (keep["ls"].ctypes.data & ~3) + 2
+    with pytest.raises(nspack.NsPackError) as e:
+        nspack.ns_pack_init(c)
+    assert e.value.code == nspack.NS_ERR_INVALID_ARG
+
+
+def test_quota_noalloc_rejects_misaligned_tables(nspack):
+    L = nspack._lib
+    sw = np.ones(2, np.uint32)
+    ss = np.asarray([0, 1], np.uint32)
+    tw = np.ones(2, np.uint32)
+    buf = np.zeros(64, np.int32)
+    good = buf.ctypes.data & ~15
+    for q, cm in ((good + 2, good + 16), (good, good + 17)):
+        rc = L.lib.ns_pack_quota_noalloc(sw.ctypes.data, 2, ss.ctypes.data, tw.ctypes.data, 2,
+                                         4, 3, q, cm, None)
+        assert rc == nspack.NS_ERR_INVALID_ARG
+
+
 def test_null_context_is_rejected(nspack):
     L = nspack._lib
     out = L.ns_pack_out()

@@ -385,6 +385,44 @@ def test_horizon_and_row_range_errors():
     assert e.value.code == -1
 
 
+def test_misaligned_row_outputs_are_refused():
+    # row fingerprints are stored as u64 and counts and lengths as int32: a
+    # pointer not aligned for its type is refused on the host, before any
+    # launch, by every call that takes one
+    from deterministic_packed_assembly_gb300 import _lib as L
+    c = make_preset("c1")
+    pk = packer_for(c)
+    out = pk.empty_out(1, c.B)
+    raw = torch.zeros(c.B * 8 + 64, dtype=torch.uint8, device="cuda:0")
+    a = raw.data_ptr()
+    st = pk.stream.cuda_stream
+    for field, off in (("row_fp", 4), ("row_learned", 2), ("row_len", 2)):
+        bad = pk.prepare(out)
+        setattr(bad, field, a + off)
+        with pytest.raises(Exception) as e:
+            pk.step(0, out=out, prepared=bad)
+        assert e.value.code == -1, field
+    for row_fp, dst in ((a + 4, a + 32), (a, a + 36)):
+        with pytest.raises(Exception) as e:
+            L.ns_pack_batch_fp(pk._ctx, row_fp, 1, c.B, dst, st)
+        assert e.value.code == -1
+    for learned, dst in ((a + 2, a + 32), (a, a + 36)):
+        with pytest.raises(Exception) as e:
+            L.ns_pack_step_learned(pk._ctx, learned, 1, c.B, dst, st)
+        assert e.value.code == -1
+    with pytest.raises(Exception) as e:
+        L.ns_pack_fingerprint(pk._ctx, a + 4, c.B, st)
+    assert e.value.code == -1
+    torch.cuda.synchronize()
+    assert int(raw.count_nonzero()) == 0  # nothing was written
+    # the context is untouched: the same update, aligned, matches the oracle
+    o = pk.step(0, out=out)
+    torch.cuda.synchronize()
+    want = oracle_for(c).rows(0)
+    assert (o["row_fp"][0].cpu().numpy().view(np.uint64) == want["row_fp"]).all()
+    pk.check()
+
+
 def test_malformed_offsets_are_reported():
     c = corpus_from_lengths([3, 4, 5, 6], T=16, B=1, max_steps=2)
     c.doc_offsets = np.asarray([0, 3, 2, 12, 18], np.int64)
