@@ -19,6 +19,23 @@ def _u32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a), dtype=np.uint32)
 
 
+def _refuse(what: str) -> None:
+    raise L.NsPackError(L.NS_ERR_INVALID_ARG, what)
+
+
+def _need(t, name: str, dtype: torch.dtype, device=None) -> None:
+    """Refuse a tensor the library would misread, or read or write past:
+    its pointer is handed over with no shape, stride or type."""
+    if not isinstance(t, torch.Tensor):
+        _refuse(f"{name}: expected a tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        _refuse(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if device is not None and t.device != device:
+        _refuse(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        _refuse(f"{name}: not contiguous")
+
+
 class Packer:
     """A packing context over a corpus resident on one CUDA device.
 
@@ -45,12 +62,10 @@ class Packer:
                  shuffle_rows: bool = False, schedule: Optional[list] = None,
                  wrap: bool = False, len_bucket: int = 0,
                  stream: Optional[torch.cuda.Stream] = None, device=None):
-        assert tokens.dtype == torch.int32 and tokens.is_contiguous()
-        assert doc_offsets.dtype == torch.int64 and doc_offsets.is_contiguous()
-        assert doc_offsets.device == tokens.device
+        _need(tokens, "tokens", torch.int32)
+        _need(doc_offsets, "doc_offsets", torch.int64, tokens.device)
         if loss_start is not None:
-            assert loss_start.dtype == torch.int32 and loss_start.is_contiguous()
-            assert loss_start.device == tokens.device
+            _need(loss_start, "loss_start", torch.int32, tokens.device)
         self.host_corpus = not tokens.is_cuda
         if self.host_corpus:
             if tokens.device.type != "cpu":
@@ -170,8 +185,22 @@ class Packer:
                     row_learned=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d),
                     row_len=torch.empty((n_steps, n_rows), dtype=torch.int32, device=d))
 
+    # the output arrays: (name, dtype, one element per position (else per row))
+    _OUT = (("tokens", torch.int32, True), ("pos", torch.int32, True),
+            ("doc", torch.int32, True), ("mask", torch.uint8, True),
+            ("row_fp", torch.int64, False), ("row_learned", torch.int32, False),
+            ("row_len", torch.int32, False))
+
     @staticmethod
     def _out_struct(out: dict) -> L.ns_pack_out:
+        dev = out["tokens"].device if isinstance(out.get("tokens"), torch.Tensor) else None
+        positions, rows = [], []
+        for name, dtype, per_position in Packer._OUT:
+            t = out.get(name)
+            if t is None and name == "row_len":
+                continue
+            _need(t, f"out[{name!r}]", dtype, dev)
+            (positions if per_position else rows).append(t.numel())
         o = L.ns_pack_out()
         o.tokens = out["tokens"].data_ptr()
         o.pos = out["pos"].data_ptr()
@@ -180,6 +209,8 @@ class Packer:
         o.row_fp = out["row_fp"].data_ptr()
         o.row_learned = out["row_learned"].data_ptr()
         o.row_len = out["row_len"].data_ptr() if out.get("row_len") is not None else None
+        # what the buffers hold, checked against every call that writes them
+        o.nspack_device, o.nspack_positions, o.nspack_rows = dev, min(positions), min(rows)
         return o
 
     @staticmethod
@@ -197,22 +228,36 @@ class Packer:
         r0, r1 = (0, self.rows_of_step(step0)) if rows is None else rows
         if out is None:
             out = self.empty_out(n_steps, r1 - r0)
+        o = prepared if prepared is not None else self._out_struct(out)
+        if hasattr(o, "nspack_rows"):
+            n = max(int(n_steps), 0) * max(int(r1) - int(r0), 0)
+            if o.nspack_device != self.device:
+                _refuse(f"Packer.step: outputs on {o.nspack_device}, the packer on {self.device}")
+            if n > o.nspack_rows or n * self.T > o.nspack_positions:
+                _refuse(f"Packer.step: the outputs hold {o.nspack_rows} rows, "
+                        f"the call writes {n}")
         st = (stream or self.stream).cuda_stream
-        L.ns_pack_step(self._ctx, step0, n_steps, r0, r1,
-                       prepared if prepared is not None else self._out_struct(out), st)
+        L.ns_pack_step(self._ctx, step0, n_steps, r0, r1, o, st)
         return out
 
     def batch_fp(self, row_fp: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
         """Fold one batch's row fingerprints (device, row order); synchronises."""
+        _need(row_fp, "row_fp", torch.int64, self.device)
         st = (stream or self.stream).cuda_stream
         return L.ns_pack_fingerprint(self._ctx, row_fp.data_ptr(), row_fp.numel(), st)
 
     def batch_fp_many(self, row_fp: torch.Tensor, out: Optional[torch.Tensor] = None,
                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """Batch fingerprints of [n_steps, n_rows] row fingerprints (async)."""
+        _need(row_fp, "row_fp", torch.int64, self.device)
+        if row_fp.dim() != 2:
+            _refuse(f"row_fp: shape {tuple(row_fp.shape)}, expected [n_steps, n_rows]")
         n_steps, n_rows = row_fp.shape
         if out is None:
             out = torch.empty(n_steps, dtype=torch.int64, device=self.device)
+        _need(out, "out", torch.int64, self.device)
+        if out.numel() < n_steps:
+            _refuse(f"out: {out.numel()} elements, the call writes {n_steps}")
         st = (stream or self.stream).cuda_stream
         L.ns_pack_batch_fp(self._ctx, row_fp.data_ptr(), n_steps, n_rows, out.data_ptr(), st)
         return out
@@ -221,9 +266,15 @@ class Packer:
                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """Learned positions of each update of [n_steps, n_rows] row counts
         (int64, async): what a trainer weighs the update's loss by."""
+        _need(row_learned, "row_learned", torch.int32, self.device)
+        if row_learned.dim() != 2:
+            _refuse(f"row_learned: shape {tuple(row_learned.shape)}, expected [n_steps, n_rows]")
         n_steps, n_rows = row_learned.shape
         if out is None:
             out = torch.empty(n_steps, dtype=torch.int64, device=self.device)
+        _need(out, "out", torch.int64, self.device)
+        if out.numel() < n_steps:
+            _refuse(f"out: {out.numel()} elements, the call writes {n_steps}")
         st = (stream or self.stream).cuda_stream
         L.ns_pack_step_learned(self._ctx, row_learned.data_ptr(), n_steps, n_rows,
                                out.data_ptr(), st)

@@ -139,6 +139,44 @@ def test_quota_noalloc_rejects_misaligned_tables(nspack):
         assert rc == nspack.NS_ERR_INVALID_ARG
 
 
+def test_packer_refuses_outputs_it_would_misread_or_write_past(nspack):
+    # the binding hands the library bare pointers: a tensor of the wrong type,
+    # not contiguous, or smaller than the call writes is refused first
+    import torch
+    from deterministic_packed_assembly_gb300.packer import Packer
+    T, B = 16, 4
+
+    def out(n, r, **over):
+        o = dict(tokens=torch.zeros(n, r, T, dtype=torch.int32),
+                 pos=torch.zeros(n, r, T, dtype=torch.int32),
+                 doc=torch.zeros(n, r, T, dtype=torch.int32),
+                 mask=torch.zeros(n, r, T, dtype=torch.uint8),
+                 row_fp=torch.zeros(n, r, dtype=torch.int64),
+                 row_learned=torch.zeros(n, r, dtype=torch.int32))
+        o.update(over)
+        return o
+
+    o = Packer.prepare(out(2, B))
+    assert (o.nspack_positions, o.nspack_rows) == (2 * B * T, 2 * B)
+    for bad in (dict(row_fp=torch.zeros(2, B, dtype=torch.int32)),
+                dict(mask=torch.zeros(2, B, T, dtype=torch.int32)),
+                dict(row_len=torch.zeros(2, B, dtype=torch.int64)),
+                dict(tokens=torch.zeros(2, 2 * B, T, dtype=torch.int32)[:, ::2]),
+                dict(pos=torch.zeros(2, 2 * B, T, dtype=torch.int32)[:, :B])):
+        with pytest.raises(nspack.NsPackError) as e:
+            Packer.prepare(out(2, B, **bad))
+        assert e.value.code == nspack.NS_ERR_INVALID_ARG, list(bad)
+    # the call's size against the buffers' (host checks only: no context)
+    pk = Packer.__new__(Packer)
+    pk.device, pk.T, pk.B, pk.schedule, pk.stream, pk._ctx = (
+        torch.device("cpu"), T, B, None, None, None)
+    for kw in (dict(n_steps=3, out=out(2, B)), dict(rows=(0, B), out=out(1, B - 1)),
+               dict(n_steps=2, out=out(1, 2 * B, row_fp=torch.zeros(1, B, dtype=torch.int64)))):
+        with pytest.raises(nspack.NsPackError) as e:
+            pk.step(0, **kw)
+        assert e.value.code == nspack.NS_ERR_INVALID_ARG
+
+
 def test_null_context_is_rejected(nspack):
     L = nspack._lib
     out = L.ns_pack_out()
