@@ -343,7 +343,14 @@ struct SideStream {
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join2, cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreate(&h->t0);
       if (e == cudaSuccess) e = cudaEventCreate(&h->t1);
-      if (e != cudaSuccess) return e;
+      if (e != cudaSuccess) {
+        // release a partial set, so that the next init creates a whole one
+        for (cudaEvent_t *ev : {&h->fork, &h->join, &h->join2, &h->t0, &h->t1})
+          if (*ev) cudaEventDestroy(*ev), *ev = nullptr;
+        for (cudaStream_t *q : {&h->s, &h->s2})
+          if (*q) cudaStreamDestroy(*q), *q = nullptr;
+        return e;
+      }
     }
     s = h->s;
     s2 = h->s2;
